@@ -1,0 +1,193 @@
+"""Seeded synthetic decode workloads (inputs only; none of the method's arithmetic).
+
+The five workloads are the decode shapes the gated-attention pages measure or
+serve, built from seeded random numbers because no page ships data:
+
+1. ``b1_l512``      B=1, KV length 512, a 1024-slot pool, slots a random
+                    subset (FreeToken PR #781, Automatic dispatch and Kernel
+                    window: query [1,16,256], two KV heads, CSR capacity 512).
+2. ``b4_ragged``    B=4, lengths 512/495/478/461 over a shuffled 4096-slot pool
+                    (FreeToken PR #781, Kernel window, the B4 row).
+3. ``b64_l4096``    B=64, length 4096, 16-slot pages placed at random in a
+                    300 000-slot pool (the bandwidth workload).
+4. ``b224_ragged``  B=224, lengths uniform in [1, 6142], slots a permutation of
+                    the pool, 1% of referenced K rows scaled by 3 (a peaky
+                    softmax); the shape of ROCm/ATOM PR #838's CONC=224,
+                    ISL 4094 / OSL 2048 serving run.
+5. ``b8_l131072``   B=8, length 131072, 64-slot pages in random order.
+
+Every workload has Hq=16, Hkv=2, D=256, scale 1/16 and BF16 q / gate / K / V
+drawn from normal distributions (gate standard deviation 2, except workload 4
+where it is 1).  Draw order, all from one ``torch.Generator`` seeded with the
+workload's seed: lengths (if random) -> slot layout -> peaky-row mask -> q ->
+gate -> K pool -> V pool.  Values are drawn in float32, scaled, then rounded to
+BF16 (round-to-nearest-even).  Every pool row is filled, referenced or not.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence
+
+import torch
+
+HQ, HKV, HEAD_DIM = 16, 2, 256
+DEFAULT_SCALE = 1.0 / 16.0
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    lengths: Optional[Sequence[int]]     # None -> drawn uniform in [len_lo, len_hi]
+    len_lo: int
+    len_hi: int
+    layout: str                          # "subset" | "pages" | "perm"
+    pool_slots: Optional[int]            # None -> exactly the referenced count
+    page: int
+    gate_std: float
+    peaky_frac: float
+    seed: int
+    num_splits: int                      # split count the workload names (0: automatic)
+    hq: int = HQ
+    hkv: int = HKV
+    head_dim: int = HEAD_DIM
+    scale: float = DEFAULT_SCALE
+
+
+WORKLOADS: List[Workload] = [
+    Workload("b1_l512", 1, [512], 0, 0, "subset", 1024, 1, 2.0, 0.0, 0, 8),
+    Workload("b4_ragged", 4, [512, 495, 478, 461], 0, 0, "subset", 4096, 1, 2.0, 0.0, 1, 0),
+    Workload("b64_l4096", 64, [4096] * 64, 0, 0, "pages", 300_000, 16, 2.0, 0.0, 2, 0),
+    Workload("b224_ragged", 224, None, 1, 6142, "perm", None, 1, 1.0, 0.01, 3, 0),
+    Workload("b8_l131072", 8, [131072] * 8, 0, 0, "pages", 1_048_576, 64, 2.0, 0.0, 4, 128),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def workload(key) -> Workload:
+    """Look a workload up by name or by its 1-based number."""
+    if isinstance(key, int):
+        return WORKLOADS[key - 1]
+    if isinstance(key, str) and key.isdigit():
+        return WORKLOADS[int(key) - 1]
+    return BY_NAME[key]
+
+
+def _randn_bf16(gen: torch.Generator, rows: int, cols: int, std: float,
+                row_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """[rows, cols] BF16 of N(0, std^2) values, drawn in float32 chunks.
+
+    ``row_scale`` (float32 [rows]) multiplies rows in float32 before the
+    rounding to BF16."""
+    out = torch.empty(rows, cols, dtype=torch.bfloat16)
+    chunk = max(1, (1 << 24) // max(cols, 1))
+    for r0 in range(0, rows, chunk):
+        r1 = min(rows, r0 + chunk)
+        x = torch.randn(r1 - r0, cols, generator=gen, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        if row_scale is not None:
+            x.mul_(row_scale[r0:r1, None])
+        out[r0:r1] = x.to(torch.bfloat16)
+    return out
+
+
+def _layout(gen: torch.Generator, lengths: List[int], layout: str, pool_slots: Optional[int],
+            page: int):
+    nnz = int(sum(lengths))
+    if layout == "subset":
+        slots = pool_slots if pool_slots is not None else nnz
+        assert slots >= nnz
+        idx = torch.randperm(slots, generator=gen)[:nnz].to(torch.int32)
+    elif layout == "perm":
+        slots = nnz if pool_slots is None else pool_slots
+        idx = torch.randperm(slots, generator=gen)[:nnz].to(torch.int32)
+    elif layout == "pages":
+        pages_needed = [int(math.ceil(L / page)) for L in lengths]
+        total_pages = sum(pages_needed)
+        slots = pool_slots if pool_slots is not None else total_pages * page
+        pool_pages = slots // page
+        assert pool_pages >= total_pages, "pool too small for the pages"
+        order = torch.randperm(pool_pages, generator=gen)[:total_pages]
+        parts = []
+        p = 0
+        for L, npg in zip(lengths, pages_needed):
+            pg = order[p:p + npg]
+            p += npg
+            s = (pg[:, None] * page + torch.arange(page)[None, :]).reshape(-1)[:L]
+            parts.append(s)
+        idx = (torch.cat(parts) if parts else torch.empty(0, dtype=torch.int64)).to(torch.int32)
+    else:
+        raise ValueError(layout)
+    return idx, slots
+
+
+def make(lengths: Sequence[int], *, seed: int, hq: int = HQ, hkv: int = HKV,
+         head_dim: int = HEAD_DIM, layout: str = "perm", pool_slots: Optional[int] = None,
+         page: int = 1, gate_std: float = 2.0, qkv_std: float = 1.0, peaky_frac: float = 0.0,
+         peaky_scale: float = 3.0, scale: float = DEFAULT_SCALE, random_lengths=None) -> dict:
+    """Build one decode batch on the CPU.
+
+    Returns a dict of CPU tensors ``q, gate`` [B, Hq, D] bf16, ``k_pool, v_pool``
+    [slots, Hkv, D] bf16, ``kv_indptr`` [B+1] int32, ``kv_indices`` [nnz] int32,
+    plus ``scale``, ``lengths`` and ``num_slots``.  ``random_lengths=(lo, hi, B)``
+    draws the lengths uniformly from [lo, hi] first."""
+    gen = torch.Generator().manual_seed(seed)
+    if random_lengths is not None:
+        lo, hi, bsz = random_lengths
+        lengths = torch.randint(lo, hi + 1, (bsz,), generator=gen).tolist()
+    lengths = [int(L) for L in lengths]
+    B = len(lengths)
+    idx, slots = _layout(gen, lengths, layout, pool_slots, page)
+    row_scale = None
+    if peaky_frac > 0.0:
+        picked = torch.rand(idx.numel(), generator=gen) < peaky_frac
+        row_scale = torch.ones(slots, dtype=torch.float32)
+        row_scale[idx[picked].long()] = peaky_scale
+    q = _randn_bf16(gen, B * hq, head_dim, qkv_std).view(B, hq, head_dim)
+    g = _randn_bf16(gen, B * hq, head_dim, gate_std).view(B, hq, head_dim)
+    k_scale = None
+    if row_scale is not None:
+        k_scale = row_scale.repeat_interleave(hkv)
+    k_pool = _randn_bf16(gen, slots * hkv, head_dim, qkv_std, k_scale).view(slots, hkv, head_dim)
+    v_pool = _randn_bf16(gen, slots * hkv, head_dim, qkv_std).view(slots, hkv, head_dim)
+    indptr = torch.zeros(B + 1, dtype=torch.int32)
+    if B:
+        indptr[1:] = torch.tensor(lengths, dtype=torch.int64).cumsum(0).to(torch.int32)
+    return dict(q=q, gate=g, k_pool=k_pool, v_pool=v_pool, kv_indptr=indptr, kv_indices=idx,
+                scale=float(scale), lengths=lengths, num_slots=slots)
+
+
+def make_workload(key, batch_limit: Optional[int] = None) -> dict:
+    """Inputs of one of the five named workloads (``batch_limit`` keeps the
+    first sequences only, for bounded CPU timing; the draw is unchanged)."""
+    w = workload(key)
+    rl = (w.len_lo, w.len_hi, w.batch) if w.lengths is None else None
+    d = make(w.lengths if w.lengths is not None else [], seed=w.seed, hq=w.hq, hkv=w.hkv,
+             head_dim=w.head_dim, layout=w.layout, pool_slots=w.pool_slots, page=w.page,
+             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl)
+    d["workload"] = w
+    d["num_splits"] = w.num_splits
+    if batch_limit is not None and batch_limit < len(d["lengths"]):
+        d = truncate_batch(d, batch_limit)
+    return d
+
+
+def truncate_batch(d: dict, nb: int) -> dict:
+    """Keep the first ``nb`` sequences of a batch (same pools)."""
+    e = dict(d)
+    nnz = int(d["kv_indptr"][nb])
+    e["q"] = d["q"][:nb].contiguous()
+    e["gate"] = d["gate"][:nb].contiguous()
+    e["kv_indptr"] = d["kv_indptr"][:nb + 1].clone()
+    e["kv_indices"] = d["kv_indices"][:nnz].clone()
+    e["lengths"] = d["lengths"][:nb]
+    return e
+
+
+def metric_bytes(lengths: Sequence[int], hq: int = HQ, hkv: int = HKV, head_dim: int = HEAD_DIM) -> int:
+    """Algorithmic HBM bytes of one call: every referenced K and V row once
+    (2 bytes per element), plus q, gate and out."""
+    n = int(sum(lengths))
+    return n * hkv * head_dim * 2 * 2 + 3 * len(lengths) * hq * head_dim * 2

@@ -1,0 +1,266 @@
+/*
+ * gda_oracle.c -- plain FP64 CPU oracle for gated split-KV GQA decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark may load or run this code.  The CUDA library
+ * never links, includes or calls it, and it shares no code, header or table
+ * with the CUDA path.
+ *
+ * What it computes (one decode token per sequence b, query head h):
+ *
+ *   kvh      = h / (Hq / Hkv)                        consecutive GQA grouping
+ *   rows     = kv_indices[kv_indptr[b] .. kv_indptr[b+1])
+ *   s_j      = scale * sum_d q[b,h,d] * K[rows_j, kvh, d]
+ *   p        = softmax(s)                             (natural exp, max-shifted)
+ *   O        = sum_j p_j * V[rows_j, kvh, :]
+ *   o_b      = RNE_bf16(O)                            (double rounded directly)
+ *   s_b      = RNE_bf16(1 / (1 + exp(-gate)))         (gate widened to double)
+ *   out      = RNE_bf16(o_b * s_b)                    (product exact in double)
+ *
+ * Sources:
+ *  - FreeToken PR #781 "Fuse the BF16 attention output sigmoid gate into the
+ *    existing Triton decode stage2", Summary: stage1 + stage2 FP32 reduction are
+ *    kept, the output is rounded to BF16, the sigmoid of the gate is taken in
+ *    BF16 (a per-device table of BF16 sigmoid values) and the product is rounded
+ *    to nearest even; Correctness: the fused output equals the unfused
+ *    Torch sigmoid followed by Torch multiply element by element.
+ *  - FreeToken PR #781, Automatic dispatch: query [1,16,256], two KV heads, a
+ *    CSR slot index, default full attention (no window, sinks or custom scale).
+ *  - cuDNN FE-OSS "Gated Attention Block (SM107)", Overview, stages (4) and (5):
+ *    O = softmax(Q K^T * scale) V with GQA H_q / H_kv, then O * sigmoid(GATE);
+ *    Forward / fp4 notes: a dead (zero-length) row produces zeros.
+ *
+ * Readings where the pages are silent: the sigmoid is the correctly rounded
+ * BF16 value of the real sigmoid (no page fixes a device's sigmoid), the KV
+ * head of query head h is h / G, a zero-length sequence gives O = 0 and
+ * lse = -inf, and rounding to BF16 is round-to-nearest-even straight from the
+ * double (never through an intermediate float, which would round twice).
+ *
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (no fast-math, no
+ * FMA contraction), so the arithmetic is the plain IEEE double arithmetic the
+ * formulas above describe, on x86-64 and on aarch64 alike.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_SHAPE (-1)
+#define ORACLE_ERR_INDEX (-2)
+#define ORACLE_ERR_NOMEM (-3)
+
+/* ---- BF16 <-> double ------------------------------------------------------ */
+
+/* Widen a BF16 bit pattern: BF16 is the upper half of an IEEE binary32. */
+double oracle_double_from_bf16(uint16_t b) {
+    uint32_t bits = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest BF16 value, ties to even, in one step.
+ * BF16: 1 sign, 8 exponent, 7 fraction bits; normal quantum 2^(E-7) for values
+ * in [2^E, 2^(E+1)), subnormal quantum 2^-133, overflow to infinity from
+ * (2 - 2^-8) * 2^127 upward.  NaN maps to the canonical quiet NaN. */
+uint16_t oracle_bf16_from_double(double x) {
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    int e;
+    (void)frexp(a, &e);            /* a in [2^(e-1), 2^e) */
+    int qexp = e - 8;              /* quantum of that binade: 8 significant bits */
+    if (qexp < -133) qexp = -133;  /* subnormal grid */
+    double r = nearbyint(ldexp(a, -qexp)); /* exact scaling, then RNE to integer */
+    double v = ldexp(r, qexp);
+    if (v >= 0x1p128) return (uint16_t)(sign | 0x7F80u);
+    float f = (float)v;            /* exact: v has at most 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+/* ---- the output gate ------------------------------------------------------ */
+
+/* RNE_bf16(sigmoid(g)) for a BF16 gate value g, sigmoid taken in double. */
+uint16_t oracle_sigmoid_bf16(uint16_t g) {
+    double x = oracle_double_from_bf16(g);
+    double s = 1.0 / (1.0 + exp(-x));
+    return oracle_bf16_from_double(s);
+}
+
+/* out = RNE_bf16(o * RNE_bf16(sigmoid(gate))), element by element.
+ * The product of two BF16 values is exact in double. */
+void oracle_gate(const uint16_t* o, const uint16_t* gate, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        double ov = oracle_double_from_bf16(o[i]);
+        double sv = oracle_double_from_bf16(oracle_sigmoid_bf16(gate[i]));
+        out[i] = oracle_bf16_from_double(ov * sv);
+    }
+}
+
+/* ---- attention for one (b, h) ---------------------------------------------- */
+
+/* Softmax-weighted sum over the positions [p0, p1) of sequence b for query
+ * head h.  Writes the normalised O (length D) and returns lse = m + ln(sum)
+ * over those positions; an empty range gives O = 0 and lse = -inf. */
+static double attend_range(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                           const int32_t* idx, int64_t p0, int64_t p1,
+                           int Hkv, int kvh, int D, double scale, double* s_buf, double* O) {
+    for (int d = 0; d < D; ++d) O[d] = 0.0;
+    if (p1 <= p0) return -INFINITY;
+    double m = -INFINITY;
+    for (int64_t j = p0; j < p1; ++j) {
+        const uint16_t* krow = k_pool + ((int64_t)idx[j] * Hkv + kvh) * D;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += oracle_double_from_bf16(q[d]) * oracle_double_from_bf16(krow[d]);
+        double s = scale * acc;
+        s_buf[j - p0] = s;
+        if (s > m) m = s;
+    }
+    double z = 0.0;
+    for (int64_t j = p0; j < p1; ++j) {
+        double p = exp(s_buf[j - p0] - m);
+        z += p;
+        const uint16_t* vrow = v_pool + ((int64_t)idx[j] * Hkv + kvh) * D;
+        for (int d = 0; d < D; ++d) O[d] += p * oracle_double_from_bf16(vrow[d]);
+    }
+    for (int d = 0; d < D; ++d) O[d] /= z;
+    return m + log(z);
+}
+
+static int check_inputs(const int32_t* indptr, const int32_t* indices, int64_t num_slots,
+                        int B, int Hq, int Hkv, int D) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return ORACLE_ERR_SHAPE;
+    if (B > 0 && indptr[0] != 0) return ORACLE_ERR_SHAPE;
+    for (int b = 0; b < B; ++b)
+        if (indptr[b + 1] < indptr[b]) return ORACLE_ERR_SHAPE;
+    int64_t nnz = B > 0 ? indptr[B] : 0;
+    for (int64_t j = 0; j < nnz; ++j)
+        if (indices[j] < 0 || indices[j] >= num_slots) return ORACLE_ERR_INDEX;
+    return ORACLE_OK;
+}
+
+/* Full path for the (b, h) pairs listed in `pairs` (2*n_pairs ints: b, h), or
+ * for every pair in row-major order when pairs == NULL.  Outputs are indexed
+ * like the inputs ([B, Hq, D] and [B, Hq]); any output pointer may be NULL.
+ *   o_f64  : O in double, before any rounding
+ *   o_bf16 : RNE_bf16(O)
+ *   out    : the gated output RNE_bf16(o_bf16 * RNE_bf16(sigmoid(gate)))
+ *   lse    : natural-log log-sum-exp of the scaled scores
+ * num_splits > 0 evaluates O through the split-merge formulation instead:
+ * split s covers positions [s*c, min(L, (s+1)*c)) with c = ceil(L / S); each
+ * split gives a normalised partial O_s and lse_s; the merge weights them by
+ * exp(lse_s - max lse) (empty splits weigh 0).  Mathematically it is the same O.
+ */
+int oracle_decode(const uint16_t* q, const uint16_t* gate,
+                  const uint16_t* k_pool, const uint16_t* v_pool,
+                  const int32_t* kv_indptr, const int32_t* kv_indices, int64_t num_slots,
+                  int B, int Hq, int Hkv, int D, double scale, int num_splits,
+                  const int32_t* pairs, int64_t n_pairs,
+                  double* o_f64, uint16_t* o_bf16, uint16_t* out, double* lse, int nthreads) {
+    int rc = check_inputs(kv_indptr, kv_indices, num_slots, B, Hq, Hkv, D);
+    if (rc != ORACLE_OK) return rc;
+    if (num_splits < 0) return ORACLE_ERR_SHAPE;
+    int G = Hq / Hkv;
+    int64_t total = pairs ? n_pairs : (int64_t)B * Hq;
+    int64_t max_len = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t L = kv_indptr[b + 1] - kv_indptr[b];
+        if (L > max_len) max_len = L;
+    }
+    for (int64_t t = 0; t < total; ++t) {
+        int b = pairs ? pairs[2 * t] : (int)(t / Hq);
+        int h = pairs ? pairs[2 * t + 1] : (int)(t % Hq);
+        if (b < 0 || b >= B || h < 0 || h >= Hq) return ORACLE_ERR_SHAPE;
+    }
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel
+    {
+        double* s_buf = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        double* O = (double*)malloc(sizeof(double) * (size_t)D);
+        int ns = num_splits > 0 ? num_splits : 1;
+        double* Os = (double*)malloc(sizeof(double) * (size_t)D * (size_t)ns);
+        double* lse_s = (double*)malloc(sizeof(double) * (size_t)ns);
+        if (!s_buf || !O || !Os || !lse_s) {
+#pragma omp atomic write
+            err = ORACLE_ERR_NOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < total; ++t) {
+                int b = pairs ? pairs[2 * t] : (int)(t / Hq);
+                int h = pairs ? pairs[2 * t + 1] : (int)(t % Hq);
+                int kvh = h / G;
+                const uint16_t* qrow = q + ((int64_t)b * Hq + h) * D;
+                const int32_t* idx = kv_indices + kv_indptr[b];
+                int64_t L = kv_indptr[b + 1] - kv_indptr[b];
+                double l_out;
+                if (num_splits == 0) {
+                    l_out = attend_range(qrow, k_pool, v_pool, idx, 0, L, Hkv, kvh, D, scale, s_buf, O);
+                } else {
+                    /* split-merge: every split's (O_s, lse_s), then the LSE merge */
+                    int64_t c = (L + num_splits - 1) / num_splits;
+                    double M = -INFINITY;
+                    for (int s = 0; s < num_splits; ++s) {
+                        int64_t p0 = (int64_t)s * c, p1 = p0 + c < L ? p0 + c : L;
+                        lse_s[s] = attend_range(qrow, k_pool, v_pool, idx, p0, p1, Hkv, kvh, D, scale,
+                                                s_buf, Os + (int64_t)s * D);
+                        if (lse_s[s] > M) M = lse_s[s];
+                    }
+                    double W = 0.0;
+                    for (int d = 0; d < D; ++d) O[d] = 0.0;
+                    if (M > -INFINITY) {
+                        for (int s = 0; s < num_splits; ++s) {
+                            if (lse_s[s] == -INFINITY) continue;
+                            double w = exp(lse_s[s] - M);
+                            W += w;
+                            for (int d = 0; d < D; ++d) O[d] += w * Os[(int64_t)s * D + d];
+                        }
+                        for (int d = 0; d < D; ++d) O[d] /= W;
+                        l_out = M + log(W);
+                    } else {
+                        l_out = -INFINITY;
+                    }
+                }
+                int64_t base = ((int64_t)b * Hq + h) * D;
+                const uint16_t* grow = gate ? gate + base : NULL;
+                for (int d = 0; d < D; ++d) {
+                    uint16_t ob = oracle_bf16_from_double(O[d]);
+                    if (o_f64) o_f64[base + d] = O[d];
+                    if (o_bf16) o_bf16[base + d] = ob;
+                    if (out && grow) {
+                        double sv = oracle_double_from_bf16(oracle_sigmoid_bf16(grow[d]));
+                        out[base + d] = oracle_bf16_from_double(oracle_double_from_bf16(ob) * sv);
+                    }
+                }
+                if (lse) lse[(int64_t)b * Hq + h] = l_out;
+            }
+        }
+        free(s_buf);
+        free(O);
+        free(Os);
+        free(lse_s);
+    }
+    return err;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
