@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of gated split-KV GQA decode attention on GB300.
+
+One step = one gated decode call (stage 1 + stage 2) over a batch already
+resident in HBM.  Default workload: B=64 sequences x 4096 KV positions, Hq=16,
+Hkv=2, D=256 (538 MB of K/V rows per call, larger than L2, so no flush is
+needed between calls).  Prints ONE JSON line (rank 0):
+
+  value      whole-job achieved HBM GB/s = algorithmic bytes of all ranks' calls
+             / max-over-ranks device time (K+V rows + q + gate + out)
+  e2e        the same through gda.decode with per-step host->device copies of
+             q, gate, kv_indptr, kv_indices and a device->host read of out
+  roofline   stage-1 kernel: algorithmic bytes / its CUDA-event duration vs the
+             measured HBM copy bandwidth
+  cpu_baseline  the FP64 oracle on the host cores (rank 0, N=1)
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  torchrun --nproc-per-node N --master-addr 127.0.0.1 bench.py --gpus N ...
+N > 1 runs independent replicas (each rank its own batch, no collective on the
+data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "gated decode attention µs/call and achieved HBM GB/s vs GB300 peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["gda_stage1.cu", "gda_device.cuh", "gda_kernels.h"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="b64_l4096")
+    p.add_argument("--splits", type=int, default=0, help="num_splits (0: automatic)")
+    p.add_argument("--variant", type=int, default=0, help="0 auto, 1 mma, 2 simt")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget (cpu_baseline)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    os.environ.setdefault("MASTER_PORT", "29533")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power = [], [], []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gated_gqa_attention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, units: int):
+    """DRAM bytes per stage-1 launch from a committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "stage1_%s_traffic.txt" % workload)
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_hash") != kernel_hash():
+            return None
+        per_unit = float(kv["dram_bytes_per_token"])
+        return per_unit * units
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def algorithmic_bytes(lengths, hq, hkv, d):
+    from gated_gqa_attention_gb300 import workloads
+    return workloads.metric_bytes(lengths, hq, hkv, d)
+
+
+def stage1_bytes(lengths, hq, hkv, d):
+    n = sum(lengths)
+    return n * hkv * d * 2 * 2 + len(lengths) * hq * d * 2
+
+
+def oracle_sample_rate(inp, budget_s: float):
+    """Time the FP64 oracle on the host: full batches until the budget is spent."""
+    import oracle
+    w = inp["workload"]
+    nbytes = algorithmic_bytes(inp["lengths"], w.hq, w.hkv, w.head_dim)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
+                      inp["scale"], want=("out",))
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or reps >= 100:
+            break
+    return nbytes * reps / dt / 1e9, reps, dt, oracle.max_threads()
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import gated_gqa_attention_gb300 as gda
+    from gated_gqa_attention_gb300 import workloads
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(world, "nccl")
+    dev_id = local
+    gda.load()
+
+    w = workloads.workload(args.workload)
+    inp = workloads.make_workload(args.workload, seed=w.seed + 1000 * rank)
+    lengths = inp["lengths"]
+    B, Hq, D = inp["q"].shape
+    Hkv = inp["k_pool"].shape[1]
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = torch.empty_like(dev["q"])
+    nbytes = algorithmic_bytes(lengths, Hq, Hkv, D)
+    s1_bytes = stage1_bytes(lengths, Hq, Hkv, D)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
+                      out=out, workspace=ws, scale=inp["scale"], num_splits=args.splits, variant=args.variant)
+
+    ws = torch.empty(gda.workspace_bytes(B, Hq, Hkv, D, args.splits), dtype=torch.uint8, device="cuda")
+    gda.workspace_init(ws)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+
+    # ---- main timed region: K calls, device time by CUDA events on the launch stream
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev_id).uuid)
+        gpu_sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        gpu_sel = str(dev_id)
+    sampler = ClockSampler(gpu_sel)
+    barrier(dist, dev_id)
+    torch.cuda.synchronize()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(dist, dev_id)
+    ms_local = e0.elapsed_time(e1)
+    ms = max_over_ranks(dist, ms_local, torch.device("cuda", dev_id))
+    total_bytes = sum_over_ranks(dist, float(nbytes) * args.steps, torch.device("cuda", dev_id))
+    value = total_bytes / (ms / 1e3) / 1e9
+    err = gda.read_error(ws)
+
+    # ---- stage-1 kernel duration (events around stage 1 of each call)
+    k1 = min(args.steps, 2000)
+    gda.timing_begin(k1)
+    for _ in range(k1):
+        call()
+    n_t, ms_t = gda.timing_end()
+    s1_us = ms_t / max(n_t, 1) * 1e3
+    achieved = s1_bytes / (s1_us / 1e6) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+
+    # ---- end to end through gda.decode with host buffers
+    host = {k: dev[k].cpu().pin_memory() for k in ("q", "gate", "kv_indptr", "kv_indices")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    k_e2e = min(args.steps, 5000)
+
+    def e2e_step():
+        for k, t in host.items():
+            dev[k].copy_(t, non_blocking=True)
+        gda.decode(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
+                   out=out, scale=inp["scale"], num_splits=args.splits)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()   # the host reads the step's result
+
+    for _ in range(3):
+        e2e_step()
+    barrier(dist, dev_id)
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        e2e_step()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, torch.device("cuda", dev_id))
+    e2e_total = sum_over_ranks(dist, float(nbytes) * k_e2e, torch.device("cuda", dev_id))
+    e2e_value = e2e_total / e2e_s / 1e9
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            v, reps, dt, cores = oracle_sample_rate(inp, args.cpu_seconds)
+            cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                   "sample": "%d full pass(es) of workload %s (B=%d) in %.1f s" % (reps, args.workload, B, dt)}
+        traffic = recorded_traffic(args.workload, sum(lengths) * Hkv)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
+            "us_per_call": round(ms / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "lengths": "%d..%d (total %d)" % (min(lengths), max(lengths),
+                                                                                          sum(lengths)),
+                       "Hq": Hq, "Hkv": Hkv, "D": D, "num_splits": args.splits or "auto",
+                       "variant": {0: "auto(mma)", 1: "mma", 2: "simt"}[args.variant],
+                       "bytes_per_call": nbytes,
+                       "l2": "inputs larger than L2 (%.0f MB of K/V rows per call), no flush" % (nbytes / 1e6),
+                       "parallelism": "replicas x%d" % world},
+            "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                         "traffic": traffic, "algorithmic_bytes": s1_bytes, "avg_us": round(s1_us, 3),
+                         "launches_timed": n_t},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": k_e2e,
+                    "us_per_step": round(e2e_s / k_e2e * 1e6, 3)},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+            "device_error_word": err,
+            "gpu": torch.cuda.get_device_name(dev_id),
+        }
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import numpy as np
+    import oracle
+    from gated_gqa_attention_gb300 import workloads
+
+    inp = workloads.make_workload(args.workload)
+    w = inp["workload"]
+    lengths = inp["lengths"]
+    B, G = len(lengths), w.hq // w.hkv
+    groups = [(b, kvh) for b in range(B) for kvh in range(w.hkv)]
+
+    def step(i):
+        b, kvh = groups[i % len(groups)]
+        pairs = np.array([(b, kvh * G + g) for g in range(G)], dtype=np.int32)
+        oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
+                      inp["scale"], pairs=pairs, want=("out",))
+        return lengths[b] * w.head_dim * 2 * 2 + G * 3 * w.head_dim * 2
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        nbytes += step(i)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = ("each step: one (sequence, KV head) group of %d query heads of workload %s, cycling over its %d groups"
+              % (G, args.workload, len(groups)))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "Hq": w.hq, "Hkv": w.hkv, "D": w.head_dim},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

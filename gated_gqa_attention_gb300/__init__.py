@@ -1,0 +1,260 @@
+"""gated_gqa_attention_gb300 -- gated split-KV GQA decode attention for GB300.
+
+A thin ctypes binding over the C ABI in ``include/gda.h`` (``lib/libgda.so``).
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensor metadata, passes device pointers and the current CUDA stream,
+and turns status codes into exceptions.  There is no CPU fallback: without the
+built library every call raises.
+
+    out = decode(q, gate, k_pool, v_pool, kv_indptr, kv_indices, scale=1/16)
+
+computes, per sequence b and query head h (FreeToken PR #781 "Fuse the BF16
+attention output sigmoid gate into the existing Triton decode stage2"):
+
+    O   = softmax(scale * q[b,h] K[rows_b, h // G]^T) V[rows_b, h // G]
+    out = bf16( bf16(O) * bf16(sigmoid(gate[b,h])) )     (round-to-nearest-even)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+__all__ = [
+    "load", "decode", "decode_ex", "gate", "workspace_bytes", "workspace_init", "reserve",
+    "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
+    "VARIANT_SIMT", "MAX_SPLITS", "LIB_PATH",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libgda.so")
+
+VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT = 0, 1, 2
+MAX_SPLITS = 256
+DEVERR_INDEX, DEVERR_TIMEOUT = 0x1, 0x2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GdaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("gate", ctypes.c_void_p), ("k_pool", ctypes.c_void_p),
+        ("v_pool", ctypes.c_void_p), ("kv_indptr", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
+        ("scale", ctypes.c_float), ("num_splits", ctypes.c_int), ("fuse_gate", ctypes.c_int),
+        ("check_indices", ctypes.c_int), ("variant", ctypes.c_int), ("min_chunk", ctypes.c_int),
+    ]
+
+
+def load(path: Optional[str] = None):
+    """Load the C-ABI library (raises when it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                "libgda.so is not built (%s); run `python -m gated_gqa_attention_gb300.build`" % p)
+        lib = ctypes.CDLL(p)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.gda_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        lib.gda_workspace_bytes.restype = ctypes.c_size_t
+        lib.gda_workspace_init.argtypes = [vp, ctypes.c_size_t, vp]
+        lib.gda_workspace_init.restype = i32
+        lib.gda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
+        lib.gda_decode.restype = i32
+        lib.gda_decode_ex.argtypes = [ctypes.POINTER(_Args), vp, ctypes.c_size_t, vp]
+        lib.gda_decode_ex.restype = i32
+        lib.gda_reserve.argtypes = [i32, i32, i32, i32, i32]
+        lib.gda_reserve.restype = i32
+        lib.gda_gate.argtypes = [vp, vp, vp, i64, vp]
+        lib.gda_gate.restype = i32
+        lib.gda_read_error.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_uint32)]
+        lib.gda_read_error.restype = i32
+        lib.gda_status_str.argtypes = [i32]
+        lib.gda_status_str.restype = ctypes.c_char_p
+        lib.gda_timing_begin.argtypes = [i32]
+        lib.gda_timing_begin.restype = i32
+        lib.gda_timing_end.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
+        lib.gda_timing_end.restype = i32
+        lib.gda_version.argtypes = []
+        lib.gda_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def status_str(status: int) -> str:
+    return load().gda_status_str(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().gda_version())
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise GdaError(rc, status_str(rc))
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check_tensor(name, t, dtype, ndim=None, device=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+
+
+def workspace_bytes(B: int, Hq: int, Hkv: int, D: int, num_splits: int = 0) -> int:
+    """Bytes of workspace decode_ex needs (0 for invalid sizes)."""
+    return int(load().gda_workspace_bytes(int(B), int(Hq), int(Hkv), int(D), int(num_splits)))
+
+
+def workspace_init(workspace, stream=None):
+    """Zero a caller-owned workspace's header (its device error word)."""
+    _check(load().gda_workspace_init(ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
+
+
+def reserve(max_B: int, Hq: int = 16, Hkv: int = 2, D: int = 256, max_splits: int = 0):
+    """Grow the library's internal workspace on the current device ahead of graph capture."""
+    _check(load().gda_reserve(int(max_B), int(Hq), int(Hkv), int(D), int(max_splits)))
+
+
+def _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out):
+    import torch
+    _check_tensor("q", q, torch.bfloat16, 3)
+    dev = q.device
+    if gate_t is not None:
+        _check_tensor("gate", gate_t, torch.bfloat16, 3, dev)
+        if gate_t.shape != q.shape:
+            raise ValueError("gate must have q's shape")
+    _check_tensor("k_pool", k_pool, torch.bfloat16, 3, dev)
+    _check_tensor("v_pool", v_pool, torch.bfloat16, 3, dev)
+    if v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool and v_pool must have the same shape")
+    _check_tensor("kv_indptr", kv_indptr, torch.int32, 1, dev)
+    _check_tensor("kv_indices", kv_indices, torch.int32, 1, dev)
+    if kv_indptr.numel() != q.shape[0] + 1:
+        raise ValueError("kv_indptr must have B + 1 entries")
+    if k_pool.shape[2] != q.shape[2]:
+        raise ValueError("head dims of q and the pools differ")
+    if out is not None:
+        _check_tensor("out", out, torch.bfloat16, 3, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+
+
+def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, scale: Optional[float] = None,
+           num_splits: int = 0, stream=None):
+    """Gated GQA decode attention through ``gda_decode`` (library-owned workspace).
+
+    q, gate_t: [B, Hq, D] bf16; k_pool, v_pool: [num_slots, Hkv, D] bf16;
+    kv_indptr: [B+1] int32; kv_indices: [nnz] int32 (all CUDA, contiguous).
+    ``num_splits <= 0`` lets the kernel plan the splits on the device."""
+    import torch
+    _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out)
+    B, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    _check(load().gda_decode(_ptr(q), _ptr(gate_t), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
+                             _ptr(kv_indices), _ptr(out), B, Hq, Hkv, D, float(scale), int(num_splits),
+                             _stream(stream)))
+    return out
+
+
+def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, workspace=None,
+              scale: Optional[float] = None, num_splits: int = 0, fuse_gate: bool = True, lse=None,
+              check_indices: bool = False, variant: int = VARIANT_AUTO, min_chunk: int = 0, stream=None):
+    """``gda_decode_ex``: caller workspace (allocated here when None), optional LSE
+    output, the unfused first half (``fuse_gate=False``), device index checks and
+    the stage-1 variant."""
+    import torch
+    _decode_checks(q, gate_t if fuse_gate else None, k_pool, v_pool, kv_indptr, kv_indices, out)
+    B, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, 2, q.device)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    nbytes = workspace_bytes(B, Hq, Hkv, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+        workspace_init(workspace, stream)
+    a = _Args(q=_ptr(q), gate=_ptr(gate_t) if fuse_gate else None, k_pool=_ptr(k_pool),
+              v_pool=_ptr(v_pool), kv_indptr=_ptr(kv_indptr), kv_indices=_ptr(kv_indices),
+              out=_ptr(out), lse=_ptr(lse), num_slots=int(k_pool.shape[0]), B=B, Hq=Hq, Hkv=Hkv, D=D,
+              scale=float(scale), num_splits=int(num_splits), fuse_gate=1 if fuse_gate else 0,
+              check_indices=1 if check_indices else 0, variant=int(variant), min_chunk=int(min_chunk))
+    _check(load().gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
+                                workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def gate(o, gate_t, out=None, stream=None):
+    """Standalone gate: out = bf16(o * bf16(sigmoid(gate))) element by element."""
+    import torch
+    _check_tensor("o", o, torch.bfloat16)
+    _check_tensor("gate", gate_t, torch.bfloat16, device=o.device)
+    if gate_t.shape != o.shape:
+        raise ValueError("gate must have o's shape")
+    if out is None:
+        out = torch.empty_like(o)
+    _check(load().gda_gate(_ptr(o), _ptr(gate_t), _ptr(out), o.numel(), _stream(stream)))
+    return out
+
+
+def timing_begin(max_calls: int):
+    """Time the stage-1 kernel of the next ``max_calls`` decode calls with CUDA events."""
+    _check(load().gda_timing_begin(int(max_calls)))
+
+
+def timing_end():
+    """(number of timed stage-1 launches, their total milliseconds); synchronises."""
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    _check(load().gda_timing_end(ctypes.byref(n), ctypes.byref(ms)))
+    return int(n.value), float(ms.value)
+
+
+def read_error(workspace=None, clear: bool = True, stream=None) -> int:
+    """The device error word of a workspace (or of the internal one); synchronises."""
+    w = ctypes.c_uint32(0)
+    ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    rc = load().gda_read_error(ptr, _stream(stream), 1 if clear else 0, ctypes.byref(w))
+    if rc not in (0, -9):
+        _check(rc)
+    return int(w.value)

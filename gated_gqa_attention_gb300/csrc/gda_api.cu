@@ -1,0 +1,363 @@
+// gda_api.cu -- the C ABI of include/gda.h: validation, workspace, planning, launches.
+//
+// Host-side checks run before any CUDA call (so they work without a GPU); nothing
+// is read back from the device on the decode path.  gda_decode keeps one workspace
+// per device and grows it with cudaMalloc (never while the stream is capturing);
+// gda_decode_ex takes the caller's workspace and allocates nothing (cuDNN FE-OSS
+// "Gated Attention Block (SM107)", Forward: execute() allocates nothing and is
+// CUDA-graph friendly; FreeToken PR #781, Summary: initialise before capture,
+// validate before launch).
+#include <mutex>
+#include <vector>
+
+#include "gda.h"
+#include "gda_device.cuh"
+#include "gda_kernels.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultMinChunk = 64;
+
+struct DeviceState {
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// stage-1 timing (gda_timing_begin / gda_timing_end)
+std::vector<cudaEvent_t> g_tev;   // pairs: [2i] before stage 1, [2i+1] after
+int g_tmax = 0, g_tused = 0;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_sizes(int B, int Hq, int Hkv, int D, int num_splits) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return GDA_ERR_SHAPE;
+  if (num_splits > GDA_MAX_SPLITS) return GDA_ERR_SPLITS;
+  if (D != gda::kD || Hq / Hkv != gda::kG) return GDA_ERR_UNSUPPORTED;
+  return GDA_OK;
+}
+
+size_t num_pieces(int B, int Hkv, int num_splits) {
+  if (num_splits > 0) return (size_t)B * Hkv * num_splits;
+  return (size_t)gda::kAutoMaxCtas + (size_t)B * Hkv;
+}
+
+struct Layout {
+  size_t o_off, lse_off, total;
+};
+
+Layout layout(int B, int Hq, int Hkv, int D, int num_splits) {
+  const size_t G = (size_t)(Hq / Hkv);
+  const size_t pieces = num_pieces(B, Hkv, num_splits);
+  Layout l;
+  l.o_off = gda::kHeaderBytes;
+  l.lse_off = round_up(l.o_off + pieces * G * (size_t)D * sizeof(float), 256);
+  l.total = round_up(l.lse_off + pieces * G * sizeof(float), 256);
+  return l;
+}
+
+int sm_count(int dev) {
+  if (g_dev[dev].sms == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+    g_dev[dev].sms = n;
+  }
+  return g_dev[dev].sms;
+}
+
+int validate_args(const gda_args* a) {
+  if (a == nullptr) return GDA_ERR_NULL;
+  int rc = check_sizes(a->B, a->Hq, a->Hkv, a->D, a->num_splits);
+  if (rc != GDA_OK) return rc;
+  if (a->check_indices && a->num_slots < 0) return GDA_ERR_SHAPE;
+  if (a->variant < 0 || a->variant > GDA_VARIANT_SIMT) return GDA_ERR_UNSUPPORTED;
+  if (a->min_chunk < 0) return GDA_ERR_SHAPE;
+  if (a->B == 0) return GDA_OK;
+  if (!a->q || !a->k_pool || !a->v_pool || !a->kv_indptr || !a->kv_indices || !a->out) return GDA_ERR_NULL;
+  if (a->fuse_gate && !a->gate) return GDA_ERR_NULL;
+  if (!aligned(a->q, 16) || !aligned(a->k_pool, 16) || !aligned(a->v_pool, 16) || !aligned(a->out, 16) ||
+      (a->gate && !aligned(a->gate, 16)) || !aligned(a->kv_indptr, 4) || !aligned(a->kv_indices, 4) ||
+      (a->lse && !aligned(a->lse, 4)))
+    return GDA_ERR_ALIGN;
+  return GDA_OK;
+}
+
+// Enqueue both stages.  Arguments validated; workspace large enough.
+int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
+  if (a->B == 0) return GDA_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDA_ERR_CUDA;
+  int sms;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    sms = sm_count(dev);
+  }
+  if (sms <= 0) return GDA_ERR_CUDA;
+  const Layout l = layout(a->B, a->Hq, a->Hkv, a->D, a->num_splits);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  int grid;
+  if (a->num_splits > 0) {
+    const long long units = (long long)a->B * a->Hkv * a->num_splits;
+    grid = (int)(units < sms ? units : sms);
+  } else {
+    grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
+  }
+  const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
+
+  gda::Stage1Params p1;
+  p1.q = reinterpret_cast<const __nv_bfloat16*>(a->q);
+  p1.k_pool = reinterpret_cast<const unsigned char*>(a->k_pool);
+  p1.v_pool = reinterpret_cast<const unsigned char*>(a->v_pool);
+  p1.indptr = a->kv_indptr;
+  p1.indices = a->kv_indices;
+  p1.o_part = reinterpret_cast<float*>(base + l.o_off);
+  p1.lse_part = reinterpret_cast<float*>(base + l.lse_off);
+  p1.hdr = reinterpret_cast<gda::WsHeader*>(base);
+  p1.num_slots = a->num_slots;
+  p1.B = a->B;
+  p1.Hq = a->Hq;
+  p1.Hkv = a->Hkv;
+  p1.scale_log2 = a->scale * 1.44269504088896340736f;
+  p1.num_splits = a->num_splits > 0 ? a->num_splits : 0;
+  p1.min_chunk = min_chunk;
+  p1.check_indices = a->check_indices ? 1 : 0;
+  const int variant = (a->variant == GDA_VARIANT_SIMT) ? gda::kVariantSimt : gda::kVariantMma;
+  cudaEvent_t t_end = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_tused < g_tmax) {
+      if (cudaEventRecord(g_tev[2 * g_tused], stream) != cudaSuccess) return GDA_ERR_CUDA;
+      t_end = g_tev[2 * g_tused + 1];
+      ++g_tused;
+    }
+  }
+  if (gda::launch_stage1(p1, variant, grid, stream) != cudaSuccess) return GDA_ERR_CUDA;
+  if (t_end != nullptr && cudaEventRecord(t_end, stream) != cudaSuccess) return GDA_ERR_CUDA;
+
+  gda::Stage2Params p2;
+  p2.gate = reinterpret_cast<const __nv_bfloat16*>(a->gate);
+  p2.indptr = a->kv_indptr;
+  p2.o_part = p1.o_part;
+  p2.lse_part = p1.lse_part;
+  p2.out = reinterpret_cast<__nv_bfloat16*>(a->out);
+  p2.lse_out = a->lse;
+  p2.B = a->B;
+  p2.Hq = a->Hq;
+  p2.Hkv = a->Hkv;
+  p2.num_splits = p1.num_splits;
+  p2.grid1 = grid;
+  p2.min_chunk = min_chunk;
+  p2.fuse_gate = a->fuse_gate ? 1 : 0;
+  if (gda::launch_stage2(p2, stream) != cudaSuccess) return GDA_ERR_CUDA;
+  return GDA_OK;
+}
+
+// Make the internal workspace of the current device at least `need` bytes.
+int ensure_workspace(size_t need, cudaStream_t stream, bool check_capture, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (d.ws_bytes >= need) {
+    *out = d.ws;
+    return GDA_OK;
+  }
+  if (check_capture) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) return GDA_ERR_CUDA;
+    if (st != cudaStreamCaptureStatusNone) return GDA_ERR_CAPTURE;
+  }
+  if (d.ws) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GDA_ERR_CUDA;
+    cudaFree(d.ws);
+    d.ws = nullptr;
+    d.ws_bytes = 0;
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, need) != cudaSuccess) return GDA_ERR_CUDA;
+  if (cudaMemset(p, 0, gda::kHeaderBytes) != cudaSuccess) {
+    cudaFree(p);
+    return GDA_ERR_CUDA;
+  }
+  d.ws = p;
+  d.ws_bytes = need;
+  *out = p;
+  return GDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gda_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits) {
+  if (check_sizes(B, Hq, Hkv, D, num_splits) != GDA_OK) return 0;
+  return layout(B, Hq, Hkv, D, num_splits).total;
+}
+
+int gda_workspace_init(void* workspace, size_t workspace_bytes, gda_stream_t stream) {
+  if (workspace == nullptr) return GDA_ERR_NULL;
+  if (!aligned(workspace, 256)) return GDA_ERR_ALIGN;
+  if (workspace_bytes < (size_t)gda::kHeaderBytes) return GDA_ERR_WORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, gda::kHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDA_ERR_CUDA;
+  return GDA_OK;
+}
+
+int gda_decode_ex(const gda_args* args, void* workspace, size_t workspace_bytes, gda_stream_t stream) {
+  int rc = validate_args(args);
+  if (rc != GDA_OK) return rc;
+  if (args->B == 0) return GDA_OK;
+  if (workspace == nullptr || !aligned(workspace, 256)) return GDA_ERR_WORKSPACE;
+  if (workspace_bytes < gda_workspace_bytes(args->B, args->Hq, args->Hkv, args->D, args->num_splits))
+    return GDA_ERR_WORKSPACE;
+  return enqueue(args, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool, const gda_bf16* v_pool,
+               const int32_t* kv_indptr, const int32_t* kv_indices, gda_bf16* out, int B, int Hq, int Hkv, int D,
+               float scale, int num_splits, gda_stream_t stream) {
+  gda_args a = {};
+  a.q = q;
+  a.gate = gate;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.out = out;
+  a.lse = nullptr;
+  a.num_slots = 0;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.scale = scale;
+  a.num_splits = num_splits;
+  a.fuse_gate = 1;
+  a.check_indices = 0;
+  a.variant = GDA_VARIANT_AUTO;
+  a.min_chunk = 0;
+  int rc = validate_args(&a);
+  if (rc != GDA_OK) return rc;
+  if (B == 0) return GDA_OK;
+  void* ws = nullptr;
+  const size_t need = gda_workspace_bytes(B, Hq, Hkv, D, num_splits);
+  rc = ensure_workspace(need, reinterpret_cast<cudaStream_t>(stream), true, &ws);
+  if (rc != GDA_OK) return rc;
+  return enqueue(&a, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {
+  int rc = check_sizes(max_B, Hq, Hkv, D, max_splits);
+  if (rc != GDA_OK) return rc;
+  // the automatic mode and every explicit split count up to max_splits must fit
+  size_t need = gda_workspace_bytes(max_B, Hq, Hkv, D, 0);
+  if (max_splits > 0) {
+    const size_t e = gda_workspace_bytes(max_B, Hq, Hkv, D, max_splits);
+    if (e > need) need = e;
+  }
+  void* ws = nullptr;
+  return ensure_workspace(need, nullptr, false, &ws);
+}
+
+int gda_gate(const gda_bf16* o, const gda_bf16* gate, gda_bf16* out, int64_t n, gda_stream_t stream) {
+  if (n < 0) return GDA_ERR_SHAPE;
+  if (n == 0) return GDA_OK;
+  if (!o || !gate || !out) return GDA_ERR_NULL;
+  if (!aligned(o, 16) || !aligned(gate, 16) || !aligned(out, 16)) return GDA_ERR_ALIGN;
+  if (gda::launch_gate(reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(gate),
+                       reinterpret_cast<__nv_bfloat16*>(out), (long long)n,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDA_ERR_CUDA;
+  return GDA_OK;
+}
+
+int gda_read_error(const void* workspace, gda_stream_t stream, int clear, uint32_t* error_word) {
+  if (error_word == nullptr) return GDA_ERR_NULL;
+  const void* ws = workspace;
+  if (ws == nullptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    ws = g_dev[dev].ws;
+  }
+  if (ws == nullptr) {
+    *error_word = 0;
+    return GDA_OK;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int w = 0;
+  if (cudaMemcpyAsync(&w, ws, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDA_ERR_CUDA;
+  if (clear && w != 0) {
+    if (cudaMemsetAsync(const_cast<void*>(ws), 0, sizeof(w), s) != cudaSuccess) return GDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDA_ERR_CUDA;
+  }
+  *error_word = w;
+  return w == 0 ? GDA_OK : GDA_ERR_DEVICE;
+}
+
+int gda_timing_begin(int max_calls) {
+  if (max_calls < 0) return GDA_ERR_SHAPE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (cudaEvent_t e : g_tev) cudaEventDestroy(e);
+  g_tev.clear();
+  g_tmax = g_tused = 0;
+  g_tev.resize(2 * (size_t)max_calls, nullptr);
+  for (size_t i = 0; i < g_tev.size(); ++i) {
+    if (cudaEventCreate(&g_tev[i]) != cudaSuccess) {
+      for (size_t j = 0; j < i; ++j) cudaEventDestroy(g_tev[j]);
+      g_tev.clear();
+      return GDA_ERR_CUDA;
+    }
+  }
+  g_tmax = max_calls;
+  return GDA_OK;
+}
+
+int gda_timing_end(int* n_timed, double* total_ms) {
+  if (n_timed == nullptr || total_ms == nullptr) return GDA_ERR_NULL;
+  std::lock_guard<std::mutex> lk(g_mu);
+  double sum = 0.0;
+  int rc = GDA_OK;
+  for (int i = 0; i < g_tused; ++i) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(g_tev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_tev[2 * i], g_tev[2 * i + 1]) != cudaSuccess) {
+      rc = GDA_ERR_CUDA;
+      break;
+    }
+    sum += ms;
+  }
+  *n_timed = rc == GDA_OK ? g_tused : 0;
+  *total_ms = rc == GDA_OK ? sum : 0.0;
+  for (cudaEvent_t e : g_tev) cudaEventDestroy(e);
+  g_tev.clear();
+  g_tmax = g_tused = 0;
+  return rc;
+}
+
+const char* gda_status_str(int status) {
+  switch (status) {
+    case GDA_OK: return "GDA_OK: success";
+    case GDA_ERR_NULL: return "GDA_ERR_NULL: a required pointer is NULL";
+    case GDA_ERR_ALIGN: return "GDA_ERR_ALIGN: a pointer is not aligned (16 bytes for bf16 tensors, 4 for indices)";
+    case GDA_ERR_SHAPE: return "GDA_ERR_SHAPE: invalid sizes (B<0, Hq<1, Hkv<1, Hq%Hkv!=0, negative count)";
+    case GDA_ERR_UNSUPPORTED: return "GDA_ERR_UNSUPPORTED: shape not served by the built kernels (D=256, Hq/Hkv=8)";
+    case GDA_ERR_SPLITS: return "GDA_ERR_SPLITS: num_splits exceeds GDA_MAX_SPLITS";
+    case GDA_ERR_WORKSPACE: return "GDA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case GDA_ERR_CAPTURE: return "GDA_ERR_CAPTURE: workspace growth requested while the stream is capturing";
+    case GDA_ERR_CUDA: return "GDA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case GDA_ERR_DEVICE: return "GDA_ERR_DEVICE: a kernel flagged an error in the workspace error word";
+    default: return "unknown gda status";
+  }
+}
+
+int gda_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// gda_device.cuh -- device helpers shared by the gated decode kernels (sm_103a).
+//
+// * PTX wrappers: mbarrier (init / arrive / expect_tx / bounded parity wait),
+//   1-D bulk copies global -> shared (the TMA bulk engine), L2 eviction
+//   policies, programmatic dependent launch, named barriers.
+// * The work schedule that stage 1 and stage 2 both derive from kv_indptr: which
+//   (sequence, KV head, position range) "pieces" each stage-1 CTA computes and
+//   where each piece's partial result lives.
+// * The BF16 gate arithmetic of FreeToken PR #781 "Fuse the BF16 attention output
+//   sigmoid gate into the existing Triton decode stage2" (Summary): O rounded to
+//   BF16, sigmoid of the gate rounded to BF16, product rounded to nearest even.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gda {
+
+// Geometry the kernels are built for (FreeToken PR #781, Automatic dispatch:
+// query [1,16,256] with two KV heads -> D = 256, G = 8 query heads per KV head).
+constexpr int kD = 256;
+constexpr int kG = 8;
+constexpr int kRowBytes = kD * 2;          // one (slot, KV head) row of K or V
+constexpr int kSmemRow = kRowBytes + 16;   // padded shared-memory row: conflict-free ldmatrix
+constexpr int kAutoMaxCtas = 1024;         // bound on the automatic-mode stage-1 grid
+constexpr int kHeaderBytes = 256;          // workspace header
+constexpr uint32_t kErrIndex = 0x1u;
+constexpr uint32_t kErrTimeout = 0x2u;
+// A pipeline wait gives up after this many SM cycles (~2 s): only a kernel bug
+// can get there; the kernel then records kErrTimeout and winds down.
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+struct WsHeader {
+  unsigned int error;   // kErr* bits, sticky until read and cleared by the host
+  unsigned int pad[63];
+};
+static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up (returns
+// false) when *abort_flag becomes nonzero or after kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue / wait for the previous kernel's results.  No-ops without PDL.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ work schedule
+//
+// Stage 1 runs a persistent grid of `grid` CTAs.  The KV stream of the batch is
+// ordered by (sequence b, KV head kvh, position j); segment sigma = b*Hkv + kvh
+// holds L_b positions.  A "piece" is the part of one segment one CTA computes; it
+// yields one partial (normalised O for the G query heads, and their LSE).
+//
+// Explicit mode (num_splits S > 0): every segment is cut into S splits, split s
+//   covering positions [s*c, min(L, (s+1)*c)), c = ceil(L/S).  Unit u = sigma*S + s
+//   goes to CTA u % grid; the partial lives at index u.  Empty splits are skipped
+//   by both stages.
+// Automatic mode (S <= 0): the whole stream of total = Hkv * nnz positions is cut
+//   into chunks of T = max(ceil(total/grid), min_chunk) positions, chunk c to CTA c;
+//   the piece (segment sigma, chunk c) lives at index c + sigma.  That index is
+//   unique (a later chunk can only meet a later-or-equal segment) and below
+//   grid + B*Hkv, which bounds the workspace.
+
+struct Piece {
+  int b, kvh, sigma;
+  int j0, j1;       // positions [j0, j1) of sequence b
+  long long id;     // partial index
+};
+
+struct Sched {
+  const int* indptr;
+  int B, Hkv, S, grid, cta;
+  long long T, total;
+  // iteration state
+  long long pos, end;  // automatic
+  int b;
+  long long u;         // explicit
+
+  __device__ __forceinline__ void begin(const int* indptr_, int B_, int Hkv_, int S_, int grid_,
+                                        int cta_, int min_chunk) {
+    indptr = indptr_;
+    B = B_;
+    Hkv = Hkv_;
+    S = S_;
+    grid = grid_;
+    cta = cta_;
+    if (S > 0) {
+      u = cta;
+      return;
+    }
+    total = (long long)Hkv * (long long)__ldg(indptr + B);
+    T = auto_chunk(total, grid, min_chunk);
+    pos = (long long)cta * T;
+    end = min(total, pos + T);
+    b = 0;
+    if (pos < end) {
+      // first sequence whose (Hkv-scaled) end lies beyond pos
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if ((long long)Hkv * __ldg(indptr + mid + 1) > pos) hi = mid; else lo = mid + 1;
+      }
+      b = lo;
+    }
+  }
+
+  static __device__ __forceinline__ long long auto_chunk(long long total, int grid, int min_chunk) {
+    long long t = (total + grid - 1) / grid;
+    return t > min_chunk ? t : (long long)min_chunk;
+  }
+
+  __device__ __forceinline__ bool next(Piece& p) {
+    if (S > 0) {
+      const long long units = (long long)B * Hkv * S;
+      while (u < units) {
+        const long long uu = u;
+        u += grid;
+        const int sigma = (int)(uu / S), s = (int)(uu % S);
+        const int bb = sigma / Hkv;
+        const int L = __ldg(indptr + bb + 1) - __ldg(indptr + bb);
+        const int c = (L + S - 1) / S;
+        const int j0 = s * c;
+        const int j1 = min(L, j0 + c);
+        if (j0 >= j1) continue;
+        p.b = bb;
+        p.kvh = sigma % Hkv;
+        p.sigma = sigma;
+        p.j0 = j0;
+        p.j1 = j1;
+        p.id = uu;
+        return true;
+      }
+      return false;
+    }
+    if (pos >= end) return false;
+    while ((long long)Hkv * __ldg(indptr + b + 1) <= pos) ++b;
+    const int ib = __ldg(indptr + b);
+    const long long base = (long long)Hkv * ib;
+    const int L = __ldg(indptr + b + 1) - ib;
+    const long long off = pos - base;
+    const int kvh = (int)(off / L);
+    const int j0 = (int)(off - (long long)kvh * L);
+    const long long seg_end = base + (long long)(kvh + 1) * L;
+    const long long stop = min(end, seg_end);
+    p.b = b;
+    p.kvh = kvh;
+    p.sigma = b * Hkv + kvh;
+    p.j0 = j0;
+    p.j1 = j0 + (int)(stop - pos);
+    p.id = (long long)cta + p.sigma;
+    pos = stop;
+    return true;
+  }
+};
+
+// Partials of segment (b, kvh) for stage 2: ids first + k, k in [0, n) (automatic
+// mode: first = c_first + sigma), or sigma*S + k (explicit mode), in position order.
+__device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh, int Hkv, int B, int S,
+                                               int grid, int min_chunk, long long* first, int* n) {
+  const int ib = __ldg(indptr + b);
+  const int L = __ldg(indptr + b + 1) - ib;
+  const int sigma = b * Hkv + kvh;
+  if (L <= 0) {
+    *first = 0;
+    *n = 0;
+    return;
+  }
+  if (S > 0) {
+    const int c = (L + S - 1) / S;
+    *first = (long long)sigma * S;
+    *n = (L + c - 1) / c;
+    return;
+  }
+  const long long total = (long long)Hkv * (long long)__ldg(indptr + B);
+  const long long T = Sched::auto_chunk(total, grid, min_chunk);
+  const long long start = (long long)Hkv * ib + (long long)kvh * L;
+  const long long c0 = start / T, c1 = (start + L - 1) / T;
+  *first = c0 + sigma;
+  *n = (int)(c1 - c0 + 1);
+}
+
+// ------------------------------------------------------------------ BF16 gate arithmetic
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Round a double to BF16 (nearest, ties to even) without double rounding: first
+// to float with round-to-odd (truncate, then set the last bit if anything was
+// dropped), which keeps 16 more bits than BF16 has, then float -> BF16 RNE.
+// (Round-to-odd as an intermediate step is exact for any target with at least
+// two fewer bits: Boldo & Melquiond, "Emulation of FMA and correctly rounded
+// sums: proved algorithms using rounding to odd", IEEE TC 2008.)
+__device__ __forceinline__ uint16_t bf16_rne_from_double(double x) {
+  float f = __double2float_rz(x);
+  if ((double)f != x && !isnan(x)) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// BF16 bits of RNE(sigmoid(g)) for a BF16 gate g, exact for all 65 536 codes.
+// Fast path in float: e = expf(-|g|) (documented max error 2 ulp), 1 + e and the
+// division correctly rounded, so the float sigmoid is within a few ulp of the
+// real value.  When its low 16 bits lie within 16 ulp of a BF16 rounding tie the
+// decision is retaken in double (exp with max error 1 ulp); |g| > 80, the
+// infinities and NaN go the double way too.  Exhaustively tested on the GPU
+// against the FP64 oracle.
+__device__ __forceinline__ uint16_t sigmoid_bf16(uint16_t gbits) {
+  const float g = bf16_bits_to_float(gbits);
+  const float a = fabsf(g);
+  if (a <= 80.0f) {
+    const float e = expf(-a);
+    const float den = __fadd_rn(1.0f, e);
+    const float s = (g >= 0.0f) ? __fdiv_rn(1.0f, den) : __fdiv_rn(e, den);
+    const uint32_t low = __float_as_uint(s) & 0xFFFFu;
+    if (low - 0x7FF0u > 0x20u) return __bfloat16_as_ushort(__float2bfloat16_rn(s));
+  }
+  const double gd = (double)g;
+  return bf16_rne_from_double(1.0 / (1.0 + exp(-gd)));
+}
+
+// RNE_bf16(o * s) for BF16 o and s.  The float product is exact unless it falls
+// below the float normal range, where it is redone exactly in double.
+__device__ __forceinline__ uint16_t gate_product_bf16(uint16_t obits, uint16_t sbits) {
+  const float o = bf16_bits_to_float(obits);
+  const float s = bf16_bits_to_float(sbits);
+  const float p = __fmul_rn(o, s);
+  if (fabsf(p) < 1.17549435e-38f && p != 0.0f) return bf16_rne_from_double((double)o * (double)s);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(p));
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+}  // namespace gda

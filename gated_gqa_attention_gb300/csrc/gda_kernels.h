@@ -1,0 +1,54 @@
+// gda_kernels.h -- launch interface between the C ABI (gda_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gda {
+
+struct WsHeader;
+
+constexpr int kVariantMma = 1;
+constexpr int kVariantSimt = 2;
+
+struct Stage1Params {
+  const __nv_bfloat16* q;
+  const unsigned char* k_pool;
+  const unsigned char* v_pool;
+  const int* indptr;
+  const int* indices;
+  float* o_part;       // [pieces][G][D]
+  float* lse_part;     // [pieces][G], log2 units
+  WsHeader* hdr;
+  long long num_slots;
+  int B, Hq, Hkv;
+  float scale_log2;    // scale * log2(e)
+  int num_splits;      // > 0 explicit, else automatic
+  int min_chunk;       // automatic mode
+  int check_indices;
+};
+
+struct Stage2Params {
+  const __nv_bfloat16* gate;
+  const int* indptr;
+  const float* o_part;
+  const float* lse_part;
+  __nv_bfloat16* out;
+  float* lse_out;      // [B, Hq] natural log, or nullptr
+  int B, Hq, Hkv;
+  int num_splits;
+  int grid1;           // stage-1 grid (automatic-mode chunking)
+  int min_chunk;
+  int fuse_gate;
+};
+
+// Stage 1: grid CTAs, persistent.  Returns the launch status.
+cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStream_t stream);
+// Stage 2: FP32 LSE merge + gate epilogue, launched as a programmatic dependent of stage 1.
+cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream);
+// Standalone gate over n elements.
+cudaError_t launch_gate(const __nv_bfloat16* o, const __nv_bfloat16* gate, __nv_bfloat16* out, long long n,
+                        cudaStream_t stream);
+
+}  // namespace gda

@@ -159,12 +159,13 @@ def make(lengths: Sequence[int], *, seed: int, hq: int = HQ, hkv: int = HKV,
                 scale=float(scale), lengths=lengths, num_slots=slots)
 
 
-def make_workload(key, batch_limit: Optional[int] = None) -> dict:
+def make_workload(key, batch_limit: Optional[int] = None, seed: Optional[int] = None) -> dict:
     """Inputs of one of the five named workloads (``batch_limit`` keeps the
-    first sequences only, for bounded CPU timing; the draw is unchanged)."""
+    first sequences only, for bounded CPU timing; the draw is unchanged;
+    ``seed`` replaces the workload's seed, e.g. for independent replicas)."""
     w = workload(key)
     rl = (w.len_lo, w.len_hi, w.batch) if w.lengths is None else None
-    d = make(w.lengths if w.lengths is not None else [], seed=w.seed, hq=w.hq, hkv=w.hkv,
+    d = make(w.lengths if w.lengths is not None else [], seed=w.seed if seed is None else seed, hq=w.hq, hkv=w.hkv,
              head_dim=w.head_dim, layout=w.layout, pool_slots=w.pool_slots, page=w.page,
              gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl)
     d["workload"] = w

@@ -1,0 +1,183 @@
+/*
+ * gda.h -- gated split-KV GQA decode attention on GB300 (sm_103a): the C ABI.
+ *
+ * One decode token per sequence attends, per query head, to the KV rows that a
+ * CSR slot index names in a paged (page size 1) KV pool; the attention output is
+ * then gated by the sigmoid of a second projection of the same shape:
+ *
+ *   out[b,h,:] = RNE_bf16( RNE_bf16(O[b,h,:]) * RNE_bf16(sigmoid(gate[b,h,:])) )
+ *   O[b,h,:]   = softmax_j(scale * q[b,h,:] . K[slot_j, h/G, :]) V[slot_j, h/G, :]
+ *   slot_j     = kv_indices[kv_indptr[b] + j],  0 <= j < kv_indptr[b+1]-kv_indptr[b]
+ *
+ * with G = Hq / Hkv consecutive query heads sharing one KV head.  Sources: FreeToken
+ * PR #781 "Fuse the BF16 attention output sigmoid gate into the existing Triton
+ * decode stage2" (Summary: split-KV stage 1, FP32 LSE merge in stage 2 with the
+ * BF16 gate and an explicit round-to-nearest-even product fused into its epilogue;
+ * Automatic dispatch: query [1,16,256], two KV heads, contiguous BF16 tensors, a
+ * CSR index, default scale); cuDNN FE-OSS "Gated Attention Block (SM107)"
+ * (Overview, stages (4) SDPA with GQA and (5) gate; Forward: the caller passes
+ * one workspace, execute allocates nothing and reads nothing back).
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller.  The library never
+ *    frees or retains them and never writes to an input.
+ *  - Every tensor is contiguous and 16-byte aligned.  BF16 values are passed as
+ *    their 16-bit patterns (gda_bf16).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) and the call returns without waiting for it.  No call except
+ *    gda_read_error reads anything back from the device.
+ *  - The return value is GDA_OK (0) or a negative gda_status; on an error nothing
+ *    has been enqueued.  Host-side checks (pointers, shapes, alignment, sizes) run
+ *    before any CUDA call, so they work without a GPU.
+ *  - Index contents are not validated on the host (that would need a read back):
+ *    an index outside [0, num_slots) is undefined behaviour unless
+ *    gda_args.check_indices is set.
+ */
+#ifndef GDA_H
+#define GDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gda_bf16;                 /* bfloat16 bit pattern */
+typedef struct CUstream_st* gda_stream_t;   /* the same type as cudaStream_t */
+
+typedef enum gda_status {
+    GDA_OK = 0,
+    GDA_ERR_NULL = -1,          /* a required pointer is NULL */
+    GDA_ERR_ALIGN = -2,         /* a pointer is not 16-byte aligned */
+    GDA_ERR_SHAPE = -3,         /* B < 0, Hq < 1, Hkv < 1, Hq % Hkv != 0, num_slots < 0, n < 0 */
+    GDA_ERR_UNSUPPORTED = -4,   /* a shape the built kernels do not serve (D != 256 or
+                                   Hq/Hkv != 8): declined, never run slowly */
+    GDA_ERR_SPLITS = -5,        /* num_splits > GDA_MAX_SPLITS */
+    GDA_ERR_WORKSPACE = -6,     /* workspace NULL, misaligned or smaller than gda_workspace_bytes */
+    GDA_ERR_CAPTURE = -7,       /* the internal workspace must grow while `stream` is capturing */
+    GDA_ERR_CUDA = -8,          /* a CUDA runtime call or launch failed */
+    GDA_ERR_DEVICE = -9         /* gda_read_error: a kernel flagged an error (see the bits below) */
+} gda_status;
+
+#define GDA_MAX_SPLITS 256
+/* Bits of the device error word (gda_read_error). */
+#define GDA_DEVERR_INDEX 0x1u    /* an index outside [0, num_slots) (check_indices only) */
+#define GDA_DEVERR_TIMEOUT 0x2u  /* a pipeline wait gave up (kernel bug guard; never expected) */
+
+/* Stage-1 kernel variant (gda_args.variant). */
+#define GDA_VARIANT_AUTO 0       /* the fastest built variant (tensor-core tiles) */
+#define GDA_VARIANT_MMA 1        /* QK and PV on mma.sync m16n8k16 bf16 tiles */
+#define GDA_VARIANT_SIMT 2       /* QK and PV as FP32 FMAs with warp-shuffle reductions */
+
+/*
+ * Full argument set of gda_decode_ex.
+ *   q, gate     [B, Hq, D] bf16            query and gate of the decode token
+ *   k_pool      [num_slots, Hkv, D] bf16   K rows, one token per slot
+ *   v_pool      [num_slots, Hkv, D] bf16   V rows
+ *   kv_indptr   [B + 1] int32              CSR row pointer, kv_indptr[0] == 0, non-decreasing
+ *   kv_indices  [kv_indptr[B]] int32       slot of each position, in position order
+ *   out         [B, Hq, D] bf16            result (may not alias an input)
+ *   lse         [B, Hq] float or NULL      natural-log log-sum-exp of the scaled scores
+ *                                          (-inf for a zero-length sequence)
+ *   num_slots   rows in the pools (used only by check_indices)
+ *   scale       score scale (1/sqrt(D) is the pages' default)
+ *   num_splits  > 0: every sequence is cut into exactly num_splits contiguous KV
+ *               splits (split s covers positions [s*c, min(L, (s+1)*c)), c = ceil(L/S));
+ *               <= 0: automatic -- the kernel cuts the concatenated KV stream of the
+ *               whole batch into equal chunks, one per resident CTA, from kv_indptr
+ *               on the device (no read back), so ragged batches stay balanced.
+ *   fuse_gate   1: out is the gated result.  0: out = RNE_bf16(O) without the gate (the
+ *               first half of the unfused path; gda_gate is the second).
+ *   check_indices 1: every index is checked on the device; a bad row is read as zeros and
+ *               GDA_DEVERR_INDEX is set in the workspace's error word.
+ *   variant     GDA_VARIANT_* (stage-1 arithmetic).
+ *   min_chunk   automatic mode: smallest chunk in tokens per CTA (0: built-in default).
+ */
+typedef struct gda_args {
+    const gda_bf16* q;
+    const gda_bf16* gate;
+    const gda_bf16* k_pool;
+    const gda_bf16* v_pool;
+    const int32_t* kv_indptr;
+    const int32_t* kv_indices;
+    gda_bf16* out;
+    float* lse;
+    int64_t num_slots;
+    int B, Hq, Hkv, D;
+    float scale;
+    int num_splits;
+    int fuse_gate;
+    int check_indices;
+    int variant;
+    int min_chunk;
+} gda_args;
+
+/* Bytes of workspace gda_decode_ex needs for these sizes (FreeToken PR #781 Summary:
+ * stage 1 writes per-split partial O and LSE that stage 2 merges).  The workspace
+ * holds a 256-byte header (error word, plan), then FP32 partials
+ * [pieces][G][D] and partial LSE [pieces][G].  Returns 0 for invalid sizes. */
+size_t gda_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
+
+/* Zero the workspace header (error word) on `stream`.  Call once after allocating
+ * a workspace for gda_decode_ex; partial buffers need no initialisation. */
+int gda_workspace_init(void* workspace, size_t workspace_bytes, gda_stream_t stream);
+
+/* Gated GQA decode attention with library-owned workspace (FreeToken PR #781,
+ * Summary and Automatic dispatch).  Two kernels are enqueued: stage 1 (split
+ * partial softmax(q K^T scale) V with running max and LSE) and stage 2 (FP32 LSE
+ * merge and the BF16 gate epilogue), the second with programmatic dependent launch.
+ * The internal workspace is one per device, shared by every stream: calls that may
+ * overlap on different streams must use gda_decode_ex with separate workspaces.
+ * It grows with cudaMalloc when needed; growth is refused with GDA_ERR_CAPTURE while
+ * `stream` is capturing (call gda_reserve before capturing a graph). */
+int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool,
+               const gda_bf16* v_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+               gda_bf16* out, int B, int Hq, int Hkv, int D, float scale, int num_splits,
+               gda_stream_t stream);
+
+/* As gda_decode with the full argument set and a caller-owned workspace of at least
+ * gda_workspace_bytes(B, Hq, Hkv, D, num_splits) bytes (256-byte aligned).
+ * Allocates nothing and reads nothing back (cuDNN FE-OSS "Gated Attention Block
+ * (SM107)", Forward: execute() allocates nothing), so it can be graph-captured. */
+int gda_decode_ex(const gda_args* args, void* workspace, size_t workspace_bytes,
+                  gda_stream_t stream);
+
+/* Grow the internal workspace of the current device for calls up to these sizes,
+ * so later gda_decode calls allocate nothing (FreeToken PR #781, Summary:
+ * initialise before capture). */
+int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
+
+/* Standalone gate, the second half of the unfused path (FreeToken PR #781,
+ * Correctness: the fused output equals Torch sigmoid followed by Torch multiply):
+ *   out[i] = RNE_bf16( o[i] * RNE_bf16(sigmoid(gate[i])) ),  0 <= i < n.
+ * o, gate, out: [n] bf16 device arrays (16-byte aligned; out may alias o). */
+int gda_gate(const gda_bf16* o, const gda_bf16* gate, gda_bf16* out, int64_t n,
+             gda_stream_t stream);
+
+/* Read (and with clear != 0, reset) the device error word of a workspace -- or of
+ * the internal workspace when workspace == NULL.  Synchronises `stream`.  Returns
+ * GDA_OK when the word is zero, GDA_ERR_DEVICE otherwise; *error_word gets the bits. */
+int gda_read_error(const void* workspace, gda_stream_t stream, int clear, uint32_t* error_word);
+
+/* Stage timing for benchmarks.  After gda_timing_begin(max_calls), each of the next
+ * max_calls decode calls (any entry point, any stream) records a CUDA event pair
+ * around its stage-1 kernel on its launch stream; stage 2 of those calls then starts
+ * after the event instead of overlapping stage 1's tail.  gda_timing_end waits for
+ * the recorded events and returns how many stage-1 launches were timed and their
+ * summed duration in milliseconds, then releases the events.  Not thread-safe
+ * against concurrent decode calls from other threads. */
+int gda_timing_begin(int max_calls);
+int gda_timing_end(int* n_timed, double* total_ms);
+
+/* Static description of a status code. */
+const char* gda_status_str(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int gda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDA_H */

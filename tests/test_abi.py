@@ -1,0 +1,156 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function that
+include/gda.h declares, and its host-side validation answers before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_gqa_attention_gb300 as gda
+from gated_gqa_attention_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gda.h")
+
+OK, ERR_NULL, ERR_ALIGN, ERR_SHAPE, ERR_UNSUPPORTED, ERR_SPLITS, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5, -6
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()  # nvcc cross-compiles without a GPU
+    return gda.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+\**(gda_[A-Za-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gda_decode", "gda_decode_ex", "gda_workspace_bytes", "gda_reserve", "gda_gate",
+                     "gda_status_str", "gda_read_error", "gda_workspace_init", "gda_version"):
+        assert required in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code in range(-9, 1):
+        s = gda.status_str(code)
+        assert s.startswith("GDA_"), s
+    assert "unknown" in gda.status_str(-100)
+    assert gda.version() >= 100
+
+
+def test_workspace_bytes(lib):
+    G, D = 8, 256
+    piece = G * D * 4 + G * 4
+    # explicit splits: B * Hkv * S pieces (+ header, 256-byte rounding)
+    b = gda.workspace_bytes(64, 16, 2, 256, 8)
+    assert b >= 256 + 64 * 2 * 8 * piece and b % 256 == 0
+    assert b - (256 + 64 * 2 * 8 * piece) < 1024
+    # automatic mode: bounded by the stage-1 grid cap + B * Hkv pieces
+    a = gda.workspace_bytes(64, 16, 2, 256, 0)
+    assert a >= 256 + (1024 + 128) * piece
+    # invalid or unsupported sizes -> 0
+    assert gda.workspace_bytes(-1, 16, 2, 256, 0) == 0
+    assert gda.workspace_bytes(4, 16, 3, 256, 0) == 0      # Hq % Hkv
+    assert gda.workspace_bytes(4, 16, 2, 128, 0) == 0      # D unsupported
+    assert gda.workspace_bytes(4, 16, 4, 256, 0) == 0      # group of 4 unsupported
+    assert gda.workspace_bytes(4, 16, 2, 256, 257) == 0    # too many splits
+
+
+def _decode(lib, ptrs=None, B=1, Hq=16, Hkv=2, D=256, scale=0.0625, splits=0):
+    p = dict(q=16, gate=16, k=16, v=16, indptr=16, indices=16, out=16)
+    if ptrs:
+        p.update(ptrs)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.gda_decode(vp(p["q"]), vp(p["gate"]), vp(p["k"]), vp(p["v"]), vp(p["indptr"]),
+                          vp(p["indices"]), vp(p["out"]), B, Hq, Hkv, D, scale, splits, None)
+
+
+def test_decode_host_validation(lib):
+    # every case below is rejected before any CUDA call (no GPU needed)
+    assert _decode(lib, {"q": 0}) == ERR_NULL
+    assert _decode(lib, {"gate": 0}) == ERR_NULL
+    assert _decode(lib, {"indices": 0}) == ERR_NULL
+    assert _decode(lib, {"out": 0}) == ERR_NULL
+    assert _decode(lib, {"q": 24}) == ERR_ALIGN
+    assert _decode(lib, {"k": 8}) == ERR_ALIGN
+    assert _decode(lib, {"indptr": 2}) == ERR_ALIGN
+    assert _decode(lib, B=-1) == ERR_SHAPE
+    assert _decode(lib, Hq=16, Hkv=3) == ERR_SHAPE
+    assert _decode(lib, Hkv=0) == ERR_SHAPE
+    assert _decode(lib, D=128) == ERR_UNSUPPORTED
+    assert _decode(lib, Hq=8, Hkv=2) == ERR_UNSUPPORTED
+    assert _decode(lib, splits=300) == ERR_SPLITS
+    # B == 0 is a valid empty call: nothing to do, no pointer needed
+    assert _decode(lib, {"q": 0, "gate": 0, "k": 0, "v": 0, "indptr": 0, "indices": 0, "out": 0}, B=0) == OK
+
+
+def test_decode_ex_host_validation(lib):
+    args = gda._Args(q=16, gate=16, k_pool=16, v_pool=16, kv_indptr=16, kv_indices=16, out=16, lse=None,
+                     num_slots=10, B=2, Hq=16, Hkv=2, D=256, scale=0.0625, num_splits=0, fuse_gate=1,
+                     check_indices=0, variant=0, min_chunk=0)
+    call = lambda a, ws=256, nbytes=1 << 30: lib.gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(ws) if ws else None,
+                                                               nbytes, None)
+    assert lib.gda_decode_ex(None, None, 0, None) == ERR_NULL
+    assert call(args, ws=0) == ERR_WORKSPACE
+    assert call(args, ws=128) == ERR_WORKSPACE                       # not 256-aligned
+    assert call(args, nbytes=1024) == ERR_WORKSPACE                  # too small
+    a2 = gda._Args.from_buffer_copy(args)
+    a2.variant = 7
+    assert call(a2) == ERR_UNSUPPORTED
+    a3 = gda._Args.from_buffer_copy(args)
+    a3.gate = None
+    assert call(a3) == ERR_NULL                                       # gate needed when fused
+    a3.fuse_gate = 0
+    a3.q = 8
+    assert call(a3) == ERR_ALIGN                                      # gate may be absent unfused
+    a4 = gda._Args.from_buffer_copy(args)
+    a4.check_indices, a4.num_slots = 1, -1
+    assert call(a4) == ERR_SHAPE
+    a5 = gda._Args.from_buffer_copy(args)
+    a5.lse = 2
+    assert call(a5) == ERR_ALIGN
+
+
+def test_gate_and_misc_host_validation(lib):
+    vp = ctypes.c_void_p
+    assert lib.gda_gate(vp(16), vp(16), vp(16), -1, None) == ERR_SHAPE
+    assert lib.gda_gate(None, None, None, 0, None) == OK              # empty
+    assert lib.gda_gate(None, vp(16), vp(16), 8, None) == ERR_NULL
+    assert lib.gda_gate(vp(16), vp(18), vp(16), 8, None) == ERR_ALIGN
+    assert lib.gda_reserve(4, 16, 2, 128, 0) == ERR_UNSUPPORTED
+    assert lib.gda_workspace_init(None, 1024, None) == ERR_NULL
+    assert lib.gda_workspace_init(vp(128), 1024, None) == ERR_ALIGN
+    assert lib.gda_workspace_init(vp(256), 16, None) == ERR_WORKSPACE
+    w = ctypes.c_uint32()
+    assert lib.gda_read_error(None, None, 0, None) == ERR_NULL
+
+
+def test_product_path_has_no_cpu_fallback():
+    # the binding refuses to run without the library rather than computing elsewhere
+    import importlib
+    pkg = os.path.join(ROOT, "gated_gqa_attention_gb300")
+    for name in os.listdir(pkg):
+        if name.endswith(".py"):
+            src = open(os.path.join(pkg, name)).read()
+            assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), name
+    for name in os.listdir(os.path.join(pkg, "csrc")):
+        src = open(os.path.join(pkg, "csrc", name)).read()
+        assert not re.search(r"#include\s+[<\"].*oracle", src), name
+    mod = importlib.import_module("gated_gqa_attention_gb300")
+    with pytest.raises(RuntimeError):
+        mod._lib_saved = mod._lib
+        try:
+            mod._lib = None
+            mod.load(os.path.join(ROOT, "does-not-exist", "libgda.so"))
+        finally:
+            mod._lib = mod._lib_saved
