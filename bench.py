@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 mma, 2 simt")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget (cpu_baseline)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kernel-only", action="store_true",
+                   help="warm-up + K calls and exit (the command profiled under ncu); prints nothing")
     return p.parse_args(argv)
 
 
@@ -249,6 +251,13 @@ def run_ours(args):
     for _ in range(max(args.warmup, 3)):
         call()
     torch.cuda.synchronize()
+    if args.kernel_only:
+        for _ in range(args.steps):
+            call()
+        torch.cuda.synchronize()
+        if gda.read_error(ws) != 0:
+            raise SystemExit("device error word set")
+        return None
 
     # ---- main timed region: K calls, device time by CUDA events on the launch stream
     try:

@@ -199,27 +199,36 @@ struct MathSimt {
     }
   }
 
+  __device__ __forceinline__ void finish_sums() {}
+
   // Publish this warp's running max (phase 1 of the CTA merge).
   template <int NCW>
   __device__ __forceinline__ void publish_max(float (*mbuf)[kG], int w, int lane) {
     if ((lane & 3) == 0) mbuf[w][lane >> 2] = m;
   }
 
-  // Add this warp's state, rescaled to the CTA-wide max, into obuf / lbuf.
+  // Store (first warp) or add this warp's state, rescaled to the CTA-wide max,
+  // into obuf / lbuf.  Every address is written by one lane, warps in a fixed order.
   template <int NCW>
   __device__ __forceinline__ void accumulate(const float (*mbuf)[kG], float (*obuf)[kD], float* lbuf, int w,
-                                             int lane) {
+                                             int lane, bool first) {
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
       float M = mbuf[0][h];
 #pragma unroll
       for (int x = 1; x < NCW; ++x) M = fmaxf(M, mbuf[x][h]);
       const float f = (M == -INFINITY) ? 0.0f : safe_exp2_diff(mbuf[w][h], M);
-      if (f != 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) atomicAdd(&obuf[h][lane * 8 + i], acc[h][i] * f);
+      float4* dst = reinterpret_cast<float4*>(&obuf[h][lane * 8]);
+      float4 a = make_float4(acc[h][0] * f, acc[h][1] * f, acc[h][2] * f, acc[h][3] * f);
+      float4 b = make_float4(acc[h][4] * f, acc[h][5] * f, acc[h][6] * f, acc[h][7] * f);
+      if (!first) {
+        const float4 a0 = dst[0], b0 = dst[1];
+        a.x += a0.x; a.y += a0.y; a.z += a0.z; a.w += a0.w;
+        b.x += b0.x; b.y += b0.y; b.z += b0.z; b.w += b0.w;
       }
-      if ((lane & 3) == 0 && (lane >> 2) == h && f != 0.0f) atomicAdd(&lbuf[h], l * f);
+      dst[0] = a;
+      dst[1] = b;
+      if ((lane & 3) == 0 && (lane >> 2) == h) lbuf[h] = first ? l * f : lbuf[h] + l * f;
     }
   }
 };
@@ -321,14 +330,19 @@ struct MathMma {
     }
   }
 
-  template <int NCW>
-  __device__ __forceinline__ void accumulate(const float (*mbuf)[kG], float (*obuf)[kD], float* lbuf, int w,
-                                             int lane) {
+  // Reduce the per-lane running sums over the 8 lanes that share a head pair
+  // (done by every warp before the ordered accumulation).
+  __device__ __forceinline__ void finish_sums() {
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+  }
+
+  template <int NCW>
+  __device__ __forceinline__ void accumulate(const float (*mbuf)[kG], float (*obuf)[kD], float* lbuf, int w,
+                                             int lane, bool first) {
     const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
     float Ma = mbuf[0][ha], Mb = mbuf[0][hb];
 #pragma unroll
@@ -341,18 +355,21 @@ struct MathMma {
 #pragma unroll
     for (int dt = 0; dt < 16; ++dt) {
       const int d = dt * 16 + g;
-      if (fa != 0.0f) {
-        atomicAdd(&obuf[ha][d], o[dt][0] * fa);
-        atomicAdd(&obuf[ha][d + 8], o[dt][2] * fa);
+      float v0 = o[dt][0] * fa, v2 = o[dt][2] * fa, v1 = o[dt][1] * fb, v3 = o[dt][3] * fb;
+      if (!first) {
+        v0 += obuf[ha][d];
+        v2 += obuf[ha][d + 8];
+        v1 += obuf[hb][d];
+        v3 += obuf[hb][d + 8];
       }
-      if (fb != 0.0f) {
-        atomicAdd(&obuf[hb][d], o[dt][1] * fb);
-        atomicAdd(&obuf[hb][d + 8], o[dt][3] * fb);
-      }
+      obuf[ha][d] = v0;
+      obuf[ha][d + 8] = v2;
+      obuf[hb][d] = v1;
+      obuf[hb][d + 8] = v3;
     }
     if (lane < 4) {
-      if (fa != 0.0f) atomicAdd(&lbuf[ha], l0 * fa);
-      if (fb != 0.0f) atomicAdd(&lbuf[hb], l1 * fb);
+      lbuf[ha] = first ? l0 * fa : lbuf[ha] + l0 * fa;
+      lbuf[hb] = first ? l1 * fb : lbuf[hb] + l1 * fb;
     }
   }
 };
@@ -523,10 +540,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
       }
     }
     // ---- merge the consumer warps' states and write the piece's partial
+    math.finish_sums();
     math.template publish_max<NCW>(sm.mbuf, warp, lane);
     named_bar_sync(1, kConsumers);
-    math.template accumulate<NCW>(sm.mbuf, sm.obuf, sm.lbuf, warp, lane);
-    named_bar_sync(1, kConsumers);
+    // ordered accumulation: deterministic summation order across warps
+#pragma unroll 1
+    for (int x = 0; x < NCW; ++x) {
+      if (warp == x) math.template accumulate<NCW>(sm.mbuf, sm.obuf, sm.lbuf, warp, lane, x == 0);
+      named_bar_sync(1, kConsumers);
+    }
     float* op = p.o_part + pc.id * (kG * kD);
     const int tid = threadIdx.x;
     for (int e = tid * 4; e < kG * kD; e += kConsumers * 4) {
@@ -539,7 +561,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
       v.z *= inv;
       v.w *= inv;
       *reinterpret_cast<float4*>(op + e) = v;
-      *reinterpret_cast<float4*>(&sm.obuf[0][0] + e) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (tid < kG) {
       float M = sm.mbuf[0][tid];
@@ -549,7 +570,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
       p.lse_part[pc.id * kG + tid] = (lsum > 0.0f) ? M + log2f(lsum) : -INFINITY;
     }
     named_bar_sync(1, kConsumers);
-    if (tid < kG) sm.lbuf[tid] = 0.0f;
   }
 }
 
