@@ -36,7 +36,7 @@ if ROOT not in sys.path:
 
 METRIC = "gated decode attention µs/call and achieved HBM GB/s vs GB300 peak (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["gda_stage1.cu", "gda_device.cuh", "gda_kernels.h"]
+KERNEL_SOURCES = ["gda_stage1.cu", "gda_stage1_tma.cu", "gda_device.cuh", "gda_kernels.h"]
 
 
 def parse_args(argv=None):
@@ -47,7 +47,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="b64_l4096")
     p.add_argument("--splits", type=int, default=0, help="num_splits (0: automatic)")
-    p.add_argument("--variant", type=int, default=0, help="0 auto, 1 mma, 2 simt")
+    p.add_argument("--variant", type=int, default=0, help="0 auto, 1 mma, 2 simt, 3 tma ring")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget (cpu_baseline)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--kernel-only", action="store_true",
@@ -334,7 +334,7 @@ def run_ours(args):
             "config": {"workload": args.workload, "B": B, "lengths": "%d..%d (total %d)" % (min(lengths), max(lengths),
                                                                                           sum(lengths)),
                        "Hq": Hq, "Hkv": Hkv, "D": D, "num_splits": args.splits or "auto",
-                       "variant": {0: "auto(mma)", 1: "mma", 2: "simt"}[args.variant],
+                       "variant": {0: "auto(mma)", 1: "mma", 2: "simt", 3: "tma-ring+mma"}[args.variant],
                        "bytes_per_call": nbytes,
                        "l2": "inputs larger than L2 (%.0f MB of K/V rows per call), no flush" % (nbytes / 1e6),
                        "parallelism": "replicas x%d" % world},

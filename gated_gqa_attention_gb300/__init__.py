@@ -24,13 +24,13 @@ from typing import Optional
 __all__ = [
     "load", "decode", "decode_ex", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
-    "VARIANT_SIMT", "MAX_SPLITS", "LIB_PATH",
+    "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libgda.so")
 
-VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT = 0, 1, 2
+VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_TMA = 0, 1, 2, 3
 MAX_SPLITS = 256
 DEVERR_INDEX, DEVERR_TIMEOUT = 0x1, 0x2
 

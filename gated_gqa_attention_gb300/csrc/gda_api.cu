@@ -76,7 +76,7 @@ int validate_args(const gda_args* a) {
   int rc = check_sizes(a->B, a->Hq, a->Hkv, a->D, a->num_splits);
   if (rc != GDA_OK) return rc;
   if (a->check_indices && a->num_slots < 0) return GDA_ERR_SHAPE;
-  if (a->variant < 0 || a->variant > GDA_VARIANT_SIMT) return GDA_ERR_UNSUPPORTED;
+  if (a->variant < 0 || a->variant > GDA_VARIANT_TMA) return GDA_ERR_UNSUPPORTED;
   if (a->min_chunk < 0) return GDA_ERR_SHAPE;
   if (a->B == 0) return GDA_OK;
   if (!a->q || !a->k_pool || !a->v_pool || !a->kv_indptr || !a->kv_indices || !a->out) return GDA_ERR_NULL;
@@ -127,7 +127,9 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.num_splits = a->num_splits > 0 ? a->num_splits : 0;
   p1.min_chunk = min_chunk;
   p1.check_indices = a->check_indices ? 1 : 0;
-  const int variant = (a->variant == GDA_VARIANT_SIMT) ? gda::kVariantSimt : gda::kVariantMma;
+  const int variant = (a->variant == GDA_VARIANT_SIMT)  ? gda::kVariantSimt
+                      : (a->variant == GDA_VARIANT_TMA) ? gda::kVariantTma
+                                                        : gda::kVariantMma;
   cudaEvent_t t_end = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);

@@ -9,8 +9,9 @@ namespace gda {
 
 struct WsHeader;
 
-constexpr int kVariantMma = 1;
-constexpr int kVariantSimt = 2;
+constexpr int kVariantMma = 1;    // register-direct loads, mma.sync tiles (default)
+constexpr int kVariantSimt = 2;   // register-direct loads, FP32 FMAs + warp shuffles
+constexpr int kVariantTma = 3;    // TMA bulk-copy ring, mma.sync tiles
 
 struct Stage1Params {
   const __nv_bfloat16* q;

@@ -1,49 +1,49 @@
-// gda_stage1.cu -- split-KV decode stage 1 on sm_103a.
+// gda_stage1.cu -- split-KV decode stage 1 on sm_103a, K/V rows loaded straight
+// into registers.
 //
 // Per piece (sequence b, KV head kvh, positions [j0, j1)) and for the G = 8 query
 // heads that share kvh, stage 1 computes the normalised partial
-//   O_piece = sum_j softmax_piece(scale * q K_j^T) V_j      and     LSE_piece (log2 units)
+//   O_piece = sum_j softmax_piece(scale * q K_j^T) V_j     and     LSE_piece (log2 units)
 // with a running max and running sum, as split-KV decode stage 1 does (FreeToken
 // PR #781 "Fuse the BF16 attention output sigmoid gate into the existing Triton
 // decode stage2", Summary: stage1 and the stage2 FP32 reduction are kept).
 //
-// GB300 design:
-//  * Persistent grid, one CTA per SM; the work schedule (gda_device.cuh) gives each
-//    CTA an equal share of the batch's KV stream, so ragged batches stay balanced.
-//  * One producer warp gathers the K and V rows of each 64-token tile behind the
-//    CSR slot index with 1-D bulk copies (the TMA bulk engine, 512 B per row,
-//    L2 evict-first) into a 3-stage shared-memory ring guarded by mbarriers; the
-//    next tile's slot indices are prefetched while the current tile is issued.
-//  * Consumer warps each take a fixed slice of every tile.  Each K/V byte is read
-//    from HBM once and used by all 8 query heads of its group.
-//  * Two consumer arithmetics: MathMma (QK^T and PV on mma.sync m16n8k16 bf16
-//    tiles, FP32 accumulate: S^T = K Q^T with the 8 heads as N, O^T += V^T P^T)
-//    and MathSimt (FP32 FMAs with a transposing warp-shuffle reduction).
-//  * At the end of a piece the consumer warps merge their states in shared memory
-//    and write one partial; stage 2 merges partials across pieces.
-//  * Every wait is bounded; a timeout (a kernel bug) sets an error bit and the CTA
-//    winds down along the same control flow, so nothing can hang.
+// GB300 design.  The K/V rows behind the CSR slot index are 512-byte rows at
+// scattered addresses (page size 1).  Measured on GB300, 16-byte vector loads
+// issued by many warps stream such rows at ~6.7 TB/s, while one 1-D bulk copy per
+// row is limited by the copy-request rate (~1.75 TB/s), so:
+//  * Persistent grid, one CTA of 8 warps per SM; the work schedule (gda_device.cuh)
+//    gives each CTA an equal share of the batch's KV stream.
+//  * Warp w takes 16-token tiles w, w+8, ... of the CTA's piece.  Each lane loads
+//    its share of the tile's K and V rows with 16-byte streaming loads straight
+//    into mma.sync fragment registers; the next tile's K loads are in flight while
+//    the softmax and PV run, the next V loads while the next QK runs.
+//  * MMA arithmetic: S^T[16 tok x 8 heads] = K Q^T and O^T[256 x 8] += V^T P^T on
+//    m16n8k16 bf16 tiles with FP32 accumulation.  The head dimension is permuted
+//    (consistently for Q, K and V) so that every 16-byte load lands in fragment
+//    slots: for QK, lane (g, t) holds dims {32c + 8t .. +7} of tokens g and g+8;
+//    for PV it holds dims {64c + 8g .. +7} of tokens 2t, 2t+1, 2t+8, 2t+9, paired
+//    by byte permutes into the V^T fragments.  P is rounded to BF16 and turned
+//    into the B operand with movmatrix.trans; the running sum adds the same
+//    rounded values.
+//  * SIMT arithmetic (variant): lane l owns dims [8l, 8l+8) of every row; 64 FP32
+//    FMAs per token and a transposing warp-shuffle reduction for the 8 scores.
+//  * At the end of a piece the 8 warps merge their (max, sum, O) in shared memory
+//    in a fixed order (deterministic) and one partial is written.
 #include "gda_device.cuh"
 #include "gda_kernels.h"
 
 namespace gda {
 
-__device__ __align__(16) unsigned char g_zero_row[kRowBytes];
+constexpr int kDirectWarps = 8;
 
-template <int NCW, int WTOK, int NSTAGE>
-struct Stage1Smem {
-  static constexpr int kTile = NCW * WTOK;
-  alignas(128) unsigned char k[NSTAGE][kTile][kSmemRow];
-  alignas(128) unsigned char v[NSTAGE][kTile][kSmemRow];
-  float obuf[kG][kD];
-  float mbuf[NCW][kG];
-  float lbuf[kG];
-  alignas(8) uint64_t full[NSTAGE];
-  alignas(8) uint64_t empty[NSTAGE];
-  int abort_flag;
-};
+__device__ __forceinline__ uint4 ld_stream(const unsigned char* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
 
-// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+}
 
 __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
@@ -54,68 +54,193 @@ __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
   }
 }
 
-__device__ __forceinline__ uint4 lds128(const void* p) {
-  return *reinterpret_cast<const uint4*>(p);
-}
+struct DirectSmem {
+  uint2 qf[16][32];               // Q^T fragments of the current piece, lane order (MMA)
+  float obuf[kG][kD];             // merge: O of the piece
+  float mbuf[kDirectWarps][kG];   // merge: each warp's running max
+  float lbuf[kG];                 // merge: running sums
+};
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
+// ------------------------------------------------------------------ MMA arithmetic
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
+struct DirectMma {
+  static constexpr int kTok = 16;
+  uint4 kr[16];     // K: [c] token g, [8 + c] token g+8; dims 32c + 8t .. +7
+  uint4 vr[4][4];   // V: tokens 2t, 2t+1, 2t+8, 2t+9; chunk c = dims 64c + 8g .. +7
+  float o[16][4];   // O^T accumulators (see pv)
+  float m0, m1;     // running max of heads 2t, 2t+1 (log2 units)
+  float l0, l1;     // per-lane running sums, reduced at the merge
+  uint32_t P0, P1;  // BF16 probabilities of tokens g / g+8, heads 2t, 2t+1
 
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return l | (h << 16);
-}
-
-__device__ __forceinline__ float safe_exp2_diff(float a, float m) {
-  // exp2(a - m) with -inf handling: a == -inf -> 0; m == -inf (so a == -inf) -> 0
-  return (a == -INFINITY) ? 0.0f : exp2f(a - m);
-}
-
-// ------------------------------------------------------------------ MathSimt
-//
-// Lane l owns dims [8l, 8l+8) of all 8 heads.  Scores: 64 FMAs per token and a
-// transposing butterfly (4 + 2 + 1 exchanges halve the live head set while
-// summing, 2 more finish the sum) that leaves lane l with the full score of head
-// (l >> 2) & 7.  PV: the probability of head h is broadcast from lane 4h.
-
-template <int WTOK>
-struct MathSimt {
-  float q[kG][8];
-  float acc[kG][8];
-  float m, l;  // state of head (lane >> 2) & 7
-
-  __device__ __forceinline__ void load_q(const __nv_bfloat16* qg, int lane) {
-#pragma unroll
-    for (int h = 0; h < kG; ++h) {
-      const uint4 r = __ldg(reinterpret_cast<const uint4*>(qg + h * kD + lane * 8));
-      unpack8(r, q[h]);
+  // Q^T fragments for every k-step, in lane order; the dims of k-step kk = 2c + h
+  // follow the K permutation: slots (2t, 2t+1) <- dims 32c + 8t + 4h + {0,1},
+  // slots (2t+8, 2t+9) <- dims 32c + 8t + 4h + {2,3}.
+  static __device__ __forceinline__ void prepare_q(const __nv_bfloat16* qg, DirectSmem& sm) {
+    for (int e = threadIdx.x; e < 16 * 32; e += blockDim.x) {
+      const int kk = e >> 5, ln = e & 31;
+      const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
+      sm.qf[kk][ln] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
     }
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.0f;
+  }
+
+  __device__ __forceinline__ void load_k(const unsigned char* kb, size_t stride, int slot_lane, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const int s0 = __shfl_sync(0xffffffffu, slot_lane, g);
+    const int s1 = __shfl_sync(0xffffffffu, slot_lane, g + 8);
+    const unsigned char* p0 = kb + (size_t)max(s0, 0) * stride + 16 * t;
+    const unsigned char* p1 = kb + (size_t)max(s1, 0) * stride + 16 * t;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) kr[c] = (s0 >= 0) ? ld_stream(p0 + 64 * c) : z;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) kr[8 + c] = (s1 >= 0) ? ld_stream(p1 + 64 * c) : z;
+  }
+
+  __device__ __forceinline__ void load_v(const unsigned char* vb, size_t stride, int slot_lane, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int tok = 2 * t + (j & 1) + 8 * (j >> 1);
+      const int s = __shfl_sync(0xffffffffu, slot_lane, tok);
+      const unsigned char* pv = vb + (size_t)max(s, 0) * stride + 16 * g;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) vr[j][c] = (s >= 0) ? ld_stream(pv + 128 * c) : z;
+    }
+  }
+
+  __device__ __forceinline__ void qk_softmax(const DirectSmem& sm, int nv, float sl2, int lane) {
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const int c = kk >> 1, h = kk & 1;
+      const uint4& r0 = kr[c];
+      const uint4& r1 = kr[8 + c];
+      const uint32_t a0 = h ? r0.z : r0.x, a2 = h ? r0.w : r0.y;
+      const uint32_t a1 = h ? r1.z : r1.x, a3 = h ? r1.w : r1.y;
+      const uint2 b = sm.qf[kk][lane];
+      mma_bf16_16816((kk & 1) ? sb : sa, a0, a1, a2, a3, b.x, b.y);
+    }
+    float s[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = (sa[i] + sb[i]) * sl2;
+    const int tg = lane >> 2;
+    if (tg >= nv) s[0] = s[1] = -INFINITY;
+    if (tg + 8 >= nv) s[2] = s[3] = -INFINITY;
+    float xa = fmaxf(s[0], s[2]), xb = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
+      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, off));
+    }
+    const float na = fmaxf(m0, xa), nb = fmaxf(m1, xb);
+    const float aa = safe_exp2_diff(m0, na), ab = safe_exp2_diff(m1, nb);
+    P0 = pack_bf16x2(safe_exp2_diff(s[0], na), safe_exp2_diff(s[1], nb));
+    P1 = pack_bf16x2(safe_exp2_diff(s[2], na), safe_exp2_diff(s[3], nb));
+    l0 = l0 * aa + (__uint_as_float(P0 << 16) + __uint_as_float(P1 << 16));
+    l1 = l1 * ab + (__uint_as_float(P0 & 0xFFFF0000u) + __uint_as_float(P1 & 0xFFFF0000u));
+    m0 = na;
+    m1 = nb;
+    if (__any_sync(0xffffffffu, (aa != 1.0f) || (ab != 1.0f))) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= aa;
+        o[i][1] *= ab;
+        o[i][2] *= aa;
+        o[i][3] *= ab;
+      }
+    }
+  }
+
+  // O^T += V^T P^T.  m-tile i holds dims row(i, g) = 64(i/8) + 8g + i%8 (rows g)
+  // and row(i, g) + 128 (rows g+8); o[i] = {O[2t][row], O[2t+1][row],
+  // O[2t][row+128], O[2t+1][row+128]}.
+  __device__ __forceinline__ void pv() {
+    const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = i >> 3, e = i & 7, w = e >> 1;
+      const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+      const uint32_t a0 = __byte_perm(word_of(vr[0][c], w), word_of(vr[1][c], w), sel);
+      const uint32_t a1 = __byte_perm(word_of(vr[0][2 + c], w), word_of(vr[1][2 + c], w), sel);
+      const uint32_t a2 = __byte_perm(word_of(vr[2][c], w), word_of(vr[3][c], w), sel);
+      const uint32_t a3 = __byte_perm(word_of(vr[2][2 + c], w), word_of(vr[3][2 + c], w), sel);
+      mma_bf16_16816(o[i], a0, a1, a2, a3, b0, b1);
+    }
+  }
+
+  __device__ __forceinline__ void finish_sums() {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+
+  __device__ __forceinline__ void publish_max(DirectSmem& sm, int w, int lane) const {
+    if (lane < 4) {
+      sm.mbuf[w][2 * lane] = m0;
+      sm.mbuf[w][2 * lane + 1] = m1;
+    }
+  }
+
+  __device__ __forceinline__ void accumulate(DirectSmem& sm, int w, int lane, bool first) const {
+    const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
+    float Ma = sm.mbuf[0][ha], Mb = sm.mbuf[0][hb];
+#pragma unroll
+    for (int x = 1; x < kDirectWarps; ++x) {
+      Ma = fmaxf(Ma, sm.mbuf[x][ha]);
+      Mb = fmaxf(Mb, sm.mbuf[x][hb]);
+    }
+    const float fa = (Ma == -INFINITY) ? 0.0f : safe_exp2_diff(m0, Ma);
+    const float fb = (Mb == -INFINITY) ? 0.0f : safe_exp2_diff(m1, Mb);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int d = 64 * (i >> 3) + 8 * g + (i & 7);
+      float v0 = o[i][0] * fa, v1 = o[i][1] * fb, v2 = o[i][2] * fa, v3 = o[i][3] * fb;
+      if (!first) {
+        v0 += sm.obuf[ha][d];
+        v1 += sm.obuf[hb][d];
+        v2 += sm.obuf[ha][d + 128];
+        v3 += sm.obuf[hb][d + 128];
+      }
+      sm.obuf[ha][d] = v0;
+      sm.obuf[hb][d] = v1;
+      sm.obuf[ha][d + 128] = v2;
+      sm.obuf[hb][d + 128] = v3;
+    }
+    if (lane < 4) {
+      sm.lbuf[ha] = first ? l0 * fa : sm.lbuf[ha] + l0 * fa;
+      sm.lbuf[hb] = first ? l1 * fb : sm.lbuf[hb] + l1 * fb;
+    }
+  }
+};
+
+// ------------------------------------------------------------------ SIMT arithmetic
+
+struct DirectSimt {
+  static constexpr int kTok = 8;
+  float q[kG][8];     // head h, dims 8l .. 8l+7
+  float acc[kG][8];
+  float m, l;         // head (lane >> 2)
+  float p[kTok];
+  float alpha;
+  uint4 kr[kTok], vr[kTok];
+
+  static __device__ __forceinline__ void prepare_q(const __nv_bfloat16*, DirectSmem&) {}
+
+  __device__ __forceinline__ void load_q_regs(const __nv_bfloat16* qg, int lane) {
+#pragma unroll
+    for (int h = 0; h < kG; ++h) unpack8(__ldg(reinterpret_cast<const uint4*>(qg + h * kD + lane * 8)), q[h]);
   }
 
   __device__ __forceinline__ void reset() {
@@ -127,9 +252,28 @@ struct MathSimt {
     l = 0.0f;
   }
 
-  __device__ __forceinline__ float score(const unsigned char* krow, int lane) {
+  __device__ __forceinline__ void load_k(const unsigned char* kb, size_t stride, int slot_lane, int lane) {
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+      const int s = __shfl_sync(0xffffffffu, slot_lane, u);
+      kr[u] = (s >= 0) ? ld_stream(kb + (size_t)max(s, 0) * stride + 16 * lane) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  __device__ __forceinline__ void load_v(const unsigned char* vb, size_t stride, int slot_lane, int lane) {
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+      const int s = __shfl_sync(0xffffffffu, slot_lane, u);
+      vr[u] = (s >= 0) ? ld_stream(vb + (size_t)max(s, 0) * stride + 16 * lane) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  // Score of head (lane >> 2) for one K row: 64 FMAs, then a transposing
+  // butterfly (4 + 2 + 1 exchanges halve the live head set while summing, two
+  // more finish the sum).
+  __device__ __forceinline__ float score(const uint4& kraw, int lane) const {
     float k[8];
-    unpack8(lds128(krow + lane * 16), k);
+    unpack8(kraw, k);
     float part[kG];
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
@@ -159,25 +303,26 @@ struct MathSimt {
     return r1;
   }
 
-  __device__ __forceinline__ void tile(const unsigned char* kb, const unsigned char* vb, int nv, float sl2,
-                                       int lane) {
-    float s[WTOK];
+  __device__ __forceinline__ void qk_softmax(const DirectSmem&, int nv, float sl2, int lane) {
+    float s[kTok];
 #pragma unroll
-    for (int t = 0; t < WTOK; ++t) s[t] = (t < nv) ? score(kb + t * kSmemRow, lane) * sl2 : -INFINITY;
+    for (int u = 0; u < kTok; ++u) s[u] = (u < nv) ? score(kr[u], lane) * sl2 : -INFINITY;
     float tmax = s[0];
 #pragma unroll
-    for (int t = 1; t < WTOK; ++t) tmax = fmaxf(tmax, s[t]);
+    for (int u = 1; u < kTok; ++u) tmax = fmaxf(tmax, s[u]);
     const float mnew = fmaxf(m, tmax);
-    const float alpha = safe_exp2_diff(m, mnew);
-    float p[WTOK];
+    alpha = safe_exp2_diff(m, mnew);
     float psum = 0.0f;
 #pragma unroll
-    for (int t = 0; t < WTOK; ++t) {
-      p[t] = safe_exp2_diff(s[t], mnew);
-      psum += p[t];
+    for (int u = 0; u < kTok; ++u) {
+      p[u] = safe_exp2_diff(s[u], mnew);
+      psum += p[u];
     }
     l = l * alpha + psum;
     m = mnew;
+  }
+
+  __device__ __forceinline__ void pv_lane(int lane) {
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
       const float a = __shfl_sync(0xffffffffu, alpha, 4 * h);
@@ -185,40 +330,32 @@ struct MathSimt {
       for (int i = 0; i < 8; ++i) acc[h][i] *= a;
     }
 #pragma unroll
-    for (int t = 0; t < WTOK; ++t) {
-      if (t < nv) {
-        float v[8];
-        unpack8(lds128(vb + t * kSmemRow + lane * 16), v);
+    for (int u = 0; u < kTok; ++u) {
+      float v[8];
+      unpack8(vr[u], v);
 #pragma unroll
-        for (int h = 0; h < kG; ++h) {
-          const float ph = __shfl_sync(0xffffffffu, p[t], 4 * h);
+      for (int h = 0; h < kG; ++h) {
+        const float ph = __shfl_sync(0xffffffffu, p[u], 4 * h);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(ph, v[i], acc[h][i]);
-        }
+        for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(ph, v[i], acc[h][i]);
       }
     }
   }
 
   __device__ __forceinline__ void finish_sums() {}
 
-  // Publish this warp's running max (phase 1 of the CTA merge).
-  template <int NCW>
-  __device__ __forceinline__ void publish_max(float (*mbuf)[kG], int w, int lane) {
-    if ((lane & 3) == 0) mbuf[w][lane >> 2] = m;
+  __device__ __forceinline__ void publish_max(DirectSmem& sm, int w, int lane) const {
+    if ((lane & 3) == 0) sm.mbuf[w][lane >> 2] = m;
   }
 
-  // Store (first warp) or add this warp's state, rescaled to the CTA-wide max,
-  // into obuf / lbuf.  Every address is written by one lane, warps in a fixed order.
-  template <int NCW>
-  __device__ __forceinline__ void accumulate(const float (*mbuf)[kG], float (*obuf)[kD], float* lbuf, int w,
-                                             int lane, bool first) {
+  __device__ __forceinline__ void accumulate(DirectSmem& sm, int w, int lane, bool first) const {
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
-      float M = mbuf[0][h];
+      float M = sm.mbuf[0][h];
 #pragma unroll
-      for (int x = 1; x < NCW; ++x) M = fmaxf(M, mbuf[x][h]);
-      const float f = (M == -INFINITY) ? 0.0f : safe_exp2_diff(mbuf[w][h], M);
-      float4* dst = reinterpret_cast<float4*>(&obuf[h][lane * 8]);
+      for (int x = 1; x < kDirectWarps; ++x) M = fmaxf(M, sm.mbuf[x][h]);
+      const float f = (M == -INFINITY) ? 0.0f : safe_exp2_diff(sm.mbuf[w][h], M);
+      float4* dst = reinterpret_cast<float4*>(&sm.obuf[h][lane * 8]);
       float4 a = make_float4(acc[h][0] * f, acc[h][1] * f, acc[h][2] * f, acc[h][3] * f);
       float4 b = make_float4(acc[h][4] * f, acc[h][5] * f, acc[h][6] * f, acc[h][7] * f);
       if (!first) {
@@ -228,330 +365,101 @@ struct MathSimt {
       }
       dst[0] = a;
       dst[1] = b;
-      if ((lane & 3) == 0 && (lane >> 2) == h) lbuf[h] = first ? l * f : lbuf[h] + l * f;
+      if ((lane & 3) == 0 && (lane >> 2) == h) sm.lbuf[h] = first ? l * f : sm.lbuf[h] + l * f;
     }
   }
 };
 
-// ------------------------------------------------------------------ MathMma
-//
-// Per 16-token slice (one warp): S^T[16 tok x 8 heads] = K[16 x 256] Q^T[256 x 8]
-// as 16 m16n8k16 steps (K from shared memory by ldmatrix, Q^T fragments held in
-// registers), the online softmax on the accumulator fragments (lane holds tokens
-// lane/4 and lane/4+8 of heads 2(lane%4), 2(lane%4)+1), P rounded to BF16 and
-// turned into the B operand by movmatrix.trans, then O^T[256 x 8] += V^T P^T as
-// 16 m16n8k16 steps (V^T from shared memory by ldmatrix.trans).  The running sum
-// adds the same BF16-rounded probabilities that multiply V.
+template <class Math>
+__device__ __forceinline__ void math_load_q(Math& m, const __nv_bfloat16* qg, int lane);
+template <>
+__device__ __forceinline__ void math_load_q<DirectMma>(DirectMma&, const __nv_bfloat16*, int) {}
+template <>
+__device__ __forceinline__ void math_load_q<DirectSimt>(DirectSimt& m, const __nv_bfloat16* qg, int lane) {
+  m.load_q_regs(qg, lane);
+}
 
-template <int WTOK>
-struct MathMma {
-  static_assert(WTOK == 16, "one m16 tile per warp");
-  uint32_t qb[16][2];
-  float o[16][4];
-  float m0, m1;  // heads 2(lane%4), 2(lane%4)+1
-  float l0, l1;  // per-lane partial sums, reduced at the merge
-
-  __device__ __forceinline__ void load_q(const __nv_bfloat16* qg, int lane) {
-    const int h = lane >> 2, dq = 2 * (lane & 3);
-    const uint32_t* base = reinterpret_cast<const uint32_t*>(qg + h * kD);
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      qb[kk][0] = __ldg(base + (kk * 16 + dq) / 2);
-      qb[kk][1] = __ldg(base + (kk * 16 + dq + 8) / 2);
-    }
-  }
-
-  __device__ __forceinline__ void reset() {
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[dt][i] = 0.0f;
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.0f;
-  }
-
-  __device__ __forceinline__ void tile(const unsigned char* kb, const unsigned char* vb, int nv, float sl2,
-                                       int lane) {
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t kaddr = smem_u32(kb) + (lane & 15) * kSmemRow + (lane >> 4) * 16;
-#pragma unroll
-    for (int kk = 0; kk < 16; kk += 2) {
-      uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-      ldsm_x4(kaddr + kk * 32, a0, a1, a2, a3);
-      ldsm_x4(kaddr + (kk + 1) * 32, c0, c1, c2, c3);
-      mma_bf16_16816(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-      mma_bf16_16816(sb, c0, c1, c2, c3, qb[kk + 1][0], qb[kk + 1][1]);
-    }
-    float s[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] = (sa[i] + sb[i]) * sl2;
-    const int t0 = lane >> 2;
-    if (t0 >= nv) s[0] = s[1] = -INFINITY;
-    if (t0 + 8 >= nv) s[2] = s[3] = -INFINITY;
-    float xa = fmaxf(s[0], s[2]), xb = fmaxf(s[1], s[3]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
-      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, off));
-    }
-    const float na = fmaxf(m0, xa), nb = fmaxf(m1, xb);
-    const float aa = safe_exp2_diff(m0, na), ab = safe_exp2_diff(m1, nb);
-    const uint32_t P0 = pack_bf16x2(safe_exp2_diff(s[0], na), safe_exp2_diff(s[1], nb));
-    const uint32_t P1 = pack_bf16x2(safe_exp2_diff(s[2], na), safe_exp2_diff(s[3], nb));
-    l0 = l0 * aa + (__uint_as_float(P0 << 16) + __uint_as_float(P1 << 16));
-    l1 = l1 * ab + (__uint_as_float(P0 & 0xFFFF0000u) + __uint_as_float(P1 & 0xFFFF0000u));
-    m0 = na;
-    m1 = nb;
-    if (__any_sync(0xffffffffu, (aa != 1.0f) || (ab != 1.0f))) {
-#pragma unroll
-      for (int dt = 0; dt < 16; ++dt) {
-        o[dt][0] *= aa;
-        o[dt][1] *= ab;
-        o[dt][2] *= aa;
-        o[dt][3] *= ab;
-      }
-    }
-    const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
-    const int mj = lane >> 3, mr = lane & 7;
-    const uint32_t vaddr = smem_u32(vb) + (mr + 8 * (mj >> 1)) * kSmemRow + 16 * (mj & 1);
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
-      mma_bf16_16816(o[dt], a0, a1, a2, a3, b0, b1);
-    }
-  }
-
-  template <int NCW>
-  __device__ __forceinline__ void publish_max(float (*mbuf)[kG], int w, int lane) {
-    if (lane < 4) {
-      mbuf[w][2 * lane] = m0;
-      mbuf[w][2 * lane + 1] = m1;
-    }
-  }
-
-  // Reduce the per-lane running sums over the 8 lanes that share a head pair
-  // (done by every warp before the ordered accumulation).
-  __device__ __forceinline__ void finish_sums() {
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-  }
-
-  template <int NCW>
-  __device__ __forceinline__ void accumulate(const float (*mbuf)[kG], float (*obuf)[kD], float* lbuf, int w,
-                                             int lane, bool first) {
-    const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
-    float Ma = mbuf[0][ha], Mb = mbuf[0][hb];
-#pragma unroll
-    for (int x = 1; x < NCW; ++x) {
-      Ma = fmaxf(Ma, mbuf[x][ha]);
-      Mb = fmaxf(Mb, mbuf[x][hb]);
-    }
-    const float fa = (Ma == -INFINITY) ? 0.0f : safe_exp2_diff(m0, Ma);
-    const float fb = (Mb == -INFINITY) ? 0.0f : safe_exp2_diff(m1, Mb);
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      const int d = dt * 16 + g;
-      float v0 = o[dt][0] * fa, v2 = o[dt][2] * fa, v1 = o[dt][1] * fb, v3 = o[dt][3] * fb;
-      if (!first) {
-        v0 += obuf[ha][d];
-        v2 += obuf[ha][d + 8];
-        v1 += obuf[hb][d];
-        v3 += obuf[hb][d + 8];
-      }
-      obuf[ha][d] = v0;
-      obuf[ha][d + 8] = v2;
-      obuf[hb][d] = v1;
-      obuf[hb][d + 8] = v3;
-    }
-    if (lane < 4) {
-      lbuf[ha] = first ? l0 * fa : lbuf[ha] + l0 * fa;
-      lbuf[hb] = first ? l1 * fb : lbuf[hb] + l1 * fb;
-    }
-  }
-};
+template <class Math>
+__device__ __forceinline__ void math_pv(Math& m, int lane);
+template <>
+__device__ __forceinline__ void math_pv<DirectMma>(DirectMma& m, int) { m.pv(); }
+template <>
+__device__ __forceinline__ void math_pv<DirectSimt>(DirectSimt& m, int lane) { m.pv_lane(lane); }
 
 // ------------------------------------------------------------------ the kernel
 
-template <class Math, int NCW, int WTOK, int NSTAGE>
-__global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params p) {
-  using Smem = Stage1Smem<NCW, WTOK, NSTAGE>;
-  constexpr int kTile = Smem::kTile;
-  constexpr int kConsumers = NCW * 32;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+template <class Math>
+__global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Stage1Params p) {
+  constexpr int kTok = Math::kTok;
+  __shared__ __align__(16) DirectSmem sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], NCW);
-    }
-    sm.abort_flag = 0;
-    fence_mbar_init();
-  }
-  for (int i = threadIdx.x; i < kG * kD; i += blockDim.x) (&sm.obuf[0][0])[i] = 0.0f;
-  if (threadIdx.x < kG) sm.lbuf[threadIdx.x] = 0.0f;
-  __syncthreads();
   // Stage 2 may start its prologue (gate loads and sigmoids) now.
   pdl_launch_dependents();
 
   Sched sched;
   sched.begin(p.indptr, p.B, p.Hkv, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk);
-  volatile int* abort_flag = &sm.abort_flag;
+  const size_t stride = (size_t)p.Hkv * kRowBytes;
 
-  if (warp == NCW) {
-    // ---------------------------------------------------------------- producer
-    const uint64_t pol = l2_policy_evict_first();
-    constexpr int kPer = (kTile + 31) / 32;
-    const size_t slot_stride = (size_t)p.Hkv * kRowBytes;
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    int issued = 0;
-
-    // tile cursor over the CTA's pieces
-    Piece pc;
-    bool have = sched.next(pc);
-    int t0 = have ? pc.j0 : 0;
-    int cur_slot[kPer];
-    int cur_n = 0, cur_kvh = 0;
-    auto load_slots = [&](const Piece& pp, int tt0, int* slots) -> int {
-      const int n = min(kTile, pp.j1 - tt0);
-      const int* idx = p.indices + __ldg(p.indptr + pp.b) + tt0;
-#pragma unroll
-      for (int r = 0; r < kPer; ++r) {
-        const int rr = lane + 32 * r;
-        slots[r] = (rr < n) ? __ldg(idx + rr) : -1;
-      }
-      return n;
-    };
-    if (have) {
-      cur_n = load_slots(pc, t0, cur_slot);
-      cur_kvh = pc.kvh;
-    }
-    while (have) {
-      if (*abort_flag) {
-        ok = false;
-        break;
-      }
-      // advance the cursor and prefetch the next tile's slots
-      int nxt_slot[kPer];
-      int nxt_n = 0, nxt_kvh = 0;
-      t0 += kTile;
-      if (t0 >= pc.j1) {
-        have = sched.next(pc);
-        if (have) t0 = pc.j0;
-      }
-      if (have) {
-        nxt_n = load_slots(pc, t0, nxt_slot);
-        nxt_kvh = pc.kvh;
-      }
-      // issue the current tile
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&sm.full[stage], kTile * 2 * kRowBytes);
-      __syncwarp();
-      const size_t head_off = (size_t)cur_kvh * kRowBytes;
-#pragma unroll
-      for (int r = 0; r < kPer; ++r) {
-        const int rr = lane + 32 * r;
-        if (rr < kTile) {
-          const unsigned char* ks = g_zero_row;
-          const unsigned char* vs = g_zero_row;
-          const int slot = cur_slot[r];
-          if (rr < cur_n) {
-            const bool bad = p.check_indices && (slot < 0 || (long long)slot >= p.num_slots);
-            if (bad) {
-              atomicOr(&p.hdr->error, kErrIndex);
-            } else {
-              ks = p.k_pool + (size_t)slot * slot_stride + head_off;
-              vs = p.v_pool + (size_t)slot * slot_stride + head_off;
-            }
-          }
-          bulk_g2s(&sm.k[stage][rr][0], ks, kRowBytes, &sm.full[stage], pol);
-          bulk_g2s(&sm.v[stage][rr][0], vs, kRowBytes, &sm.full[stage], pol);
-        }
-      }
-      ++issued;
-      if (++stage == NSTAGE) {
-        stage = 0;
-        phase ^= 1u;
-      }
-#pragma unroll
-      for (int r = 0; r < kPer; ++r) cur_slot[r] = nxt_slot[r];
-      cur_n = nxt_n;
-      cur_kvh = nxt_kvh;
-    }
-    if (!ok || *abort_flag) {
-      if (lane == 0) {
-        atomicOr(&p.hdr->error, kErrTimeout);
-        sm.abort_flag = 1;
-      }
-      // let the copies already issued land before the CTA can exit
-      const int inflight = min(issued, NSTAGE);
-      int s = stage;
-      uint32_t ph = phase;
-      for (int k = 0; k < inflight; ++k) {
-        if (--s < 0) {
-          s = NSTAGE - 1;
-          ph ^= 1u;
-        }
-        const long long t_start = clock64();
-        while (!mbar_try_wait(&sm.full[s], ph) && clock64() - t_start < kWaitLimitCycles) {
-        }
+  auto fetch_slot = [&](const int* idx, int tok0, int n) -> int {
+    int s = -1;
+    if (lane < n) {
+      s = __ldg(idx + tok0 + lane);
+      if (p.check_indices && (s < 0 || (long long)s >= p.num_slots)) {
+        atomicOr(&p.hdr->error, kErrIndex);
+        s = -1;
       }
     }
-    return;
-  }
+    return s;
+  };
 
-  // ------------------------------------------------------------------ consumers
-  Math math;
-  int stage = 0;
-  uint32_t phase = 0;
-  bool aborted = false;
   Piece pc;
   while (sched.next(pc)) {
-    math.load_q(p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD, lane);
+    const __nv_bfloat16* qg = p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD;
+    Math::prepare_q(qg, sm);
+    Math math;
+    math_load_q(math, qg, lane);
     math.reset();
-    for (int t0 = pc.j0; t0 < pc.j1; t0 += kTile) {
-      const int n = min(kTile, pc.j1 - t0);
-      const int nv = max(0, min(WTOK, n - warp * WTOK));
-      if (!aborted && !mbar_wait(&sm.full[stage], phase, abort_flag)) {
-        aborted = true;
-        if (lane == 0) {
-          atomicOr(&p.hdr->error, kErrTimeout);
-          sm.abort_flag = 1;
-        }
-      }
-      if (!aborted && nv > 0)
-        math.tile(&sm.k[stage][warp * WTOK][0], &sm.v[stage][warp * WTOK][0], nv, p.scale_log2, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);
-      if (++stage == NSTAGE) {
-        stage = 0;
-        phase ^= 1u;
+    __syncthreads();  // Q fragments in shared memory
+
+    const unsigned char* kb = p.k_pool + (size_t)pc.kvh * kRowBytes;
+    const unsigned char* vb = p.v_pool + (size_t)pc.kvh * kRowBytes;
+    const int* idx = p.indices + __ldg(p.indptr + pc.b) + pc.j0;
+    const int len = pc.j1 - pc.j0;
+    const int ntiles = (len + kTok - 1) / kTok;
+    int tile = warp;
+    if (tile < ntiles) {
+      int n = min(kTok, len - tile * kTok);
+      int slot = fetch_slot(idx, tile * kTok, n);
+      math.load_k(kb, stride, slot, lane);
+      math.load_v(vb, stride, slot, lane);
+      int ntile = tile + kDirectWarps;
+      int nn = (ntile < ntiles) ? min(kTok, len - ntile * kTok) : 0;
+      int nslot = fetch_slot(idx, ntile * kTok, nn);
+      while (true) {
+        math.qk_softmax(sm, n, p.scale_log2, lane);
+        if (nn > 0) math.load_k(kb, stride, nslot, lane);
+        math_pv(math, lane);
+        if (nn > 0) math.load_v(vb, stride, nslot, lane);
+        if (nn == 0) break;
+        n = nn;
+        ntile += kDirectWarps;
+        nn = (ntile < ntiles) ? min(kTok, len - ntile * kTok) : 0;
+        nslot = fetch_slot(idx, ntile * kTok, nn);
       }
     }
-    // ---- merge the consumer warps' states and write the piece's partial
+
+    // ---- merge the warps' states (fixed order) and write the piece's partial
     math.finish_sums();
-    math.template publish_max<NCW>(sm.mbuf, warp, lane);
-    named_bar_sync(1, kConsumers);
-    // ordered accumulation: deterministic summation order across warps
+    math.publish_max(sm, warp, lane);
+    __syncthreads();
 #pragma unroll 1
-    for (int x = 0; x < NCW; ++x) {
-      if (warp == x) math.template accumulate<NCW>(sm.mbuf, sm.obuf, sm.lbuf, warp, lane, x == 0);
-      named_bar_sync(1, kConsumers);
+    for (int x = 0; x < kDirectWarps; ++x) {
+      if (warp == x) math.accumulate(sm, warp, lane, x == 0);
+      __syncthreads();
     }
     float* op = p.o_part + pc.id * (kG * kD);
-    const int tid = threadIdx.x;
-    for (int e = tid * 4; e < kG * kD; e += kConsumers * 4) {
+    for (int e = threadIdx.x * 4; e < kG * kD; e += blockDim.x * 4) {
       const int h = e / kD;
       const float lsum = sm.lbuf[h];
       const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
@@ -562,47 +470,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
       v.w *= inv;
       *reinterpret_cast<float4*>(op + e) = v;
     }
-    if (tid < kG) {
-      float M = sm.mbuf[0][tid];
+    if (threadIdx.x < kG) {
+      float M = sm.mbuf[0][threadIdx.x];
 #pragma unroll
-      for (int x = 1; x < NCW; ++x) M = fmaxf(M, sm.mbuf[x][tid]);
-      const float lsum = sm.lbuf[tid];
-      p.lse_part[pc.id * kG + tid] = (lsum > 0.0f) ? M + log2f(lsum) : -INFINITY;
+      for (int x = 1; x < kDirectWarps; ++x) M = fmaxf(M, sm.mbuf[x][threadIdx.x]);
+      const float lsum = sm.lbuf[threadIdx.x];
+      p.lse_part[pc.id * kG + threadIdx.x] = (lsum > 0.0f) ? M + log2f(lsum) : -INFINITY;
     }
-    named_bar_sync(1, kConsumers);
+    __syncthreads();  // shared buffers free for the next piece
   }
 }
 
-// ------------------------------------------------------------------ launchers
-
-template <class Math, int NCW, int WTOK, int NSTAGE>
-static cudaError_t launch_variant(const Stage1Params& p, int grid, cudaStream_t stream) {
-  using Smem = Stage1Smem<NCW, WTOK, NSTAGE>;
-  auto kern = stage1_kernel<Math, NCW, WTOK, NSTAGE>;
-  const size_t smem = sizeof(Smem);
-  // the shared-memory opt-in is per device; set it once per device
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  kern<<<grid, (NCW + 1) * 32, smem, stream>>>(p);
-  return cudaGetLastError();
-}
-
-int stage1_tile_tokens(int variant) {
-  (void)variant;
-  return 64;
-}
+cudaError_t launch_stage1_tma(const Stage1Params& p, int grid, cudaStream_t stream);
 
 cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStream_t stream) {
-  if (variant == kVariantSimt) return launch_variant<MathSimt<8>, 8, 8, 3>(p, grid, stream);
-  return launch_variant<MathMma<16>, 4, 16, 3>(p, grid, stream);
+  if (variant == kVariantTma) return launch_stage1_tma(p, grid, stream);
+  if (variant == kVariantSimt) {
+    stage1_direct_kernel<DirectSimt><<<grid, kDirectWarps * 32, 0, stream>>>(p);
+  } else {
+    stage1_direct_kernel<DirectMma><<<grid, kDirectWarps * 32, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace gda

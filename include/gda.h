@@ -66,9 +66,13 @@ typedef enum gda_status {
 #define GDA_DEVERR_TIMEOUT 0x2u  /* a pipeline wait gave up (kernel bug guard; never expected) */
 
 /* Stage-1 kernel variant (gda_args.variant). */
-#define GDA_VARIANT_AUTO 0       /* the fastest built variant (tensor-core tiles) */
-#define GDA_VARIANT_MMA 1        /* QK and PV on mma.sync m16n8k16 bf16 tiles */
-#define GDA_VARIANT_SIMT 2       /* QK and PV as FP32 FMAs with warp-shuffle reductions */
+#define GDA_VARIANT_AUTO 0       /* the fastest built variant (GDA_VARIANT_MMA) */
+#define GDA_VARIANT_MMA 1        /* K/V rows loaded straight into registers; QK and PV on
+                                    mma.sync m16n8k16 bf16 tiles with FP32 accumulation */
+#define GDA_VARIANT_SIMT 2       /* same loads; QK and PV as FP32 FMAs with warp-shuffle
+                                    reductions */
+#define GDA_VARIANT_TMA 3        /* K/V rows gathered into a shared-memory ring by 1-D bulk
+                                    copies (TMA), then mma.sync tiles (comparison variant) */
 
 /*
  * Full argument set of gda_decode_ex.

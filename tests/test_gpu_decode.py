@@ -62,7 +62,7 @@ def small_case():
     return inp, reference(inp)
 
 
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 @pytest.mark.parametrize("splits", [0, 1, 3, 8, 64])
 def test_small_ragged_parity(gda, small_case, variant, splits):
     inp, ref = small_case
@@ -94,7 +94,7 @@ def test_gda_decode_internal_workspace(gda, small_case):
 def test_fused_equals_unfused_bitwise(gda, small_case):
     inp, ref = small_case
     dev = to_cuda(inp)
-    for variant in (1, 2):
+    for variant in (1, 2, 3):
         fused = run(gda, dev, variant=variant)
         o_only = run(gda, dev, variant=variant, fuse_gate=False)
         unfused = gda.gate(o_only, dev["gate"])
@@ -138,7 +138,7 @@ def test_placement_invariance_bitwise(gda, small_case):
 def test_single_key_and_empty_rows_exact(gda):
     inp = workloads.make([1, 0, 1, 1, 0], seed=7, layout="perm", pool_slots=50)
     ref = reference(inp)
-    for variant in (1, 2):
+    for variant in (1, 2, 3):
         out = run(gda, to_cuda(inp), variant=variant)
         torch.cuda.synchronize()
         got = bits(out)
@@ -163,7 +163,7 @@ def test_custom_scale_and_peaky_scores(gda):
     inp = workloads.make([300, 41, 1, 2048], seed=12, layout="perm", pool_slots=3000, qkv_std=2.5,
                          peaky_frac=0.05, peaky_scale=4.0, scale=0.11)
     ref = reference(inp)
-    for variant in (1, 2):
+    for variant in (1, 2, 3):
         out = run(gda, to_cuda(inp), variant=variant, num_splits=0)
         torch.cuda.synchronize()
         check_close(bits(out), ref.out)
@@ -268,8 +268,9 @@ def test_workload_parity(gda, key, splits):
     print(key, splits, stats)
 
 
-def test_workload_parity_simt_variant(gda):
+@pytest.mark.parametrize("variant", [2, 3])
+def test_workload_parity_other_variants(gda, variant):
     inp, ref, dev = workload_case("b64_l4096")
-    out = run(gda, dev, num_splits=0, variant=2)
+    out = run(gda, dev, num_splits=0, variant=variant)
     torch.cuda.synchronize()
     check_close(bits(out), ref.out)
