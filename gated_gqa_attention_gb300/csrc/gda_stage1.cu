@@ -41,10 +41,6 @@ __device__ __forceinline__ uint4 ld_stream(const unsigned char* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
-  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
-}
-
 __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -55,33 +51,44 @@ __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
 }
 
 struct DirectSmem {
-  uint2 qf[16][32];               // Q^T fragments of the current piece, lane order (MMA)
   float obuf[kG][kD];             // merge: O of the piece
   float mbuf[kDirectWarps][kG];   // merge: each warp's running max
   float lbuf[kG];                 // merge: running sums
 };
 
 // ------------------------------------------------------------------ MMA arithmetic
+//
+// Warp tile: 16 tokens.  K rows go straight into registers (one tile ahead) in a
+// permuted head-dim order that matches the mma.sync A fragments: lane (g, t)
+// holds dims {32c + 8t .. +7} of tokens g and g+8, and k-step kk = 2c + h uses
+// dims 32c + 8t + 4h + {0,1} for k-slots (2t, 2t+1) and + {2,3} for (2t+8, 2t+9);
+// the Q^T fragments use the same order.  V rows go through a per-warp cp.async
+// ring in shared memory (two tiles ahead) and reach the V^T fragments through
+// ldmatrix.trans.  O^T accumulators: o[dt] = {O[2t][16dt+g], O[2t+1][16dt+g],
+// O[2t][16dt+g+8], O[2t+1][16dt+g+8]}.
 
-struct DirectMma {
-  static constexpr int kTok = 16;
-  uint4 kr[16];     // K: [c] token g, [8 + c] token g+8; dims 32c + 8t .. +7
-  uint4 vr[4][4];   // V: tokens 2t, 2t+1, 2t+8, 2t+9; chunk c = dims 64c + 8g .. +7
-  float o[16][4];   // O^T accumulators (see pv)
-  float m0, m1;     // running max of heads 2t, 2t+1 (log2 units)
-  float l0, l1;     // per-lane running sums, reduced at the merge
-  uint32_t P0, P1;  // BF16 probabilities of tokens g / g+8, heads 2t, 2t+1
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-  // Q^T fragments for every k-step, in lane order; the dims of k-step kk = 2c + h
-  // follow the K permutation: slots (2t, 2t+1) <- dims 32c + 8t + 4h + {0,1},
-  // slots (2t+8, 2t+9) <- dims 32c + 8t + 4h + {2,3}.
-  static __device__ __forceinline__ void prepare_q(const __nv_bfloat16* qg, DirectSmem& sm) {
-    for (int e = threadIdx.x; e < 16 * 32; e += blockDim.x) {
-      const int kk = e >> 5, ln = e & 31;
-      const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
-      sm.qf[kk][ln] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
-    }
-  }
+template <int NWARP, int NV>
+struct MmaSmem {
+  uint2 qf[16][32];                                      // Q^T fragments, lane order
+  unsigned char vring[NWARP][NV][16][kSmemRow];          // per-warp V rings
+  float mbuf[NWARP][kG];                                 // each warp's running max
+  float lsum[NWARP][kG];                                 // each warp's rescaled sum
+};
+
+struct MmaWarpState {
+  uint4 kr[16];
+  float o[16][4];
+  float m0, m1, l0, l1;
+  uint32_t P0, P1;
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -105,20 +112,7 @@ struct DirectMma {
     for (int c = 0; c < 8; ++c) kr[8 + c] = (s1 >= 0) ? ld_stream(p1 + 64 * c) : z;
   }
 
-  __device__ __forceinline__ void load_v(const unsigned char* vb, size_t stride, int slot_lane, int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int tok = 2 * t + (j & 1) + 8 * (j >> 1);
-      const int s = __shfl_sync(0xffffffffu, slot_lane, tok);
-      const unsigned char* pv = vb + (size_t)max(s, 0) * stride + 16 * g;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) vr[j][c] = (s >= 0) ? ld_stream(pv + 128 * c) : z;
-    }
-  }
-
-  __device__ __forceinline__ void qk_softmax(const DirectSmem& sm, int nv, float sl2, int lane) {
+  __device__ __forceinline__ void qk_softmax(const uint2 (*qf)[32], int nv, float sl2, int lane) {
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
@@ -127,7 +121,7 @@ struct DirectMma {
       const uint4& r1 = kr[8 + c];
       const uint32_t a0 = h ? r0.z : r0.x, a2 = h ? r0.w : r0.y;
       const uint32_t a1 = h ? r1.z : r1.x, a3 = h ? r1.w : r1.y;
-      const uint2 b = sm.qf[kk][lane];
+      const uint2 b = qf[kk][lane];
       mma_bf16_16816((kk & 1) ? sb : sa, a0, a1, a2, a3, b.x, b.y);
     }
     float s[4];
@@ -161,69 +155,180 @@ struct DirectMma {
     }
   }
 
-  // O^T += V^T P^T.  m-tile i holds dims row(i, g) = 64(i/8) + 8g + i%8 (rows g)
-  // and row(i, g) + 128 (rows g+8); o[i] = {O[2t][row], O[2t+1][row],
-  // O[2t][row+128], O[2t+1][row+128]}.
-  __device__ __forceinline__ void pv() {
+  // O^T += V^T P^T with V^T fragments from a 16-row shared-memory tile
+  __device__ __forceinline__ void pv(const unsigned char* vtile, int lane) {
     const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
+    const int mj = lane >> 3, mr = lane & 7;
+    const uint32_t vaddr = smem_u32(vtile) + (mr + 8 * (mj >> 1)) * kSmemRow + 16 * (mj & 1);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int c = i >> 3, e = i & 7, w = e >> 1;
-      const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-      const uint32_t a0 = __byte_perm(word_of(vr[0][c], w), word_of(vr[1][c], w), sel);
-      const uint32_t a1 = __byte_perm(word_of(vr[0][2 + c], w), word_of(vr[1][2 + c], w), sel);
-      const uint32_t a2 = __byte_perm(word_of(vr[2][c], w), word_of(vr[3][c], w), sel);
-      const uint32_t a3 = __byte_perm(word_of(vr[2][2 + c], w), word_of(vr[3][2 + c], w), sel);
-      mma_bf16_16816(o[i], a0, a1, a2, a3, b0, b1);
-    }
-  }
-
-  __device__ __forceinline__ void finish_sums() {
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-  }
-
-  __device__ __forceinline__ void publish_max(DirectSmem& sm, int w, int lane) const {
-    if (lane < 4) {
-      sm.mbuf[w][2 * lane] = m0;
-      sm.mbuf[w][2 * lane + 1] = m1;
-    }
-  }
-
-  __device__ __forceinline__ void accumulate(DirectSmem& sm, int w, int lane, bool first) const {
-    const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
-    float Ma = sm.mbuf[0][ha], Mb = sm.mbuf[0][hb];
-#pragma unroll
-    for (int x = 1; x < kDirectWarps; ++x) {
-      Ma = fmaxf(Ma, sm.mbuf[x][ha]);
-      Mb = fmaxf(Mb, sm.mbuf[x][hb]);
-    }
-    const float fa = (Ma == -INFINITY) ? 0.0f : safe_exp2_diff(m0, Ma);
-    const float fb = (Mb == -INFINITY) ? 0.0f : safe_exp2_diff(m1, Mb);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int d = 64 * (i >> 3) + 8 * g + (i & 7);
-      float v0 = o[i][0] * fa, v1 = o[i][1] * fb, v2 = o[i][2] * fa, v3 = o[i][3] * fb;
-      if (!first) {
-        v0 += sm.obuf[ha][d];
-        v1 += sm.obuf[hb][d];
-        v2 += sm.obuf[ha][d + 128];
-        v3 += sm.obuf[hb][d + 128];
-      }
-      sm.obuf[ha][d] = v0;
-      sm.obuf[hb][d] = v1;
-      sm.obuf[ha][d + 128] = v2;
-      sm.obuf[hb][d + 128] = v3;
-    }
-    if (lane < 4) {
-      sm.lbuf[ha] = first ? l0 * fa : sm.lbuf[ha] + l0 * fa;
-      sm.lbuf[hb] = first ? l1 * fb : sm.lbuf[hb] + l1 * fb;
+    for (int dt = 0; dt < 16; ++dt) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
+      mma_bf16_16816(o[dt], a0, a1, a2, a3, b0, b1);
     }
   }
 };
+
+// Issue the cp.async copies of one V tile (16 rows; rows >= n and bad slots are
+// zero-filled) into a ring stage and commit them as one group.
+__device__ __forceinline__ void issue_v_tile(unsigned char* stage, const unsigned char* vb, size_t stride,
+                                             int slot_lane, int n, int lane) {
+  const uint32_t dst0 = smem_u32(stage) + 16 * lane;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int s = __shfl_sync(0xffffffffu, slot_lane, r);
+    const bool ok = (r < n) && (s >= 0);
+    const unsigned char* src = vb + (ok ? (size_t)s * stride : (size_t)0) + 16 * lane;
+    cp_async16(dst0 + r * kSmemRow, src, ok ? 16u : 0u);
+  }
+  cp_async_commit();
+}
+
+template <int NWARP, int NV>
+__global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params p) {
+  using Smem = MmaSmem<NWARP, NV>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Stage 2 may start its prologue (gate loads and sigmoids) now.
+  pdl_launch_dependents();
+
+  Sched sched;
+  sched.begin(p.indptr, p.B, p.Hkv, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk);
+  const size_t stride = (size_t)p.Hkv * kRowBytes;
+
+  Piece pc;
+  while (sched.next(pc)) {
+    // Q^T fragments of the piece's 8 heads (the previous piece ended with a barrier)
+    const __nv_bfloat16* qg = p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD;
+    for (int e = threadIdx.x; e < 16 * 32; e += blockDim.x) {
+      const int kk = e >> 5, ln = e & 31;
+      const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
+      sm.qf[kk][ln] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
+    }
+    __syncthreads();
+
+    const unsigned char* kb = p.k_pool + (size_t)pc.kvh * kRowBytes;
+    const unsigned char* vb = p.v_pool + (size_t)pc.kvh * kRowBytes;
+    const int* idx = p.indices + __ldg(p.indptr + pc.b) + pc.j0;
+    const int len = pc.j1 - pc.j0;
+    const int ntiles = (len + 15) >> 4;
+    const int nmine = (ntiles > warp) ? (ntiles - warp + NWARP - 1) / NWARP : 0;
+    // my k-th tile is tile warp + NWARP*k
+    auto tile_n = [&](int k) -> int {
+      const int tt = warp + NWARP * k;
+      return (k < nmine) ? min(16, len - 16 * tt) : 0;
+    };
+    auto fetch = [&](int k) -> int {
+      const int n = tile_n(k);
+      int s = -1;
+      if (lane < n) {
+        s = __ldg(idx + 16 * (warp + NWARP * k) + lane);
+        if (p.check_indices && (s < 0 || (long long)s >= p.num_slots)) {
+          atomicOr(&p.hdr->error, kErrIndex);
+          s = -1;
+        }
+      }
+      return s;
+    };
+
+    MmaWarpState st;
+    st.reset();
+    unsigned char(*ring)[16][kSmemRow] = sm.vring[warp];
+    if (nmine > 0) {
+      const int s0 = fetch(0);
+      int s1 = fetch(1), s2 = fetch(2);
+      issue_v_tile(&ring[0][0][0], vb, stride, s0, tile_n(0), lane);
+      issue_v_tile(&ring[1 % NV][0][0], vb, stride, s1, tile_n(1), lane);
+      st.load_k(kb, stride, s0, lane);
+      int stage = 0;
+      for (int k = 0; k < nmine; ++k) {
+        // V two tiles ahead (an empty group when there is no such tile)
+        issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2), lane);
+        const int s3 = fetch(k + 3);
+        st.qk_softmax(sm.qf, tile_n(k), p.scale_log2, lane);
+        if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
+        cp_async_wait<2>();
+        __syncwarp();
+        st.pv(&ring[stage][0][0], lane);
+        __syncwarp();
+        stage = (stage + 1 == NV) ? 0 : stage + 1;
+        s1 = s2;
+        s2 = s3;
+      }
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+
+    // ---- merge: per-warp slices in the (now idle) V rings, summed in a fixed order
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
+      st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
+    }
+    if (lane < 4) {
+      sm.mbuf[warp][2 * lane] = st.m0;
+      sm.mbuf[warp][2 * lane + 1] = st.m1;
+    }
+    __syncthreads();
+    {
+      const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
+      float Ma = sm.mbuf[0][ha], Mb = sm.mbuf[0][hb];
+#pragma unroll
+      for (int x = 1; x < NWARP; ++x) {
+        Ma = fmaxf(Ma, sm.mbuf[x][ha]);
+        Mb = fmaxf(Mb, sm.mbuf[x][hb]);
+      }
+      const float fa = (Ma == -INFINITY) ? 0.0f : safe_exp2_diff(st.m0, Ma);
+      const float fb = (Mb == -INFINITY) ? 0.0f : safe_exp2_diff(st.m1, Mb);
+      float* slice = reinterpret_cast<float*>(&sm.vring[warp][0][0][0]);
+#pragma unroll
+      for (int dt = 0; dt < 16; ++dt) {
+        const int d = dt * 16 + g;
+        slice[ha * kD + d] = st.o[dt][0] * fa;
+        slice[hb * kD + d] = st.o[dt][1] * fb;
+        slice[ha * kD + d + 8] = st.o[dt][2] * fa;
+        slice[hb * kD + d + 8] = st.o[dt][3] * fb;
+      }
+      if (lane < 4) {
+        sm.lsum[warp][ha] = st.l0 * fa;
+        sm.lsum[warp][hb] = st.l1 * fb;
+      }
+    }
+    __syncthreads();
+    float* op = p.o_part + pc.id * (kG * kD);
+    for (int e = threadIdx.x * 4; e < kG * kD; e += blockDim.x * 4) {
+      const int h = e / kD;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lt = 0.0f;
+#pragma unroll
+      for (int x = 0; x < NWARP; ++x) {
+        const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(&sm.vring[x][0][0][0]) + e);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+        lt += sm.lsum[x][h];
+      }
+      const float inv = (lt > 0.0f) ? 1.0f / lt : 0.0f;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+      *reinterpret_cast<float4*>(op + e) = acc;
+    }
+    if (threadIdx.x < kG) {
+      float M = sm.mbuf[0][threadIdx.x], lt = 0.0f;
+#pragma unroll
+      for (int x = 1; x < NWARP; ++x) M = fmaxf(M, sm.mbuf[x][threadIdx.x]);
+#pragma unroll
+      for (int x = 0; x < NWARP; ++x) lt += sm.lsum[x][threadIdx.x];
+      p.lse_part[pc.id * kG + threadIdx.x] = (lt > 0.0f) ? M + log2f(lt) : -INFINITY;
+    }
+    __syncthreads();  // rings and Q fragments free for the next piece
+  }
+}
 
 // ------------------------------------------------------------------ SIMT arithmetic
 
@@ -235,8 +340,6 @@ struct DirectSimt {
   float p[kTok];
   float alpha;
   uint4 kr[kTok], vr[kTok];
-
-  static __device__ __forceinline__ void prepare_q(const __nv_bfloat16*, DirectSmem&) {}
 
   __device__ __forceinline__ void load_q_regs(const __nv_bfloat16* qg, int lane) {
 #pragma unroll
@@ -370,22 +473,6 @@ struct DirectSimt {
   }
 };
 
-template <class Math>
-__device__ __forceinline__ void math_load_q(Math& m, const __nv_bfloat16* qg, int lane);
-template <>
-__device__ __forceinline__ void math_load_q<DirectMma>(DirectMma&, const __nv_bfloat16*, int) {}
-template <>
-__device__ __forceinline__ void math_load_q<DirectSimt>(DirectSimt& m, const __nv_bfloat16* qg, int lane) {
-  m.load_q_regs(qg, lane);
-}
-
-template <class Math>
-__device__ __forceinline__ void math_pv(Math& m, int lane);
-template <>
-__device__ __forceinline__ void math_pv<DirectMma>(DirectMma& m, int) { m.pv(); }
-template <>
-__device__ __forceinline__ void math_pv<DirectSimt>(DirectSimt& m, int lane) { m.pv_lane(lane); }
-
 // ------------------------------------------------------------------ the kernel
 
 template <class Math>
@@ -416,11 +503,9 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
   Piece pc;
   while (sched.next(pc)) {
     const __nv_bfloat16* qg = p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD;
-    Math::prepare_q(qg, sm);
     Math math;
-    math_load_q(math, qg, lane);
+    math.load_q_regs(qg, lane);
     math.reset();
-    __syncthreads();  // Q fragments in shared memory
 
     const unsigned char* kb = p.k_pool + (size_t)pc.kvh * kRowBytes;
     const unsigned char* vb = p.v_pool + (size_t)pc.kvh * kRowBytes;
@@ -439,7 +524,7 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
       while (true) {
         math.qk_softmax(sm, n, p.scale_log2, lane);
         if (nn > 0) math.load_k(kb, stride, nslot, lane);
-        math_pv(math, lane);
+        math.pv_lane(lane);
         if (nn > 0) math.load_v(vb, stride, nslot, lane);
         if (nn == 0) break;
         n = nn;
@@ -487,9 +572,22 @@ cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStre
   if (variant == kVariantTma) return launch_stage1_tma(p, grid, stream);
   if (variant == kVariantSimt) {
     stage1_direct_kernel<DirectSimt><<<grid, kDirectWarps * 32, 0, stream>>>(p);
-  } else {
-    stage1_direct_kernel<DirectMma><<<grid, kDirectWarps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
   }
+  constexpr int kW = 8, kNV = 3;
+  using Smem = MmaSmem<kW, kNV>;
+  auto kern = stage1_mma_kernel<kW, kNV>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  kern<<<grid, kW * 32, sizeof(Smem), stream>>>(p);
   return cudaGetLastError();
 }
 
