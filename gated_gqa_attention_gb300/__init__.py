@@ -22,7 +22,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "load", "decode", "decode_ex", "gate", "workspace_bytes", "workspace_init", "reserve",
+    "load", "decode", "decode_ex", "decode_noalloc", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
     "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH",
 ]
@@ -32,6 +32,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libgda.so")
 
 VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_TMA = 0, 1, 2, 3
 MAX_SPLITS = 256
+NOALLOC_SCRATCH_BYTES = 16 << 20
 DEVERR_INDEX, DEVERR_TIMEOUT = 0x1, 0x2
 
 _lock = threading.Lock()
@@ -75,6 +76,8 @@ def load(path: Optional[str] = None):
         lib.gda_decode.restype = i32
         lib.gda_decode_ex.argtypes = [ctypes.POINTER(_Args), vp, ctypes.c_size_t, vp]
         lib.gda_decode_ex.restype = i32
+        lib.gda_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
+        lib.gda_decode_noalloc.restype = i32
         lib.gda_reserve.argtypes = [i32, i32, i32, i32, i32]
         lib.gda_reserve.restype = i32
         lib.gda_gate.argtypes = [vp, vp, vp, i64, vp]
@@ -191,6 +194,25 @@ def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, scale: Op
     _check(load().gda_decode(_ptr(q), _ptr(gate_t), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
                              _ptr(kv_indices), _ptr(out), B, Hq, Hkv, D, float(scale), int(num_splits),
                              _stream(stream)))
+    return out
+
+
+def decode_noalloc(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out, scale: Optional[float] = None,
+                   num_splits: int = 0, stream=None):
+    """``gda_decode_noalloc``: the same result as decode() for callers that must not
+    allocate device memory.  ``out`` must be given (this call allocates nothing);
+    the library's fixed scratch area (NOALLOC_SCRATCH_BYTES per device) replaces the
+    workspace, so calls that may overlap on the GPU must not use it concurrently."""
+    _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out)
+    if out is None:
+        raise ValueError("decode_noalloc needs a preallocated out tensor")
+    B, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    _check(load().gda_decode_noalloc(_ptr(q), _ptr(gate_t), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
+                                     _ptr(kv_indices), _ptr(out), B, Hq, Hkv, D, float(scale), int(num_splits),
+                                     _stream(stream)))
     return out
 
 

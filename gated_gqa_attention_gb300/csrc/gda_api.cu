@@ -193,6 +193,32 @@ int ensure_workspace(size_t need, cudaStream_t stream, bool check_capture, void*
   return GDA_OK;
 }
 
+// ---- scratch for gda_decode_noalloc --------------------------------------------
+//
+// Callers that may not allocate device memory get a fixed scratch area instead of
+// the workspace: a file-scope device array, present on every GPU that loads this
+// library until the process exits.  In host code g_noalloc_scratch is only a
+// stand-in for the symbol; its device address comes from cudaGetSymbolAddress,
+// taken once per device with that device current.
+__device__ __align__(256) unsigned char g_noalloc_scratch[GDA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device; the first call on a device
+// looks it up and clears the header (error word) on `stream`.
+int noalloc_scratch(cudaStream_t stream, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return GDA_ERR_CUDA;
+    if (cudaMemsetAsync(ptr, 0, gda::kHeaderBytes, stream) != cudaSuccess) return GDA_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return GDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -250,6 +276,39 @@ int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool, 
   void* ws = nullptr;
   const size_t need = gda_workspace_bytes(B, Hq, Hkv, D, num_splits);
   rc = ensure_workspace(need, reinterpret_cast<cudaStream_t>(stream), true, &ws);
+  if (rc != GDA_OK) return rc;
+  return enqueue(&a, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool, const gda_bf16* v_pool,
+                       const int32_t* kv_indptr, const int32_t* kv_indices, gda_bf16* out, int B, int Hq, int Hkv,
+                       int D, float scale, int num_splits, gda_stream_t stream) {
+  gda_args a = {};
+  a.q = q;
+  a.gate = gate;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.out = out;
+  a.lse = nullptr;
+  a.num_slots = 0;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.scale = scale;
+  a.num_splits = num_splits;
+  a.fuse_gate = 1;
+  a.check_indices = 0;
+  a.variant = GDA_VARIANT_AUTO;
+  a.min_chunk = 0;
+  int rc = validate_args(&a);
+  if (rc != GDA_OK) return rc;
+  if (B == 0) return GDA_OK;
+  if (gda_workspace_bytes(B, Hq, Hkv, D, num_splits) > (size_t)GDA_NOALLOC_SCRATCH_BYTES) return GDA_ERR_WORKSPACE;
+  void* ws = nullptr;
+  rc = noalloc_scratch(reinterpret_cast<cudaStream_t>(stream), &ws);
   if (rc != GDA_OK) return rc;
   return enqueue(&a, ws, reinterpret_cast<cudaStream_t>(stream));
 }

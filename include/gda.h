@@ -147,6 +147,33 @@ int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool,
 int gda_decode_ex(const gda_args* args, void* workspace, size_t workspace_bytes,
                   gda_stream_t stream);
 
+/* Size of the fixed device scratch area that gda_decode_noalloc uses (16 MiB). */
+#define GDA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* gda_decode for callers that must not allocate device memory at all: code that
+ * runs where cudaMalloc is forbidden or unsafe -- a serving loop whose memory was
+ * budgeted and reserved up front, a custom or pooled allocator that owns all
+ * device memory, or a host thread that must never block on the driver's
+ * allocator.  The pages have no counterpart for this entry point.
+ * Same arguments, layouts and result as gda_decode.  Instead of a workspace it
+ * uses one fixed scratch area of GDA_NOALLOC_SCRATCH_BYTES in device memory that
+ * the library declares statically: every GPU that loads the library holds it
+ * until the process exits, and this call never calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ *  - Sizes whose gda_workspace_bytes(B, Hq, Hkv, D, num_splits) exceed
+ *    GDA_NOALLOC_SCRATCH_BYTES are rejected with GDA_ERR_WORKSPACE (nothing is
+ *    enqueued).  With Hq = 16, Hkv = 2, D = 256 that allows B <= 508 in automatic
+ *    mode and B * num_splits <= 1020 with explicit splits.
+ *  - The first call on each device looks up the scratch's device address and
+ *    clears its header on `stream`; make that first call before any stream capture.
+ *  - Every call on a device shares the one scratch area, which keeps the last
+ *    call's contents: calls that may overlap on the GPU (different streams without
+ *    ordering between them) race and give wrong results. */
+int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool,
+                       const gda_bf16* v_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                       gda_bf16* out, int B, int Hq, int Hkv, int D, float scale, int num_splits,
+                       gda_stream_t stream);
+
 /* Grow the internal workspace of the current device for calls up to these sizes,
  * so later gda_decode calls allocate nothing (FreeToken PR #781, Summary:
  * initialise before capture). */
