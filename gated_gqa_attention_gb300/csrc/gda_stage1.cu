@@ -14,22 +14,22 @@
 // row is limited by the copy-request rate (~1.75 TB/s), so:
 //  * Persistent grid, one CTA of 8 warps per SM; the work schedule (gda_device.cuh)
 //    gives each CTA an equal share of the batch's KV stream.
-//  * Warp w takes 16-token tiles w, w+8, ... of the CTA's piece.  Each lane loads
-//    its share of the tile's K and V rows with 16-byte streaming loads straight
-//    into mma.sync fragment registers; the next tile's K loads are in flight while
-//    the softmax and PV run, the next V loads while the next QK runs.
+//  * Warp w takes 16-token tiles w, w+8, ... of the CTA's piece.  K rows are
+//    loaded with 16-byte streaming loads straight into mma.sync fragment
+//    registers one tile ahead (and prefetched into L2 two tiles ahead); V rows go
+//    through a per-warp 3-stage cp.async ring in shared memory, two tiles ahead.
 //  * MMA arithmetic: S^T[16 tok x 8 heads] = K Q^T and O^T[256 x 8] += V^T P^T on
-//    m16n8k16 bf16 tiles with FP32 accumulation.  The head dimension is permuted
-//    (consistently for Q, K and V) so that every 16-byte load lands in fragment
-//    slots: for QK, lane (g, t) holds dims {32c + 8t .. +7} of tokens g and g+8;
-//    for PV it holds dims {64c + 8g .. +7} of tokens 2t, 2t+1, 2t+8, 2t+9, paired
-//    by byte permutes into the V^T fragments.  P is rounded to BF16 and turned
-//    into the B operand with movmatrix.trans; the running sum adds the same
-//    rounded values.
+//    m16n8k16 bf16 tiles with FP32 accumulation.  For QK the head dimension is
+//    permuted (consistently for Q and K) so every 16-byte K load lands in fragment
+//    slots: lane (g, t) holds dims {32c + 8t .. +7} of tokens g and g+8.  V^T
+//    fragments come from the ring through ldmatrix.trans.  P is rounded to BF16
+//    and turned into the B operand with movmatrix.trans; the running sum adds
+//    the same rounded values.
 //  * SIMT arithmetic (variant): lane l owns dims [8l, 8l+8) of every row; 64 FP32
 //    FMAs per token and a transposing warp-shuffle reduction for the 8 scores.
-//  * At the end of a piece the 8 warps merge their (max, sum, O) in shared memory
-//    in a fixed order (deterministic) and one partial is written.
+//  * At the end of a piece each warp writes its rescaled O into its (idle) ring
+//    and all threads add the 8 slices in a fixed order (deterministic); one
+//    partial is written per piece.
 #include "gda_device.cuh"
 #include "gda_kernels.h"
 
@@ -169,6 +169,18 @@ struct MmaWarpState {
   }
 };
 
+// Prefetch into L2 the K rows of a 16-token tile (two lanes per 512-byte row,
+// two 128-byte lines each): the whole row is requested from HBM at once, and the
+// later register loads of that tile (64 bytes per row per instruction) hit L2.
+__device__ __forceinline__ void prefetch_k_tile(const unsigned char* kb, size_t stride, int slot_lane, int lane) {
+  const int s = __shfl_sync(0xffffffffu, slot_lane, lane >> 1);
+  if (s >= 0) {
+    const unsigned char* row = kb + (size_t)s * stride + 256 * (lane & 1);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128));
+  }
+}
+
 // Issue the cp.async copies of one V tile (16 rows; rows >= n and bad slots are
 // zero-filled) into a ring stage and commit them as one group.
 __device__ __forceinline__ void issue_v_tile(unsigned char* stage, const unsigned char* vb, size_t stride,
@@ -242,10 +254,12 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
       issue_v_tile(&ring[0][0][0], vb, stride, s0, tile_n(0), lane);
       issue_v_tile(&ring[1 % NV][0][0], vb, stride, s1, tile_n(1), lane);
       st.load_k(kb, stride, s0, lane);
+      prefetch_k_tile(kb, stride, s1, lane);
       int stage = 0;
       for (int k = 0; k < nmine; ++k) {
         // V two tiles ahead (an empty group when there is no such tile)
         issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2), lane);
+        prefetch_k_tile(kb, stride, s2, lane);
         const int s3 = fetch(k + 3);
         st.qk_softmax(sm.qf, tile_n(k), p.scale_log2, lane);
         if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);

@@ -40,11 +40,12 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
            ((uint32_t)sigmoid_bf16((uint16_t)(g2 >> 16)) << 16);
   }
 
-  pdl_wait_prior_grid();
-
+  // which partials hold this segment: from kv_indptr, an input, so before the wait
   long long first;
   int n;
   segment_pieces(p.indptr, b, kvh, p.Hkv, p.B, p.num_splits, p.grid1, p.min_chunk, &first, &n);
+
+  pdl_wait_prior_grid();
 
   float M = -INFINITY, W = 0.0f;
   float acc[8];
@@ -52,10 +53,11 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
   for (int k = warp; k < n; k += kS2Warps) {
     const long long id = first + k;
-    const float lse = __ldg(p.lse_part + id * kG + g);
-    if (lse == -INFINITY) continue;
+    // the LSE and the O rows are loaded together (no dependent round trip)
+    const float lse = __ldcg(p.lse_part + id * kG + g);
     const float4* src = reinterpret_cast<const float4*>(p.o_part + (id * kG + g) * kD + lane * 8);
-    const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+    const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+    if (lse == -INFINITY) continue;
     const float Mn = fmaxf(M, lse);
     const float fo = (M == -INFINITY) ? 0.0f : exp2f(M - Mn);
     const float fn = exp2f(lse - Mn);
