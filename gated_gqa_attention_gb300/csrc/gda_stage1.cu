@@ -84,6 +84,9 @@ struct MmaSmem {
   float lsum[NWARP][kG];                                 // each warp's rescaled sum
 };
 
+// Lazy-rescale threshold of the MMA softmax, in log2 units.
+constexpr float kLazyLog2 = 8.0f;
+
 struct MmaWarpState {
   uint4 kr[16];
   float o[16][4];
@@ -130,21 +133,24 @@ struct MmaWarpState {
     const int tg = lane >> 2;
     if (tg >= nv) s[0] = s[1] = -INFINITY;
     if (tg + 8 >= nv) s[2] = s[3] = -INFINITY;
-    float xa = fmaxf(s[0], s[2]), xb = fmaxf(s[1], s[3]);
+    // Lazy rescale: the reference maxima m0/m1 move only when a score exceeds
+    // them by more than kLazyLog2 (probabilities then stay below 2^kLazyLog2);
+    // otherwise no max reduction and no rescale of O are needed.  The result is
+    // the same softmax: every probability and sum is relative to one reference.
+    const bool grow = fmaxf(s[0], s[2]) > m0 + kLazyLog2 || fmaxf(s[1], s[3]) > m1 + kLazyLog2;
+    if (__any_sync(0xffffffffu, grow)) {
+      float xa = fmaxf(s[0], s[2]), xb = fmaxf(s[1], s[3]);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
-      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, off));
-    }
-    const float na = fmaxf(m0, xa), nb = fmaxf(m1, xb);
-    const float aa = safe_exp2_diff(m0, na), ab = safe_exp2_diff(m1, nb);
-    P0 = pack_bf16x2(safe_exp2_diff(s[0], na), safe_exp2_diff(s[1], nb));
-    P1 = pack_bf16x2(safe_exp2_diff(s[2], na), safe_exp2_diff(s[3], nb));
-    l0 = l0 * aa + (__uint_as_float(P0 << 16) + __uint_as_float(P1 << 16));
-    l1 = l1 * ab + (__uint_as_float(P0 & 0xFFFF0000u) + __uint_as_float(P1 & 0xFFFF0000u));
-    m0 = na;
-    m1 = nb;
-    if (__any_sync(0xffffffffu, (aa != 1.0f) || (ab != 1.0f))) {
+      for (int off = 4; off < 32; off <<= 1) {
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, off));
+      }
+      const float na = fmaxf(m0, xa), nb = fmaxf(m1, xb);
+      const float aa = safe_exp2_diff(m0, na), ab = safe_exp2_diff(m1, nb);
+      l0 *= aa;
+      l1 *= ab;
+      m0 = na;
+      m1 = nb;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         o[i][0] *= aa;
@@ -153,6 +159,10 @@ struct MmaWarpState {
         o[i][3] *= ab;
       }
     }
+    P0 = pack_bf16x2(safe_exp2_diff(s[0], m0), safe_exp2_diff(s[1], m1));
+    P1 = pack_bf16x2(safe_exp2_diff(s[2], m0), safe_exp2_diff(s[3], m1));
+    l0 += __uint_as_float(P0 << 16) + __uint_as_float(P1 << 16);
+    l1 += __uint_as_float(P0 & 0xFFFF0000u) + __uint_as_float(P1 & 0xFFFF0000u);
   }
 
   // O^T += V^T P^T with V^T fragments from a 16-row shared-memory tile
