@@ -168,11 +168,16 @@ __device__ __forceinline__ float safe_exp2_diff(float a, float m) {
 //   covering positions [s*c, min(L, (s+1)*c)), c = ceil(L/S).  Unit u = sigma*S + s
 //   goes to CTA u % grid; the partial lives at index u.  Empty splits are skipped
 //   by both stages.
-// Automatic mode (S <= 0): the whole stream of total = Hkv * nnz positions is cut
-//   into chunks of T = max(ceil(total/grid), min_chunk) positions, chunk c to CTA c;
-//   the piece (segment sigma, chunk c) lives at index c + sigma.  That index is
-//   unique (a later chunk can only meet a later-or-equal segment) and below
-//   grid + B*Hkv, which bounds the workspace.
+// Automatic mode (S <= 0), decided on the device from kv_indptr alone:
+//   * small batches -- when cutting every segment into ceil(L_max / min_chunk)
+//     equal splits still gives at most one split per CTA (B*Hkv*S <= grid) -- use
+//     those uniform splits exactly as the explicit mode does: every CTA then has
+//     one piece and no piece boundary to cross (the latency-bound regime);
+//   * otherwise the whole stream of total = Hkv * nnz positions is cut into
+//     chunks of T = max(ceil(total/grid), min_chunk) positions, chunk c to CTA c
+//     (equal work per CTA for any length mix); the piece (segment sigma, chunk c)
+//     lives at index c + sigma.  That index is unique (a later chunk can only meet
+//     a later-or-equal segment) and below grid + B*Hkv, which bounds the workspace.
 
 struct Piece {
   int b, kvh, sigma;
@@ -194,7 +199,7 @@ struct Sched {
     indptr = indptr_;
     B = B_;
     Hkv = Hkv_;
-    S = S_;
+    S = (S_ > 0) ? S_ : auto_uniform_splits(indptr_, B_, Hkv_, grid_, min_chunk);
     grid = grid_;
     cta = cta_;
     if (S > 0) {
@@ -215,6 +220,21 @@ struct Sched {
       }
       b = lo;
     }
+  }
+
+  // Automatic mode, small batches: the uniform split count, or 0 for the
+  // chunked (stream) schedule.  Called by every lane of a full warp: the longest
+  // sequence is found with the lanes striding over the batch.
+  static __device__ __forceinline__ int auto_uniform_splits(const int* indptr, int B, int Hkv, int grid,
+                                                            int min_chunk) {
+    if ((long long)B * Hkv > grid) return 0;
+    int lmax = 0;
+    for (int b = (int)(threadIdx.x & 31); b < B; b += 32)
+      lmax = max(lmax, __ldg(indptr + b + 1) - __ldg(indptr + b));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+    const int s = max(1, (lmax + min_chunk - 1) / min_chunk);
+    return ((long long)B * Hkv * s <= grid) ? s : 0;
   }
 
   static __device__ __forceinline__ long long auto_chunk(long long total, int grid, int min_chunk) {
@@ -278,6 +298,7 @@ __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh
     *n = 0;
     return;
   }
+  if (S <= 0) S = Sched::auto_uniform_splits(indptr, B, Hkv, grid, min_chunk);
   if (S > 0) {
     const int c = (L + S - 1) / S;
     *first = (long long)sigma * S;

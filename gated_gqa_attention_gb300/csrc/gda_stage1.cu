@@ -222,15 +222,6 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
 
   Piece pc;
   while (sched.next(pc)) {
-    // Q^T fragments of the piece's 8 heads (the previous piece ended with a barrier)
-    const __nv_bfloat16* qg = p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD;
-    for (int e = threadIdx.x; e < 16 * 32; e += blockDim.x) {
-      const int kk = e >> 5, ln = e & 31;
-      const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
-      sm.qf[kk][ln] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
-    }
-    __syncthreads();
-
     const unsigned char* kb = p.k_pool + (size_t)pc.kvh * kRowBytes;
     const unsigned char* vb = p.v_pool + (size_t)pc.kvh * kRowBytes;
     const int* idx = p.indices + __ldg(p.indptr + pc.b) + pc.j0;
@@ -258,13 +249,26 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
     MmaWarpState st;
     st.reset();
     unsigned char(*ring)[16][kSmemRow] = sm.vring[warp];
+    // first loads of the piece, then the Q^T fragments (their latencies overlap)
+    int s1 = -1, s2 = -1;
     if (nmine > 0) {
       const int s0 = fetch(0);
-      int s1 = fetch(1), s2 = fetch(2);
+      s1 = fetch(1);
+      s2 = fetch(2);
       issue_v_tile(&ring[0][0][0], vb, stride, s0, tile_n(0), lane);
       issue_v_tile(&ring[1 % NV][0][0], vb, stride, s1, tile_n(1), lane);
       st.load_k(kb, stride, s0, lane);
       prefetch_k_tile(kb, stride, s1, lane);
+    }
+    // Q^T fragments of the piece's 8 heads (the previous piece ended with a barrier)
+    const __nv_bfloat16* qg = p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD;
+    for (int e = threadIdx.x; e < 16 * 32; e += blockDim.x) {
+      const int kk = e >> 5, ln = e & 31;
+      const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
+      sm.qf[kk][ln] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
+    }
+    __syncthreads();
+    if (nmine > 0) {
       int stage = 0;
       for (int k = 0; k < nmine; ++k) {
         // V two tiles ahead (an empty group when there is no such tile)
