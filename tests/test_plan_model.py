@@ -1,0 +1,115 @@
+"""A CPU model of the split plan that stage 1 and stage 2 derive on the device.
+
+The device code (Sched and segment_pieces in gda_device.cuh) decides, from
+kv_indptr alone, which CTA computes which (sequence, KV head, position range)
+piece and where the piece's partial is stored.  This model restates the same
+rules and checks their invariants over many random ragged batches: every KV
+position is covered exactly once, piece ids are unique and within the workspace
+capacity, and the list of pieces stage 2 merges for a segment is exactly the set
+stage 1 wrote.  (The GPU parity tests check the device code itself.)"""
+import random
+
+AUTO_MAX_CTAS = 1024
+
+
+def uniform_splits(indptr, Hkv, grid, min_chunk):
+    B = len(indptr) - 1
+    if B * Hkv > grid:
+        return 0
+    lmax = max([indptr[b + 1] - indptr[b] for b in range(B)] + [0])
+    s = max(1, -(-lmax // min_chunk))
+    return s if B * Hkv * s <= grid else 0
+
+
+def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
+    B = len(indptr) - 1
+    if S <= 0:
+        S = uniform_splits(indptr, Hkv, grid, min_chunk)
+    out = []
+    if S > 0:
+        for c in range(grid):
+            u = c
+            while u < B * Hkv * S:
+                sig, s = divmod(u, S)
+                b = sig // Hkv
+                L = indptr[b + 1] - indptr[b]
+                cc = -(-L // S)
+                j0, j1 = s * cc, min(L, s * cc + cc)
+                if j0 < j1:
+                    out.append((b, sig % Hkv, j0, j1, u))
+                u += grid
+        return out, S, None
+    total = Hkv * indptr[B]
+    T = max(-(-total // grid), min_chunk)
+    for c in range(grid):
+        pos, end = c * T, min(total, c * T + T)
+        if pos >= end:
+            continue
+        b = 0
+        while pos < end:
+            while Hkv * indptr[b + 1] <= pos:
+                b += 1
+            base = Hkv * indptr[b]
+            L = indptr[b + 1] - indptr[b]
+            kvh, j0 = divmod(pos - base, L)
+            stop = min(end, base + (kvh + 1) * L)
+            out.append((b, kvh, j0, j0 + stop - pos, c + b * Hkv + kvh))
+            pos = stop
+    return out, 0, T
+
+
+def stage2_ids(indptr, Hkv, b, kvh, S, T):
+    L = indptr[b + 1] - indptr[b]
+    if L <= 0:
+        return []
+    sig = b * Hkv + kvh
+    if S > 0:
+        c = -(-L // S)
+        return [sig * S + k for k in range(-(-L // c))]
+    start = Hkv * indptr[b] + kvh * L
+    return [c + sig for c in range(start // T, (start + L - 1) // T + 1)]
+
+
+def test_plan_invariants_random_batches():
+    rng = random.Random(7)
+    for _ in range(600):
+        B = rng.randint(1, 120)
+        lens = [rng.choice([0, 1, 2, 15, 16, 17, 64, 65, 300, 512, 700, 4096]) for _ in range(B)]
+        indptr = [0]
+        for L in lens:
+            indptr.append(indptr[-1] + L)
+        Hkv = rng.choice([1, 2, 4])
+        grid = rng.choice([1, 7, 152, 1024])
+        min_chunk = rng.choice([1, 16, 64])
+        S_user = rng.choice([0, 0, 0, 1, 3, 8])
+        pieces, S, T = stage1_pieces(indptr, Hkv, grid, min_chunk, S_user)
+        ids = [p[4] for p in pieces]
+        assert len(ids) == len(set(ids))
+        cap = B * Hkv * S_user if S_user > 0 else AUTO_MAX_CTAS + B * Hkv
+        assert all(0 <= i < cap for i in ids)
+        cover = {}
+        for b, kvh, j0, j1, _ in pieces:
+            for j in range(j0, j1):
+                cover[(b, kvh, j)] = cover.get((b, kvh, j), 0) + 1
+        assert all(cover.get((b, kvh, j)) == 1 for b in range(B) for kvh in range(Hkv) for j in range(lens[b]))
+        assert sum(cover.values()) == Hkv * sum(lens)
+        for b in range(B):
+            for kvh in range(Hkv):
+                mine = sorted(p[4] for p in pieces if p[0] == b and p[1] == kvh)
+                assert stage2_ids(indptr, Hkv, b, kvh, S, T) == mine
+
+
+def test_small_batches_get_one_piece_per_cta():
+    # B=4 ragged 512/495/478/461 at Hkv=2: uniform 8 splits, 64 units on 152 CTAs
+    indptr = [0, 512, 1007, 1485, 1946]
+    assert uniform_splits(indptr, 2, 152, 64) == 8
+    # B=64 x 4096 does not fit: the stream schedule balances it instead
+    indptr = [4096 * i for i in range(65)]
+    assert uniform_splits(indptr, 2, 152, 64) == 0
+    pieces, S, T = stage1_pieces(indptr, 2, 152, 64, 0)
+    per_cta = {}
+    for b, kvh, j0, j1, pid in pieces:
+        c = pid - (b * 2 + kvh)
+        per_cta[c] = per_cta.get(c, 0) + (j1 - j0)
+    assert max(per_cta.values()) - min(per_cta.values()) <= T
+    assert max(per_cta.values()) == T
