@@ -211,15 +211,32 @@ struct Sched {
     pos = (long long)cta * T;
     end = min(total, pos + T);
     b = 0;
-    if (pos < end) {
-      // first sequence whose (Hkv-scaled) end lies beyond pos
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if ((long long)Hkv * __ldg(indptr + mid + 1) > pos) hi = mid; else lo = mid + 1;
+    if (pos < end) b = first_seq_ending_after(indptr, B, Hkv, pos);
+  }
+
+  // First sequence b whose (Hkv-scaled) end Hkv*indptr[b+1] lies beyond pos (one
+  // exists).  Called by every lane of a full warp: a 32-way search, each round
+  // one load per lane, so ceil(log32 B) dependent loads instead of log2 B.
+  static __device__ __forceinline__ int first_seq_ending_after(const int* indptr, int B, int Hkv,
+                                                               long long pos) {
+    const int lane = (int)(threadIdx.x & 31);
+    int lo = 0, hi = B - 1;  // the answer lies in [lo, hi]
+    while (lo < hi) {
+      const int step = (hi - lo + 32) / 32;  // 32 candidates cover [lo, hi]
+      const int cand = min(hi, lo + lane * step);
+      const bool past = (long long)Hkv * __ldg(indptr + cand + 1) > pos;
+      const unsigned ball = __ballot_sync(0xffffffffu, past);
+      // candidates are non-decreasing in the lane index; hi itself satisfies `past`
+      if (ball == 0u) {
+        lo = min(hi, lo + 31 * step) + 1;
+      } else {
+        const int f = __ffs(ball) - 1;
+        const int cf = min(hi, lo + f * step);
+        lo = (f == 0) ? lo : min(hi, lo + (f - 1) * step) + 1;
+        hi = cf;
       }
-      b = lo;
     }
+    return lo;
   }
 
   // Automatic mode, small batches: the uniform split count, or 0 for the
