@@ -199,32 +199,42 @@ struct Sched {
     indptr = indptr_;
     B = B_;
     Hkv = Hkv_;
-    S = (S_ > 0) ? S_ : auto_uniform_splits(indptr_, B_, Hkv_, grid_, min_chunk);
     grid = grid_;
     cta = cta_;
+    // the first round of the sequence search and the batch total are loaded
+    // together (and, for small batches, the longest-sequence scan): one round trip
+    const int step0 = (B - 1 + 32) / 32;
+    const int cand0 = min(B - 1, (int)(threadIdx.x & 31) * step0);
+    const int v0 = __ldg(indptr + cand0 + 1);
+    const int ntot = __ldg(indptr + B);
+    S = (S_ > 0) ? S_ : auto_uniform_splits(indptr_, B_, Hkv_, grid_, min_chunk);
     if (S > 0) {
       u = cta;
       return;
     }
-    total = (long long)Hkv * (long long)__ldg(indptr + B);
+    total = (long long)Hkv * (long long)ntot;
     T = auto_chunk(total, grid, min_chunk);
     pos = (long long)cta * T;
     end = min(total, pos + T);
     b = 0;
-    if (pos < end) b = first_seq_ending_after(indptr, B, Hkv, pos);
+    if (pos < end) b = first_seq_ending_after(indptr, B, Hkv, pos, v0);
   }
 
   // First sequence b whose (Hkv-scaled) end Hkv*indptr[b+1] lies beyond pos (one
   // exists).  Called by every lane of a full warp: a 32-way search, each round
   // one load per lane, so ceil(log32 B) dependent loads instead of log2 B.
+  // v0: this lane's value of the first round, indptr[min(B-1, lane*step0) + 1].
   static __device__ __forceinline__ int first_seq_ending_after(const int* indptr, int B, int Hkv,
-                                                               long long pos) {
+                                                               long long pos, int v0) {
     const int lane = (int)(threadIdx.x & 31);
     int lo = 0, hi = B - 1;  // the answer lies in [lo, hi]
+    bool first = true;
     while (lo < hi) {
       const int step = (hi - lo + 32) / 32;  // 32 candidates cover [lo, hi]
       const int cand = min(hi, lo + lane * step);
-      const bool past = (long long)Hkv * __ldg(indptr + cand + 1) > pos;
+      const int v = first ? v0 : __ldg(indptr + cand + 1);
+      first = false;
+      const bool past = (long long)Hkv * v > pos;
       const unsigned ball = __ballot_sync(0xffffffffu, past);
       // candidates are non-decreasing in the lane index; hi itself satisfies `past`
       if (ball == 0u) {

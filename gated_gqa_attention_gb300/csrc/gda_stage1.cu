@@ -17,7 +17,12 @@
 //  * Warp w takes 16-token tiles w, w+8, ... of the CTA's piece.  K rows are
 //    loaded with 16-byte streaming loads straight into mma.sync fragment
 //    registers one tile ahead (and prefetched into L2 two tiles ahead); V rows go
-//    through a per-warp 3-stage cp.async ring in shared memory, two tiles ahead.
+//    through a per-warp 3-stage cp.async ring in shared memory, two tiles ahead,
+//    with an L2 evict-first hint so the streamed rows do not push the indices,
+//    q and the partials out of L2.
+//  * The first loads of the next piece (its Q^T fragments, slots and first K
+//    tile) are issued before the current piece's merge, so a piece boundary does
+//    not restart the pipeline from an empty memory queue.
 //  * MMA arithmetic: S^T[16 tok x 8 heads] = K Q^T and O^T[256 x 8] += V^T P^T on
 //    m16n8k16 bf16 tiles with FP32 accumulation.  For QK the head dimension is
 //    permuted (consistently for Q and K) so every 16-byte K load lands in fragment
@@ -67,8 +72,10 @@ struct DirectSmem {
 // ldmatrix.trans.  O^T accumulators: o[dt] = {O[2t][16dt+g], O[2t+1][16dt+g],
 // O[2t][16dt+g+8], O[2t+1][16dt+g+8]}.
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(policy)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -194,14 +201,14 @@ __device__ __forceinline__ void prefetch_k_tile(const unsigned char* kb, size_t 
 // Issue the cp.async copies of one V tile (16 rows; rows >= n and bad slots are
 // zero-filled) into a ring stage and commit them as one group.
 __device__ __forceinline__ void issue_v_tile(unsigned char* stage, const unsigned char* vb, size_t stride,
-                                             int slot_lane, int n, int lane) {
+                                             int slot_lane, int n, int lane, uint64_t policy) {
   const uint32_t dst0 = smem_u32(stage) + 16 * lane;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int s = __shfl_sync(0xffffffffu, slot_lane, r);
     const bool ok = (r < n) && (s >= 0);
     const unsigned char* src = vb + (ok ? (size_t)s * stride : (size_t)0) + 16 * lane;
-    cp_async16(dst0 + r * kSmemRow, src, ok ? 16u : 0u);
+    cp_async16(dst0 + r * kSmemRow, src, ok ? 16u : 0u, policy);
   }
   cp_async_commit();
 }
@@ -212,6 +219,7 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  static_assert(16 * 32 == 2 * NWARP * 32, "two Q fragments per thread");
 
   // Stage 2 may start its prologue (gate loads and sigmoids) now.
   pdl_launch_dependents();
@@ -219,75 +227,102 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   Sched sched;
   sched.begin(p.indptr, p.B, p.Hkv, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
+  const uint64_t pol_v = l2_policy_evict_first();
+
+  // This warp's tiles of a piece of `len` positions: tile warp + NWARP*k.
+  auto nmine_of = [&](int len) -> int {
+    const int ntiles = (len + 15) >> 4;
+    return (ntiles > warp) ? (ntiles - warp + NWARP - 1) / NWARP : 0;
+  };
+  auto tile_n = [&](int k, int len, int nmine) -> int {
+    return (k < nmine) ? min(16, len - 16 * (warp + NWARP * k)) : 0;
+  };
+  auto fetch = [&](const int* idx, int k, int len, int nmine) -> int {
+    const int n = tile_n(k, len, nmine);
+    int s = -1;
+    if (lane < n) {
+      s = __ldg(idx + 16 * (warp + NWARP * k) + lane);
+      if (p.check_indices && (s < 0 || (long long)s >= p.num_slots)) {
+        atomicOr(&p.hdr->error, kErrIndex);
+        s = -1;
+      }
+    }
+    return s;
+  };
+
+  MmaWarpState st;
+  uint2 qfrag[2];
+  int s0 = -1, s1 = -1, s2 = -1;
+  // Head of a piece: its Q^T fragments (requested first), the slots of this
+  // warp's first three tiles and the K rows of its first tile.  For every piece
+  // after the first this runs before the previous piece's merge, so the loads
+  // are in flight while the warps merge.
+  auto piece_head = [&](const Piece& pp) {
+    const __nv_bfloat16* qg = p.q + ((size_t)pp.b * p.Hq + (size_t)pp.kvh * kG) * kD;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = threadIdx.x + r * NWARP * 32;
+      const int kk = e >> 5, ln = e & 31;
+      const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
+      qfrag[r] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
+    }
+    const int* idx = p.indices + __ldg(p.indptr + pp.b) + pp.j0;
+    const int len = pp.j1 - pp.j0, nmine = nmine_of(len);
+    s0 = fetch(idx, 0, len, nmine);
+    s1 = fetch(idx, 1, len, nmine);
+    s2 = fetch(idx, 2, len, nmine);
+    if (nmine > 0) st.load_k(p.k_pool + (size_t)pp.kvh * kRowBytes, stride, s0, lane);
+  };
 
   Piece pc;
-  while (sched.next(pc)) {
+  bool have = sched.next(pc);
+  if (have) piece_head(pc);
+  while (have) {
     const unsigned char* kb = p.k_pool + (size_t)pc.kvh * kRowBytes;
     const unsigned char* vb = p.v_pool + (size_t)pc.kvh * kRowBytes;
     const int* idx = p.indices + __ldg(p.indptr + pc.b) + pc.j0;
     const int len = pc.j1 - pc.j0;
-    const int ntiles = (len + 15) >> 4;
-    const int nmine = (ntiles > warp) ? (ntiles - warp + NWARP - 1) / NWARP : 0;
-    // my k-th tile is tile warp + NWARP*k
-    auto tile_n = [&](int k) -> int {
-      const int tt = warp + NWARP * k;
-      return (k < nmine) ? min(16, len - 16 * tt) : 0;
-    };
-    auto fetch = [&](int k) -> int {
-      const int n = tile_n(k);
-      int s = -1;
-      if (lane < n) {
-        s = __ldg(idx + 16 * (warp + NWARP * k) + lane);
-        if (p.check_indices && (s < 0 || (long long)s >= p.num_slots)) {
-          atomicOr(&p.hdr->error, kErrIndex);
-          s = -1;
-        }
-      }
-      return s;
-    };
+    const int nmine = nmine_of(len);
 
-    MmaWarpState st;
-    st.reset();
+    st.reset();  // O, max and sum; the K rows of tile 0 are already in flight
     unsigned char(*ring)[16][kSmemRow] = sm.vring[warp];
-    // first loads of the piece, then the Q^T fragments (their latencies overlap)
-    int s1 = -1, s2 = -1;
     if (nmine > 0) {
-      const int s0 = fetch(0);
-      s1 = fetch(1);
-      s2 = fetch(2);
-      issue_v_tile(&ring[0][0][0], vb, stride, s0, tile_n(0), lane);
-      issue_v_tile(&ring[1 % NV][0][0], vb, stride, s1, tile_n(1), lane);
-      st.load_k(kb, stride, s0, lane);
+      issue_v_tile(&ring[0][0][0], vb, stride, s0, tile_n(0, len, nmine), lane, pol_v);
+      issue_v_tile(&ring[1 % NV][0][0], vb, stride, s1, tile_n(1, len, nmine), lane, pol_v);
       prefetch_k_tile(kb, stride, s1, lane);
     }
-    // Q^T fragments of the piece's 8 heads (the previous piece ended with a barrier)
-    const __nv_bfloat16* qg = p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD;
-    for (int e = threadIdx.x; e < 16 * 32; e += blockDim.x) {
-      const int kk = e >> 5, ln = e & 31;
-      const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
-      sm.qf[kk][ln] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
+    // the previous piece's merge ended with a barrier: the fragment buffer is free
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = threadIdx.x + r * NWARP * 32;
+      sm.qf[e >> 5][e & 31] = qfrag[r];
     }
     __syncthreads();
-    if (nmine > 0) {
-      int stage = 0;
-      for (int k = 0; k < nmine; ++k) {
-        // V two tiles ahead (an empty group when there is no such tile)
-        issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2), lane);
-        prefetch_k_tile(kb, stride, s2, lane);
-        const int s3 = fetch(k + 3);
-        st.qk_softmax(sm.qf, tile_n(k), p.scale_log2, lane);
-        if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
-        cp_async_wait<2>();
-        __syncwarp();
-        st.pv(&ring[stage][0][0], lane);
-        __syncwarp();
-        stage = (stage + 1 == NV) ? 0 : stage + 1;
-        s1 = s2;
-        s2 = s3;
-      }
+
+    int stage = 0;
+    for (int k = 0; k < nmine; ++k) {
+      // V two tiles ahead (an empty group when there is no such tile), K rows of
+      // that tile into L2, the slots three tiles ahead; then tile k's QK
+      issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
+      prefetch_k_tile(kb, stride, s2, lane);
+      const int s3 = fetch(idx, k + 3, len, nmine);
+      st.qk_softmax(sm.qf, tile_n(k, len, nmine), p.scale_log2, lane);
+      if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
+      cp_async_wait<2>();
+      __syncwarp();
+      st.pv(&ring[stage][0][0], lane);
+      __syncwarp();
+      stage = (stage + 1 == NV) ? 0 : stage + 1;
+      s1 = s2;
+      s2 = s3;
     }
     cp_async_wait<0>();
     __syncwarp();
+
+    // look ahead: the next piece's first loads go out before this piece's merge
+    Piece nx;
+    const bool have_next = sched.next(nx);
+    if (have_next) piece_head(nx);
 
     // ---- merge: per-warp slices in the (now idle) V rings, summed in a fixed order
 #pragma unroll
@@ -354,7 +389,9 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
       for (int x = 0; x < NWARP; ++x) lt += sm.lsum[x][threadIdx.x];
       p.lse_part[pc.id * kG + threadIdx.x] = (lt > 0.0f) ? M + log2f(lt) : -INFINITY;
     }
-    __syncthreads();  // rings and Q fragments free for the next piece
+    __syncthreads();  // rings, Q fragments and merge buffers free for the next piece
+    pc = nx;
+    have = have_next;
   }
 }
 
