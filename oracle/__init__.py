@@ -73,7 +73,7 @@ def _load():
         lib.oracle_decode.argtypes = [
             u16p, u16p, u16p, u16p, i32p, i32p, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-            i32p, ctypes.c_int64, f64p, u16p, u16p, f64p, ctypes.c_int]
+            ctypes.c_int, f64p, i32p, ctypes.c_int64, f64p, u16p, u16p, f64p, ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -162,7 +162,7 @@ class DecodeResult:
 
 def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, scale: float,
            num_splits: int = 0, pairs=None, want=("o_f64", "o_bf16", "out", "lse"),
-           nthreads: int = 0) -> DecodeResult:
+           nthreads: int = 0, window: int = 0, sinks=None) -> DecodeResult:
     """Gated GQA decode attention in FP64.
 
     q, gate_t: [B, Hq, D] BF16 (uint16 bits or torch bf16); k_pool, v_pool:
@@ -170,6 +170,8 @@ def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, scale: float,
     ``num_splits > 0`` evaluates O through the split-merge formulation.
     ``pairs``: optional int array [n, 2] of (b, h) to evaluate; other rows of the
     outputs are left as zeros (NaN for o_f64 / lse).
+    ``window > 0`` attends to the last ``window`` positions of each sequence only;
+    ``sinks`` ([Hq] floats) adds a per-head sink logit to every softmax denominator.
     """
     lib = _load()
     qa, ga = _u16(q), (None if gate_t is None else _u16(gate_t))
@@ -187,11 +189,15 @@ def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, scale: float,
     o_bf = np.zeros((B, Hq, D), np.uint16) if "o_bf16" in want else None
     out = np.zeros((B, Hq, D), np.uint16) if ("out" in want and ga is not None) else None
     lse = np.full((B, Hq), np.nan) if "lse" in want else None
+    sk = None
+    if sinks is not None:
+        sk = np.ascontiguousarray(np.asarray(sinks, dtype=np.float64).reshape(-1))
+        assert sk.shape == (Hq,)
     rc = lib.oracle_decode(
         _ptr(qa, ctypes.c_uint16), _ptr(ga, ctypes.c_uint16), _ptr(ka, ctypes.c_uint16),
         _ptr(va, ctypes.c_uint16), _ptr(ip, ctypes.c_int32), _ptr(ix, ctypes.c_int32),
         int(num_slots), int(B), int(Hq), int(Hkv), int(D), float(scale), int(num_splits),
-        _ptr(pr, ctypes.c_int32), int(n_pairs), _ptr(o_f64, ctypes.c_double),
+        int(window), _ptr(sk, ctypes.c_double), _ptr(pr, ctypes.c_int32), int(n_pairs), _ptr(o_f64, ctypes.c_double),
         _ptr(o_bf, ctypes.c_uint16), _ptr(out, ctypes.c_uint16), _ptr(lse, ctypes.c_double),
         int(nthreads))
     if rc != ORACLE_OK:

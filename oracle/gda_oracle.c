@@ -30,6 +30,16 @@
  *    O = softmax(Q K^T * scale) V with GQA H_q / H_kv, then O * sigmoid(GATE);
  *    Forward / fp4 notes: a dead (zero-length) row produces zeros.
  *
+ * Variants FreeToken PR #781 lists among the cases its fused path leaves to the
+ * fallback (Automatic dispatch: "no window, sinks, custom scale"; Correctness:
+ * "sinks/window and non-power GQA groups"):
+ *   window W > 0   only the last W positions of each sequence are attended
+ *                  (rows kv_indices[kv_indptr[b] + max(0, L - W) .. kv_indptr[b+1]))
+ *   sinks[h]       a per-head logit that joins the softmax denominator with a
+ *                  zero value row: O = sum_j e^{s_j} V_j / (e^{sink_h} + sum_j e^{s_j}),
+ *                  lse = log(e^{sink_h} + sum_j e^{s_j})
+ *   any G = Hq / Hkv (including non-powers of two), any scale.
+ *
  * Readings where the pages are silent: the sigmoid is the correctly rounded
  * BF16 value of the real sigmoid (no page fixes a device's sigmoid), the KV
  * head of query head h is h / G, a zero-length sequence gives O = 0 and
@@ -149,6 +159,8 @@ static int check_inputs(const int32_t* indptr, const int32_t* indices, int64_t n
 }
 
 /* Full path for the (b, h) pairs listed in `pairs` (2*n_pairs ints: b, h), or
+ * (window > 0: only the last `window` positions of each sequence; sinks != NULL:
+ * the per-head sink logits sinks[h] join every softmax denominator)
  * for every pair in row-major order when pairs == NULL.  Outputs are indexed
  * like the inputs ([B, Hq, D] and [B, Hq]); any output pointer may be NULL.
  *   o_f64  : O in double, before any rounding
@@ -164,11 +176,12 @@ int oracle_decode(const uint16_t* q, const uint16_t* gate,
                   const uint16_t* k_pool, const uint16_t* v_pool,
                   const int32_t* kv_indptr, const int32_t* kv_indices, int64_t num_slots,
                   int B, int Hq, int Hkv, int D, double scale, int num_splits,
+                  int window, const double* sinks,
                   const int32_t* pairs, int64_t n_pairs,
                   double* o_f64, uint16_t* o_bf16, uint16_t* out, double* lse, int nthreads) {
     int rc = check_inputs(kv_indptr, kv_indices, num_slots, B, Hq, Hkv, D);
     if (rc != ORACLE_OK) return rc;
-    if (num_splits < 0) return ORACLE_ERR_SHAPE;
+    if (num_splits < 0 || window < 0) return ORACLE_ERR_SHAPE;
     int G = Hq / Hkv;
     int64_t total = pairs ? n_pairs : (int64_t)B * Hq;
     int64_t max_len = 0;
@@ -204,8 +217,10 @@ int oracle_decode(const uint16_t* q, const uint16_t* gate,
                 int h = pairs ? pairs[2 * t + 1] : (int)(t % Hq);
                 int kvh = h / G;
                 const uint16_t* qrow = q + ((int64_t)b * Hq + h) * D;
-                const int32_t* idx = kv_indices + kv_indptr[b];
                 int64_t L = kv_indptr[b + 1] - kv_indptr[b];
+                int64_t first = (window > 0 && L > window) ? L - window : 0;  /* window: last positions */
+                const int32_t* idx = kv_indices + kv_indptr[b] + first;
+                L -= first;
                 double l_out;
                 if (num_splits == 0) {
                     l_out = attend_range(qrow, k_pool, v_pool, idx, 0, L, Hkv, kvh, D, scale, s_buf, O);
@@ -232,6 +247,18 @@ int oracle_decode(const uint16_t* q, const uint16_t* gate,
                         l_out = M + log(W);
                     } else {
                         l_out = -INFINITY;
+                    }
+                }
+                if (sinks) {
+                    /* the sink joins the denominator: O_total = O * Z / (Z + e^sink),
+                     * written with the max shift of both terms */
+                    double sk = sinks[h];
+                    double M = l_out > sk ? l_out : sk;
+                    if (M > -INFINITY) {
+                        double wo = (l_out == -INFINITY) ? 0.0 : exp(l_out - M);
+                        double ws = (sk == -INFINITY) ? 0.0 : exp(sk - M);
+                        for (int d = 0; d < D; ++d) O[d] = O[d] * wo / (wo + ws);
+                        l_out = M + log(wo + ws);
                     }
                 }
                 int64_t base = ((int64_t)b * Hq + h) * D;

@@ -380,3 +380,117 @@ def test_pins_reject_planted_mistakes():
     x = 1 + 2.0**-8 + 2.0**-30
     via_f32 = int(bf16_bits(torch.tensor([x], dtype=torch.float64).float().to(torch.bfloat16))[0])
     assert via_f32 != int(oracle.bf16_from_double([x])[0])
+
+
+# --------------------------------------------------------------------------- window and sinks
+
+def _ref_args(inp):
+    return (inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
+            inp["scale"])
+
+
+def _window_truncated(inp, W):
+    """The same batch with each sequence cut to its last W positions (CSR rebuilt)."""
+    ip = inp["kv_indptr"].tolist()
+    ix = inp["kv_indices"]
+    parts, new = [], [0]
+    for b in range(len(ip) - 1):
+        L = ip[b + 1] - ip[b]
+        first = max(0, L - W)
+        parts.append(ix[ip[b] + first:ip[b + 1]])
+        new.append(new[-1] + (L - first))
+    out = dict(inp)
+    out["kv_indices"] = torch.cat(parts) if parts else ix[:0]
+    out["kv_indptr"] = torch.tensor(new, dtype=torch.int32)
+    return out
+
+
+@pytest.mark.parametrize("W", [1, 3, 16, 100])
+def test_window_equals_full_attention_on_the_last_rows(W):
+    inp = _tiny(61, [40, 7, 0, 130, 16], 16, 2, 64)
+    res = oracle.decode(*_ref_args(inp), window=W)
+    trunc = _window_truncated(inp, W)
+    O_ref, lse_ref = _sdpa_reference(trunc)       # library SDPA on the kept rows
+    np.testing.assert_allclose(res.o_f64, O_ref, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(res.lse, lse_ref, rtol=1e-12, atol=1e-12)
+    bf = _brute_force(trunc)                        # brute force on the kept rows
+    np.testing.assert_allclose(res.o_f64, bf, rtol=1e-12, atol=1e-14)
+
+
+def test_window_special_cases():
+    inp = _tiny(62, [40, 7, 1], 16, 2, 64)
+    full = oracle.decode(*_ref_args(inp))
+    wide = oracle.decode(*_ref_args(inp), window=10_000)      # W >= L: unchanged
+    assert np.array_equal(full.out, wide.out) and np.array_equal(full.o_f64, wide.o_f64)
+    one = oracle.decode(*_ref_args(inp), window=1)            # W = 1: the last row exactly
+    v = bits_to_float(bf16_bits(inp["v_pool"]))
+    ip, ix = inp["kv_indptr"].tolist(), inp["kv_indices"].tolist()
+    for b in range(3):
+        last = ix[ip[b + 1] - 1]
+        for h in range(16):
+            assert np.array_equal(one.o_f64[b, h], v[last, h // 8])
+    split = oracle.decode(*_ref_args(inp), window=5, num_splits=3)
+    direct = oracle.decode(*_ref_args(inp), window=5)
+    np.testing.assert_allclose(split.o_f64, direct.o_f64, rtol=1e-12, atol=1e-14)
+
+
+def _sdpa_with_sink_key(inp, sinks):
+    """Sinks restated as one extra key per (b, h) whose score is the sink and whose
+    value row is zero, through the library SDPA in float64."""
+    q = torch.from_numpy(bits_to_float(bf16_bits(inp["q"])))
+    k = torch.from_numpy(bits_to_float(bf16_bits(inp["k_pool"])))
+    v = torch.from_numpy(bits_to_float(bf16_bits(inp["v_pool"])))
+    ip = inp["kv_indptr"].tolist()
+    ix = inp["kv_indices"].long()
+    B, Hq, D = q.shape
+    G = Hq // k.shape[1]
+    sc = inp["scale"]
+    O = torch.zeros(B, Hq, D, dtype=torch.float64)
+    lse = torch.zeros(B, Hq, dtype=torch.float64)
+    for b in range(B):
+        rows = ix[ip[b]:ip[b + 1]]
+        for h in range(Hq):
+            qh = q[b, h]
+            ksink = qh * (sinks[h] / (sc * float(qh @ qh)))        # sc * q . ksink == sink
+            kb = torch.cat([k[rows, h // G], ksink[None]])
+            vb = torch.cat([v[rows, h // G], torch.zeros(1, D, dtype=torch.float64)])
+            O[b, h] = torch.nn.functional.scaled_dot_product_attention(
+                qh[None, None, None], kb[None, None], vb[None, None], scale=sc)[0, 0, 0]
+            lse[b, h] = torch.logsumexp(kb @ qh * sc, dim=0)
+    return O.numpy(), lse.numpy()
+
+
+def test_sinks_as_an_extra_zero_value_key():
+    inp = _tiny(63, [40, 7, 0, 90], 16, 2, 64)
+    sinks = np.linspace(-3.0, 4.0, 16)
+    res = oracle.decode(*_ref_args(inp), sinks=sinks)
+    O_ref, lse_ref = _sdpa_with_sink_key(inp, sinks)
+    np.testing.assert_allclose(res.o_f64, O_ref, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(res.lse, lse_ref, rtol=1e-12, atol=1e-12)
+    # with a window as well: the sink joins the windowed softmax
+    resw = oracle.decode(*_ref_args(inp), sinks=sinks, window=9)
+    O_w, lse_w = _sdpa_with_sink_key(_window_truncated(inp, 9), sinks)
+    np.testing.assert_allclose(resw.o_f64, O_w, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(resw.lse, lse_w, rtol=1e-12, atol=1e-12)
+
+
+def test_sinks_closed_forms():
+    inp = _tiny(64, [30, 5], 16, 2, 64)
+    inp["q"] = torch.zeros_like(inp["q"])                  # every score 0
+    sinks = np.linspace(-2.0, 2.0, 16)
+    res = oracle.decode(*_ref_args(inp), sinks=sinks)
+    v = bits_to_float(bf16_bits(inp["v_pool"]))
+    ip, ix = inp["kv_indptr"].tolist(), inp["kv_indices"].numpy()
+    for b in range(2):
+        rows = ix[ip[b]:ip[b + 1]]
+        L = len(rows)
+        for h in range(16):
+            want = v[rows, h // 8].sum(axis=0) / (L + math.exp(sinks[h]))   # sum V / (L + e^sink)
+            np.testing.assert_allclose(res.o_f64[b, h], want, rtol=1e-13, atol=1e-15)
+            assert abs(res.lse[b, h] - math.log(L + math.exp(sinks[h]))) < 1e-12
+    none = oracle.decode(*_ref_args(inp))
+    minus_inf = oracle.decode(*_ref_args(inp), sinks=np.full(16, -np.inf))
+    assert np.array_equal(none.o_f64, minus_inf.o_f64) and np.array_equal(none.out, minus_inf.out)
+    empty = _tiny(65, [0, 3], 16, 2, 64)
+    r = oracle.decode(*_ref_args(empty), sinks=sinks)
+    assert np.all(r.o_f64[0] == 0.0) and np.allclose(r.lse[0], sinks)  # L = 0: O = 0, lse = sink
