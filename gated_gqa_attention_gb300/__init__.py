@@ -53,6 +53,7 @@ class _Args(ctypes.Structure):
         ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
         ("scale", ctypes.c_float), ("num_splits", ctypes.c_int), ("fuse_gate", ctypes.c_int),
         ("check_indices", ctypes.c_int), ("variant", ctypes.c_int), ("min_chunk", ctypes.c_int),
+        ("window", ctypes.c_int), ("sinks", ctypes.c_void_p),
     ]
 
 
@@ -218,10 +219,12 @@ def decode_noalloc(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out, scale:
 
 def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, workspace=None,
               scale: Optional[float] = None, num_splits: int = 0, fuse_gate: bool = True, lse=None,
-              check_indices: bool = False, variant: int = VARIANT_AUTO, min_chunk: int = 0, stream=None):
+              check_indices: bool = False, variant: int = VARIANT_AUTO, min_chunk: int = 0,
+              window: int = 0, sinks=None, stream=None):
     """``gda_decode_ex``: caller workspace (allocated here when None), optional LSE
-    output, the unfused first half (``fuse_gate=False``), device index checks and
-    the stage-1 variant."""
+    output, the unfused first half (``fuse_gate=False``), device index checks, the
+    stage-1 variant, a sliding window (last ``window`` positions) and per-head
+    attention sinks (``sinks``: [Hq] float32 CUDA tensor of logits)."""
     import torch
     _decode_checks(q, gate_t if fuse_gate else None, k_pool, v_pool, kv_indptr, kv_indices, out)
     B, Hq, D = q.shape
@@ -230,6 +233,10 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
         out = torch.empty_like(q)
     if lse is not None:
         _check_tensor("lse", lse, torch.float32, 2, q.device)
+    if sinks is not None:
+        _check_tensor("sinks", sinks, torch.float32, 1, q.device)
+        if sinks.numel() != q.shape[1]:
+            raise ValueError("sinks must have Hq entries")
     if scale is None:
         scale = 1.0 / (D ** 0.5)
     nbytes = workspace_bytes(B, Hq, Hkv, D, num_splits)
@@ -240,7 +247,8 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
               v_pool=_ptr(v_pool), kv_indptr=_ptr(kv_indptr), kv_indices=_ptr(kv_indices),
               out=_ptr(out), lse=_ptr(lse), num_slots=int(k_pool.shape[0]), B=B, Hq=Hq, Hkv=Hkv, D=D,
               scale=float(scale), num_splits=int(num_splits), fuse_gate=1 if fuse_gate else 0,
-              check_indices=1 if check_indices else 0, variant=int(variant), min_chunk=int(min_chunk))
+              check_indices=1 if check_indices else 0, variant=int(variant), min_chunk=int(min_chunk),
+              window=int(window), sinks=_ptr(sinks))
     _check(load().gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

@@ -39,26 +39,30 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int check_sizes(int B, int Hq, int Hkv, int D, int num_splits) {
   if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return GDA_ERR_SHAPE;
   if (num_splits > GDA_MAX_SPLITS) return GDA_ERR_SPLITS;
-  if (D != gda::kD || Hq / Hkv != gda::kG) return GDA_ERR_UNSUPPORTED;
+  if (D != gda::kD) return GDA_ERR_UNSUPPORTED;
   return GDA_OK;
 }
 
-size_t num_pieces(int B, int Hkv, int num_splits) {
-  if (num_splits > 0) return (size_t)B * Hkv * num_splits;
-  return (size_t)gda::kAutoMaxCtas + (size_t)B * Hkv;
+// Groups of up to 8 query heads ("virtual heads") each make one pass over their
+// KV head's rows: G = Hq / Hkv query heads per KV head need ceil(G / 8) passes.
+int passes(int Hq, int Hkv) { return (Hq / Hkv + gda::kG - 1) / gda::kG; }
+
+size_t num_pieces(int B, int vheads, int num_splits) {
+  if (num_splits > 0) return (size_t)B * vheads * num_splits;
+  return (size_t)gda::kAutoMaxCtas + (size_t)B * vheads;
 }
 
 struct Layout {
   size_t o_off, lse_off, total;
 };
 
+// Header, then FP32 partial O [pieces][8][D], then partial LSE [pieces][8].
 Layout layout(int B, int Hq, int Hkv, int D, int num_splits) {
-  const size_t G = (size_t)(Hq / Hkv);
-  const size_t pieces = num_pieces(B, Hkv, num_splits);
+  const size_t pieces = num_pieces(B, Hkv * passes(Hq, Hkv), num_splits);
   Layout l;
   l.o_off = gda::kHeaderBytes;
-  l.lse_off = round_up(l.o_off + pieces * G * (size_t)D * sizeof(float), 256);
-  l.total = round_up(l.lse_off + pieces * G * sizeof(float), 256);
+  l.lse_off = round_up(l.o_off + pieces * gda::kG * (size_t)D * sizeof(float), 256);
+  l.total = round_up(l.lse_off + pieces * gda::kG * sizeof(float), 256);
   return l;
 }
 
@@ -77,13 +81,13 @@ int validate_args(const gda_args* a) {
   if (rc != GDA_OK) return rc;
   if (a->check_indices && a->num_slots < 0) return GDA_ERR_SHAPE;
   if (a->variant < 0 || a->variant > GDA_VARIANT_TMA) return GDA_ERR_UNSUPPORTED;
-  if (a->min_chunk < 0) return GDA_ERR_SHAPE;
+  if (a->min_chunk < 0 || a->window < 0) return GDA_ERR_SHAPE;
   if (a->B == 0) return GDA_OK;
   if (!a->q || !a->k_pool || !a->v_pool || !a->kv_indptr || !a->kv_indices || !a->out) return GDA_ERR_NULL;
   if (a->fuse_gate && !a->gate) return GDA_ERR_NULL;
   if (!aligned(a->q, 16) || !aligned(a->k_pool, 16) || !aligned(a->v_pool, 16) || !aligned(a->out, 16) ||
       (a->gate && !aligned(a->gate, 16)) || !aligned(a->kv_indptr, 4) || !aligned(a->kv_indices, 4) ||
-      (a->lse && !aligned(a->lse, 4)))
+      (a->lse && !aligned(a->lse, 4)) || (a->sinks && !aligned(a->sinks, 4)))
     return GDA_ERR_ALIGN;
   return GDA_OK;
 }
@@ -101,14 +105,27 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   if (sms <= 0) return GDA_ERR_CUDA;
   const Layout l = layout(a->B, a->Hq, a->Hkv, a->D, a->num_splits);
   unsigned char* base = static_cast<unsigned char*>(ws);
+  const int npass = passes(a->Hq, a->Hkv);
+  const long long vheads = (long long)a->Hkv * npass;
+  const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
+  const int auto_grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
+  int splits = a->num_splits > 0 ? a->num_splits : 0;
+  if (splits == 0 && a->window > 0) {
+    // A window bounds every sequence's range by `window`: equal splits of at least
+    // min_chunk positions, about one per CTA (this fits the automatic workspace).
+    const long long segs = (long long)a->B * vheads;
+    const long long by_len = (a->window + min_chunk - 1) / min_chunk;
+    const long long by_grid = (auto_grid + segs - 1) / segs;
+    splits = (int)(by_len < by_grid ? by_len : by_grid);
+    if (splits < 1) splits = 1;
+  }
   int grid;
-  if (a->num_splits > 0) {
-    const long long units = (long long)a->B * a->Hkv * a->num_splits;
+  if (splits > 0) {
+    const long long units = (long long)a->B * vheads * splits;
     grid = (int)(units < sms ? units : sms);
   } else {
-    grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
+    grid = auto_grid;
   }
-  const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
 
   gda::Stage1Params p1;
   p1.q = reinterpret_cast<const __nv_bfloat16*>(a->q);
@@ -123,8 +140,11 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.B = a->B;
   p1.Hq = a->Hq;
   p1.Hkv = a->Hkv;
+  p1.G = a->Hq / a->Hkv;
+  p1.npass = npass;
+  p1.window = a->window;
   p1.scale_log2 = a->scale * 1.44269504088896340736f;
-  p1.num_splits = a->num_splits > 0 ? a->num_splits : 0;
+  p1.num_splits = splits;
   p1.min_chunk = min_chunk;
   p1.check_indices = a->check_indices ? 1 : 0;
   const int variant = (a->variant == GDA_VARIANT_SIMT)  ? gda::kVariantSimt
@@ -149,9 +169,13 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p2.lse_part = p1.lse_part;
   p2.out = reinterpret_cast<__nv_bfloat16*>(a->out);
   p2.lse_out = a->lse;
+  p2.sinks = a->sinks;
   p2.B = a->B;
   p2.Hq = a->Hq;
   p2.Hkv = a->Hkv;
+  p2.G = p1.G;
+  p2.npass = npass;
+  p2.window = a->window;
   p2.num_splits = p1.num_splits;
   p2.grid1 = grid;
   p2.min_chunk = min_chunk;
@@ -270,6 +294,8 @@ int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool, 
   a.check_indices = 0;
   a.variant = GDA_VARIANT_AUTO;
   a.min_chunk = 0;
+  a.window = 0;
+  a.sinks = nullptr;
   int rc = validate_args(&a);
   if (rc != GDA_OK) return rc;
   if (B == 0) return GDA_OK;
@@ -303,6 +329,8 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
   a.check_indices = 0;
   a.variant = GDA_VARIANT_AUTO;
   a.min_chunk = 0;
+  a.window = 0;
+  a.sinks = nullptr;
   int rc = validate_args(&a);
   if (rc != GDA_OK) return rc;
   if (B == 0) return GDA_OK;
@@ -409,7 +437,7 @@ const char* gda_status_str(int status) {
     case GDA_ERR_NULL: return "GDA_ERR_NULL: a required pointer is NULL";
     case GDA_ERR_ALIGN: return "GDA_ERR_ALIGN: a pointer is not aligned (16 bytes for bf16 tensors, 4 for indices)";
     case GDA_ERR_SHAPE: return "GDA_ERR_SHAPE: invalid sizes (B<0, Hq<1, Hkv<1, Hq%Hkv!=0, negative count)";
-    case GDA_ERR_UNSUPPORTED: return "GDA_ERR_UNSUPPORTED: shape not served by the built kernels (D=256, Hq/Hkv=8)";
+    case GDA_ERR_UNSUPPORTED: return "GDA_ERR_UNSUPPORTED: shape or option not served by the built kernels (D = 256)";
     case GDA_ERR_SPLITS: return "GDA_ERR_SPLITS: num_splits exceeds GDA_MAX_SPLITS";
     case GDA_ERR_WORKSPACE: return "GDA_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case GDA_ERR_CAPTURE: return "GDA_ERR_CAPTURE: workspace growth requested while the stream is capturing";

@@ -180,27 +180,44 @@ __device__ __forceinline__ float safe_exp2_diff(float a, float m) {
 //     a later-or-equal segment) and below grid + B*Hkv, which bounds the workspace.
 
 struct Piece {
-  int b, kvh, sigma;
-  int j0, j1;       // positions [j0, j1) of sequence b
-  long long id;     // partial index
+  int b, kvh, sigma;  // kvh: the (virtual) head of the piece, sigma = b * heads + kvh
+  int j0, j1;         // positions [j0, j1) of the sequence's attended range
+  long long base;     // kv_indices offset of position 0 of that range
+  long long id;       // partial index
 };
+
+// Attended range of sequence b: all L positions, or the last `window` of them.
+__device__ __forceinline__ void seq_range(const int* indptr, int b, int window, int* L, long long* base) {
+  const int i0 = __ldg(indptr + b), i1 = __ldg(indptr + b + 1);
+  int len = i1 - i0;
+  int off = 0;
+  if (window > 0 && len > window) {
+    off = len - window;
+    len = window;
+  }
+  *L = len;
+  *base = (long long)i0 + off;
+}
 
 struct Sched {
   const int* indptr;
-  int B, Hkv, S, grid, cta;
+  int B, Hkv, S, grid, cta, window;
   long long T, total;
   // iteration state
   long long pos, end;  // automatic
   int b;
   long long u;         // explicit
 
+  // Hkv_ here is the number of (virtual) heads that split the batch into segments.
+  // window > 0 requires S_ > 0 (the host picks the split count then).
   __device__ __forceinline__ void begin(const int* indptr_, int B_, int Hkv_, int S_, int grid_,
-                                        int cta_, int min_chunk) {
+                                        int cta_, int min_chunk, int window_) {
     indptr = indptr_;
     B = B_;
     Hkv = Hkv_;
     grid = grid_;
     cta = cta_;
+    window = window_;
     // the first round of the sequence search and the batch total are loaded
     // together (and, for small batches, the longest-sequence scan): one round trip
     const int step0 = (B - 1 + 32) / 32;
@@ -277,7 +294,9 @@ struct Sched {
         u += grid;
         const int sigma = (int)(uu / S), s = (int)(uu % S);
         const int bb = sigma / Hkv;
-        const int L = __ldg(indptr + bb + 1) - __ldg(indptr + bb);
+        int L;
+        long long base;
+        seq_range(indptr, bb, window, &L, &base);
         const int c = (L + S - 1) / S;
         const int j0 = s * c;
         const int j1 = min(L, j0 + c);
@@ -287,6 +306,7 @@ struct Sched {
         p.sigma = sigma;
         p.j0 = j0;
         p.j1 = j1;
+        p.base = base;
         p.id = uu;
         return true;
       }
@@ -307,6 +327,7 @@ struct Sched {
     p.sigma = b * Hkv + kvh;
     p.j0 = j0;
     p.j1 = j0 + (int)(stop - pos);
+    p.base = ib;
     p.id = (long long)cta + p.sigma;
     pos = stop;
     return true;
@@ -315,10 +336,13 @@ struct Sched {
 
 // Partials of segment (b, kvh) for stage 2: ids first + k, k in [0, n) (automatic
 // mode: first = c_first + sigma), or sigma*S + k (explicit mode), in position order.
+// (With a window the split count is explicit and L is the windowed length.)
 __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh, int Hkv, int B, int S,
-                                               int grid, int min_chunk, long long* first, int* n) {
+                                               int grid, int min_chunk, int window, long long* first, int* n) {
   const int ib = __ldg(indptr + b);
-  const int L = __ldg(indptr + b + 1) - ib;
+  int L;
+  long long base;
+  seq_range(indptr, b, window, &L, &base);
   const int sigma = b * Hkv + kvh;
   if (L <= 0) {
     *first = 0;

@@ -24,6 +24,9 @@ struct Stage1Params {
   WsHeader* hdr;
   long long num_slots;
   int B, Hq, Hkv;
+  int G;               // query heads per KV head (Hq / Hkv)
+  int npass;           // ceil(G / 8): groups of 8 query heads per KV head ("virtual heads")
+  int window;          // > 0: attend to the last `window` positions only
   float scale_log2;    // scale * log2(e)
   int num_splits;      // > 0 explicit, else automatic
   int min_chunk;       // automatic mode
@@ -37,7 +40,9 @@ struct Stage2Params {
   const float* lse_part;
   __nv_bfloat16* out;
   float* lse_out;      // [B, Hq] natural log, or nullptr
+  const float* sinks;  // [Hq] sink logits (natural units), or nullptr
   int B, Hq, Hkv;
+  int G, npass, window;
   int num_splits;
   int grid1;           // stage-1 grid (automatic-mode chunking)
   int min_chunk;

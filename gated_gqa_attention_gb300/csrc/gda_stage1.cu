@@ -42,6 +42,14 @@ namespace gda {
 
 constexpr int kDirectWarps = 8;
 
+// Query heads of virtual head vh (a group of up to 8 query heads sharing KV head
+// vh / npass): their first row in q and how many of the 8 slots are real.
+__device__ __forceinline__ const __nv_bfloat16* group_q(const Stage1Params& p, int b, int vh, int* gv) {
+  const int kvh = vh / p.npass, pass = vh - kvh * p.npass;
+  *gv = min(kG, p.G - kG * pass);
+  return p.q + ((size_t)b * p.Hq + (size_t)kvh * p.G + (size_t)kG * pass) * kD;
+}
+
 __device__ __forceinline__ uint4 ld_stream(const unsigned char* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   pdl_launch_dependents();
 
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk);
+  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
   const uint64_t pol_v = l2_policy_evict_first();
 
@@ -258,29 +266,31 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   // after the first this runs before the previous piece's merge, so the loads
   // are in flight while the warps merge.
   auto piece_head = [&](const Piece& pp) {
-    const __nv_bfloat16* qg = p.q + ((size_t)pp.b * p.Hq + (size_t)pp.kvh * kG) * kD;
+    int gv;
+    const __nv_bfloat16* qg = group_q(p, pp.b, pp.kvh, &gv);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int e = threadIdx.x + r * NWARP * 32;
       const int kk = e >> 5, ln = e & 31;
       const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
-      qfrag[r] = __ldg(reinterpret_cast<const uint2*>(qg + g * kD + 32 * c + 8 * t + 4 * h));
+      const __nv_bfloat16* row = qg + min(g, gv - 1) * kD;  // never addresses a row beyond the group
+      qfrag[r] = (g < gv) ? __ldg(reinterpret_cast<const uint2*>(row + 32 * c + 8 * t + 4 * h)) : make_uint2(0u, 0u);
     }
-    const int* idx = p.indices + __ldg(p.indptr + pp.b) + pp.j0;
+    const int* idx = p.indices + pp.base + pp.j0;
     const int len = pp.j1 - pp.j0, nmine = nmine_of(len);
     s0 = fetch(idx, 0, len, nmine);
     s1 = fetch(idx, 1, len, nmine);
     s2 = fetch(idx, 2, len, nmine);
-    if (nmine > 0) st.load_k(p.k_pool + (size_t)pp.kvh * kRowBytes, stride, s0, lane);
+    if (nmine > 0) st.load_k(p.k_pool + (size_t)(pp.kvh / p.npass) * kRowBytes, stride, s0, lane);
   };
 
   Piece pc;
   bool have = sched.next(pc);
   if (have) piece_head(pc);
   while (have) {
-    const unsigned char* kb = p.k_pool + (size_t)pc.kvh * kRowBytes;
-    const unsigned char* vb = p.v_pool + (size_t)pc.kvh * kRowBytes;
-    const int* idx = p.indices + __ldg(p.indptr + pc.b) + pc.j0;
+    const unsigned char* kb = p.k_pool + (size_t)(pc.kvh / p.npass) * kRowBytes;
+    const unsigned char* vb = p.v_pool + (size_t)(pc.kvh / p.npass) * kRowBytes;
+    const int* idx = p.indices + pc.base + pc.j0;
     const int len = pc.j1 - pc.j0;
     const int nmine = nmine_of(len);
 
@@ -406,9 +416,13 @@ struct DirectSimt {
   float alpha;
   uint4 kr[kTok], vr[kTok];
 
-  __device__ __forceinline__ void load_q_regs(const __nv_bfloat16* qg, int lane) {
+  __device__ __forceinline__ void load_q_regs(const __nv_bfloat16* qg, int gv, int lane) {
 #pragma unroll
-    for (int h = 0; h < kG; ++h) unpack8(__ldg(reinterpret_cast<const uint4*>(qg + h * kD + lane * 8)), q[h]);
+    for (int h = 0; h < kG; ++h) {
+      const __nv_bfloat16* row = qg + min(h, gv - 1) * kD;  // never addresses a row beyond the group
+      const uint4 r = (h < gv) ? __ldg(reinterpret_cast<const uint4*>(row + lane * 8)) : make_uint4(0u, 0u, 0u, 0u);
+      unpack8(r, q[h]);
+    }
   }
 
   __device__ __forceinline__ void reset() {
@@ -550,7 +564,7 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
   pdl_launch_dependents();
 
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk);
+  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
 
   auto fetch_slot = [&](const int* idx, int tok0, int n) -> int {
@@ -567,14 +581,15 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
 
   Piece pc;
   while (sched.next(pc)) {
-    const __nv_bfloat16* qg = p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD;
+    int gv;
+    const __nv_bfloat16* qg = group_q(p, pc.b, pc.kvh, &gv);
     Math math;
-    math.load_q_regs(qg, lane);
+    math.load_q_regs(qg, gv, lane);
     math.reset();
 
-    const unsigned char* kb = p.k_pool + (size_t)pc.kvh * kRowBytes;
-    const unsigned char* vb = p.v_pool + (size_t)pc.kvh * kRowBytes;
-    const int* idx = p.indices + __ldg(p.indptr + pc.b) + pc.j0;
+    const unsigned char* kb = p.k_pool + (size_t)(pc.kvh / p.npass) * kRowBytes;
+    const unsigned char* vb = p.v_pool + (size_t)(pc.kvh / p.npass) * kRowBytes;
+    const int* idx = p.indices + pc.base + pc.j0;
     const int len = pc.j1 - pc.j0;
     const int ntiles = (len + kTok - 1) / kTok;
     int tile = warp;

@@ -68,13 +68,13 @@ struct MathMma {
   float m0, m1;  // heads 2(lane%4), 2(lane%4)+1
   float l0, l1;  // per-lane partial sums, reduced at the merge
 
-  __device__ __forceinline__ void load_q(const __nv_bfloat16* qg, int lane) {
+  __device__ __forceinline__ void load_q(const __nv_bfloat16* qg, int gv, int lane) {
     const int h = lane >> 2, dq = 2 * (lane & 3);
-    const uint32_t* base = reinterpret_cast<const uint32_t*>(qg + h * kD);
+    const uint32_t* base = reinterpret_cast<const uint32_t*>(qg + min(h, gv - 1) * kD);  // stays in the group
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      qb[kk][0] = __ldg(base + (kk * 16 + dq) / 2);
-      qb[kk][1] = __ldg(base + (kk * 16 + dq + 8) / 2);
+      qb[kk][0] = (h < gv) ? __ldg(base + (kk * 16 + dq) / 2) : 0u;
+      qb[kk][1] = (h < gv) ? __ldg(base + (kk * 16 + dq + 8) / 2) : 0u;
     }
   }
 
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
   pdl_launch_dependents();
 
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk);
+  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window);
   volatile int* abort_flag = &sm.abort_flag;
 
   if (warp == NCW) {
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
     int cur_n = 0, cur_kvh = 0;
     auto load_slots = [&](const Piece& pp, int tt0, int* slots) -> int {
       const int n = min(kTile, pp.j1 - tt0);
-      const int* idx = p.indices + __ldg(p.indptr + pp.b) + tt0;
+      const int* idx = p.indices + pp.base + tt0;
 #pragma unroll
       for (int r = 0; r < kPer; ++r) {
         const int rr = lane + 32 * r;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
     };
     if (have) {
       cur_n = load_slots(pc, t0, cur_slot);
-      cur_kvh = pc.kvh;
+      cur_kvh = pc.kvh / p.npass;
     }
     while (have) {
       if (*abort_flag) {
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
       }
       if (have) {
         nxt_n = load_slots(pc, t0, nxt_slot);
-        nxt_kvh = pc.kvh;
+        nxt_kvh = pc.kvh / p.npass;
       }
       // issue the current tile
       if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) {
@@ -335,7 +335,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
   bool aborted = false;
   Piece pc;
   while (sched.next(pc)) {
-    math.load_q(p.q + ((size_t)pc.b * p.Hq + (size_t)pc.kvh * kG) * kD, lane);
+    {
+      // query heads of virtual head pc.kvh: up to 8 of KV head pc.kvh / npass
+      const int kvh = pc.kvh / p.npass, pass = pc.kvh - kvh * p.npass;
+      const int gv = min(kG, p.G - kG * pass);
+      math.load_q(p.q + ((size_t)pc.b * p.Hq + (size_t)kvh * p.G + (size_t)kG * pass) * kD, gv, lane);
+    }
     math.reset();
     for (int t0 = pc.j0; t0 < pc.j1; t0 += kTile) {
       const int n = min(kTile, pc.j1 - t0);

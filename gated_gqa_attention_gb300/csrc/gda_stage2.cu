@@ -8,6 +8,8 @@
 // sigmoid of the gate rounded to BF16, their product rounded to nearest even --
 // so no separate sigmoid or multiply kernel runs.  A zero-length sequence gives
 // O = 0 (cuDNN FE-OSS "Gated Attention Block (SM107)": a dead row produces zeros).
+// Optional per-head attention sinks join the merged denominator here (FreeToken
+// PR #781, Automatic dispatch lists sinks among the cases of the general path).
 //
 // One CTA per (sequence, query head), 4 warps.  The prologue -- loading the gate
 // and computing its BF16 sigmoid -- runs before griddepcontrol.wait, overlapping
@@ -28,7 +30,9 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
 
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, h = bh % p.Hq;
-  const int kvh = h / kG, g = h % kG;
+  // query head h belongs to KV head h / G; its slot g in virtual head vh (groups of 8)
+  const int kvh = h / p.G, r = h - kvh * p.G;
+  const int vh = kvh * p.npass + r / kG, g = r % kG;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // prologue: this thread's two gate values and their BF16 sigmoids
@@ -43,7 +47,9 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   // which partials hold this segment: from kv_indptr, an input, so before the wait
   long long first;
   int n;
-  segment_pieces(p.indptr, b, kvh, p.Hkv, p.B, p.num_splits, p.grid1, p.min_chunk, &first, &n);
+  segment_pieces(p.indptr, b, vh, p.Hkv * p.npass, p.B, p.num_splits, p.grid1, p.min_chunk, p.window, &first, &n);
+  // attention sink (a logit in the softmax denominator with no value row), log2 units
+  const float sink2 = (p.sinks != nullptr) ? __ldg(p.sinks + h) * 1.44269504088896340736f : -INFINITY;
 
   pdl_wait_prior_grid();
 
@@ -75,9 +81,9 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   }
   __syncthreads();
 
-  float Mt = s_m[0];
+  float Mt = sink2;
 #pragma unroll
-  for (int x = 1; x < kS2Warps; ++x) Mt = fmaxf(Mt, s_m[x]);
+  for (int x = 0; x < kS2Warps; ++x) Mt = fmaxf(Mt, s_m[x]);
   float o0 = 0.0f, o1 = 0.0f, Wt = 0.0f;
   if (Mt != -INFINITY) {
 #pragma unroll
@@ -87,6 +93,7 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
       o1 += s_acc[x][2 * tid + 1] * f;
       Wt += s_w[x] * f;
     }
+    if (sink2 != -INFINITY) Wt += exp2f(sink2 - Mt);
     o0 /= Wt;
     o1 /= Wt;
   }

@@ -9,7 +9,9 @@
  *   O[b,h,:]   = softmax_j(scale * q[b,h,:] . K[slot_j, h/G, :]) V[slot_j, h/G, :]
  *   slot_j     = kv_indices[kv_indptr[b] + j],  0 <= j < kv_indptr[b+1]-kv_indptr[b]
  *
- * with G = Hq / Hkv consecutive query heads sharing one KV head.  Sources: FreeToken
+ * with G = Hq / Hkv consecutive query heads sharing one KV head (any G >= 1; the
+ * kernels handle the query heads of a KV head in groups of up to 8, so for G > 8
+ * the KV head's rows are read once per group).  Sources: FreeToken
  * PR #781 "Fuse the BF16 attention output sigmoid gate into the existing Triton
  * decode stage2" (Summary: split-KV stage 1, FP32 LSE merge in stage 2 with the
  * BF16 gate and an explicit round-to-nearest-even product fused into its epilogue;
@@ -51,8 +53,8 @@ typedef enum gda_status {
     GDA_ERR_NULL = -1,          /* a required pointer is NULL */
     GDA_ERR_ALIGN = -2,         /* a pointer is not 16-byte aligned */
     GDA_ERR_SHAPE = -3,         /* B < 0, Hq < 1, Hkv < 1, Hq % Hkv != 0, num_slots < 0, n < 0 */
-    GDA_ERR_UNSUPPORTED = -4,   /* a shape the built kernels do not serve (D != 256 or
-                                   Hq/Hkv != 8): declined, never run slowly */
+    GDA_ERR_UNSUPPORTED = -4,   /* a shape or option the built kernels do not serve (D != 256,
+                                   an unknown variant): declined, never run slowly */
     GDA_ERR_SPLITS = -5,        /* num_splits > GDA_MAX_SPLITS */
     GDA_ERR_WORKSPACE = -6,     /* workspace NULL, misaligned or smaller than gda_workspace_bytes */
     GDA_ERR_CAPTURE = -7,       /* the internal workspace must grow while `stream` is capturing */
@@ -97,6 +99,15 @@ typedef enum gda_status {
  *               GDA_DEVERR_INDEX is set in the workspace's error word.
  *   variant     GDA_VARIANT_* (stage-1 arithmetic).
  *   min_chunk   automatic mode: smallest chunk in tokens per CTA (0: built-in default).
+ *   window      > 0: sliding window -- sequence b attends only to its last `window`
+ *               positions, kv_indices[kv_indptr[b+1] - min(L, window) .. kv_indptr[b+1]);
+ *               0: all positions.  With num_splits <= 0 the split count is then chosen
+ *               on the host (equal splits of the window).
+ *   sinks       [Hq] float sink logits or NULL: attention sinks, one logit per query head
+ *               that joins the softmax denominator with a zero value row,
+ *               O = sum_j e^{s_j} V_j / (e^{sink_h} + sum_j e^{s_j}); lse includes it.
+ * (FreeToken PR #781, Automatic dispatch and Correctness: window, sinks, custom scale
+ * and non-power-of-two GQA groups are the cases of the general path.)
  */
 typedef struct gda_args {
     const gda_bf16* q;
@@ -115,12 +126,15 @@ typedef struct gda_args {
     int check_indices;
     int variant;
     int min_chunk;
+    int window;
+    const float* sinks;
 } gda_args;
 
 /* Bytes of workspace gda_decode_ex needs for these sizes (FreeToken PR #781 Summary:
  * stage 1 writes per-split partial O and LSE that stage 2 merges).  The workspace
  * holds a 256-byte header (error word, plan), then FP32 partials
- * [pieces][G][D] and partial LSE [pieces][G].  Returns 0 for invalid sizes. */
+ * [pieces][8][D] and partial LSE [pieces][8].  Returns 0 for invalid sizes.  The
+ * size for num_splits <= 0 also covers every call with a window. */
 size_t gda_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
 
 /* Zero the workspace header (error word) on `stream`.  Call once after allocating

@@ -62,7 +62,9 @@ def test_workspace_bytes(lib):
     assert gda.workspace_bytes(-1, 16, 2, 256, 0) == 0
     assert gda.workspace_bytes(4, 16, 3, 256, 0) == 0      # Hq % Hkv
     assert gda.workspace_bytes(4, 16, 2, 128, 0) == 0      # D unsupported
-    assert gda.workspace_bytes(4, 16, 4, 256, 0) == 0      # group of 4 unsupported
+    assert gda.workspace_bytes(4, 16, 4, 256, 0) > 0       # any group size (here 4)
+    # G = 16 makes two passes (virtual heads of 8): twice the pieces of G = 8 at the same Hkv
+    assert gda.workspace_bytes(4, 32, 2, 256, 8) > 1.9 * gda.workspace_bytes(4, 16, 2, 256, 8)
     assert gda.workspace_bytes(4, 16, 2, 256, 257) == 0    # too many splits
 
 
@@ -88,7 +90,6 @@ def test_decode_host_validation(lib):
     assert _decode(lib, Hq=16, Hkv=3) == ERR_SHAPE
     assert _decode(lib, Hkv=0) == ERR_SHAPE
     assert _decode(lib, D=128) == ERR_UNSUPPORTED
-    assert _decode(lib, Hq=8, Hkv=2) == ERR_UNSUPPORTED
     assert _decode(lib, splits=300) == ERR_SPLITS
     # B == 0 is a valid empty call: nothing to do, no pointer needed
     assert _decode(lib, {"q": 0, "gate": 0, "k": 0, "v": 0, "indptr": 0, "indices": 0, "out": 0}, B=0) == OK
@@ -97,7 +98,7 @@ def test_decode_host_validation(lib):
 def test_decode_ex_host_validation(lib):
     args = gda._Args(q=16, gate=16, k_pool=16, v_pool=16, kv_indptr=16, kv_indices=16, out=16, lse=None,
                      num_slots=10, B=2, Hq=16, Hkv=2, D=256, scale=0.0625, num_splits=0, fuse_gate=1,
-                     check_indices=0, variant=0, min_chunk=0)
+                     check_indices=0, variant=0, min_chunk=0, window=0, sinks=None)
     call = lambda a, ws=256, nbytes=1 << 30: lib.gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(ws) if ws else None,
                                                                nbytes, None)
     assert lib.gda_decode_ex(None, None, 0, None) == ERR_NULL
@@ -119,6 +120,12 @@ def test_decode_ex_host_validation(lib):
     a5 = gda._Args.from_buffer_copy(args)
     a5.lse = 2
     assert call(a5) == ERR_ALIGN
+    a6 = gda._Args.from_buffer_copy(args)
+    a6.window = -1
+    assert call(a6) == ERR_SHAPE
+    a7 = gda._Args.from_buffer_copy(args)
+    a7.sinks = 6
+    assert call(a7) == ERR_ALIGN
 
 
 def test_gate_and_misc_host_validation(lib):

@@ -1,0 +1,105 @@
+"""Decode-kernel variants on the GPU against the FP64 oracle: sliding window,
+attention sinks, any GQA group size (FreeToken PR #781, Automatic dispatch and
+Correctness: window, sinks, custom scale and non-power-of-two GQA groups are the
+cases of the general path).  Same tolerance as the main parity tests."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_gqa_attention_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 4e-3, 1.6e-2
+LENS = [0, 1, 5, 63, 64, 65, 200, 1000, 16, 129, 4096]
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def check_close(got, want):
+    g = oracle.double_from_bf16(got)
+    w = oracle.double_from_bf16(want)
+    bad = np.abs(g - w) > ATOL + RTOL * np.abs(w)
+    assert not bad.any(), "%d / %d out of tolerance, worst %.3g" % (bad.sum(), bad.size, np.abs(g - w).max())
+
+
+def run(gda, inp, **kw):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    sinks = kw.pop("sinks", None)
+    lse = kw.pop("lse", None)
+    out = gda.decode_ex(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"],
+                        scale=d["scale"], sinks=None if sinks is None else torch.as_tensor(
+                            sinks, dtype=torch.float32).cuda(), lse=lse, **kw)
+    torch.cuda.synchronize()
+    return bits(out)
+
+
+def reference(inp, **kw):
+    return oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"],
+                         inp["kv_indices"], inp["scale"], **kw)
+
+
+@pytest.fixture(scope="module")
+def batch():
+    return workloads.make(LENS, seed=201, layout="perm", pool_slots=8000)
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("window", [1, 7, 64, 300, 100_000])
+def test_sliding_window(gda, batch, variant, window):
+    ref = reference(batch, window=window)
+    for splits in (0, 3):
+        check_close(run(gda, batch, window=window, num_splits=splits, variant=variant), ref.out)
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+def test_attention_sinks(gda, batch, variant):
+    rng = np.random.default_rng(5)
+    sinks = rng.normal(0.0, 3.0, 16).astype(np.float32)
+    sinks[3] = -np.inf                     # a head without a sink
+    sinks[7] = 40.0                        # a sink that dominates the softmax
+    ref = reference(batch, sinks=sinks.astype(np.float64))
+    for splits in (0, 5):
+        check_close(run(gda, batch, sinks=sinks, num_splits=splits, variant=variant), ref.out)
+
+
+def test_sinks_lse_and_empty_rows(gda, batch):
+    sinks = np.linspace(-2, 2, 16).astype(np.float32)
+    ref = reference(batch, sinks=sinks.astype(np.float64))
+    lse = torch.empty(len(LENS), 16, dtype=torch.float32, device="cuda")
+    got = run(gda, batch, sinks=sinks, lse=lse)
+    check_close(got, ref.out)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)   # L = 0 rows: lse = sink
+    assert np.all(got[0] == 0)
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 16), (16, 8), (6, 2), (16, 4), (12, 2), (14, 2), (32, 2), (48, 2), (24, 1)])
+@pytest.mark.parametrize("variant", [1, 2, 3])
+def test_gqa_group_sizes(gda, hq, hkv, variant):
+    inp = workloads.make([1, 37, 300, 0, 129], seed=300 + hq + hkv, hq=hq, hkv=hkv, layout="perm", pool_slots=1000)
+    ref = reference(inp)
+    for splits in (0, 4):
+        check_close(run(gda, inp, num_splits=splits, variant=variant), ref.out)
+
+
+def test_everything_together(gda):
+    inp = workloads.make([700, 1, 0, 2500, 90], seed=401, hq=12, hkv=2, layout="pages", page=16,
+                         pool_slots=4000, scale=0.09, peaky_frac=0.02)
+    sinks = np.linspace(-1, 3, 12).astype(np.float32)
+    ref = reference(inp, window=333, sinks=sinks.astype(np.float64))
+    lse = torch.empty(5, 12, dtype=torch.float32, device="cuda")
+    got = run(gda, inp, window=333, sinks=sinks, lse=lse)
+    check_close(got, ref.out)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
+
+
+def test_window_on_the_ragged_workload(gda):
+    inp = workloads.make_workload("b224_ragged")
+    pairs = np.array([(b, h) for b in range(0, 224, 7) for h in (0, 5, 8, 15)])
+    ref = reference(inp, window=1024, pairs=pairs)
+    got = run(gda, inp, window=1024)
+    idx = tuple(pairs.T)
+    check_close(got[idx], ref.out[idx])
