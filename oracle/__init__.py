@@ -75,6 +75,10 @@ def _load():
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
             ctypes.c_int, f64p, i32p, ctypes.c_int64, f64p, u16p, u16p, f64p, ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_qk_norm_rope_kv_write.argtypes = [
+            u16p, ctypes.c_int64, u16p, u16p, ctypes.c_double, u16p, u16p, ctypes.c_int, i32p,
+            u16p, u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_qk_norm_rope_kv_write.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -203,3 +207,34 @@ def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, scale: float,
     if rc != ORACLE_OK:
         raise ValueError("oracle_decode rejected its inputs (status %d)" % rc)
     return DecodeResult(o_f64, o_bf, out, lse)
+
+
+def qk_norm_rope_kv_write(qgkv, w_q, w_k, eps: float, cos_t, sin_t, rope_dim: int, slots, k_pool, v_pool,
+                          Hq: int, Hkv: int, D: int):
+    """The step before attention, in FP64 with one BF16 rounding per output.
+
+    qgkv: [B, (2 Hq + 2 Hkv) * D] BF16 rows [q | gate | k | v]; w_q / w_k: [D] BF16 or
+    None (no norm); cos_t / sin_t: [B, rope_dim] BF16; slots: [B] int32.  Returns
+    (q_out [B, Hq, D], gate_out [B, Hq, D], k_pool, v_pool) as uint16 bit arrays; the
+    pools are copies of the given ones with the new rows written."""
+    lib = _load()
+    x = _u16(qgkv)
+    B = x.shape[0]
+    x = x.reshape(B, -1)
+    wq = None if w_q is None else _u16(w_q)
+    wk = None if w_k is None else _u16(w_k)
+    cs = _u16(cos_t).reshape(B, -1) if rope_dim else np.zeros((B, 0), np.uint16)
+    sn = _u16(sin_t).reshape(B, -1) if rope_dim else np.zeros((B, 0), np.uint16)
+    sl = _i32(slots)
+    kp = _u16(k_pool).copy()
+    vp = _u16(v_pool).copy()
+    qo = np.zeros((B, Hq, D), np.uint16)
+    go = np.zeros((B, Hq, D), np.uint16)
+    rc = lib.oracle_qk_norm_rope_kv_write(
+        _ptr(x, ctypes.c_uint16), int(x.shape[1]), _ptr(wq, ctypes.c_uint16), _ptr(wk, ctypes.c_uint16),
+        float(eps), _ptr(cs, ctypes.c_uint16), _ptr(sn, ctypes.c_uint16), int(rope_dim),
+        _ptr(sl, ctypes.c_int32), _ptr(qo, ctypes.c_uint16), _ptr(go, ctypes.c_uint16),
+        _ptr(kp, ctypes.c_uint16), _ptr(vp, ctypes.c_uint16), int(kp.shape[0]), int(B), int(Hq), int(Hkv), int(D))
+    if rc != ORACLE_OK:
+        raise ValueError("oracle_qk_norm_rope_kv_write rejected its inputs (status %d)" % rc)
+    return qo, go, kp, vp

@@ -283,6 +283,74 @@ int oracle_decode(const uint16_t* q, const uint16_t* gate,
     return err;
 }
 
+/* ---- the step before attention: Q/K RMSNorm, partial RoPE, KV write ------------
+ *
+ * cuDNN FE-OSS "Gated Attention Block (SM107)", Overview stages (2)+(3): per head,
+ * an optional RMSNorm of Q and K (weights w_q_norm, w_k_norm [D]) and a rotary
+ * embedding of the first rope_dim dims in the rotate-half convention (Weights and
+ * tables: cos, sin [B, rope_dim]); V passes through.  The projection output of
+ * one token is the flat row [q (Hq*D) | gate (Hq*D) | k (Hkv*D) | v (Hkv*D)]
+ * (W_qkvg column blocks Q | GATE | K | V).  For each token b:
+ *   y   = x / sqrt(mean(x^2) + eps) * w           (RMSNorm, when w != NULL)
+ *   for i < rope_dim/2, j = i + rope_dim/2:
+ *     out_i = y_i cos_i - y_j sin_i,   out_j = y_j cos_j + y_i sin_j
+ *   out_i = y_i for i >= rope_dim
+ * all in double, rounded once to BF16.  Outputs: q_out [B,Hq,D], gate_out [B,Hq,D]
+ * (a copy), and the token's K and V rows written to k_pool / v_pool at slots[b].
+ */
+static void norm_rope_row(const uint16_t* x, const uint16_t* w, double eps, const uint16_t* cs,
+                          const uint16_t* sn, int rope_dim, int D, uint16_t* out) {
+    double y[1024];
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d) {
+        y[d] = oracle_double_from_bf16(x[d]);
+        ss += y[d] * y[d];
+    }
+    if (w) {
+        double r = 1.0 / sqrt(ss / D + eps);
+        for (int d = 0; d < D; ++d) y[d] = y[d] * r * oracle_double_from_bf16(w[d]);
+    }
+    int half = rope_dim / 2;
+    for (int d = 0; d < D; ++d) {
+        double v = y[d];
+        if (d < half) {
+            v = y[d] * oracle_double_from_bf16(cs[d]) - y[d + half] * oracle_double_from_bf16(sn[d]);
+        } else if (d < rope_dim) {
+            v = y[d] * oracle_double_from_bf16(cs[d]) + y[d - half] * oracle_double_from_bf16(sn[d]);
+        }
+        out[d] = oracle_bf16_from_double(v);
+    }
+}
+
+int oracle_qk_norm_rope_kv_write(const uint16_t* qgkv, int64_t row_stride, const uint16_t* w_q,
+                                 const uint16_t* w_k, double eps, const uint16_t* cos_t,
+                                 const uint16_t* sin_t, int rope_dim, const int32_t* slots,
+                                 uint16_t* q_out, uint16_t* gate_out, uint16_t* k_pool,
+                                 uint16_t* v_pool, int64_t num_slots, int B, int Hq, int Hkv, int D) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || D > 1024 || rope_dim < 0 || rope_dim > D || rope_dim % 2)
+        return ORACLE_ERR_SHAPE;
+    if (row_stride < (int64_t)(2 * Hq + 2 * Hkv) * D) return ORACLE_ERR_SHAPE;
+    for (int b = 0; b < B; ++b)
+        if (slots[b] < 0 || slots[b] >= num_slots) return ORACLE_ERR_INDEX;
+    for (int b = 0; b < B; ++b) {
+        const uint16_t* row = qgkv + (int64_t)b * row_stride;
+        const uint16_t* cs = cos_t + (int64_t)b * rope_dim;
+        const uint16_t* sn = sin_t + (int64_t)b * rope_dim;
+        for (int h = 0; h < Hq; ++h) {
+            norm_rope_row(row + (int64_t)h * D, w_q, eps, cs, sn, rope_dim, D,
+                          q_out + ((int64_t)b * Hq + h) * D);
+            memcpy(gate_out + ((int64_t)b * Hq + h) * D, row + (int64_t)(Hq + h) * D, sizeof(uint16_t) * D);
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            norm_rope_row(row + (int64_t)(2 * Hq + h) * D, w_k, eps, cs, sn, rope_dim, D,
+                          k_pool + ((int64_t)slots[b] * Hkv + h) * D);
+            memcpy(v_pool + ((int64_t)slots[b] * Hkv + h) * D, row + (int64_t)(2 * Hq + Hkv + h) * D,
+                   sizeof(uint16_t) * D);
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
