@@ -22,7 +22,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "load", "decode", "decode_ex", "decode_noalloc", "gate", "workspace_bytes", "workspace_init", "reserve",
+    "load", "decode", "decode_ex", "decode_noalloc", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
     "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH",
 ]
@@ -79,6 +79,9 @@ def load(path: Optional[str] = None):
         lib.gda_decode_ex.restype = i32
         lib.gda_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
         lib.gda_decode_noalloc.restype = i32
+        lib.gda_qk_norm_rope_kv_write.argtypes = [vp, i64, vp, vp, f32, vp, vp, i32, vp, i64, vp, vp, vp, vp,
+                                                  i32, i32, i32, i32, vp]
+        lib.gda_qk_norm_rope_kv_write.restype = i32
         lib.gda_reserve.argtypes = [i32, i32, i32, i32, i32]
         lib.gda_reserve.restype = i32
         lib.gda_gate.argtypes = [vp, vp, vp, i64, vp]
@@ -252,6 +255,33 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
     _check(load().gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def qk_norm_rope_kv_write(qgkv, slots, k_pool, v_pool, Hq: int, w_q_norm=None, w_k_norm=None, eps: float = 1e-6,
+                          cos=None, sin=None, rope_dim: int = 0, q_out=None, gate_out=None, stream=None):
+    """The step before attention: q_out = rope(rmsnorm(q)), the token's K row
+    rope(rmsnorm(k)) and V row written into the pools at ``slots``, and the gate
+    copied out.  qgkv: [B, (2 Hq + 2 Hkv) * D] bf16 rows [q | gate | k | v]."""
+    import torch
+    _check_tensor("qgkv", qgkv, torch.bfloat16, 2)
+    dev = qgkv.device
+    _check_tensor("slots", slots, torch.int32, 1, dev)
+    _check_tensor("k_pool", k_pool, torch.bfloat16, 3, dev)
+    _check_tensor("v_pool", v_pool, torch.bfloat16, 3, dev)
+    B = qgkv.shape[0]
+    num_slots, Hkv, D = k_pool.shape
+    for name, t in (("w_q_norm", w_q_norm), ("w_k_norm", w_k_norm), ("cos", cos), ("sin", sin)):
+        if t is not None:
+            _check_tensor(name, t, torch.bfloat16, device=dev)
+    if q_out is None:
+        q_out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    if gate_out is None:
+        gate_out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    _check(load().gda_qk_norm_rope_kv_write(
+        _ptr(qgkv), qgkv.shape[1], _ptr(w_q_norm), _ptr(w_k_norm), float(eps), _ptr(cos), _ptr(sin),
+        int(rope_dim), _ptr(slots), num_slots, _ptr(q_out), _ptr(gate_out), _ptr(k_pool), _ptr(v_pool),
+        B, int(Hq), Hkv, D, _stream(stream)))
+    return q_out, gate_out
 
 
 def gate(o, gate_t, out=None, stream=None):

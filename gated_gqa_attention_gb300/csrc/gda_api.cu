@@ -341,6 +341,46 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
   return enqueue(&a, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gda_qk_norm_rope_kv_write(const gda_bf16* qgkv, int64_t row_stride, const gda_bf16* w_q_norm,
+                              const gda_bf16* w_k_norm, float eps, const gda_bf16* cos_t, const gda_bf16* sin_t,
+                              int rope_dim, const int32_t* slots, int64_t num_slots, gda_bf16* q_out,
+                              gda_bf16* gate_out, gda_bf16* k_pool, gda_bf16* v_pool, int B, int Hq, int Hkv, int D,
+                              gda_stream_t stream) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || num_slots < 0) return GDA_ERR_SHAPE;
+  if (row_stride < (int64_t)(2 * Hq + 2 * Hkv) * D) return GDA_ERR_SHAPE;
+  if (rope_dim < 0 || rope_dim > D) return GDA_ERR_SHAPE;
+  if (D != gda::kD || rope_dim % 16 != 0) return GDA_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f)) return GDA_ERR_SHAPE;
+  if (B == 0) return GDA_OK;
+  if (!qgkv || !slots || !q_out || !k_pool || !v_pool) return GDA_ERR_NULL;
+  if (rope_dim > 0 && (!cos_t || !sin_t)) return GDA_ERR_NULL;
+  if (!aligned(qgkv, 16) || row_stride % 8 != 0 || !aligned(q_out, 16) || !aligned(k_pool, 16) ||
+      !aligned(v_pool, 16) || (gate_out && !aligned(gate_out, 16)) || (w_q_norm && !aligned(w_q_norm, 16)) ||
+      (w_k_norm && !aligned(w_k_norm, 16)) || (cos_t && !aligned(cos_t, 16)) || (sin_t && !aligned(sin_t, 16)) ||
+      !aligned(slots, 4))
+    return GDA_ERR_ALIGN;
+  gda::PrepParams p;
+  p.qgkv = reinterpret_cast<const __nv_bfloat16*>(qgkv);
+  p.row_stride = row_stride;
+  p.w_q = reinterpret_cast<const __nv_bfloat16*>(w_q_norm);
+  p.w_k = reinterpret_cast<const __nv_bfloat16*>(w_k_norm);
+  p.eps = eps;
+  p.cos_t = reinterpret_cast<const __nv_bfloat16*>(cos_t);
+  p.sin_t = reinterpret_cast<const __nv_bfloat16*>(sin_t);
+  p.rope_dim = rope_dim;
+  p.slots = slots;
+  p.num_slots = num_slots;
+  p.q_out = reinterpret_cast<__nv_bfloat16*>(q_out);
+  p.gate_out = reinterpret_cast<__nv_bfloat16*>(gate_out);
+  p.k_pool = reinterpret_cast<__nv_bfloat16*>(k_pool);
+  p.v_pool = reinterpret_cast<__nv_bfloat16*>(v_pool);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  if (gda::launch_prep(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDA_ERR_CUDA;
+  return GDA_OK;
+}
+
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {
   int rc = check_sizes(max_B, Hq, Hkv, D, max_splits);
   if (rc != GDA_OK) return rc;

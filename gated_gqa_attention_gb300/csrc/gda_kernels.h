@@ -49,6 +49,27 @@ struct Stage2Params {
   int fuse_gate;
 };
 
+struct PrepParams {
+  const __nv_bfloat16* qgkv;   // [B, row_stride] rows [q | gate | k | v]
+  long long row_stride;        // elements between tokens
+  const __nv_bfloat16* w_q;    // [D] or nullptr (no Q norm)
+  const __nv_bfloat16* w_k;    // [D] or nullptr (no K norm)
+  float eps;
+  const __nv_bfloat16* cos_t;  // [B, rope_dim]
+  const __nv_bfloat16* sin_t;  // [B, rope_dim]
+  int rope_dim;                // 0 or a multiple of 16 up to D
+  const int* slots;            // [B]
+  long long num_slots;
+  __nv_bfloat16* q_out;        // [B, Hq, D]
+  __nv_bfloat16* gate_out;     // [B, Hq, D] or nullptr
+  __nv_bfloat16* k_pool;       // [num_slots, Hkv, D]
+  __nv_bfloat16* v_pool;
+  int B, Hq, Hkv;
+};
+
+// The step before attention (Q/K RMSNorm, partial RoPE, KV write).
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+
 // Stage 1: grid CTAs, persistent.  Returns the launch status.
 cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStream_t stream);
 // Stage 2: FP32 LSE merge + gate epilogue, launched as a programmatic dependent of stage 1.

@@ -193,6 +193,32 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
  * initialise before capture). */
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
 
+/* The step before attention for one decode token per sequence (cuDNN FE-OSS "Gated
+ * Attention Block (SM107)", Overview stages (2)+(3), Weights and tables): from the
+ * token's projection row [q (Hq*D) | gate (Hq*D) | k (Hkv*D) | v (Hkv*D)] (W_qkvg
+ * column blocks Q | GATE | K | V) it writes
+ *   q_out[b,h,:]         = rope(rmsnorm(q[b,h,:], w_q_norm))
+ *   k_pool[slots[b],h,:] = rope(rmsnorm(k[b,h,:], w_k_norm))
+ *   v_pool[slots[b],h,:] = v[b,h,:]
+ *   gate_out[b,h,:]      = gate[b,h,:]              (skipped when gate_out is NULL)
+ * rmsnorm(x, w) = x / sqrt(mean(x^2) + eps) * w (no norm when w is NULL); rope rotates
+ * the first rope_dim dims in the rotate-half convention with cos/sin [B, rope_dim]:
+ * out_i = y_i cos_i - y_{i+r/2} sin_i and out_{i+r/2} = y_{i+r/2} cos_{i+r/2} + y_i sin_{i+r/2}
+ * for i < r/2 (r = rope_dim); other dims pass through.  FP32 arithmetic, one RNE
+ * rounding to bf16.
+ *   qgkv      [B, row_stride] bf16, row_stride >= (2 Hq + 2 Hkv) D, a multiple of 8
+ *   w_q_norm, w_k_norm  [D] bf16 or NULL; cos_t, sin_t [B, rope_dim] bf16 (rope_dim = 0: none)
+ *   slots     [B] int32: each token's slot in the pools; a slot outside [0, num_slots)
+ *             is not written
+ *   q_out, gate_out [B, Hq, D] bf16; k_pool, v_pool [num_slots, Hkv, D] bf16 (written)
+ * D = 256 and rope_dim a multiple of 16 (else GDA_ERR_UNSUPPORTED). */
+int gda_qk_norm_rope_kv_write(const gda_bf16* qgkv, int64_t row_stride, const gda_bf16* w_q_norm,
+                              const gda_bf16* w_k_norm, float eps, const gda_bf16* cos_t,
+                              const gda_bf16* sin_t, int rope_dim, const int32_t* slots,
+                              int64_t num_slots, gda_bf16* q_out, gda_bf16* gate_out,
+                              gda_bf16* k_pool, gda_bf16* v_pool, int B, int Hq, int Hkv, int D,
+                              gda_stream_t stream);
+
 /* Standalone gate, the second half of the unfused path (FreeToken PR #781,
  * Correctness: the fused output equals Torch sigmoid followed by Torch multiply):
  *   out[i] = RNE_bf16( o[i] * RNE_bf16(sigmoid(gate[i])) ),  0 <= i < n.
