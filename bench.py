@@ -53,6 +53,13 @@ def parse_args(argv=None):
     p.add_argument("--graph", type=int, default=4,
                    help="calls per captured CUDA graph in the timed region (0: eager launches); the pages "
                         "time 4 calls per graph")
+    p.add_argument("--hq", type=int, default=0, help="override the workload's query heads (0: keep)")
+    p.add_argument("--hkv", type=int, default=0, help="override the workload's KV heads (0: keep)")
+    p.add_argument("--window", type=int, default=0, help="sliding window (0: full attention)")
+    p.add_argument("--sinks", type=float, default=None, help="give every query head this sink logit")
+    p.add_argument("--op", choices=["decode", "prep"], default="decode",
+                   help="decode: the gated decode attention call (default); prep: the step before it "
+                        "(Q/K RMSNorm + partial RoPE + KV write) on the workload's batch")
     p.add_argument("--kernel-only", action="store_true",
                    help="warm-up + K calls and exit (the command profiled under ncu); prints nothing")
     return p.parse_args(argv)
@@ -235,19 +242,34 @@ def run_ours(args):
     gda.load()
 
     w = workloads.workload(args.workload)
-    inp = workloads.make_workload(args.workload, seed=w.seed + 1000 * rank)
+    if args.hq or args.hkv:
+        # the workload's lengths and layout with another head geometry
+        hq, hkv = args.hq or w.hq, args.hkv or w.hkv
+        rl = (w.len_lo, w.len_hi, w.batch) if w.lengths is None else None
+        inp = workloads.make(w.lengths if w.lengths is not None else [], seed=w.seed + 1000 * rank, hq=hq, hkv=hkv,
+                             head_dim=w.head_dim, layout=w.layout, pool_slots=w.pool_slots, page=w.page,
+                             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl)
+        inp["workload"] = w
+    else:
+        inp = workloads.make_workload(args.workload, seed=w.seed + 1000 * rank)
     lengths = inp["lengths"]
     B, Hq, D = inp["q"].shape
     Hkv = inp["k_pool"].shape[1]
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     out = torch.empty_like(dev["q"])
-    nbytes = algorithmic_bytes(lengths, Hq, Hkv, D)
-    s1_bytes = stage1_bytes(lengths, Hq, Hkv, D)
+    # algorithmic bytes: every attended K/V row once, plus q, gate, out (for G > 8 the
+    # kernels stream each KV head's rows once per group of 8 query heads, which the
+    # achieved fraction then shows)
+    att = [min(L, args.window) if args.window > 0 else L for L in lengths]
+    nbytes = algorithmic_bytes(att, Hq, Hkv, D)
+    s1_bytes = stage1_bytes(att, Hq, Hkv, D)
     stream = torch.cuda.current_stream()
+    sinks = None if args.sinks is None else torch.full((Hq,), float(args.sinks), dtype=torch.float32, device="cuda")
 
     def call():
         gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
-                      out=out, workspace=ws, scale=inp["scale"], num_splits=args.splits, variant=args.variant)
+                      out=out, workspace=ws, scale=inp["scale"], num_splits=args.splits, variant=args.variant,
+                      window=args.window, sinks=sinks)
 
     ws = torch.empty(gda.workspace_bytes(B, Hq, Hkv, D, args.splits), dtype=torch.uint8, device="cuda")
     gda.workspace_init(ws)
@@ -365,7 +387,7 @@ def run_ours(args):
                        "variant": {0: "auto(mma)", 1: "mma", 2: "simt", 3: "tma-ring+mma"}[args.variant],
                        "bytes_per_call": nbytes,
                        "l2": "inputs larger than L2 (%.0f MB of K/V rows per call), no flush" % (nbytes / 1e6),
-                       "parallelism": "replicas x%d" % world,
+                       "parallelism": "replicas x%d" % world, "window": args.window, "sinks": args.sinks,
                        "launch": ("CUDA graph of %d calls, replayed" % args.graph) if args.graph > 0 else "eager"},
             "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
@@ -429,8 +451,73 @@ def run_reference(args):
     }
 
 
+def run_prep(args):
+    """Time gda_qk_norm_rope_kv_write on the workload's batch (one decode token per
+    sequence): rope_dim 64, both norms, graph replay of 4 calls.  Bytes: every row of
+    the projection output read once, and q, gate, the K and V rows written."""
+    import torch
+    import gated_gqa_attention_gb300 as gda
+    from gated_gqa_attention_gb300 import workloads
+
+    torch.cuda.set_device(0)
+    gda.load()
+    w = workloads.workload(args.workload)
+    B, Hq, Hkv, D = w.batch, w.hq, w.hkv, w.head_dim
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    qgkv = torch.randn(B, (2 * Hq + 2 * Hkv) * D, generator=gen).to(torch.bfloat16).cuda()
+    wq = torch.rand(D, generator=gen).add(0.5).to(torch.bfloat16).cuda()
+    wk = torch.rand(D, generator=gen).add(0.5).to(torch.bfloat16).cuda()
+    ang = torch.rand(B, 32, generator=gen) * 6.28
+    cos = torch.cat([ang.cos(), ang.cos()], 1).to(torch.bfloat16).cuda()
+    sin = torch.cat([ang.sin(), ang.sin()], 1).to(torch.bfloat16).cuda()
+    slots_n = max(4 * B, 1024)
+    slots = torch.randperm(slots_n, generator=gen)[:B].to(torch.int32).cuda()
+    kp = torch.zeros(slots_n, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    q_out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    g_out = torch.empty_like(q_out)
+    call = lambda: gda.qk_norm_rope_kv_write(qgkv, slots, kp, vp, Hq, w_q_norm=wq, w_k_norm=wk, cos=cos, sin=sin,
+                                             rope_dim=64, q_out=q_out, gate_out=g_out)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    R = 4
+    steps = R * max(1, (args.steps + R - 1) // R)
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph):
+            for _ in range(R):
+                call()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps // R):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    nbytes = 2 * B * (2 * Hq + 2 * Hkv) * D * 2
+    gbs = nbytes * steps / (ms / 1e3) / 1e9
+    peak, kind = measured_hbm_peak()
+    return {"metric": "qk-norm + rope + kv-write µs/call and achieved HBM GB/s (1 GPU)", "op": "prep",
+            "value": round(gbs, 2), "unit": "GB/s", "us_per_call": round(ms / steps * 1e3, 3), "steps": steps,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "rope_dim": 64,
+                       "bytes_per_call": nbytes, "launch": "CUDA graph of 4 calls, replayed"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind}}
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.op == "prep":
+        line = run_prep(args)
+        print(json.dumps(line), flush=True)
+        return
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
