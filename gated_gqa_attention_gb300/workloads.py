@@ -22,6 +22,11 @@ where it is 1).  Draw order, all from one ``torch.Generator`` seeded with the
 workload's seed: lengths (if random) -> slot layout -> peaky-row mask -> q ->
 gate -> K pool -> V pool.  Values are drawn in float32, scaled, then rounded to
 BF16 (round-to-nearest-even).  Every pool row is filled, referenced or not.
+
+FP8 KV cache (``kv="e4m3"``): the same float32 draws of the pools are divided by a
+per-tensor descale, saturated to the e4m3 range (+-448) and converted to
+torch.float8_e4m3fn; the descale is the one a 6-sigma calibration gives,
+6 * std * (largest row factor) / 448, rounded to float32.  q and gate stay BF16.
 """
 from __future__ import annotations
 
@@ -32,6 +37,7 @@ from typing import List, Optional, Sequence
 import torch
 
 HQ, HKV, HEAD_DIM = 16, 2, 256
+E4M3_MAX = 448.0
 DEFAULT_SCALE = 1.0 / 16.0
 
 
@@ -93,6 +99,24 @@ def _randn_bf16(gen: torch.Generator, rows: int, cols: int, std: float,
     return out
 
 
+def _randn_e4m3(gen: torch.Generator, rows: int, cols: int, std: float, descale: float,
+                row_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """[rows, cols] float8_e4m3fn codes of the same float32 draws as _randn_bf16,
+    divided by ``descale`` and saturated at +-448."""
+    out = torch.empty(rows, cols, dtype=torch.float8_e4m3fn)
+    chunk = max(1, (1 << 24) // max(cols, 1))
+    for r0 in range(0, rows, chunk):
+        r1 = min(rows, r0 + chunk)
+        x = torch.randn(r1 - r0, cols, generator=gen, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        if row_scale is not None:
+            x.mul_(row_scale[r0:r1, None])
+        x.div_(descale).clamp_(-E4M3_MAX, E4M3_MAX)
+        out[r0:r1] = x.to(torch.float8_e4m3fn)
+    return out
+
+
 def _layout(gen: torch.Generator, lengths: List[int], layout: str, pool_slots: Optional[int],
             page: int):
     nnz = int(sum(lengths))
@@ -126,13 +150,17 @@ def _layout(gen: torch.Generator, lengths: List[int], layout: str, pool_slots: O
 def make(lengths: Sequence[int], *, seed: int, hq: int = HQ, hkv: int = HKV,
          head_dim: int = HEAD_DIM, layout: str = "perm", pool_slots: Optional[int] = None,
          page: int = 1, gate_std: float = 2.0, qkv_std: float = 1.0, peaky_frac: float = 0.0,
-         peaky_scale: float = 3.0, scale: float = DEFAULT_SCALE, random_lengths=None) -> dict:
+         peaky_scale: float = 3.0, scale: float = DEFAULT_SCALE, random_lengths=None,
+         kv: str = "bf16") -> dict:
     """Build one decode batch on the CPU.
 
     Returns a dict of CPU tensors ``q, gate`` [B, Hq, D] bf16, ``k_pool, v_pool``
-    [slots, Hkv, D] bf16, ``kv_indptr`` [B+1] int32, ``kv_indices`` [nnz] int32,
-    plus ``scale``, ``lengths`` and ``num_slots``.  ``random_lengths=(lo, hi, B)``
-    draws the lengths uniformly from [lo, hi] first."""
+    [slots, Hkv, D] bf16 (float8_e4m3fn with ``kv="e4m3"``), ``kv_indptr`` [B+1]
+    int32, ``kv_indices`` [nnz] int32, plus ``scale``, ``lengths``, ``num_slots``
+    and the pools' ``k_descale`` / ``v_descale`` (1.0 for BF16 pools).
+    ``random_lengths=(lo, hi, B)`` draws the lengths uniformly from [lo, hi] first."""
+    if kv not in ("bf16", "e4m3"):
+        raise ValueError(kv)
     gen = torch.Generator().manual_seed(seed)
     if random_lengths is not None:
         lo, hi, bsz = random_lengths
@@ -150,24 +178,34 @@ def make(lengths: Sequence[int], *, seed: int, hq: int = HQ, hkv: int = HKV,
     k_scale = None
     if row_scale is not None:
         k_scale = row_scale.repeat_interleave(hkv)
-    k_pool = _randn_bf16(gen, slots * hkv, head_dim, qkv_std, k_scale).view(slots, hkv, head_dim)
-    v_pool = _randn_bf16(gen, slots * hkv, head_dim, qkv_std).view(slots, hkv, head_dim)
+    if kv == "e4m3":
+        peak = peaky_scale if peaky_frac > 0.0 else 1.0
+        k_descale = float(torch.tensor(6.0 * qkv_std * max(peak, 1.0) / E4M3_MAX, dtype=torch.float32))
+        v_descale = float(torch.tensor(6.0 * qkv_std / E4M3_MAX, dtype=torch.float32))
+        k_pool = _randn_e4m3(gen, slots * hkv, head_dim, qkv_std, k_descale, k_scale).view(slots, hkv, head_dim)
+        v_pool = _randn_e4m3(gen, slots * hkv, head_dim, qkv_std, v_descale).view(slots, hkv, head_dim)
+    else:
+        k_descale = v_descale = 1.0
+        k_pool = _randn_bf16(gen, slots * hkv, head_dim, qkv_std, k_scale).view(slots, hkv, head_dim)
+        v_pool = _randn_bf16(gen, slots * hkv, head_dim, qkv_std).view(slots, hkv, head_dim)
     indptr = torch.zeros(B + 1, dtype=torch.int32)
     if B:
         indptr[1:] = torch.tensor(lengths, dtype=torch.int64).cumsum(0).to(torch.int32)
     return dict(q=q, gate=g, k_pool=k_pool, v_pool=v_pool, kv_indptr=indptr, kv_indices=idx,
-                scale=float(scale), lengths=lengths, num_slots=slots)
+                scale=float(scale), lengths=lengths, num_slots=slots, k_descale=k_descale,
+                v_descale=v_descale, kv=kv)
 
 
-def make_workload(key, batch_limit: Optional[int] = None, seed: Optional[int] = None) -> dict:
+def make_workload(key, batch_limit: Optional[int] = None, seed: Optional[int] = None, kv: str = "bf16") -> dict:
     """Inputs of one of the five named workloads (``batch_limit`` keeps the
     first sequences only, for bounded CPU timing; the draw is unchanged;
-    ``seed`` replaces the workload's seed, e.g. for independent replicas)."""
+    ``seed`` replaces the workload's seed, e.g. for independent replicas;
+    ``kv="e4m3"`` gives the same workload over an FP8 KV cache)."""
     w = workload(key)
     rl = (w.len_lo, w.len_hi, w.batch) if w.lengths is None else None
     d = make(w.lengths if w.lengths is not None else [], seed=w.seed if seed is None else seed, hq=w.hq, hkv=w.hkv,
              head_dim=w.head_dim, layout=w.layout, pool_slots=w.pool_slots, page=w.page,
-             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl)
+             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl, kv=kv)
     d["workload"] = w
     d["num_splits"] = w.num_splits
     if batch_limit is not None and batch_limit < len(d["lengths"]):
@@ -187,8 +225,9 @@ def truncate_batch(d: dict, nb: int) -> dict:
     return e
 
 
-def metric_bytes(lengths: Sequence[int], hq: int = HQ, hkv: int = HKV, head_dim: int = HEAD_DIM) -> int:
+def metric_bytes(lengths: Sequence[int], hq: int = HQ, hkv: int = HKV, head_dim: int = HEAD_DIM,
+                 kv_bytes: int = 2) -> int:
     """Algorithmic HBM bytes of one call: every referenced K and V row once
-    (2 bytes per element), plus q, gate and out."""
+    (``kv_bytes`` per element: 2 for BF16, 1 for e4m3), plus q, gate and out."""
     n = int(sum(lengths))
-    return n * hkv * head_dim * 2 * 2 + 3 * len(lengths) * hq * head_dim * 2
+    return n * hkv * head_dim * kv_bytes * 2 + 3 * len(lengths) * hq * head_dim * 2

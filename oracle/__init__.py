@@ -66,12 +66,15 @@ def _load():
         lib.oracle_double_from_bf16.restype = ctypes.c_double
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        lib.oracle_double_from_e4m3.argtypes = [ctypes.c_uint8]
+        lib.oracle_double_from_e4m3.restype = ctypes.c_double
         lib.oracle_sigmoid_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_sigmoid_bf16.restype = ctypes.c_uint16
         lib.oracle_gate.argtypes = [u16p, u16p, u16p, ctypes.c_int64]
         lib.oracle_gate.restype = None
         lib.oracle_decode.argtypes = [
-            u16p, u16p, u16p, u16p, i32p, i32p, ctypes.c_int64,
+            u16p, u16p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+            i32p, i32p, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
             ctypes.c_int, f64p, i32p, ctypes.c_int64, f64p, u16p, u16p, f64p, ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
@@ -104,6 +107,21 @@ def _u16(a) -> np.ndarray:
     return t.numpy().view(np.uint16)
 
 
+def _kv(a):
+    """A K or V pool: (uint16 BF16 bits, False) or (uint8 e4m3 codes, True).
+    Accepts numpy uint16 / uint8 arrays or torch bfloat16 / float8_e4m3fn / uint8
+    tensors (CPU)."""
+    if isinstance(a, np.ndarray):
+        if a.dtype == np.uint8:
+            return np.ascontiguousarray(a), True
+        return _u16(a), False
+    import torch  # local: only when a tensor is passed
+    t = a.detach().cpu().contiguous()
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return t.view(torch.uint8).numpy(), True
+    return _u16(t), False
+
+
 def _i32(a) -> np.ndarray:
     if isinstance(a, np.ndarray):
         return np.ascontiguousarray(a, dtype=np.int32)
@@ -130,6 +148,17 @@ def bf16_from_double(x) -> np.ndarray:
     for i, v in enumerate(flat):
         out[i] = lib.oracle_bf16_from_double(float(v))
     return out.reshape(xs.shape)
+
+
+def double_from_e4m3(codes) -> np.ndarray:
+    """Values of e4m3 codes (uint8), one element at a time through the C oracle."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    flat = c.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.float64)
+    for i, v in enumerate(flat):
+        out[i] = lib.oracle_double_from_e4m3(int(v))
+    return out.reshape(c.shape)
 
 
 def sigmoid_bf16(g_bits) -> np.ndarray:
@@ -166,7 +195,8 @@ class DecodeResult:
 
 def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, scale: float,
            num_splits: int = 0, pairs=None, want=("o_f64", "o_bf16", "out", "lse"),
-           nthreads: int = 0, window: int = 0, sinks=None) -> DecodeResult:
+           nthreads: int = 0, window: int = 0, sinks=None, k_descale: float = 1.0,
+           v_descale: float = 1.0) -> DecodeResult:
     """Gated GQA decode attention in FP64.
 
     q, gate_t: [B, Hq, D] BF16 (uint16 bits or torch bf16); k_pool, v_pool:
@@ -176,10 +206,14 @@ def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, scale: float,
     outputs are left as zeros (NaN for o_f64 / lse).
     ``window > 0`` attends to the last ``window`` positions of each sequence only;
     ``sinks`` ([Hq] floats) adds a per-head sink logit to every softmax denominator.
+    FP8 pools (uint8 / float8_e4m3fn e4m3 codes) take the values
+    ``k_descale * e4m3(code)`` and ``v_descale * e4m3(code)``; with BF16 pools the
+    descales are not used.
     """
     lib = _load()
     qa, ga = _u16(q), (None if gate_t is None else _u16(gate_t))
-    ka, va = _u16(k_pool), _u16(v_pool)
+    (ka, kfp8), (va, vfp8) = _kv(k_pool), _kv(v_pool)
+    assert kfp8 == vfp8, "K and V pools must have the same element type"
     ip, ix = _i32(kv_indptr), _i32(kv_indices)
     B, Hq, D = qa.shape
     num_slots, Hkv, Dk = ka.shape
@@ -198,8 +232,8 @@ def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, scale: float,
         sk = np.ascontiguousarray(np.asarray(sinks, dtype=np.float64).reshape(-1))
         assert sk.shape == (Hq,)
     rc = lib.oracle_decode(
-        _ptr(qa, ctypes.c_uint16), _ptr(ga, ctypes.c_uint16), _ptr(ka, ctypes.c_uint16),
-        _ptr(va, ctypes.c_uint16), _ptr(ip, ctypes.c_int32), _ptr(ix, ctypes.c_int32),
+        _ptr(qa, ctypes.c_uint16), _ptr(ga, ctypes.c_uint16), ka.ctypes.data_as(ctypes.c_void_p),
+        va.ctypes.data_as(ctypes.c_void_p), int(kfp8), float(k_descale), float(v_descale), _ptr(ip, ctypes.c_int32), _ptr(ix, ctypes.c_int32),
         int(num_slots), int(B), int(Hq), int(Hkv), int(D), float(scale), int(num_splits),
         int(window), _ptr(sk, ctypes.c_double), _ptr(pr, ctypes.c_int32), int(n_pairs), _ptr(o_f64, ctypes.c_double),
         _ptr(o_bf, ctypes.c_uint16), _ptr(out, ctypes.c_uint16), _ptr(lse, ctypes.c_double),

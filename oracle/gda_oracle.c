@@ -40,6 +40,11 @@
  *                  lse = log(e^{sink_h} + sum_j e^{s_j})
  *   any G = Hq / Hkv (including non-powers of two), any scale.
  *
+ * FP8 KV cache (cuDNN FE-OSS "Gated Attention Block (SM107)", API, QuantSpec:
+ * static per-tensor scales with dtype torch.float8_e4m3fn): the K and V pools may
+ * hold e4m3 codes; the value of a code c is descale * e4m3(c), with one descale
+ * for K and one for V, and everything above runs on those values unchanged.
+ *
  * Readings where the pages are silent: the sigmoid is the correctly rounded
  * BF16 value of the real sigmoid (no page fixes a device's sigmoid), the KV
  * head of query head h is h / G, a zero-length sequence gives O = 0 and
@@ -96,6 +101,35 @@ uint16_t oracle_bf16_from_double(double x) {
     return (uint16_t)(sign | (uint16_t)(bits >> 16));
 }
 
+/* ---- e4m3 -> double ---------------------------------------------------------
+ * The e4m3 ("fn") 8-bit float that torch.float8_e4m3fn stores: 1 sign bit, 4
+ * exponent bits with bias 7, 3 fraction bits; exponent field 0 holds the
+ * subnormals m * 2^-9; exponent field 15 with fraction 7 is NaN; there are no
+ * infinities, so the largest finite value is 1.75 * 2^8 = 448. */
+double oracle_double_from_e4m3(uint8_t c) {
+    int e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);          /* 0.m * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10); /* 1.m * 2^(e-7) */
+    return (c & 0x80) ? -v : v;
+}
+
+/* A K or V pool: BF16 bit patterns, or e4m3 codes scaled by a per-tensor descale. */
+typedef struct {
+    const void* data;
+    int fp8;
+    double descale;
+} kv_pool;
+
+static double kv_value(const kv_pool* p, int64_t off) {
+    if (p->fp8) return p->descale * oracle_double_from_e4m3(((const uint8_t*)p->data)[off]);
+    return oracle_double_from_bf16(((const uint16_t*)p->data)[off]);
+}
+
 /* ---- the output gate ------------------------------------------------------ */
 
 /* RNE_bf16(sigmoid(g)) for a BF16 gate value g, sigmoid taken in double. */
@@ -120,17 +154,17 @@ void oracle_gate(const uint16_t* o, const uint16_t* gate, uint16_t* out, int64_t
 /* Softmax-weighted sum over the positions [p0, p1) of sequence b for query
  * head h.  Writes the normalised O (length D) and returns lse = m + ln(sum)
  * over those positions; an empty range gives O = 0 and lse = -inf. */
-static double attend_range(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+static double attend_range(const uint16_t* q, const kv_pool* kp, const kv_pool* vp,
                            const int32_t* idx, int64_t p0, int64_t p1,
                            int Hkv, int kvh, int D, double scale, double* s_buf, double* O) {
     for (int d = 0; d < D; ++d) O[d] = 0.0;
     if (p1 <= p0) return -INFINITY;
     double m = -INFINITY;
     for (int64_t j = p0; j < p1; ++j) {
-        const uint16_t* krow = k_pool + ((int64_t)idx[j] * Hkv + kvh) * D;
+        int64_t krow = ((int64_t)idx[j] * Hkv + kvh) * D;
         double acc = 0.0;
         for (int d = 0; d < D; ++d)
-            acc += oracle_double_from_bf16(q[d]) * oracle_double_from_bf16(krow[d]);
+            acc += oracle_double_from_bf16(q[d]) * kv_value(kp, krow + d);
         double s = scale * acc;
         s_buf[j - p0] = s;
         if (s > m) m = s;
@@ -139,8 +173,8 @@ static double attend_range(const uint16_t* q, const uint16_t* k_pool, const uint
     for (int64_t j = p0; j < p1; ++j) {
         double p = exp(s_buf[j - p0] - m);
         z += p;
-        const uint16_t* vrow = v_pool + ((int64_t)idx[j] * Hkv + kvh) * D;
-        for (int d = 0; d < D; ++d) O[d] += p * oracle_double_from_bf16(vrow[d]);
+        int64_t vrow = ((int64_t)idx[j] * Hkv + kvh) * D;
+        for (int d = 0; d < D; ++d) O[d] += p * kv_value(vp, vrow + d);
     }
     for (int d = 0; d < D; ++d) O[d] /= z;
     return m + log(z);
@@ -171,9 +205,12 @@ static int check_inputs(const int32_t* indptr, const int32_t* indices, int64_t n
  * split s covers positions [s*c, min(L, (s+1)*c)) with c = ceil(L / S); each
  * split gives a normalised partial O_s and lse_s; the merge weights them by
  * exp(lse_s - max lse) (empty splits weigh 0).  Mathematically it is the same O.
+ * kv_fp8 != 0: k_pool and v_pool hold e4m3 codes (one byte per element) whose
+ * values are k_descale * e4m3(c) and v_descale * e4m3(c); otherwise they hold
+ * BF16 bit patterns and the descales are not used.
  */
 int oracle_decode(const uint16_t* q, const uint16_t* gate,
-                  const uint16_t* k_pool, const uint16_t* v_pool,
+                  const void* k_pool, const void* v_pool, int kv_fp8, double k_descale, double v_descale,
                   const int32_t* kv_indptr, const int32_t* kv_indices, int64_t num_slots,
                   int B, int Hq, int Hkv, int D, double scale, int num_splits,
                   int window, const double* sinks,
@@ -195,6 +232,8 @@ int oracle_decode(const uint16_t* q, const uint16_t* gate,
         if (b < 0 || b >= B || h < 0 || h >= Hq) return ORACLE_ERR_SHAPE;
     }
     int err = ORACLE_OK;
+    const kv_pool kp = {k_pool, kv_fp8 != 0, k_descale};
+    const kv_pool vp = {v_pool, kv_fp8 != 0, v_descale};
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #else
@@ -223,14 +262,14 @@ int oracle_decode(const uint16_t* q, const uint16_t* gate,
                 L -= first;
                 double l_out;
                 if (num_splits == 0) {
-                    l_out = attend_range(qrow, k_pool, v_pool, idx, 0, L, Hkv, kvh, D, scale, s_buf, O);
+                    l_out = attend_range(qrow, &kp, &vp, idx, 0, L, Hkv, kvh, D, scale, s_buf, O);
                 } else {
                     /* split-merge: every split's (O_s, lse_s), then the LSE merge */
                     int64_t c = (L + num_splits - 1) / num_splits;
                     double M = -INFINITY;
                     for (int s = 0; s < num_splits; ++s) {
                         int64_t p0 = (int64_t)s * c, p1 = p0 + c < L ? p0 + c : L;
-                        lse_s[s] = attend_range(qrow, k_pool, v_pool, idx, p0, p1, Hkv, kvh, D, scale,
+                        lse_s[s] = attend_range(qrow, &kp, &vp, idx, p0, p1, Hkv, kvh, D, scale,
                                                 s_buf, Os + (int64_t)s * D);
                         if (lse_s[s] > M) M = lse_s[s];
                     }
