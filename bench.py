@@ -36,7 +36,10 @@ if ROOT not in sys.path:
 
 METRIC = "gated decode attention µs/call and achieved HBM GB/s vs GB300 peak (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["gda_stage1.cu", "gda_stage1_tma.cu", "gda_device.cuh", "gda_kernels.h"]
+KERNEL_SOURCES = {
+    "bf16": ["gda_stage1.cu", "gda_stage1_tma.cu", "gda_device.cuh", "gda_kernels.h"],
+    "e4m3": ["gda_stage1_fp8.cu", "gda_device.cuh", "gda_kernels.h"],
+}
 
 
 def parse_args(argv=None):
@@ -57,6 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--hkv", type=int, default=0, help="override the workload's KV heads (0: keep)")
     p.add_argument("--window", type=int, default=0, help="sliding window (0: full attention)")
     p.add_argument("--sinks", type=float, default=None, help="give every query head this sink logit")
+    p.add_argument("--kv", choices=["bf16", "e4m3"], default="bf16",
+                   help="KV-cache element type: bf16, or e4m3 codes with per-tensor descales (FP8 cache)")
     p.add_argument("--op", choices=["decode", "prep"], default="decode",
                    help="decode: the gated decode attention call (default); prep: the step before it "
                         "(Q/K RMSNorm + partial RoPE + KV write) on the workload's batch")
@@ -176,25 +181,27 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(kv: str = "bf16") -> str:
     h = hashlib.sha256()
-    for n in KERNEL_SOURCES:
+    for n in KERNEL_SOURCES[kv]:
         with open(os.path.join(ROOT, "gated_gqa_attention_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, units: int):
+def recorded_traffic(workload: str, units: int, kv: str = "bf16"):
     """DRAM bytes per stage-1 launch from a committed ncu summary, if it was taken
     on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "stage1_%s_traffic.txt" % workload)
+    name = "stage1_%s_traffic.txt" % workload if kv == "bf16" else "stage1_%s_%s_traffic.txt" % (kv, workload)
+    path = os.path.join(ROOT, "profiles", name)
+    kv_type = kv
     try:
         kv = {}
         for line in open(path):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_hash") != kernel_hash():
+        if kv.get("kernel_hash") != kernel_hash(kv_type):
             return None
         per_unit = float(kv["dram_bytes_per_token"])
         return per_unit * units
@@ -202,25 +209,25 @@ def recorded_traffic(workload: str, units: int):
         return None
 
 
-def algorithmic_bytes(lengths, hq, hkv, d):
+def algorithmic_bytes(lengths, hq, hkv, d, kv_bytes=2):
     from gated_gqa_attention_gb300 import workloads
-    return workloads.metric_bytes(lengths, hq, hkv, d)
+    return workloads.metric_bytes(lengths, hq, hkv, d, kv_bytes)
 
 
-def stage1_bytes(lengths, hq, hkv, d):
+def stage1_bytes(lengths, hq, hkv, d, kv_bytes=2):
     n = sum(lengths)
-    return n * hkv * d * 2 * 2 + len(lengths) * hq * d * 2
+    return n * hkv * d * kv_bytes * 2 + len(lengths) * hq * d * 2
 
 
 def oracle_sample_rate(inp, budget_s: float):
     """Time the FP64 oracle on the host: full batches until the budget is spent."""
     import oracle
     w = inp["workload"]
-    nbytes = algorithmic_bytes(inp["lengths"], w.hq, w.hkv, w.head_dim)
+    nbytes = algorithmic_bytes(inp["lengths"], w.hq, w.hkv, w.head_dim, inp["k_pool"].element_size())
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
-                      inp["scale"], want=("out",))
+                      inp["scale"], want=("out",), k_descale=inp["k_descale"], v_descale=inp["v_descale"])
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s or reps >= 100:
@@ -248,10 +255,11 @@ def run_ours(args):
         rl = (w.len_lo, w.len_hi, w.batch) if w.lengths is None else None
         inp = workloads.make(w.lengths if w.lengths is not None else [], seed=w.seed + 1000 * rank, hq=hq, hkv=hkv,
                              head_dim=w.head_dim, layout=w.layout, pool_slots=w.pool_slots, page=w.page,
-                             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl)
+                             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl,
+                             kv=args.kv)
         inp["workload"] = w
     else:
-        inp = workloads.make_workload(args.workload, seed=w.seed + 1000 * rank)
+        inp = workloads.make_workload(args.workload, seed=w.seed + 1000 * rank, kv=args.kv)
     lengths = inp["lengths"]
     B, Hq, D = inp["q"].shape
     Hkv = inp["k_pool"].shape[1]
@@ -261,15 +269,17 @@ def run_ours(args):
     # kernels stream each KV head's rows once per group of 8 query heads, which the
     # achieved fraction then shows)
     att = [min(L, args.window) if args.window > 0 else L for L in lengths]
-    nbytes = algorithmic_bytes(att, Hq, Hkv, D)
-    s1_bytes = stage1_bytes(att, Hq, Hkv, D)
+    kvb = inp["k_pool"].element_size()
+    nbytes = algorithmic_bytes(att, Hq, Hkv, D, kvb)
+    s1_bytes = stage1_bytes(att, Hq, Hkv, D, kvb)
+    kd, vd = inp["k_descale"], inp["v_descale"]
     stream = torch.cuda.current_stream()
     sinks = None if args.sinks is None else torch.full((Hq,), float(args.sinks), dtype=torch.float32, device="cuda")
 
     def call():
         gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
                       out=out, workspace=ws, scale=inp["scale"], num_splits=args.splits, variant=args.variant,
-                      window=args.window, sinks=sinks)
+                      window=args.window, sinks=sinks, k_descale=kd, v_descale=vd)
 
     ws = torch.empty(gda.workspace_bytes(B, Hq, Hkv, D, args.splits), dtype=torch.uint8, device="cuda")
     gda.workspace_init(ws)
@@ -354,7 +364,7 @@ def run_ours(args):
         for k, t in host.items():
             dev[k].copy_(t, non_blocking=True)
         gda.decode(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
-                   out=out, scale=inp["scale"], num_splits=args.splits)
+                   out=out, scale=inp["scale"], num_splits=args.splits, k_descale=kd, v_descale=vd)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()   # the host reads the step's result
 
@@ -375,21 +385,23 @@ def run_ours(args):
             v, reps, dt, cores = oracle_sample_rate(inp, args.cpu_seconds)
             cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": "%d full pass(es) of workload %s (B=%d) in %.1f s" % (reps, args.workload, B, dt)}
-        traffic = recorded_traffic(args.workload, sum(lengths) * Hkv)
+        traffic = recorded_traffic(args.workload, sum(att) * Hkv, args.kv)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(ms / steps, 6),
             "us_per_call": round(ms / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None,
+            "dtype": "bf16" if args.kv == "bf16" else "e4m3 KV (f16 MMA, f32 accumulate), bf16 q/gate/out",
+            "data": "synthetic",
             "config": {"workload": args.workload, "B": B, "lengths": "%d..%d (total %d)" % (min(lengths), max(lengths),
                                                                                           sum(lengths)),
-                       "Hq": Hq, "Hkv": Hkv, "D": D, "num_splits": args.splits or "auto",
+                       "Hq": Hq, "Hkv": Hkv, "D": D, "num_splits": args.splits or "auto", "kv": args.kv,
                        "variant": {0: "auto(mma)", 1: "mma", 2: "simt", 3: "tma-ring+mma"}[args.variant],
                        "bytes_per_call": nbytes,
                        "l2": "inputs larger than L2 (%.0f MB of K/V rows per call), no flush" % (nbytes / 1e6),
                        "parallelism": "replicas x%d" % world, "window": args.window, "sinks": args.sinks,
                        "launch": ("CUDA graph of %d calls, replayed" % args.graph) if args.graph > 0 else "eager"},
-            "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": round(achieved, 1), "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": "stage1" if args.kv == "bf16" else "stage1_fp8", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                          "traffic": traffic, "algorithmic_bytes": s1_bytes, "avg_us": round(s1_us, 3),
                          "launches_timed": n_t},
@@ -417,18 +429,20 @@ def run_reference(args):
     import oracle
     from gated_gqa_attention_gb300 import workloads
 
-    inp = workloads.make_workload(args.workload)
+    inp = workloads.make_workload(args.workload, kv=args.kv)
     w = inp["workload"]
     lengths = inp["lengths"]
     B, G = len(lengths), w.hq // w.hkv
+    kvb = inp["k_pool"].element_size()
     groups = [(b, kvh) for b in range(B) for kvh in range(w.hkv)]
 
     def step(i):
         b, kvh = groups[i % len(groups)]
         pairs = np.array([(b, kvh * G + g) for g in range(G)], dtype=np.int32)
         oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
-                      inp["scale"], pairs=pairs, want=("out",))
-        return lengths[b] * w.head_dim * 2 * 2 + G * 3 * w.head_dim * 2
+                      inp["scale"], pairs=pairs, want=("out",), k_descale=inp["k_descale"],
+                      v_descale=inp["v_descale"])
+        return lengths[b] * w.head_dim * kvb * 2 + G * 3 * w.head_dim * 2
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -444,7 +458,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "Hq": w.hq, "Hkv": w.hkv, "D": w.head_dim},
+        "config": {"workload": args.workload, "B": B, "Hq": w.hq, "Hkv": w.hkv, "D": w.head_dim, "kv": args.kv},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -13,6 +13,9 @@ attention output sigmoid gate into the existing Triton decode stage2"):
 
     O   = softmax(scale * q[b,h] K[rows_b, h // G]^T) V[rows_b, h // G]
     out = bf16( bf16(O) * bf16(sigmoid(gate[b,h])) )     (round-to-nearest-even)
+
+K/V pools of dtype torch.float8_e4m3fn (or uint8 e4m3 codes) select the FP8-cache
+kernels; their values are ``k_descale * e4m3(code)`` and ``v_descale * e4m3(code)``.
 """
 from __future__ import annotations
 
@@ -24,13 +27,14 @@ from typing import Optional
 __all__ = [
     "load", "decode", "decode_ex", "decode_noalloc", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
-    "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH",
+    "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH", "KV_BF16", "KV_E4M3",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libgda.so")
 
 VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_TMA = 0, 1, 2, 3
+KV_BF16, KV_E4M3 = 0, 1
 MAX_SPLITS = 256
 NOALLOC_SCRATCH_BYTES = 16 << 20
 DEVERR_INDEX, DEVERR_TIMEOUT = 0x1, 0x2
@@ -53,7 +57,8 @@ class _Args(ctypes.Structure):
         ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
         ("scale", ctypes.c_float), ("num_splits", ctypes.c_int), ("fuse_gate", ctypes.c_int),
         ("check_indices", ctypes.c_int), ("variant", ctypes.c_int), ("min_chunk", ctypes.c_int),
-        ("window", ctypes.c_int), ("sinks", ctypes.c_void_p),
+        ("window", ctypes.c_int), ("sinks", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
+        ("k_descale", ctypes.c_float), ("v_descale", ctypes.c_float),
     ]
 
 
@@ -77,6 +82,8 @@ def load(path: Optional[str] = None):
         lib.gda_decode.restype = i32
         lib.gda_decode_ex.argtypes = [ctypes.POINTER(_Args), vp, ctypes.c_size_t, vp]
         lib.gda_decode_ex.restype = i32
+        lib.gda_decode_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, vp]
+        lib.gda_decode_e4m3.restype = i32
         lib.gda_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
         lib.gda_decode_noalloc.restype = i32
         lib.gda_qk_norm_rope_kv_write.argtypes = [vp, i64, vp, vp, f32, vp, vp, i32, vp, i64, vp, vp, vp, vp,
@@ -156,7 +163,15 @@ def reserve(max_B: int, Hq: int = 16, Hkv: int = 2, D: int = 256, max_splits: in
     _check(load().gda_reserve(int(max_B), int(Hq), int(Hkv), int(D), int(max_splits)))
 
 
+def _kv_dtype(k_pool) -> int:
+    """KV_E4M3 for float8_e4m3fn / uint8 pools, else KV_BF16."""
+    import torch
+    return KV_E4M3 if isinstance(k_pool, torch.Tensor) and k_pool.dtype in (torch.float8_e4m3fn, torch.uint8) \
+        else KV_BF16
+
+
 def _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out):
+    """Checks tensor metadata; returns the pools' element type (KV_BF16 or KV_E4M3)."""
     import torch
     _check_tensor("q", q, torch.bfloat16, 3)
     dev = q.device
@@ -164,8 +179,10 @@ def _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out):
         _check_tensor("gate", gate_t, torch.bfloat16, 3, dev)
         if gate_t.shape != q.shape:
             raise ValueError("gate must have q's shape")
-    _check_tensor("k_pool", k_pool, torch.bfloat16, 3, dev)
-    _check_tensor("v_pool", v_pool, torch.bfloat16, 3, dev)
+    kv = _kv_dtype(k_pool)
+    kdt = k_pool.dtype if kv == KV_E4M3 else torch.bfloat16
+    _check_tensor("k_pool", k_pool, kdt, 3, dev)
+    _check_tensor("v_pool", v_pool, kdt, 3, dev)
     if v_pool.shape != k_pool.shape:
         raise ValueError("k_pool and v_pool must have the same shape")
     _check_tensor("kv_indptr", kv_indptr, torch.int32, 1, dev)
@@ -178,23 +195,30 @@ def _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out):
         _check_tensor("out", out, torch.bfloat16, 3, dev)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
+    return kv
 
 
 def decode(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, scale: Optional[float] = None,
-           num_splits: int = 0, stream=None):
+           num_splits: int = 0, stream=None, k_descale: float = 1.0, v_descale: float = 1.0):
     """Gated GQA decode attention through ``gda_decode`` (library-owned workspace).
 
-    q, gate_t: [B, Hq, D] bf16; k_pool, v_pool: [num_slots, Hkv, D] bf16;
+    q, gate_t: [B, Hq, D] bf16; k_pool, v_pool: [num_slots, Hkv, D] bf16, or
+    float8_e4m3fn / uint8 e4m3 codes (then ``gda_decode_e4m3`` with the descales);
     kv_indptr: [B+1] int32; kv_indices: [nnz] int32 (all CUDA, contiguous).
     ``num_splits <= 0`` lets the kernel plan the splits on the device."""
     import torch
-    _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out)
+    kv = _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out)
     B, Hq, D = q.shape
     Hkv = k_pool.shape[1]
     if out is None:
         out = torch.empty_like(q)
     if scale is None:
         scale = 1.0 / (D ** 0.5)
+    if kv == KV_E4M3:
+        _check(load().gda_decode_e4m3(_ptr(q), _ptr(gate_t), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
+                                      _ptr(kv_indices), _ptr(out), B, Hq, Hkv, D, float(scale), float(k_descale),
+                                      float(v_descale), int(num_splits), _stream(stream)))
+        return out
     _check(load().gda_decode(_ptr(q), _ptr(gate_t), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indptr),
                              _ptr(kv_indices), _ptr(out), B, Hq, Hkv, D, float(scale), int(num_splits),
                              _stream(stream)))
@@ -207,7 +231,8 @@ def decode_noalloc(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out, scale:
     allocate device memory.  ``out`` must be given (this call allocates nothing);
     the library's fixed scratch area (NOALLOC_SCRATCH_BYTES per device) replaces the
     workspace, so calls that may overlap on the GPU must not use it concurrently."""
-    _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out)
+    if _decode_checks(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out) != KV_BF16:
+        raise TypeError("decode_noalloc serves bf16 pools only")
     if out is None:
         raise ValueError("decode_noalloc needs a preallocated out tensor")
     B, Hq, D = q.shape
@@ -223,13 +248,14 @@ def decode_noalloc(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out, scale:
 def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, workspace=None,
               scale: Optional[float] = None, num_splits: int = 0, fuse_gate: bool = True, lse=None,
               check_indices: bool = False, variant: int = VARIANT_AUTO, min_chunk: int = 0,
-              window: int = 0, sinks=None, stream=None):
+              window: int = 0, sinks=None, stream=None, k_descale: float = 1.0, v_descale: float = 1.0):
     """``gda_decode_ex``: caller workspace (allocated here when None), optional LSE
     output, the unfused first half (``fuse_gate=False``), device index checks, the
-    stage-1 variant, a sliding window (last ``window`` positions) and per-head
-    attention sinks (``sinks``: [Hq] float32 CUDA tensor of logits)."""
+    stage-1 variant, a sliding window (last ``window`` positions), per-head
+    attention sinks (``sinks``: [Hq] float32 CUDA tensor of logits) and, for e4m3
+    pools, the per-tensor descales."""
     import torch
-    _decode_checks(q, gate_t if fuse_gate else None, k_pool, v_pool, kv_indptr, kv_indices, out)
+    kv = _decode_checks(q, gate_t if fuse_gate else None, k_pool, v_pool, kv_indptr, kv_indices, out)
     B, Hq, D = q.shape
     Hkv = k_pool.shape[1]
     if out is None:
@@ -251,7 +277,8 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
               out=_ptr(out), lse=_ptr(lse), num_slots=int(k_pool.shape[0]), B=B, Hq=Hq, Hkv=Hkv, D=D,
               scale=float(scale), num_splits=int(num_splits), fuse_gate=1 if fuse_gate else 0,
               check_indices=1 if check_indices else 0, variant=int(variant), min_chunk=int(min_chunk),
-              window=int(window), sinks=_ptr(sinks))
+              window=int(window), sinks=_ptr(sinks), kv_dtype=kv, k_descale=float(k_descale),
+              v_descale=float(v_descale))
     _check(load().gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

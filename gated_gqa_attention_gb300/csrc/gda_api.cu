@@ -7,6 +7,8 @@
 // "Gated Attention Block (SM107)", Forward: execute() allocates nothing and is
 // CUDA-graph friendly; FreeToken PR #781, Summary: initialise before capture,
 // validate before launch).
+#include <math.h>
+
 #include <mutex>
 #include <vector>
 
@@ -82,6 +84,11 @@ int validate_args(const gda_args* a) {
   if (a->check_indices && a->num_slots < 0) return GDA_ERR_SHAPE;
   if (a->variant < 0 || a->variant > GDA_VARIANT_TMA) return GDA_ERR_UNSUPPORTED;
   if (a->min_chunk < 0 || a->window < 0) return GDA_ERR_SHAPE;
+  if (a->kv_dtype != GDA_KV_BF16 && a->kv_dtype != GDA_KV_E4M3) return GDA_ERR_UNSUPPORTED;
+  if (a->kv_dtype == GDA_KV_E4M3) {
+    if (a->variant != GDA_VARIANT_AUTO && a->variant != GDA_VARIANT_MMA) return GDA_ERR_UNSUPPORTED;
+    if (!isfinite(a->k_descale) || !isfinite(a->v_descale)) return GDA_ERR_ARG;
+  }
   if (a->B == 0) return GDA_OK;
   if (!a->q || !a->k_pool || !a->v_pool || !a->kv_indptr || !a->kv_indices || !a->out) return GDA_ERR_NULL;
   if (a->fuse_gate && !a->gate) return GDA_ERR_NULL;
@@ -143,7 +150,11 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.G = a->Hq / a->Hkv;
   p1.npass = npass;
   p1.window = a->window;
-  p1.scale_log2 = a->scale * 1.44269504088896340736f;
+  const bool fp8 = a->kv_dtype == GDA_KV_E4M3;
+  // e4m3 pools: k_descale joins the score scale (one rounding, from double)
+  p1.scale_log2 = fp8 ? (float)((double)a->scale * (double)a->k_descale * 1.4426950408889634074)
+                      : a->scale * 1.44269504088896340736f;
+  p1.v_descale = fp8 ? a->v_descale : 1.0f;
   p1.num_splits = splits;
   p1.min_chunk = min_chunk;
   p1.check_indices = a->check_indices ? 1 : 0;
@@ -159,7 +170,9 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
       ++g_tused;
     }
   }
-  if (gda::launch_stage1(p1, variant, grid, stream) != cudaSuccess) return GDA_ERR_CUDA;
+  const cudaError_t le =
+      fp8 ? gda::launch_stage1_fp8(p1, grid, stream) : gda::launch_stage1(p1, variant, grid, stream);
+  if (le != cudaSuccess) return GDA_ERR_CUDA;
   if (t_end != nullptr && cudaEventRecord(t_end, stream) != cudaSuccess) return GDA_ERR_CUDA;
 
   gda::Stage2Params p2;
@@ -296,6 +309,38 @@ int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool, 
   a.min_chunk = 0;
   a.window = 0;
   a.sinks = nullptr;
+  int rc = validate_args(&a);
+  if (rc != GDA_OK) return rc;
+  if (B == 0) return GDA_OK;
+  void* ws = nullptr;
+  const size_t need = gda_workspace_bytes(B, Hq, Hkv, D, num_splits);
+  rc = ensure_workspace(need, reinterpret_cast<cudaStream_t>(stream), true, &ws);
+  if (rc != GDA_OK) return rc;
+  return enqueue(&a, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gda_decode_e4m3(const gda_bf16* q, const gda_bf16* gate, const uint8_t* k_pool, const uint8_t* v_pool,
+                    const int32_t* kv_indptr, const int32_t* kv_indices, gda_bf16* out, int B, int Hq, int Hkv,
+                    int D, float scale, float k_descale, float v_descale, int num_splits, gda_stream_t stream) {
+  gda_args a = {};
+  a.q = q;
+  a.gate = gate;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.out = out;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.scale = scale;
+  a.num_splits = num_splits;
+  a.fuse_gate = 1;
+  a.variant = GDA_VARIANT_AUTO;
+  a.kv_dtype = GDA_KV_E4M3;
+  a.k_descale = k_descale;
+  a.v_descale = v_descale;
   int rc = validate_args(&a);
   if (rc != GDA_OK) return rc;
   if (B == 0) return GDA_OK;
@@ -483,10 +528,11 @@ const char* gda_status_str(int status) {
     case GDA_ERR_CAPTURE: return "GDA_ERR_CAPTURE: workspace growth requested while the stream is capturing";
     case GDA_ERR_CUDA: return "GDA_ERR_CUDA: a CUDA call or kernel launch failed";
     case GDA_ERR_DEVICE: return "GDA_ERR_DEVICE: a kernel flagged an error in the workspace error word";
+    case GDA_ERR_ARG: return "GDA_ERR_ARG: a scalar argument is outside its domain (non-finite descale)";
     default: return "unknown gda status";
   }
 }
 
-int gda_version(void) { return 100; }
+int gda_version(void) { return 110; }
 
 }  // extern "C"

@@ -27,10 +27,11 @@ struct Stage1Params {
   int G;               // query heads per KV head (Hq / Hkv)
   int npass;           // ceil(G / 8): groups of 8 query heads per KV head ("virtual heads")
   int window;          // > 0: attend to the last `window` positions only
-  float scale_log2;    // scale * log2(e)
+  float scale_log2;    // scale * log2(e) (e4m3 pools: scale * k_descale * log2(e))
   int num_splits;      // > 0 explicit, else automatic
   int min_chunk;       // automatic mode
   int check_indices;
+  float v_descale;     // e4m3 pools: V = v_descale * e4m3(code)
 };
 
 struct Stage2Params {
@@ -72,6 +73,8 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
 
 // Stage 1: grid CTAs, persistent.  Returns the launch status.
 cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStream_t stream);
+// Stage 1 over e4m3 K/V pools (same partials, same schedule).
+cudaError_t launch_stage1_fp8(const Stage1Params& p, int grid, cudaStream_t stream);
 // Stage 2: FP32 LSE merge + gate epilogue, launched as a programmatic dependent of stage 1.
 cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream);
 // Standalone gate over n elements.

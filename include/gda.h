@@ -59,7 +59,8 @@ typedef enum gda_status {
     GDA_ERR_WORKSPACE = -6,     /* workspace NULL, misaligned or smaller than gda_workspace_bytes */
     GDA_ERR_CAPTURE = -7,       /* the internal workspace must grow while `stream` is capturing */
     GDA_ERR_CUDA = -8,          /* a CUDA runtime call or launch failed */
-    GDA_ERR_DEVICE = -9         /* gda_read_error: a kernel flagged an error (see the bits below) */
+    GDA_ERR_DEVICE = -9,        /* gda_read_error: a kernel flagged an error (see the bits below) */
+    GDA_ERR_ARG = -10           /* a scalar argument outside its domain (a non-finite descale) */
 } gda_status;
 
 #define GDA_MAX_SPLITS 256
@@ -76,11 +77,17 @@ typedef enum gda_status {
 #define GDA_VARIANT_TMA 3        /* K/V rows gathered into a shared-memory ring by 1-D bulk
                                     copies (TMA), then mma.sync tiles (comparison variant) */
 
+/* Element type of the K and V pools (gda_args.kv_dtype). */
+#define GDA_KV_BF16 0            /* bf16 values */
+#define GDA_KV_E4M3 1            /* e4m3 codes (torch.float8_e4m3fn bytes) with per-tensor descales:
+                                    K = k_descale * e4m3(code), V = v_descale * e4m3(code) */
+
 /*
  * Full argument set of gda_decode_ex.
  *   q, gate     [B, Hq, D] bf16            query and gate of the decode token
- *   k_pool      [num_slots, Hkv, D] bf16   K rows, one token per slot
- *   v_pool      [num_slots, Hkv, D] bf16   V rows
+ *   k_pool      [num_slots, Hkv, D] bf16   K rows, one token per slot (e4m3 bytes when
+ *                                          kv_dtype == GDA_KV_E4M3)
+ *   v_pool      [num_slots, Hkv, D] bf16   V rows (likewise)
  *   kv_indptr   [B + 1] int32              CSR row pointer, kv_indptr[0] == 0, non-decreasing
  *   kv_indices  [kv_indptr[B]] int32       slot of each position, in position order
  *   out         [B, Hq, D] bf16            result (may not alias an input)
@@ -106,14 +113,19 @@ typedef enum gda_status {
  *   sinks       [Hq] float sink logits or NULL: attention sinks, one logit per query head
  *               that joins the softmax denominator with a zero value row,
  *               O = sum_j e^{s_j} V_j / (e^{sink_h} + sum_j e^{s_j}); lse includes it.
+ *   kv_dtype    GDA_KV_BF16 or GDA_KV_E4M3 (an FP8 KV cache, cuDNN FE-OSS "Gated Attention
+ *               Block (SM107)", API, QuantSpec: static per-tensor scales, e4m3 codes).
+ *               E4M3 is served by GDA_VARIANT_AUTO / GDA_VARIANT_MMA only.
+ *   k_descale, v_descale  per-tensor factors of an e4m3 cache (finite; else GDA_ERR_ARG);
+ *               not used for bf16 pools.
  * (FreeToken PR #781, Automatic dispatch and Correctness: window, sinks, custom scale
  * and non-power-of-two GQA groups are the cases of the general path.)
  */
 typedef struct gda_args {
     const gda_bf16* q;
     const gda_bf16* gate;
-    const gda_bf16* k_pool;
-    const gda_bf16* v_pool;
+    const void* k_pool;
+    const void* v_pool;
     const int32_t* kv_indptr;
     const int32_t* kv_indices;
     gda_bf16* out;
@@ -128,6 +140,9 @@ typedef struct gda_args {
     int min_chunk;
     int window;
     const float* sinks;
+    int kv_dtype;
+    float k_descale;
+    float v_descale;
 } gda_args;
 
 /* Bytes of workspace gda_decode_ex needs for these sizes (FreeToken PR #781 Summary:
@@ -160,6 +175,17 @@ int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool,
  * (SM107)", Forward: execute() allocates nothing), so it can be graph-captured. */
 int gda_decode_ex(const gda_args* args, void* workspace, size_t workspace_bytes,
                   gda_stream_t stream);
+
+/* As gda_decode over an FP8 KV cache: k_pool and v_pool hold e4m3 codes
+ * ([num_slots, Hkv, D] bytes, 16-byte aligned) whose values are k_descale * e4m3(c)
+ * and v_descale * e4m3(c) (cuDNN FE-OSS "Gated Attention Block (SM107)", API,
+ * QuantSpec: static per-tensor scales; e4m3 as torch.float8_e4m3fn).  q and gate stay
+ * bf16, the output and its rounding are those of gda_decode.  Same library-owned
+ * workspace as gda_decode.  Non-finite descales: GDA_ERR_ARG. */
+int gda_decode_e4m3(const gda_bf16* q, const gda_bf16* gate, const uint8_t* k_pool,
+                    const uint8_t* v_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                    gda_bf16* out, int B, int Hq, int Hkv, int D, float scale, float k_descale,
+                    float v_descale, int num_splits, gda_stream_t stream);
 
 /* Size of the fixed device scratch area that gda_decode_noalloc uses (16 MiB). */
 #define GDA_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -13,6 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gda.h")
 
 OK, ERR_NULL, ERR_ALIGN, ERR_SHAPE, ERR_UNSUPPORTED, ERR_SPLITS, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5, -6
+ERR_ARG = -10
 
 
 @pytest.fixture(scope="module")
@@ -41,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         s = gda.status_str(code)
         assert s.startswith("GDA_"), s
     assert "unknown" in gda.status_str(-100)
@@ -126,6 +127,48 @@ def test_decode_ex_host_validation(lib):
     a7 = gda._Args.from_buffer_copy(args)
     a7.sinks = 6
     assert call(a7) == ERR_ALIGN
+    # e4m3 pools: the MMA kernel only, finite descales, a known element type
+    a8 = gda._Args.from_buffer_copy(args)
+    a8.kv_dtype = 2
+    assert call(a8) == ERR_UNSUPPORTED
+    a8.kv_dtype = gda.KV_E4M3
+    a8.variant = gda.VARIANT_SIMT
+    assert call(a8) == ERR_UNSUPPORTED
+    a8.variant = gda.VARIANT_TMA
+    assert call(a8) == ERR_UNSUPPORTED
+    a8.variant = gda.VARIANT_MMA
+    a8.k_descale, a8.v_descale = float("nan"), 1.0
+    assert call(a8) == ERR_ARG
+    a8.k_descale, a8.v_descale = 1.0, float("inf")
+    assert call(a8) == ERR_ARG
+    a8.v_descale = 1.0
+    a8.v_pool = 8
+    assert call(a8) == ERR_ALIGN
+    # the descales of a bf16 call are not used (left zero by the struct's initialiser)
+    a9 = gda._Args.from_buffer_copy(args)
+    a9.k_descale = float("nan")
+    a9.B = 0
+    assert call(a9) == OK
+
+
+def _decode_e4m3(lib, ptrs=None, B=1, Hq=16, Hkv=2, D=256, scale=0.0625, kd=1.0, vd=1.0, splits=0):
+    p = dict(q=16, gate=16, k=16, v=16, indptr=16, indices=16, out=16)
+    if ptrs:
+        p.update(ptrs)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return lib.gda_decode_e4m3(vp(p["q"]), vp(p["gate"]), vp(p["k"]), vp(p["v"]), vp(p["indptr"]),
+                               vp(p["indices"]), vp(p["out"]), B, Hq, Hkv, D, scale, kd, vd, splits, None)
+
+
+def test_decode_e4m3_host_validation(lib):
+    assert _decode_e4m3(lib, {"k": 0}) == ERR_NULL
+    assert _decode_e4m3(lib, {"v": 24}) == ERR_ALIGN
+    assert _decode_e4m3(lib, kd=float("nan")) == ERR_ARG
+    assert _decode_e4m3(lib, vd=float("-inf")) == ERR_ARG
+    assert _decode_e4m3(lib, D=128) == ERR_UNSUPPORTED
+    assert _decode_e4m3(lib, Hq=16, Hkv=3) == ERR_SHAPE
+    assert _decode_e4m3(lib, splits=257) == ERR_SPLITS
+    assert _decode_e4m3(lib, {"q": 0, "gate": 0, "k": 0, "v": 0, "indptr": 0, "indices": 0, "out": 0}, B=0) == OK
 
 
 def test_gate_and_misc_host_validation(lib):
