@@ -12,8 +12,8 @@
 // pipeline per iteration is unchanged while the arithmetic per byte doubles.
 //  * Persistent grid, one CTA of 8 warps per SM; warp w takes tiles w, w+8, ...
 //    of its CTA's piece.  K rows (256 bytes) are loaded with 16-byte streaming
-//    loads straight into registers one tile ahead and prefetched into L2 two
-//    tiles ahead; V rows go through a per-warp 3-stage cp.async ring two tiles
+//    loads straight into registers about one tile ahead and prefetched into L2
+//    two tiles ahead; V rows go through a per-warp 3-stage cp.async ring two tiles
 //    ahead (L2 evict-first hint).
 //  * e4m3 values are exact in FP16, so the codes are widened with
 //    cvt.rn.f16x2.e4m3x2 and the tiles run as m16n8k16 f16 MMAs with FP32
@@ -21,7 +21,9 @@
 //    (its largest magnitude lands in [2^14, 2^15)); that factor and k_descale
 //    are folded into the score scale, v_descale into the partial's normalisation.
 //  * QK: S^T[32 tok x 8 heads] = K Q^T, two m-tiles.  Lane (g, t) loads dims
-//    {64c + 16t .. +15} (c = 0..3) of tokens g, g+8, g+16, g+24; k-step
+//    {64c + 16t .. +15} (c = 0..3) of tokens g, g+8, g+16, g+24 (chunk c of the
+//    next tile is loaded once QK has used chunk c + 1 of this one, chunk 3 after
+//    the last MMA, so each load is about one tile ahead of its use); k-step
 //    kk = 4c + h uses dims 64c + 16t + 4h + {0,1} for k-slots (2t, 2t+1) and
 //    + {2,3} for (2t+8, 2t+9); the Q^T fragments use the same order.
 //  * PV: O^T[256 x 8] += V^T P^T, two k-steps of 16 tokens.  The V^T fragment
@@ -140,23 +142,49 @@ struct Fp8WarpState {
     }
   }
 
-  __device__ __forceinline__ void qk_softmax(const uint2 (*qf)[32], int nv, float sl2, int lane) {
+  // QK of the tile in kr, then the softmax update.  After the K registers of chunk
+  // c have had their last use, chunk c of the next tile (slots slot_next) is
+  // loaded into them one chunk later (measured: one chunk later than the earliest
+  // point is faster on randomly placed rows), so every K load is about one tile
+  // ahead of its use.
+  __device__ __forceinline__ void qk_softmax(const uint2 (*qf)[32], int nv, float sl2, int lane,
+                                             const unsigned char* kb, size_t stride, int slot_next, bool more) {
+    const int g = lane >> 2, t = lane & 3;
+    const unsigned char* rn[4];
+    bool okn[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int sn = __shfl_sync(0xffffffffu, slot_next, g + 8 * j);
+      okn[j] = more && sn >= 0;
+      rn[j] = kb + (size_t)max(sn, 0) * stride + 16 * t;
+    }
     float acc[4][4];  // [m-tile * 2 + (kk & 1)][4]
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      const int c = kk >> 2, h = kk & 3;
-      const uint2 b = qf[kk][lane];
+    for (int c = 0; c < 4; ++c) {
 #pragma unroll
-      for (int mtile = 0; mtile < 2; ++mtile) {
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(word(kr[8 * mtile + c], h), a0, a2);
-        e4m3x4_to_f16x2x2(word(kr[8 * mtile + 4 + c], h), a1, a3);
-        mma_f16_16816(acc[2 * mtile + (kk & 1)], a0, a1, a2, a3, b.x, b.y);
+      for (int h = 0; h < 4; ++h) {
+        const int kk = 4 * c + h;
+        const uint2 b = qf[kk][lane];
+#pragma unroll
+        for (int mtile = 0; mtile < 2; ++mtile) {
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(word(kr[8 * mtile + c], h), a0, a2);
+          e4m3x4_to_f16x2x2(word(kr[8 * mtile + 4 + c], h), a1, a3);
+          mma_f16_16816(acc[2 * mtile + (kk & 1)], a0, a1, a2, a3, b.x, b.y);
+        }
       }
+      if (more && c >= 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) kr[4 * j + c - 1] = okn[j] ? ld_stream16(rn[j] + 64 * (c - 1)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (more) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kr[4 * j + 3] = okn[j] ? ld_stream16(rn[j] + 64 * 3) : make_uint4(0u, 0u, 0u, 0u);
     }
     float s[8];
 #pragma unroll
@@ -384,8 +412,7 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_kernel(Stage1Params p)
       issue_v_tile8(&ring[(k + 2) % kNV8][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
       prefetch_k_tile8(kb, stride, s2);
       const int s3 = fetch(idx, k + 3, len, nmine);
-      st.qk_softmax(sm.qf, tile_n(k, len, nmine), sl2, lane);
-      if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
+      st.qk_softmax(sm.qf, tile_n(k, len, nmine), sl2, lane, kb, stride, s1, k + 1 < nmine);
       cp_async_wait_group<2>();
       __syncwarp();
       st.pv(&ring[stage][0][0], lane);

@@ -262,7 +262,7 @@ int main() {
   const size_t READ_BYTES = (size_t)512 << 20; // 512 MiB gathered per launch
   uint8_t* pool; CK(cudaMalloc(&pool, POOL_BYTES)); CK(cudaMemset(pool, 1, POOL_BYTES));
   unsigned *out, *err; CK(cudaMalloc(&out, 64)); CK(cudaMalloc(&err, 4)); CK(cudaMemset(err, 0, 4));
-  int* idx; CK(cudaMalloc(&idx, (READ_BYTES / 512) * 4));
+  int* idx; CK(cudaMalloc(&idx, (READ_BYTES / 256) * 4));   // room for the 256-byte rows
   std::mt19937 rng(1);
   auto make = [&](int RB) -> int {
     int nrows = (int)(READ_BYTES / RB), prow = (int)(POOL_BYTES / RB);
@@ -270,10 +270,30 @@ int main() {
     cudaMemcpy(idx, p.data(), (size_t)nrows * 4, cudaMemcpyHostToDevice);
     return nrows;
   };
+  // rows in runs of `page` consecutive rows (a paged pool), the pages in random order
+  auto make_paged = [&](int RB, int page) -> int {
+    int nrows = (int)(READ_BYTES / RB), npages = (int)(POOL_BYTES / RB) / page;
+    std::vector<int> pg(npages); for (int i = 0; i < npages; ++i) pg[i] = i; std::shuffle(pg.begin(), pg.end(), rng);
+    std::vector<int> p(nrows); for (int i = 0; i < nrows; ++i) p[i] = pg[i / page] * page + i % page;
+    cudaMemcpy(idx, p.data(), (size_t)nrows * 4, cudaMemcpyHostToDevice);
+    return nrows;
+  };
   // stream copy reference
   { float ms = timeit([&] { cudaMemcpyAsync(pool + POOL_BYTES / 2, pool, POOL_BYTES / 2, cudaMemcpyDeviceToDevice); }, 10);
     printf("memcpy D2D %.1f GB/s (read+write)\n", (double)POOL_BYTES / ms / 1e6); }
   int n;
+  n = make(256);
+  printf("-- 256-byte rows (one FP8 K or V row), random\n");
+  run_ldg<256, 8>(pool, idx, n, out, sms, 2, 512); run_ldg<256, 16>(pool, idx, n, out, sms, 2, 512);
+  run_ldg<256, 8>(pool, idx, n, out, sms, 4, 512);
+  run_cpa<256, 128, 3>(pool, idx, n, out, sms); run_cpa<256, 256, 3>(pool, idx, n, out, sms);
+  n = make_paged(256, 16);
+  printf("-- 256-byte rows in random 16-row pages\n");
+  run_ldg<256, 8>(pool, idx, n, out, sms, 2, 512); run_ldg<256, 16>(pool, idx, n, out, sms, 2, 512);
+  n = make_paged(512, 16);
+  printf("-- 512-byte rows in random 16-row pages\n");
+  run_ldg<512, 4>(pool, idx, n, out, sms, 2, 512);
+  printf("-- 512-byte rows, random\n");
   n = make(512);
   run_tma<512, 64, 3>(pool, idx, n, out, err, sms);  run_tma<512, 128, 3>(pool, idx, n, out, err, sms);
   run_tma<512, 64, 6>(pool, idx, n, out, err, sms);  run_tma<512, 128, 3>(pool, idx, n, out, err, sms);
