@@ -231,3 +231,75 @@ def metric_bytes(lengths: Sequence[int], hq: int = HQ, hkv: int = HKV, head_dim:
     (``kv_bytes`` per element: 2 for BF16, 1 for e4m3), plus q, gate and out."""
     n = int(sum(lengths))
     return n * hkv * head_dim * kv_bytes * 2 + 3 * len(lengths) * hq * head_dim * 2
+
+
+# ------------------------------------------------------------------ prefill / extend
+
+PREFILL_HQ, PREFILL_HKV = 32, 2
+
+
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    name: str
+    batch: int
+    sq: int                 # query tokens per sequence
+    skv: int                # key/value tokens per sequence (the queries are the last sq of them)
+    causal: bool
+    seed: int
+    hq: int = PREFILL_HQ
+    hkv: int = PREFILL_HKV
+    head_dim: int = HEAD_DIM
+    gate_std: float = 2.0
+
+
+# The geometry of cuDNN FE-OSS "Gated Attention Block (SM107)", Performance: B=1,
+# h_q=32, h_kv=2, d=256, causal and dense (no mask); the sequence lengths are
+# this module's choice (the page's tables did not survive extraction).
+PREFILL_WORKLOADS: List[PrefillWorkload] = [
+    PrefillWorkload("p1_s4096_causal", 1, 4096, 4096, True, 10),
+    PrefillWorkload("p1_s4096_dense", 1, 4096, 4096, False, 11),
+    PrefillWorkload("p1_s512_causal", 1, 512, 512, True, 12),
+    PrefillWorkload("p4_extend_q1024_kv8192", 4, 1024, 8192, True, 13),
+]
+PREFILL_BY_NAME = {w.name: w for w in PREFILL_WORKLOADS}
+
+
+def make_prefill(batch: int, sq: int, skv: int, *, seed: int, hq: int = PREFILL_HQ, hkv: int = PREFILL_HKV,
+                 head_dim: int = HEAD_DIM, gate_std: float = 2.0, qkv_std: float = 1.0,
+                 scale: Optional[float] = None, causal: bool = True, kv_lens=None) -> dict:
+    """Prefill / extend inputs on the CPU: q, gate [B, Sq, Hq, D] and k, v [B, Skv, Hkv, D]
+    BF16 drawn from N(0, std^2) (draw order q, gate, k, v from one generator seeded
+    with ``seed``), plus ``scale`` (1/sqrt(D) by default), ``causal`` and ``kv_lens``
+    ([B] int32 or None)."""
+    gen = torch.Generator().manual_seed(seed)
+    q = _randn_bf16(gen, batch * sq * hq, head_dim, qkv_std).view(batch, sq, hq, head_dim)
+    g = _randn_bf16(gen, batch * sq * hq, head_dim, gate_std).view(batch, sq, hq, head_dim)
+    k = _randn_bf16(gen, batch * skv * hkv, head_dim, qkv_std).view(batch, skv, hkv, head_dim)
+    v = _randn_bf16(gen, batch * skv * hkv, head_dim, qkv_std).view(batch, skv, hkv, head_dim)
+    kl = None if kv_lens is None else torch.tensor(list(kv_lens), dtype=torch.int32)
+    return dict(q=q, gate=g, k=k, v=v, scale=float(scale if scale is not None else 1.0 / math.sqrt(head_dim)),
+                causal=bool(causal), kv_lens=kl)
+
+
+def make_prefill_workload(key: str, seed: Optional[int] = None) -> dict:
+    w = PREFILL_BY_NAME[key]
+    d = make_prefill(w.batch, w.sq, w.skv, seed=w.seed if seed is None else seed, hq=w.hq, hkv=w.hkv,
+                     head_dim=w.head_dim, gate_std=w.gate_std, causal=w.causal)
+    d["workload"] = w
+    return d
+
+
+def prefill_flops(batch: int, sq: int, skv: int, hq: int, head_dim: int, causal: bool, kv_lens=None) -> int:
+    """Algorithmic FLOPs of one prefill call: 4 * D per visible (query, key) pair per
+    query head (QK^T and PV, multiply-add = 2)."""
+    total = 0
+    for b in range(batch):
+        L = skv if kv_lens is None else int(kv_lens[b])
+        if causal:
+            off = L - sq
+            # visible keys of query i: min(L, max(0, i + off + 1))
+            vis = sum(min(L, max(0, i + off + 1)) for i in range(sq))
+        else:
+            vis = sq * L
+        total += vis
+    return 4 * head_dim * hq * total

@@ -82,6 +82,10 @@ def _load():
             u16p, ctypes.c_int64, u16p, u16p, ctypes.c_double, u16p, u16p, ctypes.c_int, i32p,
             u16p, u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_qk_norm_rope_kv_write.restype = ctypes.c_int
+        lib.oracle_prefill.argtypes = [
+            u16p, u16p, u16p, u16p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_double, ctypes.c_int, i32p, ctypes.c_int64, f64p, u16p, u16p, f64p, ctypes.c_int]
+        lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -272,3 +276,38 @@ def qk_norm_rope_kv_write(qgkv, w_q, w_k, eps: float, cos_t, sin_t, rope_dim: in
     if rc != ORACLE_OK:
         raise ValueError("oracle_qk_norm_rope_kv_write rejected its inputs (status %d)" % rc)
     return qo, go, kp, vp
+
+
+def prefill(q, gate_t, k, v, scale: float, causal: bool = True, kv_lens=None, rows=None,
+            want=("o_f64", "o_bf16", "out", "lse"), nthreads: int = 0) -> DecodeResult:
+    """Gated SDPA for prefill / extend in FP64 (cuDNN FE-OSS "Gated Attention Block
+    (SM107)", Overview stages (4)-(5), fuse_gate).
+
+    q, gate_t: [B, Sq, Hq, D] BF16; k, v: [B, Skv, Hkv, D] BF16.  With ``causal`` key j
+    is visible to query i when j <= i + (L - Sq), L = kv_lens[b] (Skv when None);
+    keys j >= L are never visible.  ``rows``: optional int array [n, 3] of (b, i, h) to
+    evaluate; other rows of the outputs are left as zeros (NaN for o_f64 / lse).
+    Returns o_f64 / o_bf16 / out [B, Sq, Hq, D] and lse [B, Hq, Sq] (natural log)."""
+    lib = _load()
+    qa, ka, va = _u16(q), _u16(k), _u16(v)
+    ga = None if gate_t is None else _u16(gate_t)
+    B, Sq, Hq, D = qa.shape
+    Bk, Skv, Hkv, Dk = ka.shape
+    assert Bk == B and Dk == D and va.shape == ka.shape
+    kl = None if kv_lens is None else _i32(kv_lens)
+    rr, n_rows = None, 0
+    if rows is not None:
+        rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+        n_rows = rr.shape[0]
+    o_f64 = np.full((B, Sq, Hq, D), np.nan) if "o_f64" in want else None
+    o_bf = np.zeros((B, Sq, Hq, D), np.uint16) if "o_bf16" in want else None
+    out = np.zeros((B, Sq, Hq, D), np.uint16) if ("out" in want and ga is not None) else None
+    lse = np.full((B, Hq, Sq), np.nan) if "lse" in want else None
+    rc = lib.oracle_prefill(
+        _ptr(qa, ctypes.c_uint16), _ptr(ga, ctypes.c_uint16), _ptr(ka, ctypes.c_uint16), _ptr(va, ctypes.c_uint16),
+        _ptr(kl, ctypes.c_int32), int(B), int(Sq), int(Skv), int(Hq), int(Hkv), int(D), float(scale),
+        1 if causal else 0, _ptr(rr, ctypes.c_int32), int(n_rows), _ptr(o_f64, ctypes.c_double),
+        _ptr(o_bf, ctypes.c_uint16), _ptr(out, ctypes.c_uint16), _ptr(lse, ctypes.c_double), int(nthreads))
+    if rc != ORACLE_OK:
+        raise ValueError("oracle_prefill rejected its inputs (status %d)" % rc)
+    return DecodeResult(o_f64, o_bf, out, lse)

@@ -390,6 +390,108 @@ int oracle_qk_norm_rope_kv_write(const uint16_t* qgkv, int64_t row_stride, const
     return ORACLE_OK;
 }
 
+/* ---- prefill / extend: gated SDPA over per-sequence K and V -------------------
+ *
+ * cuDNN FE-OSS "Gated Attention Block (SM107)", Overview stage (4) SDPA
+ * O = softmax(Q K^T * scale + mask) V with GQA H_q / H_kv, and stage (5) with the
+ * Fusion knob fuse_gate: O *= sigmoid(GATE) in the SDPA epilogue, after the dead-row
+ * select; Forward: return_lse writes the softmax statistics [B, H_q, S] in fp32,
+ * seq_lens gives per-batch KV lengths (padding).  Layout: q, gate [B, Sq, Hq, D];
+ * k, v [B, Skv, Hkv, D] (BF16 bits).  For sequence b with L = kv_lens[b] (Skv when
+ * kv_lens is NULL) key j is visible to query i when j < L and, with the causal mask,
+ * j <= i + (L - Sq): the Sq queries are the last Sq positions of the L keys (a
+ * plain prefill has Sq == L).  A query with no visible key is a dead row: O = 0 and
+ * lse = -inf.  Then, per element, out = RNE(RNE(O) * RNE(sigmoid(gate))) as in the
+ * decode path.  Every sum runs over j in increasing order, in double.
+ *   rows / n_rows: optional (b, i, h) triples to evaluate (NULL: all), outputs indexed
+ *   like the inputs ([B, Sq, Hq, D]; lse [B, Hq, Sq]); any output may be NULL.
+ */
+int oracle_prefill(const uint16_t* q, const uint16_t* gate, const uint16_t* k, const uint16_t* v,
+                   const int32_t* kv_lens, int B, int Sq, int Skv, int Hq, int Hkv, int D, double scale,
+                   int causal, const int32_t* rows, int64_t n_rows, double* o_f64, uint16_t* o_bf16,
+                   uint16_t* out, double* lse, int nthreads) {
+    if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return ORACLE_ERR_SHAPE;
+    if (kv_lens)
+        for (int b = 0; b < B; ++b)
+            if (kv_lens[b] < 0 || kv_lens[b] > Skv) return ORACLE_ERR_SHAPE;
+    int64_t total = rows ? n_rows : (int64_t)B * Sq * Hq;
+    for (int64_t t = 0; rows && t < total; ++t)
+        if (rows[3 * t] < 0 || rows[3 * t] >= B || rows[3 * t + 1] < 0 || rows[3 * t + 1] >= Sq ||
+            rows[3 * t + 2] < 0 || rows[3 * t + 2] >= Hq)
+            return ORACLE_ERR_SHAPE;
+    int G = Hq / Hkv;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel
+    {
+        double* sc = (double*)malloc(sizeof(double) * (size_t)(Skv > 0 ? Skv : 1));
+        double* O = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!sc || !O) {
+#pragma omp atomic write
+            err = ORACLE_ERR_NOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = 0; t < total; ++t) {
+                int b, i, h;
+                if (rows) {
+                    b = rows[3 * t];
+                    i = rows[3 * t + 1];
+                    h = rows[3 * t + 2];
+                } else {
+                    b = (int)(t / ((int64_t)Sq * Hq));
+                    i = (int)((t / Hq) % Sq);
+                    h = (int)(t % Hq);
+                }
+                int L = kv_lens ? kv_lens[b] : Skv;
+                int64_t last = causal ? (int64_t)i + (L - Sq) : (int64_t)L - 1;  /* last visible key */
+                if (last > L - 1) last = L - 1;
+                const uint16_t* qi = q + (((int64_t)b * Sq + i) * Hq + h) * D;
+                int kvh = h / G;
+                for (int d = 0; d < D; ++d) O[d] = 0.0;
+                double l_out = -INFINITY;
+                if (last >= 0) {
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j <= last; ++j) {
+                        const uint16_t* kj = k + (((int64_t)b * Skv + j) * Hkv + kvh) * D;
+                        double acc = 0.0;
+                        for (int d = 0; d < D; ++d)
+                            acc += oracle_double_from_bf16(qi[d]) * oracle_double_from_bf16(kj[d]);
+                        sc[j] = scale * acc;
+                        if (sc[j] > m) m = sc[j];
+                    }
+                    double z = 0.0;
+                    for (int64_t j = 0; j <= last; ++j) {
+                        double p = exp(sc[j] - m);
+                        z += p;
+                        const uint16_t* vj = v + (((int64_t)b * Skv + j) * Hkv + kvh) * D;
+                        for (int d = 0; d < D; ++d) O[d] += p * oracle_double_from_bf16(vj[d]);
+                    }
+                    for (int d = 0; d < D; ++d) O[d] /= z;
+                    l_out = m + log(z);
+                }
+                int64_t base = (((int64_t)b * Sq + i) * Hq + h) * D;
+                for (int d = 0; d < D; ++d) {
+                    uint16_t ob = oracle_bf16_from_double(O[d]);
+                    if (o_f64) o_f64[base + d] = O[d];
+                    if (o_bf16) o_bf16[base + d] = ob;
+                    if (out && gate) {
+                        double sv = oracle_double_from_bf16(oracle_sigmoid_bf16(gate[base + d]));
+                        out[base + d] = oracle_bf16_from_double(oracle_double_from_bf16(ob) * sv);
+                    }
+                }
+                if (lse) lse[((int64_t)b * Hq + h) * Sq + i] = l_out;
+            }
+        }
+        free(sc);
+        free(O);
+    }
+    return err;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
