@@ -62,9 +62,10 @@ def parse_args(argv=None):
     p.add_argument("--sinks", type=float, default=None, help="give every query head this sink logit")
     p.add_argument("--kv", choices=["bf16", "e4m3"], default="bf16",
                    help="KV-cache element type: bf16, or e4m3 codes with per-tensor descales (FP8 cache)")
-    p.add_argument("--op", choices=["decode", "prep"], default="decode",
+    p.add_argument("--op", choices=["decode", "prep", "prefill"], default="decode",
                    help="decode: the gated decode attention call (default); prep: the step before it "
-                        "(Q/K RMSNorm + partial RoPE + KV write) on the workload's batch")
+                        "(Q/K RMSNorm + partial RoPE + KV write) on the workload's batch; prefill: the "
+                        "prefill / extend gated SDPA (--workload p1_s4096_causal by default)")
     p.add_argument("--kernel-only", action="store_true",
                    help="warm-up + K calls and exit (the command profiled under ncu); prints nothing")
     return p.parse_args(argv)
@@ -170,6 +171,16 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
+
+def measured_bf16_peak(sustained: bool = False):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return (1700.0 if sustained else 1900.0), "fallback"
+
 
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -526,10 +537,115 @@ def run_prep(args):
                          "frac": round(gbs / peak, 4), "peak_kind": kind}}
 
 
+def run_prefill(args):
+    """Time gda_prefill (tcgen05 gated SDPA) on a prefill workload: algorithmic FLOPs
+    (4 * D per visible (query, key) pair per query head) over the CUDA-event time of K
+    eager calls; beside it the unfused torch chain the cuDNN block page compares with
+    (torch SDPA, then torch sigmoid and multiply) on the same inputs, and the FP64
+    oracle on a sample of rows."""
+    import torch
+    import gated_gqa_attention_gb300 as gda
+    from gated_gqa_attention_gb300 import workloads
+
+    torch.cuda.set_device(0)
+    gda.load()
+    key = args.workload if args.workload in workloads.PREFILL_BY_NAME else "p1_s4096_causal"
+    inp = workloads.make_prefill_workload(key)
+    w = inp["workload"]
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    B, Sq, Hq, D = inp["q"].shape
+    Skv, Hkv = inp["k"].shape[1], inp["k"].shape[2]
+    out = torch.empty_like(dev["q"])
+    flops = workloads.prefill_flops(B, Sq, Skv, Hq, D, w.causal)
+    call = lambda: gda.prefill(dev["q"], dev["gate"], dev["k"], dev["v"], out=out, scale=inp["scale"],
+                               causal=w.causal)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 200))
+    stream = torch.cuda.current_stream()
+    try:
+        uuid = str(torch.cuda.get_device_properties(0).uuid)
+        gpu_sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        gpu_sel = "0"
+    sampler = ClockSampler(gpu_sel)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / steps
+    tflops = flops / (ms / 1e3) / 1e12
+    err = gda.prefill_read_error()
+    peak, kind = measured_bf16_peak()
+
+    # the unfused torch chain on the same inputs: SDPA ([B, H, S, D]), sigmoid, multiply
+    qt, kt, vt = (dev[n].transpose(1, 2) for n in ("q", "k", "v"))
+    gt = dev["gate"]
+    off = Skv - Sq
+
+    def torch_chain():
+        if w.causal and off > 0:
+            mask = torch.ones(Sq, Skv, dtype=torch.bool, device="cuda").tril(diagonal=off)
+            o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=inp["scale"],
+                                                                 enable_gqa=True)
+        else:
+            o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=w.causal, scale=inp["scale"],
+                                                                 enable_gqa=True)
+        return o.transpose(1, 2) * torch.sigmoid(gt)
+    torch_ms = None
+    try:
+        for _ in range(3):
+            torch_chain()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_t = max(1, min(steps, 50))
+        t0.record(stream)
+        for _ in range(n_t):
+            torch_chain()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        torch_ms = t0.elapsed_time(t1) / n_t
+    except RuntimeError as e:  # a backend that declines the shape
+        torch_ms = "unavailable: %s" % str(e).splitlines()[0][:120]
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        rng = np.random.default_rng(0)
+        n_rows, t0c, done = 0, time.perf_counter(), 0.0
+        while time.perf_counter() - t0c < min(args.cpu_seconds, 10.0):
+            rows = np.stack([rng.integers(0, B, 64), rng.integers(0, Sq, 64), rng.integers(0, Hq, 64)], 1)
+            oracle.prefill(inp["q"], inp["gate"], inp["k"], inp["v"], inp["scale"], causal=w.causal,
+                           rows=rows.astype(np.int32), want=("out",))
+            n_rows += 64
+            for bb, ii, _ in rows:
+                done += 4.0 * D * (min(Skv, ii + (Skv - Sq) + 1) if w.causal else Skv)
+        dt = time.perf_counter() - t0c
+        cpu = {"value": round(done / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": "%d random (b, i, h) query rows of workload %s in %.1f s" % (n_rows, key, dt)}
+    return {"metric": "prefill gated SDPA TFLOP/s (algorithmic) vs GB300 bf16 peak (1 GPU)", "op": "prefill",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4), "steps": steps,
+            "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16 (tcgen05, f32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": key, "B": B, "Sq": Sq, "Skv": Skv, "Hq": Hq, "Hkv": Hkv, "D": D,
+                       "causal": w.causal, "flops_per_call": flops, "launch": "eager"},
+            "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": round(tflops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "peak_kind": kind},
+            "torch_chain_ms": torch_ms,
+            "speedup_vs_torch_chain": (round(torch_ms / ms, 3) if isinstance(torch_ms, float) else None),
+            "cpu_baseline": cpu, "clocks": clocks, "device_error_word": err, "gpu_launches": steps}
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.op == "prep":
-        line = run_prep(args)
+    if args.op in ("prep", "prefill"):
+        line = run_prep(args) if args.op == "prep" else run_prefill(args)
         print(json.dumps(line), flush=True)
         return
     line = run_reference(args) if args.impl == "reference" else run_ours(args)

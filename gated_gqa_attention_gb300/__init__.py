@@ -25,7 +25,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "load", "decode", "decode_ex", "decode_noalloc", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
+    "load", "decode", "decode_ex", "decode_noalloc", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
     "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH", "KV_BF16", "KV_E4M3",
 ]
@@ -84,6 +84,10 @@ def load(path: Optional[str] = None):
         lib.gda_decode_ex.restype = i32
         lib.gda_decode_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, vp]
         lib.gda_decode_e4m3.restype = i32
+        lib.gda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp]
+        lib.gda_prefill.restype = i32
+        lib.gda_prefill_read_error.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_uint32)]
+        lib.gda_prefill_read_error.restype = i32
         lib.gda_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
         lib.gda_decode_noalloc.restype = i32
         lib.gda_qk_norm_rope_kv_write.argtypes = [vp, i64, vp, vp, f32, vp, vp, i32, vp, i64, vp, vp, vp, vp,
@@ -282,6 +286,57 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
     _check(load().gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def prefill(q, gate_t, k, v, *, kv_lens=None, out=None, lse=None, scale: Optional[float] = None,
+            causal: bool = True, error_word=None, stream=None):
+    """Prefill / extend gated SDPA through ``gda_prefill`` (tcgen05 kernel).
+
+    q, gate_t: [B, Sq, Hq, D] bf16 (gate_t None: out = bf16(O)); k, v: [B, Skv, Hkv, D]
+    bf16; kv_lens: [B] int32 or None; lse: [B, Hq, Sq] float32 or None; error_word:
+    a 1-element int32/uint32 CUDA tensor or None (the library's word)."""
+    import torch
+    _check_tensor("q", q, torch.bfloat16, 4)
+    dev = q.device
+    B, Sq, Hq, D = q.shape
+    if gate_t is not None:
+        _check_tensor("gate", gate_t, torch.bfloat16, 4, dev)
+        if gate_t.shape != q.shape:
+            raise ValueError("gate must have q's shape")
+    _check_tensor("k", k, torch.bfloat16, 4, dev)
+    _check_tensor("v", v, torch.bfloat16, 4, dev)
+    if v.shape != k.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Skv, Hkv, D] with q's B and D")
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if kv_lens is not None:
+        _check_tensor("kv_lens", kv_lens, torch.int32, 1, dev)
+        if kv_lens.numel() != B:
+            raise ValueError("kv_lens must have B entries")
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, 3, dev)
+        if tuple(lse.shape) != (B, Hq, Sq):
+            raise ValueError("lse must be [B, Hq, Sq]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_tensor("out", out, torch.bfloat16, 4, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    _check(load().gda_prefill(_ptr(q), _ptr(gate_t), _ptr(k), _ptr(v), _ptr(kv_lens), _ptr(out), _ptr(lse),
+                              B, Sq, Skv, Hq, Hkv, D, float(scale), 1 if causal else 0, _ptr(error_word),
+                              _stream(stream)))
+    return out
+
+
+def prefill_read_error(clear: bool = True, stream=None) -> int:
+    """The library's prefill error word on the current device (synchronises)."""
+    w = ctypes.c_uint32(0)
+    rc = load().gda_prefill_read_error(_stream(stream), 1 if clear else 0, ctypes.byref(w))
+    if rc not in (0, -9):
+        _check(rc)
+    return int(w.value)
 
 
 def qk_norm_rope_kv_write(qgkv, slots, k_pool, v_pool, Hq: int, w_q_norm=None, w_k_norm=None, eps: float = 1e-6,

@@ -256,6 +256,24 @@ int noalloc_scratch(cudaStream_t stream, void** out) {
   return GDA_OK;
 }
 
+// ---- the library's prefill error word (gda_prefill with error_word == NULL) ---------
+__device__ unsigned int g_prefill_error;
+unsigned int* g_prefill_error_ptr[kMaxDevices] = {};
+
+int prefill_error_word(cudaStream_t stream, unsigned int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_prefill_error_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_prefill_error) != cudaSuccess || ptr == nullptr) return GDA_ERR_CUDA;
+    if (cudaMemsetAsync(ptr, 0, sizeof(unsigned int), stream) != cudaSuccess) return GDA_ERR_CUDA;
+    g_prefill_error_ptr[dev] = static_cast<unsigned int*>(ptr);
+  }
+  *out = g_prefill_error_ptr[dev];
+  return GDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -424,6 +442,62 @@ int gda_qk_norm_rope_kv_write(const gda_bf16* qgkv, int64_t row_stride, const gd
   p.Hkv = Hkv;
   if (gda::launch_prep(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDA_ERR_CUDA;
   return GDA_OK;
+}
+
+int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, const gda_bf16* v,
+                const int32_t* kv_lens, gda_bf16* out, float* lse, int B, int Sq, int Skv, int Hq, int Hkv,
+                int D, float scale, int causal, uint32_t* error_word, gda_stream_t stream) {
+  if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return GDA_ERR_SHAPE;
+  if (D != gda::kD) return GDA_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return GDA_ERR_ARG;
+  if (B == 0 || Sq == 0) return GDA_OK;
+  if (!q || !out || (Skv > 0 && (!k || !v))) return GDA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(out, 16) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||
+      (gate && !aligned(gate, 16)) || (kv_lens && !aligned(kv_lens, 4)) || (lse && !aligned(lse, 4)) ||
+      (error_word && !aligned(error_word, 4)))
+    return GDA_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* err = error_word;
+  if (err == nullptr) {
+    int rc = prefill_error_word(s, &err);
+    if (rc != GDA_OK) return rc;
+  }
+  gda::PrefillParams p;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+  p.kv_lens = kv_lens;
+  p.error = err;
+  p.B = B;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.causal = causal ? 1 : 0;
+  p.fuse_gate = gate ? 1 : 0;
+  // with Skv == 0 the key maps still need a valid base: the queries' (never loaded)
+  const void* kb = Skv > 0 ? static_cast<const void*>(k) : static_cast<const void*>(q);
+  const void* vb = Skv > 0 ? static_cast<const void*>(v) : static_cast<const void*>(q);
+  if (gda::launch_prefill(p, q, kb, vb, gate, s) != cudaSuccess) return GDA_ERR_CUDA;
+  return GDA_OK;
+}
+
+int gda_prefill_read_error(gda_stream_t stream, int clear, uint32_t* error_word) {
+  if (error_word == nullptr) return GDA_ERR_NULL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* dev_word = nullptr;
+  int rc = prefill_error_word(s, &dev_word);
+  if (rc != GDA_OK) return rc;
+  unsigned int w = 0;
+  if (cudaMemcpyAsync(&w, dev_word, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDA_ERR_CUDA;
+  if (clear && w != 0) {
+    if (cudaMemsetAsync(dev_word, 0, sizeof(w), s) != cudaSuccess) return GDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDA_ERR_CUDA;
+  }
+  *error_word = w;
+  return w == 0 ? GDA_OK : GDA_ERR_DEVICE;
 }
 
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {

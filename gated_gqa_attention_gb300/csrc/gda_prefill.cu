@@ -1,0 +1,479 @@
+// gda_prefill.cu -- prefill / extend gated SDPA on sm_103a with tcgen05 MMAs, TMEM
+// accumulators and TMA loads.
+//
+// Computes, per sequence b, query i and query head h (cuDNN FE-OSS "Gated Attention
+// Block (SM107)", Overview stage (4) SDPA O = softmax(Q K^T * scale + mask) V with
+// GQA H_q / H_kv, and stage (5) fused into the SDPA epilogue, Fusion knobs,
+// fuse_gate: O *= sigmoid(GATE) after the dead-row select):
+//   keys visible to query i: j < L (L = kv_lens[b], or Skv) and, causal, j <= i + (L - Sq)
+//   O   = sum_j softmax_j(scale * q_i . k_j) v_j            (a dead row gives O = 0)
+//   out = RNE_bf16(RNE_bf16(O) * RNE_bf16(sigmoid(gate)))   (the decode path's gate)
+//   lse = natural-log log-sum-exp of the visible scaled scores ([B, Hq, Sq], optional)
+//
+// GB300 design (one CTA of 4 warps per (128-query block, query head, sequence)):
+//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings the Q tile [128 x 256] once
+//    and K / V tiles [64 x 256] into a double buffer, one tile ahead; the gate tile
+//    is staged by TMA into the freed K buffers for the epilogue.
+//  * tcgen05.mma (kind::f16, BF16 operands, FP32 accumulation, M = 128) issued by
+//    one thread: S = Q K^T (N = 64, sixteen k-steps of 16) into TMEM columns
+//    [0, 64), and O += P V (N = 256, four k-steps) into TMEM columns [256, 512).
+//    Completion is signalled by tcgen05.commit on an mbarrier.
+//  * Softmax: thread r owns query row r = TMEM lane r; it reads its 64 scores with
+//    tcgen05.ld, keeps a running max (moved lazily, by more than 2^8, as the decode
+//    kernels do; O in TMEM is rescaled then) and sum, and writes P (BF16) to shared
+//    memory in the swizzled K-major layout the next MMA reads.
+//  * Epilogue: O row from TMEM, divided by the sum, rounded to BF16, gated with the
+//    BF16 sigmoid of the staged gate row, stored.
+// Every wait is bounded; on a timeout the CTA records kErrTimeout, stops issuing
+// work, waits (bounded) for what it issued, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "gda_device.cuh"
+#include "gda_kernels.h"
+
+namespace gda {
+
+namespace {
+
+constexpr int kPM = 128;            // query rows per CTA (MMA M)
+constexpr int kPN = 64;             // keys per tile (MMA N of S)
+constexpr int kPThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;      // S accumulator columns [0, 64)
+constexpr uint32_t kTmemO = 256;    // O accumulator columns [256, 512)
+
+// shared memory plan (offsets from a 1024-byte aligned base)
+constexpr uint32_t kQBlk = kPM * 128;             // one 64-column block of Q: 16 KiB
+constexpr uint32_t kKVBlk = kPN * 128;            // one 64-column block of a K or V tile: 8 KiB
+constexpr uint32_t kOffQ = 0;                     // 4 blocks, 64 KiB
+constexpr uint32_t kOffK = kOffQ + 4 * kQBlk;     // 2 buffers x 4 blocks, 64 KiB
+constexpr uint32_t kOffV = kOffK + 8 * kKVBlk;    // 2 buffers x 4 blocks, 64 KiB
+constexpr uint32_t kOffP = kOffV + 8 * kKVBlk;    // 128 rows x 128 B, 16 KiB
+constexpr uint32_t kOffBar = kOffP + kPM * 128;   // mbarriers and the TMEM address
+constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;  // + alignment slack
+
+// ---- PTX wrappers (tcgen05, TMA) ----
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// all prior tcgen05 MMAs of this thread arrive on `bar` when complete
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 columns of 32 bits: thread t of the warp gets lane (warp base + t), columns col .. col+31
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  uint32_t r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// TMA: a 4-D tile (x innermost) into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (descriptor version 1):
+// start address, leading and stride byte offsets, all encoded >> 4.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+struct PrefillBars {
+  uint64_t q, k[2], v[2], s, o, g;
+  uint32_t tmem;
+  int abort;
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, PrefillParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PrefillBars& bars = *reinterpret_cast<PrefillBars*>(sm + kOffBar);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nqb = (p.Sq + kPM - 1) / kPM;
+  const int qb = nqb - 1 - (int)blockIdx.x;  // the longest causal blocks first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kvh = h / (p.Hq / p.Hkv);
+  const int L = p.kv_lens ? __ldg(p.kv_lens + b) : p.Skv;
+  const int i0 = qb * kPM;
+  const int off = L - p.Sq;  // causal: key j visible to query i when j <= i + off
+  int last_key = L - 1;
+  if (p.causal) last_key = min(last_key, i0 + kPM - 1 + off);
+  const int ntiles = (last_key >= 0) ? (last_key / kPN + 1) : 0;
+
+  if (tid == 0) {
+    mbar_init(&bars.q, 1);
+    mbar_init(&bars.k[0], 1);
+    mbar_init(&bars.k[1], 1);
+    mbar_init(&bars.v[0], 1);
+    mbar_init(&bars.v[1], 1);
+    mbar_init(&bars.s, 1);
+    mbar_init(&bars.o, 1);
+    mbar_init(&bars.g, 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars.tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem;
+  volatile int* abort_flag = &bars.abort;
+  bool ok = true;
+  auto fail = [&]() {
+    if (ok) {
+      ok = false;
+      bars.abort = 1;
+      atomicOr(p.error, kErrTimeout);
+    }
+  };
+
+  const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV),
+                 sP = smem_u32(sm + kOffP);
+  const uint32_t idS = idesc_bf16(kPM, kPN, 0), idO = idesc_bf16(kPM, 256, 1);
+  // thread 0's record of what it started: MMA groups committed and TMA loads armed
+  // per barrier (the n-th arm of a barrier completes its phase n - 1)
+  int issued_s = 0, issued_o = 0, arm_q = 0, arm_g = 0, arm_k[2] = {0, 0}, arm_v[2] = {0, 0};
+
+  auto load_kv = [&](int j) {  // thread 0: K and V tile j into buffer j & 1
+    const int bf = j & 1;
+    ++arm_k[bf];
+    ++arm_v[bf];
+    mbar_arrive_expect_tx(&bars.k[bf], 4 * kKVBlk);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      tma_load_4d(sm + kOffK + (bf * 4 + c) * kKVBlk, &tk, 64 * c, kvh, j * kPN, b, &bars.k[bf]);
+    mbar_arrive_expect_tx(&bars.v[bf], 4 * kKVBlk);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      tma_load_4d(sm + kOffV + (bf * 4 + c) * kKVBlk, &tv, 64 * c, kvh, j * kPN, b, &bars.v[bf]);
+  };
+
+  if (tid == 0 && ntiles > 0) {
+    ++arm_q;
+    mbar_arrive_expect_tx(&bars.q, 4 * kQBlk);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffQ + c * kQBlk, &tq, 64 * c, h, i0, b, &bars.q);
+    load_kv(0);
+  }
+
+  const int r = tid;  // query row of this thread = TMEM lane
+  const int qi = i0 + r;
+  const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+  float m_run = -INFINITY, l_run = 0.0f;
+
+  for (int j = 0; j < ntiles; ++j) {
+    const int bf = j & 1;
+    // ---- S = Q K^T (thread 0)
+    if (tid == 0 && ok) {
+      if (j == 0 && !mbar_wait(&bars.q, 0, abort_flag)) fail();
+      if (ok && !mbar_wait(&bars.k[bf], (j >> 1) & 1, abort_flag)) fail();
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + (bf * 4 + (kk >> 2)) * kKVBlk + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tmem + kTmemS, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars.s);
+        ++issued_s;
+      }
+    }
+    if (ok && !mbar_wait(&bars.s, j & 1, abort_flag)) fail();
+    // PV of the previous tile must be done before P and O are touched again
+    if (ok && j > 0 && !mbar_wait(&bars.o, (j - 1) & 1, abort_flag)) fail();
+    // one CTA-wide decision, so the warp-collective TMEM accesses below stay convergent
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // the other buffer (tile j - 1) is free: load tile j + 1 into it
+    if (tid == 0 && j + 1 < ntiles) load_kv(j + 1);
+
+    // ---- softmax of row r over keys [64 j, 64 j + 64)
+    float s[64];
+    tmem_ld32(t_row + kTmemS, s);
+    tmem_ld32(t_row + kTmemS + 32, s + 32);
+    tmem_wait_ld();
+    const int k0 = j * kPN;
+    const bool need_mask = (k0 + kPN > L) || (p.causal && k0 + kPN - 1 > i0 + off);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      float x = s[c] * p.scale_log2;
+      if (need_mask) {
+        const int kj = k0 + c;
+        if (kj >= L || (p.causal && kj > qi + off)) x = -INFINITY;
+      }
+      s[c] = x;
+      mx = fmaxf(mx, x);
+    }
+    // lazy max: it moves only by more than 2^8, so probabilities stay below 2^8
+    float alpha = 1.0f;
+    if (mx > m_run + 8.0f) {
+      alpha = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mx);
+      l_run *= alpha;
+      m_run = mx;
+    }
+    // rescale O rows in TMEM (PV of the previous tile has completed); the TMEM
+    // accesses are warp-collective, so a warp rescales when any of its rows must
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        float o[32];
+        tmem_ld32(t_row + kTmemO + c0, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        tmem_st32(t_row + kTmemO + c0, o);
+      }
+      tmem_wait_st();
+    }
+    // P (BF16) into row r of the swizzled K-major tile: 16-byte chunk c at c ^ (r & 7)
+    unsigned char* prow = sm + kOffP + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = safe_exp2_diff(s[8 * c + 2 * e], m_run), p1 = safe_exp2_diff(s[8 * c + 2 * e + 1], m_run);
+        w[e] = pack_bf16x2(p0, p1);
+        l_run += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+      *reinterpret_cast<uint4*>(prow + 16 * (c ^ (r & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- O += P V (thread 0)
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      if (!mbar_wait(&bars.v[bf], (j >> 1) & 1, abort_flag)) {
+        fail();
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = sdesc_sw128(sP + kk * 32, 16, 1024);
+          // V is MN-major (dims contiguous): LBO = stride between 64-dim blocks,
+          // SBO = stride between groups of 8 key rows; k-step kk = key rows 16 kk ..
+          const uint64_t bd = sdesc_sw128(sV + bf * 4 * kKVBlk + kk * 16 * 128, kKVBlk, 1024);
+          umma_bf16(tmem + kTmemO, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars.o);
+        ++issued_o;
+        if (j + 1 == ntiles) {
+          // both K buffers are free (S of the last tile is done): stage the gate tile there
+          if (p.fuse_gate) {
+            ++arm_g;
+            mbar_arrive_expect_tx(&bars.g, 4 * kQBlk);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffK + c * kQBlk, &tg, 64 * c, h, i0, b, &bars.g);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- epilogue: O / l, BF16, gate, store
+  if (ok && ntiles > 0) {
+    if (!mbar_wait(&bars.o, (ntiles - 1) & 1, abort_flag)) fail();
+    if (ok && p.fuse_gate && !mbar_wait(&bars.g, 0, abort_flag)) fail();
+  }
+  if (__syncthreads_or(!ok)) ok = false;  // CTA-uniform from here on
+  tc_fence_after();
+  if (ok) {
+    const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+    __nv_bfloat16* orow = p.out + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD;
+    const unsigned char* grow = sm + kOffK + r * 128;  // gate row r of block c at + c * kQBlk
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      float o[32];
+      if (ntiles > 0) {
+        tmem_ld32(t_row + kTmemO + c0, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+      }
+      if (qi >= p.Sq) continue;  // a row past the end (after the warp-collective load)
+      uint32_t res[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint16_t ob0 = float_to_bf16_bits(o[2 * e] * inv), ob1 = float_to_bf16_bits(o[2 * e + 1] * inv);
+        uint32_t v = (uint32_t)ob0 | ((uint32_t)ob1 << 16);
+        if (p.fuse_gate) {
+          const int d = c0 + 2 * e;  // gate elements d, d + 1 of row r
+          uint32_t g2;
+          if (ntiles > 0) {
+            const int cb = d >> 6, ch = (d & 63) >> 3;
+            g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kQBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
+          } else {
+            g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
+          }
+          v = (uint32_t)gate_product_bf16(ob0, sigmoid_bf16((uint16_t)(g2 & 0xFFFFu))) |
+              ((uint32_t)gate_product_bf16(ob1, sigmoid_bf16((uint16_t)(g2 >> 16))) << 16);
+        }
+        res[e] = v;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        reinterpret_cast<uint4*>(orow + c0)[e] = make_uint4(res[4 * e], res[4 * e + 1], res[4 * e + 2], res[4 * e + 3]);
+    }
+    if (p.lse && qi < p.Sq) {
+      p.lse[((size_t)b * p.Hq + h) * p.Sq + qi] =
+          (l_run > 0.0f) ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+    }
+  }
+
+  // ---- teardown: on an abort, wait (bounded) for the MMAs and copies this CTA started
+  if (tid == 0 && !ok) {
+    int dummy = 0;
+    volatile int* none = &dummy;
+    if (issued_s > 0) mbar_wait(&bars.s, (issued_s - 1) & 1, none);
+    if (issued_o > 0) mbar_wait(&bars.o, (issued_o - 1) & 1, none);
+    if (arm_q > 0) mbar_wait(&bars.q, (arm_q - 1) & 1, none);
+    if (arm_g > 0) mbar_wait(&bars.g, (arm_g - 1) & 1, none);
+    for (int x = 0; x < 2; ++x) {
+      if (arm_k[x] > 0) mbar_wait(&bars.k[x], (arm_k[x] - 1) & 1, none);
+      if (arm_v[x] > 0) mbar_wait(&bars.v[x], (arm_v[x] - 1) & 1, none);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// [B, S, H, D] BF16, box {64, 1, rows, 1}, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2, (cuuint64_t)S * H * kD * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k, const void* v, const void* gate,
+                           cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tg;
+  // S = 0 still needs a valid map: use extent 1 (nothing is loaded then)
+  if (!make_map(&tq, q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM) || !make_map(&tk, k, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
+      !make_map(&tv, v, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
+      !make_map(&tg, gate ? gate : q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const dim3 grid((unsigned)((p.Sq + kPM - 1) / kPM), (unsigned)p.Hq, (unsigned)p.B);
+  prefill_kernel<<<grid, kPThreads, kSmemBytes, stream>>>(tq, tk, tv, tg, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gda

@@ -187,6 +187,32 @@ int gda_decode_e4m3(const gda_bf16* q, const gda_bf16* gate, const uint8_t* k_po
                     gda_bf16* out, int B, int Hq, int Hkv, int D, float scale, float k_descale,
                     float v_descale, int num_splits, gda_stream_t stream);
 
+/* Prefill / extend gated SDPA (cuDNN FE-OSS "Gated Attention Block (SM107)", Overview
+ * stages (4) SDPA with GQA H_q / H_kv and (5) the gate; Fusion knobs: fuse_gate puts
+ * O *= sigmoid(GATE) in the SDPA epilogue, after the dead-row select; Forward:
+ * return_lse, seq_lens).
+ *   q, gate   [B, Sq, Hq, D] bf16          queries and gate (gate NULL: out = RNE_bf16(O))
+ *   k, v      [B, Skv, Hkv, D] bf16        keys and values of each sequence
+ *   kv_lens   [B] int32 or NULL            valid keys per sequence (0 <= L_b <= Skv; NULL: Skv)
+ *   out       [B, Sq, Hq, D] bf16          RNE_bf16(RNE_bf16(O) * RNE_bf16(sigmoid(gate)))
+ *   lse       [B, Hq, Sq] float or NULL    natural-log log-sum-exp (-inf for a dead row)
+ *   causal    1: key j is visible to query i when j <= i + (L_b - Sq) (the queries are the
+ *             last Sq of the L_b positions); 0: every key j < L_b is visible
+ *   error_word  device uint32 the kernel ORs GDA_DEVERR_* bits into, or NULL for the
+ *             library's own word (gda_prefill_read_error)
+ * D = 256 only (GDA_ERR_UNSUPPORTED otherwise).  All tensors contiguous, device
+ * pointers 16-byte aligned (4 for kv_lens / lse / error_word).  One kernel on `stream`,
+ * no allocation, no read back; the tensor-map set-up runs on the host per call.
+ * A query row with no visible key gives O = 0 (out = 0) and lse = -inf. */
+int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, const gda_bf16* v,
+                const int32_t* kv_lens, gda_bf16* out, float* lse, int B, int Sq, int Skv, int Hq, int Hkv,
+                int D, float scale, int causal, uint32_t* error_word, gda_stream_t stream);
+
+/* The library's prefill error word (used when gda_prefill gets error_word == NULL) on
+ * the current device: synchronises `stream`, stores the bits in *error_word, clears
+ * them when `clear` is nonzero; GDA_OK when zero, GDA_ERR_DEVICE otherwise. */
+int gda_prefill_read_error(gda_stream_t stream, int clear, uint32_t* error_word);
+
 /* Size of the fixed device scratch area that gda_decode_noalloc uses (16 MiB). */
 #define GDA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

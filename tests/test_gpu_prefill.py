@@ -1,0 +1,111 @@
+"""Prefill / extend gated SDPA on the GPU (tcgen05 kernel) against the FP64 oracle.
+
+cuDNN FE-OSS "Gated Attention Block (SM107)", Overview stages (4)-(5) with fuse_gate:
+O = softmax(Q K^T * scale + mask) V with GQA, out = RNE(RNE(O) * RNE(sigmoid(gate))).
+Tolerance as in the decode tests: |err| <= 4e-3 + 1.6e-2 |ref| on the gated output
+(P is rounded to BF16 before the PV product, sums in FP32)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_gqa_attention_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 4e-3, 1.6e-2
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def check_close(got, want, rows=None):
+    g = oracle.double_from_bf16(got)
+    w = oracle.double_from_bf16(want)
+    if rows is not None:
+        idx = tuple(np.asarray(rows).T)
+        g, w = g[idx], w[idx]
+    bad = np.abs(g - w) > ATOL + RTOL * np.abs(w)
+    assert not bad.any(), "%d / %d out of tolerance, worst %.3g" % (bad.sum(), bad.size, np.abs(g - w).max())
+    return float(np.abs(g - w).max()) if g.size else 0.0
+
+
+def to_cuda(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def run(gda, d, gate=True, lse=None):
+    out = gda.prefill(d["q"], d["gate"] if gate else None, d["k"], d["v"], kv_lens=d["kv_lens"], lse=lse,
+                      scale=d["scale"], causal=d["causal"])
+    torch.cuda.synchronize()
+    return bits(out)
+
+
+def reference(inp, rows=None):
+    return oracle.prefill(inp["q"], inp["gate"], inp["k"], inp["v"], inp["scale"], causal=inp["causal"],
+                          kv_lens=inp["kv_lens"], rows=rows)
+
+
+CASES = [
+    # B, Sq, Skv, Hq, Hkv, causal, kv_lens
+    (1, 128, 128, 1, 1, True, None),            # one CTA, one diagonal
+    (1, 128, 128, 1, 1, False, None),
+    (1, 200, 200, 2, 1, True, None),            # ragged query and key tails
+    (2, 300, 300, 4, 2, False, None),
+    (1, 77, 333, 2, 2, True, None),             # extend: 77 new tokens after 256 cached
+    (3, 130, 190, 4, 1, True, [190, 64, 0]),    # padded keys; an empty sequence (dead rows)
+    (2, 256, 256, 32, 2, True, None),           # the page's head geometry
+    (1, 64, 1000, 2, 2, False, [700]),
+]
+
+
+@pytest.mark.parametrize("B,Sq,Skv,Hq,Hkv,causal,kv_lens", CASES)
+def test_prefill_parity(gda, B, Sq, Skv, Hq, Hkv, causal, kv_lens):
+    inp = workloads.make_prefill(B, Sq, Skv, seed=500 + Sq + Skv, hq=Hq, hkv=Hkv, causal=causal, kv_lens=kv_lens)
+    dev = to_cuda(inp)
+    ref = reference(inp)
+    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
+    check_close(run(gda, dev, lse=lse), ref.out)
+    got_lse = lse.cpu().numpy()
+    live = np.isfinite(ref.lse)
+    np.testing.assert_allclose(got_lse[live], ref.lse[live], atol=2e-3, rtol=1e-4)
+    assert np.all(np.isneginf(got_lse[~live]))
+    assert gda.prefill_read_error() == 0
+
+
+def test_prefill_unfused_and_deterministic(gda):
+    inp = workloads.make_prefill(2, 160, 160, seed=41, hq=4, hkv=2, causal=True)
+    dev = to_cuda(inp)
+    ref = reference(inp)
+    check_close(run(gda, dev, gate=False), ref.o_bf16)
+    a = run(gda, dev)
+    b = run(gda, dev)
+    assert np.array_equal(a, b)
+    # the fused gate equals the standalone gate applied to the unfused output, bit for bit
+    o = run(gda, dev, gate=False)
+    assert np.array_equal(a, oracle.gate(o, bits(inp["gate"])))
+
+
+def test_prefill_scores_that_move_the_max(gda):
+    """Keys that grow along the sequence force repeated rescaling of O in TMEM."""
+    inp = workloads.make_prefill(1, 256, 512, seed=43, hq=2, hkv=1, causal=False)
+    ramp = torch.linspace(0.2, 6.0, 512)[None, :, None, None]
+    inp["k"] = (inp["k"].float() * ramp).to(torch.bfloat16)
+    inp["scale"] = 0.25
+    dev = to_cuda(inp)
+    check_close(run(gda, dev), reference(inp).out)
+
+
+@pytest.mark.parametrize("key", ["p1_s512_causal", "p1_s4096_causal", "p1_s4096_dense", "p4_extend_q1024_kv8192"])
+def test_prefill_workload_sampled(gda, key):
+    inp = workloads.make_prefill_workload(key)
+    dev = to_cuda(inp)
+    out = run(gda, dev)
+    B, Sq, Hq = inp["q"].shape[:3]
+    rng = np.random.default_rng(3)
+    rows = np.stack([rng.integers(0, B, 48), rng.integers(0, Sq, 48), rng.integers(0, Hq, 48)], axis=1)
+    rows = np.concatenate([rows, [[0, 0, 0], [B - 1, Sq - 1, Hq - 1], [0, Sq - 1, 0]]]).astype(np.int32)
+    ref = reference(inp, rows=rows)
+    check_close(out, ref.out, rows=rows)
+    assert gda.prefill_read_error() == 0
