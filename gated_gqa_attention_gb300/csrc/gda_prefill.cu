@@ -10,22 +10,26 @@
 //   out = RNE_bf16(RNE_bf16(O) * RNE_bf16(sigmoid(gate)))   (the decode path's gate)
 //   lse = natural-log log-sum-exp of the visible scaled scores ([B, Hq, Sq], optional)
 //
-// GB300 design (one CTA of 4 warps per (128-query block, query head, sequence)):
-//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) brings the Q tile [128 x 256] once
-//    and K / V tiles [64 x 256] into a double buffer, one tile ahead; the gate tile
-//    is staged by TMA into the freed K buffers for the epilogue.
-//  * tcgen05.mma (kind::f16, BF16 operands, FP32 accumulation, M = 128) issued by
-//    one thread: S = Q K^T (N = 64, sixteen k-steps of 16) into TMEM columns
-//    [0, 64), and O += P V (N = 256, four k-steps) into TMEM columns [256, 512).
-//    Completion is signalled by tcgen05.commit on an mbarrier.
-//  * Softmax: thread r owns query row r = TMEM lane r; it reads its 64 scores with
-//    tcgen05.ld, keeps a running max (moved lazily, by more than 2^8, as the decode
-//    kernels do; O in TMEM is rescaled then) and sum, and writes P (BF16) to shared
-//    memory in the swizzled K-major layout the next MMA reads.
-//  * Epilogue: O row from TMEM, divided by the sum, rounded to BF16, gated with the
-//    BF16 sigmoid of the staged gate row, stored.
-// Every wait is bounded; on a timeout the CTA records kErrTimeout, stops issuing
-// work, waits (bounded) for what it issued, frees its TMEM and returns.
+// GB300 design: one CTA per (128-query block, query head, sequence), three roles
+// that hand tiles to each other through mbarriers (full / empty pairs):
+//  * warp 4, TMA producer: the Q tile [128 x 256] once, K and V tiles [64 x 256] into
+//    two-stage rings (cp.async.bulk.tensor, 128-byte swizzle), and at the end the
+//    gate tile into the freed K ring (the gate tile staged by TMA for the epilogue).
+//  * warp 5, MMA issuer (one lane; it also owns the TMEM allocation): tcgen05.mma
+//    kind::f16, BF16 operands, FP32 accumulation, M = 128.  S(j) = Q K(j)^T (N = 64,
+//    sixteen k-steps) into one of two TMEM S buffers, then O += P(j-1) V(j-1)
+//    (N = 256, four k-steps) into TMEM columns [256, 512): the tensor core computes
+//    S(j) while the softmax works on tile j - 1.  tcgen05.commit signals completion.
+//  * warps 0-3, softmax and epilogue: thread r owns query row r = TMEM lane r; it
+//    reads its 64 scores with tcgen05.ld, keeps a running max (moved lazily, by more
+//    than 2^8, as the decode kernels do; O in TMEM is rescaled then) and sum, and
+//    writes P (BF16) into one of two shared-memory buffers in the swizzled K-major
+//    layout the PV MMA reads.  Epilogue: O row from TMEM, divided by the sum,
+//    rounded to BF16, gated with the BF16 sigmoid of the staged gate row (from a
+//    per-device table of all 65 536 BF16 sigmoids), stored.
+// Every wait is bounded; on a timeout the CTA records kErrTimeout, every role stops,
+// waits (bounded) for the copies and MMAs it started, the TMEM is freed and the CTA
+// returns.  TMEM accesses stay warp-convergent (decisions combined with __all_sync).
 #include <cuda.h>
 
 #include "gda_device.cuh"
@@ -37,9 +41,12 @@ namespace {
 
 constexpr int kPM = 128;            // query rows per CTA (MMA M)
 constexpr int kPN = 64;             // keys per tile (MMA N of S)
-constexpr int kPThreads = 128;
+constexpr int kSoftmaxWarps = 4;   // warps 0-3: softmax and epilogue, one query row per thread
+constexpr int kLoadWarp = 4;       // TMA producer
+constexpr int kMmaWarp = 5;        // MMA issuer; allocates and frees TMEM
+constexpr int kPThreads = 6 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;      // S accumulator columns [0, 64)
+constexpr uint32_t kTmemS = 0;      // S accumulators: columns [0, 64) and [64, 128)
 constexpr uint32_t kTmemO = 256;    // O accumulator columns [256, 512)
 
 // shared memory plan (offsets from a 1024-byte aligned base)
@@ -48,9 +55,10 @@ constexpr uint32_t kKVBlk = kPN * 128;            // one 64-column block of a K 
 constexpr uint32_t kOffQ = 0;                     // 4 blocks, 64 KiB
 constexpr uint32_t kOffK = kOffQ + 4 * kQBlk;     // 2 buffers x 4 blocks, 64 KiB
 constexpr uint32_t kOffV = kOffK + 8 * kKVBlk;    // 2 buffers x 4 blocks, 64 KiB
-constexpr uint32_t kOffP = kOffV + 8 * kKVBlk;    // 128 rows x 128 B, 16 KiB
-constexpr uint32_t kOffBar = kOffP + kPM * 128;   // mbarriers and the TMEM address
-constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;  // + alignment slack
+constexpr uint32_t kPBuf = kPM * 128;             // one P tile: 128 rows x 128 B, 16 KiB
+constexpr uint32_t kOffP = kOffV + 8 * kKVBlk;    // 2 buffers, 32 KiB
+constexpr uint32_t kOffBar = kOffP + 2 * kPBuf;   // mbarriers and the TMEM address
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
 
 // ---- PTX wrappers (tcgen05, TMA) ----
 
@@ -142,11 +150,25 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// BF16 sigmoid table: entry g = RNE_bf16(sigmoid(g)) for every BF16 code g, filled
+// once per device with the certified sigmoid_bf16 (FreeToken PR #781, Summary: a
+// per-device table of BF16 sigmoid values, 128 KiB).  The prefill epilogue gates
+// Sq * Hq * D elements, where one table load is far cheaper than the computation.
+__device__ uint16_t g_sigmoid_table[65536];
+
+__global__ void sigmoid_table_kernel() {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 65536) g_sigmoid_table[i] = sigmoid_bf16((uint16_t)i);
+}
+
 struct PrefillBars {
-  uint64_t q, k[2], v[2], s, o, g;
+  uint64_t q, g;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint32_t tmem;
   int abort;
 };
+static_assert(sizeof(PrefillBars) <= 256, "barrier block");
 
 }  // namespace
 
@@ -156,7 +178,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PrefillBars& bars = *reinterpret_cast<PrefillBars*>(sm + kOffBar);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqb = (p.Sq + kPM - 1) / kPM;
   const int qb = nqb - 1 - (int)blockIdx.x;  // the longest causal blocks first
   const int h = blockIdx.y, b = blockIdx.z;
@@ -170,17 +192,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bars.q, 1);
-    mbar_init(&bars.k[0], 1);
-    mbar_init(&bars.k[1], 1);
-    mbar_init(&bars.v[0], 1);
-    mbar_init(&bars.v[1], 1);
-    mbar_init(&bars.s, 1);
-    mbar_init(&bars.o, 1);
     mbar_init(&bars.g, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.k_full[x], 1);
+      mbar_init(&bars.k_empty[x], 1);
+      mbar_init(&bars.v_full[x], 1);
+      mbar_init(&bars.v_empty[x], 1);
+      mbar_init(&bars.s_full[x], 1);
+      mbar_init(&bars.s_empty[x], kSoftmaxWarps);
+      mbar_init(&bars.p_full[x], kSoftmaxWarps);
+      mbar_init(&bars.p_empty[x], 1);
+    }
     bars.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars.tmem, kTmemCols);
     tmem_relinquish();
   }
@@ -189,228 +215,252 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem;
   volatile int* abort_flag = &bars.abort;
-  bool ok = true;
   auto fail = [&]() {
-    if (ok) {
-      ok = false;
-      bars.abort = 1;
-      atomicOr(p.error, kErrTimeout);
-    }
+    if (bars.abort == 0) atomicOr(p.error, kErrTimeout);
+    bars.abort = 1;
   };
 
-  const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV),
-                 sP = smem_u32(sm + kOffP);
-  const uint32_t idS = idesc_bf16(kPM, kPN, 0), idO = idesc_bf16(kPM, 256, 1);
-  // thread 0's record of what it started: MMA groups committed and TMA loads armed
-  // per barrier (the n-th arm of a barrier completes its phase n - 1)
-  int issued_s = 0, issued_o = 0, arm_q = 0, arm_g = 0, arm_k[2] = {0, 0}, arm_v[2] = {0, 0};
-
-  auto load_kv = [&](int j) {  // thread 0: K and V tile j into buffer j & 1
-    const int bf = j & 1;
-    ++arm_k[bf];
-    ++arm_v[bf];
-    mbar_arrive_expect_tx(&bars.k[bf], 4 * kKVBlk);
+  if (warp == kLoadWarp) {
+    // ---------------- TMA producer (one lane)
+    if (lane == 0 && ntiles > 0) {
+      int arm_q = 0, arm_g = 0, arm_k[2] = {0, 0}, arm_v[2] = {0, 0};
+      bool ok = true;
+      ++arm_q;
+      mbar_arrive_expect_tx(&bars.q, 4 * kQBlk);
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      tma_load_4d(sm + kOffK + (bf * 4 + c) * kKVBlk, &tk, 64 * c, kvh, j * kPN, b, &bars.k[bf]);
-    mbar_arrive_expect_tx(&bars.v[bf], 4 * kKVBlk);
+      for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffQ + c * kQBlk, &tq, 64 * c, h, i0, b, &bars.q);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int x = j & 1, n = j >> 1;
+        // K(j) once S(j - 2) has read the buffer, V(j) once PV(j - 2) has
+        if (j >= 2 && !mbar_wait(&bars.k_empty[x], (n - 1) & 1, abort_flag)) { ok = false; break; }
+        ++arm_k[x];
+        mbar_arrive_expect_tx(&bars.k_full[x], 4 * kKVBlk);
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      tma_load_4d(sm + kOffV + (bf * 4 + c) * kKVBlk, &tv, 64 * c, kvh, j * kPN, b, &bars.v[bf]);
-  };
-
-  if (tid == 0 && ntiles > 0) {
-    ++arm_q;
-    mbar_arrive_expect_tx(&bars.q, 4 * kQBlk);
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(sm + kOffK + (x * 4 + c) * kKVBlk, &tk, 64 * c, kvh, j * kPN, b, &bars.k_full[x]);
+        if (j >= 2 && !mbar_wait(&bars.v_empty[x], (n - 1) & 1, abort_flag)) { ok = false; break; }
+        ++arm_v[x];
+        mbar_arrive_expect_tx(&bars.v_full[x], 4 * kKVBlk);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffQ + c * kQBlk, &tq, 64 * c, h, i0, b, &bars.q);
-    load_kv(0);
-  }
-
-  const int r = tid;  // query row of this thread = TMEM lane
-  const int qi = i0 + r;
-  const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-  float m_run = -INFINITY, l_run = 0.0f;
-
-  for (int j = 0; j < ntiles; ++j) {
-    const int bf = j & 1;
-    // ---- S = Q K^T (thread 0)
-    if (tid == 0 && ok) {
-      if (j == 0 && !mbar_wait(&bars.q, 0, abort_flag)) fail();
-      if (ok && !mbar_wait(&bars.k[bf], (j >> 1) & 1, abort_flag)) fail();
-      if (ok) {
-        tc_fence_after();
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(sm + kOffV + (x * 4 + c) * kKVBlk, &tv, 64 * c, kvh, j * kPN, b, &bars.v_full[x]);
+      }
+      if (ok && p.fuse_gate) {
+        // the gate tile goes into the K ring once the last two S products have read it
+        const int jl = ntiles - 1;
+        if (!mbar_wait(&bars.k_empty[jl & 1], (jl >> 1) & 1, abort_flag)) ok = false;
+        if (ok && ntiles >= 2 && !mbar_wait(&bars.k_empty[(jl - 1) & 1], ((jl - 1) >> 1) & 1, abort_flag)) ok = false;
+        if (ok) {
+          ++arm_g;
+          mbar_arrive_expect_tx(&bars.g, 4 * kQBlk);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + (bf * 4 + (kk >> 2)) * kKVBlk + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tmem + kTmemS, ad, bd, idS, kk > 0 ? 1u : 0u);
+          for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffK + c * kQBlk, &tg, 64 * c, h, i0, b, &bars.g);
         }
-        umma_commit(&bars.s);
-        ++issued_s;
+      }
+      if (!ok) {
+        fail();
+        // wait (bounded) for every copy this CTA started before its memory goes away
+        int dummy = 0;
+        volatile int* none = &dummy;
+        if (arm_q > 0) mbar_wait(&bars.q, (arm_q - 1) & 1, none);
+        if (arm_g > 0) mbar_wait(&bars.g, (arm_g - 1) & 1, none);
+        for (int x = 0; x < 2; ++x) {
+          if (arm_k[x] > 0) mbar_wait(&bars.k_full[x], (arm_k[x] - 1) & 1, none);
+          if (arm_v[x] > 0) mbar_wait(&bars.v_full[x], (arm_v[x] - 1) & 1, none);
+        }
       }
     }
-    if (ok && !mbar_wait(&bars.s, j & 1, abort_flag)) fail();
-    // PV of the previous tile must be done before P and O are touched again
-    if (ok && j > 0 && !mbar_wait(&bars.o, (j - 1) & 1, abort_flag)) fail();
-    // one CTA-wide decision, so the warp-collective TMEM accesses below stay convergent
-    if (__syncthreads_or(!ok)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    // the other buffer (tile j - 1) is free: load tile j + 1 into it
-    if (tid == 0 && j + 1 < ntiles) load_kv(j + 1);
-
-    // ---- softmax of row r over keys [64 j, 64 j + 64)
-    float s[64];
-    tmem_ld32(t_row + kTmemS, s);
-    tmem_ld32(t_row + kTmemS + 32, s + 32);
-    tmem_wait_ld();
-    const int k0 = j * kPN;
-    const bool need_mask = (k0 + kPN > L) || (p.causal && k0 + kPN - 1 > i0 + off);
-    float mx = -INFINITY;
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer (one lane): S(j) runs while the softmax works on tile j - 1
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV),
+                     sP = smem_u32(sm + kOffP);
+      const uint32_t idS = idesc_bf16(kPM, kPN, 0), idO = idesc_bf16(kPM, 256, 1);
+      uint64_t* last_bar = nullptr;  // the barrier of the last commit and its phase parity
+      int last_par = 0;
+      bool ok = mbar_wait(&bars.q, 0, abort_flag);
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          const int x = j & 1, n = j >> 1;
+          ok = mbar_wait(&bars.k_full[x], n & 1, abort_flag);
+          if (ok && j >= 2) ok = mbar_wait(&bars.s_empty[x], (n - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      float x = s[c] * p.scale_log2;
-      if (need_mask) {
-        const int kj = k0 + c;
-        if (kj >= L || (p.causal && kj > qi + off)) x = -INFINITY;
+          for (int kk = 0; kk < 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sK + (x * 4 + (kk >> 2)) * kKVBlk + (kk & 3) * 32, 16, 1024);
+            umma_bf16(tmem + kTmemS + x * kPN, ad, bd, idS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars.s_full[x]);
+          umma_commit(&bars.k_empty[x]);
+          last_bar = &bars.k_empty[x];
+          last_par = n & 1;
+        }
+        if (j >= 1) {
+          const int jp = j - 1, y = jp & 1, ny = jp >> 1;
+          ok = mbar_wait(&bars.p_full[y], ny & 1, abort_flag);
+          if (ok) ok = mbar_wait(&bars.v_full[y], ny & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(sP + y * kPBuf + kk * 32, 16, 1024);
+            // V is MN-major (dims contiguous): LBO = stride between 64-dim blocks,
+            // SBO = stride between groups of 8 key rows; k-step kk = key rows 16 kk ..
+            const uint64_t bd = sdesc_sw128(sV + y * 4 * kKVBlk + kk * 16 * 128, kKVBlk, 1024);
+            umma_bf16(tmem + kTmemO, ad, bd, idO, (jp > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars.p_empty[y]);
+          umma_commit(&bars.v_empty[y]);
+          last_bar = &bars.v_empty[y];
+          last_par = ny & 1;
+        }
       }
-      s[c] = x;
-      mx = fmaxf(mx, x);
+      if (!ok) {
+        fail();
+        // the last commit covers every MMA issued before it: wait for it (bounded)
+        int dummy = 0;
+        volatile int* none = &dummy;
+        if (last_bar != nullptr) mbar_wait(last_bar, last_par, none);
+      }
     }
-    // lazy max: it moves only by more than 2^8, so probabilities stay below 2^8
-    float alpha = 1.0f;
-    if (mx > m_run + 8.0f) {
-      alpha = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mx);
-      l_run *= alpha;
-      m_run = mx;
+  } else {
+    // ---------------- softmax and epilogue: thread r owns query row r (TMEM lane r)
+    const int r = tid;
+    const int qi = i0 + r;
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int x = j & 1, n = j >> 1;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[x], n & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      float s[64];
+      tmem_ld32(t_row + kTmemS + x * kPN, s);
+      tmem_ld32(t_row + kTmemS + x * kPN + 32, s + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_empty[x]);  // the S buffer may be overwritten
+
+      const int k0 = j * kPN;
+      const bool need_mask = (k0 + kPN > L) || (p.causal && k0 + kPN - 1 > i0 + off);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float v = s[c] * p.scale_log2;
+        if (need_mask) {
+          const int kj = k0 + c;
+          if (kj >= L || (p.causal && kj > qi + off)) v = -INFINITY;
+        }
+        s[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      // lazy max: it moves only by more than 2^8, so probabilities stay below 2^8
+      float alpha = 1.0f;
+      if (mx > m_run + 8.0f) {
+        alpha = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mx);
+        l_run *= alpha;
+        m_run = mx;
+      }
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
+      if (rescale) {
+        // O must hold PV(j - 1) before it is rescaled
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          float o[32];
+          tmem_ld32(t_row + kTmemO + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(t_row + kTmemO + c0, o);
+        }
+        tmem_wait_st();
+      }
+      // P buffer x is free once PV(j - 2) has read it
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[x], (n - 1) & 1, abort_flag));
+        if (!ok) break;
+      }
+      unsigned char* prow = sm + kOffP + x * kPBuf + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = safe_exp2_diff(s[8 * c + 2 * e], m_run), p1 = safe_exp2_diff(s[8 * c + 2 * e + 1], m_run);
+          w[e] = pack_bf16x2(p0, p1);
+          l_run += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+        *reinterpret_cast<uint4*>(prow + 16 * (c ^ (r & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full[x]);
     }
-    // rescale O rows in TMEM (PV of the previous tile has completed); the TMEM
-    // accesses are warp-collective, so a warp rescales when any of its rows must
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+    if (!ok) fail();
+
+    // ---- epilogue: O / l, BF16, gate, store
+    if (ok && ntiles > 0) {
+      const int jl = ntiles - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag));
+      if (ok && p.fuse_gate) ok = __all_sync(0xffffffffu, mbar_wait(&bars.g, 0, abort_flag));
+      if (!ok) fail();
+      tc_fence_after();
+    }
+    if (ok) {
+      const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      __nv_bfloat16* orow = p.out + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD;
+      const unsigned char* grow = sm + kOffK + r * 128;  // gate row r of block c at + c * kQBlk
       for (int c0 = 0; c0 < 256; c0 += 32) {
         float o[32];
-        tmem_ld32(t_row + kTmemO + c0, o);
-        tmem_wait_ld();
+        if (ntiles > 0) {
+          tmem_ld32(t_row + kTmemO + c0, o);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        tmem_st32(t_row + kTmemO + c0, o);
-      }
-      tmem_wait_st();
-    }
-    // P (BF16) into row r of the swizzled K-major tile: 16-byte chunk c at c ^ (r & 7)
-    unsigned char* prow = sm + kOffP + r * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p0 = safe_exp2_diff(s[8 * c + 2 * e], m_run), p1 = safe_exp2_diff(s[8 * c + 2 * e + 1], m_run);
-        w[e] = pack_bf16x2(p0, p1);
-        l_run += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
-      }
-      *reinterpret_cast<uint4*>(prow + 16 * (c ^ (r & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- O += P V (thread 0)
-    if (tid == 0 && ok) {
-      tc_fence_after();
-      if (!mbar_wait(&bars.v[bf], (j >> 1) & 1, abort_flag)) {
-        fail();
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = sdesc_sw128(sP + kk * 32, 16, 1024);
-          // V is MN-major (dims contiguous): LBO = stride between 64-dim blocks,
-          // SBO = stride between groups of 8 key rows; k-step kk = key rows 16 kk ..
-          const uint64_t bd = sdesc_sw128(sV + bf * 4 * kKVBlk + kk * 16 * 128, kKVBlk, 1024);
-          umma_bf16(tmem + kTmemO, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
         }
-        umma_commit(&bars.o);
-        ++issued_o;
-        if (j + 1 == ntiles) {
-          // both K buffers are free (S of the last tile is done): stage the gate tile there
+        if (qi >= p.Sq) continue;  // a row past the end (after the warp-collective load)
+        uint32_t res[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint16_t ob0 = float_to_bf16_bits(o[2 * e] * inv), ob1 = float_to_bf16_bits(o[2 * e + 1] * inv);
+          uint32_t v = (uint32_t)ob0 | ((uint32_t)ob1 << 16);
           if (p.fuse_gate) {
-            ++arm_g;
-            mbar_arrive_expect_tx(&bars.g, 4 * kQBlk);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffK + c * kQBlk, &tg, 64 * c, h, i0, b, &bars.g);
+            const int d = c0 + 2 * e;  // gate elements d, d + 1 of row r
+            uint32_t g2;
+            if (ntiles > 0) {
+              const int cb = d >> 6, ch = (d & 63) >> 3;
+              g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kQBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
+            } else {
+              g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
+            }
+            const uint16_t s0 = __ldg(g_sigmoid_table + (g2 & 0xFFFFu)), s1 = __ldg(g_sigmoid_table + (g2 >> 16));
+            v = (uint32_t)gate_product_bf16(ob0, s0) | ((uint32_t)gate_product_bf16(ob1, s1) << 16);
           }
+          res[e] = v;
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          reinterpret_cast<uint4*>(orow + c0)[e] = make_uint4(res[4 * e], res[4 * e + 1], res[4 * e + 2], res[4 * e + 3]);
+      }
+      if (p.lse && qi < p.Sq) {
+        p.lse[((size_t)b * p.Hq + h) * p.Sq + qi] =
+            (l_run > 0.0f) ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
       }
     }
   }
 
-  // ---- epilogue: O / l, BF16, gate, store
-  if (ok && ntiles > 0) {
-    if (!mbar_wait(&bars.o, (ntiles - 1) & 1, abort_flag)) fail();
-    if (ok && p.fuse_gate && !mbar_wait(&bars.g, 0, abort_flag)) fail();
-  }
-  if (__syncthreads_or(!ok)) ok = false;  // CTA-uniform from here on
-  tc_fence_after();
-  if (ok) {
-    const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-    __nv_bfloat16* orow = p.out + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD;
-    const unsigned char* grow = sm + kOffK + r * 128;  // gate row r of block c at + c * kQBlk
-    for (int c0 = 0; c0 < 256; c0 += 32) {
-      float o[32];
-      if (ntiles > 0) {
-        tmem_ld32(t_row + kTmemO + c0, o);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.0f;
-      }
-      if (qi >= p.Sq) continue;  // a row past the end (after the warp-collective load)
-      uint32_t res[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const uint16_t ob0 = float_to_bf16_bits(o[2 * e] * inv), ob1 = float_to_bf16_bits(o[2 * e + 1] * inv);
-        uint32_t v = (uint32_t)ob0 | ((uint32_t)ob1 << 16);
-        if (p.fuse_gate) {
-          const int d = c0 + 2 * e;  // gate elements d, d + 1 of row r
-          uint32_t g2;
-          if (ntiles > 0) {
-            const int cb = d >> 6, ch = (d & 63) >> 3;
-            g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kQBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
-          } else {
-            g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
-          }
-          v = (uint32_t)gate_product_bf16(ob0, sigmoid_bf16((uint16_t)(g2 & 0xFFFFu))) |
-              ((uint32_t)gate_product_bf16(ob1, sigmoid_bf16((uint16_t)(g2 >> 16))) << 16);
-        }
-        res[e] = v;
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        reinterpret_cast<uint4*>(orow + c0)[e] = make_uint4(res[4 * e], res[4 * e + 1], res[4 * e + 2], res[4 * e + 3]);
-    }
-    if (p.lse && qi < p.Sq) {
-      p.lse[((size_t)b * p.Hq + h) * p.Sq + qi] =
-          (l_run > 0.0f) ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
-    }
-  }
-
-  // ---- teardown: on an abort, wait (bounded) for the MMAs and copies this CTA started
-  if (tid == 0 && !ok) {
-    int dummy = 0;
-    volatile int* none = &dummy;
-    if (issued_s > 0) mbar_wait(&bars.s, (issued_s - 1) & 1, none);
-    if (issued_o > 0) mbar_wait(&bars.o, (issued_o - 1) & 1, none);
-    if (arm_q > 0) mbar_wait(&bars.q, (arm_q - 1) & 1, none);
-    if (arm_g > 0) mbar_wait(&bars.g, (arm_g - 1) & 1, none);
-    for (int x = 0; x < 2; ++x) {
-      if (arm_k[x] > 0) mbar_wait(&bars.k[x], (arm_k[x] - 1) & 1, none);
-      if (arm_v[x] > 0) mbar_wait(&bars.v[x], (arm_v[x] - 1) & 1, none);
-    }
-  }
+  // ---- teardown: every role is done (or gave up and waited for what it started)
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -468,6 +518,10 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k,
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    // the sigmoid table, once per device, on the same stream ahead of the first use
+    sigmoid_table_kernel<<<256, 256, 0, stream>>>();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }

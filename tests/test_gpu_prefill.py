@@ -109,3 +109,20 @@ def test_prefill_workload_sampled(gda, key):
     ref = reference(inp, rows=rows)
     check_close(out, ref.out, rows=rows)
     assert gda.prefill_read_error() == 0
+
+
+def test_prefill_gate_covers_every_bf16_code(gda):
+    """O = 1 exactly (one visible key whose V row is 1.0), so out = RNE(sigmoid(g)):
+    all 65 536 gate codes through the fused epilogue against the oracle's sigmoid."""
+    B, Sq, Hq, D = 1, 16, 16, 256
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(B, Sq, Hq, D)
+    inp = workloads.make_prefill(B, Sq, 1, seed=7, hq=Hq, hkv=1, causal=False)
+    inp["gate"] = codes.view(torch.bfloat16)
+    inp["v"] = torch.ones_like(inp["v"])
+    dev = to_cuda(inp)
+    got = run(gda, dev)
+    want = oracle.sigmoid_bf16(codes.numpy().view(np.uint16))
+    g, w = oracle.double_from_bf16(got), oracle.double_from_bf16(want)
+    nan = np.isnan(w)
+    assert np.array_equal(np.isnan(g), nan)
+    assert np.array_equal(got[~nan], want[~nan])
