@@ -449,7 +449,7 @@ int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, cons
                 int D, float scale, int causal, uint32_t* error_word, gda_stream_t stream) {
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return GDA_ERR_SHAPE;
   if (D != gda::kD) return GDA_ERR_UNSUPPORTED;
-  if (!isfinite(scale)) return GDA_ERR_ARG;
+  if (!isfinite(scale) || !(scale > 0.0f)) return GDA_ERR_ARG;
   if (B == 0 || Sq == 0) return GDA_OK;
   if (!q || !out || (Skv > 0 && (!k || !v))) return GDA_ERR_NULL;
   if (!aligned(q, 16) || !aligned(out, 16) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||

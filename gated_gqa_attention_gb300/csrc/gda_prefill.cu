@@ -122,6 +122,21 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2^x on the SFU (ex2.approx, subnormal results flushed): P is rounded to BF16 right
+// after, far coarser than the instruction's error.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// {lo, hi} -> BF16x2, round to nearest even (lo in the low half)
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 // TMA: a 4-D tile (x innermost) into shared memory, completing on `bar`
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
                                             uint64_t* bar) {
@@ -347,16 +362,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
       const int k0 = j * kPN;
       const bool need_mask = (k0 + kPN > L) || (p.causal && k0 + kPN - 1 > i0 + off);
-      float mx = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float v = s[c] * p.scale_log2;
-        if (need_mask) {
+        for (int c = 0; c < 64; ++c) {
           const int kj = k0 + c;
-          if (kj >= L || (p.causal && kj > qi + off)) v = -INFINITY;
+          if (kj >= L || (p.causal && kj > qi + off)) s[c] = -INFINITY;
         }
-        s[c] = v;
-        mx = fmaxf(mx, v);
+      }
+      // tile max of the scaled scores: the largest raw score times scale * log2(e)
+      // (the scale is positive; a row with no visible key stays at -inf)
+      float mx;
+      {
+        float e4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) e4[c & 3] = fmaxf(e4[c & 3], s[c]);
+        mx = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3])) * p.scale_log2;
       }
       // lazy max: it moves only by more than 2^8, so probabilities stay below 2^8
       float alpha = 1.0f;
@@ -387,17 +407,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!ok) break;
       }
       unsigned char* prow = sm + kOffP + x * kPBuf + r * 128;
+      // p = 2^(s * scale_log2 - m): one FFMA and one SFU op per score (a masked score
+      // gives 2^-inf = 0; a row with no visible key yet uses m = 0)
+      const float mneg = (m_run == -INFINITY) ? 0.0f : -m_run;
+      float la = 0.0f, lb = 0.0f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = safe_exp2_diff(s[8 * c + 2 * e], m_run), p1 = safe_exp2_diff(s[8 * c + 2 * e + 1], m_run);
-          w[e] = pack_bf16x2(p0, p1);
-          l_run += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+          const float p0 = ex2_approx(fmaf(s[8 * c + 2 * e], p.scale_log2, mneg));
+          const float p1 = ex2_approx(fmaf(s[8 * c + 2 * e + 1], p.scale_log2, mneg));
+          w[e] = bf16x2_rn(p0, p1);
+          la += __uint_as_float(w[e] << 16);
+          lb += __uint_as_float(w[e] & 0xFFFF0000u);
         }
         *reinterpret_cast<uint4*>(prow + 16 * (c ^ (r & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      l_run += la + lb;
       fence_async_smem();
       tc_fence_before();
       __syncwarp();

@@ -200,6 +200,7 @@ int gda_decode_e4m3(const gda_bf16* q, const gda_bf16* gate, const uint8_t* k_po
  *             last Sq of the L_b positions); 0: every key j < L_b is visible
  *   error_word  device uint32 the kernel ORs GDA_DEVERR_* bits into, or NULL for the
  *             library's own word (gda_prefill_read_error)
+ * scale must be finite and > 0 (GDA_ERR_ARG otherwise).
  * D = 256 only (GDA_ERR_UNSUPPORTED otherwise).  All tensors contiguous, device
  * pointers 16-byte aligned (4 for kv_lens / lse / error_word).  One kernel on `stream`,
  * no allocation, no read back; the tensor-map set-up runs on the host per call.

@@ -204,3 +204,26 @@ def test_product_path_has_no_cpu_fallback():
             mod.load(os.path.join(ROOT, "does-not-exist", "libgda.so"))
         finally:
             mod._lib = mod._lib_saved
+
+
+def test_prefill_host_validation(lib):
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+
+    def call(q=16, gate=16, k=16, v=16, lens=0, out=16, lse=0, B=1, Sq=8, Skv=8, Hq=4, Hkv=2, D=256,
+             scale=0.0625, causal=1, err=0):
+        return lib.gda_prefill(vp(q), vp(gate), vp(k), vp(v), vp(lens), vp(out), vp(lse), B, Sq, Skv, Hq, Hkv, D,
+                               scale, causal, vp(err), None)
+    assert call(q=0) == ERR_NULL
+    assert call(out=0) == ERR_NULL
+    assert call(k=0) == ERR_NULL
+    assert call(q=24) == ERR_ALIGN
+    assert call(lse=2) == ERR_ALIGN
+    assert call(Hq=4, Hkv=3) == ERR_SHAPE
+    assert call(Sq=-1) == ERR_SHAPE
+    assert call(D=128) == ERR_UNSUPPORTED
+    assert call(scale=0.0) == ERR_ARG
+    assert call(scale=-0.5) == ERR_ARG
+    assert call(scale=float("inf")) == ERR_ARG
+    assert call(B=0, q=0, k=0, v=0, out=0) == OK
+    assert call(Sq=0, q=0, k=0, v=0, out=0) == OK
+    assert lib.gda_prefill_read_error(None, 0, None) == ERR_NULL
