@@ -12,19 +12,20 @@
 //
 // GB300 design: one CTA per (128-query block, query head, sequence), three roles
 // that hand tiles to each other through mbarriers (full / empty pairs):
-//  * warp 4, TMA producer: the Q tile [128 x 256] once, K and V tiles [64 x 256] into
+//  * warp 8, TMA producer: the Q tile [128 x 256] once, K and V tiles [64 x 256] into
 //    two-stage rings (cp.async.bulk.tensor, 128-byte swizzle), and at the end the
 //    gate tile into the freed K ring (the gate tile staged by TMA for the epilogue).
-//  * warp 5, MMA issuer (one lane; it also owns the TMEM allocation): tcgen05.mma
+//  * warp 9, MMA issuer (one lane; it also owns the TMEM allocation): tcgen05.mma
 //    kind::f16, BF16 operands, FP32 accumulation, M = 128.  S(j) = Q K(j)^T (N = 64,
 //    sixteen k-steps) into one of two TMEM S buffers, then O += P(j-1) V(j-1)
 //    (N = 256, four k-steps) into TMEM columns [256, 512): the tensor core computes
 //    S(j) while the softmax works on tile j - 1.  tcgen05.commit signals completion.
-//  * warps 0-3, softmax and epilogue: thread r owns query row r = TMEM lane r; it
-//    reads its 64 scores with tcgen05.ld, keeps a running max (moved lazily, by more
-//    than 2^8, as the decode kernels do; O in TMEM is rescaled then) and sum, and
-//    writes P (BF16) into one of two shared-memory buffers in the swizzled K-major
-//    layout the PV MMA reads.  Epilogue: O row from TMEM, divided by the sum,
+//  * warps 0-7, softmax and epilogue: the two warps w and w + 4 share query rows
+//    32 w .. + 31 (TMEM lanes), each taking 32 of a tile's 64 scores (tcgen05.ld);
+//    they agree on the row max through TMEM and a named barrier, keep a running
+//    max (moved lazily, by more than 2^8, as the decode kernels do; O in TMEM is
+//    rescaled then) and sum, and write P (BF16) into one of two shared-memory
+//    buffers in the swizzled K-major layout the PV MMA reads.  Epilogue: O row from TMEM, divided by the sum,
 //    rounded to BF16, gated with the BF16 sigmoid of the staged gate row (from a
 //    per-device table of all 65 536 BF16 sigmoids), stored.
 // Every wait is bounded; on a timeout the CTA records kErrTimeout, every role stops,
@@ -41,12 +42,13 @@ namespace {
 
 constexpr int kPM = 128;            // query rows per CTA (MMA M)
 constexpr int kPN = 64;             // keys per tile (MMA N of S)
-constexpr int kSoftmaxWarps = 4;   // warps 0-3: softmax and epilogue, one query row per thread
-constexpr int kLoadWarp = 4;       // TMA producer
-constexpr int kMmaWarp = 5;        // MMA issuer; allocates and frees TMEM
-constexpr int kPThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 8;   // warps 0-7: softmax and epilogue; warp w: rows 32 (w % 4) .., column half w / 4
+constexpr int kLoadWarp = 8;       // TMA producer
+constexpr int kMmaWarp = 9;        // MMA issuer; allocates and frees TMEM
+constexpr int kPThreads = 10 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;      // S accumulators: columns [0, 64) and [64, 128)
+constexpr uint32_t kTmemX = 128;    // exchange between a row's two halves: [128, 134)
 constexpr uint32_t kTmemO = 256;    // O accumulator columns [256, 512)
 
 // shared memory plan (offsets from a 1024-byte aligned base)
@@ -119,6 +121,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v)) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -180,6 +190,8 @@ struct PrefillBars {
   uint64_t q, g;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
+  uint64_t xm[4][2];  // per row quarter and tile parity: both halves stored their max
+  uint64_t xl[4];     // per row quarter: both halves stored their sum
   uint32_t tmem;
   int abort;
 };
@@ -217,6 +229,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&bars.s_empty[x], kSoftmaxWarps);
       mbar_init(&bars.p_full[x], kSoftmaxWarps);
       mbar_init(&bars.p_empty[x], 1);
+    }
+    for (int q4 = 0; q4 < 4; ++q4) {
+      mbar_init(&bars.xm[q4][0], 2);
+      mbar_init(&bars.xm[q4][1], 2);
+      mbar_init(&bars.xl[q4], 2);
     }
     bars.abort = 0;
     fence_mbar_init();
@@ -341,10 +358,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     }
   } else {
-    // ---------------- softmax and epilogue: thread r owns query row r (TMEM lane r)
-    const int r = tid;
+    // ---------------- softmax and epilogue: warp w owns rows 32 (w % 4) .. + 31 (its
+    // TMEM lane quarter) and columns [32 h, 32 h + 32) of each S tile, h = w / 4; the
+    // two warps of a row quarter agree on the row max through TMEM and an mbarrier
+    // (bounded waits throughout, so a partner that gave up cannot hold a warp forever)
+    const int rg = warp & 3, hc = warp >> 2;
+    const int r = 32 * rg + lane;
     const int qi = i0 + r;
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_row = tmem + ((uint32_t)(rg * 32) << 16);
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -352,33 +373,46 @@ __global__ void __launch_bounds__(kPThreads, 1)
       ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[x], n & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      float s[64];
-      tmem_ld32(t_row + kTmemS + x * kPN, s);
-      tmem_ld32(t_row + kTmemS + x * kPN + 32, s + 32);
+      float s[32];
+      tmem_ld32(t_row + kTmemS + x * kPN + 32 * hc, s);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_empty[x]);  // the S buffer may be overwritten
 
-      const int k0 = j * kPN;
-      const bool need_mask = (k0 + kPN > L) || (p.causal && k0 + kPN - 1 > i0 + off);
+      const int k0 = j * kPN + 32 * hc;  // key of s[0]
+      const bool need_mask = (k0 + 32 > L) || (p.causal && k0 + 31 > i0 + off);
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const int kj = k0 + c;
           if (kj >= L || (p.causal && kj > qi + off)) s[c] = -INFINITY;
         }
       }
       // tile max of the scaled scores: the largest raw score times scale * log2(e)
       // (the scale is positive; a row with no visible key stays at -inf)
-      float mx;
+      float hm;
       {
         float e4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 64; ++c) e4[c & 3] = fmaxf(e4[c & 3], s[c]);
-        mx = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3])) * p.scale_log2;
+        for (int c = 0; c < 32; ++c) e4[c & 3] = fmaxf(e4[c & 3], s[c]);
+        hm = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
       }
+      // exchange the half maxima (parity-buffered TMEM columns), then release S
+      tmem_st1(t_row + kTmemX + 2 * x + hc, hm);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.xm[rg][x]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xm[rg][x], n & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const float hm_other = tmem_ld1(t_row + kTmemX + 2 * x + (1 - hc));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_empty[x]);  // the S buffer may be overwritten
+      const float mx = fmaxf(hm, hm_other) * p.scale_log2;
+
       // lazy max: it moves only by more than 2^8, so probabilities stay below 2^8
+      // (both halves of a row take the same decisions from the same values)
       float alpha = 1.0f;
       if (mx > m_run + 8.0f) {
         alpha = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mx);
@@ -387,11 +421,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
       if (rescale) {
-        // O must hold PV(j - 1) before it is rescaled
+        // O must hold PV(j - 1) before it is rescaled; this warp rescales its half of O
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        for (int c0 = 0; c0 < 256; c0 += 32) {
+        for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
           float o[32];
           tmem_ld32(t_row + kTmemO + c0, o);
           tmem_wait_ld();
@@ -412,7 +446,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const float mneg = (m_run == -INFINITY) ? 0.0f : -m_run;
       float la = 0.0f, lb = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -422,7 +456,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           la += __uint_as_float(w[e] << 16);
           lb += __uint_as_float(w[e] & 0xFFFF0000u);
         }
-        *reinterpret_cast<uint4*>(prow + 16 * (c ^ (r & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
+        const int ch = 4 * hc + c;  // 16-byte chunk of the 128-byte P row
+        *reinterpret_cast<uint4*>(prow + 16 * (ch ^ (r & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       l_run += la + lb;
       fence_async_smem();
@@ -432,7 +467,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     if (!ok) fail();
 
-    // ---- epilogue: O / l, BF16, gate, store
+    // ---- epilogue: O / l, BF16, gate, store (this warp: columns [128 h, 128 h + 128))
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag));
@@ -440,11 +475,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!ok) fail();
       tc_fence_after();
     }
+    // the row's sum is the two halves' sums (exchanged through TMEM like the maxima)
+    if (ok && ntiles > 0) {
+      tmem_st1(t_row + kTmemX + 4 + hc, l_run);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.xl[rg]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xl[rg], 0, abort_flag));
+      if (!ok) fail();
+      tc_fence_after();
+      if (ok) {
+        l_run += tmem_ld1(t_row + kTmemX + 4 + (1 - hc));
+        tmem_wait_ld();
+      }
+    }
     if (ok) {
       const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
       __nv_bfloat16* orow = p.out + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD;
       const unsigned char* grow = sm + kOffK + r * 128;  // gate row r of block c at + c * kQBlk
-      for (int c0 = 0; c0 < 256; c0 += 32) {
+      for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
         float o[32];
         if (ntiles > 0) {
           tmem_ld32(t_row + kTmemO + c0, o);
@@ -477,7 +527,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int e = 0; e < 4; ++e)
           reinterpret_cast<uint4*>(orow + c0)[e] = make_uint4(res[4 * e], res[4 * e + 1], res[4 * e + 2], res[4 * e + 3]);
       }
-      if (p.lse && qi < p.Sq) {
+      if (p.lse && qi < p.Sq && hc == 0) {
         p.lse[((size_t)b * p.Hq + h) * p.Sq + qi] =
             (l_run > 0.0f) ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
       }
