@@ -69,6 +69,7 @@ struct PrepParams {
 };
 
 struct PrefillParams {
+  const __nv_bfloat16* q;      // [B, Sq, Hq, D] (loaded into TMEM by the softmax warps)
   __nv_bfloat16* out;          // [B, Sq, Hq, D]
   float* lse;                  // [B, Hq, Sq] natural log, or nullptr
   const __nv_bfloat16* gate;   // [B, Sq, Hq, D] (read directly only for rows with no visible key)

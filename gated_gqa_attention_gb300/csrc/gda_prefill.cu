@@ -1,5 +1,5 @@
 // gda_prefill.cu -- prefill / extend gated SDPA on sm_103a with tcgen05 MMAs, TMEM
-// accumulators and TMA loads.
+// operands and accumulators, and TMA loads.
 //
 // Computes, per sequence b, query i and query head h (cuDNN FE-OSS "Gated Attention
 // Block (SM107)", Overview stage (4) SDPA O = softmax(Q K^T * scale + mask) V with
@@ -10,27 +10,31 @@
 //   out = RNE_bf16(RNE_bf16(O) * RNE_bf16(sigmoid(gate)))   (the decode path's gate)
 //   lse = natural-log log-sum-exp of the visible scaled scores ([B, Hq, Sq], optional)
 //
-// GB300 design: one CTA per (128-query block, query head, sequence), three roles
-// that hand tiles to each other through mbarriers (full / empty pairs):
-//  * warp 8, TMA producer: the Q tile [128 x 256] once, K and V tiles [64 x 256] into
-//    two-stage rings (cp.async.bulk.tensor, 128-byte swizzle), and at the end the
-//    gate tile into the freed K ring (the gate tile staged by TMA for the epilogue).
+// GB300 design: one CTA per (128-query block, query head, sequence), roles that hand
+// tiles to each other through mbarriers (full / empty pairs, every wait bounded):
+//  * TMEM (512 columns) holds every MMA operand that is not streamed: Q as the A
+//    operand of S = Q K^T (columns [128, 256), BF16 pairs), two S accumulators
+//    (columns [0, 64) and [64, 128), FP32) whose first half is overwritten by P
+//    (BF16 pairs) as the A operand of O += P V, and O (columns [256, 512), FP32).
+//    Shared memory then holds only the streamed K and V tiles, in three-stage rings.
+//  * warps 8 and 10, TMA producers (cp.async.bulk.tensor, 128-byte swizzle): K and V
+//    tiles [64 x 256] into their rings as soon as the MMA that last read a stage has
+//    completed; at the end warp 8 stages the gate tile into the freed K ring.
 //  * warp 9, MMA issuer (one lane; it also owns the TMEM allocation): tcgen05.mma
 //    kind::f16, BF16 operands, FP32 accumulation, M = 128.  S(j) = Q K(j)^T (N = 64,
-//    sixteen k-steps) into one of two TMEM S buffers, then O += P(j-1) V(j-1)
-//    (N = 256, four k-steps) into TMEM columns [256, 512): the tensor core computes
-//    S(j) while the softmax works on tile j - 1.  tcgen05.commit signals completion.
-//  * warps 0-7, softmax and epilogue: the two warps w and w + 4 share query rows
-//    32 w .. + 31 (TMEM lanes), each taking 32 of a tile's 64 scores (tcgen05.ld);
-//    they agree on the row max through TMEM and a named barrier, keep a running
-//    max (moved lazily, by more than 2^8, as the decode kernels do; O in TMEM is
-//    rescaled then) and sum, and write P (BF16) into one of two shared-memory
-//    buffers in the swizzled K-major layout the PV MMA reads.  Epilogue: O row from TMEM, divided by the sum,
-//    rounded to BF16, gated with the BF16 sigmoid of the staged gate row (from a
-//    per-device table of all 65 536 BF16 sigmoids), stored.
-// Every wait is bounded; on a timeout the CTA records kErrTimeout, every role stops,
-// waits (bounded) for the copies and MMAs it started, the TMEM is freed and the CTA
-// returns.  TMEM accesses stay warp-convergent (decisions combined with __all_sync).
+//    sixteen k-steps, A from TMEM), then O += P(j-1) V(j-1) (N = 256, four k-steps, A
+//    from TMEM): the tensor core computes S(j) while the softmax works on tile j - 1.
+//  * warps 0-7, softmax and epilogue: warps w and w + 4 share query rows 32 w .. + 31
+//    (TMEM lanes), each reading 32 of a tile's 64 scores (tcgen05.ld); they first
+//    write Q into TMEM, then per tile agree on the row max through shared memory,
+//    keep a running max (moved lazily, by more than 2^8, as the decode kernels do;
+//    O in TMEM is rescaled then) and sum, and write P (BF16) over their S buffer
+//    with tcgen05.st.  Epilogue: O row from TMEM, divided by the sum, rounded to
+//    BF16, gated with the BF16 sigmoid of the staged gate row (an SFU fast path,
+//    and a per-device table of all 65 536 BF16 sigmoids near rounding ties), stored.
+// On a timeout the CTA records kErrTimeout, every role stops, waits (bounded) for the
+// copies and MMAs it started, the TMEM is freed and the CTA returns.  TMEM accesses
+// stay warp-convergent (decisions combined with __all_sync).
 #include <cuda.h>
 
 #include "gda_device.cuh"
@@ -42,25 +46,28 @@ namespace {
 
 constexpr int kPM = 128;            // query rows per CTA (MMA M)
 constexpr int kPN = 64;             // keys per tile (MMA N of S)
-constexpr int kSoftmaxWarps = 8;   // warps 0-7: softmax and epilogue; warp w: rows 32 (w % 4) .., column half w / 4
-constexpr int kLoadWarp = 8;       // TMA producer
-constexpr int kMmaWarp = 9;        // MMA issuer; allocates and frees TMEM
-constexpr int kPThreads = 10 * 32;
+constexpr int kKST = 3;             // K ring stages
+constexpr int kVST = 3;             // V ring stages
+constexpr int kSoftmaxWarps = 8;    // warps 0-7: softmax and epilogue
+constexpr int kLoadWarp = 8;        // TMA producer: K tiles, then the gate tile
+constexpr int kMmaWarp = 9;         // MMA issuer; allocates and frees TMEM
+constexpr int kLoadWarpV = 10;      // TMA producer: V tiles
+constexpr int kPThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;      // S accumulators: columns [0, 64) and [64, 128)
-constexpr uint32_t kTmemX = 128;    // exchange between a row's two halves: [128, 134)
-constexpr uint32_t kTmemO = 256;    // O accumulator columns [256, 512)
+constexpr uint32_t kTmemS = 0;      // S / P buffers: columns [0, 64) and [64, 128)
+constexpr uint32_t kTmemQ = 128;    // Q: columns [128, 256), two BF16 per column
+constexpr uint32_t kTmemO = 256;    // O accumulator: columns [256, 512)
 
 // shared memory plan (offsets from a 1024-byte aligned base)
-constexpr uint32_t kQBlk = kPM * 128;             // one 64-column block of Q: 16 KiB
+constexpr uint32_t kQBlk = kPM * 128;             // one 64-column block of a 128-row tile (the gate): 16 KiB
 constexpr uint32_t kKVBlk = kPN * 128;            // one 64-column block of a K or V tile: 8 KiB
-constexpr uint32_t kOffQ = 0;                     // 4 blocks, 64 KiB
-constexpr uint32_t kOffK = kOffQ + 4 * kQBlk;     // 2 buffers x 4 blocks, 64 KiB
-constexpr uint32_t kOffV = kOffK + 8 * kKVBlk;    // 2 buffers x 4 blocks, 64 KiB
-constexpr uint32_t kPBuf = kPM * 128;             // one P tile: 128 rows x 128 B, 16 KiB
-constexpr uint32_t kOffP = kOffV + 8 * kKVBlk;    // 2 buffers, 32 KiB
-constexpr uint32_t kOffBar = kOffP + 2 * kPBuf;   // mbarriers and the TMEM address
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
+constexpr uint32_t kKVTile = 4 * kKVBlk;          // one K or V tile: 32 KiB
+constexpr uint32_t kOffK = 0;                     // K ring (the gate tile reuses its first 64 KiB)
+constexpr uint32_t kOffV = kOffK + kKST * kKVTile; // V ring
+constexpr uint32_t kOffX = kOffV + kVST * kKVTile; // row max [parity][half][row] and sum [half][row] exchange
+constexpr uint32_t kOffBar = kOffX + 3072;         // mbarriers and the TMEM address
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
+static_assert(kKST * kKVTile >= 4 * kQBlk, "the gate tile fits the K ring");
 
 // ---- PTX wrappers (tcgen05, TMA) ----
 
@@ -76,15 +83,15 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+// D (TMEM) += A (TMEM) * B (shared memory descriptor)
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -121,13 +128,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
-  uint32_t r;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
-  return __uint_as_float(r);
-}
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v)) : "memory");
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -157,6 +163,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// TMA: a 5-D tile into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (descriptor version 1):
 // start address, leading and stride byte offsets, all encoded >> 4.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -181,30 +197,53 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
 // Sq * Hq * D elements, where one table load is far cheaper than the computation.
 __device__ uint16_t g_sigmoid_table[65536];
 
+// RNE_bf16(sigmoid(g)) for the epilogue: for |g| <= 16 the float sigmoid from the SFU
+// (2^x and 1/x approximations) is within 24 float ulp of the real value (argument
+// rounding |g| * 2^-24 relative, 2^x ~2^-22, 1/x and the add ~2^-23), so its BF16
+// rounding is the correct one unless the low 16 bits lie within 32 of the tie; those
+// codes, |g| > 16 and NaN read the table.  Exhaustively checked against the FP64
+// oracle on all 65 536 codes through the fused epilogue.
+__device__ __forceinline__ uint16_t sigmoid_bf16_fast(uint16_t gbits) {
+  const float g = __uint_as_float((uint32_t)gbits << 16);
+  const float a = fabsf(g);
+  if (a <= 16.0f) {
+    // e = exp(-|g|) in (0, 1]: sigmoid(g) = 1 / (1 + e) for g >= 0, e / (1 + e) for g < 0
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-a * 1.44269504088896341f));
+    const float den = 1.0f + e;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(den));
+    const float sg = (g >= 0.0f) ? r : e * r;
+    const uint32_t low = __float_as_uint(sg) & 0xFFFFu;
+    if (low - 0x7FE0u > 0x40u) return __bfloat16_as_ushort(__float2bfloat16_rn(sg));
+  }
+  return __ldg(g_sigmoid_table + gbits);
+}
+
 __global__ void sigmoid_table_kernel() {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < 65536) g_sigmoid_table[i] = sigmoid_bf16((uint16_t)i);
 }
 
 struct PrefillBars {
-  uint64_t q, g;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
-  uint64_t xm[4][2];  // per row quarter and tile parity: both halves stored their max
-  uint64_t xl[4];     // per row quarter: both halves stored their sum
+  uint64_t qf, g;                                   // Q in TMEM (8 softmax warps); gate tile landed
+  uint64_t k_full[kKST], k_empty[kKST], v_full[kVST], v_empty[kVST];
+  uint64_t s_full[2], p_full[2], p_empty[2];        // per S / P buffer
+  uint64_t xm[4][2];                                // per row quarter and tile parity: both maxima stored
+  uint64_t xl[4];                                   // per row quarter: both sums stored
   uint32_t tmem;
   int abort;
 };
-static_assert(sizeof(PrefillBars) <= 256, "barrier block");
+static_assert(sizeof(PrefillBars) <= 512, "barrier block");
 
 }  // namespace
 
 __global__ void __launch_bounds__(kPThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, PrefillParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                   const __grid_constant__ CUtensorMap tg, PrefillParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PrefillBars& bars = *reinterpret_cast<PrefillBars*>(sm + kOffBar);
+  float* xbuf = reinterpret_cast<float*>(sm + kOffX);  // [parity][half][row]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqb = (p.Sq + kPM - 1) / kPM;
   const int qb = nqb - 1 - (int)blockIdx.x;  // the longest causal blocks first
@@ -218,15 +257,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int ntiles = (last_key >= 0) ? (last_key / kPN + 1) : 0;
 
   if (tid == 0) {
-    mbar_init(&bars.q, 1);
+    mbar_init(&bars.qf, kSoftmaxWarps);
     mbar_init(&bars.g, 1);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kKST; ++x) {
       mbar_init(&bars.k_full[x], 1);
       mbar_init(&bars.k_empty[x], 1);
+    }
+    for (int x = 0; x < kVST; ++x) {
       mbar_init(&bars.v_full[x], 1);
       mbar_init(&bars.v_empty[x], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.s_full[x], 1);
-      mbar_init(&bars.s_empty[x], kSoftmaxWarps);
       mbar_init(&bars.p_full[x], kSoftmaxWarps);
       mbar_init(&bars.p_empty[x], 1);
     }
@@ -252,36 +294,33 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bars.abort = 1;
   };
 
-  if (warp == kLoadWarp) {
-    // ---------------- TMA producer (one lane)
+  if (warp == kLoadWarp || warp == kLoadWarpV) {
+    // ---------------- TMA producers (one lane each): K tiles (then the gate tile) from
+    // warp kLoadWarp, V tiles from warp kLoadWarpV, each into its own ring as soon as
+    // the MMA that last read the stage has completed
+    const bool is_k = warp == kLoadWarp;
     if (lane == 0 && ntiles > 0) {
-      int arm_q = 0, arm_g = 0, arm_k[2] = {0, 0}, arm_v[2] = {0, 0};
+      const int nst = is_k ? kKST : kVST;
+      int arm_g = 0, arm[3] = {0, 0, 0};
+      uint64_t* full = is_k ? bars.k_full : bars.v_full;
+      uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
+      const CUtensorMap* map = is_k ? &tk : &tv;
+      const uint32_t base = is_k ? kOffK : kOffV;
       bool ok = true;
-      ++arm_q;
-      mbar_arrive_expect_tx(&bars.q, 4 * kQBlk);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffQ + c * kQBlk, &tq, 64 * c, h, i0, b, &bars.q);
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int x = j & 1, n = j >> 1;
-        // K(j) once S(j - 2) has read the buffer, V(j) once PV(j - 2) has
-        if (j >= 2 && !mbar_wait(&bars.k_empty[x], (n - 1) & 1, abort_flag)) { ok = false; break; }
-        ++arm_k[x];
-        mbar_arrive_expect_tx(&bars.k_full[x], 4 * kKVBlk);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tma_load_4d(sm + kOffK + (x * 4 + c) * kKVBlk, &tk, 64 * c, kvh, j * kPN, b, &bars.k_full[x]);
-        if (j >= 2 && !mbar_wait(&bars.v_empty[x], (n - 1) & 1, abort_flag)) { ok = false; break; }
-        ++arm_v[x];
-        mbar_arrive_expect_tx(&bars.v_full[x], 4 * kKVBlk);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tma_load_4d(sm + kOffV + (x * 4 + c) * kKVBlk, &tv, 64 * c, kvh, j * kPN, b, &bars.v_full[x]);
+        const int x = j % nst, n = j / nst;
+        // stage x is free once the MMA of tile j - nst (S for K, PV for V) has completed
+        if (j >= nst && !mbar_wait(&empty[x], (n - 1) & 1, abort_flag)) { ok = false; break; }
+        ++arm[x];
+        mbar_arrive_expect_tx(&full[x], kKVTile);
+        // one copy of the whole tile: box {64 elements, 64 rows, 4 column blocks}
+        tma_load_5d(sm + base + x * kKVTile, map, 0, j * kPN, 0, kvh, b, &full[x]);
       }
-      if (ok && p.fuse_gate) {
-        // the gate tile goes into the K ring once the last two S products have read it
+      if (ok && is_k && p.fuse_gate) {
+        // the gate tile goes into the K ring once the last S product (and so every
+        // earlier one: MMAs complete in order) has read it
         const int jl = ntiles - 1;
-        if (!mbar_wait(&bars.k_empty[jl & 1], (jl >> 1) & 1, abort_flag)) ok = false;
-        if (ok && ntiles >= 2 && !mbar_wait(&bars.k_empty[(jl - 1) & 1], ((jl - 1) >> 1) & 1, abort_flag)) ok = false;
+        if (!mbar_wait(&bars.k_empty[jl % kKST], (jl / kKST) & 1, abort_flag)) ok = false;
         if (ok) {
           ++arm_g;
           mbar_arrive_expect_tx(&bars.g, 4 * kQBlk);
@@ -291,62 +330,57 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (!ok) {
         fail();
-        // wait (bounded) for every copy this CTA started before its memory goes away
+        // wait (bounded) for every copy this producer started before its memory goes away
         int dummy = 0;
         volatile int* none = &dummy;
-        if (arm_q > 0) mbar_wait(&bars.q, (arm_q - 1) & 1, none);
         if (arm_g > 0) mbar_wait(&bars.g, (arm_g - 1) & 1, none);
-        for (int x = 0; x < 2; ++x) {
-          if (arm_k[x] > 0) mbar_wait(&bars.k_full[x], (arm_k[x] - 1) & 1, none);
-          if (arm_v[x] > 0) mbar_wait(&bars.v_full[x], (arm_v[x] - 1) & 1, none);
-        }
+        for (int x = 0; x < nst; ++x)
+          if (arm[x] > 0) mbar_wait(&full[x], (arm[x] - 1) & 1, none);
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (one lane): S(j) runs while the softmax works on tile j - 1
     if (lane == 0 && ntiles > 0) {
-      const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV),
-                     sP = smem_u32(sm + kOffP);
+      const uint32_t sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV);
       const uint32_t idS = idesc_bf16(kPM, kPN, 0), idO = idesc_bf16(kPM, 256, 1);
       uint64_t* last_bar = nullptr;  // the barrier of the last commit and its phase parity
       int last_par = 0;
-      bool ok = mbar_wait(&bars.q, 0, abort_flag);
+      bool ok = mbar_wait(&bars.qf, 0, abort_flag);
       for (int j = 0; j <= ntiles && ok; ++j) {
         if (j < ntiles) {
-          const int x = j & 1, n = j >> 1;
-          ok = mbar_wait(&bars.k_full[x], n & 1, abort_flag);
-          if (ok && j >= 2) ok = mbar_wait(&bars.s_empty[x], (n - 1) & 1, abort_flag);
+          const int ks = j % kKST, sb = j & 1;
+          ok = mbar_wait(&bars.k_full[ks], (j / kKST) & 1, abort_flag);
+          // S buffer sb held P(j - 2): PV(j - 2) must have read it
+          if (ok && j >= 2) ok = mbar_wait(&bars.p_empty[sb], ((j - 2) >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sK + (x * 4 + (kk >> 2)) * kKVBlk + (kk & 3) * 32, 16, 1024);
-            umma_bf16(tmem + kTmemS + x * kPN, ad, bd, idS, kk > 0 ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(sK + ks * kKVTile + (kk >> 2) * kKVBlk + (kk & 3) * 32, 16, 1024);
+            umma_bf16_ts(tmem + kTmemS + sb * kPN, tmem + kTmemQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&bars.s_full[x]);
-          umma_commit(&bars.k_empty[x]);
-          last_bar = &bars.k_empty[x];
-          last_par = n & 1;
+          umma_commit(&bars.s_full[sb]);
+          umma_commit(&bars.k_empty[ks]);
+          last_bar = &bars.k_empty[ks];
+          last_par = (j / kKST) & 1;
         }
         if (j >= 1) {
-          const int jp = j - 1, y = jp & 1, ny = jp >> 1;
-          ok = mbar_wait(&bars.p_full[y], ny & 1, abort_flag);
-          if (ok) ok = mbar_wait(&bars.v_full[y], ny & 1, abort_flag);
+          const int jp = j - 1, pb = jp & 1, vs = jp % kVST;
+          ok = mbar_wait(&bars.p_full[pb], (jp >> 1) & 1, abort_flag);
+          if (ok) ok = mbar_wait(&bars.v_full[vs], (jp / kVST) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(sP + y * kPBuf + kk * 32, 16, 1024);
             // V is MN-major (dims contiguous): LBO = stride between 64-dim blocks,
             // SBO = stride between groups of 8 key rows; k-step kk = key rows 16 kk ..
-            const uint64_t bd = sdesc_sw128(sV + y * 4 * kKVBlk + kk * 16 * 128, kKVBlk, 1024);
-            umma_bf16(tmem + kTmemO, ad, bd, idO, (jp > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(sV + vs * kKVTile + kk * 16 * 128, kKVBlk, 1024);
+            umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kPN + 8 * kk, bd, idO, (jp > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&bars.p_empty[y]);
-          umma_commit(&bars.v_empty[y]);
-          last_bar = &bars.v_empty[y];
-          last_par = ny & 1;
+          umma_commit(&bars.p_empty[pb]);
+          umma_commit(&bars.v_empty[vs]);
+          last_bar = &bars.v_empty[vs];
+          last_par = (jp / kVST) & 1;
         }
       }
       if (!ok) {
@@ -359,22 +393,45 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
   } else {
     // ---------------- softmax and epilogue: warp w owns rows 32 (w % 4) .. + 31 (its
-    // TMEM lane quarter) and columns [32 h, 32 h + 32) of each S tile, h = w / 4; the
-    // two warps of a row quarter agree on the row max through TMEM and an mbarrier
-    // (bounded waits throughout, so a partner that gave up cannot hold a warp forever)
+    // TMEM lane quarter) and keys [32 h, 32 h + 32) of each tile, h = w / 4
     const int rg = warp & 3, hc = warp >> 2;
     const int r = 32 * rg + lane;
     const int qi = i0 + r;
     const uint32_t t_row = tmem + ((uint32_t)(rg * 32) << 16);
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
+
+    // Q row r, elements [128 h, 128 h + 128), into TMEM columns kTmemQ + 64 h ..
+    // (two BF16 per column, the lower element in the lower half); rows past Sq are 0
+    if (ntiles > 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.Sq + min(qi, p.Sq - 1)) * p.Hq + h) * kD + 128 * hc);
+#pragma unroll
+      for (int c0 = 0; c0 < 2; ++c0) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = (qi < p.Sq) ? __ldg(src + 8 * c0 + i) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        tmem_st16(t_row + kTmemQ + 64 * hc + 32 * c0, w);
+        tmem_st16(t_row + kTmemQ + 64 * hc + 32 * c0 + 16, w + 16);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.qf);
+    }
+
     for (int j = 0; j < ntiles; ++j) {
-      const int x = j & 1, n = j >> 1;
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[x], n & 1, abort_flag));
+      const int sb = j & 1, ns = j >> 1;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[sb], ns & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       float s[32];
-      tmem_ld32(t_row + kTmemS + x * kPN + 32 * hc, s);
+      tmem_ld32(t_row + kTmemS + sb * kPN + 32 * hc, s);
       tmem_wait_ld();
 
       const int k0 = j * kPN + 32 * hc;  // key of s[0]
@@ -386,8 +443,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (kj >= L || (p.causal && kj > qi + off)) s[c] = -INFINITY;
         }
       }
-      // tile max of the scaled scores: the largest raw score times scale * log2(e)
-      // (the scale is positive; a row with no visible key stays at -inf)
       float hm;
       {
         float e4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -395,21 +450,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int c = 0; c < 32; ++c) e4[c & 3] = fmaxf(e4[c & 3], s[c]);
         hm = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
       }
-      // exchange the half maxima (parity-buffered TMEM columns), then release S
-      tmem_st1(t_row + kTmemX + 2 * x + hc, hm);
-      tmem_wait_st();
-      tc_fence_before();
+      // the two halves of the row agree on the tile max (parity-buffered shared slots);
+      // after this both have read their S, so P may overwrite it
+      xbuf[(sb * 2 + hc) * kPM + r] = hm;
+      tc_fence_before();  // this warp's S reads are ordered before the partner's P writes
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.xm[rg][x]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xm[rg][x], n & 1, abort_flag));
+      if (lane == 0) mbar_arrive(&bars.xm[rg][sb]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xm[rg][sb], ns & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const float hm_other = tmem_ld1(t_row + kTmemX + 2 * x + (1 - hc));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_empty[x]);  // the S buffer may be overwritten
-      const float mx = fmaxf(hm, hm_other) * p.scale_log2;
+      const float mx = fmaxf(hm, xbuf[(sb * 2 + (1 - hc)) * kPM + r]) * p.scale_log2;
 
       // lazy max: it moves only by more than 2^8, so probabilities stay below 2^8
       // (both halves of a row take the same decisions from the same values)
@@ -419,8 +469,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         l_run *= alpha;
         m_run = mx;
       }
-      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
-      if (rescale) {
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // O must hold PV(j - 1) before it is rescaled; this warp rescales its half of O
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
         if (!ok) break;
@@ -435,35 +484,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         tmem_wait_st();
       }
-      // P buffer x is free once PV(j - 2) has read it
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[x], (n - 1) & 1, abort_flag));
-        if (!ok) break;
-      }
-      unsigned char* prow = sm + kOffP + x * kPBuf + r * 128;
       // p = 2^(s * scale_log2 - m): one FFMA and one SFU op per score (a masked score
-      // gives 2^-inf = 0; a row with no visible key yet uses m = 0)
+      // gives 2^-inf = 0; a row with no visible key yet uses m = 0); P (BF16 pairs)
+      // over the first half of the S buffer: keys 32 h .. at columns 16 h ..
       const float mneg = (m_run == -INFINITY) ? 0.0f : -m_run;
+      uint32_t w[16];
       float la = 0.0f, lb = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2_approx(fmaf(s[8 * c + 2 * e], p.scale_log2, mneg));
-          const float p1 = ex2_approx(fmaf(s[8 * c + 2 * e + 1], p.scale_log2, mneg));
-          w[e] = bf16x2_rn(p0, p1);
-          la += __uint_as_float(w[e] << 16);
-          lb += __uint_as_float(w[e] & 0xFFFF0000u);
-        }
-        const int ch = 4 * hc + c;  // 16-byte chunk of the 128-byte P row
-        *reinterpret_cast<uint4*>(prow + 16 * (ch ^ (r & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int e = 0; e < 16; ++e) {
+        const float p0 = ex2_approx(fmaf(s[2 * e], p.scale_log2, mneg));
+        const float p1 = ex2_approx(fmaf(s[2 * e + 1], p.scale_log2, mneg));
+        w[e] = bf16x2_rn(p0, p1);
+        la += __uint_as_float(w[e] << 16);
+        lb += __uint_as_float(w[e] & 0xFFFF0000u);
       }
       l_run += la + lb;
-      fence_async_smem();
+      tmem_st16(t_row + kTmemS + sb * kPN + 16 * hc, w);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full[x]);
+      if (lane == 0) mbar_arrive(&bars.p_full[sb]);
     }
     if (!ok) fail();
 
@@ -471,24 +511,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag));
+      // the row's sum is the two halves' sums
+      if (ok) {
+        xbuf[(4 + hc) * kPM + r] = l_run;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.xl[rg]);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.xl[rg], 0, abort_flag));
+        if (ok) l_run += xbuf[(4 + (1 - hc)) * kPM + r];
+      }
       if (ok && p.fuse_gate) ok = __all_sync(0xffffffffu, mbar_wait(&bars.g, 0, abort_flag));
       if (!ok) fail();
       tc_fence_after();
-    }
-    // the row's sum is the two halves' sums (exchanged through TMEM like the maxima)
-    if (ok && ntiles > 0) {
-      tmem_st1(t_row + kTmemX + 4 + hc, l_run);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.xl[rg]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xl[rg], 0, abort_flag));
-      if (!ok) fail();
-      tc_fence_after();
-      if (ok) {
-        l_run += tmem_ld1(t_row + kTmemX + 4 + (1 - hc));
-        tmem_wait_ld();
-      }
     }
     if (ok) {
       const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
@@ -518,7 +551,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             } else {
               g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
             }
-            const uint16_t s0 = __ldg(g_sigmoid_table + (g2 & 0xFFFFu)), s1 = __ldg(g_sigmoid_table + (g2 >> 16));
+            const uint16_t s0 = sigmoid_bf16_fast((uint16_t)(g2 & 0xFFFFu)), s1 = sigmoid_bf16_fast((uint16_t)(g2 >> 16));
             v = (uint32_t)gate_product_bf16(ob0, s0) | ((uint32_t)gate_product_bf16(ob1, s1) << 16);
           }
           res[e] = v;
@@ -578,14 +611,29 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K or V [B, S, H, D] BF16 as a 5-D tensor {64 elements, S, 4 column blocks, H, B} with
+// box {64, rows, 4, 1, 1}: one copy fills a tile laid out [block][row][128 B] (128-byte
+// swizzle), the layout the MMA descriptors read
+bool make_map_kv(CUtensorMap* m, const void* base, int B, int S, int H, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[5] = {64, (cuuint64_t)S, 4, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[4] = {(cuuint64_t)H * kD * 2, 128, (cuuint64_t)kD * 2, (cuuint64_t)S * H * kD * 2};
+  const cuuint32_t box[5] = {64, (cuuint32_t)rows, 4, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k, const void* v, const void* gate,
                            cudaStream_t stream) {
-  CUtensorMap tq, tk, tv, tg;
+  CUtensorMap tk, tv, tg;
   // S = 0 still needs a valid map: use extent 1 (nothing is loaded then)
-  if (!make_map(&tq, q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM) || !make_map(&tk, k, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
-      !make_map(&tv, v, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
+  if (!make_map_kv(&tk, k, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
+      !make_map_kv(&tv, v, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
       !make_map(&tg, gate ? gate : q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
@@ -603,7 +651,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k,
     attr_set[dev] = true;
   }
   const dim3 grid((unsigned)((p.Sq + kPM - 1) / kPM), (unsigned)p.Hq, (unsigned)p.B);
-  prefill_kernel<<<grid, kPThreads, kSmemBytes, stream>>>(tq, tk, tv, tg, p);
+  prefill_kernel<<<grid, kPThreads, kSmemBytes, stream>>>(tk, tv, tg, p);
   return cudaGetLastError();
 }
 
