@@ -31,7 +31,8 @@
 //    O in TMEM is rescaled then) and sum, and write P (BF16) over their S buffer
 //    with tcgen05.st.  Epilogue: O row from TMEM, divided by the sum, rounded to
 //    BF16, gated with the BF16 sigmoid of the staged gate row (an SFU fast path,
-//    and a per-device table of all 65 536 BF16 sigmoids near rounding ties), stored.
+//    and a per-device table of all 65 536 BF16 sigmoids near rounding ties), staged
+//    in shared memory and written with TMA stores.
 // On a timeout the CTA records kErrTimeout, every role stops, waits (bounded) for the
 // copies and MMAs it started, the TMEM is freed and the CTA returns.  TMEM accesses
 // stay warp-convergent (decisions combined with __all_sync).
@@ -46,28 +47,30 @@ namespace {
 
 constexpr int kPM = 128;            // query rows per CTA (MMA M)
 constexpr int kPN = 64;             // keys per tile (MMA N of S)
-constexpr int kKST = 3;             // K ring stages
-constexpr int kVST = 3;             // V ring stages
+constexpr int kKST = 2;             // K ring stages
+constexpr int kVST = 2;             // V ring stages
+constexpr int kNSB = 4;             // S / P buffers in TMEM
 constexpr int kSoftmaxWarps = 8;    // warps 0-7: softmax and epilogue
 constexpr int kLoadWarp = 8;        // TMA producer: K tiles, then the gate tile
 constexpr int kMmaWarp = 9;         // MMA issuer; allocates and frees TMEM
 constexpr int kLoadWarpV = 10;      // TMA producer: V tiles
 constexpr int kPThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;      // S / P buffers: columns [0, 64) and [64, 128)
-constexpr uint32_t kTmemQ = 128;    // Q: columns [128, 256), two BF16 per column
+constexpr uint32_t kTmemS = 0;      // S / P buffers: columns [64 n, 64 n + 64), n < kNSB
 constexpr uint32_t kTmemO = 256;    // O accumulator: columns [256, 512)
 
 // shared memory plan (offsets from a 1024-byte aligned base)
 constexpr uint32_t kQBlk = kPM * 128;             // one 64-column block of a 128-row tile (the gate): 16 KiB
 constexpr uint32_t kKVBlk = kPN * 128;            // one 64-column block of a K or V tile: 8 KiB
 constexpr uint32_t kKVTile = 4 * kKVBlk;          // one K or V tile: 32 KiB
-constexpr uint32_t kOffK = 0;                     // K ring (the gate tile reuses its first 64 KiB)
-constexpr uint32_t kOffV = kOffK + kKST * kKVTile; // V ring
+constexpr uint32_t kOffQ = 0;                      // Q tile [4 blocks][128 rows][128 B]; the gate tile at the end
+constexpr uint32_t kOffK = kOffQ + 4 * kQBlk;      // K ring
+constexpr uint32_t kOffV = kOffK + kKST * kKVTile; // V ring; the output tile is staged here at the end
 constexpr uint32_t kOffX = kOffV + kVST * kKVTile; // row max [parity][half][row] and sum [half][row] exchange
 constexpr uint32_t kOffBar = kOffX + 3072;         // mbarriers and the TMEM address
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
-static_assert(kKST * kKVTile >= 4 * kQBlk, "the gate tile fits the K ring");
+static_assert(kVST * kKVTile >= 4 * kQBlk, "the output tile fits the V ring");
+static_assert(kNSB * kPN <= kTmemO, "S / P buffers below O");
 
 // ---- PTX wrappers (tcgen05, TMA) ----
 
@@ -83,6 +86,17 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (TMEM) += A (shared memory descriptor) * B (shared memory descriptor)
+__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 // D (TMEM) += A (TMEM) * B (shared memory descriptor)
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -153,16 +167,6 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   return d;
 }
 
-// TMA: a 4-D tile (x innermost) into shared memory, completing on `bar`
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-      "%5}], [%6];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // TMA: a 5-D tile into shared memory, completing on `bar`
 __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
                                             uint64_t* bar) {
@@ -172,6 +176,20 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
       : "memory");
 }
+
+// TMA: a 4-D tile from shared memory to global (rows past the tensor's end are
+// dropped); completion tracked by the bulk-group mechanism
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int x, int y, int z, int w, const void* src) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (descriptor version 1):
 // start address, leading and stride byte offsets, all encoded >> 4.
@@ -219,17 +237,33 @@ __device__ __forceinline__ uint16_t sigmoid_bf16_fast(uint16_t gbits) {
   return __ldg(g_sigmoid_table + gbits);
 }
 
+// RNE_bf16(o * s) for BF16 o and s, as gate_product_bf16 computes it, with the exact
+// double-precision path for products below the float normal range kept out of line:
+// inlined, the compiler may evaluate it for every element, and FP64 on this part is
+// far slower than the rest of the epilogue.
+__device__ __noinline__ uint16_t gate_product_tiny(float o, float s) {
+  return bf16_rne_from_double((double)o * (double)s);
+}
+__device__ __forceinline__ uint16_t gate_product_fast(uint16_t obits, uint16_t sbits) {
+  const float o = __uint_as_float((uint32_t)obits << 16);
+  const float s = __uint_as_float((uint32_t)sbits << 16);
+  const float p = __fmul_rn(o, s);
+  if (fabsf(p) < 1.17549435e-38f && p != 0.0f) return gate_product_tiny(o, s);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(p));
+}
+
 __global__ void sigmoid_table_kernel() {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < 65536) g_sigmoid_table[i] = sigmoid_bf16((uint16_t)i);
 }
 
 struct PrefillBars {
-  uint64_t qf, g;                                   // Q in TMEM (8 softmax warps); gate tile landed
+  uint64_t qf, g;                                   // Q tile landed; gate tile landed
   uint64_t k_full[kKST], k_empty[kKST], v_full[kVST], v_empty[kVST];
-  uint64_t s_full[2], p_full[2], p_empty[2];        // per S / P buffer
+  uint64_t s_full[kNSB], p_full[kNSB], p_empty[kNSB];  // per S / P buffer
   uint64_t xm[4][2];                                // per row quarter and tile parity: both maxima stored
   uint64_t xl[4];                                   // per row quarter: both sums stored
+  uint64_t ost;                                     // output tile staged (8 softmax warps)
   uint32_t tmem;
   int abort;
 };
@@ -238,8 +272,10 @@ static_assert(sizeof(PrefillBars) <= 512, "barrier block");
 }  // namespace
 
 __global__ void __launch_bounds__(kPThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                   const __grid_constant__ CUtensorMap tg, PrefillParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv,
+                   const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap to,
+                   PrefillParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PrefillBars& bars = *reinterpret_cast<PrefillBars*>(sm + kOffBar);
@@ -257,7 +293,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int ntiles = (last_key >= 0) ? (last_key / kPN + 1) : 0;
 
   if (tid == 0) {
-    mbar_init(&bars.qf, kSoftmaxWarps);
+    mbar_init(&bars.qf, 1);
     mbar_init(&bars.g, 1);
     for (int x = 0; x < kKST; ++x) {
       mbar_init(&bars.k_full[x], 1);
@@ -267,7 +303,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&bars.v_full[x], 1);
       mbar_init(&bars.v_empty[x], 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kNSB; ++x) {
       mbar_init(&bars.s_full[x], 1);
       mbar_init(&bars.p_full[x], kSoftmaxWarps);
       mbar_init(&bars.p_empty[x], 1);
@@ -276,6 +312,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&bars.xm[q4][0], 2);
       mbar_init(&bars.xm[q4][1], 2);
       mbar_init(&bars.xl[q4], 2);
+    mbar_init(&bars.ost, kSoftmaxWarps);
     }
     bars.abort = 0;
     fence_mbar_init();
@@ -307,6 +344,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const CUtensorMap* map = is_k ? &tk : &tv;
       const uint32_t base = is_k ? kOffK : kOffV;
       bool ok = true;
+      if (is_k) {
+        ++arm_g;  // (the Q copy shares the gate's bookkeeping slot: both land in the Q buffer)
+        mbar_arrive_expect_tx(&bars.qf, 4 * kQBlk);
+        tma_load_5d(sm + kOffQ, &tq, 0, i0, 0, h, b, &bars.qf);
+      }
       for (int j = 0; j < ntiles && ok; ++j) {
         const int x = j % nst, n = j / nst;
         // stage x is free once the MMA of tile j - nst (S for K, PV for V) has completed
@@ -316,16 +358,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // one copy of the whole tile: box {64 elements, 64 rows, 4 column blocks}
         tma_load_5d(sm + base + x * kKVTile, map, 0, j * kPN, 0, kvh, b, &full[x]);
       }
+      int arm_gate = 0;
       if (ok && is_k && p.fuse_gate) {
-        // the gate tile goes into the K ring once the last S product (and so every
-        // earlier one: MMAs complete in order) has read it
+        // the gate tile goes into the Q buffer once the last S product (and so every
+        // earlier one: MMAs complete in order) has read Q
         const int jl = ntiles - 1;
         if (!mbar_wait(&bars.k_empty[jl % kKST], (jl / kKST) & 1, abort_flag)) ok = false;
         if (ok) {
-          ++arm_g;
+          ++arm_gate;
           mbar_arrive_expect_tx(&bars.g, 4 * kQBlk);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tma_load_4d(sm + kOffK + c * kQBlk, &tg, 64 * c, h, i0, b, &bars.g);
+          tma_load_5d(sm + kOffQ, &tg, 0, i0, 0, h, b, &bars.g);
         }
       }
       if (!ok) {
@@ -333,55 +375,61 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // wait (bounded) for every copy this producer started before its memory goes away
         int dummy = 0;
         volatile int* none = &dummy;
-        if (arm_g > 0) mbar_wait(&bars.g, (arm_g - 1) & 1, none);
+        if (arm_g > 0) mbar_wait(&bars.qf, 0, none);
+        if (arm_gate > 0) mbar_wait(&bars.g, 0, none);
         for (int x = 0; x < nst; ++x)
           if (arm[x] > 0) mbar_wait(&full[x], (arm[x] - 1) & 1, none);
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer (one lane): S(j) runs while the softmax works on tile j - 1
+    // ---------------- MMA issuer (one lane): S runs two tiles ahead of PV, so the
+    // tensor core has S(j + 1), S(j + 2) queued while the softmax works on tile j
     if (lane == 0 && ntiles > 0) {
-      const uint32_t sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV);
+      const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV);
       const uint32_t idS = idesc_bf16(kPM, kPN, 0), idO = idesc_bf16(kPM, 256, 1);
       uint64_t* last_bar = nullptr;  // the barrier of the last commit and its phase parity
       int last_par = 0;
+      auto issue_s = [&](int j) -> bool {
+        const int ks = j % kKST, sb = j % kNSB;
+        if (!mbar_wait(&bars.k_full[ks], (j / kKST) & 1, abort_flag)) return false;
+        // S buffer sb held P(j - kNSB): PV(j - kNSB) must have read it
+        if (j >= kNSB && !mbar_wait(&bars.p_empty[sb], ((j / kNSB) - 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + ks * kKVTile + (kk >> 2) * kKVBlk + (kk & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem + kTmemS + sb * kPN, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars.s_full[sb]);
+        umma_commit(&bars.k_empty[ks]);
+        last_bar = &bars.k_empty[ks];
+        last_par = (j / kKST) & 1;
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int pb = j % kNSB, vs = j % kVST;
+        if (!mbar_wait(&bars.p_full[pb], (j / kNSB) & 1, abort_flag)) return false;
+        if (!mbar_wait(&bars.v_full[vs], (j / kVST) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // V is MN-major (dims contiguous): LBO = stride between 64-dim blocks,
+          // SBO = stride between groups of 8 key rows; k-step kk = key rows 16 kk ..
+          const uint64_t bd = sdesc_sw128(sV + vs * kKVTile + kk * 16 * 128, kKVBlk, 1024);
+          umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kPN + 8 * kk, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars.p_empty[pb]);
+        umma_commit(&bars.v_empty[vs]);
+        last_bar = &bars.v_empty[vs];
+        last_par = (j / kVST) & 1;
+        return true;
+      };
       bool ok = mbar_wait(&bars.qf, 0, abort_flag);
-      for (int j = 0; j <= ntiles && ok; ++j) {
-        if (j < ntiles) {
-          const int ks = j % kKST, sb = j & 1;
-          ok = mbar_wait(&bars.k_full[ks], (j / kKST) & 1, abort_flag);
-          // S buffer sb held P(j - 2): PV(j - 2) must have read it
-          if (ok && j >= 2) ok = mbar_wait(&bars.p_empty[sb], ((j - 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const uint64_t bd = sdesc_sw128(sK + ks * kKVTile + (kk >> 2) * kKVBlk + (kk & 3) * 32, 16, 1024);
-            umma_bf16_ts(tmem + kTmemS + sb * kPN, tmem + kTmemQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&bars.s_full[sb]);
-          umma_commit(&bars.k_empty[ks]);
-          last_bar = &bars.k_empty[ks];
-          last_par = (j / kKST) & 1;
-        }
-        if (j >= 1) {
-          const int jp = j - 1, pb = jp & 1, vs = jp % kVST;
-          ok = mbar_wait(&bars.p_full[pb], (jp >> 1) & 1, abort_flag);
-          if (ok) ok = mbar_wait(&bars.v_full[vs], (jp / kVST) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // V is MN-major (dims contiguous): LBO = stride between 64-dim blocks,
-            // SBO = stride between groups of 8 key rows; k-step kk = key rows 16 kk ..
-            const uint64_t bd = sdesc_sw128(sV + vs * kKVTile + kk * 16 * 128, kKVBlk, 1024);
-            umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kPN + 8 * kk, bd, idO, (jp > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&bars.p_empty[pb]);
-          umma_commit(&bars.v_empty[vs]);
-          last_bar = &bars.v_empty[vs];
-          last_par = (jp / kVST) & 1;
-        }
+      for (int j = 0; j < 2 && j < ntiles && ok; ++j) ok = issue_s(j);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        if (j + 2 < ntiles) ok = issue_s(j + 2);
+        if (ok) ok = issue_pv(j);
       }
       if (!ok) {
         fail();
@@ -401,33 +449,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
 
-    // Q row r, elements [128 h, 128 h + 128), into TMEM columns kTmemQ + 64 h ..
-    // (two BF16 per column, the lower element in the lower half); rows past Sq are 0
-    if (ntiles > 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.Sq + min(qi, p.Sq - 1)) * p.Hq + h) * kD + 128 * hc);
-#pragma unroll
-      for (int c0 = 0; c0 < 2; ++c0) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = (qi < p.Sq) ? __ldg(src + 8 * c0 + i) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-        tmem_st16(t_row + kTmemQ + 64 * hc + 32 * c0, w);
-        tmem_st16(t_row + kTmemQ + 64 * hc + 32 * c0 + 16, w + 16);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.qf);
-    }
-
     for (int j = 0; j < ntiles; ++j) {
-      const int sb = j & 1, ns = j >> 1;
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[sb], ns & 1, abort_flag));
+      const int sb = j % kNSB, x2 = j & 1;  // S / P buffer; parity slot of the max exchange
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[sb], (j / kNSB) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       float s[32];
@@ -452,14 +476,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       // the two halves of the row agree on the tile max (parity-buffered shared slots);
       // after this both have read their S, so P may overwrite it
-      xbuf[(sb * 2 + hc) * kPM + r] = hm;
+      xbuf[(x2 * 2 + hc) * kPM + r] = hm;
       tc_fence_before();  // this warp's S reads are ordered before the partner's P writes
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.xm[rg][sb]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xm[rg][sb], ns & 1, abort_flag));
+      if (lane == 0) mbar_arrive(&bars.xm[rg][x2]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xm[rg][x2], (j >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const float mx = fmaxf(hm, xbuf[(sb * 2 + (1 - hc)) * kPM + r]) * p.scale_log2;
+      const float mx = fmaxf(hm, xbuf[(x2 * 2 + (1 - hc)) * kPM + r]) * p.scale_log2;
 
       // lazy max: it moves only by more than 2^8, so probabilities stay below 2^8
       // (both halves of a row take the same decisions from the same values)
@@ -471,7 +495,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // O must hold PV(j - 1) before it is rescaled; this warp rescales its half of O
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) % kNSB], ((j - 1) / kNSB) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
@@ -510,7 +534,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ---- epilogue: O / l, BF16, gate, store (this warp: columns [128 h, 128 h + 128))
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl % kNSB], (jl / kNSB) & 1, abort_flag));
       // the row's sum is the two halves' sums
       if (ok) {
         xbuf[(4 + hc) * kPM + r] = l_run;
@@ -524,9 +548,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc_fence_after();
     }
     if (ok) {
+      // the gated tile is staged in the V ring (free: the last PV has completed) in the
+      // swizzled [column block][row][128 B] layout and written by TMA stores
       const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-      __nv_bfloat16* orow = p.out + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD;
-      const unsigned char* grow = sm + kOffK + r * 128;  // gate row r of block c at + c * kQBlk
+      unsigned char* ostage = sm + kOffV;
+      const unsigned char* grow = sm + kOffQ + r * 128;  // gate row r of block c at + c * kQBlk
       for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
         float o[32];
         if (ntiles > 0) {
@@ -536,8 +562,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.0f;
         }
-        if (qi >= p.Sq) continue;  // a row past the end (after the warp-collective load)
         uint32_t res[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) res[e] = 0u;
+        // a row past the end (after the warp-collective load) is not computed; TMA drops it
+        if (qi < p.Sq)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const uint16_t ob0 = float_to_bf16_bits(o[2 * e] * inv), ob1 = float_to_bf16_bits(o[2 * e + 1] * inv);
@@ -552,17 +581,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
               g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
             }
             const uint16_t s0 = sigmoid_bf16_fast((uint16_t)(g2 & 0xFFFFu)), s1 = sigmoid_bf16_fast((uint16_t)(g2 >> 16));
-            v = (uint32_t)gate_product_bf16(ob0, s0) | ((uint32_t)gate_product_bf16(ob1, s1) << 16);
+            v = (uint32_t)gate_product_fast(ob0, s0) | ((uint32_t)gate_product_fast(ob1, s1) << 16);
           }
           res[e] = v;
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          reinterpret_cast<uint4*>(orow + c0)[e] = make_uint4(res[4 * e], res[4 * e + 1], res[4 * e + 2], res[4 * e + 3]);
+        for (int u = 0; u < 4; ++u) {
+          const int cb = (c0 + 8 * u) >> 6, ch = ((c0 + 8 * u) & 63) >> 3;
+          *reinterpret_cast<uint4*>(ostage + cb * kQBlk + r * 128 + 16 * (ch ^ (r & 7))) =
+              make_uint4(res[4 * u], res[4 * u + 1], res[4 * u + 2], res[4 * u + 3]);
+        }
       }
       if (p.lse && qi < p.Sq && hc == 0) {
         p.lse[((size_t)b * p.Hq + h) * p.Sq + qi] =
             (l_run > 0.0f) ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.ost);
+      if (tid == 0) {
+        // every softmax warp has staged its part: four TMA stores, then wait until they
+        // have read the staging buffer before the CTA's shared memory goes away
+        if (mbar_wait(&bars.ost, 0, abort_flag)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tma_store_4d(&to, 64 * c, h, i0, b, ostage + c * kQBlk);
+          tma_store_commit_and_wait_read();
+        } else {
+          fail();
+        }
       }
     }
   }
@@ -630,11 +676,13 @@ bool make_map_kv(CUtensorMap* m, const void* base, int B, int S, int H, int rows
 
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k, const void* v, const void* gate,
                            cudaStream_t stream) {
-  CUtensorMap tk, tv, tg;
+  CUtensorMap tq, tk, tv, tg, to;
   // S = 0 still needs a valid map: use extent 1 (nothing is loaded then)
-  if (!make_map_kv(&tk, k, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
+  if (!make_map_kv(&tq, q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM) ||
+      !make_map_kv(&tk, k, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
       !make_map_kv(&tv, v, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
-      !make_map(&tg, gate ? gate : q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM))
+      !make_map_kv(&tg, gate ? gate : q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM) ||
+      !make_map(&to, p.out, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -651,7 +699,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k,
     attr_set[dev] = true;
   }
   const dim3 grid((unsigned)((p.Sq + kPM - 1) / kPM), (unsigned)p.Hq, (unsigned)p.B);
-  prefill_kernel<<<grid, kPThreads, kSmemBytes, stream>>>(tk, tv, tg, p);
+  prefill_kernel<<<grid, kPThreads, kSmemBytes, stream>>>(tq, tk, tv, tg, to, p);
   return cudaGetLastError();
 }
 
