@@ -215,28 +215,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
 // Sq * Hq * D elements, where one table load is far cheaper than the computation.
 __device__ uint16_t g_sigmoid_table[65536];
 
-// RNE_bf16(sigmoid(g)) for the epilogue: for |g| <= 16 the float sigmoid from the SFU
-// (2^x and 1/x approximations) is within 24 float ulp of the real value (argument
-// rounding |g| * 2^-24 relative, 2^x ~2^-22, 1/x and the add ~2^-23), so its BF16
-// rounding is the correct one unless the low 16 bits lie within 32 of the tie; those
-// codes, |g| > 16 and NaN read the table.  Exhaustively checked against the FP64
-// oracle on all 65 536 codes through the fused epilogue.
-__device__ __forceinline__ uint16_t sigmoid_bf16_fast(uint16_t gbits) {
-  const float g = __uint_as_float((uint32_t)gbits << 16);
-  const float a = fabsf(g);
-  if (a <= 16.0f) {
-    // e = exp(-|g|) in (0, 1]: sigmoid(g) = 1 / (1 + e) for g >= 0, e / (1 + e) for g < 0
-    float e, r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-a * 1.44269504088896341f));
-    const float den = 1.0f + e;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(den));
-    const float sg = (g >= 0.0f) ? r : e * r;
-    const uint32_t low = __float_as_uint(sg) & 0xFFFFu;
-    if (low - 0x7FE0u > 0x40u) return __bfloat16_as_ushort(__float2bfloat16_rn(sg));
-  }
-  return __ldg(g_sigmoid_table + gbits);
-}
-
 // RNE_bf16(o * s) for BF16 o and s, as gate_product_bf16 computes it, with the exact
 // double-precision path for products below the float normal range kept out of line:
 // inlined, the compiler may evaluate it for every element, and FP64 on this part is
@@ -566,24 +544,63 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) res[e] = 0u;
         // a row past the end (after the warp-collective load) is not computed; TMA drops it
-        if (qi < p.Sq)
+        if (qi < p.Sq) {
+          uint16_t ob[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint16_t ob0 = float_to_bf16_bits(o[2 * e] * inv), ob1 = float_to_bf16_bits(o[2 * e + 1] * inv);
-          uint32_t v = (uint32_t)ob0 | ((uint32_t)ob1 << 16);
+          for (int i = 0; i < 32; ++i) ob[i] = float_to_bf16_bits(o[i] * inv);
           if (p.fuse_gate) {
-            const int d = c0 + 2 * e;  // gate elements d, d + 1 of row r
-            uint32_t g2;
-            if (ntiles > 0) {
-              const int cb = d >> 6, ch = (d & 63) >> 3;
-              g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kQBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
-            } else {
-              g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
+            // RNE_bf16(sigmoid(g)) from the SFU: for |g| <= 16 the float sigmoid (2^x and 1/x
+            // approximations) is within 24 float ulp of the real value (argument rounding
+            // |g| * 2^-24 relative, 2^x ~2^-22, 1/x and the add ~2^-23), so its BF16
+            // rounding is the correct one unless its low 16 bits lie within 32 of the tie.
+            // Branch-free over the 32 elements (so their SFU chains interleave); the rare
+            // elements that need the exact path (the table of all 65 536 BF16 sigmoids,
+            // the exact product) are marked and redone afterwards.  Exhaustively checked
+            // against the FP64 oracle on all 65 536 gate codes through this epilogue.
+            uint32_t gb[32];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int d = c0 + 2 * e;  // gate elements d, d + 1 of row r
+              uint32_t g2;
+              if (ntiles > 0) {
+                const int cb = d >> 6, ch = (d & 63) >> 3;
+                g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kQBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
+              } else {
+                g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
+              }
+              gb[2 * e] = g2 & 0xFFFFu;
+              gb[2 * e + 1] = g2 >> 16;
             }
-            const uint16_t s0 = sigmoid_bf16_fast((uint16_t)(g2 & 0xFFFFu)), s1 = sigmoid_bf16_fast((uint16_t)(g2 >> 16));
-            v = (uint32_t)gate_product_fast(ob0, s0) | ((uint32_t)gate_product_fast(ob1, s1) << 16);
+            uint32_t need = 0u;
+            uint16_t out16[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = __uint_as_float(gb[i] << 16);
+              const float a = fabsf(g);
+              float e, rc;
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-fminf(a, 16.0f) * 1.44269504088896341f));
+              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(1.0f + e));
+              const float sg = (g >= 0.0f) ? rc : e * rc;
+              const uint32_t low = __float_as_uint(sg) & 0xFFFFu;
+              const float sv = __uint_as_float((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(sg)) << 16);
+              const float pr = __fmul_rn(__uint_as_float((uint32_t)ob[i] << 16), sv);
+              // exact fallback: |g| > 16 or NaN, a float sigmoid near a BF16 tie, or a
+              // product below the float normal range
+              const bool bad = !(a <= 16.0f) || (low - 0x7FE0u <= 0x40u) || (fabsf(pr) < 1.17549435e-38f && pr != 0.0f);
+              need |= bad ? (1u << i) : 0u;
+              out16[i] = __bfloat16_as_ushort(__float2bfloat16_rn(pr));
+            }
+            if (need) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if ((need >> i) & 1u) out16[i] = gate_product_fast(ob[i], __ldg(g_sigmoid_table + gb[i]));
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) res[e] = (uint32_t)out16[2 * e] | ((uint32_t)out16[2 * e + 1] << 16);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) res[e] = (uint32_t)ob[2 * e] | ((uint32_t)ob[2 * e + 1] << 16);
           }
-          res[e] = v;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
