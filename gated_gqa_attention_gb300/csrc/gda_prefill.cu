@@ -12,27 +12,27 @@
 //
 // GB300 design: one CTA per (128-query block, query head, sequence), roles that hand
 // tiles to each other through mbarriers (full / empty pairs, every wait bounded):
-//  * TMEM (512 columns) holds every MMA operand that is not streamed: Q as the A
-//    operand of S = Q K^T (columns [128, 256), BF16 pairs), two S accumulators
-//    (columns [0, 64) and [64, 128), FP32) whose first half is overwritten by P
-//    (BF16 pairs) as the A operand of O += P V, and O (columns [256, 512), FP32).
-//    Shared memory then holds only the streamed K and V tiles, in three-stage rings.
-//  * warps 8 and 10, TMA producers (cp.async.bulk.tensor, 128-byte swizzle): K and V
-//    tiles [64 x 256] into their rings as soon as the MMA that last read a stage has
-//    completed; at the end warp 8 stages the gate tile into the freed K ring.
+//  * Shared memory: the Q tile [128 x 256] (128-byte swizzle, [column block][row]
+//    [128 B]), two-stage K and V rings of [64 x 256] tiles.  At the end the Q buffer
+//    takes the gate tile and the V ring the gated output tile.
+//  * TMEM (512 columns): four S / P buffers (columns [64 n, 64 n + 64), FP32 scores,
+//    their first half then overwritten by P as BF16 pairs) and O (columns [256, 512)).
+//  * warps 8 and 10, TMA producers (cp.async.bulk.tensor, one 5-D box per tile): Q,
+//    then K tiles, then the gate tile (warp 8); V tiles (warp 10); each stage is
+//    refilled as soon as the MMA that last read it has completed.
 //  * warp 9, MMA issuer (one lane; it also owns the TMEM allocation): tcgen05.mma
 //    kind::f16, BF16 operands, FP32 accumulation, M = 128.  S(j) = Q K(j)^T (N = 64,
-//    sixteen k-steps, A from TMEM), then O += P(j-1) V(j-1) (N = 256, four k-steps, A
-//    from TMEM): the tensor core computes S(j) while the softmax works on tile j - 1.
+//    sixteen k-steps, A and B from shared memory) runs two tiles ahead of
+//    O += P(j) V(j) (N = 256, four k-steps, A = P from TMEM, B = V MN-major), so the
+//    tensor core has work queued while the softmax works on tile j.
 //  * warps 0-7, softmax and epilogue: warps w and w + 4 share query rows 32 w .. + 31
-//    (TMEM lanes), each reading 32 of a tile's 64 scores (tcgen05.ld); they first
-//    write Q into TMEM, then per tile agree on the row max through shared memory,
-//    keep a running max (moved lazily, by more than 2^8, as the decode kernels do;
-//    O in TMEM is rescaled then) and sum, and write P (BF16) over their S buffer
-//    with tcgen05.st.  Epilogue: O row from TMEM, divided by the sum, rounded to
-//    BF16, gated with the BF16 sigmoid of the staged gate row (an SFU fast path,
-//    and a per-device table of all 65 536 BF16 sigmoids near rounding ties), staged
-//    in shared memory and written with TMA stores.
+//    (TMEM lanes), each reading 32 of a tile's 64 scores (tcgen05.ld); per tile they
+//    agree on the row max through shared memory, keep a running max (moved lazily,
+//    by more than 2^8, as the decode kernels do; O in TMEM is rescaled then) and sum,
+//    and write P (BF16) over their S buffer with tcgen05.st.  Epilogue: O row from
+//    TMEM, divided by the sum, rounded to BF16, gated with the BF16 sigmoid of the
+//    staged gate row (an SFU fast path, and a per-device table of all 65 536 BF16
+//    sigmoids near rounding ties), staged in shared memory, written by TMA stores.
 // On a timeout the CTA records kErrTimeout, every role stops, waits (bounded) for the
 // copies and MMAs it started, the TMEM is freed and the CTA returns.  TMEM accesses
 // stay warp-convergent (decisions combined with __all_sync).
