@@ -15,6 +15,7 @@
 #include "gda.h"
 #include "gda_device.cuh"
 #include "gda_kernels.h"
+#include "gda_prefill.h"
 
 namespace {
 
@@ -463,7 +464,6 @@ int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, cons
     if (rc != GDA_OK) return rc;
   }
   gda::PrefillParams p;
-  p.q = reinterpret_cast<const __nv_bfloat16*>(q);
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.gate = reinterpret_cast<const __nv_bfloat16*>(gate);

@@ -68,23 +68,6 @@ struct PrepParams {
   int B, Hq, Hkv;
 };
 
-struct PrefillParams {
-  const __nv_bfloat16* q;      // [B, Sq, Hq, D] (loaded into TMEM by the softmax warps)
-  __nv_bfloat16* out;          // [B, Sq, Hq, D]
-  float* lse;                  // [B, Hq, Sq] natural log, or nullptr
-  const __nv_bfloat16* gate;   // [B, Sq, Hq, D] (read directly only for rows with no visible key)
-  const int* kv_lens;          // [B] or nullptr (all Skv)
-  unsigned int* error;         // device error word (kErr* bits)
-  int B, Sq, Skv, Hq, Hkv;
-  float scale_log2;            // scale * log2(e)
-  int causal;
-  int fuse_gate;
-};
-
-// Prefill / extend gated SDPA (tcgen05); q, k, v, gate are [B, S, H, 256] BF16.
-cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k, const void* v, const void* gate,
-                           cudaStream_t stream);
-
 // The step before attention (Q/K RMSNorm, partial RoPE, KV write).
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
 

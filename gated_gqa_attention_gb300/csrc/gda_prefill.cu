@@ -40,6 +40,7 @@
 
 #include "gda_device.cuh"
 #include "gda_kernels.h"
+#include "gda_prefill.h"
 
 namespace gda {
 
