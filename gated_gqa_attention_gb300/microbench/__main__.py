@@ -1,14 +1,24 @@
-"""Build and run the gather probe (needs a GPU): python -m gated_gqa_attention_gb300.microbench"""
+"""Build and run a probe (needs a GPU):
+
+    python -m gated_gqa_attention_gb300.microbench [gather|mma|tma]
+
+gather: how scattered K/V rows stream (16-byte loads, cp.async, 1-D bulk copies);
+mma:    tcgen05.mma throughput per instruction shape (M = 128, N = 64 / 128 / 256,
+        A from TMEM or shared memory, B K-major or MN-major);
+tma:    tensor-map (cp.async.bulk.tensor) throughput for [64 x 256] BF16 tiles of an
+        L2-resident [1, S, 2, 256] tensor through 2 / 4 / 6-stage rings."""
 import os
 import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
+PROBES = {"gather": "gather_probe.cu", "mma": "mma_probe.cu", "tma": "tma_probe.cu"}
 
 
 def main():
-    src = os.path.join(HERE, "gather_probe.cu")
-    exe = os.path.join(HERE, "gather_probe")
+    which = sys.argv[1] if len(sys.argv) > 1 else "gather"
+    src = os.path.join(HERE, PROBES[which])
+    exe = os.path.join(HERE, which + "_probe")
     subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-o", exe, src],
                    check=True)
     sys.exit(subprocess.run([exe]).returncode)
