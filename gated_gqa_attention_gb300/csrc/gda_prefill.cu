@@ -12,21 +12,26 @@
 //
 // GB300 design: one CTA per (128-query block, query head, sequence), roles that hand
 // tiles to each other through mbarriers (full / empty pairs, every wait bounded):
-//  * Shared memory: the Q tile [128 x 256] (128-byte swizzle, [column block][row]
-//    [128 B]), two-stage K and V rings of [64 x 256] tiles.  At the end the Q buffer
-//    takes the gate tile and the V ring the gated output tile.
-//  * TMEM (512 columns): four S / P buffers (columns [64 n, 64 n + 64), FP32 scores,
-//    their first half then overwritten by P as BF16 pairs) and O (columns [256, 512)).
-//  * warps 8 and 10, TMA producers (cp.async.bulk.tensor, one 5-D box per tile): Q,
-//    then K tiles, then the gate tile (warp 8); V tiles (warp 10); each stage is
-//    refilled as soon as the MMA that last read it has completed.
-//  * warp 9, MMA issuer (one lane; it also owns the TMEM allocation): tcgen05.mma
-//    kind::f16, BF16 operands, FP32 accumulation, M = 128.  S(j) = Q K(j)^T (N = 64,
-//    sixteen k-steps, A and B from shared memory) runs two tiles ahead of
-//    O += P(j) V(j) (N = 256, four k-steps, A = P from TMEM, B = V MN-major), so the
-//    tensor core has work queued while the softmax works on tile j.
+//  * Keys go in tiles of 128, so every MMA has N = 128 and runs at the full tensor
+//    rate.  Shared memory: the Q tile [128 x 256] (128-byte swizzle, [column block]
+//    [row][128 B]), and K and V each as two half tiles, a half being 128 keys x 128
+//    head dimensions ([2 column blocks][128 rows][128 B], 32 KiB): half h of tile
+//    j + 1 is loaded as soon as the MMAs of tile j that read half h have completed.
+//    At the end the Q buffer takes the gate tile and the V halves the output tile.
+//  * TMEM (512 columns): two S / P buffers (columns [128 n, 128 n + 128), FP32
+//    scores, their first half then overwritten by P as BF16 pairs) and O (columns
+//    [256, 512)).
+//  * warps 8 and 10, TMA producers (cp.async.bulk.tensor, one 5-D box per half):
+//    Q, then K halves, then the gate tile (warp 8); V halves (warp 10).
+//  * two MMA issuers (one lane each; tcgen05.mma kind::f16, BF16 operands, FP32
+//    accumulation, M = 128, N = 128): warp 9 (which also owns the TMEM allocation)
+//    issues S(j) = Q K(j)^T (16 k-steps, A and B from shared memory), warp 11 issues
+//    O += P(j) V(j) (per 128-dimension half of O, 8 k-steps, A = P from TMEM, B = V
+//    MN-major).  Any wait in an issuing thread lets the tensor pipe drain behind it;
+//    with the two products in separate warps, one keeps the pipe fed while the
+//    other waits, and each waits once per tile.
 //  * warps 0-7, softmax and epilogue: warps w and w + 4 share query rows 32 w .. + 31
-//    (TMEM lanes), each reading 32 of a tile's 64 scores (tcgen05.ld); per tile they
+//    (TMEM lanes), each reading 64 of a tile's 128 scores (tcgen05.ld); per tile they
 //    agree on the row max through shared memory, keep a running max (moved lazily,
 //    by more than 2^8, as the decode kernels do; O in TMEM is rescaled then) and sum,
 //    and write P (BF16) over their S buffer with tcgen05.st.  Epilogue: O row from
@@ -47,30 +52,29 @@ namespace gda {
 namespace {
 
 constexpr int kPM = 128;            // query rows per CTA (MMA M)
-constexpr int kPN = 64;             // keys per tile (MMA N of S)
-constexpr int kKST = 2;             // K ring stages
-constexpr int kVST = 2;             // V ring stages
-constexpr int kNSB = 4;             // S / P buffers in TMEM
+constexpr int kPN = 128;            // keys per tile (MMA N of S)
+constexpr int kNSB = 2;             // S / P buffers in TMEM
 constexpr int kSoftmaxWarps = 8;    // warps 0-7: softmax and epilogue
-constexpr int kLoadWarp = 8;        // TMA producer: K tiles, then the gate tile
-constexpr int kMmaWarp = 9;         // MMA issuer; allocates and frees TMEM
-constexpr int kLoadWarpV = 10;      // TMA producer: V tiles
-constexpr int kPThreads = 11 * 32;
+constexpr int kLoadWarp = 8;        // TMA producer: Q, K halves, then the gate tile
+constexpr int kMmaWarp = 9;         // S = Q K^T issuer; allocates and frees TMEM
+constexpr int kLoadWarpV = 10;      // TMA producer: V halves
+constexpr int kPvWarp = 11;         // O += P V issuer
+constexpr int kPThreads = 12 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;      // S / P buffers: columns [64 n, 64 n + 64), n < kNSB
+constexpr uint32_t kTmemS = 0;      // S / P buffers: columns [128 n, 128 n + 128), n < kNSB
 constexpr uint32_t kTmemO = 256;    // O accumulator: columns [256, 512)
 
 // shared memory plan (offsets from a 1024-byte aligned base)
-constexpr uint32_t kQBlk = kPM * 128;             // one 64-column block of a 128-row tile (the gate): 16 KiB
-constexpr uint32_t kKVBlk = kPN * 128;            // one 64-column block of a K or V tile: 8 KiB
-constexpr uint32_t kKVTile = 4 * kKVBlk;          // one K or V tile: 32 KiB
+constexpr uint32_t kBlk = 128 * 128;               // one 64-column block of 128 rows: 16 KiB
+constexpr uint32_t kHalf = 2 * kBlk;               // a half tile: 2 column blocks, 32 KiB
 constexpr uint32_t kOffQ = 0;                      // Q tile [4 blocks][128 rows][128 B]; the gate tile at the end
-constexpr uint32_t kOffK = kOffQ + 4 * kQBlk;      // K ring
-constexpr uint32_t kOffV = kOffK + kKST * kKVTile; // V ring; the output tile is staged here at the end
-constexpr uint32_t kOffX = kOffV + kVST * kKVTile; // row max [parity][half][row] and sum [half][row] exchange
+constexpr uint32_t kOffK = kOffQ + 4 * kBlk;       // K halves: slot h holds head dimensions [128 h, 128 h + 128)
+constexpr uint32_t kOffV = kOffK + 2 * kHalf;      // V halves; the output tile is staged here at the end
+constexpr uint32_t kOffX = kOffV + 2 * kHalf;      // row max [parity][half][row] and sum [half][row] exchange
 constexpr uint32_t kOffBar = kOffX + 3072;         // mbarriers and the TMEM address
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
-static_assert(kVST * kKVTile >= 4 * kQBlk, "the output tile fits the V ring");
+static_assert(kPM == 128 && kPN == 128, "one 64-column block is 128 rows of 128 B");
+static_assert(2 * kHalf >= 4 * kBlk, "the output tile fits the V halves");
 static_assert(kNSB * kPN <= kTmemO, "S / P buffers below O");
 
 // ---- PTX wrappers (tcgen05, TMA) ----
@@ -238,7 +242,7 @@ __global__ void sigmoid_table_kernel() {
 
 struct PrefillBars {
   uint64_t qf, g;                                   // Q tile landed; gate tile landed
-  uint64_t k_full[kKST], k_empty[kKST], v_full[kVST], v_empty[kVST];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];  // per half slot
   uint64_t s_full[kNSB], p_full[kNSB], p_empty[kNSB];  // per S / P buffer
   uint64_t xm[4][2];                                // per row quarter and tile parity: both maxima stored
   uint64_t xl[4];                                   // per row quarter: both sums stored
@@ -274,11 +278,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (tid == 0) {
     mbar_init(&bars.qf, 1);
     mbar_init(&bars.g, 1);
-    for (int x = 0; x < kKST; ++x) {
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.k_full[x], 1);
       mbar_init(&bars.k_empty[x], 1);
-    }
-    for (int x = 0; x < kVST; ++x) {
       mbar_init(&bars.v_full[x], 1);
       mbar_init(&bars.v_empty[x], 1);
     }
@@ -291,8 +293,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&bars.xm[q4][0], 2);
       mbar_init(&bars.xm[q4][1], 2);
       mbar_init(&bars.xl[q4], 2);
-    mbar_init(&bars.ost, kSoftmaxWarps);
     }
+    mbar_init(&bars.ost, kSoftmaxWarps);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -311,41 +313,39 @@ __global__ void __launch_bounds__(kPThreads, 1)
   };
 
   if (warp == kLoadWarp || warp == kLoadWarpV) {
-    // ---------------- TMA producers (one lane each): K tiles (then the gate tile) from
-    // warp kLoadWarp, V tiles from warp kLoadWarpV, each into its own ring as soon as
-    // the MMA that last read the stage has completed
+    // ---------------- TMA producers (one lane each): K halves (then the gate tile) from
+    // warp kLoadWarp, V halves from warp kLoadWarpV.  Half h of tile j goes into slot h
+    // once the MMAs of tile j - 1 that read slot h have completed.
     const bool is_k = warp == kLoadWarp;
     if (lane == 0 && ntiles > 0) {
-      const int nst = is_k ? kKST : kVST;
-      int arm_g = 0, arm[3] = {0, 0, 0};
+      int arm_g = 0, arm_gate = 0, arm[2] = {0, 0};
       uint64_t* full = is_k ? bars.k_full : bars.v_full;
       uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
       const CUtensorMap* map = is_k ? &tk : &tv;
       const uint32_t base = is_k ? kOffK : kOffV;
       bool ok = true;
       if (is_k) {
-        ++arm_g;  // (the Q copy shares the gate's bookkeeping slot: both land in the Q buffer)
-        mbar_arrive_expect_tx(&bars.qf, 4 * kQBlk);
+        ++arm_g;
+        mbar_arrive_expect_tx(&bars.qf, 4 * kBlk);
         tma_load_5d(sm + kOffQ, &tq, 0, i0, 0, h, b, &bars.qf);
       }
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int x = j % nst, n = j / nst;
-        // stage x is free once the MMA of tile j - nst (S for K, PV for V) has completed
-        if (j >= nst && !mbar_wait(&empty[x], (n - 1) & 1, abort_flag)) { ok = false; break; }
-        ++arm[x];
-        mbar_arrive_expect_tx(&full[x], kKVTile);
-        // one copy of the whole tile: box {64 elements, 64 rows, 4 column blocks}
-        tma_load_5d(sm + base + x * kKVTile, map, 0, j * kPN, 0, kvh, b, &full[x]);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (j > 0 && !mbar_wait(&empty[hh], (j - 1) & 1, abort_flag)) { ok = false; break; }
+          ++arm[hh];
+          mbar_arrive_expect_tx(&full[hh], kHalf);
+          // box {64 elements, 128 rows, 2 column blocks}: head dimensions [128 hh, 128 hh + 128)
+          tma_load_5d(sm + base + hh * kHalf, map, 0, j * kPN, 2 * hh, kvh, b, &full[hh]);
+        }
       }
-      int arm_gate = 0;
       if (ok && is_k && p.fuse_gate) {
-        // the gate tile goes into the Q buffer once the last S product (and so every
-        // earlier one: MMAs complete in order) has read Q
+        // the gate tile goes into the Q buffer once the last S product has read Q (its
+        // last commit covers every earlier MMA of the S issuer)
         const int jl = ntiles - 1;
-        if (!mbar_wait(&bars.k_empty[jl % kKST], (jl / kKST) & 1, abort_flag)) ok = false;
+        if (!mbar_wait(&bars.k_empty[1], jl & 1, abort_flag)) ok = false;
         if (ok) {
           ++arm_gate;
-          mbar_arrive_expect_tx(&bars.g, 4 * kQBlk);
+          mbar_arrive_expect_tx(&bars.g, 4 * kBlk);
           tma_load_5d(sm + kOffQ, &tg, 0, i0, 0, h, b, &bars.g);
         }
       }
@@ -356,59 +356,39 @@ __global__ void __launch_bounds__(kPThreads, 1)
         volatile int* none = &dummy;
         if (arm_g > 0) mbar_wait(&bars.qf, 0, none);
         if (arm_gate > 0) mbar_wait(&bars.g, 0, none);
-        for (int x = 0; x < nst; ++x)
+        for (int x = 0; x < 2; ++x)
           if (arm[x] > 0) mbar_wait(&full[x], (arm[x] - 1) & 1, none);
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer (one lane): S runs two tiles ahead of PV, so the
-    // tensor core has S(j + 1), S(j + 2) queued while the softmax works on tile j
+    // ---------------- S issuer (one lane): S(j) = Q K(j)^T into S buffer j % 2, which
+    // P(j - 2) occupied; one wait point per tile
     if (lane == 0 && ntiles > 0) {
-      const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK), sV = smem_u32(sm + kOffV);
-      const uint32_t idS = idesc_bf16(kPM, kPN, 0), idO = idesc_bf16(kPM, 256, 1);
+      const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK);
+      const uint32_t idS = idesc_bf16(kPM, kPN, 0);
       uint64_t* last_bar = nullptr;  // the barrier of the last commit and its phase parity
       int last_par = 0;
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % kKST, sb = j % kNSB;
-        if (!mbar_wait(&bars.k_full[ks], (j / kKST) & 1, abort_flag)) return false;
-        // S buffer sb held P(j - kNSB): PV(j - kNSB) must have read it
-        if (j >= kNSB && !mbar_wait(&bars.p_empty[sb], ((j / kNSB) - 1) & 1, abort_flag)) return false;
+      bool ok = mbar_wait(&bars.qf, 0, abort_flag);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int sb = j & 1;
+        ok = mbar_wait(&bars.k_full[0], j & 1, abort_flag) && mbar_wait(&bars.k_full[1], j & 1, abort_flag);
+        if (ok && j >= kNSB) ok = mbar_wait(&bars.p_empty[sb], ((j >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kQBlk + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + ks * kKVTile + (kk >> 2) * kKVBlk + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + kTmemS + sb * kPN, ad, bd, idS, kk > 0 ? 1u : 0u);
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) {
+            const int kk = 8 * hh + k8;  // k-step: head dimensions 16 kk .. 16 kk + 15
+            const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sK + hh * kHalf + ((kk >> 2) & 1) * kBlk + (kk & 3) * 32, 16, 1024);
+            umma_bf16_ss(tmem + kTmemS + sb * kPN, ad, bd, idS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars.k_empty[hh]);
         }
         umma_commit(&bars.s_full[sb]);
-        umma_commit(&bars.k_empty[ks]);
-        last_bar = &bars.k_empty[ks];
-        last_par = (j / kKST) & 1;
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        const int pb = j % kNSB, vs = j % kVST;
-        if (!mbar_wait(&bars.p_full[pb], (j / kNSB) & 1, abort_flag)) return false;
-        if (!mbar_wait(&bars.v_full[vs], (j / kVST) & 1, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // V is MN-major (dims contiguous): LBO = stride between 64-dim blocks,
-          // SBO = stride between groups of 8 key rows; k-step kk = key rows 16 kk ..
-          const uint64_t bd = sdesc_sw128(sV + vs * kKVTile + kk * 16 * 128, kKVBlk, 1024);
-          umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kPN + 8 * kk, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bars.p_empty[pb]);
-        umma_commit(&bars.v_empty[vs]);
-        last_bar = &bars.v_empty[vs];
-        last_par = (j / kVST) & 1;
-        return true;
-      };
-      bool ok = mbar_wait(&bars.qf, 0, abort_flag);
-      for (int j = 0; j < 2 && j < ntiles && ok; ++j) ok = issue_s(j);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 2 < ntiles) ok = issue_s(j + 2);
-        if (ok) ok = issue_pv(j);
+        last_bar = &bars.s_full[sb];
+        last_par = (j >> 1) & 1;
       }
       if (!ok) {
         fail();
@@ -418,9 +398,47 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (last_bar != nullptr) mbar_wait(last_bar, last_par, none);
       }
     }
+  } else if (warp == kPvWarp) {
+    // ---------------- PV issuer (one lane): O += P(j) V(j), per 128-dimension half of O
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t sV = smem_u32(sm + kOffV);
+      const uint32_t idO = idesc_bf16(kPM, 128, 1);
+      uint64_t* last_bar = nullptr;
+      int last_par = 0;
+      bool ok = true;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int pb = j & 1;
+        ok = mbar_wait(&bars.p_full[pb], (j >> 1) & 1, abort_flag) &&
+             mbar_wait(&bars.v_full[0], j & 1, abort_flag) && mbar_wait(&bars.v_full[1], j & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // V half hh is MN-major (dims contiguous): LBO = stride between its two 64-dim
+            // blocks, SBO = 8 key rows; k-step kk = keys 16 kk .. 16 kk + 15, whose P is
+            // in columns 8 kk .. 8 kk + 7 of the S buffer
+            const uint64_t bd = sdesc_sw128(sV + hh * kHalf + kk * 16 * 128, kBlk, 1024);
+            umma_bf16_ts(tmem + kTmemO + 128 * hh, tmem + kTmemS + pb * kPN + 8 * kk, bd, idO,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars.v_empty[hh]);
+        }
+        umma_commit(&bars.p_empty[pb]);
+        last_bar = &bars.p_empty[pb];
+        last_par = (j >> 1) & 1;
+      }
+      if (!ok) {
+        fail();
+        int dummy = 0;
+        volatile int* none = &dummy;
+        if (last_bar != nullptr) mbar_wait(last_bar, last_par, none);
+      }
+    }
   } else {
     // ---------------- softmax and epilogue: warp w owns rows 32 (w % 4) .. + 31 (its
-    // TMEM lane quarter) and keys [32 h, 32 h + 32) of each tile, h = w / 4
+    // TMEM lane quarter) and keys [64 h, 64 h + 64) of each tile, h = w / 4
     const int rg = warp & 3, hc = warp >> 2;
     const int r = 32 * rg + lane;
     const int qi = i0 + r;
@@ -429,19 +447,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool ok = true;
 
     for (int j = 0; j < ntiles; ++j) {
-      const int sb = j % kNSB, x2 = j & 1;  // S / P buffer; parity slot of the max exchange
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[sb], (j / kNSB) & 1, abort_flag));
+      const int sb = j & 1, x2 = j & 1;  // S / P buffer; parity slot of the max exchange
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[sb], (j >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      float s[32];
-      tmem_ld32(t_row + kTmemS + sb * kPN + 32 * hc, s);
+      float s[64];
+      tmem_ld32(t_row + kTmemS + sb * kPN + 64 * hc, s);
+      tmem_ld32(t_row + kTmemS + sb * kPN + 64 * hc + 32, s + 32);
       tmem_wait_ld();
 
-      const int k0 = j * kPN + 32 * hc;  // key of s[0]
-      const bool need_mask = (k0 + 32 > L) || (p.causal && k0 + 31 > i0 + off);
+      const int k0 = j * kPN + 64 * hc;  // key of s[0]
+      const bool need_mask = (k0 + 64 > L) || (p.causal && k0 + 63 > i0 + off);
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const int kj = k0 + c;
           if (kj >= L || (p.causal && kj > qi + off)) s[c] = -INFINITY;
         }
@@ -450,7 +469,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       {
         float e4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) e4[c & 3] = fmaxf(e4[c & 3], s[c]);
+        for (int c = 0; c < 64; ++c) e4[c & 3] = fmaxf(e4[c & 3], s[c]);
         hm = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
       }
       // the two halves of the row agree on the tile max (parity-buffered shared slots);
@@ -474,7 +493,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // O must hold PV(j - 1) before it is rescaled; this warp rescales its half of O
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) % kNSB], ((j - 1) / kNSB) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
@@ -489,12 +508,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       // p = 2^(s * scale_log2 - m): one FFMA and one SFU op per score (a masked score
       // gives 2^-inf = 0; a row with no visible key yet uses m = 0); P (BF16 pairs)
-      // over the first half of the S buffer: keys 32 h .. at columns 16 h ..
+      // over the first half of the S buffer: keys 64 h .. at columns 32 h ..
       const float mneg = (m_run == -INFINITY) ? 0.0f : -m_run;
-      uint32_t w[16];
+      uint32_t w[32];
       float la = 0.0f, lb = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
+      for (int e = 0; e < 32; ++e) {
         const float p0 = ex2_approx(fmaf(s[2 * e], p.scale_log2, mneg));
         const float p1 = ex2_approx(fmaf(s[2 * e + 1], p.scale_log2, mneg));
         w[e] = bf16x2_rn(p0, p1);
@@ -502,7 +521,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         lb += __uint_as_float(w[e] & 0xFFFF0000u);
       }
       l_run += la + lb;
-      tmem_st16(t_row + kTmemS + sb * kPN + 16 * hc, w);
+      tmem_st16(t_row + kTmemS + sb * kPN + 32 * hc, w);
+      tmem_st16(t_row + kTmemS + sb * kPN + 32 * hc + 16, w + 16);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -513,7 +533,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ---- epilogue: O / l, BF16, gate, store (this warp: columns [128 h, 128 h + 128))
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl % kNSB], (jl / kNSB) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag));
       // the row's sum is the two halves' sums
       if (ok) {
         xbuf[(4 + hc) * kPM + r] = l_run;
@@ -531,7 +551,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // swizzled [column block][row][128 B] layout and written by TMA stores
       const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
       unsigned char* ostage = sm + kOffV;
-      const unsigned char* grow = sm + kOffQ + r * 128;  // gate row r of block c at + c * kQBlk
+      const unsigned char* grow = sm + kOffQ + r * 128;  // gate row r of block c at + c * kBlk
       for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
         float o[32];
         if (ntiles > 0) {
@@ -565,7 +585,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
               uint32_t g2;
               if (ntiles > 0) {
                 const int cb = d >> 6, ch = (d & 63) >> 3;
-                g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kQBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
+                g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
               } else {
                 g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
               }
@@ -606,7 +626,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int cb = (c0 + 8 * u) >> 6, ch = ((c0 + 8 * u) & 63) >> 3;
-          *reinterpret_cast<uint4*>(ostage + cb * kQBlk + r * 128 + 16 * (ch ^ (r & 7))) =
+          *reinterpret_cast<uint4*>(ostage + cb * kBlk + r * 128 + 16 * (ch ^ (r & 7))) =
               make_uint4(res[4 * u], res[4 * u + 1], res[4 * u + 2], res[4 * u + 3]);
         }
       }
@@ -622,7 +642,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // have read the staging buffer before the CTA's shared memory goes away
         if (mbar_wait(&bars.ost, 0, abort_flag)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tma_store_4d(&to, 64 * c, h, i0, b, ostage + c * kQBlk);
+          for (int c = 0; c < 4; ++c) tma_store_4d(&to, 64 * c, h, i0, b, ostage + c * kBlk);
           tma_store_commit_and_wait_read();
         } else {
           fail();
@@ -675,15 +695,15 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// K or V [B, S, H, D] BF16 as a 5-D tensor {64 elements, S, 4 column blocks, H, B} with
-// box {64, rows, 4, 1, 1}: one copy fills a tile laid out [block][row][128 B] (128-byte
-// swizzle), the layout the MMA descriptors read
-bool make_map_kv(CUtensorMap* m, const void* base, int B, int S, int H, int rows) {
+// Q, K, V or the gate [B, S, H, D] BF16 as a 5-D tensor {64 elements, S, 4 column
+// blocks, H, B} with box {64, rows, blocks, 1, 1}: one copy fills a tile laid out
+// [block][row][128 B] (128-byte swizzle), the layout the MMA descriptors read
+bool make_map_kv(CUtensorMap* m, const void* base, int B, int S, int H, int rows, int blocks) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[5] = {64, (cuuint64_t)S, 4, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[4] = {(cuuint64_t)H * kD * 2, 128, (cuuint64_t)kD * 2, (cuuint64_t)S * H * kD * 2};
-  const cuuint32_t box[5] = {64, (cuuint32_t)rows, 4, 1, 1};
+  const cuuint32_t box[5] = {64, (cuuint32_t)rows, (cuuint32_t)blocks, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -696,10 +716,10 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k,
                            cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tg, to;
   // S = 0 still needs a valid map: use extent 1 (nothing is loaded then)
-  if (!make_map_kv(&tq, q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM) ||
-      !make_map_kv(&tk, k, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
-      !make_map_kv(&tv, v, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN) ||
-      !make_map_kv(&tg, gate ? gate : q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM) ||
+  if (!make_map_kv(&tq, q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM, 4) ||
+      !make_map_kv(&tk, k, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN, 2) ||
+      !make_map_kv(&tv, v, p.B, p.Skv > 0 ? p.Skv : 1, p.Hkv, kPN, 2) ||
+      !make_map_kv(&tg, gate ? gate : q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM, 4) ||
       !make_map(&to, p.out, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
