@@ -68,14 +68,17 @@ constexpr uint32_t kTmemO = 256;    // O accumulator: columns [256, 512)
 constexpr uint32_t kBlk = 128 * 128;               // one 64-column block of 128 rows: 16 KiB
 constexpr uint32_t kHalf = 2 * kBlk;               // a half tile: 2 column blocks, 32 KiB
 constexpr uint32_t kOffQ = 0;                      // Q tile [4 blocks][128 rows][128 B]; the gate tile at the end
-constexpr uint32_t kOffK = kOffQ + 4 * kBlk;       // K halves: slot h holds head dimensions [128 h, 128 h + 128)
-constexpr uint32_t kOffV = kOffK + 2 * kHalf;      // V halves; the output tile is staged here at the end
-constexpr uint32_t kOffX = kOffV + 2 * kHalf;      // row max [parity][half][row] and sum [half][row] exchange
-constexpr uint32_t kOffBar = kOffX + 3072;         // mbarriers and the TMEM address
-constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
+constexpr int kKSlots = 3;                         // K ring: three half slots (half n of the K stream in slot n % 3)
+constexpr uint32_t kOffK = kOffQ + 4 * kBlk;       // K ring
+constexpr uint32_t kOffV = kOffK + kKSlots * kHalf; // V halves (slot h: head dimensions [128 h, 128 h + 128));
+                                                   // the output tile is staged here at the end
+constexpr uint32_t kOffX = kOffV + 2 * kHalf;      // row max exchange [parity][half][row]; the sums reuse a slot
+constexpr uint32_t kOffBar = kOffX + 2048;         // mbarriers and the TMEM address
+constexpr uint32_t kSmemBytes = kOffBar + 512;     // the dynamic shared memory base is 1024-byte aligned (checked)
 static_assert(kPM == 128 && kPN == 128, "one 64-column block is 128 rows of 128 B");
 static_assert(2 * kHalf >= 4 * kBlk, "the output tile fits the V halves");
 static_assert(kNSB * kPN <= kTmemO, "S / P buffers below O");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // ---- PTX wrappers (tcgen05, TMA) ----
 
@@ -242,7 +245,7 @@ __global__ void sigmoid_table_kernel() {
 
 struct PrefillBars {
   uint64_t qf, g;                                   // Q tile landed; gate tile landed
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];  // per half slot
+  uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[2], v_empty[2];  // per half slot
   uint64_t s_full[kNSB], p_full[kNSB], p_empty[kNSB];  // per S / P buffer
   uint64_t xm[4][2];                                // per row quarter and tile parity: both maxima stored
   uint64_t xl[4];                                   // per row quarter: both sums stored
@@ -259,8 +262,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                    const __grid_constant__ CUtensorMap tv,
                    const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap to,
                    PrefillParams p) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw;
+  // the 128-byte swizzled tiles need a 1024-byte aligned base, which the layout takes
+  // without slack: a misaligned base is reported, not used (the same for every CTA)
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.error, kErrTimeout);
+    return;
+  }
   PrefillBars& bars = *reinterpret_cast<PrefillBars*>(sm + kOffBar);
   float* xbuf = reinterpret_cast<float*>(sm + kOffX);  // [parity][half][row]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -278,9 +287,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (tid == 0) {
     mbar_init(&bars.qf, 1);
     mbar_init(&bars.g, 1);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kKSlots; ++x) {
       mbar_init(&bars.k_full[x], 1);
       mbar_init(&bars.k_empty[x], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.v_full[x], 1);
       mbar_init(&bars.v_empty[x], 1);
     }
@@ -294,7 +305,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&bars.xm[q4][1], 2);
       mbar_init(&bars.xl[q4], 2);
     }
-    mbar_init(&bars.ost, kSoftmaxWarps);
+    mbar_init(&bars.ost, kPThreads / 32);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -312,37 +323,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bars.abort = 1;
   };
 
+  float m_run = -INFINITY, l_run = 0.0f;  // softmax warps: running row max (log2 units) and sum
+
   if (warp == kLoadWarp || warp == kLoadWarpV) {
     // ---------------- TMA producers (one lane each): K halves (then the gate tile) from
-    // warp kLoadWarp, V halves from warp kLoadWarpV.  Half h of tile j goes into slot h
-    // once the MMAs of tile j - 1 that read slot h have completed.
+    // warp kLoadWarp, V halves from warp kLoadWarpV.  Half n = 2 j + h of the stream
+    // (head dimensions [128 h, 128 h + 128) of tile j) goes into slot n % nslot once
+    // the MMAs that read the slot's previous half have completed.
     const bool is_k = warp == kLoadWarp;
     if (lane == 0 && ntiles > 0) {
-      int arm_g = 0, arm_gate = 0, arm[2] = {0, 0};
+      int arm_g = 0, arm_gate = 0, arm[kKSlots] = {};
       uint64_t* full = is_k ? bars.k_full : bars.v_full;
       uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
       const CUtensorMap* map = is_k ? &tk : &tv;
       const uint32_t base = is_k ? kOffK : kOffV;
+      const int nslot = is_k ? kKSlots : 2;
       bool ok = true;
       if (is_k) {
         ++arm_g;
         mbar_arrive_expect_tx(&bars.qf, 4 * kBlk);
         tma_load_5d(sm + kOffQ, &tq, 0, i0, 0, h, b, &bars.qf);
       }
-      for (int j = 0; j < ntiles && ok; ++j) {
-        for (int hh = 0; hh < 2; ++hh) {
-          if (j > 0 && !mbar_wait(&empty[hh], (j - 1) & 1, abort_flag)) { ok = false; break; }
-          ++arm[hh];
-          mbar_arrive_expect_tx(&full[hh], kHalf);
-          // box {64 elements, 128 rows, 2 column blocks}: head dimensions [128 hh, 128 hh + 128)
-          tma_load_5d(sm + base + hh * kHalf, map, 0, j * kPN, 2 * hh, kvh, b, &full[hh]);
-        }
+      for (int n = 0; n < 2 * ntiles; ++n) {
+        const int x = n % nslot, u = n / nslot;  // slot and its use count
+        if (u > 0 && !mbar_wait(&empty[x], (u - 1) & 1, abort_flag)) { ok = false; break; }
+        ++arm[x];
+        mbar_arrive_expect_tx(&full[x], kHalf);
+        // box {64 elements, 128 rows, 2 column blocks}: keys 128 j .., head dimensions 128 h ..
+        tma_load_5d(sm + base + x * kHalf, map, 0, (n >> 1) * kPN, 2 * (n & 1), kvh, b, &full[x]);
       }
       if (ok && is_k && p.fuse_gate) {
         // the gate tile goes into the Q buffer once the last S product has read Q (its
         // last commit covers every earlier MMA of the S issuer)
-        const int jl = ntiles - 1;
-        if (!mbar_wait(&bars.k_empty[1], jl & 1, abort_flag)) ok = false;
+        const int nl = 2 * ntiles - 1;  // the last K half
+        if (!mbar_wait(&bars.k_empty[nl % kKSlots], (nl / kKSlots) & 1, abort_flag)) ok = false;
         if (ok) {
           ++arm_gate;
           mbar_arrive_expect_tx(&bars.g, 4 * kBlk);
@@ -356,7 +370,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         volatile int* none = &dummy;
         if (arm_g > 0) mbar_wait(&bars.qf, 0, none);
         if (arm_gate > 0) mbar_wait(&bars.g, 0, none);
-        for (int x = 0; x < 2; ++x)
+        for (int x = 0; x < nslot; ++x)
           if (arm[x] > 0) mbar_wait(&full[x], (arm[x] - 1) & 1, none);
       }
     }
@@ -371,7 +385,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       bool ok = mbar_wait(&bars.qf, 0, abort_flag);
       for (int j = 0; j < ntiles && ok; ++j) {
         const int sb = j & 1;
-        ok = mbar_wait(&bars.k_full[0], j & 1, abort_flag) && mbar_wait(&bars.k_full[1], j & 1, abort_flag);
+        const int x0 = (2 * j) % kKSlots, x1 = (2 * j + 1) % kKSlots;  // the slots of K(j)'s halves
+        ok = mbar_wait(&bars.k_full[x0], ((2 * j) / kKSlots) & 1, abort_flag) &&
+             mbar_wait(&bars.k_full[x1], ((2 * j + 1) / kKSlots) & 1, abort_flag);
         if (ok && j >= kNSB) ok = mbar_wait(&bars.p_empty[sb], ((j >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -381,10 +397,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int k8 = 0; k8 < 8; ++k8) {
             const int kk = 8 * hh + k8;  // k-step: head dimensions 16 kk .. 16 kk + 15
             const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sK + hh * kHalf + ((kk >> 2) & 1) * kBlk + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sK + (hh ? x1 : x0) * kHalf + ((kk >> 2) & 1) * kBlk + (kk & 3) * 32, 16, 1024);
             umma_bf16_ss(tmem + kTmemS + sb * kPN, ad, bd, idS, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&bars.k_empty[hh]);
+          umma_commit(&bars.k_empty[hh ? x1 : x0]);
         }
         umma_commit(&bars.s_full[sb]);
         last_bar = &bars.s_full[sb];
@@ -443,7 +459,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int r = 32 * rg + lane;
     const int qi = i0 + r;
     const uint32_t t_row = tmem + ((uint32_t)(rg * 32) << 16);
-    float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
 
     for (int j = 0; j < ntiles; ++j) {
@@ -529,30 +544,48 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (lane == 0) mbar_arrive(&bars.p_full[sb]);
     }
     if (!ok) fail();
+  }
 
-    // ---- epilogue: O / l, BF16, gate, store (this warp: columns [128 h, 128 h + 128))
+  // ---------------- epilogue, all twelve warps: warp w reads TMEM lane quarter w % 4
+  // (rows 32 (w % 4) ..) and 32-column chunks {0, 1, 2} (warps 0-3), {4, 5, 6} (4-7) or
+  // {3, 7} (8-11) of O; O / l, BF16, gate, staged in the V halves (free once the last
+  // PV has completed) in the swizzled [column block][row][128 B] layout, TMA stores
+  __syncwarp();
+  {
+    const int eq = warp & 3;
+    const int r = 32 * eq + lane;
+    const int qi = i0 + r;
+    const uint32_t t_row = tmem + ((uint32_t)(eq * 32) << 16);
+    bool ok = (*abort_flag == 0);
+    const int xs = ntiles & 1;  // exchange slot for the row sums (last used at tile ntiles - 2)
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag));
       // the row's sum is the two halves' sums
       if (ok) {
-        xbuf[(4 + hc) * kPM + r] = l_run;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.xl[rg]);
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.xl[rg], 0, abort_flag));
-        if (ok) l_run += xbuf[(4 + (1 - hc)) * kPM + r];
+        if (warp < kSoftmaxWarps) {
+          xbuf[(xs * 2 + (warp >> 2)) * kPM + r] = l_run;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.xl[eq]);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.xl[eq], 0, abort_flag));
       }
       if (ok && p.fuse_gate) ok = __all_sync(0xffffffffu, mbar_wait(&bars.g, 0, abort_flag));
       if (!ok) fail();
       tc_fence_after();
     }
     if (ok) {
-      // the gated tile is staged in the V ring (free: the last PV has completed) in the
-      // swizzled [column block][row][128 B] layout and written by TMA stores
-      const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      const float l_row = (ntiles > 0) ? xbuf[xs * 2 * kPM + r] + xbuf[(xs * 2 + 1) * kPM + r] : 0.0f;
+      const float inv = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
       unsigned char* ostage = sm + kOffV;
+      unsigned char* orow = ostage + r * 128;             // output row r of block c at + c * kBlk
       const unsigned char* grow = sm + kOffQ + r * 128;  // gate row r of block c at + c * kBlk
-      for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
+      const int nch = (warp < kSoftmaxWarps) ? 3 : 2;
+      uint32_t needs[3] = {0u, 0u, 0u};  // per chunk: elements whose exact product is still to do
+#pragma unroll
+      for (int ci = 0; ci < 3; ++ci) {
+        if (ci >= nch) break;
+        const int c0 = 32 * ((warp < kSoftmaxWarps) ? (4 * (warp >> 2) + ci) : (ci ? 7 : 3));
         float o[32];
         if (ntiles > 0) {
           tmem_ld32(t_row + kTmemO + c0, o);
@@ -561,85 +594,103 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.0f;
         }
-        uint32_t res[16];
+        uint32_t res[16];  // BF16 pairs: elements c0 + 2 e (low half) and c0 + 2 e + 1
 #pragma unroll
         for (int e = 0; e < 16; ++e) res[e] = 0u;
         // a row past the end (after the warp-collective load) is not computed; TMA drops it
         if (qi < p.Sq) {
-          uint16_t ob[32];
+          // every BF16 rounding here is done two values at a time (cvt.rn.bf16x2.f32)
+          uint32_t ob[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ob[i] = float_to_bf16_bits(o[i] * inv);
+          for (int e = 0; e < 16; ++e) ob[e] = bf16x2_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
           if (p.fuse_gate) {
-            // RNE_bf16(sigmoid(g)) from the SFU: for |g| <= 16 the float sigmoid (2^x and 1/x
-            // approximations) is within 24 float ulp of the real value (argument rounding
-            // |g| * 2^-24 relative, 2^x ~2^-22, 1/x and the add ~2^-23), so its BF16
-            // rounding is the correct one unless its low 16 bits lie within 32 of the tie.
-            // Branch-free over the 32 elements (so their SFU chains interleave); the rare
-            // elements that need the exact path (the table of all 65 536 BF16 sigmoids,
-            // the exact product) are marked and redone afterwards.  Exhaustively checked
-            // against the FP64 oracle on all 65 536 gate codes through this epilogue.
-            uint32_t gb[32];
+            // RNE_bf16(sigmoid(g)) from the SFU: for |g| <= 16, 1 / (1 + 2^(-g log2 e))
+            // (2^x and 1/x approximations) is within 24 float ulp of the real value
+            // (argument rounding |g| log2 e * 2^-24, 2^x ~2^-22, the add and 1/x ~2^-23),
+            // so its BF16 rounding is the correct one unless its low 16 bits lie within 32
+            // of the tie.  Branch-free over the 32 elements (so their SFU chains
+            // interleave); an element that needs the exact path (|g| > 16 or NaN, a
+            // sigmoid near a tie, a product below the float normal range) is staged
+            // ungated, marked, and redone after the chunk from the table of all 65 536
+            // BF16 sigmoids.  Exhaustively checked against the FP64 oracle on all 65 536
+            // gate codes through this epilogue.
+            uint32_t gp[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int d = c0 + 2 * e;  // gate elements d, d + 1 of row r
-              uint32_t g2;
               if (ntiles > 0) {
                 const int cb = d >> 6, ch = (d & 63) >> 3;
-                g2 = *reinterpret_cast<const uint32_t*>(grow + cb * kBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
+                gp[e] = *reinterpret_cast<const uint32_t*>(grow + cb * kBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
               } else {
-                g2 = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
+                gp[e] = __ldg(reinterpret_cast<const uint32_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
               }
-              gb[2 * e] = g2 & 0xFFFFu;
-              gb[2 * e + 1] = g2 >> 16;
             }
             uint32_t need = 0u;
-            uint16_t out16[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float g = __uint_as_float(gb[i] << 16);
-              const float a = fabsf(g);
-              float e, rc;
-              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-fminf(a, 16.0f) * 1.44269504088896341f));
-              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(1.0f + e));
-              const float sg = (g >= 0.0f) ? rc : e * rc;
-              const uint32_t low = __float_as_uint(sg) & 0xFFFFu;
-              const float sv = __uint_as_float((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(sg)) << 16);
-              const float pr = __fmul_rn(__uint_as_float((uint32_t)ob[i] << 16), sv);
-              // exact fallback: |g| > 16 or NaN, a float sigmoid near a BF16 tie, or a
-              // product below the float normal range
-              const bool bad = !(a <= 16.0f) || (low - 0x7FE0u <= 0x40u) || (fabsf(pr) < 1.17549435e-38f && pr != 0.0f);
-              need |= bad ? (1u << i) : 0u;
-              out16[i] = __bfloat16_as_ushort(__float2bfloat16_rn(pr));
+            for (int e = 0; e < 16; ++e) {
+              float sg[2], pr[2];
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const float g = __uint_as_float(t ? (gp[e] & 0xFFFF0000u) : (gp[e] << 16));
+                float ex, rc;
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(g * -1.44269504088896341f));
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(1.0f + ex));
+                sg[t] = rc;
+                const uint32_t low = __float_as_uint(rc) & 0xFFFFu;
+                need |= (!(fabsf(g) <= 16.0f) || (low - 0x7FE0u <= 0x40u)) ? (1u << (2 * e + t)) : 0u;
+              }
+              const uint32_t sv = bf16x2_rn(sg[0], sg[1]);
+              pr[0] = __fmul_rn(__uint_as_float(ob[e] << 16), __uint_as_float(sv << 16));
+              pr[1] = __fmul_rn(__uint_as_float(ob[e] & 0xFFFF0000u), __uint_as_float(sv & 0xFFFF0000u));
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                need |= (fabsf(pr[t]) < 1.17549435e-38f && pr[t] != 0.0f) ? (1u << (2 * e + t)) : 0u;
+              res[e] = bf16x2_rn(pr[0], pr[1]);
+              // a marked element is staged as O (BF16) and finished below
+              const uint32_t m2 = (need >> (2 * e)) & 3u;
+              if (m2) res[e] = (res[e] & ~((m2 & 1u) * 0xFFFFu) & ~((m2 >> 1) * 0xFFFF0000u)) |
+                               (ob[e] & (((m2 & 1u) * 0xFFFFu) | ((m2 >> 1) * 0xFFFF0000u)));
             }
-            if (need) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if ((need >> i) & 1u) out16[i] = gate_product_fast(ob[i], __ldg(g_sigmoid_table + gb[i]));
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) res[e] = (uint32_t)out16[2 * e] | ((uint32_t)out16[2 * e + 1] << 16);
+            needs[ci] = need;
           } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) res[e] = (uint32_t)ob[2 * e] | ((uint32_t)ob[2 * e + 1] << 16);
+            for (int e = 0; e < 16; ++e) res[e] = ob[e];
           }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int cb = (c0 + 8 * u) >> 6, ch = ((c0 + 8 * u) & 63) >> 3;
-          *reinterpret_cast<uint4*>(ostage + cb * kBlk + r * 128 + 16 * (ch ^ (r & 7))) =
+          *reinterpret_cast<uint4*>(orow + cb * kBlk + 16 * (ch ^ (r & 7))) =
               make_uint4(res[4 * u], res[4 * u + 1], res[4 * u + 2], res[4 * u + 3]);
         }
       }
-      if (p.lse && qi < p.Sq && hc == 0) {
+      // the marked elements: exact sigmoid from the table, exact product (each lane only
+      // touches its own row)
+#pragma unroll
+      for (int ci = 0; ci < 3; ++ci) {
+        uint32_t m = needs[ci];
+        const int c0 = 32 * ((warp < kSoftmaxWarps) ? (4 * (warp >> 2) + ci) : (ci ? 7 : 3));
+        while (m != 0u) {
+          const int d = c0 + __ffs(m) - 1;
+          m &= m - 1u;
+          const int cb = d >> 6, ch = (d & 63) >> 3;
+          uint16_t* op = reinterpret_cast<uint16_t*>(orow + cb * kBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7));
+          const uint16_t gb = (ntiles > 0)
+              ? *reinterpret_cast<const uint16_t*>(grow + cb * kBlk + 16 * (ch ^ (r & 7)) + 2 * (d & 7))
+              : __ldg(reinterpret_cast<const uint16_t*>(p.gate + (((size_t)b * p.Sq + qi) * p.Hq + h) * kD + d));
+          *op = gate_product_fast(*op, __ldg(g_sigmoid_table + gb));
+        }
+      }
+      if (p.lse && qi < p.Sq && warp < 4) {
         p.lse[((size_t)b * p.Hq + h) * p.Sq + qi] =
-            (l_run > 0.0f) ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+            (l_row > 0.0f) ? (m_run + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
       }
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ost);
       if (tid == 0) {
-        // every softmax warp has staged its part: four TMA stores, then wait until they
-        // have read the staging buffer before the CTA's shared memory goes away
+        // every warp has staged its part: four TMA stores, then wait until they have read
+        // the staging buffer before the CTA's shared memory goes away
         if (mbar_wait(&bars.ost, 0, abort_flag)) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tma_store_4d(&to, 64 * c, h, i0, b, ostage + c * kBlk);
