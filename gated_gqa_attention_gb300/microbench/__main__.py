@@ -1,18 +1,20 @@
 """Build and run a probe (needs a GPU):
 
-    python -m gated_gqa_attention_gb300.microbench [gather|mma|tma]
+    python -m gated_gqa_attention_gb300.microbench [gather|mma|tma|issue]
 
 gather: how scattered K/V rows stream (16-byte loads, cp.async, 1-D bulk copies);
 mma:    tcgen05.mma throughput per instruction shape (M = 128, N = 64 / 128 / 256,
         A from TMEM or shared memory, B K-major or MN-major);
 tma:    tensor-map (cp.async.bulk.tensor) throughput for [64 x 256] BF16 tiles of an
-        L2-resident [1, S, 2, 256] tensor through 2 / 4 / 6-stage rings."""
+        L2-resident [1, S, 2, 256] tensor through 2 / 4 / 6-stage rings;
+issue:  how waits in the MMA-issuing thread stall the tensor pipe, and the attention
+        mainloop's MMA schedules (64-key tiles, 128-key tiles with one or two issuers)."""
 import os
 import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-PROBES = {"gather": "gather_probe.cu", "mma": "mma_probe.cu", "tma": "tma_probe.cu"}
+PROBES = {"gather": "gather_probe.cu", "mma": "mma_probe.cu", "tma": "tma_probe.cu", "issue": "issue_probe.cu"}
 
 
 def main():
