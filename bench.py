@@ -8,8 +8,12 @@ needed between calls).  Prints ONE JSON line (rank 0):
 
   value      whole-job achieved HBM GB/s = algorithmic bytes of all ranks' calls
              / max-over-ranks device time (K+V rows + q + gate + out)
-  e2e        the same through gda.decode with per-step host->device copies of
-             q, gate, kv_indptr, kv_indices and a device->host read of out
+  e2e        the same measured from host memory: per step, one copy of the packed
+             inputs (q, gate, kv_indptr, kv_indices) from pinned host memory, the
+             decode, one copy of out back and a wait, all inside gda_decode_step_host;
+             the kernels read the inputs from and write out into pinned host memory
+             in place, over the host-device link (bf16 pools without window or
+             sinks; otherwise per-tensor copies around gda.decode)
   roofline   stage-1 kernel: algorithmic bytes / its CUDA-event duration vs the
              measured HBM copy bandwidth
   cpu_baseline  the FP64 oracle on the host cores (rank 0, N=1)
@@ -364,20 +368,37 @@ def run_ours(args):
     achieved = s1_bytes / (s1_us / 1e6) / 1e9
     peak, peak_kind = measured_hbm_peak()
 
-    # ---- end to end through gda.decode with host buffers
-    host = {k: dev[k].cpu().pin_memory() for k in ("q", "gate", "kv_indptr", "kv_indices")}
+    # ---- end to end with host buffers: per step, the inputs go from pinned host memory
+    # to the device, the decode runs, the result comes back and the host waits for it
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
     k_e2e = min(args.steps, 5000)
+    step_api = args.kv == "bf16" and args.window == 0 and args.sinks is None
+    if step_api:
+        # gda_decode_step_host: one packed block in, the decode, one copy out, one wait
+        B_, Hq_, D_ = dev["q"].shape
+        nnz_ = dev["kv_indices"].numel()
+        _, blk = gda.step_layout(B_, Hq_, D_, nnz_)
+        host_in = torch.zeros(blk, dtype=torch.uint8).pin_memory()
+        gda.pack_step(host_in, dev["q"], dev["gate"], dev["kv_indptr"], dev["kv_indices"])
+        h2d = blk   # read by the kernels in place over the host-device link
+        e2e_api = "gda_decode_step_host (inputs read and result written in pinned host memory)"
+        # the step's marshalled C call; each step: decode from host_in into out_h, wait
+        e2e_step = gda.StepHost(host_in, None, dev["k_pool"], dev["v_pool"], None, out_h, B_, Hq_, nnz_,
+                                scale=inp["scale"], num_splits=args.splits, map_in=True, map_out=True,
+                                stream=stream)
+    else:
+        host = {k: dev[k].cpu().pin_memory() for k in ("q", "gate", "kv_indptr", "kv_indices")}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        e2e_api = "gda_decode (per-tensor copies)"
 
-    def e2e_step():
-        for k, t in host.items():
-            dev[k].copy_(t, non_blocking=True)
-        gda.decode(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
-                   out=out, scale=inp["scale"], num_splits=args.splits, k_descale=kd, v_descale=vd)
-        out_h.copy_(out, non_blocking=True)
-        stream.synchronize()   # the host reads the step's result
+        def e2e_step():
+            for k, t in host.items():
+                dev[k].copy_(t, non_blocking=True)
+            gda.decode(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
+                       out=out, scale=inp["scale"], num_splits=args.splits, k_descale=kd, v_descale=vd)
+            out_h.copy_(out, non_blocking=True)
+            stream.synchronize()   # the host reads the step's result
 
     for _ in range(3):
         e2e_step()
@@ -418,7 +439,7 @@ def run_ours(args):
                          "launches_timed": n_t},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": k_e2e,
+                    "d2h_bytes_per_step": d2h, "steps": k_e2e, "api": e2e_api,
                     "us_per_step": round(e2e_s / k_e2e * 1e6, 3)},
             "gpu_launches": 2 * steps,
             "clocks": clocks,

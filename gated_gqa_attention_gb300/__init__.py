@@ -25,7 +25,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "load", "decode", "decode_ex", "decode_noalloc", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
+    "load", "decode", "decode_ex", "decode_noalloc", "decode_step_host", "StepHost", "step_layout", "pack_step", "STEP_MAP_IN", "STEP_MAP_OUT", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
     "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH", "KV_BF16", "KV_E4M3",
 ]
@@ -93,6 +93,11 @@ def load(path: Optional[str] = None):
         lib.gda_qk_norm_rope_kv_write.argtypes = [vp, i64, vp, vp, f32, vp, vp, i32, vp, i64, vp, vp, vp, vp,
                                                   i32, i32, i32, i32, vp]
         lib.gda_qk_norm_rope_kv_write.restype = i32
+        lib.gda_step_layout.argtypes = [i32, i32, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
+        lib.gda_step_layout.restype = ctypes.c_size_t
+        lib.gda_decode_step_host.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, vp, vp, i32, i32, i32, i32, i64, f32,
+                                             i32, i32, i32, vp]
+        lib.gda_decode_step_host.restype = i32
         lib.gda_reserve.argtypes = [i32, i32, i32, i32, i32]
         lib.gda_reserve.restype = i32
         lib.gda_gate.argtypes = [vp, vp, vp, i64, vp]
@@ -247,6 +252,92 @@ def decode_noalloc(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out, scale:
                                      _ptr(kv_indices), _ptr(out), B, Hq, Hkv, D, float(scale), int(num_splits),
                                      _stream(stream)))
     return out
+
+
+def step_layout(B: int, Hq: int, D: int, nnz: int):
+    """``gda_step_layout``: (offsets of q, gate, kv_indptr, kv_indices; total bytes) of
+    one decode step's inputs packed into a single block."""
+    off = (ctypes.c_size_t * 4)()
+    total = load().gda_step_layout(int(B), int(Hq), int(D), int(nnz), off)
+    if total == 0:
+        raise ValueError("gda_step_layout: sizes out of range")
+    return tuple(int(x) for x in off), int(total)
+
+
+def pack_step(host_in, q, gate_t, kv_indptr, kv_indices):
+    """Write one step's CPU tensors into the packed host block ``host_in`` (a uint8
+    CPU tensor, pinned for asynchronous copies) at the offsets of step_layout."""
+    import torch
+    B, Hq, D = q.shape
+    nnz = kv_indices.numel()
+    off, total = step_layout(B, Hq, D, nnz)
+    if host_in.dtype != torch.uint8 or host_in.device.type != "cpu" or host_in.numel() < total:
+        raise ValueError("host_in must be a CPU uint8 tensor of at least %d bytes" % total)
+    parts = ((q, torch.bfloat16), (gate_t, torch.bfloat16), (kv_indptr, torch.int32), (kv_indices, torch.int32))
+    for (t, dt), o in zip(parts, off):
+        if t.dtype != dt:
+            raise TypeError("pack_step: expected %s, got %s" % (dt, t.dtype))
+        b = t.detach().cpu().contiguous().view(torch.uint8).reshape(-1)
+        host_in[o:o + b.numel()].copy_(b)
+    return host_in
+
+
+STEP_MAP_IN, STEP_MAP_OUT = 0x1, 0x2
+
+
+class StepHost:
+    """A decode step bound to fixed buffers: the packed pinned inputs ``host_in``
+    (step_layout), the device staging ``dev_in`` / ``dev_out`` (None when mapped) and
+    the pinned result ``host_out`` [B, Hq, D] bf16.  Everything is checked and
+    marshalled once here; each call is then one ``gda_decode_step_host`` call (copy
+    in, decode, copy out, wait).  ``map_in`` / ``map_out``: the kernels read host_in /
+    write host_out in place over the host-device link instead of copies."""
+
+    def __init__(self, host_in, dev_in, k_pool, v_pool, dev_out, host_out, B: int, Hq: int, nnz: int,
+                 scale: Optional[float] = None, num_splits: int = 0, map_in: bool = False, map_out: bool = False,
+                 synchronize: bool = True, stream=None):
+        import torch
+        _check_tensor("k_pool", k_pool, torch.bfloat16, 3)
+        _check_tensor("v_pool", v_pool, torch.bfloat16, 3, k_pool.device)
+        Hkv, D = k_pool.shape[1], k_pool.shape[2]
+        _, total = step_layout(B, Hq, D, nnz)
+        if host_in.device.type != "cpu" or host_out.device.type != "cpu":
+            raise ValueError("host_in and host_out must be CPU tensors")
+        if host_in.numel() * host_in.element_size() < total:
+            raise ValueError("host_in holds fewer than %d bytes" % total)
+        if not map_in and (dev_in is None or not dev_in.is_cuda or dev_in.numel() * dev_in.element_size() < total):
+            raise ValueError("dev_in must be a CUDA tensor of at least %d bytes" % total)
+        if tuple(host_out.shape) != (B, Hq, D) or host_out.dtype != torch.bfloat16:
+            raise ValueError("host_out must be a [B, Hq, D] bf16 tensor")
+        if not map_out and (dev_out is None or tuple(dev_out.shape) != (B, Hq, D)):
+            raise ValueError("dev_out must be a [B, Hq, D] CUDA tensor")
+        if scale is None:
+            scale = 1.0 / (D ** 0.5)
+        vp = ctypes.c_void_p
+        flags = (STEP_MAP_IN if map_in else 0) | (STEP_MAP_OUT if map_out else 0)
+        self.host_in, self.dev_in, self.dev_out, self.host_out = host_in, dev_in, dev_out, host_out
+        self.k_pool, self.v_pool = k_pool, v_pool   # kept alive with the call's pointers
+        self.in_bytes, self.out_bytes = total, host_out.numel() * 2
+        self._f = load().gda_decode_step_host
+        self._args = (vp(_ptr(host_in)), vp(_ptr(dev_in)), total, vp(_ptr(k_pool)), vp(_ptr(v_pool)),
+                      vp(_ptr(dev_out)), vp(_ptr(host_out)), int(B), int(Hq), int(Hkv), int(D), int(nnz),
+                      float(scale), int(num_splits), flags, 1 if synchronize else 0, _stream(stream))
+
+    def __call__(self):
+        rc = self._f(*self._args)
+        if rc != 0:
+            _check(rc)
+        return self.host_out
+
+
+def decode_step_host(host_in, dev_in, k_pool, v_pool, dev_out, host_out, B: int, Hq: int, nnz: int,
+                     scale: Optional[float] = None, num_splits: int = 0, map_in: bool = False,
+                     map_out: bool = False, synchronize: bool = True, stream=None):
+    """``gda_decode_step_host`` once (see StepHost, which keeps the marshalled call for
+    repeated steps)."""
+    return StepHost(host_in, dev_in, k_pool, v_pool, dev_out, host_out, B, Hq, nnz, scale=scale,
+                    num_splits=num_splits, map_in=map_in, map_out=map_out, synchronize=synchronize,
+                    stream=stream)()
 
 
 def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, workspace=None,

@@ -1,7 +1,8 @@
 // gda_api.cu -- the C ABI of include/gda.h: validation, workspace, planning, launches.
 //
 // Host-side checks run before any CUDA call (so they work without a GPU); nothing
-// is read back from the device on the decode path.  gda_decode keeps one workspace
+// is read back from the device on the decode path (gda_decode_step_host's copy of its
+// result to host memory aside).  gda_decode keeps one workspace
 // per device and grows it with cudaMalloc (never while the stream is capturing);
 // gda_decode_ex takes the caller's workspace and allocates nothing (cuDNN FE-OSS
 // "Gated Attention Block (SM107)", Forward: execute() allocates nothing and is
@@ -514,6 +515,97 @@ int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {
   return ensure_workspace(need, nullptr, false, &ws);
 }
 
+size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]) {
+  if (offsets == nullptr || B < 1 || Hq < 1 || D < 1 || nnz < 0) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t qg = (size_t)B * Hq * D * sizeof(gda_bf16);
+  offsets[0] = 0;
+  offsets[1] = up(qg);
+  offsets[2] = offsets[1] + up(qg);
+  offsets[3] = offsets[2] + up((size_t)(B + 1) * sizeof(int32_t));
+  return offsets[3] + up((size_t)nnz * sizeof(int32_t));
+}
+
+int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, const gda_bf16* k_pool,
+                         const gda_bf16* v_pool, gda_bf16* dev_out, void* host_out, int B, int Hq, int Hkv, int D,
+                         int64_t nnz, float scale, int num_splits, int flags, int synchronize, gda_stream_t stream) {
+  if (B < 0 || nnz < 0) return GDA_ERR_SHAPE;
+  if ((flags & ~(GDA_STEP_MAP_IN | GDA_STEP_MAP_OUT)) != 0) return GDA_ERR_ARG;
+  if (B == 0) return GDA_OK;
+  size_t off[4];
+  const size_t total = gda_step_layout(B, Hq, D, nnz, off);
+  if (total == 0) return GDA_ERR_SHAPE;
+  if (in_bytes != total) return GDA_ERR_SHAPE;
+  const bool map_in = (flags & GDA_STEP_MAP_IN) != 0, map_out = (flags & GDA_STEP_MAP_OUT) != 0;
+  if (host_in == nullptr || host_out == nullptr || (!map_in && dev_in == nullptr) || (!map_out && dev_out == nullptr))
+    return GDA_ERR_NULL;
+  if (!aligned(host_in, 256) && map_in) return GDA_ERR_ALIGN;
+  if (!map_in && !aligned(dev_in, 256)) return GDA_ERR_ALIGN;
+  // the decode's own checks on the views, with placeholder bases for mapped memory
+  // (whose device addresses are only known after a CUDA query), so a bad call
+  // enqueues nothing
+  const unsigned char* din = static_cast<const unsigned char*>(map_in ? host_in : dev_in);
+  gda_args a = {};
+  a.q = reinterpret_cast<const gda_bf16*>(din + off[0]);
+  a.gate = reinterpret_cast<const gda_bf16*>(din + off[1]);
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.kv_indptr = reinterpret_cast<const int32_t*>(din + off[2]);
+  a.kv_indices = reinterpret_cast<const int32_t*>(din + off[3]);
+  a.out = map_out ? static_cast<gda_bf16*>(host_out) : dev_out;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.scale = scale;
+  a.num_splits = num_splits;
+  a.fuse_gate = 1;
+  a.variant = GDA_VARIANT_AUTO;
+  int rc = validate_args(&a);
+  if (rc != GDA_OK) return rc;
+  // mapped host memory: the device address of each pointer (page-locked host memory only)
+  auto device_view = [](const void* h, void** d) -> int {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, h) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GDA_ERR_ARG;
+    }
+    if (pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr) return GDA_ERR_ARG;
+    *d = pa.devicePointer;
+    return GDA_OK;
+  };
+  if (map_in) {
+    void* d = nullptr;
+    rc = device_view(host_in, &d);
+    if (rc != GDA_OK) return rc;
+    const unsigned char* db = static_cast<const unsigned char*>(d);
+    a.q = reinterpret_cast<const gda_bf16*>(db + off[0]);
+    a.gate = reinterpret_cast<const gda_bf16*>(db + off[1]);
+    a.kv_indptr = reinterpret_cast<const int32_t*>(db + off[2]);
+    a.kv_indices = reinterpret_cast<const int32_t*>(db + off[3]);
+  }
+  if (map_out) {
+    void* d = nullptr;
+    rc = device_view(host_out, &d);
+    if (rc != GDA_OK) return rc;
+    if (!aligned(d, 16)) return GDA_ERR_ALIGN;
+    a.out = static_cast<gda_bf16*>(d);
+  }
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  rc = ensure_workspace(gda_workspace_bytes(B, Hq, Hkv, D, num_splits), st, true, &ws);
+  if (rc != GDA_OK) return rc;
+  if (!map_in && cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return GDA_ERR_CUDA;
+  rc = enqueue(&a, ws, st);
+  if (rc != GDA_OK) return rc;
+  const size_t out_bytes = (size_t)B * Hq * D * sizeof(gda_bf16);
+  if (!map_out && cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GDA_ERR_CUDA;
+  if (synchronize && cudaStreamSynchronize(st) != cudaSuccess) return GDA_ERR_CUDA;
+  return GDA_OK;
+}
+
 int gda_gate(const gda_bf16* o, const gda_bf16* gate, gda_bf16* out, int64_t n, gda_stream_t stream) {
   if (n < 0) return GDA_ERR_SHAPE;
   if (n == 0) return GDA_OK;
@@ -608,6 +700,6 @@ const char* gda_status_str(int status) {
   }
 }
 
-int gda_version(void) { return 110; }
+int gda_version(void) { return 111; }
 
 }  // extern "C"

@@ -21,13 +21,15 @@
  * one workspace, execute allocates nothing and reads nothing back).
  *
  * Conventions for every entry point:
- *  - Tensor pointers are DEVICE pointers owned by the caller.  The library never
- *    frees or retains them and never writes to an input.
+ *  - Tensor pointers are DEVICE pointers owned by the caller (gda_decode_step_host
+ *    also takes two HOST pointers, host_in and host_out).  The library never frees or
+ *    retains them and never writes to an input.
  *  - Every tensor is contiguous and 16-byte aligned.  BF16 values are passed as
  *    their 16-bit patterns (gda_bf16).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
  *    stream) and the call returns without waiting for it.  No call except
- *    gda_read_error reads anything back from the device.
+ *    gda_read_error (and gda_decode_step_host, whose job it is) reads anything back
+ *    from the device.
  *  - The return value is GDA_OK (0) or a negative gda_status; on an error nothing
  *    has been enqueued.  Host-side checks (pointers, shapes, alignment, sizes) run
  *    before any CUDA call, so they work without a GPU.
@@ -245,6 +247,50 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
  * so later gda_decode calls allocate nothing (FreeToken PR #781, Summary:
  * initialise before capture). */
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
+
+/* Byte layout of one decode step's inputs packed into a single block, as
+ * gda_decode_step_host takes them: q [B, Hq, D] bf16 at offsets[0] (= 0), gate
+ * [B, Hq, D] bf16 at offsets[1], kv_indptr [B + 1] int32 at offsets[2] and
+ * kv_indices [nnz] int32 at offsets[3], each part starting on a 256-byte boundary.
+ * Returns the block's size in bytes (a multiple of 256), or 0 when a size is out of
+ * range (B < 1, Hq < 1, D < 1, nnz < 0) or offsets is NULL.  The pages have no
+ * counterpart: the block only lets one step's inputs cross the bus in one copy. */
+size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]);
+
+/* One decode step whose inputs and result live in host memory.  It is gda_decode
+ * (FreeToken PR #781, Summary: the decode entry point; cuDNN FE-OSS "Gated Attention
+ * Block (SM107)", Overview stages (4)-(5)) with the host<->device traffic around it,
+ * all enqueued on `stream`:
+ *   1. one copy of in_bytes from host_in (the packed block, gda_step_layout) to dev_in
+ *      (skipped with GDA_STEP_MAP_IN: the kernels then read host_in in place);
+ *   2. gda_decode on the views of dev_in, with the device-resident caches k_pool and
+ *      v_pool, into dev_out [B, Hq, D] (into host_out with GDA_STEP_MAP_OUT);
+ *   3. one copy of dev_out (B * Hq * D bf16) to host_out (skipped with GDA_STEP_MAP_OUT);
+ *   4. with synchronize != 0, a wait for the stream, after which host_out holds the
+ *      gated output and host_in may be reused.
+ * host_in and host_out should be page-locked host memory (cudaHostAlloc, or a pinned
+ * torch tensor) for the copies to be asynchronous; pageable memory works, but the
+ * runtime then stages it through its own buffers.  dev_in is device memory,
+ * 256-byte aligned, at least gda_step_layout(...) bytes; in_bytes must equal that
+ * size.  As for gda_decode, every kv_indices entry must name a row of the pools, and
+ * kv_indptr[B] must equal nnz (index contents are not checked on the host).  The workspace is the library's, as for gda_decode (gda_reserve first
+ * to keep the call allocation-free).  Returns the first failing step's status;
+ * nothing after a failed step is enqueued.  Without synchronize the caller must not
+ * touch host_in or read host_out before the stream has passed this call. */
+int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, const gda_bf16* k_pool,
+                         const gda_bf16* v_pool, gda_bf16* dev_out, void* host_out, int B, int Hq, int Hkv,
+                         int D, int64_t nnz, float scale, int num_splits, int flags, int synchronize,
+                         gda_stream_t stream);
+/* flags of gda_decode_step_host (bitwise or):
+ *   GDA_STEP_MAP_IN   the kernels read the inputs from host_in itself over the
+ *                     host-device link (no copy; dev_in may be NULL);
+ *   GDA_STEP_MAP_OUT  stage 2 writes the result into host_out itself (no copy; dev_out
+ *                     may be NULL).
+ * A mapped pointer must be page-locked host memory that the device can address
+ * (cudaHostAlloc or cudaHostRegister on a system with unified addressing); the call
+ * checks that with cudaPointerGetAttributes and returns GDA_ERR_ARG otherwise. */
+#define GDA_STEP_MAP_IN 0x1
+#define GDA_STEP_MAP_OUT 0x2
 
 /* The step before attention for one decode token per sequence (cuDNN FE-OSS "Gated
  * Attention Block (SM107)", Overview stages (2)+(3), Weights and tables): from the

@@ -227,3 +227,49 @@ def test_prefill_host_validation(lib):
     assert call(B=0, q=0, k=0, v=0, out=0) == OK
     assert call(Sq=0, q=0, k=0, v=0, out=0) == OK
     assert lib.gda_prefill_read_error(None, 0, None) == ERR_NULL
+
+
+def test_step_host_layout_and_validation(lib):
+    # gda_step_layout: 256-byte aligned parts q | gate | kv_indptr | kv_indices
+    lib.gda_step_layout.restype = ctypes.c_size_t
+    lib.gda_step_layout.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                    ctypes.POINTER(ctypes.c_size_t)]
+    off = (ctypes.c_size_t * 4)()
+    total = lib.gda_step_layout(3, 4, 256, 10, off)
+    qg = 3 * 4 * 256 * 2
+    assert list(off) == [0, qg, 2 * qg, 2 * qg + 256] and total == 2 * qg + 512
+    assert all(o % 256 == 0 for o in off) and total % 256 == 0
+    assert lib.gda_step_layout(0, 4, 256, 10, off) == 0
+    assert lib.gda_step_layout(3, 4, 256, -1, off) == 0
+    assert lib.gda_step_layout(3, 4, 256, 10, None) == 0
+    # gda_decode_step_host: every host-side check before any CUDA call
+    vp = ctypes.c_void_p
+    f = lib.gda_decode_step_host
+    f.restype = ctypes.c_int
+    f.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    B, Hq, Hkv, D, nnz = 3, 4, 2, 256, 10
+    total = lib.gda_step_layout(B, Hq, D, nnz, off)
+
+    def call(host_in=4096, dev_in=4096, nbytes=total, k=4096, v=4096, dout=4096, hout=4096, B=B, Hq=Hq, Hkv=Hkv,
+             D=D, nnz=nnz, splits=0, flags=0):
+        return f(vp(host_in) if host_in else None, vp(dev_in) if dev_in else None, nbytes, vp(k) if k else None,
+                 vp(v) if v else None, vp(dout) if dout else None, vp(hout) if hout else None, B, Hq, Hkv, D, nnz,
+                 0.0625, splits, flags, 1, None)
+
+    assert call(B=0) == OK
+    assert call(B=-1) == ERR_SHAPE
+    assert call(nbytes=total - 256) == ERR_SHAPE
+    assert call(nnz=-2) == ERR_SHAPE
+    assert call(host_in=0) == ERR_NULL
+    assert call(hout=0) == ERR_NULL
+    assert call(dev_in=4096 + 128) == ERR_ALIGN
+    assert call(k=0) == ERR_NULL
+    assert call(v=4096 + 8) == ERR_ALIGN
+    assert call(dout=4096 + 2) == ERR_ALIGN
+    assert call(D=128, nbytes=lib.gda_step_layout(B, Hq, 128, nnz, off)) == ERR_UNSUPPORTED
+    assert call(Hkv=3) == ERR_SHAPE
+    assert call(splits=300) == ERR_SPLITS
+    assert call(flags=4) == ERR_ARG                       # an unknown flag
+    assert call(dev_in=0) == ERR_NULL and call(dout=0) == ERR_NULL
+    assert call(host_in=4096 + 16, flags=1) == ERR_ALIGN  # a mapped block starts on 256 bytes

@@ -91,6 +91,44 @@ def test_gda_decode_internal_workspace(gda, small_case):
     assert gda.read_error() == 0
 
 
+def test_decode_step_host_matches_decode(gda, small_case):
+    # host block in, decode, host result out: the same bits as gda.decode on device
+    # tensors, within tolerance of the oracle; a second step reuses the staging with
+    # changed inputs and without waiting inside the call
+    inp, ref = small_case
+    dev = to_cuda(inp)
+    B, Hq, D = inp["q"].shape
+    nnz = inp["kv_indices"].numel()
+    off, total = gda.step_layout(B, Hq, D, nnz)
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    gda.pack_step(host_in, inp["q"], inp["gate"], inp["kv_indptr"], inp["kv_indices"])
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    dev_out = torch.empty_like(dev["q"])
+    host_out = torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory()
+    for splits in (0, 5):
+        want = gda.decode(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
+                          scale=inp["scale"], num_splits=splits)
+        torch.cuda.synchronize()
+        # copies, or the kernels reading / writing the pinned host buffers in place
+        for map_in in (False, True):
+            for map_out in (False, True):
+                host_out.fill_(7.0)
+                gda.decode_step_host(host_in, None if map_in else dev_in, dev["k_pool"], dev["v_pool"],
+                                     None if map_out else dev_out, host_out, B, Hq, nnz, scale=inp["scale"],
+                                     num_splits=splits, map_in=map_in, map_out=map_out)
+                assert np.array_equal(bits(host_out), bits(want)), (splits, map_in, map_out)
+        check_close(bits(host_out), ref.out)
+    # a second step: other q and gate through the same block, no wait inside the call
+    inp2 = dict(inp, q=inp["q"].flip(1).contiguous(), gate=(-inp["gate"]).contiguous())
+    gda.pack_step(host_in, inp2["q"], inp2["gate"], inp["kv_indptr"], inp["kv_indices"])
+    step = gda.StepHost(host_in, None, dev["k_pool"], dev["v_pool"], None, host_out, B, Hq, nnz,
+                        scale=inp["scale"], map_in=True, map_out=True, synchronize=False)
+    step()
+    torch.cuda.current_stream().synchronize()
+    check_close(bits(host_out), reference(inp2).out)
+    assert gda.read_error() == 0
+
+
 def test_fused_equals_unfused_bitwise(gda, small_case):
     inp, ref = small_case
     dev = to_cuda(inp)
