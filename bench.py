@@ -55,6 +55,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="b64_l4096")
     p.add_argument("--splits", type=int, default=0, help="num_splits (0: automatic)")
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 mma, 2 simt, 3 tma ring")
+    p.add_argument("--max-len", type=int, default=-1,
+                   help="host-known bound on the sequence lengths passed to the decode (-1: the batch's "
+                        "longest sequence, as a scheduler knows it; 0: no bound)")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget (cpu_baseline)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--graph", type=int, default=4,
@@ -291,10 +294,16 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     sinks = None if args.sinks is None else torch.full((Hq,), float(args.sinks), dtype=torch.float32, device="cuda")
 
+    max_len = (max(lengths) if len(lengths) else 0) if args.max_len < 0 else args.max_len
+    # the library's dispatch rule for the one-kernel cluster path (include/gda.h, max_len)
+    sms = torch.cuda.get_device_properties(dev["q"].device).multi_processor_count
+    small_path = (0 < max_len <= 2048 and args.splits <= 0 and args.variant == 0 and args.kv == "bf16"
+                  and Hq // Hkv <= 8 and B * Hkv * 8 <= 2 * sms)
+
     def call():
         gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
                       out=out, workspace=ws, scale=inp["scale"], num_splits=args.splits, variant=args.variant,
-                      window=args.window, sinks=sinks, k_descale=kd, v_descale=vd)
+                      window=args.window, sinks=sinks, k_descale=kd, v_descale=vd, max_len=max_len)
 
     ws = torch.empty(gda.workspace_bytes(B, Hq, Hkv, D, args.splits), dtype=torch.uint8, device="cuda")
     gda.workspace_init(ws)
@@ -417,7 +426,8 @@ def run_ours(args):
             v, reps, dt, cores = oracle_sample_rate(inp, args.cpu_seconds)
             cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": "%d full pass(es) of workload %s (B=%d) in %.1f s" % (reps, args.workload, B, dt)}
-        traffic = recorded_traffic(args.workload, sum(att) * Hkv, args.kv)
+        # the recorded counters are stage 1's; the one-kernel path has none recorded
+        traffic = None if small_path else recorded_traffic(args.workload, sum(att) * Hkv, args.kv)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(ms / steps, 6),
@@ -428,12 +438,16 @@ def run_ours(args):
             "config": {"workload": args.workload, "B": B, "lengths": "%d..%d (total %d)" % (min(lengths), max(lengths),
                                                                                           sum(lengths)),
                        "Hq": Hq, "Hkv": Hkv, "D": D, "num_splits": args.splits or "auto", "kv": args.kv,
-                       "variant": {0: "auto(mma)", 1: "mma", 2: "simt", 3: "tma-ring+mma"}[args.variant],
+                       "variant": ("cluster (one kernel)" if small_path else
+                                   {0: "auto(mma)", 1: "mma", 2: "simt", 3: "tma-ring+mma"}[args.variant]),
+                       "max_len_hint": max_len,
                        "bytes_per_call": nbytes,
                        "l2": "inputs larger than L2 (%.0f MB of K/V rows per call), no flush" % (nbytes / 1e6),
                        "parallelism": "replicas x%d" % world, "window": args.window, "sinks": args.sinks,
                        "launch": ("CUDA graph of %d calls, replayed" % args.graph) if args.graph > 0 else "eager"},
-            "roofline": {"bound": "hbm", "kernel": "stage1" if args.kv == "bf16" else "stage1_fp8", "achieved": round(achieved, 1), "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": ("small_decode (one cluster kernel)" if small_path else
+                                                    "stage1" if args.kv == "bf16" else "stage1_fp8"),
+                         "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                          "traffic": traffic, "algorithmic_bytes": s1_bytes, "avg_us": round(s1_us, 3),
                          "launches_timed": n_t},

@@ -58,7 +58,7 @@ class _Args(ctypes.Structure):
         ("scale", ctypes.c_float), ("num_splits", ctypes.c_int), ("fuse_gate", ctypes.c_int),
         ("check_indices", ctypes.c_int), ("variant", ctypes.c_int), ("min_chunk", ctypes.c_int),
         ("window", ctypes.c_int), ("sinks", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
-        ("k_descale", ctypes.c_float), ("v_descale", ctypes.c_float),
+        ("k_descale", ctypes.c_float), ("v_descale", ctypes.c_float), ("max_len", ctypes.c_int),
     ]
 
 
@@ -343,12 +343,14 @@ def decode_step_host(host_in, dev_in, k_pool, v_pool, dev_out, host_out, B: int,
 def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, workspace=None,
               scale: Optional[float] = None, num_splits: int = 0, fuse_gate: bool = True, lse=None,
               check_indices: bool = False, variant: int = VARIANT_AUTO, min_chunk: int = 0,
-              window: int = 0, sinks=None, stream=None, k_descale: float = 1.0, v_descale: float = 1.0):
+              window: int = 0, sinks=None, stream=None, k_descale: float = 1.0, v_descale: float = 1.0,
+              max_len: int = 0):
     """``gda_decode_ex``: caller workspace (allocated here when None), optional LSE
     output, the unfused first half (``fuse_gate=False``), device index checks, the
     stage-1 variant, a sliding window (last ``window`` positions), per-head
-    attention sinks (``sinks``: [Hq] float32 CUDA tensor of logits) and, for e4m3
-    pools, the per-tensor descales."""
+    attention sinks (``sinks``: [Hq] float32 CUDA tensor of logits), for e4m3
+    pools the per-tensor descales, and ``max_len``: a host-known bound on every
+    sequence's length (0: none), which lets small batches run as one cluster kernel."""
     import torch
     kv = _decode_checks(q, gate_t if fuse_gate else None, k_pool, v_pool, kv_indptr, kv_indices, out)
     B, Hq, D = q.shape
@@ -373,7 +375,7 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
               scale=float(scale), num_splits=int(num_splits), fuse_gate=1 if fuse_gate else 0,
               check_indices=1 if check_indices else 0, variant=int(variant), min_chunk=int(min_chunk),
               window=int(window), sinks=_ptr(sinks), kv_dtype=kv, k_descale=float(k_descale),
-              v_descale=float(v_descale))
+              v_descale=float(v_descale), max_len=int(max_len))
     _check(load().gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

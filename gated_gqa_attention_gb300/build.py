@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libgda.so")
-SOURCES = ["gda_api.cu", "gda_stage1.cu", "gda_stage1_fp8.cu", "gda_stage1_tma.cu", "gda_stage2.cu",
+SOURCES = ["gda_api.cu", "gda_stage1.cu", "gda_stage1_fp8.cu", "gda_stage1_tma.cu", "gda_stage2.cu", "gda_small.cu",
            "gda_prep.cu", "gda_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

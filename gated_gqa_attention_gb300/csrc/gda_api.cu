@@ -17,6 +17,7 @@
 #include "gda_device.cuh"
 #include "gda_kernels.h"
 #include "gda_prefill.h"
+#include "gda_small.h"
 
 namespace {
 
@@ -85,7 +86,7 @@ int validate_args(const gda_args* a) {
   if (rc != GDA_OK) return rc;
   if (a->check_indices && a->num_slots < 0) return GDA_ERR_SHAPE;
   if (a->variant < 0 || a->variant > GDA_VARIANT_TMA) return GDA_ERR_UNSUPPORTED;
-  if (a->min_chunk < 0 || a->window < 0) return GDA_ERR_SHAPE;
+  if (a->min_chunk < 0 || a->window < 0 || a->max_len < 0) return GDA_ERR_SHAPE;
   if (a->kv_dtype != GDA_KV_BF16 && a->kv_dtype != GDA_KV_E4M3) return GDA_ERR_UNSUPPORTED;
   if (a->kv_dtype == GDA_KV_E4M3) {
     if (a->variant != GDA_VARIANT_AUTO && a->variant != GDA_VARIANT_MMA) return GDA_ERR_UNSUPPORTED;
@@ -112,6 +113,42 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
     sms = sm_count(dev);
   }
   if (sms <= 0) return GDA_ERR_CUDA;
+
+  // small batches with a host-known length bound: one cluster kernel (no partials)
+  if (a->max_len > 0 && a->max_len <= gda::kSmallMaxLen && a->num_splits <= 0 && a->variant == GDA_VARIANT_AUTO &&
+      a->kv_dtype == GDA_KV_BF16 && !a->check_indices && a->Hq / a->Hkv <= gda::kG &&
+      (long long)a->B * a->Hkv * gda::kSmallCluster <= 2LL * sms) {
+    gda::SmallParams ps;
+    ps.q = reinterpret_cast<const __nv_bfloat16*>(a->q);
+    ps.gate = reinterpret_cast<const __nv_bfloat16*>(a->gate);
+    ps.k_pool = reinterpret_cast<const __nv_bfloat16*>(a->k_pool);
+    ps.v_pool = reinterpret_cast<const __nv_bfloat16*>(a->v_pool);
+    ps.indptr = a->kv_indptr;
+    ps.indices = a->kv_indices;
+    ps.out = reinterpret_cast<__nv_bfloat16*>(a->out);
+    ps.lse_out = a->lse;
+    ps.sinks = a->sinks;
+    ps.B = a->B;
+    ps.Hq = a->Hq;
+    ps.Hkv = a->Hkv;
+    ps.G = a->Hq / a->Hkv;
+    ps.scale_log2 = a->scale * 1.44269504088896340736f;
+    ps.window = a->window;
+    ps.fuse_gate = a->fuse_gate ? 1 : 0;
+    cudaEvent_t s_end = nullptr;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (g_tused < g_tmax) {
+        if (cudaEventRecord(g_tev[2 * g_tused], stream) != cudaSuccess) return GDA_ERR_CUDA;
+        s_end = g_tev[2 * g_tused + 1];
+        ++g_tused;
+      }
+    }
+    if (gda::launch_small(ps, stream) != cudaSuccess) return GDA_ERR_CUDA;
+    if (s_end != nullptr && cudaEventRecord(s_end, stream) != cudaSuccess) return GDA_ERR_CUDA;
+    return GDA_OK;
+  }
+
   const Layout l = layout(a->B, a->Hq, a->Hkv, a->D, a->num_splits);
   unsigned char* base = static_cast<unsigned char*>(ws);
   const int npass = passes(a->Hq, a->Hkv);
@@ -561,6 +598,8 @@ int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, con
   a.num_splits = num_splits;
   a.fuse_gate = 1;
   a.variant = GDA_VARIANT_AUTO;
+  // nnz bounds every sequence's length: small steps take the one-kernel path
+  a.max_len = nnz < (int64_t)0x7FFFFFFF ? (int)nnz : 0x7FFFFFFF;
   int rc = validate_args(&a);
   if (rc != GDA_OK) return rc;
   // mapped host memory: the device address of each pointer (page-locked host memory only)
@@ -700,6 +739,6 @@ const char* gda_status_str(int status) {
   }
 }
 
-int gda_version(void) { return 111; }
+int gda_version(void) { return 112; }
 
 }  // extern "C"

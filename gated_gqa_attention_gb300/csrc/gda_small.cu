@@ -1,0 +1,271 @@
+// gda_small.cu -- single-pass gated decode for small batches on sm_103a.
+//
+// The same result as stage 1 + stage 2 (FreeToken PR #781, Summary: split-KV
+// partial softmax per split, FP32 log-sum-exp merge, the BF16 gate in the merge's
+// epilogue; cuDNN FE-OSS "Gated Attention Block (SM107)", Overview stages (4)-(5)),
+// computed in one launch for batches whose latency, not bandwidth, sets the time.
+//
+// One thread-block cluster of 8 CTAs per (sequence b, KV head): CTA r takes the r-th
+// eighth of the sequence's attended positions, in chunks of 64 whose K and V rows
+// the CTA's 256 threads bring into shared memory (cp.async, two buffers, the next
+// chunk in flight during the current one).  Per chunk, on the tensor cores
+// (mma.sync m16n8k16, BF16 in, FP32 accumulate; the G <= 8 query heads are the rows):
+//   S = Q K^T     warp w takes positions 8w .. 8w + 7 (16 k-steps over the 256 dims);
+//   softmax       the chunk's max per head through shared memory, an online update of
+//                 the running max (log2 units) and sum, P = 2^(S - max) as BF16;
+//   O += P V      warp w owns head dimensions 32w .. 32w + 31 of every head.
+// Each CTA then stores its state of query head G*kvh + g into the shared memory of
+// CTA g of the cluster (distributed shared memory); after one cluster barrier, CTA g
+// merges the 8 states (with the attention sink), divides by the sum, rounds to BF16,
+// applies the BF16 gate, and writes out and lse.  No partials go through HBM and no
+// second kernel runs.
+#include "gda_device.cuh"
+#include "gda_small.h"
+
+namespace gda {
+
+namespace {
+
+constexpr int kSC = kSmallCluster;  // CTAs per cluster
+constexpr int kSW = 8;              // warps per CTA
+constexpr int kChunk = 64;          // positions per shared-memory chunk (8 per warp in S)
+
+struct SmallSmem {
+  unsigned char k[2][kChunk][kSmemRow];  // K rows of a chunk (padded rows: conflict-free
+  unsigned char v[2][kChunk][kSmemRow];  // ldmatrix), V rows; two buffers
+  uint32_t p[kG][kChunk / 2];            // P of the chunk: BF16 pairs [head][position pair]
+  float wmax[kSW][kG];                   // per warp and head: max of the warp's 8 scores
+  float wsum[kSW][kG];                   // per warp and head: sum of its BF16 probabilities
+  float o[kSC][kD];  // incoming: unnormalised O of CTA x for the head this CTA finalises
+  float m[kSC];      // its running max (log2 units)
+  float l[kSC];      // its sum
+};
+constexpr size_t kSmallSmem = sizeof(SmallSmem);
+
+// all threads of all CTAs of the cluster: writes before it (also into other CTAs'
+// shared memory) are visible after it
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the address that p (in this CTA's shared memory) has in CTA `rank`'s shared memory
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+// 16 bytes global -> shared; src_bytes = 0 zero-fills the destination
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ float quad_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(kSC, 1, 1) __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SmallSmem& sm = *reinterpret_cast<SmallSmem*>(smem_raw);
+  const int r = blockIdx.x;  // rank in the cluster (the grid's x extent is the cluster)
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = lane >> 2, qd = lane & 3;  // fragment row (query head of the group) and quad lane
+  const int G = p.G;
+
+  // independent loads first: the range, Q as A fragments (rows 8..15 and heads >= G
+  // are zero), the gate element this CTA finalises (its sigmoid comes later)
+  int L;
+  long long base;
+  seq_range(p.indptr, b, p.window, &L, &base);
+  uint32_t qa[16][2];  // k-step ks: a0 = q[h][16 ks + 2 qd ..], a2 = q[h][16 ks + 8 + 2 qd ..]
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((size_t)b * p.Hq + kvh * G + h) * kD);
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks) {
+      qa[ks][0] = (h < G) ? __ldg(qrow + 8 * ks + qd) : 0u;
+      qa[ks][1] = (h < G) ? __ldg(qrow + 8 * ks + 4 + qd) : 0u;
+    }
+  }
+  const int hf = kvh * G + r;  // the query head this CTA finalises (r < G)
+  uint16_t gbits = 0;
+  if (r < G && p.fuse_gate) gbits = __bfloat16_as_ushort(p.gate[((size_t)b * p.Hq + hf) * kD + tid]);
+
+  const int c = (L + kSC - 1) / kSC;
+  const int lo = min(L, r * c), hi = min(L, lo + c);
+  const int nch = (hi - lo + kChunk - 1) / kChunk;
+  const size_t row_stride = (size_t)p.Hkv * kD;  // elements between slots
+
+  // chunk c into buffer c & 1: thread t copies pieces t % 4 + 4 k (k < 8) of the K and V
+  // rows of position t / 4; positions past the range are zero-filled
+  auto load_chunk = [&](int cidx) {
+    const int j = tid >> 2, pos = lo + cidx * kChunk + j;
+    const bool ok = pos < hi;
+    const int slot = ok ? __ldg(p.indices + base + pos) : 0;
+    const size_t off = (size_t)slot * row_stride + (size_t)kvh * kD;
+    const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_pool + (ok ? off : 0));
+    const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.v_pool + (ok ? off : 0));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int piece = qd + 4 * k;
+      cp_async16(&sm.k[cidx & 1][j][piece * 16], ks + piece * 16, ok ? 16u : 0u);
+      cp_async16(&sm.v[cidx & 1][j][piece * 16], vs + piece * 16, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  if (nch > 0) load_chunk(0);
+  if (nch > 1) load_chunk(1);
+
+  float m_run = -INFINITY, l_run = 0.0f;  // head h (identical in every thread of row h)
+  float oacc[4][4];                        // O of head h, dims 32 warp + 8 nt + 2 qd .. (c0, c1)
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.0f;
+
+  for (int cidx = 0; cidx < nch; ++cidx) {
+    if (cidx + 1 < nch) cp_async_wait<1>(); else cp_async_wait<0>();
+    __syncthreads();
+    const int buf = cidx & 1;
+    const int n = min(kChunk, hi - lo - cidx * kChunk);  // positions in this chunk
+
+    // S = Q K^T for positions 8 warp .. 8 warp + 7
+    float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    {
+      // ldmatrix x4: matrix i = dims 8 i .. of rows 8 warp + lane % 8 -> b0, b1 of two k-steps
+      const uint32_t kaddr = smem_u32(&sm.k[buf][8 * warp + (lane & 7)][0]) + (lane >> 3) * 16;
+#pragma unroll
+      for (int kp = 0; kp < 8; ++kp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kaddr + kp * 64, b0, b1, b2, b3);
+        mma_bf16_16816(sacc, qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
+        mma_bf16_16816(sacc, qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+      }
+    }
+    // scores (log2 units) of positions 8 warp + 2 qd, + 1; past the chunk's end -inf
+    const int j0 = 8 * warp + 2 * qd;
+    const float s0 = (j0 < n) ? sacc[0] * p.scale_log2 : -INFINITY;
+    const float s1 = (j0 + 1 < n) ? sacc[1] * p.scale_log2 : -INFINITY;
+    const float wm = quad_max(fmaxf(s0, s1));
+    if (qd == 0) sm.wmax[warp][h] = wm;
+    __syncthreads();
+    float cmax = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kSW; ++w) cmax = fmaxf(cmax, sm.wmax[w][h]);
+    const float m_new = fmaxf(m_run, cmax);
+    const float alpha = (m_new == -INFINITY) ? 1.0f : safe_exp2_diff(m_run, m_new);
+    float p0 = 0.0f, p1 = 0.0f;
+    if (m_new != -INFINITY) {
+      p0 = safe_exp2_diff(s0, m_new);
+      p1 = safe_exp2_diff(s1, m_new);
+    }
+    const uint32_t pp = pack_bf16x2(p0, p1);
+    sm.p[h][4 * warp + qd] = pp;
+    const float ws = quad_sum(__uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u));
+    if (qd == 0) sm.wsum[warp][h] = ws;
+    __syncthreads();
+    float csum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kSW; ++w) csum += sm.wsum[w][h];
+    l_run = l_run * alpha + csum;
+    m_run = m_new;
+
+    // O += P V over the chunk's 64 positions, this warp's 32 dims (4 n-tiles)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      oacc[nt][0] *= alpha;
+      oacc[nt][1] *= alpha;
+    }
+#pragma unroll
+    for (int kt = 0; kt < kChunk / 16; ++kt) {
+      const uint32_t a0 = sm.p[h][8 * kt + qd], a2 = sm.p[h][8 * kt + 4 + qd];
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        // x4.trans: positions 16 kt + lane % 8 (+ 8 for matrices 1, 3), dims of n-tiles 2 np, 2 np + 1
+        const int pos = 16 * kt + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int dim = 32 * warp + 16 * np + 8 * (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(smem_u32(&sm.v[buf][pos][dim * 2]), b0, b1, b2, b3);
+        mma_bf16_16816(oacc[2 * np], a0, 0u, a2, 0u, b0, b1);
+        mma_bf16_16816(oacc[2 * np + 1], a0, 0u, a2, 0u, b2, b3);
+      }
+    }
+    __syncthreads();  // buffer buf and the P tile are free
+    if (cidx + 2 < nch) load_chunk(cidx + 2);
+  }
+
+  // this CTA's state of head h into slot r of the CTA that finalises it
+  if (h < G) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int dim = 32 * warp + 8 * nt + 2 * qd;
+      st_cluster_v2(cluster_addr(&sm.o[r][dim], (uint32_t)h), oacc[nt][0], oacc[nt][1]);
+    }
+    if (warp == 0 && qd == 0) {
+      st_cluster_f32(cluster_addr(&sm.m[r], (uint32_t)h), m_run);
+      st_cluster_f32(cluster_addr(&sm.l[r], (uint32_t)h), l_run);
+    }
+  }
+  const uint16_t sig = (r < G && p.fuse_gate) ? sigmoid_bf16(gbits) : (uint16_t)0;
+
+  // every state has arrived where it is merged after this; afterwards each CTA reads
+  // only its own shared memory, so no second barrier is needed before leaving
+  cluster_sync_all();
+
+  if (r < G) {
+    // query head hf: merge the kSC states (and the sink), normalise, round, gate
+    const float sink2 = (p.sinks != nullptr) ? __ldg(p.sinks + hf) * 1.44269504088896340736f : -INFINITY;
+    float M = sink2;
+#pragma unroll
+    for (int x = 0; x < kSC; ++x) M = fmaxf(M, sm.m[x]);
+    float acc = 0.0f, W = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int x = 0; x < kSC; ++x) {
+        const float f = safe_exp2_diff(sm.m[x], M);
+        acc = fmaf(sm.o[x][tid], f, acc);
+        W = fmaf(sm.l[x], f, W);
+      }
+      if (sink2 != -INFINITY) W += exp2f(sink2 - M);
+      acc /= W;
+    }
+    const uint16_t ob = float_to_bf16_bits(acc);
+    const size_t row = ((size_t)b * p.Hq + hf) * kD;
+    reinterpret_cast<uint16_t*>(p.out)[row + tid] = p.fuse_gate ? gate_product_bf16(ob, sig) : ob;
+    if (p.lse_out != nullptr && tid == 0)
+      p.lse_out[(size_t)b * p.Hq + hf] = (M == -INFINITY) ? -INFINITY : (M + log2f(W)) * 0.69314718055994530942f;
+  }
+}
+
+cudaError_t launch_small(const SmallParams& p, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(small_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const dim3 grid((unsigned)kSC, (unsigned)p.Hkv, (unsigned)p.B);
+  small_decode_kernel<<<grid, kSW * 32, kSmallSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gda

@@ -120,6 +120,15 @@ typedef enum gda_status {
  *               E4M3 is served by GDA_VARIANT_AUTO / GDA_VARIANT_MMA only.
  *   k_descale, v_descale  per-tensor factors of an e4m3 cache (finite; else GDA_ERR_ARG);
  *               not used for bf16 pools.
+ *   max_len     0, or an upper bound on every sequence's KV length that the caller knows
+ *               on the host (a scheduler's batch maximum).  With a bound of at most
+ *               2048, automatic splits (num_splits <= 0), GDA_VARIANT_AUTO, bf16 pools,
+ *               no check_indices, Hq / Hkv <= 8 and B * Hkv * 8 <= 2 * SMs, the call
+ *               runs as ONE kernel: a thread-block cluster of 8 CTAs per (sequence, KV
+ *               head) that merges its partial softmax states in distributed shared
+ *               memory and applies the gate, with no workspace traffic.  The result
+ *               is the same function within the tolerance of the split path.  A bound
+ *               below an actual length still gives the right result, only slower.
  * (FreeToken PR #781, Automatic dispatch and Correctness: window, sinks, custom scale
  * and non-power-of-two GQA groups are the cases of the general path.)
  */
@@ -145,6 +154,7 @@ typedef struct gda_args {
     int kv_dtype;
     float k_descale;
     float v_descale;
+    int max_len;
 } gda_args;
 
 /* Bytes of workspace gda_decode_ex needs for these sizes (FreeToken PR #781 Summary:

@@ -1,0 +1,145 @@
+"""The one-kernel small-batch decode path (a thread-block cluster of 8 CTAs per
+(sequence, KV head), partial states merged in distributed shared memory, the gate
+in the same kernel), taken when the caller passes a host-known length bound
+max_len <= 2048.  Against the FP64 oracle under the tolerance of the other decode
+tests: |gpu - oracle| <= 4e-3 + 1.6e-2 |oracle|; windows, sinks, lse, empty
+sequences, GQA group sizes, the ungated output, and the page's B1 / B4 workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_gqa_attention_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 4e-3, 1.6e-2
+LENS = [0, 1, 5, 63, 64, 65, 200, 1000, 16, 129, 2048]
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def check_close(got, want):
+    g = oracle.double_from_bf16(got)
+    w = oracle.double_from_bf16(want)
+    bad = np.abs(g - w) > ATOL + RTOL * np.abs(w)
+    assert not bad.any(), "%d / %d out of tolerance, worst %.3g" % (bad.sum(), bad.size, np.abs(g - w).max())
+
+
+def to_cuda(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def run(gda, inp, max_len, workspace=None, **kw):
+    d = to_cuda(inp)
+    sinks = kw.pop("sinks", None)
+    out = gda.decode_ex(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"],
+                        scale=d["scale"], max_len=max_len, workspace=workspace,
+                        sinks=None if sinks is None else torch.as_tensor(sinks, dtype=torch.float32).cuda(), **kw)
+    torch.cuda.synchronize()
+    return bits(out)
+
+
+def reference(inp, **kw):
+    return oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"],
+                         inp["kv_indices"], inp["scale"], **kw)
+
+
+@pytest.fixture(scope="module")
+def batch():
+    inp = workloads.make(LENS, seed=211, layout="perm", pool_slots=8000)
+    return inp, reference(inp)
+
+
+def test_cluster_path_is_taken_and_matches(gda, batch):
+    # the cluster path writes no partials: a sentinel-filled workspace stays untouched
+    # past its header, while the split path (no bound) fills it
+    inp, ref = batch
+    B, Hq, D = inp["q"].shape
+    Hkv = inp["k_pool"].shape[1]
+    nbytes = gda.workspace_bytes(B, Hq, Hkv, D, 0)
+    ws = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    gda.workspace_init(ws)
+    got = run(gda, inp, max(LENS), workspace=ws)
+    check_close(got, ref.out)
+    assert bool((ws[256:] == 0xA5).all()), "partials were written: the split path ran"
+    got2 = run(gda, inp, 0, workspace=ws)
+    check_close(got2, ref.out)
+    assert not bool((ws[256:] == 0xA5).all())
+
+
+def test_bound_below_the_lengths_is_still_correct(gda, batch):
+    inp, ref = batch
+    check_close(run(gda, inp, 5), ref.out)
+
+
+def test_deterministic(gda, batch):
+    inp, _ = batch
+    assert np.array_equal(run(gda, inp, 2048), run(gda, inp, 2048))
+
+
+@pytest.mark.parametrize("window", [1, 7, 64, 300, 100_000])
+def test_window(gda, batch, window):
+    inp, _ = batch
+    check_close(run(gda, inp, 2048, window=window), reference(inp, window=window).out)
+
+
+def test_sinks_lse_and_empty_rows(gda, batch):
+    inp, _ = batch
+    rng = np.random.default_rng(7)
+    sinks = rng.normal(0.0, 3.0, 16).astype(np.float32)
+    sinks[3] = -np.inf                     # a head without a sink
+    sinks[7] = 40.0                        # a sink that dominates the softmax
+    ref = reference(inp, sinks=sinks.astype(np.float64))
+    lse = torch.empty(len(LENS), 16, dtype=torch.float32, device="cuda")
+    got = run(gda, inp, 2048, sinks=sinks, lse=lse)
+    check_close(got, ref.out)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
+    assert np.all(got[0] == 0)             # L = 0: O = 0 whatever the sink
+
+
+def test_lse_without_sinks(gda, batch):
+    inp, ref = batch
+    lse = torch.empty(len(LENS), 16, dtype=torch.float32, device="cuda")
+    check_close(run(gda, inp, 2048, lse=lse), ref.out)
+    got = lse.cpu().numpy()
+    assert np.all(np.isneginf(got[0])) and np.all(np.isneginf(ref.lse[0]))
+    np.testing.assert_allclose(got[1:], ref.lse[1:], atol=2e-3, rtol=1e-4)
+
+
+def test_ungated_output(gda, batch):
+    inp, ref = batch
+    check_close(run(gda, inp, 2048, fuse_gate=False), ref.o_bf16)
+
+
+# group sizes the path takes (G <= 8 and B * Hkv * 8 <= 2 * SMs for B = 5)
+@pytest.mark.parametrize("hq,hkv", [(6, 2), (16, 4), (12, 2), (14, 2), (4, 4), (2, 1), (8, 1)])
+def test_gqa_group_sizes(gda, hq, hkv):
+    inp = workloads.make([1, 37, 300, 0, 129], seed=500 + hq + hkv, hq=hq, hkv=hkv, layout="perm", pool_slots=1000)
+    check_close(run(gda, inp, 300), reference(inp).out)
+
+
+@pytest.mark.parametrize("key", ["b1_l512", "b4_ragged"])
+def test_page_workloads(gda, key):
+    inp = workloads.make_workload(key)
+    check_close(run(gda, inp, int(max(inp["lengths"]))), reference(inp).out)
+
+
+def test_step_host_takes_the_cluster_path(gda):
+    # gda_decode_step_host passes nnz as the bound: B4 ragged runs as one kernel, and
+    # its result equals decode_ex with the same bound bit for bit
+    inp = workloads.make_workload("b4_ragged")
+    d = to_cuda(inp)
+    B, Hq, D = inp["q"].shape
+    nnz = inp["kv_indices"].numel()
+    _, total = gda.step_layout(B, Hq, D, nnz)
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    gda.pack_step(host_in, inp["q"], inp["gate"], inp["kv_indptr"], inp["kv_indices"])
+    host_out = torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory()
+    gda.decode_step_host(host_in, None, d["k_pool"], d["v_pool"], None, host_out, B, Hq, nnz, scale=inp["scale"],
+                         map_in=True, map_out=True)
+    want = run(gda, inp, nnz)
+    assert np.array_equal(bits(host_out), want)
+    check_close(bits(host_out), reference(inp).out)
