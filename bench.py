@@ -55,6 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="b64_l4096")
     p.add_argument("--splits", type=int, default=0, help="num_splits (0: automatic)")
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 mma, 2 simt, 3 tma ring")
+    p.add_argument("--no-extra-timing", action="store_true",
+                   help="skip the pages'-method and cold-cache timings")
     p.add_argument("--max-len", type=int, default=-1,
                    help="host-known bound on the sequence lengths passed to the decode (-1: the batch's "
                         "longest sequence, as a scheduler knows it; 0: no bound)")
@@ -237,20 +239,22 @@ def stage1_bytes(lengths, hq, hkv, d, kv_bytes=2):
     return n * hkv * d * kv_bytes * 2 + len(lengths) * hq * d * 2
 
 
-def oracle_sample_rate(inp, budget_s: float):
-    """Time the FP64 oracle on the host: full batches until the budget is spent."""
+def oracle_sample_rate(inp, budget_s: float, nthreads: int = 0):
+    """Time the FP64 oracle on the host: full batches until the budget is spent
+    (nthreads 0: every core the oracle's OpenMP uses; 1: one core)."""
     import oracle
     w = inp["workload"]
     nbytes = algorithmic_bytes(inp["lengths"], w.hq, w.hkv, w.head_dim, inp["k_pool"].element_size())
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
-                      inp["scale"], want=("out",), k_descale=inp["k_descale"], v_descale=inp["v_descale"])
+                      inp["scale"], want=("out",), k_descale=inp["k_descale"], v_descale=inp["v_descale"],
+                      nthreads=nthreads)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s or reps >= 100:
             break
-    return nbytes * reps / dt / 1e9, reps, dt, oracle.max_threads()
+    return nbytes * reps / dt / 1e9, reps, dt, (oracle.max_threads() if nthreads == 0 else nthreads)
 
 
 # ------------------------------------------------------------------ our arm
@@ -377,6 +381,43 @@ def run_ours(args):
     achieved = s1_bytes / (s1_us / 1e6) / 1e9
     peak, peak_kind = measured_hbm_peak()
 
+    # ---- the pages' warm method (a CUDA graph of R calls, 14 samples of 50 replays,
+    # the median), and a cold figure: 512 MiB (4x L2) read before each timed call (a
+    # read leaves clean lines, so no write-back lands in the timed call), then a
+    # device-side delay so the call is already enqueued when its start event fires;
+    # the median over the calls
+    pages_method = None
+    if args.graph > 0 and not args.no_extra_timing:
+        per = []
+        for _ in range(14):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(50):
+                graph.replay()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            per.append(a0.elapsed_time(a1) * 1e3 / (50 * args.graph))
+        per.sort()
+        pages_method = {"us_per_call_median": round(0.5 * (per[6] + per[7]), 3), "samples": 14,
+                        "replays_per_sample": 50, "calls_per_replay": args.graph}
+    cold = None
+    if not args.no_extra_timing:
+        flush = torch.ones(64 << 20, dtype=torch.int64, device=dev["q"].device)  # 512 MiB
+        cs = []
+        for _ in range(30):
+            flush.sum()
+            torch.cuda._sleep(200000)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            call()
+            c1.record(stream)
+            torch.cuda.synchronize()
+            cs.append(c0.elapsed_time(c1) * 1e3)
+        cs.sort()
+        cold = {"us_per_call_median": round(0.5 * (cs[14] + cs[15]), 3), "samples": 30,
+                "evicted_bytes_before_each": 512 << 20, "launch": "eager, enqueued ahead"}
+        del flush
+
     # ---- end to end with host buffers: per step, the inputs go from pinned host memory
     # to the device, the decode runs, the result comes back and the host waits for it
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -426,6 +467,9 @@ def run_ours(args):
             v, reps, dt, cores = oracle_sample_rate(inp, args.cpu_seconds)
             cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": "%d full pass(es) of workload %s (B=%d) in %.1f s" % (reps, args.workload, B, dt)}
+            v1, reps1, dt1, _ = oracle_sample_rate(inp, max(1.0, args.cpu_seconds / 3), nthreads=1)
+            cpu["one_core"] = {"value": round(v1, 4), "unit": "GB/s",
+                               "sample": "%d full pass(es) in %.1f s on 1 thread" % (reps1, dt1)}
         # the recorded counters are stage 1's; the one-kernel path has none recorded
         traffic = None if small_path else recorded_traffic(args.workload, sum(att) * Hkv, args.kv)
         line = {
@@ -455,7 +499,9 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": k_e2e, "api": e2e_api,
                     "us_per_step": round(e2e_s / k_e2e * 1e6, 3)},
-            "gpu_launches": 2 * steps,
+            "gpu_launches": (1 if small_path else 2) * steps,
+            "timing_pages_method": pages_method,
+            "cold": cold,
             "clocks": clocks,
             "device_error_word": err,
             "gpu": torch.cuda.get_device_name(dev_id),
