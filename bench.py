@@ -300,9 +300,8 @@ def run_ours(args):
 
     max_len = (max(lengths) if len(lengths) else 0) if args.max_len < 0 else args.max_len
     # the library's dispatch rule for the one-kernel cluster path (include/gda.h, max_len)
-    sms = torch.cuda.get_device_properties(dev["q"].device).multi_processor_count
     small_path = (0 < max_len <= 2048 and args.splits <= 0 and args.variant == 0 and args.kv == "bf16"
-                  and Hq // Hkv <= 8 and B * Hkv * 8 <= 2 * sms)
+                  and Hq // Hkv <= 8 and B * Hkv <= gda.small_path_clusters())
 
     def call():
         gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],

@@ -117,7 +117,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   // small batches with a host-known length bound: one cluster kernel (no partials)
   if (a->max_len > 0 && a->max_len <= gda::kSmallMaxLen && a->num_splits <= 0 && a->variant == GDA_VARIANT_AUTO &&
       a->kv_dtype == GDA_KV_BF16 && !a->check_indices && a->Hq / a->Hkv <= gda::kG &&
-      (long long)a->B * a->Hkv * gda::kSmallCluster <= 2LL * sms) {
+      (long long)a->B * a->Hkv <= (long long)gda::small_max_clusters()) {
     gda::SmallParams ps;
     ps.q = reinterpret_cast<const __nv_bfloat16*>(a->q);
     ps.gate = reinterpret_cast<const __nv_bfloat16*>(a->gate);
@@ -551,6 +551,8 @@ int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {
   void* ws = nullptr;
   return ensure_workspace(need, nullptr, false, &ws);
 }
+
+int gda_small_path_clusters(void) { return gda::small_max_clusters(); }
 
 size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]) {
   if (offsets == nullptr || B < 1 || Hq < 1 || D < 1 || nnz < 0) return 0;

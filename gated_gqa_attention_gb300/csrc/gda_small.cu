@@ -252,17 +252,47 @@ __global__ void __cluster_dims__(kSC, 1, 1) __launch_bounds__(kSW * 32, 1) small
   }
 }
 
+namespace {
+bool g_small_attr[64] = {};
+int g_small_clusters[64] = {};
+
+cudaError_t small_attr(int dev) {
+  if (!g_small_attr[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(small_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
+    if (e != cudaSuccess) return e;
+    g_small_attr[dev] = true;
+  }
+  return cudaSuccess;
+}
+}  // namespace
+
+int small_max_clusters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (g_small_clusters[dev] == 0) {
+    if (small_attr(dev) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)kSC, 1, 1);
+    cfg.blockDim = dim3(kSW * 32, 1, 1);
+    cfg.dynamicSmemBytes = kSmallSmem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, small_decode_kernel, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    g_small_clusters[dev] = n;
+  }
+  return g_small_clusters[dev];
+}
+
 cudaError_t launch_small(const SmallParams& p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(small_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  e = small_attr(dev);
+  if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)kSC, (unsigned)p.Hkv, (unsigned)p.B);
   small_decode_kernel<<<grid, kSW * 32, kSmallSmem, stream>>>(p);
   return cudaGetLastError();

@@ -29,4 +29,9 @@ struct SmallParams {
 // grid (kSmallCluster, Hkv, B) in clusters of kSmallCluster CTAs
 cudaError_t launch_small(const SmallParams& p, cudaStream_t stream);
 
+// How many of the kernel's clusters the current device runs at once (one CTA per SM
+// and 8 SMs of one GPC per cluster: fewer than SMs / 8); 0 when the query fails.
+// The path is only worth it when every (sequence, KV head) cluster fits in one wave.
+int small_max_clusters();
+
 }  // namespace gda
