@@ -300,8 +300,9 @@ def run_ours(args):
 
     max_len = (max(lengths) if len(lengths) else 0) if args.max_len < 0 else args.max_len
     # the library's dispatch rule for the one-kernel cluster path (include/gda.h, max_len)
-    small_path = (0 < max_len <= 2048 and args.splits <= 0 and args.variant == 0 and args.kv == "bf16"
-                  and Hq // Hkv <= 8 and B * Hkv <= gda.small_path_clusters())
+    small_c = (gda.small_path_cluster(B * Hkv, max_len) if (args.splits <= 0 and args.variant == 0 and
+                                                              args.kv == "bf16" and Hq // Hkv <= 8) else 0)
+    small_path = small_c > 0
 
     def call():
         gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
@@ -481,14 +482,14 @@ def run_ours(args):
             "config": {"workload": args.workload, "B": B, "lengths": "%d..%d (total %d)" % (min(lengths), max(lengths),
                                                                                           sum(lengths)),
                        "Hq": Hq, "Hkv": Hkv, "D": D, "num_splits": args.splits or "auto", "kv": args.kv,
-                       "variant": ("cluster (one kernel)" if small_path else
+                       "variant": ("cluster of %d (one kernel)" % small_c if small_path else
                                    {0: "auto(mma)", 1: "mma", 2: "simt", 3: "tma-ring+mma"}[args.variant]),
                        "max_len_hint": max_len,
                        "bytes_per_call": nbytes,
                        "l2": "inputs larger than L2 (%.0f MB of K/V rows per call), no flush" % (nbytes / 1e6),
                        "parallelism": "replicas x%d" % world, "window": args.window, "sinks": args.sinks,
                        "launch": ("CUDA graph of %d calls, replayed" % args.graph) if args.graph > 0 else "eager"},
-            "roofline": {"bound": "hbm", "kernel": ("small_decode (one cluster kernel)" if small_path else
+            "roofline": {"bound": "hbm", "kernel": ("small_decode (one kernel, %d-CTA clusters)" % small_c if small_path else
                                                     "stage1" if args.kv == "bf16" else "stage1_fp8"),
                          "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,

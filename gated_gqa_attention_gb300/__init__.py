@@ -25,7 +25,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "load", "decode", "decode_ex", "decode_noalloc", "decode_step_host", "StepHost", "step_layout", "small_path_clusters", "pack_step", "STEP_MAP_IN", "STEP_MAP_OUT", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
+    "load", "decode", "decode_ex", "decode_noalloc", "decode_step_host", "StepHost", "step_layout", "small_path_cluster", "pack_step", "STEP_MAP_IN", "STEP_MAP_OUT", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
     "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH", "KV_BF16", "KV_E4M3",
 ]
@@ -93,8 +93,8 @@ def load(path: Optional[str] = None):
         lib.gda_qk_norm_rope_kv_write.argtypes = [vp, i64, vp, vp, f32, vp, vp, i32, vp, i64, vp, vp, vp, vp,
                                                   i32, i32, i32, i32, vp]
         lib.gda_qk_norm_rope_kv_write.restype = i32
-        lib.gda_small_path_clusters.argtypes = []
-        lib.gda_small_path_clusters.restype = i32
+        lib.gda_small_path_cluster.argtypes = [i64, i32]
+        lib.gda_small_path_cluster.restype = i32
         lib.gda_step_layout.argtypes = [i32, i32, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
         lib.gda_step_layout.restype = ctypes.c_size_t
         lib.gda_decode_step_host.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, vp, vp, i32, i32, i32, i32, i64, f32,
@@ -256,10 +256,11 @@ def decode_noalloc(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out, scale:
     return out
 
 
-def small_path_clusters() -> int:
-    """``gda_small_path_clusters``: how many (sequence, KV head) pairs the one-kernel
-    small-batch path takes on the current device (0: unavailable)."""
-    return int(load().gda_small_path_clusters())
+def small_path_cluster(pairs: int, max_len: int) -> int:
+    """``gda_small_path_cluster``: the cluster size (8, 4 or 2) a bf16 decode of
+    ``pairs`` = B * Hkv (sequence, KV head) pairs with the length bound ``max_len``
+    takes through the one-kernel path on the current device, or 0 (split path)."""
+    return int(load().gda_small_path_cluster(int(pairs), int(max_len)))
 
 
 def step_layout(B: int, Hq: int, D: int, nnz: int):

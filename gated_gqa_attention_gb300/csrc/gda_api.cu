@@ -115,9 +115,11 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   if (sms <= 0) return GDA_ERR_CUDA;
 
   // small batches with a host-known length bound: one cluster kernel (no partials)
-  if (a->max_len > 0 && a->max_len <= gda::kSmallMaxLen && a->num_splits <= 0 && a->variant == GDA_VARIANT_AUTO &&
-      a->kv_dtype == GDA_KV_BF16 && !a->check_indices && a->Hq / a->Hkv <= gda::kG &&
-      (long long)a->B * a->Hkv <= (long long)gda::small_max_clusters()) {
+  const int small_c = (a->num_splits <= 0 && a->variant == GDA_VARIANT_AUTO && a->kv_dtype == GDA_KV_BF16 &&
+                       !a->check_indices && a->Hq / a->Hkv <= gda::kG)
+                          ? gda::small_cluster_for((long long)a->B * a->Hkv, a->max_len)
+                          : 0;
+  if (small_c > 0) {
     gda::SmallParams ps;
     ps.q = reinterpret_cast<const __nv_bfloat16*>(a->q);
     ps.gate = reinterpret_cast<const __nv_bfloat16*>(a->gate);
@@ -144,7 +146,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
         ++g_tused;
       }
     }
-    if (gda::launch_small(ps, stream) != cudaSuccess) return GDA_ERR_CUDA;
+    if (gda::launch_small(ps, small_c, stream) != cudaSuccess) return GDA_ERR_CUDA;
     if (s_end != nullptr && cudaEventRecord(s_end, stream) != cudaSuccess) return GDA_ERR_CUDA;
     return GDA_OK;
   }
@@ -552,7 +554,10 @@ int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {
   return ensure_workspace(need, nullptr, false, &ws);
 }
 
-int gda_small_path_clusters(void) { return gda::small_max_clusters(); }
+int gda_small_path_cluster(int64_t pairs, int max_len) {
+  if (pairs < 0) return 0;
+  return gda::small_cluster_for((long long)pairs, max_len);
+}
 
 size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]) {
   if (offsets == nullptr || B < 1 || Hq < 1 || D < 1 || nnz < 0) return 0;

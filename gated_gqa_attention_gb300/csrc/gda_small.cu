@@ -5,8 +5,10 @@
 // epilogue; cuDNN FE-OSS "Gated Attention Block (SM107)", Overview stages (4)-(5)),
 // computed in one launch for batches whose latency, not bandwidth, sets the time.
 //
-// One thread-block cluster of 8 CTAs per (sequence b, KV head): CTA r takes the r-th
-// eighth of the sequence's attended positions, in chunks of 64 whose K and V rows
+// One thread-block cluster of C = 8, 4 or 2 CTAs per (sequence b, KV head) (the host
+// takes the largest C whose clusters all run at once and leave each CTA at most 256
+// positions): CTA r takes the r-th of C
+// parts of the sequence's attended positions, in chunks of 64 whose K and V rows
 // the CTA's 256 threads bring into shared memory (cp.async, two buffers, the next
 // chunk in flight during the current one).  Per chunk, on the tensor cores
 // (mma.sync m16n8k16, BF16 in, FP32 accumulate; the G <= 8 query heads are the rows):
@@ -15,9 +17,9 @@
 //                 the running max (log2 units) and sum, P = 2^(S - max) as BF16;
 //   O += P V      warp w owns head dimensions 32w .. 32w + 31 of every head.
 // Each CTA then stores its state of query head G*kvh + g into the shared memory of
-// CTA g of the cluster (distributed shared memory); after one cluster barrier, CTA g
-// merges the 8 states (with the attention sink), divides by the sum, rounds to BF16,
-// applies the BF16 gate, and writes out and lse.  No partials go through HBM and no
+// CTA g % C of the cluster (distributed shared memory); after one cluster barrier,
+// that CTA merges the C states (with the attention sink), divides by the sum, rounds
+// to BF16, applies the BF16 gate, and writes out and lse.  No partials go through HBM and no
 // second kernel runs.
 #include "gda_device.cuh"
 #include "gda_small.h"
@@ -26,7 +28,6 @@ namespace gda {
 
 namespace {
 
-constexpr int kSC = kSmallCluster;  // CTAs per cluster
 constexpr int kSW = 8;              // warps per CTA
 constexpr int kChunk = 64;          // positions per shared-memory chunk (8 per warp in S)
 
@@ -36,9 +37,11 @@ struct SmallSmem {
   uint32_t p[kG][kChunk / 2];            // P of the chunk: BF16 pairs [head][position pair]
   float wmax[kSW][kG];                   // per warp and head: max of the warp's 8 scores
   float wsum[kSW][kG];                   // per warp and head: sum of its BF16 probabilities
-  float o[kSC][kD];  // incoming: unnormalised O of CTA x for the head this CTA finalises
-  float m[kSC];      // its running max (log2 units)
-  float l[kSC];      // its sum
+  // incoming states, slot (g / C) * C + x: CTA x's unnormalised O of query head g of the
+  // group (finalised by CTA g % C), its running max (log2 units) and sum
+  float o[kG][kD];
+  float m[kG];
+  float l[kG];
 };
 constexpr size_t kSmallSmem = sizeof(SmallSmem);
 
@@ -79,7 +82,10 @@ __device__ __forceinline__ float quad_sum(float x) {
 
 }  // namespace
 
-__global__ void __cluster_dims__(kSC, 1, 1) __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p) {
+template <int C>
+__global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p) {
+  static_assert(C == 2 || C == 4 || C == 8, "cluster sizes");
+  constexpr int kFin = kG / C;  // query heads each CTA finalises
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SmallSmem& sm = *reinterpret_cast<SmallSmem*>(smem_raw);
   const int r = blockIdx.x;  // rank in the cluster (the grid's x extent is the cluster)
@@ -102,11 +108,17 @@ __global__ void __cluster_dims__(kSC, 1, 1) __launch_bounds__(kSW * 32, 1) small
       qa[ks][1] = (h < G) ? __ldg(qrow + 8 * ks + 4 + qd) : 0u;
     }
   }
-  const int hf = kvh * G + r;  // the query head this CTA finalises (r < G)
-  uint16_t gbits = 0;
-  if (r < G && p.fuse_gate) gbits = __bfloat16_as_ushort(p.gate[((size_t)b * p.Hq + hf) * kD + tid]);
+  // the query heads this CTA finalises: r + C k of the group (when below G)
+  uint16_t gbits[kFin];
+#pragma unroll
+  for (int k = 0; k < kFin; ++k) {
+    const int hl = r + C * k;
+    gbits[k] = (hl < G && p.fuse_gate)
+                   ? __bfloat16_as_ushort(p.gate[((size_t)b * p.Hq + kvh * G + hl) * kD + tid])
+                   : (uint16_t)0;
+  }
 
-  const int c = (L + kSC - 1) / kSC;
+  const int c = (L + C - 1) / C;
   const int lo = min(L, r * c), hi = min(L, lo + c);
   const int nch = (hi - lo + kChunk - 1) / kChunk;
   const size_t row_stride = (size_t)p.Hkv * kD;  // elements between slots
@@ -209,93 +221,140 @@ __global__ void __cluster_dims__(kSC, 1, 1) __launch_bounds__(kSW * 32, 1) small
     if (cidx + 2 < nch) load_chunk(cidx + 2);
   }
 
-  // this CTA's state of head h into slot r of the CTA that finalises it
+  // this CTA's state of head h into slot (h / C) * C + r of CTA h % C, which finalises it
   if (h < G) {
+    const int slot = (h / C) * C + r;
+    const uint32_t dst = (uint32_t)(h % C);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const int dim = 32 * warp + 8 * nt + 2 * qd;
-      st_cluster_v2(cluster_addr(&sm.o[r][dim], (uint32_t)h), oacc[nt][0], oacc[nt][1]);
+      st_cluster_v2(cluster_addr(&sm.o[slot][dim], dst), oacc[nt][0], oacc[nt][1]);
     }
     if (warp == 0 && qd == 0) {
-      st_cluster_f32(cluster_addr(&sm.m[r], (uint32_t)h), m_run);
-      st_cluster_f32(cluster_addr(&sm.l[r], (uint32_t)h), l_run);
+      st_cluster_f32(cluster_addr(&sm.m[slot], dst), m_run);
+      st_cluster_f32(cluster_addr(&sm.l[slot], dst), l_run);
     }
   }
-  const uint16_t sig = (r < G && p.fuse_gate) ? sigmoid_bf16(gbits) : (uint16_t)0;
+  uint16_t sig[kFin];
+#pragma unroll
+  for (int k = 0; k < kFin; ++k) sig[k] = (r + C * k < G && p.fuse_gate) ? sigmoid_bf16(gbits[k]) : (uint16_t)0;
 
   // every state has arrived where it is merged after this; afterwards each CTA reads
   // only its own shared memory, so no second barrier is needed before leaving
   cluster_sync_all();
 
-  if (r < G) {
-    // query head hf: merge the kSC states (and the sink), normalise, round, gate
+#pragma unroll
+  for (int k = 0; k < kFin; ++k) {
+    const int hl = r + C * k;
+    if (hl >= G) break;
+    // query head hf: merge the C states (and the sink), normalise, round, gate
+    const int hf = kvh * G + hl;
     const float sink2 = (p.sinks != nullptr) ? __ldg(p.sinks + hf) * 1.44269504088896340736f : -INFINITY;
     float M = sink2;
 #pragma unroll
-    for (int x = 0; x < kSC; ++x) M = fmaxf(M, sm.m[x]);
+    for (int x = 0; x < C; ++x) M = fmaxf(M, sm.m[k * C + x]);
     float acc = 0.0f, W = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int x = 0; x < kSC; ++x) {
-        const float f = safe_exp2_diff(sm.m[x], M);
-        acc = fmaf(sm.o[x][tid], f, acc);
-        W = fmaf(sm.l[x], f, W);
+      for (int x = 0; x < C; ++x) {
+        const float f = safe_exp2_diff(sm.m[k * C + x], M);
+        acc = fmaf(sm.o[k * C + x][tid], f, acc);
+        W = fmaf(sm.l[k * C + x], f, W);
       }
       if (sink2 != -INFINITY) W += exp2f(sink2 - M);
       acc /= W;
     }
     const uint16_t ob = float_to_bf16_bits(acc);
     const size_t row = ((size_t)b * p.Hq + hf) * kD;
-    reinterpret_cast<uint16_t*>(p.out)[row + tid] = p.fuse_gate ? gate_product_bf16(ob, sig) : ob;
+    reinterpret_cast<uint16_t*>(p.out)[row + tid] = p.fuse_gate ? gate_product_bf16(ob, sig[k]) : ob;
     if (p.lse_out != nullptr && tid == 0)
       p.lse_out[(size_t)b * p.Hq + hf] = (M == -INFINITY) ? -INFINITY : (M + log2f(W)) * 0.69314718055994530942f;
   }
 }
 
 namespace {
-bool g_small_attr[64] = {};
-int g_small_clusters[64] = {};
 
-cudaError_t small_attr(int dev) {
-  if (!g_small_attr[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(small_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
+template <int C>
+cudaError_t small_attr_c() {
+  return cudaFuncSetAttribute(small_decode_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
+}
+
+// cluster index 0, 1, 2 for C = 8, 4, 2
+int cidx_of(int C) { return C == 8 ? 0 : (C == 4 ? 1 : 2); }
+
+bool g_small_attr[64][3] = {};
+int g_small_clusters[64][3] = {};
+
+cudaError_t small_attr(int dev, int C) {
+  bool& done = g_small_attr[dev][cidx_of(C)];
+  if (!done) {
+    const cudaError_t e = (C == 8) ? small_attr_c<8>() : (C == 4) ? small_attr_c<4>() : small_attr_c<2>();
     if (e != cudaSuccess) return e;
-    g_small_attr[dev] = true;
+    done = true;
   }
   return cudaSuccess;
 }
+
+void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int C, dim3 grid, cudaStream_t stream) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = grid;
+  cfg->blockDim = dim3(kSW * 32, 1, 1);
+  cfg->dynamicSmemBytes = kSmallSmem;
+  cfg->stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
 }  // namespace
 
-int small_max_clusters() {
+int small_max_clusters(int C) {
+  if (C != 8 && C != 4 && C != 2) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (g_small_clusters[dev] == 0) {
-    if (small_attr(dev) != cudaSuccess) return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)kSC, 1, 1);
-    cfg.blockDim = dim3(kSW * 32, 1, 1);
-    cfg.dynamicSmemBytes = kSmallSmem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, small_decode_kernel, &cfg) != cudaSuccess || n <= 0) {
+  int& n = g_small_clusters[dev][cidx_of(C)];
+  if (n == 0) {
+    if (small_attr(dev, C) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    cluster_config(&cfg, attr, C, dim3((unsigned)C, 1, 1), nullptr);
+    int got = 0;
+    const cudaError_t e = (C == 8) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<8>, &cfg)
+                          : (C == 4) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<4>, &cfg)
+                                     : cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<2>, &cfg);
+    if (e != cudaSuccess || got <= 0) {
       (void)cudaGetLastError();
       return 0;
     }
-    g_small_clusters[dev] = n;
+    n = got;
   }
-  return g_small_clusters[dev];
+  return n;
 }
 
-cudaError_t launch_small(const SmallParams& p, cudaStream_t stream) {
+int small_cluster_for(long long pairs, int max_len) {
+  if (max_len <= 0 || max_len > kSmallMaxLen) return 0;
+  for (int C = 8; C >= 2; C /= 2)
+    if (max_len <= 256 * C && pairs <= (long long)small_max_clusters(C)) return C;
+  return 0;
+}
+
+cudaError_t launch_small(const SmallParams& p, int C, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  e = small_attr(dev);
+  e = small_attr(dev, C);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)kSC, (unsigned)p.Hkv, (unsigned)p.B);
-  small_decode_kernel<<<grid, kSW * 32, kSmallSmem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  cluster_config(&cfg, attr, C, dim3((unsigned)C, (unsigned)p.Hkv, (unsigned)p.B), stream);
+  if (C == 8) return cudaLaunchKernelEx(&cfg, small_decode_kernel<8>, p);
+  if (C == 4) return cudaLaunchKernelEx(&cfg, small_decode_kernel<4>, p);
+  if (C == 2) return cudaLaunchKernelEx(&cfg, small_decode_kernel<2>, p);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gda

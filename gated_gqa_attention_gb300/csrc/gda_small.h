@@ -7,7 +7,6 @@
 
 namespace gda {
 
-constexpr int kSmallCluster = 8;    // CTAs per (sequence, KV head): one cluster
 constexpr int kSmallMaxLen = 2048;  // longest sequence (host bound) the path takes
 
 struct SmallParams {
@@ -26,12 +25,18 @@ struct SmallParams {
   int fuse_gate;
 };
 
-// grid (kSmallCluster, Hkv, B) in clusters of kSmallCluster CTAs
-cudaError_t launch_small(const SmallParams& p, cudaStream_t stream);
+// grid (C, Hkv, B) in clusters of C = 8, 4 or 2 CTAs, one per (sequence, KV head)
+cudaError_t launch_small(const SmallParams& p, int C, cudaStream_t stream);
 
-// How many of the kernel's clusters the current device runs at once (one CTA per SM
-// and 8 SMs of one GPC per cluster: fewer than SMs / 8); 0 when the query fails.
-// The path is only worth it when every (sequence, KV head) cluster fits in one wave.
-int small_max_clusters();
+// How many of the kernel's C-CTA clusters the current device runs at once (one CTA
+// per SM and the C SMs of a cluster in one GPC); 0 when the query fails.
+int small_max_clusters(int C);
+
+// The cluster size for `pairs` (sequence, KV head) pairs whose lengths are at most
+// max_len, or 0 for the split path: the largest C whose clusters all run at once (one
+// wave) and give each CTA at most 256 positions (max_len <= 256 C).  Measured on
+// GB300 against the split path: 0.55-0.8x its time inside these bounds, slower
+// outside them.
+int small_cluster_for(long long pairs, int max_len);
 
 }  // namespace gda

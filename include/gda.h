@@ -123,10 +123,11 @@ typedef enum gda_status {
  *   max_len     0, or an upper bound on every sequence's KV length that the caller knows
  *               on the host (a scheduler's batch maximum).  With a bound of at most
  *               2048, automatic splits (num_splits <= 0), GDA_VARIANT_AUTO, bf16 pools,
- *               no check_indices, Hq / Hkv <= 8 and at most as many (sequence, KV head)
- *               pairs as the device runs 8-CTA clusters of this kernel at once, the call
- *               runs as ONE kernel: a thread-block cluster of 8 CTAs per (sequence, KV
- *               head) that merges its partial softmax states in distributed shared
+ *               no check_indices, Hq / Hkv <= 8, and few enough (sequence, KV head) pairs
+ *               (gda_small_path_cluster), the call runs as ONE kernel: a thread-block
+ *               cluster of 8, 4 or 2 CTAs per (sequence, KV head) (the most that fit in
+ *               one wave, at most 256 positions per CTA) that merges its partial
+ *               softmax states in distributed shared
  *               memory and applies the gate, with no workspace traffic.  The result
  *               is the same function within the tolerance of the split path.  A bound
  *               below an actual length still gives the right result, only slower.
@@ -259,10 +260,11 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
  * initialise before capture). */
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
 
-/* How many (sequence, KV head) pairs the one-kernel small-batch path takes on the
- * current device (gda_args.max_len): the number of its 8-CTA clusters the device runs
- * at once.  Returns 0 when the query fails; a CUDA call, not a host-only check. */
-int gda_small_path_clusters(void);
+/* The cluster size (8, 4 or 2 CTAs per (sequence, KV head)) that a bf16 decode with
+ * `pairs` = B * Hkv (sequence, KV head) pairs and the length bound max_len takes on the
+ * current device through the one-kernel path, or 0 when it takes the split path
+ * (gda_args.max_len).  A CUDA occupancy query on first use, not a host-only check. */
+int gda_small_path_cluster(int64_t pairs, int max_len);
 
 /* Byte layout of one decode step's inputs packed into a single block, as
  * gda_decode_step_host takes them: q [B, Hq, D] bf16 at offsets[0] (= 0), gate

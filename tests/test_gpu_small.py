@@ -48,8 +48,10 @@ def reference(inp, **kw):
 
 
 def test_one_wave_holds_the_test_batches(gda):
-    # the path takes at most as many pairs as the device runs clusters at once
-    assert gda.small_path_clusters() >= 2 * len(LENS)
+    # the test batches take the 8-CTA clusters (one wave, <= 256 positions per CTA)
+    assert gda.small_path_cluster(2 * len(LENS), 2048) == 8
+    assert gda.small_path_cluster(2 * len(LENS), 4096) == 0       # beyond the length bound
+    assert gda.small_path_cluster(10_000, 128) == 0               # beyond one wave
 
 
 @pytest.fixture(scope="module")
@@ -148,3 +150,24 @@ def test_step_host_takes_the_cluster_path(gda):
     want = run(gda, inp, nnz)
     assert np.array_equal(bits(host_out), want)
     check_close(bits(host_out), reference(inp).out)
+
+
+@pytest.mark.parametrize("B,lmax,C", [(16, 1024, 4), (32, 512, 2)])
+def test_smaller_clusters(gda, B, lmax, C):
+    # more pairs than 8-CTA clusters fit at once: 4- and 2-CTA clusters (each CTA at
+    # most 256 positions), same parity and no partials written
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.integers(0, lmax + 1, B)]
+    lens[0], lens[1] = lmax, 0
+    inp = workloads.make(lens, seed=600 + B, layout="perm", pool_slots=sum(lens) + 100)
+    Hkv = inp["k_pool"].shape[1]
+    assert gda.small_path_cluster(B * Hkv, lmax) == C
+    _, Hq, D = inp["q"].shape
+    ws = torch.full((gda.workspace_bytes(B, Hq, Hkv, D, 0),), 0xA5, dtype=torch.uint8, device="cuda")
+    gda.workspace_init(ws)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    got = run(gda, inp, lmax, workspace=ws, lse=lse)
+    assert bool((ws[256:] == 0xA5).all()), "partials were written: the split path ran"
+    ref = reference(inp)
+    check_close(got, ref.out)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
