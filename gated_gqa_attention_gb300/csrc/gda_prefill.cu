@@ -274,8 +274,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
   float* xbuf = reinterpret_cast<float*>(sm + kOffX);  // [parity][half][row]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqb = (p.Sq + kPM - 1) / kPM;
-  const int qb = nqb - 1 - (int)blockIdx.x;  // the longest causal blocks first
-  const int h = blockIdx.y, b = blockIdx.z;
+  // CTAs start in linear order (x fastest): x enumerates (query block, head) with the
+  // head fastest, so every head's longest causal blocks come first (longest-first
+  // scheduling keeps the last wave short)
+  const int qb = nqb - 1 - (int)blockIdx.x / p.Hq;
+  const int h = (int)blockIdx.x % p.Hq, b = blockIdx.y;
   const int kvh = h / (p.Hq / p.Hkv);
   const int L = p.kv_lens ? __ldg(p.kv_lens + b) : p.Skv;
   const int i0 = qb * kPM;
@@ -787,7 +790,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k,
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const dim3 grid((unsigned)((p.Sq + kPM - 1) / kPM), (unsigned)p.Hq, (unsigned)p.B);
+  const dim3 grid((unsigned)(((p.Sq + kPM - 1) / kPM) * p.Hq), (unsigned)p.B, 1u);
   prefill_kernel<<<grid, kPThreads, kSmemBytes, stream>>>(tq, tk, tv, tg, to, p);
   return cudaGetLastError();
 }
