@@ -5,7 +5,7 @@
 // epilogue; cuDNN FE-OSS "Gated Attention Block (SM107)", Overview stages (4)-(5)),
 // computed in one launch for batches whose latency, not bandwidth, sets the time.
 //
-// One thread-block cluster of C = 8, 4 or 2 CTAs per (sequence b, KV head) (the host
+// One thread-block cluster of C = 8, 4, 2 or 1 CTAs per (sequence b, KV head) (the host
 // takes the largest C whose clusters all run at once and leave each CTA at most 256
 // positions): CTA r takes the r-th of C
 // parts of the sequence's attended positions, in chunks of 64 whose K and V rows
@@ -84,7 +84,7 @@ __device__ __forceinline__ float quad_sum(float x) {
 
 template <int C>
 __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p) {
-  static_assert(C == 2 || C == 4 || C == 8, "cluster sizes");
+  static_assert(C == 1 || C == 2 || C == 4 || C == 8, "cluster sizes");
   constexpr int kFin = kG / C;  // query heads each CTA finalises
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SmallSmem& sm = *reinterpret_cast<SmallSmem*>(smem_raw);
@@ -279,16 +279,19 @@ cudaError_t small_attr_c() {
   return cudaFuncSetAttribute(small_decode_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
 }
 
-// cluster index 0, 1, 2 for C = 8, 4, 2
-int cidx_of(int C) { return C == 8 ? 0 : (C == 4 ? 1 : 2); }
+// cluster index 0, 1, 2, 3 for C = 8, 4, 2, 1
+int cidx_of(int C) { return C == 8 ? 0 : (C == 4 ? 1 : (C == 2 ? 2 : 3)); }
 
-bool g_small_attr[64][3] = {};
-int g_small_clusters[64][3] = {};
+bool g_small_attr[64][4] = {};
+int g_small_clusters[64][4] = {};
 
 cudaError_t small_attr(int dev, int C) {
   bool& done = g_small_attr[dev][cidx_of(C)];
   if (!done) {
-    const cudaError_t e = (C == 8) ? small_attr_c<8>() : (C == 4) ? small_attr_c<4>() : small_attr_c<2>();
+    const cudaError_t e = (C == 8)   ? small_attr_c<8>()
+                          : (C == 4) ? small_attr_c<4>()
+                          : (C == 2) ? small_attr_c<2>()
+                                     : small_attr_c<1>();
     if (e != cudaSuccess) return e;
     done = true;
   }
@@ -312,7 +315,7 @@ void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int C, d
 }  // namespace
 
 int small_max_clusters(int C) {
-  if (C != 8 && C != 4 && C != 2) return 0;
+  if (C != 8 && C != 4 && C != 2 && C != 1) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   int& n = g_small_clusters[dev][cidx_of(C)];
@@ -322,9 +325,10 @@ int small_max_clusters(int C) {
     cudaLaunchAttribute attr[1];
     cluster_config(&cfg, attr, C, dim3((unsigned)C, 1, 1), nullptr);
     int got = 0;
-    const cudaError_t e = (C == 8) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<8>, &cfg)
+    const cudaError_t e = (C == 8)   ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<8>, &cfg)
                           : (C == 4) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<4>, &cfg)
-                                     : cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<2>, &cfg);
+                          : (C == 2) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<2>, &cfg)
+                                     : cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<1>, &cfg);
     if (e != cudaSuccess || got <= 0) {
       (void)cudaGetLastError();
       return 0;
@@ -336,7 +340,7 @@ int small_max_clusters(int C) {
 
 int small_cluster_for(long long pairs, int max_len) {
   if (max_len <= 0 || max_len > kSmallMaxLen) return 0;
-  for (int C = 8; C >= 2; C /= 2)
+  for (int C = 8; C >= 1; C /= 2)
     if (max_len <= 256 * C && pairs <= (long long)small_max_clusters(C)) return C;
   return 0;
 }
@@ -354,6 +358,7 @@ cudaError_t launch_small(const SmallParams& p, int C, cudaStream_t stream) {
   if (C == 8) return cudaLaunchKernelEx(&cfg, small_decode_kernel<8>, p);
   if (C == 4) return cudaLaunchKernelEx(&cfg, small_decode_kernel<4>, p);
   if (C == 2) return cudaLaunchKernelEx(&cfg, small_decode_kernel<2>, p);
+  if (C == 1) return cudaLaunchKernelEx(&cfg, small_decode_kernel<1>, p);
   return cudaErrorInvalidValue;
 }
 

@@ -25,7 +25,7 @@ struct SmallParams {
   int fuse_gate;
 };
 
-// grid (C, Hkv, B) in clusters of C = 8, 4 or 2 CTAs, one per (sequence, KV head)
+// grid (C, Hkv, B) in clusters of C = 8, 4, 2 or 1 CTAs, one per (sequence, KV head)
 cudaError_t launch_small(const SmallParams& p, int C, cudaStream_t stream);
 
 // How many of the kernel's C-CTA clusters the current device runs at once (one CTA

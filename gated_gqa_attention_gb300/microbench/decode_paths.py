@@ -1,5 +1,5 @@
 """Decode-path sweep (needs a GPU): for B in {1, 4, 8, 12, 16, 24, 32, 48, 64} and
-equal lengths L in {128, 512, 1024, 2048}, the µs per call of gda_decode_ex with the
+equal lengths L in {128, 256, 512, 1024, 2048}, the µs per call of gda_decode_ex with the
 length bound (the library picks the one-kernel cluster path when it applies) and
 without it (the split path), each a CUDA graph of 4 calls replayed; the cluster size
 gda_small_path_cluster chose is printed beside them."""
@@ -37,7 +37,7 @@ def main():
     gda.load()
     print("%3s %5s %9s %12s %10s %6s" % ("B", "L", "cluster C", "one-kernel", "split", "ratio"))
     for B in (1, 4, 8, 12, 16, 24, 32, 48, 64):
-        for L in (128, 512, 1024, 2048):
+        for L in (128, 256, 512, 1024, 2048):
             inp = workloads.make([L] * B, seed=7, layout="perm", pool_slots=max(4096, B * L + 100))
             d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
             out = torch.empty_like(d["q"])

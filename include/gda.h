@@ -125,7 +125,7 @@ typedef enum gda_status {
  *               2048, automatic splits (num_splits <= 0), GDA_VARIANT_AUTO, bf16 pools,
  *               no check_indices, Hq / Hkv <= 8, and few enough (sequence, KV head) pairs
  *               (gda_small_path_cluster), the call runs as ONE kernel: a thread-block
- *               cluster of 8, 4 or 2 CTAs per (sequence, KV head) (the most that fit in
+ *               cluster of 8, 4, 2 or 1 CTAs per (sequence, KV head) (the most that fit in
  *               one wave, at most 256 positions per CTA) that merges its partial
  *               softmax states in distributed shared
  *               memory and applies the gate, with no workspace traffic.  The result
@@ -260,7 +260,7 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
  * initialise before capture). */
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
 
-/* The cluster size (8, 4 or 2 CTAs per (sequence, KV head)) that a bf16 decode with
+/* The cluster size (8, 4, 2 or 1 CTAs per (sequence, KV head)) that a bf16 decode with
  * `pairs` = B * Hkv (sequence, KV head) pairs and the length bound max_len takes on the
  * current device through the one-kernel path, or 0 when it takes the split path
  * (gda_args.max_len).  A CUDA occupancy query on first use, not a host-only check. */

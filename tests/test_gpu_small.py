@@ -152,9 +152,9 @@ def test_step_host_takes_the_cluster_path(gda):
     check_close(bits(host_out), reference(inp).out)
 
 
-@pytest.mark.parametrize("B,lmax,C", [(16, 1024, 4), (32, 512, 2)])
+@pytest.mark.parametrize("B,lmax,C", [(16, 1024, 4), (32, 512, 2), (48, 256, 1)])
 def test_smaller_clusters(gda, B, lmax, C):
-    # more pairs than 8-CTA clusters fit at once: 4- and 2-CTA clusters (each CTA at
+    # more pairs than 8-CTA clusters fit at once: 4-, 2- and 1-CTA clusters (each CTA at
     # most 256 positions), same parity and no partials written
     rng = np.random.default_rng(B)
     lens = [int(x) for x in rng.integers(0, lmax + 1, B)]
