@@ -301,7 +301,7 @@ def run_ours(args):
     max_len = (max(lengths) if len(lengths) else 0) if args.max_len < 0 else args.max_len
     # the library's dispatch rule for the one-kernel cluster path (include/gda.h, max_len)
     small_c = (gda.small_path_cluster(B * Hkv, max_len) if (args.splits <= 0 and args.variant == 0 and
-                                                              args.kv == "bf16" and Hq // Hkv <= 8) else 0)
+                                                              Hq // Hkv <= 8) else 0)
     small_path = small_c > 0
 
     def call():

@@ -115,16 +115,16 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   if (sms <= 0) return GDA_ERR_CUDA;
 
   // small batches with a host-known length bound: one cluster kernel (no partials)
-  const int small_c = (a->num_splits <= 0 && a->variant == GDA_VARIANT_AUTO && a->kv_dtype == GDA_KV_BF16 &&
-                       !a->check_indices && a->Hq / a->Hkv <= gda::kG)
+  const int small_c = (a->num_splits <= 0 && a->variant == GDA_VARIANT_AUTO && !a->check_indices &&
+                       a->Hq / a->Hkv <= gda::kG)
                           ? gda::small_cluster_for((long long)a->B * a->Hkv, a->max_len)
                           : 0;
   if (small_c > 0) {
     gda::SmallParams ps;
     ps.q = reinterpret_cast<const __nv_bfloat16*>(a->q);
     ps.gate = reinterpret_cast<const __nv_bfloat16*>(a->gate);
-    ps.k_pool = reinterpret_cast<const __nv_bfloat16*>(a->k_pool);
-    ps.v_pool = reinterpret_cast<const __nv_bfloat16*>(a->v_pool);
+    ps.k_pool = a->k_pool;
+    ps.v_pool = a->v_pool;
     ps.indptr = a->kv_indptr;
     ps.indices = a->kv_indices;
     ps.out = reinterpret_cast<__nv_bfloat16*>(a->out);
@@ -134,7 +134,12 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
     ps.Hq = a->Hq;
     ps.Hkv = a->Hkv;
     ps.G = a->Hq / a->Hkv;
-    ps.scale_log2 = a->scale * 1.44269504088896340736f;
+    const bool fp8 = a->kv_dtype == GDA_KV_E4M3;
+    // e4m3 pools: k_descale joins the score scale (one rounding, from double)
+    ps.scale_log2 = fp8 ? (float)((double)a->scale * (double)a->k_descale * 1.4426950408889634074)
+                        : a->scale * 1.44269504088896340736f;
+    ps.kv_fp8 = fp8 ? 1 : 0;
+    ps.v_descale = fp8 ? a->v_descale : 1.0f;
     ps.window = a->window;
     ps.fuse_gate = a->fuse_gate ? 1 : 0;
     cudaEvent_t s_end = nullptr;

@@ -71,6 +71,29 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// FP16 counterparts of the BF16 tensor-core helpers (the e4m3 cache's operands)
+__device__ __forceinline__ void mma_f16_16816(float* c, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float f16_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
+__device__ __forceinline__ float f16_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+// four e4m3 codes (bytes 0..3 of w) -> two f16 pairs (bytes 0, 1 and bytes 2, 3); exact
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ float quad_max(float x) {
   x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
   return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
@@ -82,7 +105,10 @@ __device__ __forceinline__ float quad_sum(float x) {
 
 }  // namespace
 
-template <int C>
+// F8: the pools hold e4m3 codes; K and V are widened to FP16 while being staged, Q
+// goes to FP16 with one power-of-two factor per group, the MMAs run in FP16, and
+// v_descale scales the merged O (k_descale is in scale_log2)
+template <int C, bool F8>
 __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p) {
   static_assert(C == 1 || C == 2 || C == 4 || C == 8, "cluster sizes");
   constexpr int kFin = kG / C;  // query heads each CTA finalises
@@ -108,6 +134,29 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
       qa[ks][1] = (h < G) ? __ldg(qrow + 8 * ks + 4 + qd) : 0u;
     }
   }
+  float sl2 = p.scale_log2;
+  if (F8) {
+    // every warp holds the whole group's Q: its largest magnitude sets 2^e, which puts
+    // it in [2^14, 2^15) (every BF16 value down to 2^-14 below it stays exact in FP16)
+    float mx = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(qa[ks][i] << 16)), fabsf(__uint_as_float(qa[ks][i] & 0xFFFF0000u))));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const uint32_t qm = __float_as_uint(mx);
+    int e = (qm == 0u) ? 0 : 141 - (int)((qm >> 23) & 0xFFu);
+    e = max(-126, min(127, e));
+    const float qs = __uint_as_float((uint32_t)(e + 127) << 23);
+    sl2 = ldexpf(p.scale_log2, -e);
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        qa[ks][i] = f16x2_rn(__uint_as_float(qa[ks][i] << 16) * qs, __uint_as_float(qa[ks][i] & 0xFFFF0000u) * qs);
+  }
   // the query heads this CTA finalises: r + C k of the group (when below G)
   uint16_t gbits[kFin];
 #pragma unroll
@@ -123,15 +172,54 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
   const int nch = (hi - lo + kChunk - 1) / kChunk;
   const size_t row_stride = (size_t)p.Hkv * kD;  // elements between slots
 
-  // chunk c into buffer c & 1: thread t copies pieces t % 4 + 4 k (k < 8) of the K and V
-  // rows of position t / 4; positions past the range are zero-filled
+  // e4m3 rows (256 B): thread t loads the 64-byte piece t % 4 of the K and V rows of
+  // position t / 4 into registers; store_chunk widens them to FP16 into buffer c & 1
+  // (the same row layout as BF16 rows).  Positions past the range read as zeros.
+  uint4 rk[4], rv[4];
+  auto fetch_raw = [&](int cidx) {
+    const int pos = lo + cidx * kChunk + (tid >> 2);
+    const bool ok = cidx < nch && pos < hi;
+    const int slot = ok ? __ldg(p.indices + base + pos) : 0;
+    const size_t off = ((size_t)slot * row_stride + (size_t)kvh * kD) + (size_t)qd * 64;  // bytes (1 per code)
+    const uint4* ks = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(p.k_pool) + off);
+    const uint4* vs = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(p.v_pool) + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      rk[i] = ok ? __ldg(ks + i) : make_uint4(0u, 0u, 0u, 0u);
+      rv[i] = ok ? __ldg(vs + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  auto store_chunk = [&](int cidx) {
+    const int j = tid >> 2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t wk[4] = {rk[i].x, rk[i].y, rk[i].z, rk[i].w}, wv[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
+      uint32_t fk[8], fv[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        e4m3x4_to_f16(wk[u], fk[2 * u], fk[2 * u + 1]);
+        e4m3x4_to_f16(wv[u], fv[2 * u], fv[2 * u + 1]);
+      }
+      // codes 64 qd + 16 i .. + 15 -> FP16 elements at byte 2 (64 qd + 16 i)
+      uint4* dk = reinterpret_cast<uint4*>(&sm.k[cidx & 1][j][2 * (64 * qd + 16 * i)]);
+      uint4* dv = reinterpret_cast<uint4*>(&sm.v[cidx & 1][j][2 * (64 * qd + 16 * i)]);
+      dk[0] = make_uint4(fk[0], fk[1], fk[2], fk[3]);
+      dk[1] = make_uint4(fk[4], fk[5], fk[6], fk[7]);
+      dv[0] = make_uint4(fv[0], fv[1], fv[2], fv[3]);
+      dv[1] = make_uint4(fv[4], fv[5], fv[6], fv[7]);
+    }
+  };
+  // BF16 rows: chunk c into buffer c & 1 by cp.async: thread t copies pieces t % 4 + 4 k
+  // (k < 8) of the K and V rows of position t / 4; positions past the range are zero-filled
   auto load_chunk = [&](int cidx) {
     const int j = tid >> 2, pos = lo + cidx * kChunk + j;
     const bool ok = pos < hi;
     const int slot = ok ? __ldg(p.indices + base + pos) : 0;
     const size_t off = (size_t)slot * row_stride + (size_t)kvh * kD;
-    const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_pool + (ok ? off : 0));
-    const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.v_pool + (ok ? off : 0));
+    const unsigned char* ks =
+        reinterpret_cast<const unsigned char*>(static_cast<const __nv_bfloat16*>(p.k_pool) + (ok ? off : 0));
+    const unsigned char* vs =
+        reinterpret_cast<const unsigned char*>(static_cast<const __nv_bfloat16*>(p.v_pool) + (ok ? off : 0));
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int piece = qd + 4 * k;
@@ -140,8 +228,14 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
     }
     cp_async_commit();
   };
-  if (nch > 0) load_chunk(0);
-  if (nch > 1) load_chunk(1);
+  if (F8) {
+    fetch_raw(0);
+    if (nch > 0) store_chunk(0);
+    fetch_raw(1);  // in flight during chunk 0
+  } else {
+    if (nch > 0) load_chunk(0);
+    if (nch > 1) load_chunk(1);
+  }
 
   float m_run = -INFINITY, l_run = 0.0f;  // head h (identical in every thread of row h)
   float oacc[4][4];                        // O of head h, dims 32 warp + 8 nt + 2 qd .. (c0, c1)
@@ -151,7 +245,9 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
     for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.0f;
 
   for (int cidx = 0; cidx < nch; ++cidx) {
-    if (cidx + 1 < nch) cp_async_wait<1>(); else cp_async_wait<0>();
+    if (!F8) {
+      if (cidx + 1 < nch) cp_async_wait<1>(); else cp_async_wait<0>();
+    }
     __syncthreads();
     const int buf = cidx & 1;
     const int n = min(kChunk, hi - lo - cidx * kChunk);  // positions in this chunk
@@ -165,14 +261,19 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
       for (int kp = 0; kp < 8; ++kp) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kaddr + kp * 64, b0, b1, b2, b3);
-        mma_bf16_16816(sacc, qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
-        mma_bf16_16816(sacc, qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+        if (F8) {
+          mma_f16_16816(sacc, qa[2 * kp][0], qa[2 * kp][1], b0, b1);
+          mma_f16_16816(sacc, qa[2 * kp + 1][0], qa[2 * kp + 1][1], b2, b3);
+        } else {
+          mma_bf16_16816(sacc, qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
+          mma_bf16_16816(sacc, qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+        }
       }
     }
     // scores (log2 units) of positions 8 warp + 2 qd, + 1; past the chunk's end -inf
     const int j0 = 8 * warp + 2 * qd;
-    const float s0 = (j0 < n) ? sacc[0] * p.scale_log2 : -INFINITY;
-    const float s1 = (j0 + 1 < n) ? sacc[1] * p.scale_log2 : -INFINITY;
+    const float s0 = (j0 < n) ? sacc[0] * sl2 : -INFINITY;
+    const float s1 = (j0 + 1 < n) ? sacc[1] * sl2 : -INFINITY;
     const float wm = quad_max(fmaxf(s0, s1));
     if (qd == 0) sm.wmax[warp][h] = wm;
     __syncthreads();
@@ -186,9 +287,11 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
       p0 = safe_exp2_diff(s0, m_new);
       p1 = safe_exp2_diff(s1, m_new);
     }
-    const uint32_t pp = pack_bf16x2(p0, p1);
+    // P rounded to the MMA's type; the sum adds the rounded values the MMA uses
+    const uint32_t pp = F8 ? f16x2_rn(p0, p1) : pack_bf16x2(p0, p1);
     sm.p[h][4 * warp + qd] = pp;
-    const float ws = quad_sum(__uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u));
+    const float ws = quad_sum(F8 ? (f16_lo(pp) + f16_hi(pp))
+                                 : (__uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u)));
     if (qd == 0) sm.wsum[warp][h] = ws;
     __syncthreads();
     float csum = 0.0f;
@@ -213,12 +316,24 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
         const int dim = 32 * warp + 16 * np + 8 * (lane >> 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_trans(smem_u32(&sm.v[buf][pos][dim * 2]), b0, b1, b2, b3);
-        mma_bf16_16816(oacc[2 * np], a0, 0u, a2, 0u, b0, b1);
-        mma_bf16_16816(oacc[2 * np + 1], a0, 0u, a2, 0u, b2, b3);
+        if (F8) {
+          mma_f16_16816(oacc[2 * np], a0, a2, b0, b1);
+          mma_f16_16816(oacc[2 * np + 1], a0, a2, b2, b3);
+        } else {
+          mma_bf16_16816(oacc[2 * np], a0, 0u, a2, 0u, b0, b1);
+          mma_bf16_16816(oacc[2 * np + 1], a0, 0u, a2, 0u, b2, b3);
+        }
       }
     }
     __syncthreads();  // buffer buf and the P tile are free
-    if (cidx + 2 < nch) load_chunk(cidx + 2);
+    if (F8) {
+      if (cidx + 1 < nch) {
+        store_chunk(cidx + 1);  // its codes arrived during this chunk
+        fetch_raw(cidx + 2);
+      }
+    } else if (cidx + 2 < nch) {
+      load_chunk(cidx + 2);
+    }
   }
 
   // this CTA's state of head h into slot (h / C) * C + r of CTA h % C, which finalises it
@@ -262,7 +377,7 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
         W = fmaf(sm.l[k * C + x], f, W);
       }
       if (sink2 != -INFINITY) W += exp2f(sink2 - M);
-      acc /= W;
+      acc = F8 ? acc * p.v_descale / W : acc / W;
     }
     const uint16_t ob = float_to_bf16_bits(acc);
     const size_t row = ((size_t)b * p.Hq + hf) * kD;
@@ -276,7 +391,11 @@ namespace {
 
 template <int C>
 cudaError_t small_attr_c() {
-  return cudaFuncSetAttribute(small_decode_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
+  const cudaError_t e =
+      cudaFuncSetAttribute(small_decode_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(small_decode_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmallSmem);
 }
 
 // cluster index 0, 1, 2, 3 for C = 8, 4, 2, 1
@@ -325,10 +444,11 @@ int small_max_clusters(int C) {
     cudaLaunchAttribute attr[1];
     cluster_config(&cfg, attr, C, dim3((unsigned)C, 1, 1), nullptr);
     int got = 0;
-    const cudaError_t e = (C == 8)   ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<8>, &cfg)
-                          : (C == 4) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<4>, &cfg)
-                          : (C == 2) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<2>, &cfg)
-                                     : cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<1>, &cfg);
+    // (the e4m3 instances have the same launch shape and shared memory)
+    const cudaError_t e = (C == 8)   ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<8, false>, &cfg)
+                          : (C == 4) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<4, false>, &cfg)
+                          : (C == 2) ? cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<2, false>, &cfg)
+                                     : cudaOccupancyMaxActiveClusters(&got, small_decode_kernel<1, false>, &cfg);
     if (e != cudaSuccess || got <= 0) {
       (void)cudaGetLastError();
       return 0;
@@ -355,10 +475,17 @@ cudaError_t launch_small(const SmallParams& p, int C, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   cluster_config(&cfg, attr, C, dim3((unsigned)C, (unsigned)p.Hkv, (unsigned)p.B), stream);
-  if (C == 8) return cudaLaunchKernelEx(&cfg, small_decode_kernel<8>, p);
-  if (C == 4) return cudaLaunchKernelEx(&cfg, small_decode_kernel<4>, p);
-  if (C == 2) return cudaLaunchKernelEx(&cfg, small_decode_kernel<2>, p);
-  if (C == 1) return cudaLaunchKernelEx(&cfg, small_decode_kernel<1>, p);
+  if (p.kv_fp8) {
+    if (C == 8) return cudaLaunchKernelEx(&cfg, small_decode_kernel<8, true>, p);
+    if (C == 4) return cudaLaunchKernelEx(&cfg, small_decode_kernel<4, true>, p);
+    if (C == 2) return cudaLaunchKernelEx(&cfg, small_decode_kernel<2, true>, p);
+    if (C == 1) return cudaLaunchKernelEx(&cfg, small_decode_kernel<1, true>, p);
+  } else {
+    if (C == 8) return cudaLaunchKernelEx(&cfg, small_decode_kernel<8, false>, p);
+    if (C == 4) return cudaLaunchKernelEx(&cfg, small_decode_kernel<4, false>, p);
+    if (C == 2) return cudaLaunchKernelEx(&cfg, small_decode_kernel<2, false>, p);
+    if (C == 1) return cudaLaunchKernelEx(&cfg, small_decode_kernel<1, false>, p);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -12,15 +12,17 @@ constexpr int kSmallMaxLen = 2048;  // longest sequence (host bound) the path ta
 struct SmallParams {
   const __nv_bfloat16* q;       // [B, Hq, D]
   const __nv_bfloat16* gate;    // [B, Hq, D] (fuse_gate)
-  const __nv_bfloat16* k_pool;  // [num_slots, Hkv, D]
-  const __nv_bfloat16* v_pool;  // [num_slots, Hkv, D]
+  const void* k_pool;           // [num_slots, Hkv, D] bf16, or e4m3 codes (kv_fp8)
+  const void* v_pool;           // [num_slots, Hkv, D] likewise
   const int32_t* indptr;        // [B + 1]
   const int32_t* indices;       // [indptr[B]]
   __nv_bfloat16* out;           // [B, Hq, D]
   float* lse_out;               // [B, Hq] natural log, or null
   const float* sinks;           // [Hq] sink logits, or null
   int B, Hq, Hkv, G;            // G = Hq / Hkv <= 8
-  float scale_log2;             // scale * log2(e)
+  float scale_log2;             // scale * log2(e) (times k_descale for e4m3 pools)
+  int kv_fp8;                   // the pools hold e4m3 codes
+  float v_descale;              // e4m3 pools: V = v_descale * e4m3(code)
   int window;                   // > 0: the last `window` positions only
   int fuse_gate;
 };

@@ -122,8 +122,8 @@ typedef enum gda_status {
  *               not used for bf16 pools.
  *   max_len     0, or an upper bound on every sequence's KV length that the caller knows
  *               on the host (a scheduler's batch maximum).  With a bound of at most
- *               2048, automatic splits (num_splits <= 0), GDA_VARIANT_AUTO, bf16 pools,
- *               no check_indices, Hq / Hkv <= 8, and few enough (sequence, KV head) pairs
+ *               2048, automatic splits (num_splits <= 0), GDA_VARIANT_AUTO, bf16 or e4m3
+ *               pools, no check_indices, Hq / Hkv <= 8, and few enough (sequence, KV head) pairs
  *               (gda_small_path_cluster), the call runs as ONE kernel: a thread-block
  *               cluster of 8, 4, 2 or 1 CTAs per (sequence, KV head) (the most that fit in
  *               one wave, at most 256 positions per CTA) that merges its partial
@@ -260,7 +260,7 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
  * initialise before capture). */
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
 
-/* The cluster size (8, 4, 2 or 1 CTAs per (sequence, KV head)) that a bf16 decode with
+/* The cluster size (8, 4, 2 or 1 CTAs per (sequence, KV head)) that a decode with
  * `pairs` = B * Hkv (sequence, KV head) pairs and the length bound max_len takes on the
  * current device through the one-kernel path, or 0 when it takes the split path
  * (gda_args.max_len).  A CUDA occupancy query on first use, not a host-only check. */

@@ -171,3 +171,49 @@ def test_smaller_clusters(gda, B, lmax, C):
     ref = reference(inp)
     check_close(got, ref.out)
     np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
+
+
+def _check_fp8(got, want, v_scale):
+    # the FP8 tests' tolerance: the absolute term grows with the V scale
+    g = oracle.double_from_bf16(got)
+    w = oracle.double_from_bf16(want)
+    bad = np.abs(g - w) > ATOL * max(1.0, v_scale) + RTOL * np.abs(w)
+    assert not bad.any(), "%d / %d out of tolerance, worst %.3g" % (bad.sum(), bad.size, np.abs(g - w).max())
+
+
+@pytest.mark.parametrize("key", ["b1_l512", "b4_ragged"])
+def test_e4m3_pools(gda, key):
+    # an FP8 (e4m3) cache through the one-kernel path: K and V widened to FP16 while
+    # staged, Q to FP16 with one power-of-two factor, the descales folded in
+    inp = workloads.make_workload(key, kv="e4m3")
+    ml = int(max(inp["lengths"]))
+    d = to_cuda(inp)
+    B, Hq, D = inp["q"].shape
+    Hkv = inp["k_pool"].shape[1]
+    assert gda.small_path_cluster(B * Hkv, ml) > 0
+    ws = torch.full((gda.workspace_bytes(B, Hq, Hkv, D, 0),), 0xA5, dtype=torch.uint8, device="cuda")
+    gda.workspace_init(ws)
+    for kd, vd in ((inp["k_descale"], inp["v_descale"]), (inp["k_descale"] * 0.5, inp["v_descale"] * 3.5)):
+        out = gda.decode_ex(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"],
+                            scale=inp["scale"], max_len=ml, workspace=ws, k_descale=kd, v_descale=vd)
+        torch.cuda.synchronize()
+        assert bool((ws[256:] == 0xA5).all()), "partials were written: the split path ran"
+        ref = oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"],
+                            inp["kv_indices"], inp["scale"], k_descale=kd, v_descale=vd)
+        _check_fp8(bits(out), ref.out, vd / inp["v_descale"])
+
+
+def test_e4m3_sinks_window_lse(gda):
+    inp = workloads.make([0, 1, 65, 700, 129, 2048], seed=77, layout="perm", pool_slots=4000, kv="e4m3")
+    d = to_cuda(inp)
+    sinks = np.linspace(-2, 2, 16).astype(np.float32)
+    lse = torch.empty(6, 16, dtype=torch.float32, device="cuda")
+    out = gda.decode_ex(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"],
+                        scale=inp["scale"], max_len=2048, window=300, lse=lse,
+                        sinks=torch.as_tensor(sinks).cuda(), k_descale=inp["k_descale"], v_descale=inp["v_descale"])
+    torch.cuda.synchronize()
+    ref = oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
+                        inp["scale"], window=300, sinks=sinks.astype(np.float64), k_descale=inp["k_descale"],
+                        v_descale=inp["v_descale"])
+    _check_fp8(bits(out), ref.out, 1.0)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
