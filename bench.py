@@ -12,8 +12,8 @@ needed between calls).  Prints ONE JSON line (rank 0):
              inputs (q, gate, kv_indptr, kv_indices) from pinned host memory, the
              decode, one copy of out back and a wait, all inside gda_decode_step_host;
              the kernels read the inputs from and write out into pinned host memory
-             in place, over the host-device link (bf16 pools without window or
-             sinks; otherwise per-tensor copies around gda.decode)
+             in place, over the host-device link (without window or sinks;
+             otherwise per-tensor copies around gda.decode)
   roofline   stage-1 kernel: algorithmic bytes / its CUDA-event duration vs the
              measured HBM copy bandwidth
   cpu_baseline  the FP64 oracle on the host cores (rank 0, N=1)
@@ -423,7 +423,7 @@ def run_ours(args):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     d2h = out_h.numel() * out_h.element_size()
     k_e2e = min(args.steps, 5000)
-    step_api = args.kv == "bf16" and args.window == 0 and args.sinks is None
+    step_api = args.window == 0 and args.sinks is None
     if step_api:
         # gda_decode_step_host: one packed block in, the decode, one copy out, one wait
         B_, Hq_, D_ = dev["q"].shape
@@ -436,7 +436,7 @@ def run_ours(args):
         # the step's marshalled C call; each step: decode from host_in into out_h, wait
         e2e_step = gda.StepHost(host_in, None, dev["k_pool"], dev["v_pool"], None, out_h, B_, Hq_, nnz_,
                                 scale=inp["scale"], num_splits=args.splits, map_in=True, map_out=True,
-                                stream=stream)
+                                stream=stream, k_descale=kd, v_descale=vd)
     else:
         host = {k: dev[k].cpu().pin_memory() for k in ("q", "gate", "kv_indptr", "kv_indices")}
         h2d = sum(t.numel() * t.element_size() for t in host.values())

@@ -97,8 +97,8 @@ def load(path: Optional[str] = None):
         lib.gda_small_path_cluster.restype = i32
         lib.gda_step_layout.argtypes = [i32, i32, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
         lib.gda_step_layout.restype = ctypes.c_size_t
-        lib.gda_decode_step_host.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, vp, vp, i32, i32, i32, i32, i64, f32,
-                                             i32, i32, i32, vp]
+        lib.gda_decode_step_host.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, i32, f32, f32, vp, vp, i32, i32, i32,
+                                             i32, i64, f32, i32, i32, i32, vp]
         lib.gda_decode_step_host.restype = i32
         lib.gda_reserve.argtypes = [i32, i32, i32, i32, i32]
         lib.gda_reserve.restype = i32
@@ -304,10 +304,12 @@ class StepHost:
 
     def __init__(self, host_in, dev_in, k_pool, v_pool, dev_out, host_out, B: int, Hq: int, nnz: int,
                  scale: Optional[float] = None, num_splits: int = 0, map_in: bool = False, map_out: bool = False,
-                 synchronize: bool = True, stream=None):
+                 synchronize: bool = True, stream=None, k_descale: float = 1.0, v_descale: float = 1.0):
         import torch
-        _check_tensor("k_pool", k_pool, torch.bfloat16, 3)
-        _check_tensor("v_pool", v_pool, torch.bfloat16, 3, k_pool.device)
+        kv = _kv_dtype(k_pool)
+        dt = torch.bfloat16 if kv == KV_BF16 else k_pool.dtype
+        _check_tensor("k_pool", k_pool, dt, 3)
+        _check_tensor("v_pool", v_pool, dt, 3, k_pool.device)
         Hkv, D = k_pool.shape[1], k_pool.shape[2]
         _, total = step_layout(B, Hq, D, nnz)
         if host_in.device.type != "cpu" or host_out.device.type != "cpu":
@@ -329,8 +331,9 @@ class StepHost:
         self.in_bytes, self.out_bytes = total, host_out.numel() * 2
         self._f = load().gda_decode_step_host
         self._args = (vp(_ptr(host_in)), vp(_ptr(dev_in)), total, vp(_ptr(k_pool)), vp(_ptr(v_pool)),
-                      vp(_ptr(dev_out)), vp(_ptr(host_out)), int(B), int(Hq), int(Hkv), int(D), int(nnz),
-                      float(scale), int(num_splits), flags, 1 if synchronize else 0, _stream(stream))
+                      kv, float(k_descale), float(v_descale), vp(_ptr(dev_out)), vp(_ptr(host_out)), int(B), int(Hq),
+                      int(Hkv), int(D), int(nnz), float(scale), int(num_splits), flags, 1 if synchronize else 0,
+                      _stream(stream))
 
     def __call__(self):
         rc = self._f(*self._args)
@@ -341,12 +344,13 @@ class StepHost:
 
 def decode_step_host(host_in, dev_in, k_pool, v_pool, dev_out, host_out, B: int, Hq: int, nnz: int,
                      scale: Optional[float] = None, num_splits: int = 0, map_in: bool = False,
-                     map_out: bool = False, synchronize: bool = True, stream=None):
+                     map_out: bool = False, synchronize: bool = True, stream=None, k_descale: float = 1.0,
+                     v_descale: float = 1.0):
     """``gda_decode_step_host`` once (see StepHost, which keeps the marshalled call for
     repeated steps)."""
     return StepHost(host_in, dev_in, k_pool, v_pool, dev_out, host_out, B, Hq, nnz, scale=scale,
                     num_splits=num_splits, map_in=map_in, map_out=map_out, synchronize=synchronize,
-                    stream=stream)()
+                    stream=stream, k_descale=k_descale, v_descale=v_descale)()
 
 
 def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, workspace=None,

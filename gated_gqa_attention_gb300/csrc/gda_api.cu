@@ -575,9 +575,10 @@ size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]) {
   return offsets[3] + up((size_t)nnz * sizeof(int32_t));
 }
 
-int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, const gda_bf16* k_pool,
-                         const gda_bf16* v_pool, gda_bf16* dev_out, void* host_out, int B, int Hq, int Hkv, int D,
-                         int64_t nnz, float scale, int num_splits, int flags, int synchronize, gda_stream_t stream) {
+int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, const void* k_pool,
+                         const void* v_pool, int kv_dtype, float k_descale, float v_descale, gda_bf16* dev_out,
+                         void* host_out, int B, int Hq, int Hkv, int D, int64_t nnz, float scale, int num_splits,
+                         int flags, int synchronize, gda_stream_t stream) {
   if (B < 0 || nnz < 0) return GDA_ERR_SHAPE;
   if ((flags & ~(GDA_STEP_MAP_IN | GDA_STEP_MAP_OUT)) != 0) return GDA_ERR_ARG;
   if (B == 0) return GDA_OK;
@@ -610,6 +611,9 @@ int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, con
   a.num_splits = num_splits;
   a.fuse_gate = 1;
   a.variant = GDA_VARIANT_AUTO;
+  a.kv_dtype = kv_dtype;
+  a.k_descale = k_descale;
+  a.v_descale = v_descale;
   // nnz bounds every sequence's length: small steps take the one-kernel path
   a.max_len = nnz < (int64_t)0x7FFFFFFF ? (int)nnz : 0x7FFFFFFF;
   int rc = validate_args(&a);

@@ -282,7 +282,8 @@ size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]);
  *   1. one copy of in_bytes from host_in (the packed block, gda_step_layout) to dev_in
  *      (skipped with GDA_STEP_MAP_IN: the kernels then read host_in in place);
  *   2. gda_decode on the views of dev_in, with the device-resident caches k_pool and
- *      v_pool, into dev_out [B, Hq, D] (into host_out with GDA_STEP_MAP_OUT);
+ *      v_pool (GDA_KV_BF16, or GDA_KV_E4M3 codes with k_descale and v_descale as in
+ *      gda_args), into dev_out [B, Hq, D] (into host_out with GDA_STEP_MAP_OUT);
  *   3. one copy of dev_out (B * Hq * D bf16) to host_out (skipped with GDA_STEP_MAP_OUT);
  *   4. with synchronize != 0, a wait for the stream, after which host_out holds the
  *      gated output and host_in may be reused.
@@ -295,10 +296,10 @@ size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]);
  * to keep the call allocation-free).  Returns the first failing step's status;
  * nothing after a failed step is enqueued.  Without synchronize the caller must not
  * touch host_in or read host_out before the stream has passed this call. */
-int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, const gda_bf16* k_pool,
-                         const gda_bf16* v_pool, gda_bf16* dev_out, void* host_out, int B, int Hq, int Hkv,
-                         int D, int64_t nnz, float scale, int num_splits, int flags, int synchronize,
-                         gda_stream_t stream);
+int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, const void* k_pool,
+                         const void* v_pool, int kv_dtype, float k_descale, float v_descale, gda_bf16* dev_out,
+                         void* host_out, int B, int Hq, int Hkv, int D, int64_t nnz, float scale, int num_splits,
+                         int flags, int synchronize, gda_stream_t stream);
 /* flags of gda_decode_step_host (bitwise or):
  *   GDA_STEP_MAP_IN   the kernels read the inputs from host_in itself over the
  *                     host-device link (no copy; dev_in may be NULL);

@@ -246,16 +246,17 @@ def test_step_host_layout_and_validation(lib):
     vp = ctypes.c_void_p
     f = lib.gda_decode_step_host
     f.restype = ctypes.c_int
-    f.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                  ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    f.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, ctypes.c_int, ctypes.c_float, ctypes.c_float, vp, vp, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, vp]
     B, Hq, Hkv, D, nnz = 3, 4, 2, 256, 10
     total = lib.gda_step_layout(B, Hq, D, nnz, off)
 
     def call(host_in=4096, dev_in=4096, nbytes=total, k=4096, v=4096, dout=4096, hout=4096, B=B, Hq=Hq, Hkv=Hkv,
-             D=D, nnz=nnz, splits=0, flags=0):
+             D=D, nnz=nnz, splits=0, flags=0, kv=0, kd=1.0):
         return f(vp(host_in) if host_in else None, vp(dev_in) if dev_in else None, nbytes, vp(k) if k else None,
-                 vp(v) if v else None, vp(dout) if dout else None, vp(hout) if hout else None, B, Hq, Hkv, D, nnz,
-                 0.0625, splits, flags, 1, None)
+                 vp(v) if v else None, kv, kd, 1.0, vp(dout) if dout else None, vp(hout) if hout else None, B, Hq,
+                 Hkv, D, nnz, 0.0625, splits, flags, 1, None)
 
     assert call(B=0) == OK
     assert call(B=-1) == ERR_SHAPE
@@ -273,3 +274,5 @@ def test_step_host_layout_and_validation(lib):
     assert call(flags=4) == ERR_ARG                       # an unknown flag
     assert call(dev_in=0) == ERR_NULL and call(dout=0) == ERR_NULL
     assert call(host_in=4096 + 16, flags=1) == ERR_ALIGN  # a mapped block starts on 256 bytes
+    assert call(kv=7) == ERR_UNSUPPORTED                  # an unknown cache type
+    assert call(kv=1, kd=float("nan")) == ERR_ARG         # e4m3 with a non-finite descale

@@ -217,3 +217,25 @@ def test_e4m3_sinks_window_lse(gda):
                         v_descale=inp["v_descale"])
     _check_fp8(bits(out), ref.out, 1.0)
     np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
+
+
+def test_step_host_e4m3(gda):
+    # the host-memory step over an FP8 cache: the same bits as decode_ex with the bound
+    inp = workloads.make_workload("b4_ragged", kv="e4m3")
+    d = to_cuda(inp)
+    B, Hq, D = inp["q"].shape
+    nnz = inp["kv_indices"].numel()
+    _, total = gda.step_layout(B, Hq, D, nnz)
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    gda.pack_step(host_in, inp["q"], inp["gate"], inp["kv_indptr"], inp["kv_indices"])
+    host_out = torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory()
+    kd, vd = inp["k_descale"], inp["v_descale"]
+    gda.decode_step_host(host_in, None, d["k_pool"], d["v_pool"], None, host_out, B, Hq, nnz, scale=inp["scale"],
+                         map_in=True, map_out=True, k_descale=kd, v_descale=vd)
+    want = gda.decode_ex(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["kv_indptr"], d["kv_indices"],
+                         scale=inp["scale"], max_len=nnz, k_descale=kd, v_descale=vd)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host_out), bits(want))
+    ref = oracle.decode(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["kv_indptr"], inp["kv_indices"],
+                        inp["scale"], k_descale=kd, v_descale=vd)
+    _check_fp8(bits(host_out), ref.out, 1.0)
