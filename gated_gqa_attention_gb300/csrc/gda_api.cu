@@ -61,9 +61,12 @@ struct Layout {
   size_t o_off, lse_off, total;
 };
 
-// Header, then FP32 partial O [pieces][8][D], then partial LSE [pieces][8].
+// Header, then FP32 partial O [pieces][8][D], then partial LSE [pieces][8].  With two
+// passes the size covers both schedules: per virtual head, and paired (one piece per
+// KV head holding both groups' partials), which needs 2 num_pieces(B, Hkv).
 Layout layout(int B, int Hq, int Hkv, int D, int num_splits) {
-  const size_t pieces = num_pieces(B, Hkv * passes(Hq, Hkv), num_splits);
+  const int np = passes(Hq, Hkv);
+  const size_t pieces = (np == 2) ? 2 * num_pieces(B, Hkv, num_splits) : num_pieces(B, Hkv * np, num_splits);
   Layout l;
   l.o_off = gda::kHeaderBytes;
   l.lse_off = round_up(l.o_off + pieces * gda::kG * (size_t)D * sizeof(float), 256);
@@ -159,7 +162,14 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   const Layout l = layout(a->B, a->Hq, a->Hkv, a->D, a->num_splits);
   unsigned char* base = static_cast<unsigned char*>(ws);
   const int npass = passes(a->Hq, a->Hkv);
-  const long long vheads = (long long)a->Hkv * npass;
+  const bool fp8 = a->kv_dtype == GDA_KV_E4M3;
+  const int variant = (a->variant == GDA_VARIANT_SIMT)  ? gda::kVariantSimt
+                      : (a->variant == GDA_VARIANT_TMA) ? gda::kVariantTma
+                                                        : gda::kVariantMma;
+  // G = 9..16 on the MMA kernel: both groups of a KV head in one piece (one HBM read)
+  const bool paired = npass == 2 && !fp8 && variant == gda::kVariantMma;
+  // the heads that split the batch into segments for the schedule
+  const long long vheads = paired ? (long long)a->Hkv : (long long)a->Hkv * npass;
   const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
   const int auto_grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
   int splits = a->num_splits > 0 ? a->num_splits : 0;
@@ -195,8 +205,8 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.Hkv = a->Hkv;
   p1.G = a->Hq / a->Hkv;
   p1.npass = npass;
+  p1.paired = paired ? 1 : 0;
   p1.window = a->window;
-  const bool fp8 = a->kv_dtype == GDA_KV_E4M3;
   // e4m3 pools: k_descale joins the score scale (one rounding, from double)
   p1.scale_log2 = fp8 ? (float)((double)a->scale * (double)a->k_descale * 1.4426950408889634074)
                       : a->scale * 1.44269504088896340736f;
@@ -204,9 +214,6 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.num_splits = splits;
   p1.min_chunk = min_chunk;
   p1.check_indices = a->check_indices ? 1 : 0;
-  const int variant = (a->variant == GDA_VARIANT_SIMT)  ? gda::kVariantSimt
-                      : (a->variant == GDA_VARIANT_TMA) ? gda::kVariantTma
-                                                        : gda::kVariantMma;
   cudaEvent_t t_end = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -234,6 +241,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p2.Hkv = a->Hkv;
   p2.G = p1.G;
   p2.npass = npass;
+  p2.paired = p1.paired;
   p2.window = a->window;
   p2.num_splits = p1.num_splits;
   p2.grid1 = grid;

@@ -1,8 +1,9 @@
 // gda_stage1.cu -- split-KV decode stage 1 on sm_103a, K/V rows loaded straight
 // into registers.
 //
-// Per piece (sequence b, KV head kvh, positions [j0, j1)) and for the G = 8 query
-// heads that share kvh, stage 1 computes the normalised partial
+// Per piece (sequence b, KV head kvh, positions [j0, j1)) and for a group of up to
+// 8 query heads that share kvh (with G = 9..16 on the MMA kernel, both groups at
+// once), stage 1 computes the normalised partial
 //   O_piece = sum_j softmax_piece(scale * q K_j^T) V_j     and     LSE_piece (log2 units)
 // with a running max and running sum, as split-KV decode stage 1 does (FreeToken
 // PR #781 "Fuse the BF16 attention output sigmoid gate into the existing Triton
@@ -91,12 +92,13 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int NWARP, int NV>
+template <int NWARP, int NV, int NG>
 struct MmaSmem {
-  uint2 qf[16][32];                                      // Q^T fragments, lane order
+  uint2 qf[NG][16][32];                                  // Q^T fragments per group, lane order
   unsigned char vring[NWARP][NV][16][kSmemRow];          // per-warp V rings
   float mbuf[NWARP][kG];                                 // each warp's running max
   float lsum[NWARP][kG];                                 // each warp's rescaled sum
+  float4 xs[NG > 1 ? NWARP : 1][2][32];                  // two groups: S^T for the partner warp's group
 };
 
 // Lazy-rescale threshold of the MMA softmax, in log2 units.
@@ -180,9 +182,83 @@ struct MmaWarpState {
     l1 += __uint_as_float(P0 & 0xFFFF0000u) + __uint_as_float(P1 & 0xFFFF0000u);
   }
 
+  // Unscaled S^T of the register K tile against both groups' Q^T fragments (one
+  // A fragment, two MMA chains per group; the same summation order as qk_softmax).
+  __device__ __forceinline__ void qk_raw2(const uint2 (*qa)[32], const uint2 (*qb)[32], float* sa_out,
+                                          float* sb_out, int lane) {
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const int c = kk >> 1, h = kk & 1;
+      const uint4& r0 = kr[c];
+      const uint4& r1 = kr[8 + c];
+      const uint32_t x0 = h ? r0.z : r0.x, x2 = h ? r0.w : r0.y;
+      const uint32_t x1 = h ? r1.z : r1.x, x3 = h ? r1.w : r1.y;
+      const uint2 fa = qa[kk][lane], fb = qb[kk][lane];
+      mma_bf16_16816(h ? a1 : a0, x0, x1, x2, x3, fa.x, fa.y);
+      mma_bf16_16816(h ? b1 : b0, x0, x1, x2, x3, fb.x, fb.y);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      sa_out[i] = a0[i] + a1[i];
+      sb_out[i] = b0[i] + b1[i];
+    }
+  }
+
+  // Online softmax over two 16-token tiles of the same 8 heads: s (na valid rows)
+  // and u (nb valid rows), both unscaled.  Same lazy rescale as qk_softmax; returns
+  // the BF16 P fragments of each tile and adds their rounded values to the sums.
+  __device__ __forceinline__ void softmax2(float* s, int na, float* u, int nb, float sl2, int lane,
+                                           uint32_t& A0, uint32_t& A1, uint32_t& B0, uint32_t& B1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s[i] *= sl2;
+      u[i] *= sl2;
+    }
+    const int tg = lane >> 2;
+    if (tg >= na) s[0] = s[1] = -INFINITY;
+    if (tg + 8 >= na) s[2] = s[3] = -INFINITY;
+    if (tg >= nb) u[0] = u[1] = -INFINITY;
+    if (tg + 8 >= nb) u[2] = u[3] = -INFINITY;
+    float xa = fmaxf(fmaxf(s[0], s[2]), fmaxf(u[0], u[2]));
+    float xb = fmaxf(fmaxf(s[1], s[3]), fmaxf(u[1], u[3]));
+    const bool grow = xa > m0 + kLazyLog2 || xb > m1 + kLazyLog2;
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, off));
+      }
+      const float na_ = fmaxf(m0, xa), nb_ = fmaxf(m1, xb);
+      const float aa = safe_exp2_diff(m0, na_), ab = safe_exp2_diff(m1, nb_);
+      l0 *= aa;
+      l1 *= ab;
+      m0 = na_;
+      m1 = nb_;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= aa;
+        o[i][1] *= ab;
+        o[i][2] *= aa;
+        o[i][3] *= ab;
+      }
+    }
+    A0 = pack_bf16x2(safe_exp2_diff(s[0], m0), safe_exp2_diff(s[1], m1));
+    A1 = pack_bf16x2(safe_exp2_diff(s[2], m0), safe_exp2_diff(s[3], m1));
+    B0 = pack_bf16x2(safe_exp2_diff(u[0], m0), safe_exp2_diff(u[1], m1));
+    B1 = pack_bf16x2(safe_exp2_diff(u[2], m0), safe_exp2_diff(u[3], m1));
+    l0 += __uint_as_float(A0 << 16) + __uint_as_float(A1 << 16) + __uint_as_float(B0 << 16) +
+          __uint_as_float(B1 << 16);
+    l1 += __uint_as_float(A0 & 0xFFFF0000u) + __uint_as_float(A1 & 0xFFFF0000u) +
+          __uint_as_float(B0 & 0xFFFF0000u) + __uint_as_float(B1 & 0xFFFF0000u);
+  }
+
   // O^T += V^T P^T with V^T fragments from a 16-row shared-memory tile
-  __device__ __forceinline__ void pv(const unsigned char* vtile, int lane) {
-    const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
+  __device__ __forceinline__ void pv(const unsigned char* vtile, int lane) { pv_with(vtile, P0, P1, lane); }
+
+  __device__ __forceinline__ void pv_with(const unsigned char* vtile, uint32_t p0, uint32_t p1, int lane) {
+    const uint32_t b0 = movmatrix_trans(p0), b1 = movmatrix_trans(p1);
     const int mj = lane >> 3, mr = lane & 7;
     const uint32_t vaddr = smem_u32(vtile) + (mr + 8 * (mj >> 1)) * kSmemRow + 16 * (mj & 1);
 #pragma unroll
@@ -221,30 +297,50 @@ __device__ __forceinline__ void issue_v_tile(unsigned char* stage, const unsigne
   cp_async_commit();
 }
 
-template <int NWARP, int NV>
+// PAIR (G = 9..16, two groups of 8 query heads per KV head): one piece per
+// (sequence, KV head) serves both groups, and every K/V row is loaded once.
+// Warp w loads tiles w + NWARP*k as without PAIR and computes S^T of its tile for
+// both groups (one K fragment, two MMA chains); warps w and w ^ NWARP/2 form a
+// pair, the first half of the warps owning group 0 and the second half group 1.
+// Each step a warp leaves the partner group's S^T in shared memory, the pair meets
+// at a named barrier, and each warp then runs the softmax and PV of its own group
+// over both tiles: its own (its V ring) and the partner's (the partner's V ring).
+// The partial of (piece, group) is written at piece * 2 + group.  Without PAIR,
+// one piece per (sequence, virtual head).
+template <int NWARP, int NV, bool PAIR>
 __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params p) {
-  using Smem = MmaSmem<NWARP, NV>;
+  constexpr int NG = PAIR ? 2 : 1;  // query-head groups per piece
+  constexpr int WPG = NWARP / NG;   // warps per group
+  using Smem = MmaSmem<NWARP, NV, NG>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  static_assert(16 * 32 == 2 * NWARP * 32, "two Q fragments per thread");
+  const int grp = warp / WPG;                 // this warp's group
+  const int partner = warp ^ (NWARP / 2);     // PAIR: the warp of the other group on the same tiles
+  static_assert(NG * 16 * 32 == 2 * NG * NWARP * 32, "2 NG Q fragments per thread");
+  static_assert(!PAIR || NWARP == 8, "PAIR: four pairs, named barriers 1 .. 4");
 
   // Stage 2 may start its prologue (gate loads and sigmoids) now.
   pdl_launch_dependents();
 
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window);
+  sched.begin(p.indptr, p.B, PAIR ? p.Hkv : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk,
+              p.window);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
   const uint64_t pol_v = l2_policy_evict_first();
+  // KV head of a piece (its scheduled head is the KV head itself when PAIR)
+  auto kv_head = [&](const Piece& pp) -> int { return PAIR ? pp.kvh : pp.kvh / p.npass; };
 
-  // This warp's tiles of a piece of `len` positions: tile warp + NWARP*k.
-  auto nmine_of = [&](int len) -> int {
+  // Warp w's tiles of a piece of `len` positions: tile w + NWARP*k.
+  auto nmine_for = [&](int w, int len) -> int {
     const int ntiles = (len + 15) >> 4;
-    return (ntiles > warp) ? (ntiles - warp + NWARP - 1) / NWARP : 0;
+    return (ntiles > w) ? (ntiles - w + NWARP - 1) / NWARP : 0;
   };
-  auto tile_n = [&](int k, int len, int nmine) -> int {
-    return (k < nmine) ? min(16, len - 16 * (warp + NWARP * k)) : 0;
+  auto tile_n_for = [&](int w, int k, int len, int nm) -> int {
+    return (k < nm) ? min(16, len - 16 * (w + NWARP * k)) : 0;
   };
+  auto nmine_of = [&](int len) -> int { return nmine_for(warp, len); };
+  auto tile_n = [&](int k, int len, int nmine) -> int { return tile_n_for(warp, k, len, nmine); };
   auto fetch = [&](const int* idx, int k, int len, int nmine) -> int {
     const int n = tile_n(k, len, nmine);
     int s = -1;
@@ -259,19 +355,19 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   };
 
   MmaWarpState st;
-  uint2 qfrag[2];
+  uint2 qfrag[2 * NG];
   int s0 = -1, s1 = -1, s2 = -1;
   // Head of a piece: its Q^T fragments (requested first), the slots of this
   // warp's first three tiles and the K rows of its first tile.  For every piece
   // after the first this runs before the previous piece's merge, so the loads
   // are in flight while the warps merge.
   auto piece_head = [&](const Piece& pp) {
-    int gv;
-    const __nv_bfloat16* qg = group_q(p, pp.b, pp.kvh, &gv);
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < 2 * NG; ++r) {
       const int e = threadIdx.x + r * NWARP * 32;
-      const int kk = e >> 5, ln = e & 31;
+      const int fg = e >> 9, kk = (e >> 5) & 15, ln = e & 31;  // group, k-step, lane
+      int gv;
+      const __nv_bfloat16* qg = group_q(p, pp.b, PAIR ? pp.kvh * p.npass + fg : pp.kvh, &gv);
       const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
       const __nv_bfloat16* row = qg + min(g, gv - 1) * kD;  // never addresses a row beyond the group
       qfrag[r] = (g < gv) ? __ldg(reinterpret_cast<const uint2*>(row + 32 * c + 8 * t + 4 * h)) : make_uint2(0u, 0u);
@@ -281,50 +377,86 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
     s0 = fetch(idx, 0, len, nmine);
     s1 = fetch(idx, 1, len, nmine);
     s2 = fetch(idx, 2, len, nmine);
-    if (nmine > 0) st.load_k(p.k_pool + (size_t)(pp.kvh / p.npass) * kRowBytes, stride, s0, lane);
+    if (nmine > 0) st.load_k(p.k_pool + (size_t)kv_head(pp) * kRowBytes, stride, s0, lane);
   };
 
   Piece pc;
   bool have = sched.next(pc);
   if (have) piece_head(pc);
   while (have) {
-    const unsigned char* kb = p.k_pool + (size_t)(pc.kvh / p.npass) * kRowBytes;
-    const unsigned char* vb = p.v_pool + (size_t)(pc.kvh / p.npass) * kRowBytes;
+    const unsigned char* kb = p.k_pool + (size_t)kv_head(pc) * kRowBytes;
+    const unsigned char* vb = p.v_pool + (size_t)kv_head(pc) * kRowBytes;
     const int* idx = p.indices + pc.base + pc.j0;
     const int len = pc.j1 - pc.j0;
     const int nmine = nmine_of(len);
 
     st.reset();  // O, max and sum; the K rows of tile 0 are already in flight
     unsigned char(*ring)[16][kSmemRow] = sm.vring[warp];
-    if (nmine > 0) {
+    // steps of this warp's loop: its tiles, or with PAIR those of the pair's first
+    // warp (the one with more tiles), so that both partners meet at every barrier
+    const int nsteps = PAIR ? nmine_for(warp & (NWARP / 2 - 1), len) : nmine;
+    if (nsteps > 0) {
       issue_v_tile(&ring[0][0][0], vb, stride, s0, tile_n(0, len, nmine), lane, pol_v);
       issue_v_tile(&ring[1 % NV][0][0], vb, stride, s1, tile_n(1, len, nmine), lane, pol_v);
       prefetch_k_tile(kb, stride, s1, lane);
     }
     // the previous piece's merge ended with a barrier: the fragment buffer is free
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < 2 * NG; ++r) {
       const int e = threadIdx.x + r * NWARP * 32;
-      sm.qf[e >> 5][e & 31] = qfrag[r];
+      sm.qf[e >> 9][(e >> 5) & 15][e & 31] = qfrag[r];
     }
     __syncthreads();
 
     int stage = 0;
-    for (int k = 0; k < nmine; ++k) {
-      // V two tiles ahead (an empty group when there is no such tile), K rows of
-      // that tile into L2, the slots three tiles ahead; then tile k's QK
-      issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
-      prefetch_k_tile(kb, stride, s2, lane);
-      const int s3 = fetch(idx, k + 3, len, nmine);
-      st.qk_softmax(sm.qf, tile_n(k, len, nmine), p.scale_log2, lane);
-      if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
-      cp_async_wait<2>();
-      __syncwarp();
-      st.pv(&ring[stage][0][0], lane);
-      __syncwarp();
-      stage = (stage + 1 == NV) ? 0 : stage + 1;
-      s1 = s2;
-      s2 = s3;
+    if constexpr (PAIR) {
+      unsigned char(*pring)[16][kSmemRow] = sm.vring[partner];
+      const int nmp = nmine_for(partner, len);
+      const int bar = 1 + (warp & (NWARP / 2 - 1));
+      for (int k = 0; k < nsteps; ++k) {
+        // K rows of tile k+2 into L2 and the slots of tile k+3; tile k's S^T for both
+        // groups (the partner's group to shared memory); the K rows of tile k+1
+        prefetch_k_tile(kb, stride, s2, lane);
+        const int s3 = fetch(idx, k + 3, len, nmine);
+        const int nown = tile_n(k, len, nmine);
+        float so[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
+        if (nown > 0) st.qk_raw2(sm.qf[grp], sm.qf[grp ^ 1], so, sx, lane);
+        sm.xs[warp][k & 1][lane] = make_float4(sx[0], sx[1], sx[2], sx[3]);
+        if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
+        cp_async_wait<1>();  // this warp's V tile k has landed (tile k+1 may be in flight)
+        // The pair meets: both V tiles k and both S^T are visible, and the partner
+        // has finished step k-1, so ring stage (k+2) % NV (read as stage (k-1) % NV)
+        // and the S^T buffer of step k+2 are free.
+        named_bar_sync(bar, 64);
+        issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
+        const float4 sp = sm.xs[partner][k & 1][lane];
+        float su[4] = {sp.x, sp.y, sp.z, sp.w};
+        const int npar = tile_n_for(partner, k, len, nmp);
+        uint32_t A0, A1, B0, B1;
+        st.softmax2(so, nown, su, npar, p.scale_log2, lane, A0, A1, B0, B1);
+        if (nown > 0) st.pv_with(&ring[stage][0][0], A0, A1, lane);
+        if (npar > 0) st.pv_with(&pring[stage][0][0], B0, B1, lane);
+        stage = (stage + 1 == NV) ? 0 : stage + 1;
+        s1 = s2;
+        s2 = s3;
+      }
+    } else {
+      for (int k = 0; k < nmine; ++k) {
+        // V two tiles ahead (an empty group when there is no such tile), K rows of
+        // that tile into L2, the slots three tiles ahead; then tile k's QK
+        issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
+        prefetch_k_tile(kb, stride, s2, lane);
+        const int s3 = fetch(idx, k + 3, len, nmine);
+        st.qk_softmax(sm.qf[0], tile_n(k, len, nmine), p.scale_log2, lane);
+        if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
+        cp_async_wait<2>();
+        __syncwarp();
+        st.pv(&ring[stage][0][0], lane);
+        __syncwarp();
+        stage = (stage + 1 == NV) ? 0 : stage + 1;
+        s1 = s2;
+        s2 = s3;
+      }
     }
     cp_async_wait<0>();
     __syncwarp();
@@ -347,11 +479,12 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
     __syncthreads();
     {
       const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
-      float Ma = sm.mbuf[0][ha], Mb = sm.mbuf[0][hb];
+      const int x0 = grp * WPG;  // this group's warps: x0 .. x0 + WPG - 1
+      float Ma = sm.mbuf[x0][ha], Mb = sm.mbuf[x0][hb];
 #pragma unroll
-      for (int x = 1; x < NWARP; ++x) {
-        Ma = fmaxf(Ma, sm.mbuf[x][ha]);
-        Mb = fmaxf(Mb, sm.mbuf[x][hb]);
+      for (int x = 1; x < WPG; ++x) {
+        Ma = fmaxf(Ma, sm.mbuf[x0 + x][ha]);
+        Mb = fmaxf(Mb, sm.mbuf[x0 + x][hb]);
       }
       const float fa = (Ma == -INFINITY) ? 0.0f : safe_exp2_diff(st.m0, Ma);
       const float fb = (Mb == -INFINITY) ? 0.0f : safe_exp2_diff(st.m1, Mb);
@@ -370,14 +503,15 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
       }
     }
     __syncthreads();
-    float* op = p.o_part + pc.id * (kG * kD);
-    for (int e = threadIdx.x * 4; e < kG * kD; e += blockDim.x * 4) {
-      const int h = e / kD;
+    // partial (piece, group) at piece * NG + group: NG * 8 heads from pc.id * NG
+    float* op = p.o_part + pc.id * (NG * kG * kD);
+    for (int e = threadIdx.x * 4; e < NG * kG * kD; e += blockDim.x * 4) {
+      const int x0 = (e / (kG * kD)) * WPG, el = e % (kG * kD), h = el / kD;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       float lt = 0.0f;
 #pragma unroll
-      for (int x = 0; x < NWARP; ++x) {
-        const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(&sm.vring[x][0][0][0]) + e);
+      for (int x = x0; x < x0 + WPG; ++x) {
+        const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(&sm.vring[x][0][0][0]) + el);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -391,13 +525,14 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
       acc.w *= inv;
       *reinterpret_cast<float4*>(op + e) = acc;
     }
-    if (threadIdx.x < kG) {
-      float M = sm.mbuf[0][threadIdx.x], lt = 0.0f;
+    if (threadIdx.x < NG * kG) {
+      const int x0 = (threadIdx.x / kG) * WPG, h = threadIdx.x % kG;
+      float M = sm.mbuf[x0][h], lt = 0.0f;
 #pragma unroll
-      for (int x = 1; x < NWARP; ++x) M = fmaxf(M, sm.mbuf[x][threadIdx.x]);
+      for (int x = 1; x < WPG; ++x) M = fmaxf(M, sm.mbuf[x0 + x][h]);
 #pragma unroll
-      for (int x = 0; x < NWARP; ++x) lt += sm.lsum[x][threadIdx.x];
-      p.lse_part[pc.id * kG + threadIdx.x] = (lt > 0.0f) ? M + log2f(lt) : -INFINITY;
+      for (int x = 0; x < WPG; ++x) lt += sm.lsum[x0 + x][h];
+      p.lse_part[pc.id * (NG * kG) + threadIdx.x] = (lt > 0.0f) ? M + log2f(lt) : -INFINITY;
     }
     __syncthreads();  // rings, Q fragments and merge buffers free for the next piece
     pc = nx;
@@ -648,15 +783,10 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
 
 cudaError_t launch_stage1_tma(const Stage1Params& p, int grid, cudaStream_t stream);
 
-cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStream_t stream) {
-  if (variant == kVariantTma) return launch_stage1_tma(p, grid, stream);
-  if (variant == kVariantSimt) {
-    stage1_direct_kernel<DirectSimt><<<grid, kDirectWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
-  }
-  constexpr int kW = 8, kNV = 3;
-  using Smem = MmaSmem<kW, kNV>;
-  auto kern = stage1_mma_kernel<kW, kNV>;
+template <int NWARP, int NV, bool PAIR>
+cudaError_t launch_mma(const Stage1Params& p, int grid, cudaStream_t stream) {
+  using Smem = MmaSmem<NWARP, NV, PAIR ? 2 : 1>;
+  auto kern = stage1_mma_kernel<NWARP, NV, PAIR>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -667,8 +797,18 @@ cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStre
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  kern<<<grid, kW * 32, sizeof(Smem), stream>>>(p);
+  kern<<<grid, NWARP * 32, sizeof(Smem), stream>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStream_t stream) {
+  if (variant == kVariantTma) return launch_stage1_tma(p, grid, stream);
+  if (variant == kVariantSimt) {
+    stage1_direct_kernel<DirectSimt><<<grid, kDirectWarps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  constexpr int kW = 8, kNV = 3;
+  return p.paired ? launch_mma<kW, kNV, true>(p, grid, stream) : launch_mma<kW, kNV, false>(p, grid, stream);
 }
 
 }  // namespace gda

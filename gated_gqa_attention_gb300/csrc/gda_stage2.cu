@@ -30,9 +30,14 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
 
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, h = bh % p.Hq;
-  // query head h belongs to KV head h / G; its slot g in virtual head vh (groups of 8)
+  // query head h belongs to KV head h / G; its slot g in group `pass` (groups of 8).
+  // Stage 1 scheduled pieces per virtual head vh = kvh * npass + pass, or, paired,
+  // per KV head with the partial of (piece, group) at piece * npass + group.
   const int kvh = h / p.G, r = h - kvh * p.G;
-  const int vh = kvh * p.npass + r / kG, g = r % kG;
+  const int pass = r / kG, g = r % kG;
+  const int sched_h = p.paired ? kvh : kvh * p.npass + pass;
+  const int sched_n = p.paired ? p.Hkv : p.Hkv * p.npass;
+  const int id_mul = p.paired ? p.npass : 1, id_add = p.paired ? pass : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // prologue: this thread's two gate values and their BF16 sigmoids
@@ -47,7 +52,7 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   // which partials hold this segment: from kv_indptr, an input, so before the wait
   long long first;
   int n;
-  segment_pieces(p.indptr, b, vh, p.Hkv * p.npass, p.B, p.num_splits, p.grid1, p.min_chunk, p.window, &first, &n);
+  segment_pieces(p.indptr, b, sched_h, sched_n, p.B, p.num_splits, p.grid1, p.min_chunk, p.window, &first, &n);
   // attention sink (a logit in the softmax denominator with no value row), log2 units
   const float sink2 = (p.sinks != nullptr) ? __ldg(p.sinks + h) * 1.44269504088896340736f : -INFINITY;
 
@@ -58,7 +63,7 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
   for (int k = warp; k < n; k += kS2Warps) {
-    const long long id = first + k;
+    const long long id = (first + k) * id_mul + id_add;
     // the LSE and the O rows are loaded together (no dependent round trip)
     const float lse = __ldcg(p.lse_part + id * kG + g);
     const float4* src = reinterpret_cast<const float4*>(p.o_part + (id * kG + g) * kD + lane * 8);

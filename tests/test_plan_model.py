@@ -113,3 +113,31 @@ def test_small_batches_get_one_piece_per_cta():
         per_cta[c] = per_cta.get(c, 0) + (j1 - j0)
     assert max(per_cta.values()) - min(per_cta.values()) <= T
     assert max(per_cta.values()) == T
+
+
+def test_paired_partials_fit_the_workspace():
+    # G = 9..16 on the MMA kernel: pieces are scheduled per (sequence, KV head) and
+    # the partial of (piece, group) sits at piece * 2 + group.  The workspace holds
+    # 2 x the pieces of the per-KV-head schedule, at least what the per-virtual-head
+    # schedule of the other kernels needs; stage 2 finds exactly stage 1's slots.
+    rng = random.Random(11)
+    for _ in range(300):
+        B = rng.randint(1, 80)
+        lens = [rng.choice([0, 1, 16, 17, 65, 700, 4096]) for _ in range(B)]
+        indptr = [0]
+        for L in lens:
+            indptr.append(indptr[-1] + L)
+        Hkv = rng.choice([1, 2, 4])
+        grid = rng.choice([7, 152, 1024])
+        S_user = rng.choice([0, 0, 2, 8])
+        pieces, S, T = stage1_pieces(indptr, Hkv, grid, 64, S_user)
+        cap = 2 * (B * Hkv * S_user if S_user > 0 else AUTO_MAX_CTAS + B * Hkv)
+        cap_vheads = B * 2 * Hkv * S_user if S_user > 0 else AUTO_MAX_CTAS + B * 2 * Hkv
+        assert cap >= cap_vheads
+        slots = [p[4] * 2 + g for p in pieces for g in (0, 1)]
+        assert len(slots) == len(set(slots)) and all(0 <= s < cap for s in slots)
+        for b in range(B):
+            for kvh in range(Hkv):
+                for g in (0, 1):
+                    want = sorted(p[4] * 2 + g for p in pieces if p[0] == b and p[1] == kvh)
+                    assert [i * 2 + g for i in stage2_ids(indptr, Hkv, b, kvh, S, T)] == want
