@@ -134,3 +134,47 @@ def test_paired_groups_workload_sample(gda):
     got = run(gda, inp)
     idx = tuple(pairs.T)
     check_close(got[idx], ref.out[idx])
+
+
+def test_paired_groups_deterministic_and_placement_invariant(gda):
+    # the paired kernel merges the four warps of a group in a fixed order: repeated
+    # calls and a permuted pool (same rows at other slots) give the same bits
+    inp = workloads.make([4096, 700, 1, 2500], seed=611, hq=32, hkv=2, layout="perm", pool_slots=9000)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    n = inp["k_pool"].shape[0]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(n)
+    moved = dict(inp)
+    moved["k_pool"] = inp["k_pool"][perm]
+    moved["v_pool"] = inp["v_pool"][perm]
+    moved["kv_indices"] = inv[inp["kv_indices"].long()].to(torch.int32)
+    for kw in ({}, {"num_splits": 5}):
+        a, b, c = run(gda, inp, **kw), run(gda, inp, **kw), run(gda, moved, **kw)
+        assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+def test_paired_groups_check_indices(gda):
+    inp = workloads.make([300, 200], seed=612, hq=32, hkv=2, layout="perm", pool_slots=600)
+    ws = torch.empty(gda.workspace_bytes(2, 32, 2, 256, 0), dtype=torch.uint8, device="cuda")
+    gda.workspace_init(ws)
+    run(gda, inp, workspace=ws, check_indices=True)
+    assert gda.read_error(ws) == 0
+    bad = inp["kv_indices"].clone()
+    bad[17] = 600         # == num_slots: out of range
+    bad[450] = -1
+    run(gda, dict(inp, kv_indices=bad), workspace=ws, check_indices=True)
+    assert gda.read_error(ws) & gda.DEVERR_INDEX
+
+
+def test_paired_groups_caller_workspace_sizes(gda):
+    # the caller-sized workspace (workspace_bytes) holds the paired schedule's
+    # partials in automatic and explicit-split modes, with a window too
+    lens = [1, 4096, 33, 2000, 0, 5000, 65]
+    inp = workloads.make(lens, seed=613, hq=24, hkv=2, layout="perm", pool_slots=12000)
+    for splits, window in ((0, 0), (3, 0), (0, 700)):
+        ws = torch.empty(gda.workspace_bytes(len(lens), 24, 2, 256, splits), dtype=torch.uint8, device="cuda")
+        gda.workspace_init(ws)
+        ref = reference(inp, window=window)
+        check_close(run(gda, inp, workspace=ws, num_splits=splits, window=window), ref.out)
+        assert gda.read_error(ws) == 0
