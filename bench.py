@@ -303,11 +303,14 @@ def run_ours(args):
     small_c = (gda.small_path_cluster(B * Hkv, max_len) if (args.splits <= 0 and args.variant == 0 and
                                                               Hq // Hkv <= 8) else 0)
     small_path = small_c > 0
+    # with the bound, the batch's exact total too (a scheduler knows both on the host)
+    total_len = int(sum(lengths)) if max_len > 0 else 0
 
     def call():
         gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
                       out=out, workspace=ws, scale=inp["scale"], num_splits=args.splits, variant=args.variant,
-                      window=args.window, sinks=sinks, k_descale=kd, v_descale=vd, max_len=max_len)
+                      window=args.window, sinks=sinks, k_descale=kd, v_descale=vd, max_len=max_len,
+                      total_len=total_len)
 
     ws = torch.empty(gda.workspace_bytes(B, Hq, Hkv, D, args.splits), dtype=torch.uint8, device="cuda")
     gda.workspace_init(ws)

@@ -25,7 +25,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "load", "decode", "decode_ex", "decode_noalloc", "decode_step_host", "StepHost", "step_layout", "small_path_cluster", "pack_step", "STEP_MAP_IN", "STEP_MAP_OUT", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
+    "load", "decode", "decode_ex", "decode_noalloc", "decode_step_host", "StepHost", "step_layout", "small_path_cluster", "auto_splits", "pack_step", "STEP_MAP_IN", "STEP_MAP_OUT", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
     "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
     "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH", "KV_BF16", "KV_E4M3",
 ]
@@ -59,6 +59,7 @@ class _Args(ctypes.Structure):
         ("check_indices", ctypes.c_int), ("variant", ctypes.c_int), ("min_chunk", ctypes.c_int),
         ("window", ctypes.c_int), ("sinks", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
         ("k_descale", ctypes.c_float), ("v_descale", ctypes.c_float), ("max_len", ctypes.c_int),
+        ("total_len", ctypes.c_int64),
     ]
 
 
@@ -95,6 +96,8 @@ def load(path: Optional[str] = None):
         lib.gda_qk_norm_rope_kv_write.restype = i32
         lib.gda_small_path_cluster.argtypes = [i64, i32]
         lib.gda_small_path_cluster.restype = i32
+        lib.gda_auto_splits.argtypes = [i32, i32, i32, i32, i32, i64]
+        lib.gda_auto_splits.restype = i32
         lib.gda_step_layout.argtypes = [i32, i32, i32, i64, ctypes.POINTER(ctypes.c_size_t)]
         lib.gda_step_layout.restype = ctypes.c_size_t
         lib.gda_decode_step_host.argtypes = [vp, vp, ctypes.c_size_t, vp, vp, i32, f32, f32, vp, vp, i32, i32, i32,
@@ -256,6 +259,13 @@ def decode_noalloc(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out, scale:
     return out
 
 
+def auto_splits(B: int, heads: int, grid: int, lmax: int, total: int, min_chunk: int = 0) -> int:
+    """``gda_auto_splits``: the automatic split rule for B sequences (longest lmax,
+    total ``total`` positions), ``heads`` segments per sequence, ``grid`` stage-1 CTAs:
+    the uniform split count, 0 for the stream schedule, -1 for invalid arguments."""
+    return int(load().gda_auto_splits(int(B), int(heads), int(grid), int(min_chunk), int(lmax), int(total)))
+
+
 def small_path_cluster(pairs: int, max_len: int) -> int:
     """``gda_small_path_cluster``: the cluster size (8, 4 or 2) a bf16 decode of
     ``pairs`` = B * Hkv (sequence, KV head) pairs with the length bound ``max_len``
@@ -357,13 +367,15 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
               scale: Optional[float] = None, num_splits: int = 0, fuse_gate: bool = True, lse=None,
               check_indices: bool = False, variant: int = VARIANT_AUTO, min_chunk: int = 0,
               window: int = 0, sinks=None, stream=None, k_descale: float = 1.0, v_descale: float = 1.0,
-              max_len: int = 0):
+              max_len: int = 0, total_len: int = 0):
     """``gda_decode_ex``: caller workspace (allocated here when None), optional LSE
     output, the unfused first half (``fuse_gate=False``), device index checks, the
     stage-1 variant, a sliding window (last ``window`` positions), per-head
     attention sinks (``sinks``: [Hq] float32 CUDA tensor of logits), for e4m3
     pools the per-tensor descales, and ``max_len``: a host-known bound on every
-    sequence's length (0: none), which lets small batches run as one cluster kernel."""
+    sequence's length (0: none), which lets small batches run as one cluster kernel,
+    and ``total_len``: the batch's exact number of KV positions (kv_indptr[B], 0: not
+    given); with both, the split count is chosen on the host (``auto_splits``)."""
     import torch
     kv = _decode_checks(q, gate_t if fuse_gate else None, k_pool, v_pool, kv_indptr, kv_indices, out)
     B, Hq, D = q.shape
@@ -388,7 +400,7 @@ def decode_ex(q, gate_t, k_pool, v_pool, kv_indptr, kv_indices, out=None, *, wor
               scale=float(scale), num_splits=int(num_splits), fuse_gate=1 if fuse_gate else 0,
               check_indices=1 if check_indices else 0, variant=int(variant), min_chunk=int(min_chunk),
               window=int(window), sinks=_ptr(sinks), kv_dtype=kv, k_descale=float(k_descale),
-              v_descale=float(v_descale), max_len=int(max_len))
+              v_descale=float(v_descale), max_len=int(max_len), total_len=int(total_len))
     _check(load().gda_decode_ex(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

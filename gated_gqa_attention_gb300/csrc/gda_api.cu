@@ -89,7 +89,7 @@ int validate_args(const gda_args* a) {
   if (rc != GDA_OK) return rc;
   if (a->check_indices && a->num_slots < 0) return GDA_ERR_SHAPE;
   if (a->variant < 0 || a->variant > GDA_VARIANT_TMA) return GDA_ERR_UNSUPPORTED;
-  if (a->min_chunk < 0 || a->window < 0 || a->max_len < 0) return GDA_ERR_SHAPE;
+  if (a->min_chunk < 0 || a->window < 0 || a->max_len < 0 || a->total_len < 0) return GDA_ERR_SHAPE;
   if (a->kv_dtype != GDA_KV_BF16 && a->kv_dtype != GDA_KV_E4M3) return GDA_ERR_UNSUPPORTED;
   if (a->kv_dtype == GDA_KV_E4M3) {
     if (a->variant != GDA_VARIANT_AUTO && a->variant != GDA_VARIANT_MMA) return GDA_ERR_UNSUPPORTED;
@@ -103,6 +103,29 @@ int validate_args(const gda_args* a) {
       (a->lse && !aligned(a->lse, 4)) || (a->sinks && !aligned(a->sinks, 4)))
     return GDA_ERR_ALIGN;
   return GDA_OK;
+}
+
+// The automatic split rule on the host: the same arithmetic as the device's
+// (Sched::auto_uniform_splits) on a longest length lmax and a total n that the
+// caller knows; 0 selects the stream schedule.
+int host_uniform_splits(long long B, long long heads, long long grid, int min_chunk, long long lmax, long long n) {
+  const long long units1 = B * heads;
+  if (units1 > grid) return 0;
+  if (units1 == 0) return 1;
+  if (heads * n >= (long long)gda::kStreamMinPerCta * grid) return 0;
+  if (4 * lmax * B > 5 * n) return 0;
+  long long s_opt = 1;
+  while (16 * s_opt * s_opt <= lmax) s_opt *= 2;
+  const long long s_len = lmax > 0 ? (lmax + min_chunk - 1) / min_chunk : 1;
+  long long s = s_opt < s_len ? s_opt : s_len;
+  const long long s_wave = grid / units1;
+  if (s >= s_wave) {
+    long long p2 = 1;
+    while (2 * p2 <= s_wave) p2 *= 2;
+    s = (5 * p2 * units1 >= 4 * grid) ? p2 : s_wave;
+    if (5 * s * units1 < 4 * grid) return 0;
+  }
+  return (int)s;
 }
 
 // Enqueue both stages.  Arguments validated; workspace large enough.
@@ -173,6 +196,12 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
   const int auto_grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
   int splits = a->num_splits > 0 ? a->num_splits : 0;
+  if (splits == 0 && a->window == 0 && a->max_len > 0 && a->total_len > 0) {
+    // the caller knows a bound on the longest length and the exact total: the rule
+    // runs here, and uniform splits launch as explicit ones (no scan of kv_indptr
+    // on the device, no idle CTAs)
+    splits = host_uniform_splits(a->B, vheads, auto_grid, min_chunk, a->max_len, a->total_len);
+  }
   if (splits == 0 && a->window > 0) {
     // A window bounds every sequence's range by `window`: equal splits of at least
     // min_chunk positions, about one per CTA (this fits the automatic workspace).
@@ -567,6 +596,11 @@ int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {
   return ensure_workspace(need, nullptr, false, &ws);
 }
 
+int gda_auto_splits(int B, int heads, int grid, int min_chunk, int lmax, int64_t total) {
+  if (B < 0 || heads < 1 || grid < 1 || lmax < 0 || total < 0) return -1;
+  return host_uniform_splits(B, heads, grid, min_chunk > 0 ? min_chunk : kDefaultMinChunk, lmax, total);
+}
+
 int gda_small_path_cluster(int64_t pairs, int max_len) {
   if (pairs < 0) return 0;
   return gda::small_cluster_for((long long)pairs, max_len);
@@ -622,8 +656,7 @@ int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, con
   a.kv_dtype = kv_dtype;
   a.k_descale = k_descale;
   a.v_descale = v_descale;
-  // nnz bounds every sequence's length: small steps take the one-kernel path
-  a.max_len = nnz < (int64_t)0x7FFFFFFF ? (int)nnz : 0x7FFFFFFF;
+  a.total_len = nnz;  // kv_indptr[B] == nnz; max_len is read below
   int rc = validate_args(&a);
   if (rc != GDA_OK) return rc;
   // mapped host memory: the device address of each pointer (page-locked host memory only)
@@ -658,6 +691,20 @@ int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, con
   void* ws = nullptr;
   rc = ensure_workspace(gda_workspace_bytes(B, Hq, Hkv, D, num_splits), st, true, &ws);
   if (rc != GDA_OK) return rc;
+  // The longest sequence, read on the host from kv_indptr in host_in (B + 1 values),
+  // once every check above has passed: the dispatch's exact bound (none if kv_indptr
+  // is not monotone).
+  {
+    const int32_t* hp = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(host_in) + off[2]);
+    long long lmax = 0;
+    bool mono = true;
+    for (int b = 0; b < B && mono; ++b) {
+      const long long d = (long long)hp[b + 1] - (long long)hp[b];
+      mono = d >= 0;
+      if (d > lmax) lmax = d;
+    }
+    a.max_len = mono ? (int)(lmax < 0x7FFFFFFF ? lmax : 0x7FFFFFFF) : 0;
+  }
   if (!map_in && cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return GDA_ERR_CUDA;
   rc = enqueue(&a, ws, st);

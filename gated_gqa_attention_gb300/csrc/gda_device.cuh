@@ -199,6 +199,10 @@ __device__ __forceinline__ void seq_range(const int* indptr, int b, int window, 
   *base = (long long)i0 + off;
 }
 
+// Automatic mode: per-CTA stream length from which the chunked schedule is used
+// even for batches that fit one wave of uniform splits.
+constexpr int kStreamMinPerCta = 3072;
+
 struct Sched {
   const int* indptr;
   int B, Hkv, S, grid, cta, window;
@@ -266,19 +270,47 @@ struct Sched {
     return lo;
   }
 
-  // Automatic mode, small batches: the uniform split count, or 0 for the
-  // chunked (stream) schedule.  Called by every lane of a full warp: the longest
-  // sequence is found with the lanes striding over the batch.
+  // Automatic mode: the uniform split count S (every segment cut into S equal
+  // pieces), or 0 for the chunked (stream) schedule.  Called by every lane of a
+  // full warp: the longest sequence is found with the lanes striding over the batch.
+  // The rule comes from split sweeps on GB300 (equal lengths, B = 1 .. 128, L = 512
+  // .. 32768, every S in 1 .. 128):
+  //  * a call costs about a + b L/S (stage 1, one piece per CTA) + c S (stage 2
+  //    merges S partials per head), c/b ~ 8 positions, so the best S is near
+  //    sqrt(lmax / 8): S_opt, the smallest power of two with 16 S^2 > lmax, and at
+  //    most ceil(lmax / min_chunk);
+  //  * at most one wave of CTAs (B Hkv S <= grid); when the wave bounds S, the
+  //    power of two below the bound if it keeps >= 80 % of the CTAs busy (pieces
+  //    aligned to the warps' tiles), else the bound itself, and with < 80 % busy
+  //    the stream schedule;
+  //  * the stream schedule once each CTA would stream >= 3072 positions (it then
+  //    wins by 1-3 %: no idle SMs) or when the lengths are far from equal
+  //    (lmax > 1.25 x the mean: S pieces of the longest sequence bound the call).
   static __device__ __forceinline__ int auto_uniform_splits(const int* indptr, int B, int Hkv, int grid,
                                                             int min_chunk) {
-    if ((long long)B * Hkv > grid) return 0;
+    const long long units1 = (long long)B * Hkv;  // one piece per segment
+    if (units1 > grid) return 0;
+    if (units1 == 0) return 1;
+    const long long n = __ldg(indptr + B);  // issued with the scan's loads: one round trip
     int lmax = 0;
     for (int b = (int)(threadIdx.x & 31); b < B; b += 32)
       lmax = max(lmax, __ldg(indptr + b + 1) - __ldg(indptr + b));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
-    const int s = max(1, (lmax + min_chunk - 1) / min_chunk);
-    return ((long long)B * Hkv * s <= grid) ? s : 0;
+    if ((long long)Hkv * n >= (long long)kStreamMinPerCta * grid) return 0;
+    if (4LL * lmax * B > 5LL * n) return 0;
+    int s_opt = 1;
+    while (16LL * s_opt * s_opt <= lmax) s_opt *= 2;
+    const int s_len = max(1, (lmax + min_chunk - 1) / min_chunk);
+    int s = min(s_opt, s_len);
+    const int s_wave = (int)(grid / units1);
+    if (s >= s_wave) {
+      int p2 = 1;
+      while (2 * p2 <= s_wave) p2 *= 2;
+      s = (5LL * p2 * units1 >= 4LL * grid) ? p2 : s_wave;
+      if (5LL * s * units1 < 4LL * grid) return 0;
+    }
+    return s;
   }
 
   static __device__ __forceinline__ long long auto_chunk(long long total, int grid, int min_chunk) {

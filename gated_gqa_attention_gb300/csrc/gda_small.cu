@@ -6,7 +6,7 @@
 // computed in one launch for batches whose latency, not bandwidth, sets the time.
 //
 // One thread-block cluster of C = 8, 4, 2 or 1 CTAs per (sequence b, KV head) (the host
-// takes the largest C whose clusters all run at once and leave each CTA at most 256
+// takes the largest C whose clusters all run at once and leave each CTA at most 128
 // positions): CTA r takes the r-th of C
 // parts of the sequence's attended positions, in chunks of 64 whose K and V rows
 // the CTA's 256 threads bring into shared memory (cp.async, two buffers, the next
@@ -461,7 +461,7 @@ int small_max_clusters(int C) {
 int small_cluster_for(long long pairs, int max_len) {
   if (max_len <= 0 || max_len > kSmallMaxLen) return 0;
   for (int C = 8; C >= 1; C /= 2)
-    if (max_len <= 256 * C && pairs <= (long long)small_max_clusters(C)) return C;
+    if (max_len <= 128 * C && pairs <= (long long)small_max_clusters(C)) return C;
   return 0;
 }
 

@@ -7,7 +7,7 @@
 
 namespace gda {
 
-constexpr int kSmallMaxLen = 2048;  // longest sequence (host bound) the path takes
+constexpr int kSmallMaxLen = 1024;  // longest sequence (host bound) the path takes
 
 struct SmallParams {
   const __nv_bfloat16* q;       // [B, Hq, D]
@@ -36,9 +36,9 @@ int small_max_clusters(int C);
 
 // The cluster size for `pairs` (sequence, KV head) pairs whose lengths are at most
 // max_len, or 0 for the split path: the largest C whose clusters all run at once (one
-// wave) and give each CTA at most 256 positions (max_len <= 256 C).  Measured on
-// GB300 against the split path: 0.55-0.8x its time inside these bounds, slower
-// outside them.
+// wave) and give each CTA at most 128 positions (max_len <= 128 C).  Measured on
+// GB300 against the split path with its split count chosen on the host: 0.67-0.9x
+// its time inside these bounds; with 256 positions per CTA mostly slower.
 int small_cluster_for(long long pairs, int max_len);
 
 }  // namespace gda

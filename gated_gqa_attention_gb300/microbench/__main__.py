@@ -1,6 +1,6 @@
 """Build and run a probe (needs a GPU):
 
-    python -m gated_gqa_attention_gb300.microbench [gather|mma|tma|issue|paths]
+    python -m gated_gqa_attention_gb300.microbench [gather|mma|tma|issue|paths|splits]
 
 gather: how scattered K/V rows stream (16-byte loads, cp.async, 1-D bulk copies);
 mma:    tcgen05.mma throughput per instruction shape (M = 128, N = 64 / 128 / 256,
@@ -10,7 +10,10 @@ tma:    tensor-map (cp.async.bulk.tensor) throughput for [64 x 256] BF16 tiles o
 issue:  how waits in the MMA-issuing thread stall the tensor pipe, and the attention
         mainloop's MMA schedules (64-key tiles, 128-key tiles with one or two issuers);
 paths:  the decode's one-kernel cluster path against the split path over batch and
-        length (decode_paths.py)."""
+        length (decode_paths.py);
+splits: every explicit split count against the automatic schedule per (batch, length)
+        bucket (split_sweep.py; an optional second argument names a JSON output, or
+        `cross` times uniform splits against the stream schedule near the rule's bounds)."""
 import os
 import subprocess
 import sys
@@ -24,6 +27,13 @@ def main():
     if which == "paths":
         from gated_gqa_attention_gb300.microbench import decode_paths
         decode_paths.main()
+        return
+    if which == "splits":
+        from gated_gqa_attention_gb300.microbench import split_sweep
+        if len(sys.argv) > 2 and sys.argv[2] == "cross":
+            split_sweep.crossover()
+        else:
+            split_sweep.main(sys.argv[2] if len(sys.argv) > 2 else None)
         return
     src = os.path.join(HERE, PROBES[which])
     exe = os.path.join(HERE, which + "_probe")

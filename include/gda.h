@@ -122,15 +122,20 @@ typedef enum gda_status {
  *               not used for bf16 pools.
  *   max_len     0, or an upper bound on every sequence's KV length that the caller knows
  *               on the host (a scheduler's batch maximum).  With a bound of at most
- *               2048, automatic splits (num_splits <= 0), GDA_VARIANT_AUTO, bf16 or e4m3
+ *               1024, automatic splits (num_splits <= 0), GDA_VARIANT_AUTO, bf16 or e4m3
  *               pools, no check_indices, Hq / Hkv <= 8, and few enough (sequence, KV head) pairs
  *               (gda_small_path_cluster), the call runs as ONE kernel: a thread-block
  *               cluster of 8, 4, 2 or 1 CTAs per (sequence, KV head) (the most that fit in
- *               one wave, at most 256 positions per CTA) that merges its partial
+ *               one wave, at most 128 positions per CTA) that merges its partial
  *               softmax states in distributed shared
  *               memory and applies the gate, with no workspace traffic.  The result
  *               is the same function within the tolerance of the split path.  A bound
  *               below an actual length still gives the right result, only slower.
+ *   total_len   0, or the batch's exact number of KV positions (kv_indptr[B]) known on
+ *               the host.  With max_len > 0 too, automatic splits and no window, the
+ *               split count is chosen on the host (gda_auto_splits with lmax = max_len)
+ *               and uniform splits launch as explicit ones: no scan of kv_indptr on the
+ *               device and no idle CTAs.  A wrong value changes only the speed.
  * (FreeToken PR #781, Automatic dispatch and Correctness: window, sinks, custom scale
  * and non-power-of-two GQA groups are the cases of the general path.)
  */
@@ -157,6 +162,7 @@ typedef struct gda_args {
     float k_descale;
     float v_descale;
     int max_len;
+    int64_t total_len;
 } gda_args;
 
 /* Bytes of workspace gda_decode_ex needs for these sizes (FreeToken PR #781 Summary:
@@ -266,6 +272,22 @@ int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
  * (gda_args.max_len).  A CUDA occupancy query on first use, not a host-only check. */
 int gda_small_path_cluster(int64_t pairs, int max_len);
 
+/* The automatic split rule ("chosen per (B, length) from measured time", FreeToken
+ * PR #781, Performance), evaluated for B sequences whose longest has lmax positions
+ * and whose total is `total`, `heads` segments per sequence (KV heads, or groups of
+ * 8 query heads) and `grid` stage-1 CTAs: the uniform split count S (every sequence
+ * cut into S equal pieces), or 0 for the stream schedule (equal chunks of the whole
+ * batch).  The device applies the same rule to kv_indptr when the caller passes no
+ * bound; gda_args.max_len with total_len applies it on the host.  -1 for invalid
+ * arguments; min_chunk <= 0 takes the library default (64).  Pure host arithmetic.
+ * The rule, measured on GB300:
+ *  - about sqrt(lmax / 8) splits (a power of two), at least min_chunk positions each;
+ *  - at most one wave of CTAs; when the wave bounds S, the power of two below it if
+ *    >= 80 % of the CTAs stay busy, else the bound; below 80 % busy, the stream;
+ *  - the stream once each CTA would take >= 3072 positions, or when the longest
+ *    sequence is more than 1.25 x the mean. */
+int gda_auto_splits(int B, int heads, int grid, int min_chunk, int lmax, int64_t total);
+
 /* Byte layout of one decode step's inputs packed into a single block, as
  * gda_decode_step_host takes them: q [B, Hq, D] bf16 at offsets[0] (= 0), gate
  * [B, Hq, D] bf16 at offsets[1], kv_indptr [B + 1] int32 at offsets[2] and
@@ -292,7 +314,10 @@ size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]);
  * runtime then stages it through its own buffers.  dev_in is device memory,
  * 256-byte aligned, at least gda_step_layout(...) bytes; in_bytes must equal that
  * size.  As for gda_decode, every kv_indices entry must name a row of the pools, and
- * kv_indptr[B] must equal nnz (index contents are not checked on the host).  The workspace is the library's, as for gda_decode (gda_reserve first
+ * kv_indptr[B] must equal nnz (index contents are not checked on the host).  The
+ * host reads the B + 1 kv_indptr values of host_in to pass the longest length and
+ * nnz as gda_args.max_len and total_len (the one-kernel path or a host-chosen split
+ * count where they apply).  The workspace is the library's, as for gda_decode (gda_reserve first
  * to keep the call allocation-free).  Returns the first failing step's status;
  * nothing after a failed step is enqueued.  Without synchronize the caller must not
  * touch host_in or read host_out before the stream has passed this call. */

@@ -127,6 +127,9 @@ def test_decode_ex_host_validation(lib):
     a7 = gda._Args.from_buffer_copy(args)
     a7.sinks = 6
     assert call(a7) == ERR_ALIGN
+    a7 = gda._Args.from_buffer_copy(args)
+    a7.total_len = -1
+    assert call(a7) == ERR_SHAPE
     # e4m3 pools: the MMA kernel only, finite descales, a known element type
     a8 = gda._Args.from_buffer_copy(args)
     a8.kv_dtype = 2
@@ -276,3 +279,29 @@ def test_step_host_layout_and_validation(lib):
     assert call(host_in=4096 + 16, flags=1) == ERR_ALIGN  # a mapped block starts on 256 bytes
     assert call(kv=7) == ERR_UNSUPPORTED                  # an unknown cache type
     assert call(kv=1, kd=float("nan")) == ERR_ARG         # e4m3 with a non-finite descale
+
+
+def test_auto_splits_matches_the_plan_model(lib):
+    # gda_auto_splits (host) restates the device rule; the CPU plan model restates
+    # both: they agree on random batches, and invalid arguments give -1
+    import random
+    import test_plan_model as plan
+    rng = random.Random(21)
+    for _ in range(3000):
+        B = rng.randint(0, 200)
+        lens = [rng.choice([0, 1, 16, 65, 300, 512, 2048, 3000, 8192, 32768]) for _ in range(B)]
+        if rng.random() < 0.5:
+            lens = [lens[0] if B else 0] * B
+        indptr = [0]
+        for L in lens:
+            indptr.append(indptr[-1] + L)
+        heads, grid, mc = rng.choice([1, 2, 4, 8]), rng.choice([7, 148, 152]), rng.choice([16, 64])
+        lmax = max(lens + [0])
+        assert gda.auto_splits(B, heads, grid, lmax, indptr[-1], mc) == plan.uniform_splits(indptr, heads, grid, mc)
+    assert gda.auto_splits(-1, 2, 152, 10, 10) == -1
+    assert gda.auto_splits(4, 0, 152, 10, 10) == -1
+    assert gda.auto_splits(4, 2, 152, 10, -5) == -1
+    # the bench workloads: stream for b64_l4096 and b8_l131072, 8 splits for B4 ragged
+    assert gda.auto_splits(64, 2, 152, 4096, 64 * 4096) == 0
+    assert gda.auto_splits(8, 2, 152, 131072, 8 * 131072) == 0
+    assert gda.auto_splits(4, 2, 152, 512, 1946) == 8

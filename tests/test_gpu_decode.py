@@ -312,3 +312,21 @@ def test_workload_parity_other_variants(gda, variant):
     out = run(gda, dev, num_splits=0, variant=variant)
     torch.cuda.synchronize()
     check_close(bits(out), ref.out)
+
+
+@pytest.mark.parametrize("lens", [[5000], [2048] * 4, [3000, 2900, 3100], [700] * 24, [64] * 40])
+def test_host_planned_splits(gda, lens):
+    # max_len with the exact total: the host applies the split rule and uniform
+    # splits run as explicit ones -- the same bits as that explicit count, and the
+    # oracle's result within the tolerance
+    inp = workloads.make(lens, seed=71 + len(lens), layout="perm", pool_slots=sum(lens) + 500)
+    ref = reference(inp)
+    dev = to_cuda(inp)
+    S = gda.auto_splits(len(lens), 2, 152, max(lens), sum(lens))
+    # variant MMA (not AUTO) keeps the call off the one-kernel cluster path
+    planned = run(gda, dev, max_len=max(lens), total_len=sum(lens), variant=1)
+    torch.cuda.synchronize()
+    check_close(bits(planned), ref.out)
+    explicit = run(gda, dev, num_splits=S, variant=1) if S > 0 else run(gda, dev, variant=1)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(planned), bits(explicit))

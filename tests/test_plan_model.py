@@ -12,13 +12,35 @@ import random
 AUTO_MAX_CTAS = 1024
 
 
+STREAM_MIN_PER_CTA = 3072
+
+
 def uniform_splits(indptr, Hkv, grid, min_chunk):
+    """The automatic split rule (Sched::auto_uniform_splits): S uniform splits, or 0
+    for the stream schedule."""
     B = len(indptr) - 1
-    if B * Hkv > grid:
+    units1 = B * Hkv
+    if units1 > grid:
         return 0
+    if units1 == 0:
+        return 1
     lmax = max([indptr[b + 1] - indptr[b] for b in range(B)] + [0])
-    s = max(1, -(-lmax // min_chunk))
-    return s if B * Hkv * s <= grid else 0
+    n = indptr[B]
+    if Hkv * n >= STREAM_MIN_PER_CTA * grid or 4 * lmax * B > 5 * n:
+        return 0
+    s_opt = 1
+    while 16 * s_opt * s_opt <= lmax:
+        s_opt *= 2
+    s = min(s_opt, max(1, -(-lmax // min_chunk)))
+    s_wave = grid // units1
+    if s >= s_wave:
+        p2 = 1
+        while 2 * p2 <= s_wave:
+            p2 *= 2
+        s = p2 if 5 * p2 * units1 >= 4 * grid else s_wave
+        if 5 * s * units1 < 4 * grid:
+            return 0
+    return s
 
 
 def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
@@ -97,6 +119,21 @@ def test_plan_invariants_random_batches():
             for kvh in range(Hkv):
                 mine = sorted(p[4] for p in pieces if p[0] == b and p[1] == kvh)
                 assert stage2_ids(indptr, Hkv, b, kvh, S, T) == mine
+
+
+def test_split_rule_on_measured_buckets():
+    # the choices the GB300 sweeps found best (Hkv = 2, 152 CTAs, equal lengths)
+    eq = lambda B, L: [L * i for i in range(B + 1)]
+    want = {(1, 512): 8, (1, 2048): 16, (1, 8192): 32, (1, 32768): 64, (2, 32768): 32, (4, 2048): 16,
+            (4, 32768): 16, (8, 2048): 8, (16, 512): 4, (24, 8192): 3, (32, 2048): 2, (64, 512): 1,
+            (64, 2048): 1, (64, 3072): 1,
+            # stream schedule: >= 3072 positions per CTA, < 80 % of the CTAs busy, more than a wave
+            (64, 4096): 0, (16, 32768): 0, (8, 131072): 0, (48, 4096): 0, (128, 512): 0}
+    for (B, L), S in want.items():
+        assert uniform_splits(eq(B, L), 2, 152, 64) == S, (B, L)
+    # far from equal lengths: the stream schedule balances them
+    assert uniform_splits([0, 8000, 8100, 8200, 30000], 2, 152, 64) == 0
+    assert uniform_splits([0], 2, 152, 64) == 1 and uniform_splits([0, 0, 0], 2, 152, 64) == 1
 
 
 def test_small_batches_get_one_piece_per_cta():
