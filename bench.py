@@ -487,7 +487,7 @@ def run_ours(args):
                        "Hq": Hq, "Hkv": Hkv, "D": D, "num_splits": args.splits or "auto", "kv": args.kv,
                        "variant": ("cluster of %d (one kernel)" % small_c if small_path else
                                    {0: "auto(mma)", 1: "mma", 2: "simt", 3: "tma-ring+mma"}[args.variant]),
-                       "max_len_hint": max_len,
+                       "max_len_hint": max_len, "total_len_hint": total_len,
                        "bytes_per_call": nbytes,
                        "l2": "inputs larger than L2 (%.0f MB of K/V rows per call), no flush" % (nbytes / 1e6),
                        "parallelism": "replicas x%d" % world, "window": args.window, "sinks": args.sinks,
