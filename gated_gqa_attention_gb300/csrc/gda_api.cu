@@ -343,14 +343,15 @@ int noalloc_scratch(cudaStream_t stream, void** out) {
 __device__ unsigned int g_prefill_error;
 unsigned int* g_prefill_error_ptr[kMaxDevices] = {};
 
-int prefill_error_word(cudaStream_t stream, unsigned int** out) {
+int prefill_error_word(unsigned int** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_prefill_error_ptr[dev] == nullptr) {
     void* ptr = nullptr;
+    // a zero-initialised __device__ word: nothing to enqueue (so a call refused later,
+    // e.g. under capture, leaves no work behind)
     if (cudaGetSymbolAddress(&ptr, g_prefill_error) != cudaSuccess || ptr == nullptr) return GDA_ERR_CUDA;
-    if (cudaMemsetAsync(ptr, 0, sizeof(unsigned int), stream) != cudaSuccess) return GDA_ERR_CUDA;
     g_prefill_error_ptr[dev] = static_cast<unsigned int*>(ptr);
   }
   *out = g_prefill_error_ptr[dev];
@@ -542,7 +543,7 @@ int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   unsigned int* err = error_word;
   if (err == nullptr) {
-    int rc = prefill_error_word(s, &err);
+    int rc = prefill_error_word(&err);
     if (rc != GDA_OK) return rc;
   }
   gda::PrefillParams p;
@@ -562,7 +563,9 @@ int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, cons
   // with Skv == 0 the key maps still need a valid base: the queries' (never loaded)
   const void* kb = Skv > 0 ? static_cast<const void*>(k) : static_cast<const void*>(q);
   const void* vb = Skv > 0 ? static_cast<const void*>(v) : static_cast<const void*>(q);
-  if (gda::launch_prefill(p, q, kb, vb, gate, s) != cudaSuccess) return GDA_ERR_CUDA;
+  const cudaError_t le = gda::launch_prefill(p, q, kb, vb, gate, s);
+  if (le == cudaErrorStreamCaptureUnsupported) return GDA_ERR_CAPTURE;  // first use while capturing
+  if (le != cudaSuccess) return GDA_ERR_CUDA;
   return GDA_OK;
 }
 
@@ -570,7 +573,7 @@ int gda_prefill_read_error(gda_stream_t stream, int clear, uint32_t* error_word)
   if (error_word == nullptr) return GDA_ERR_NULL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   unsigned int* dev_word = nullptr;
-  int rc = prefill_error_word(s, &dev_word);
+  int rc = prefill_error_word(&dev_word);
   if (rc != GDA_OK) return rc;
   unsigned int w = 0;
   if (cudaMemcpyAsync(&w, dev_word, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDA_ERR_CUDA;

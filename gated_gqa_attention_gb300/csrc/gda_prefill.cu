@@ -43,6 +43,8 @@
 // stay warp-convergent (decisions combined with __all_sync).
 #include <cuda.h>
 
+#include <mutex>
+
 #include "gda_device.cuh"
 #include "gda_kernels.h"
 #include "gda_prefill.h"
@@ -766,6 +768,34 @@ bool make_map_kv(CUtensorMap* m, const void* base, int B, int S, int H, int rows
 
 }  // namespace
 
+// First use on a device: the kernel's shared-memory limit and the sigmoid table.
+// The table is built on a private stream that is waited for before the device is
+// marked ready, so every later call, on any stream or thread, finds it complete.
+// Refused while `stream` is capturing: the table must exist outside any graph.
+static cudaError_t prefill_init(int dev, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool ready[64] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  if (ready[dev]) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
+  e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaStream_t own = nullptr;
+  e = cudaStreamCreateWithFlags(&own, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return e;
+  sigmoid_table_kernel<<<256, 256, 0, own>>>();
+  e = cudaGetLastError();
+  const cudaError_t es = cudaStreamSynchronize(own);
+  cudaStreamDestroy(own);
+  if (e != cudaSuccess) return e;
+  if (es != cudaSuccess) return es;
+  ready[dev] = true;
+  return cudaSuccess;
+}
+
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k, const void* v, const void* gate,
                            cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tg, to;
@@ -776,20 +806,12 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k,
       !make_map_kv(&tg, gate ? gate : q, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM, 4) ||
       !make_map(&to, p.out, p.B, p.Sq > 0 ? p.Sq : 1, p.Hq, kPM))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // the sigmoid table, once per device, on the same stream ahead of the first use
-    sigmoid_table_kernel<<<256, 256, 0, stream>>>();
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  e = prefill_init(dev, stream);
+  if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(((p.Sq + kPM - 1) / kPM) * p.Hq), (unsigned)p.B, 1u);
   prefill_kernel<<<grid, kPThreads, kSmemBytes, stream>>>(tq, tk, tv, tg, to, p);
   return cudaGetLastError();

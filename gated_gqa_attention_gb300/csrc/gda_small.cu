@@ -21,6 +21,7 @@
 // that CTA merges the C states (with the attention sink), divides by the sum, rounds
 // to BF16, applies the BF16 gate, and writes out and lse.  No partials go through HBM and no
 // second kernel runs.
+#include <atomic>
 #include "gda_device.cuh"
 #include "gda_small.h"
 
@@ -401,11 +402,12 @@ cudaError_t small_attr_c() {
 // cluster index 0, 1, 2, 3 for C = 8, 4, 2, 1
 int cidx_of(int C) { return C == 8 ? 0 : (C == 4 ? 1 : (C == 2 ? 2 : 3)); }
 
-bool g_small_attr[64][4] = {};
-int g_small_clusters[64][4] = {};
+// per device and cluster size (idempotent; atomics, as calls may come from any thread)
+std::atomic<bool> g_small_attr[64][4];
+std::atomic<int> g_small_clusters[64][4];
 
 cudaError_t small_attr(int dev, int C) {
-  bool& done = g_small_attr[dev][cidx_of(C)];
+  std::atomic<bool>& done = g_small_attr[dev][cidx_of(C)];
   if (!done) {
     const cudaError_t e = (C == 8)   ? small_attr_c<8>()
                           : (C == 4) ? small_attr_c<4>()
@@ -437,7 +439,7 @@ int small_max_clusters(int C) {
   if (C != 8 && C != 4 && C != 2 && C != 1) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  int& n = g_small_clusters[dev][cidx_of(C)];
+  std::atomic<int>& n = g_small_clusters[dev][cidx_of(C)];
   if (n == 0) {
     if (small_attr(dev, C) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg;

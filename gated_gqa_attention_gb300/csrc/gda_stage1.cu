@@ -36,6 +36,7 @@
 //  * At the end of a piece each warp writes its rescaled O into its (idle) ring
 //    and all threads add the 8 slices in a fixed order (deterministic); one
 //    partial is written per piece.
+#include <atomic>
 #include "gda_device.cuh"
 #include "gda_kernels.h"
 
@@ -787,7 +788,7 @@ template <int NWARP, int NV, bool PAIR>
 cudaError_t launch_mma(const Stage1Params& p, int grid, cudaStream_t stream) {
   using Smem = MmaSmem<NWARP, NV, PAIR ? 2 : 1>;
   auto kern = stage1_mma_kernel<NWARP, NV, PAIR>;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // zero-initialised: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -35,6 +35,7 @@
 //  * Merge: each warp writes its rescaled O^T fragments into its idle ring in
 //    fragment order (conflict-free float4 stores); all threads add the 8 warps'
 //    slices in a fixed order and write one partial per piece.
+#include <atomic>
 #include <cuda_fp16.h>
 
 #include "gda_device.cuh"
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_kernel(Stage1Params p)
 }  // namespace
 
 cudaError_t launch_stage1_fp8(const Stage1Params& p, int grid, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // zero-initialised: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -28,6 +28,7 @@
 //    and write one partial; stage 2 merges partials across pieces.
 //  * Every wait is bounded; a timeout (a kernel bug) sets an error bit and the CTA
 //    winds down along the same control flow, so nothing can hang.
+#include <atomic>
 #include "gda_device.cuh"
 #include "gda_kernels.h"
 
@@ -403,7 +404,7 @@ static cudaError_t launch_variant(const Stage1Params& p, int grid, cudaStream_t 
   auto kern = stage1_kernel<Math, NCW, WTOK, NSTAGE>;
   const size_t smem = sizeof(Smem);
   // the shared-memory opt-in is per device; set it once per device
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // zero-initialised: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -224,6 +224,9 @@ int gda_decode_e4m3(const gda_bf16* q, const gda_bf16* gate, const uint8_t* k_po
  * D = 256 only (GDA_ERR_UNSUPPORTED otherwise).  All tensors contiguous, device
  * pointers 16-byte aligned (4 for kv_lens / lse / error_word).  One kernel on `stream`,
  * no allocation, no read back; the tensor-map set-up runs on the host per call.
+ * The first call on a device also builds the library's 128 KiB BF16 sigmoid table
+ * and waits for it (on a stream of its own), so make it before any stream capture:
+ * made while `stream` is capturing, it returns GDA_ERR_CAPTURE and enqueues nothing.
  * A query row with no visible key gives O = 0 (out = 0) and lse = -inf. */
 int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, const gda_bf16* v,
                 const int32_t* kv_lens, gda_bf16* out, float* lse, int B, int Sq, int Skv, int Hq, int Hkv,

@@ -126,3 +126,46 @@ def test_prefill_gate_covers_every_bf16_code(gda):
     nan = np.isnan(w)
     assert np.array_equal(np.isnan(g), nan)
     assert np.array_equal(got[~nan], want[~nan])
+
+
+_FIRST_USE = r'''
+import numpy as np, torch
+import gated_gqa_attention_gb300 as gda
+torch.manual_seed(0)
+q = torch.randn(1, 256, 8, 256, device="cuda").to(torch.bfloat16)
+gate = (2 * torch.randn(1, 256, 8, 256, device="cuda")).to(torch.bfloat16)
+k = torch.randn(1, 256, 2, 256, device="cuda").to(torch.bfloat16)
+v = torch.randn(1, 256, 2, 256, device="cuda").to(torch.bfloat16)
+torch.cuda.synchronize()
+a, b = torch.cuda.Stream(), torch.cuda.Stream()
+outs = []
+for s in (a, b):      # the first two calls of the process, back to back on two streams
+    with torch.cuda.stream(s):
+        outs.append(gda.prefill(q, gate, k, v, scale=0.0625, causal=True))
+torch.cuda.synchronize()
+again = gda.prefill(q, gate, k, v, scale=0.0625, causal=True)
+g = torch.cuda.CUDAGraph()
+side = torch.cuda.Stream()
+side.wait_stream(torch.cuda.current_stream())
+with torch.cuda.stream(side):
+    with torch.cuda.graph(g):
+        captured = gda.prefill(q, gate, k, v, scale=0.0625, causal=True)
+g.replay()
+torch.cuda.synchronize()
+for o in outs + [captured]:
+    assert torch.equal(o.view(torch.int16), again.view(torch.int16))
+assert gda.prefill_read_error() == 0
+print("first-use ok")
+'''
+
+
+def test_first_use_on_two_streams_and_capture():
+    # The per-device sigmoid table is built and waited for on first use, so a second
+    # stream's first call cannot read it early; capture after first use replays the
+    # same bits.  A fresh process, so this really is the library's first prefill.
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_USE], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "first-use ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
