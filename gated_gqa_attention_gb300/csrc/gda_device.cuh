@@ -288,27 +288,35 @@ struct Sched {
   //    (lmax > 1.25 x the mean: S pieces of the longest sequence bound the call).
   static __device__ __forceinline__ int auto_uniform_splits(const int* indptr, int B, int Hkv, int grid,
                                                             int min_chunk) {
-    const long long units1 = (long long)B * Hkv;  // one piece per segment
-    if (units1 > grid) return 0;
+    if ((long long)B * Hkv > grid) return 0;
+    const int units1 = B * Hkv;  // one piece per segment; <= grid
     if (units1 == 0) return 1;
-    const long long n = __ldg(indptr + B);  // issued with the scan's loads: one round trip
-    int lmax = 0;
-    for (int b = (int)(threadIdx.x & 31); b < B; b += 32)
-      lmax = max(lmax, __ldg(indptr + b + 1) - __ldg(indptr + b));
+    // the longest length and the total from the same loads (kv_indptr[0] = 0): no
+    // further round trip, which every CTA's start and stage 2's prologue would wait on
+    int lmax = 0, n = 0;
+    for (int b = (int)(threadIdx.x & 31); b < B; b += 32) {
+      const int len = __ldg(indptr + b + 1) - __ldg(indptr + b);
+      lmax = max(lmax, len);
+      n += len;
+    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+    for (int off = 16; off > 0; off >>= 1) {
+      lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+      n += __shfl_xor_sync(0xffffffffu, n, off);
+    }
     if ((long long)Hkv * n >= (long long)kStreamMinPerCta * grid) return 0;
     if (4LL * lmax * B > 5LL * n) return 0;
-    int s_opt = 1;
-    while (16LL * s_opt * s_opt <= lmax) s_opt *= 2;
+    // (closed forms, short dependent chains: every CTA's start waits on this)
+    // s_opt: the smallest power of two p with 16 p^2 > lmax, 2^max(0, (h - 2) / 2)
+    // with h the index of lmax's top bit
+    const int s_opt = (lmax > 0) ? (1 << max(0, (31 - __clz(lmax) - 2) / 2)) : 1;
     const int s_len = max(1, (lmax + min_chunk - 1) / min_chunk);
     int s = min(s_opt, s_len);
-    const int s_wave = (int)(grid / units1);
+    const int s_wave = grid / units1;
     if (s >= s_wave) {
-      int p2 = 1;
-      while (2 * p2 <= s_wave) p2 *= 2;
-      s = (5LL * p2 * units1 >= 4LL * grid) ? p2 : s_wave;
-      if (5LL * s * units1 < 4LL * grid) return 0;
+      const int p2 = 1 << (31 - __clz(s_wave));  // the largest power of two <= s_wave
+      s = (5 * p2 * units1 >= 4 * grid) ? p2 : s_wave;
+      if (5 * s * units1 < 4 * grid) return 0;
     }
     return s;
   }
