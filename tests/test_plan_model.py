@@ -178,3 +178,42 @@ def test_paired_partials_fit_the_workspace():
                 for g in (0, 1):
                     want = sorted(p[4] * 2 + g for p in pieces if p[0] == b and p[1] == kvh)
                     assert [i * 2 + g for i in stage2_ids(indptr, Hkv, b, kvh, S, T)] == want
+
+
+def test_paired_kernel_tile_arithmetic():
+    # The paired stage-1 loop (G = 9 .. 16, 8 warps): warp w loads tiles w + 8k of a
+    # piece (16 positions each); warps w and w ^ 4 are partners; both run the step
+    # count of the pair's first warp (w & 3), and at step k warp w takes its own tile
+    # (when k < its tile count) and its partner's (when k < the partner's count) for
+    # its own group (w // 4).  Every tile is loaded once, every group sees every tile
+    # once, and the shared step count covers both partners' tiles.
+    NW = 8
+
+    def nmine(w, length):
+        ntiles = (length + 15) // 16
+        return (ntiles - w + NW - 1) // NW if ntiles > w else 0
+
+    def tile_n(w, k, length):
+        return min(16, length - 16 * (w + NW * k)) if k < nmine(w, length) else 0
+
+    for length in list(range(0, 700)) + [1023, 1024, 1025, 4096, 3449, 5000]:
+        ntiles = (length + 15) // 16
+        loaded = [0] * ntiles
+        seen = {0: [0] * ntiles, 1: [0] * ntiles}
+        positions = {0: 0, 1: 0}
+        for w in range(NW):
+            partner, grp = w ^ 4, w // 4
+            steps = nmine(w & 3, length)
+            assert steps >= nmine(w, length) and steps >= nmine(partner, length)
+            assert steps == nmine(partner & 3, length)  # both partners meet at every barrier
+            for k in range(nmine(w, length)):
+                loaded[w + NW * k] += 1
+            for k in range(steps):
+                for owner in (w, partner):
+                    n = tile_n(owner, k, length)
+                    if n > 0:
+                        seen[grp][owner + NW * k] += 1
+                        positions[grp] += n
+        assert loaded == [1] * ntiles
+        assert seen[0] == [1] * ntiles and seen[1] == [1] * ntiles
+        assert positions[0] == positions[1] == length
