@@ -217,3 +217,32 @@ def test_paired_kernel_tile_arithmetic():
         assert loaded == [1] * ntiles
         assert seen[0] == [1] * ntiles and seen[1] == [1] * ntiles
         assert positions[0] == positions[1] == length
+
+
+def test_cluster_kernel_partition_and_merge_slots():
+    # The one-kernel path: a cluster of C CTAs per (sequence, KV head).  CTA r takes
+    # positions [min(L, r c), min(L, r c + c)), c = ceil(L / C), and stores its state
+    # of query head h (h < G <= 8) in slot (h // C) * C + r of CTA h % C; CTA r'
+    # finalises heads r' + C k, reading slots k C + x for x < C.  Every state lands in
+    # a distinct slot of one of 8, and each finaliser reads exactly its head's C states.
+    for C in (1, 2, 4, 8):
+        for L in list(range(0, 300)) + [1023, 1024, 1025]:
+            c = (L + C - 1) // C
+            got = []
+            for r in range(C):
+                lo = min(L, r * c)
+                got.extend(range(lo, min(L, lo + c)))
+            assert got == list(range(L))
+        for G in range(1, 9):
+            slots = {}
+            for r in range(C):
+                for h in range(G):
+                    key = (h % C, (h // C) * C + r)
+                    assert key not in slots and key[1] < 8
+                    slots[key] = (h, r)
+            for rp in range(C):
+                k = 0
+                while rp + C * k < G:
+                    h = rp + C * k
+                    assert [slots[(rp, k * C + x)] for x in range(C)] == [(h, x) for x in range(C)]
+                    k += 1
