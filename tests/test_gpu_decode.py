@@ -38,19 +38,31 @@ def reference(inp, pairs=None):
                          inp["kv_indices"], inp["scale"], pairs=pairs)
 
 
+def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    # BF16 codes on one ordered integer line (sign-magnitude: +0 and -0 coincide)
+    def ordered(x):
+        x = np.asarray(x).astype(np.int64) & 0xFFFF
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
 def check_close(got_bits: np.ndarray, want_bits: np.ndarray, pairs=None):
     g = oracle.double_from_bf16(got_bits)
     w = oracle.double_from_bf16(want_bits)
+    gb, wb = np.asarray(got_bits), np.asarray(want_bits)
     if pairs is not None:
         idx = tuple(np.asarray(pairs).T)
-        g, w = g[idx], w[idx]
+        g, w, gb, wb = g[idx], w[idx], gb[idx], wb[idx]
     err = np.abs(g - w)
     lim = ATOL + RTOL * np.abs(w)
     bad = err > lim
     assert not bad.any(), "%d / %d elements out of tolerance; worst err %.3g at ref %.3g" % (
         bad.sum(), bad.size, err.max(), w.flat[np.argmax(err - lim)])
-    rms = math.sqrt(float(np.mean(w * w))) or 1.0
-    return dict(max_abs=float(err.max()) if err.size else 0.0, max_rel_rms=float(err.max() / rms) if err.size else 0.0)
+    rms = math.sqrt(float(np.mean(w * w))) if w.size else 1.0
+    rms = rms or 1.0
+    ulp = bf16_ulp_distance(gb, wb)
+    return dict(max_abs=float(err.max()) if err.size else 0.0, max_rel_rms=float(err.max() / rms) if err.size else 0.0,
+                max_ulp=int(ulp.max()) if ulp.size else 0)
 
 
 SMALL = [0, 1, 5, 63, 64, 65, 200, 1000, 777, 16, 129]
