@@ -813,6 +813,6 @@ const char* gda_status_str(int status) {
   }
 }
 
-int gda_version(void) { return 112; }
+int gda_version(void) { return 200; }  // 0.2.0: gda_args gained total_len
 
 }  // extern "C"
