@@ -10,8 +10,9 @@
  *   slot_j     = kv_indices[kv_indptr[b] + j],  0 <= j < kv_indptr[b+1]-kv_indptr[b]
  *
  * with G = Hq / Hkv consecutive query heads sharing one KV head (any G >= 1; the
- * kernels handle the query heads of a KV head in groups of up to 8, so for G > 8
- * the KV head's rows are read once per group).  Sources: FreeToken
+ * kernels handle the query heads of a KV head in groups of up to 8: for G = 9 .. 16
+ * the default kernel serves both groups from one read of the KV head's rows, and
+ * otherwise, or on the other kernels, the rows are read once per group).  Sources: FreeToken
  * PR #781 "Fuse the BF16 attention output sigmoid gate into the existing Triton
  * decode stage2" (Summary: split-KV stage 1, FP32 LSE merge in stage 2 with the
  * BF16 gate and an explicit round-to-nearest-even product fused into its epilogue;
@@ -59,7 +60,8 @@ typedef enum gda_status {
                                    an unknown variant): declined, never run slowly */
     GDA_ERR_SPLITS = -5,        /* num_splits > GDA_MAX_SPLITS */
     GDA_ERR_WORKSPACE = -6,     /* workspace NULL, misaligned or smaller than gda_workspace_bytes */
-    GDA_ERR_CAPTURE = -7,       /* the internal workspace must grow while `stream` is capturing */
+    GDA_ERR_CAPTURE = -7,       /* set-up needed while `stream` is capturing: the internal
+                                   workspace must grow, or gda_prefill's first use on a device */
     GDA_ERR_CUDA = -8,          /* a CUDA runtime call or launch failed */
     GDA_ERR_DEVICE = -9,        /* gda_read_error: a kernel flagged an error (see the bits below) */
     GDA_ERR_ARG = -10           /* a scalar argument outside its domain (a non-finite descale) */
