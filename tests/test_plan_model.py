@@ -246,3 +246,35 @@ def test_cluster_kernel_partition_and_merge_slots():
                     h = rp + C * k
                     assert [slots[(rp, k * C + x)] for x in range(C)] == [(h, x) for x in range(C)]
                     k += 1
+
+
+def test_device_closed_forms_equal_the_loops():
+    # The device evaluates the rule with closed forms (Sched::auto_uniform_splits):
+    # s_opt = 2^max(0, (h - 2) / 2) with h the index of lmax's top bit (C's truncating
+    # division), and the largest power of two <= s_wave from its top bit.  The host
+    # rule and this model use the loops; the two agree everywhere.
+    def s_opt_loop(lmax):
+        p = 1
+        while 16 * p * p <= lmax:
+            p *= 2
+        return p
+
+    def s_opt_closed(lmax):
+        if lmax <= 0:
+            return 1
+        h = lmax.bit_length() - 1
+        k = int((h - 2) / 2)          # truncation toward zero, as in C
+        return 1 << max(0, k)
+
+    def p2_loop(w):
+        p = 1
+        while 2 * p <= w:
+            p *= 2
+        return p
+
+    rng = random.Random(3)
+    cases = list(range(0, 1 << 15)) + [rng.randrange(0, 2 ** 31) for _ in range(20000)] + [2 ** 31 - 1]
+    for lmax in cases:
+        assert s_opt_closed(lmax) == s_opt_loop(lmax), lmax
+    for w in range(1, 4096):
+        assert (1 << (w.bit_length() - 1)) == p2_loop(w), w
