@@ -28,6 +28,9 @@ struct DeviceState {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   int sms = 0;
+  // Buffers the internal workspace outgrew.  They are never freed: a CUDA graph
+  // captured while one of them was current still reads and writes it on replay.
+  std::vector<void*> retired;
 };
 
 std::mutex g_mu;
@@ -280,7 +283,10 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   return GDA_OK;
 }
 
-// Make the internal workspace of the current device at least `need` bytes.
+// Make the internal workspace of the current device at least `need` bytes.  A
+// growth allocates a new buffer of at least twice the old size and keeps the old
+// one allocated until the process exits, so a graph captured on it stays valid;
+// the retired buffers then total less than the current one.
 int ensure_workspace(size_t need, cudaStream_t stream, bool check_capture, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDA_ERR_CUDA;
@@ -295,20 +301,17 @@ int ensure_workspace(size_t need, cudaStream_t stream, bool check_capture, void*
     if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) return GDA_ERR_CUDA;
     if (st != cudaStreamCaptureStatusNone) return GDA_ERR_CAPTURE;
   }
-  if (d.ws) {
-    if (cudaDeviceSynchronize() != cudaSuccess) return GDA_ERR_CUDA;
-    cudaFree(d.ws);
-    d.ws = nullptr;
-    d.ws_bytes = 0;
-  }
+  const size_t grown = round_up(need > 2 * d.ws_bytes ? need : 2 * d.ws_bytes, 256);
   void* p = nullptr;
-  if (cudaMalloc(&p, need) != cudaSuccess) return GDA_ERR_CUDA;
-  if (cudaMemset(p, 0, gda::kHeaderBytes) != cudaSuccess) {
+  if (cudaMalloc(&p, grown) != cudaSuccess) return GDA_ERR_CUDA;
+  // the header (error word) starts at zero before any stream can use the buffer
+  if (cudaMemset(p, 0, gda::kHeaderBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(p);
     return GDA_ERR_CUDA;
   }
+  if (d.ws) d.retired.push_back(d.ws);
   d.ws = p;
-  d.ws_bytes = need;
+  d.ws_bytes = grown;
   *out = p;
   return GDA_OK;
 }
@@ -662,6 +665,20 @@ int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, con
   a.total_len = nnz;  // kv_indptr[B] == nnz; max_len is read below
   int rc = validate_args(&a);
   if (rc != GDA_OK) return rc;
+  // kv_indptr is in host memory here (B + 1 values): check it before anything is
+  // enqueued, since the kernels would otherwise read kv_indices past the end of the
+  // block, and take the longest length as the dispatch's exact bound
+  {
+    const int32_t* hp = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(host_in) + off[2]);
+    if (hp[0] != 0 || (int64_t)hp[B] != nnz) return GDA_ERR_SHAPE;
+    long long lmax = 0;
+    for (int b = 0; b < B; ++b) {
+      const long long d = (long long)hp[b + 1] - (long long)hp[b];
+      if (d < 0) return GDA_ERR_SHAPE;
+      if (d > lmax) lmax = d;
+    }
+    a.max_len = (int)(lmax < 0x7FFFFFFF ? lmax : 0x7FFFFFFF);
+  }
   // mapped host memory: the device address of each pointer (page-locked host memory only)
   auto device_view = [](const void* h, void** d) -> int {
     cudaPointerAttributes pa;
@@ -694,20 +711,6 @@ int gda_decode_step_host(const void* host_in, void* dev_in, size_t in_bytes, con
   void* ws = nullptr;
   rc = ensure_workspace(gda_workspace_bytes(B, Hq, Hkv, D, num_splits), st, true, &ws);
   if (rc != GDA_OK) return rc;
-  // The longest sequence, read on the host from kv_indptr in host_in (B + 1 values),
-  // once every check above has passed: the dispatch's exact bound (none if kv_indptr
-  // is not monotone).
-  {
-    const int32_t* hp = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(host_in) + off[2]);
-    long long lmax = 0;
-    bool mono = true;
-    for (int b = 0; b < B && mono; ++b) {
-      const long long d = (long long)hp[b + 1] - (long long)hp[b];
-      mono = d >= 0;
-      if (d > lmax) lmax = d;
-    }
-    a.max_len = mono ? (int)(lmax < 0x7FFFFFFF ? lmax : 0x7FFFFFFF) : 0;
-  }
   if (!map_in && cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return GDA_ERR_CUDA;
   rc = enqueue(&a, ws, st);

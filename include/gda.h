@@ -184,8 +184,12 @@ int gda_workspace_init(void* workspace, size_t workspace_bytes, gda_stream_t str
  * merge and the BF16 gate epilogue), the second with programmatic dependent launch.
  * The internal workspace is one per device, shared by every stream: calls that may
  * overlap on different streams must use gda_decode_ex with separate workspaces.
- * It grows with cudaMalloc when needed; growth is refused with GDA_ERR_CAPTURE while
- * `stream` is capturing (call gda_reserve before capturing a graph). */
+ * It grows with cudaMalloc when needed (to at least twice its size, with a device
+ * synchronisation); growth is refused with GDA_ERR_CAPTURE while `stream` is
+ * capturing (call gda_reserve before capturing a graph).  A growth never frees the
+ * buffer it replaces: a graph captured earlier keeps reading and writing that buffer
+ * on replay, so it stays valid after later, larger calls.  Replaced buffers stay
+ * allocated until the process exits (together less than the current one). */
 int gda_decode(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k_pool,
                const gda_bf16* v_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
                gda_bf16* out, int B, int Hq, int Hkv, int D, float scale, int num_splits,
@@ -268,7 +272,8 @@ int gda_decode_noalloc(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* 
 
 /* Grow the internal workspace of the current device for calls up to these sizes,
  * so later gda_decode calls allocate nothing (FreeToken PR #781, Summary:
- * initialise before capture). */
+ * initialise before capture).  Like a growth inside gda_decode it keeps the buffer it
+ * replaces allocated, so graphs captured before it stay valid. */
 int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits);
 
 /* The cluster size (8, 4, 2 or 1 CTAs per (sequence, KV head)) that a decode with
@@ -318,11 +323,12 @@ size_t gda_step_layout(int B, int Hq, int D, int64_t nnz, size_t offsets[4]);
  * torch tensor) for the copies to be asynchronous; pageable memory works, but the
  * runtime then stages it through its own buffers.  dev_in is device memory,
  * 256-byte aligned, at least gda_step_layout(...) bytes; in_bytes must equal that
- * size.  As for gda_decode, every kv_indices entry must name a row of the pools, and
- * kv_indptr[B] must equal nnz (index contents are not checked on the host).  The
- * host reads the B + 1 kv_indptr values of host_in to pass the longest length and
- * nnz as gda_args.max_len and total_len (the one-kernel path or a host-chosen split
- * count where they apply).  The workspace is the library's, as for gda_decode (gda_reserve first
+ * size.  As for gda_decode, every kv_indices entry must name a row of the pools (index
+ * contents are not checked on the host).  The host reads the B + 1 kv_indptr values
+ * of host_in: kv_indptr[0] != 0, kv_indptr[B] != nnz or a decreasing pair returns
+ * GDA_ERR_SHAPE with nothing enqueued; otherwise the longest length and nnz go in as
+ * gda_args.max_len and total_len (the one-kernel path or a host-chosen split count
+ * where they apply).  The workspace is the library's, as for gda_decode (gda_reserve first
  * to keep the call allocation-free).  Returns the first failing step's status;
  * nothing after a failed step is enqueued.  Without synchronize the caller must not
  * touch host_in or read host_out before the stream has passed this call. */

@@ -280,6 +280,20 @@ def test_step_host_layout_and_validation(lib):
     assert call(kv=7) == ERR_UNSUPPORTED                  # an unknown cache type
     assert call(kv=1, kd=float("nan")) == ERR_ARG         # e4m3 with a non-finite descale
 
+    # kv_indptr is read from the host block before anything is enqueued: a first entry
+    # other than 0, a last entry other than nnz, or a decreasing pair is refused (the
+    # kernels would read kv_indices past the end of the block)
+    import numpy as np
+    raw = np.zeros(total + 256, dtype=np.uint8)
+    base = raw.ctypes.data
+    shift = (-base) % 256
+    block = raw[shift:shift + total]
+    ip = block[off[2]:off[2] + 4 * (B + 1)].view(np.int32)
+    for bad in ([1, 4, 7, 10], [0, 4, 7, 9], [0, 4, 7, 11], [0, 6, 4, 10], [0, -1, 4, 10]):
+        ip[:] = bad
+        assert call(host_in=base + shift) == ERR_SHAPE, bad
+    assert call(host_in=base + shift, nbytes=total - 256) == ERR_SHAPE
+
 
 def test_auto_splits_matches_the_plan_model(lib):
     # gda_auto_splits (host) restates the device rule; the CPU plan model restates
