@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+from canary import Guarded, check_all
 from gated_gqa_attention_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -79,9 +80,24 @@ def small_case():
 def test_small_ragged_parity(gda, small_case, variant, splits):
     inp, ref = small_case
     dev = to_cuda(inp)
-    out = run(gda, dev, num_splits=splits, variant=variant)
-    torch.cuda.synchronize()
-    check_close(bits(out), ref.out)
+    out, lse, ws = guarded_io(gda, dev, splits)
+    run(gda, dev, num_splits=splits, variant=variant, out=out.t, lse=lse.t, workspace=ws.t)
+    check_all(out=out, lse=lse, workspace=ws)
+    check_close(bits(out.t), ref.out)
+    got_lse, fin = lse.t.cpu().numpy().astype(np.float64), np.isfinite(ref.lse)
+    assert np.array_equal(np.isneginf(got_lse), np.isneginf(ref.lse))
+    np.testing.assert_allclose(got_lse[fin], ref.lse[fin], atol=2e-3, rtol=1e-4)
+
+
+def guarded_io(gda, dev, splits):
+    """out, lse and a workspace, each inside 0xFF guard bands (canary.Guarded)."""
+    B, Hq, D = dev["q"].shape
+    Hkv = dev["k_pool"].shape[1]
+    out = Guarded.like(dev["q"])
+    lse = Guarded((B, Hq), torch.float32)
+    ws = Guarded((max(gda.workspace_bytes(B, Hq, Hkv, D, splits), 256),), torch.uint8)
+    gda.workspace_init(ws.t)
+    return out, lse, ws
 
 
 @pytest.mark.parametrize("min_chunk", [1, 16, 64, 100, 1000])
@@ -290,6 +306,42 @@ def test_internal_workspace_refuses_growth_during_capture(gda):
     check_close(bits(out), reference(inp, pairs=pairs).out, pairs=pairs)
 
 
+def test_graph_stays_valid_after_internal_workspace_growth(gda):
+    # a graph captured on the internal workspace keeps that buffer: growing the
+    # workspace later (gda_reserve, or a larger eager gda_decode) must not free it,
+    # so the replay still gives the oracle's result
+    inp = workloads.make([100, 260, 7], seed=24, layout="perm", pool_slots=600)
+    dev = to_cuda(inp)
+    gda.reserve(3, 16, 2, 256, 8)
+    out = torch.empty_like(dev["q"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gda.decode(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
+                   out=out, scale=dev["scale"], num_splits=8)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gda.decode(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
+                   out=out, scale=dev["scale"], num_splits=8)
+    # growth past anything this process used: 512 sequences x 2 KV heads x 256 splits
+    # (2 GiB of partials); the drop in free memory shows that a new buffer came
+    free0 = torch.cuda.mem_get_info()[0]
+    gda.reserve(512, 16, 2, 256, 256)
+    assert free0 - torch.cuda.mem_get_info()[0] >= gda.workspace_bytes(512, 16, 2, 256, 256) // 2
+    big = workloads.make([33] * 40, seed=25, layout="perm", pool_slots=2000)
+    dbig = to_cuda(big)
+    out_big = gda.decode(dbig["q"], dbig["gate"], dbig["k_pool"], dbig["v_pool"], dbig["kv_indptr"],
+                         dbig["kv_indices"], scale=dbig["scale"], num_splits=200)
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    check_close(bits(out), reference(inp).out)
+    check_close(bits(out_big), reference(big).out)
+    assert gda.read_error() == 0
+
+
 # ------------------------------------------------------------------ the named workloads, full size
 
 _cache = {}
@@ -311,10 +363,11 @@ def workload_case(key):
 ])
 def test_workload_parity(gda, key, splits):
     inp, ref, dev = workload_case(key)
-    out = run(gda, dev, num_splits=splits)
-    torch.cuda.synchronize()
-    stats = check_close(bits(out), ref.out)
-    assert gda.read_error() == 0
+    out, lse, ws = guarded_io(gda, dev, splits)
+    run(gda, dev, num_splits=splits, out=out.t, lse=lse.t, workspace=ws.t)
+    check_all(out=out, lse=lse, workspace=ws)
+    stats = check_close(bits(out.t), ref.out)
+    assert gda.read_error(ws.t) == 0
     print(key, splits, stats)
 
 

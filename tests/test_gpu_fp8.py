@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+from canary import Guarded, check_all
 from gated_gqa_attention_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -220,6 +221,14 @@ def workload_case(key):
     ("b8_l131072", 0, 0), ("b8_l131072", 64, 1),
 ])
 def test_workload_parity(gda, key, splits, form):
+    # out, lse and the workspace inside 0xFF guard bands (canary.Guarded)
     inp, ref, dev = workload_case(key)
-    worst = check_close(run(gda, dev, num_splits=splits, variant=form), ref.out)
+    B, Hq, D = inp["q"].shape
+    out, lse = Guarded.like(dev["q"]), Guarded((B, Hq), torch.float32)
+    ws = Guarded((gda.workspace_bytes(B, Hq, inp["k_pool"].shape[1], D, splits),), torch.uint8)
+    gda.workspace_init(ws.t)
+    got = run(gda, dev, num_splits=splits, variant=form, out=out.t, lse=lse.t, workspace=ws.t)
+    check_all(out=out, lse=lse, workspace=ws)
+    worst = check_close(got, ref.out)
+    assert gda.read_error(ws.t) == 0
     print(key, splits, form, worst)

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+from canary import Guarded, check_all
 from gated_gqa_attention_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -35,9 +36,9 @@ def to_cuda(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def run(gda, d, gate=True, lse=None):
+def run(gda, d, gate=True, lse=None, out=None):
     out = gda.prefill(d["q"], d["gate"] if gate else None, d["k"], d["v"], kv_lens=d["kv_lens"], lse=lse,
-                      scale=d["scale"], causal=d["causal"])
+                      out=out, scale=d["scale"], causal=d["causal"])
     torch.cuda.synchronize()
     return bits(out)
 
@@ -65,9 +66,11 @@ def test_prefill_parity(gda, B, Sq, Skv, Hq, Hkv, causal, kv_lens):
     inp = workloads.make_prefill(B, Sq, Skv, seed=500 + Sq + Skv, hq=Hq, hkv=Hkv, causal=causal, kv_lens=kv_lens)
     dev = to_cuda(inp)
     ref = reference(inp)
-    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
-    check_close(run(gda, dev, lse=lse), ref.out)
-    got_lse = lse.cpu().numpy()
+    # out and lse inside 0xFF guard bands (canary.Guarded)
+    out, lse = Guarded.like(dev["q"]), Guarded((B, Hq, Sq), torch.float32, fill=float("nan"))
+    check_close(run(gda, dev, lse=lse.t, out=out.t), ref.out)
+    check_all(out=out, lse=lse)
+    got_lse = lse.t.cpu().numpy()
     live = np.isfinite(ref.lse)
     np.testing.assert_allclose(got_lse[live], ref.lse[live], atol=2e-3, rtol=1e-4)
     assert np.all(np.isneginf(got_lse[~live]))
@@ -99,15 +102,27 @@ def test_prefill_scores_that_move_the_max(gda):
 
 @pytest.mark.parametrize("key", ["p1_s512_causal", "p1_s4096_causal", "p1_s4096_dense", "p4_extend_q1024_kv8192"])
 def test_prefill_workload_sampled(gda, key):
+    # one random query row from every (128-query block, head, sequence) tile -- each a
+    # CTA of the kernel -- plus random rows and the corners; out and lse inside guard bands
     inp = workloads.make_prefill_workload(key)
     dev = to_cuda(inp)
-    out = run(gda, dev)
     B, Sq, Hq = inp["q"].shape[:3]
+    out, lse = Guarded.like(dev["q"]), Guarded((B, Hq, Sq), torch.float32)
+    got = run(gda, dev, lse=lse.t, out=out.t)
+    check_all(out=out, lse=lse)
     rng = np.random.default_rng(3)
-    rows = np.stack([rng.integers(0, B, 48), rng.integers(0, Sq, 48), rng.integers(0, Hq, 48)], axis=1)
-    rows = np.concatenate([rows, [[0, 0, 0], [B - 1, Sq - 1, Hq - 1], [0, Sq - 1, 0]]]).astype(np.int32)
+    nblk = (Sq + 127) // 128
+    bb, qb, hh = np.meshgrid(np.arange(B), np.arange(nblk), np.arange(Hq), indexing="ij")
+    bb, qb, hh = bb.ravel(), qb.ravel(), hh.ravel()
+    ii = np.minimum(qb * 128 + rng.integers(0, 128, bb.size), Sq - 1)
+    per_tile = np.stack([bb, ii, hh], axis=1)
+    rnd = np.stack([rng.integers(0, B, 48), rng.integers(0, Sq, 48), rng.integers(0, Hq, 48)], axis=1)
+    rows = np.concatenate([per_tile, rnd, [[0, 0, 0], [B - 1, Sq - 1, Hq - 1], [0, Sq - 1, 0]]]).astype(np.int32)
     ref = reference(inp, rows=rows)
-    check_close(out, ref.out, rows=rows)
+    check_close(got, ref.out, rows=rows)
+    idx = (rows[:, 0], rows[:, 2], rows[:, 1])
+    got_lse = lse.t.cpu().numpy()[idx]
+    np.testing.assert_allclose(got_lse, ref.lse[idx], atol=2e-3, rtol=1e-4)
     assert gda.prefill_read_error() == 0
 
 

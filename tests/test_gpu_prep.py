@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import oracle
+from canary import Guarded, check_all
 from gated_gqa_attention_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -53,12 +54,15 @@ def test_prep_matches_oracle(gda, B, Hq, Hkv, rope_dim, norm):
     qgkv, wq, wk, cos, sin, slots, kp, vp = make(B, Hq, Hkv, rope_dim, seed=B + Hq + rope_dim)
     ref_q, ref_g, ref_kp, ref_vp = oracle.qk_norm_rope_kv_write(
         qgkv, wq if norm else None, wk if norm else None, 1e-6, cos, sin, rope_dim, slots, kp, vp, Hq, Hkv, D)
-    dk, dv = kp.cuda(), vp.cuda()
+    # every buffer the kernel writes sits inside 0xFF guard bands (canary.Guarded)
+    gk, gv = Guarded.copy_of(kp.cuda()), Guarded.copy_of(vp.cuda())
+    gq, gg = Guarded((B, Hq, D), torch.bfloat16), Guarded((B, Hq, D), torch.bfloat16)
+    dk, dv = gk.t, gv.t
     q_out, g_out = gda.qk_norm_rope_kv_write(
         qgkv.cuda(), slots.cuda(), dk, dv, Hq, w_q_norm=wq.cuda() if norm else None,
         w_k_norm=wk.cuda() if norm else None, eps=1e-6, cos=cos.cuda() if rope_dim else None,
-        sin=sin.cuda() if rope_dim else None, rope_dim=rope_dim)
-    torch.cuda.synchronize()
+        sin=sin.cuda() if rope_dim else None, rope_dim=rope_dim, q_out=gq.t, gate_out=gg.t)
+    check_all(k_pool=gk, v_pool=gv, q_out=gq, gate_out=gg)
     got_q, got_k, got_v = bits(q_out), bits(dk), bits(dv)
     assert np.array_equal(bits(g_out), ref_g)                 # gate copied
     assert np.array_equal(got_v, ref_vp)                       # V written, rest untouched

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+from canary import Guarded, check_all
 from gated_gqa_attention_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -100,10 +101,12 @@ def test_sinks_lse_and_empty_rows(gda, batch):
     sinks[3] = -np.inf                     # a head without a sink
     sinks[7] = 40.0                        # a sink that dominates the softmax
     ref = reference(inp, sinks=sinks.astype(np.float64))
-    lse = torch.empty(len(LENS), 16, dtype=torch.float32, device="cuda")
-    got = run(gda, inp, 1024, sinks=sinks, lse=lse)
+    # out and lse inside 0xFF guard bands (canary.Guarded)
+    out, lse = Guarded((len(LENS), 16, 256), torch.bfloat16), Guarded((len(LENS), 16), torch.float32)
+    got = run(gda, inp, 1024, sinks=sinks, lse=lse.t, out=out.t)
+    check_all(out=out, lse=lse)
     check_close(got, ref.out)
-    np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
+    np.testing.assert_allclose(lse.t.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
     assert np.all(got[0] == 0)             # L = 0: O = 0 whatever the sink
 
 
@@ -131,7 +134,11 @@ def test_gqa_group_sizes(gda, hq, hkv):
 @pytest.mark.parametrize("key", ["b1_l512", "b4_ragged"])
 def test_page_workloads(gda, key):
     inp = workloads.make_workload(key)
-    check_close(run(gda, inp, int(max(inp["lengths"]))), reference(inp).out)
+    B = inp["q"].shape[0]
+    out, lse = Guarded((B, 16, 256), torch.bfloat16), Guarded((B, 16), torch.float32)
+    got = run(gda, inp, int(max(inp["lengths"])), out=out.t, lse=lse.t)
+    check_all(out=out, lse=lse)
+    check_close(got, reference(inp).out)
 
 
 def test_step_host_takes_the_cluster_path(gda):
