@@ -71,10 +71,16 @@ def parse_args(argv=None):
     p.add_argument("--sinks", type=float, default=None, help="give every query head this sink logit")
     p.add_argument("--kv", choices=["bf16", "e4m3"], default="bf16",
                    help="KV-cache element type: bf16, or e4m3 codes with per-tensor descales (FP8 cache)")
-    p.add_argument("--op", choices=["decode", "prep", "prefill"], default="decode",
+    p.add_argument("--op", choices=["decode", "prep", "prefill", "splits", "splits-cross", "paths"],
+                   default="decode",
                    help="decode: the gated decode attention call (default); prep: the step before it "
                         "(Q/K RMSNorm + partial RoPE + KV write) on the workload's batch; prefill: the "
-                        "prefill / extend gated SDPA (--workload p1_s4096_causal by default)")
+                        "prefill / extend gated SDPA (--workload p1_s4096_causal by default); splits / "
+                        "splits-cross / paths: the sweeps behind the split rule and the one-kernel "
+                        "dispatch (tables, not a bench line)")
+    p.add_argument("--sweep-out", default=None, help="--op splits: also write the table as JSON here")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the per-workload speeds of the other decode workloads (default run only)")
     p.add_argument("--kernel-only", action="store_true",
                    help="warm-up + K calls and exit (the command profiled under ncu); prints nothing")
     return p.parse_args(argv)
@@ -463,6 +469,12 @@ def run_ours(args):
     e2e_total = sum_over_ranks(dist, float(nbytes) * k_e2e, torch.device("cuda", dev_id))
     e2e_value = e2e_total / e2e_s / 1e9
 
+    # ---- the other workloads' speeds (the default bf16 run on one GPU only)
+    configs = None
+    if (world == 1 and args.kv == "bf16" and args.workload == "b64_l4096" and not (args.hq or args.hkv)
+            and args.window == 0 and args.sinks is None and not args.no_configs):
+        configs = config_speeds(measured_hbm_peak()[0])
+
     line = None
     if rank == 0:
         cpu = None
@@ -505,6 +517,7 @@ def run_ours(args):
             "gpu_launches": (1 if small_path else 2) * steps,
             "timing_pages_method": pages_method,
             "cold": cold,
+            "configs": configs,
             "clocks": clocks,
             "device_error_word": err,
             "gpu": torch.cuda.get_device_name(dev_id),
@@ -512,6 +525,99 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+# ------------------------------------------------------------------ the other workloads
+
+# (workload, KV type, num_splits, what the call is) timed beside the headline
+CONFIG_LINES = [
+    ("b1_l512", "bf16", 8, "S = 8 as the workload names it (split path, two kernels)"),
+    ("b1_l512", "bf16", 0, "automatic with the host-known bound (dispatch)"),
+    ("b4_ragged", "bf16", 0, "automatic with the host-known bound (dispatch)"),
+    ("b224_ragged", "bf16", 0, "automatic with the host-known bound and total (dispatch)"),
+    ("b8_l131072", "bf16", 0, "automatic with the host-known bound and total (dispatch)"),
+    ("b64_l4096", "e4m3", 0, "FP8 (e4m3) KV cache, automatic with the host-known bound and total"),
+]
+
+
+def time_graph_us(call, stream, samples=7, target_s=0.02):
+    """Median microseconds per call of `call` replayed from a CUDA graph of 4 calls:
+    the pages' warm method (kernel window, no host work), with the replays per
+    sample sized so one sample lasts about target_s."""
+    import torch
+    R = 4
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            for _ in range(R):
+                call()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    reps = max(5, min(2000, int(target_s / max(t0.elapsed_time(t1) / 1e3, 1e-6))))
+    per = []
+    for _ in range(samples):
+        t0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        per.append(t0.elapsed_time(t1) * 1e3 / (reps * R))
+    per.sort()
+    return per[len(per) // 2], reps * R
+
+
+def config_speeds(peak):
+    """µs per call and GB/s of every workload other than the headline one, each through
+    its default call: the inputs' lengths, layout and peaky rows as the parity tests
+    draw them, their values drawn on the device (workloads.make, values_device)."""
+    import torch
+    import gated_gqa_attention_gb300 as gda
+    from gated_gqa_attention_gb300 import workloads
+    stream = torch.cuda.current_stream()
+    lines = []
+    for key, kv, splits, what in CONFIG_LINES:
+        d = workloads.make_workload(key, kv=kv, values_device="cuda")
+        dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        lengths = d["lengths"]
+        B, Hq, D = dev["q"].shape
+        Hkv = dev["k_pool"].shape[1]
+        kvb = dev["k_pool"].element_size()
+        max_len, total_len = (max(lengths), sum(lengths)) if splits <= 0 else (0, 0)
+        small_c = gda.small_path_cluster(B * Hkv, max_len) if splits <= 0 and Hq // Hkv <= 8 else 0
+        out = torch.empty_like(dev["q"])
+        ws = torch.empty(gda.workspace_bytes(B, Hq, Hkv, D, splits), dtype=torch.uint8, device="cuda")
+        gda.workspace_init(ws)
+
+        def call():
+            gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], dev["kv_indices"],
+                          out=out, workspace=ws, scale=d["scale"], num_splits=splits, k_descale=d["k_descale"],
+                          v_descale=d["v_descale"], max_len=max_len, total_len=total_len)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        us, n = time_graph_us(call, stream)
+        nbytes = algorithmic_bytes(lengths, Hq, Hkv, D, kvb)
+        gbs = nbytes / (us / 1e6) / 1e9
+        err = gda.read_error(ws)
+        lines.append({"workload": key, "kv": kv, "num_splits": splits or "auto", "call": what,
+                      "path": ("one kernel, clusters of %d CTAs" % small_c if small_c else "split path (2 kernels)"),
+                      "B": B, "lengths": "%d..%d (total %d)" % (min(lengths), max(lengths), sum(lengths)),
+                      "us_per_call": round(us, 3), "GBs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                      "bytes_per_call": nbytes, "calls_timed": n, "device_error_word": err})
+        del dev, out, ws, d
+        torch.cuda.empty_cache()
+    return {"method": "CUDA graph of 4 calls, median of 7 samples (the pages' warm method)",
+            "values": "drawn on the device (same recipe, layout and lengths as the parity tests)", "lines": lines}
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -760,8 +866,168 @@ def run_prefill(args):
             "cpu_baseline": cpu, "clocks": clocks, "device_error_word": err, "gpu_launches": steps}
 
 
+# ------------------------------------------------------------------ sweeps behind the dispatch rules
+
+def _per_call_us(f, calls=200):
+    """Microseconds per call of f replayed from a CUDA graph of 4 calls."""
+    import torch
+    for _ in range(5):
+        f()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph):
+            for _ in range(4):
+                f()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(calls // 4):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / calls * 1e3
+
+
+def _sweep_batch(B, L, seed, hq=16, hkv=2, d=256):
+    """Equal-length batch made on the device (timing only): N(0, 1) q, gate and K/V
+    rows, slots a random permutation of the pool."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    n = B * L
+    slots = n + 64
+    mk = lambda *sh: torch.randn(*sh, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q, gate = mk(B, hq, d), mk(B, hq, d)
+    k_pool, v_pool = mk(slots, hkv, d), mk(slots, hkv, d)
+    indptr = (torch.arange(B + 1, device="cuda", dtype=torch.int64) * L).to(torch.int32)
+    indices = torch.randperm(slots, generator=g, device="cuda")[:n].to(torch.int32)
+    return q, gate, k_pool, v_pool, indptr, indices
+
+
+SWEEP_SPLITS = (1, 2, 4, 8, 16, 32, 64, 128)
+
+
+def run_split_sweep(args):
+    """The split-count sweep ("chosen per (B, length) from measured time", FreeToken PR
+    #781): for B equal-length sequences, B in {1 .. 128} and L in {512 .. 32768} (B L <=
+    2^21), the µs per call with every explicit split count S in 1 .. 128, with the
+    automatic schedule planned on the device (no length bound), and with the full
+    dispatch (the longest length and the total passed: the one-kernel path where it
+    applies, else the rule on the host).  Prints a table; --sweep-out writes JSON."""
+    import torch
+    import gated_gqa_attention_gb300 as gda
+    torch.cuda.set_device(0)
+    gda.load()
+    HQ, HKV, D = 16, 2, 256
+    rows = []
+    print("%4s %6s | %s | %9s %9s %6s | %9s" % ("B", "L", " ".join("%8s" % ("S=%d" % s) for s in SWEEP_SPLITS),
+                                                "best S", "auto", "a/best", "dispatch"))
+    for B in (1, 2, 4, 8, 16, 32, 64, 128):
+        for L in (512, 2048, 8192, 32768):
+            if B * L > (1 << 21):
+                continue
+            q, gate, kp, vp, indptr, idx = _sweep_batch(B, L, seed=1000 + B + L)
+            out = torch.empty_like(q)
+            t = {}
+            for S in SWEEP_SPLITS + (0,):
+                ws = torch.empty(gda.workspace_bytes(B, HQ, HKV, D, S), dtype=torch.uint8, device="cuda")
+                gda.workspace_init(ws)
+                t[S] = _per_call_us(lambda: gda.decode_ex(q, gate, kp, vp, indptr, idx, out=out, workspace=ws,
+                                                          scale=D ** -0.5, num_splits=S), calls=100)
+            ws = torch.empty(gda.workspace_bytes(B, HQ, HKV, D, 0), dtype=torch.uint8, device="cuda")
+            gda.workspace_init(ws)
+            disp = _per_call_us(lambda: gda.decode_ex(q, gate, kp, vp, indptr, idx, out=out, workspace=ws,
+                                                      scale=D ** -0.5, max_len=L, total_len=B * L), calls=100)
+            best = min(SWEEP_SPLITS, key=lambda s: t[s])
+            rows.append({"B": B, "L": L, "us_by_splits": {str(s): round(t[s], 3) for s in SWEEP_SPLITS},
+                         "best_splits": best, "best_us": round(t[best], 3), "auto_us": round(t[0], 3),
+                         "dispatch_us": round(disp, 3), "cluster": gda.small_path_cluster(B * HKV, L)})
+            print("%4d %6d | %s | %4d %4.1f %9.2f %6.3f | %9.2f" % (
+                B, L, " ".join("%8.2f" % t[s] for s in SWEEP_SPLITS), best, t[best], t[0], t[0] / t[best], disp),
+                flush=True)
+            del q, gate, kp, vp, indptr, idx, out, ws
+            torch.cuda.empty_cache()
+    if args.sweep_out:
+        with open(args.sweep_out, "w") as f:
+            json.dump(rows, f, indent=1)
+
+
+# (B, L, S): S the one-wave uniform count near the rule's bounds
+SPLIT_CROSS = [(64, 3072, 1), (64, 4096, 1), (64, 5120, 1), (64, 6144, 1), (32, 6144, 2), (32, 8192, 2),
+               (32, 10240, 2), (16, 12288, 4), (16, 16384, 4), (16, 20480, 4), (8, 2048, 8), (8, 2048, 9),
+               (8, 32768, 8), (8, 32768, 9), (4, 2048, 16), (4, 2048, 19), (4, 32768, 16), (4, 32768, 19),
+               (2, 32768, 32), (2, 32768, 38), (1, 32768, 64), (1, 32768, 76), (48, 4096, 1), (48, 8192, 1),
+               (24, 8192, 3), (24, 8192, 2)]
+
+
+def run_split_cross(args):
+    """Explicit uniform splits against the automatic schedule around the rule's bounds
+    (positions per CTA near 3072; the power of two below the wave bound against the
+    bound itself; waves that leave CTAs idle)."""
+    import torch
+    import gated_gqa_attention_gb300 as gda
+    torch.cuda.set_device(0)
+    gda.load()
+    HQ, HKV, D = 16, 2, 256
+    for B, L, S in SPLIT_CROSS:
+        q, gate, kp, vp, indptr, idx = _sweep_batch(B, L, seed=5)
+        out = torch.empty_like(q)
+        t = {}
+        for s in (0, S):
+            ws = torch.empty(gda.workspace_bytes(B, HQ, HKV, D, s), dtype=torch.uint8, device="cuda")
+            gda.workspace_init(ws)
+            t[s] = _per_call_us(lambda: gda.decode_ex(q, gate, kp, vp, indptr, idx, out=out, workspace=ws,
+                                                      scale=D ** -0.5, num_splits=s), calls=200)
+        print("B %3d L %6d per-CTA %6d | auto %8.2f | S=%3d %8.2f | S/auto %.3f" % (
+            B, L, (HKV * B * L + 151) // 152, t[0], S, t[S], t[S] / t[0]), flush=True)
+        del q, gate, kp, vp, indptr, idx, out, ws
+        torch.cuda.empty_cache()
+
+
+def run_paths(args):
+    """The decode's one-kernel cluster path against the split path: B in {1 .. 64} and
+    equal lengths L in {128 .. 2048}, the µs per call with the length bound (the
+    one-kernel path where the library takes it), without it (split path, split count
+    planned on the device), and on the split path with the bound and the total (split
+    count from the host rule); the cluster size the library chose beside them."""
+    import torch
+    import gated_gqa_attention_gb300 as gda
+    from gated_gqa_attention_gb300 import workloads
+    torch.cuda.set_device(0)
+    gda.load()
+    print("%3s %5s %9s %12s %10s %13s %6s" % ("B", "L", "cluster C", "one-kernel", "split", "split (host)",
+                                               "ratio"))
+    for B in (1, 4, 8, 12, 16, 24, 32, 48, 64):
+        for L in (128, 256, 512, 1024, 2048):
+            inp = workloads.make([L] * B, seed=7, layout="perm", pool_slots=max(4096, B * L + 100))
+            d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+            out = torch.empty_like(d["q"])
+            _, Hq, D = d["q"].shape
+            Hkv = d["k_pool"].shape[1]
+            ws = torch.empty(gda.workspace_bytes(B, Hq, Hkv, D, 0), dtype=torch.uint8, device="cuda")
+            gda.workspace_init(ws)
+            t = {}
+            for ml in (L, 0):
+                t[ml] = _per_call_us(lambda: gda.decode_ex(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["kv_indptr"],
+                                                           d["kv_indices"], out=out, workspace=ws, scale=inp["scale"],
+                                                           max_len=ml))
+            th = _per_call_us(lambda: gda.decode_ex(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["kv_indptr"],
+                                                    d["kv_indices"], out=out, workspace=ws, scale=inp["scale"],
+                                                    max_len=L, total_len=B * L, variant=gda.VARIANT_MMA))
+            print("%3d %5d %9d %9.2f us %7.2f us %10.2f us %6.2f" % (B, L, gda.small_path_cluster(B * Hkv, L), t[L],
+                                                                    t[0], th, t[L] / min(t[0], th)), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.op in ("splits", "splits-cross", "paths"):
+        {"splits": run_split_sweep, "splits-cross": run_split_cross, "paths": run_paths}[args.op](args)
+        return
     if args.op in ("prep", "prefill"):
         line = run_prep(args) if args.op == "prep" else run_prefill(args)
         print(json.dumps(line), flush=True)

@@ -82,15 +82,18 @@ def workload(key) -> Workload:
 
 def _randn_bf16(gen: torch.Generator, rows: int, cols: int, std: float,
                 row_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """[rows, cols] BF16 of N(0, std^2) values, drawn in float32 chunks.
+    """[rows, cols] BF16 of N(0, std^2) values, drawn in float32 chunks on the
+    generator's device.
 
     ``row_scale`` (float32 [rows]) multiplies rows in float32 before the
     rounding to BF16."""
-    out = torch.empty(rows, cols, dtype=torch.bfloat16)
+    out = torch.empty(rows, cols, dtype=torch.bfloat16, device=gen.device)
+    if row_scale is not None:
+        row_scale = row_scale.to(gen.device)
     chunk = max(1, (1 << 24) // max(cols, 1))
     for r0 in range(0, rows, chunk):
         r1 = min(rows, r0 + chunk)
-        x = torch.randn(r1 - r0, cols, generator=gen, dtype=torch.float32)
+        x = torch.randn(r1 - r0, cols, generator=gen, dtype=torch.float32, device=gen.device)
         if std != 1.0:
             x.mul_(std)
         if row_scale is not None:
@@ -103,11 +106,13 @@ def _randn_e4m3(gen: torch.Generator, rows: int, cols: int, std: float, descale:
                 row_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
     """[rows, cols] float8_e4m3fn codes of the same float32 draws as _randn_bf16,
     divided by ``descale`` and saturated at +-448."""
-    out = torch.empty(rows, cols, dtype=torch.float8_e4m3fn)
+    out = torch.empty(rows, cols, dtype=torch.float8_e4m3fn, device=gen.device)
+    if row_scale is not None:
+        row_scale = row_scale.to(gen.device)
     chunk = max(1, (1 << 24) // max(cols, 1))
     for r0 in range(0, rows, chunk):
         r1 = min(rows, r0 + chunk)
-        x = torch.randn(r1 - r0, cols, generator=gen, dtype=torch.float32)
+        x = torch.randn(r1 - r0, cols, generator=gen, dtype=torch.float32, device=gen.device)
         if std != 1.0:
             x.mul_(std)
         if row_scale is not None:
@@ -151,14 +156,18 @@ def make(lengths: Sequence[int], *, seed: int, hq: int = HQ, hkv: int = HKV,
          head_dim: int = HEAD_DIM, layout: str = "perm", pool_slots: Optional[int] = None,
          page: int = 1, gate_std: float = 2.0, qkv_std: float = 1.0, peaky_frac: float = 0.0,
          peaky_scale: float = 3.0, scale: float = DEFAULT_SCALE, random_lengths=None,
-         kv: str = "bf16") -> dict:
+         kv: str = "bf16", values_device: Optional[str] = None) -> dict:
     """Build one decode batch on the CPU.
 
     Returns a dict of CPU tensors ``q, gate`` [B, Hq, D] bf16, ``k_pool, v_pool``
     [slots, Hkv, D] bf16 (float8_e4m3fn with ``kv="e4m3"``), ``kv_indptr`` [B+1]
     int32, ``kv_indices`` [nnz] int32, plus ``scale``, ``lengths``, ``num_slots``
     and the pools' ``k_descale`` / ``v_descale`` (1.0 for BF16 pools).
-    ``random_lengths=(lo, hi, B)`` draws the lengths uniformly from [lo, hi] first."""
+    ``random_lengths=(lo, hi, B)`` draws the lengths uniformly from [lo, hi] first.
+    ``values_device="cuda"``: the lengths, layout and peaky-row mask are drawn as
+    above, but q, gate and the pools from a CUDA generator seeded with ``seed`` and
+    left on the device (the same distributions, other values; seconds instead of a
+    minute for the largest pools, for timing runs)."""
     if kv not in ("bf16", "e4m3"):
         raise ValueError(kv)
     gen = torch.Generator().manual_seed(seed)
@@ -173,6 +182,8 @@ def make(lengths: Sequence[int], *, seed: int, hq: int = HQ, hkv: int = HKV,
         picked = torch.rand(idx.numel(), generator=gen) < peaky_frac
         row_scale = torch.ones(slots, dtype=torch.float32)
         row_scale[idx[picked].long()] = peaky_scale
+    if values_device is not None:
+        gen = torch.Generator(device=values_device).manual_seed(seed)
     q = _randn_bf16(gen, B * hq, head_dim, qkv_std).view(B, hq, head_dim)
     g = _randn_bf16(gen, B * hq, head_dim, gate_std).view(B, hq, head_dim)
     k_scale = None
@@ -196,16 +207,19 @@ def make(lengths: Sequence[int], *, seed: int, hq: int = HQ, hkv: int = HKV,
                 v_descale=v_descale, kv=kv)
 
 
-def make_workload(key, batch_limit: Optional[int] = None, seed: Optional[int] = None, kv: str = "bf16") -> dict:
+def make_workload(key, batch_limit: Optional[int] = None, seed: Optional[int] = None, kv: str = "bf16",
+                  values_device: Optional[str] = None) -> dict:
     """Inputs of one of the five named workloads (``batch_limit`` keeps the
     first sequences only, for bounded CPU timing; the draw is unchanged;
     ``seed`` replaces the workload's seed, e.g. for independent replicas;
-    ``kv="e4m3"`` gives the same workload over an FP8 KV cache)."""
+    ``kv="e4m3"`` gives the same workload over an FP8 KV cache;
+    ``values_device`` as in make())."""
     w = workload(key)
     rl = (w.len_lo, w.len_hi, w.batch) if w.lengths is None else None
     d = make(w.lengths if w.lengths is not None else [], seed=w.seed if seed is None else seed, hq=w.hq, hkv=w.hkv,
              head_dim=w.head_dim, layout=w.layout, pool_slots=w.pool_slots, page=w.page,
-             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl, kv=kv)
+             gate_std=w.gate_std, peaky_frac=w.peaky_frac, scale=w.scale, random_lengths=rl, kv=kv,
+             values_device=values_device)
     d["workload"] = w
     d["num_splits"] = w.num_splits
     if batch_limit is not None and batch_limit < len(d["lengths"]):
