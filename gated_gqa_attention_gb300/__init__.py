@@ -26,7 +26,7 @@ from typing import Optional
 
 __all__ = [
     "load", "decode", "decode_ex", "decode_noalloc", "decode_step_host", "StepHost", "step_layout", "small_path_cluster", "auto_splits", "pack_step", "STEP_MAP_IN", "STEP_MAP_OUT", "prefill", "prefill_read_error", "qk_norm_rope_kv_write", "gate", "workspace_bytes", "workspace_init", "reserve",
-    "read_error", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
+    "read_error", "debug_wait_limit", "timing_begin", "timing_end", "status_str", "version", "GdaError", "VARIANT_AUTO", "VARIANT_MMA",
     "VARIANT_SIMT", "VARIANT_TMA", "MAX_SPLITS", "LIB_PATH", "KV_BF16", "KV_E4M3",
 ]
 
@@ -117,6 +117,8 @@ def load(path: Optional[str] = None):
         lib.gda_timing_end.restype = i32
         lib.gda_version.argtypes = []
         lib.gda_version.restype = i32
+        lib.gda_debug_wait_limit.argtypes = [i64]
+        lib.gda_debug_wait_limit.restype = i32
         _lib = lib
         return lib
 
@@ -508,6 +510,13 @@ def timing_end():
     ms = ctypes.c_double(0.0)
     _check(load().gda_timing_end(ctypes.byref(n), ctypes.byref(ms)))
     return int(n.value), float(ms.value)
+
+
+def debug_wait_limit(cycles: int):
+    """``gda_debug_wait_limit``: the pipeline wait limit (SM cycles) of later calls;
+    a short limit makes the waiting kernels take their timeout path (failure-path
+    tests only); ``cycles <= 0`` restores the default."""
+    _check(load().gda_debug_wait_limit(int(cycles)))
 
 
 def read_error(workspace=None, clear: bool = True, stream=None) -> int:

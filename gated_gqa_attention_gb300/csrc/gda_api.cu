@@ -10,6 +10,7 @@
 // validate before launch).
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -35,6 +36,15 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Pipeline wait limit in SM cycles for later launches (0: gda::kWaitLimitCycles);
+// gda_debug_wait_limit sets it for the failure-path test.
+std::atomic<long long> g_wait_limit{0};
+
+long long wait_limit() {
+  const long long w = g_wait_limit.load();
+  return w > 0 ? w : gda::kWaitLimitCycles;
+}
 
 // stage-1 timing (gda_timing_begin / gda_timing_end)
 std::vector<cudaEvent_t> g_tev;   // pairs: [2i] before stage 1, [2i+1] after
@@ -246,6 +256,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.num_splits = splits;
   p1.min_chunk = min_chunk;
   p1.check_indices = a->check_indices ? 1 : 0;
+  p1.wait_limit = wait_limit();
   cudaEvent_t t_end = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -563,6 +574,7 @@ int gda_prefill(const gda_bf16* q, const gda_bf16* gate, const gda_bf16* k, cons
   p.scale_log2 = scale * 1.44269504088896340736f;
   p.causal = causal ? 1 : 0;
   p.fuse_gate = gate ? 1 : 0;
+  p.wait_limit = wait_limit();
   // with Skv == 0 the key maps still need a valid base: the queries' (never loaded)
   const void* kb = Skv > 0 ? static_cast<const void*>(k) : static_cast<const void*>(q);
   const void* vb = Skv > 0 ? static_cast<const void*>(v) : static_cast<const void*>(q);
@@ -816,6 +828,11 @@ const char* gda_status_str(int status) {
   }
 }
 
-int gda_version(void) { return 200; }  // 0.2.0: gda_args gained total_len
+int gda_debug_wait_limit(int64_t cycles) {
+  g_wait_limit.store(cycles > 0 && cycles < gda::kWaitLimitCycles ? (long long)cycles : 0);
+  return GDA_OK;
+}
+
+int gda_version(void) { return 300; }  // 0.3.0: gda_debug_wait_limit
 
 }  // extern "C"

@@ -72,16 +72,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete.  Gives up (returns
-// false) when *abort_flag becomes nonzero or after kWaitLimitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// false) when *abort_flag becomes nonzero or after `limit` SM cycles.  A limit below
+// kWaitLimitCycles is the failure-path test's: the wait then polls without
+// suspending and checks the clock on every poll, so any wait that does not
+// complete within that many cycles gives up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          long long limit = kWaitLimitCycles) {
+  if (limit < kWaitLimitCycles) {
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity)) {
+      if (*abort_flag || clock64() - t0 > limit) return false;
+    }
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitLimitCycles) return false;
+      if (clock64() - t0 > limit) return false;
     }
   }
 }

@@ -33,6 +33,8 @@ struct Stage1Params {
   int min_chunk;       // automatic mode
   int check_indices;
   float v_descale;     // e4m3 pools: V = v_descale * e4m3(code)
+  long long wait_limit;  // SM cycles after which a pipeline wait gives up (kWaitLimitCycles;
+                         // shorter only in the failure-path test)
 };
 
 struct Stage2Params {

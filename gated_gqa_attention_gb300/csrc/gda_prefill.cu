@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       for (int n = 0; n < 2 * ntiles; ++n) {
         const int x = n % nslot, u = n / nslot;  // slot and its use count
-        if (u > 0 && !mbar_wait(&empty[x], (u - 1) & 1, abort_flag)) { ok = false; break; }
+        if (u > 0 && !mbar_wait(&empty[x], (u - 1) & 1, abort_flag, p.wait_limit)) { ok = false; break; }
         ++arm[x];
         mbar_arrive_expect_tx(&full[x], kHalf);
         // box {64 elements, 128 rows, 2 column blocks}: keys 128 j .., head dimensions 128 h ..
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // the gate tile goes into the Q buffer once the last S product has read Q (its
         // last commit covers every earlier MMA of the S issuer)
         const int nl = 2 * ntiles - 1;  // the last K half
-        if (!mbar_wait(&bars.k_empty[nl % kKSlots], (nl / kKSlots) & 1, abort_flag)) ok = false;
+        if (!mbar_wait(&bars.k_empty[nl % kKSlots], (nl / kKSlots) & 1, abort_flag, p.wait_limit)) ok = false;
         if (ok) {
           ++arm_gate;
           mbar_arrive_expect_tx(&bars.g, 4 * kBlk);
@@ -387,13 +387,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint32_t idS = idesc_bf16(kPM, kPN, 0);
       uint64_t* last_bar = nullptr;  // the barrier of the last commit and its phase parity
       int last_par = 0;
-      bool ok = mbar_wait(&bars.qf, 0, abort_flag);
+      bool ok = mbar_wait(&bars.qf, 0, abort_flag, p.wait_limit);
       for (int j = 0; j < ntiles && ok; ++j) {
         const int sb = j & 1;
         const int x0 = (2 * j) % kKSlots, x1 = (2 * j + 1) % kKSlots;  // the slots of K(j)'s halves
-        ok = mbar_wait(&bars.k_full[x0], ((2 * j) / kKSlots) & 1, abort_flag) &&
-             mbar_wait(&bars.k_full[x1], ((2 * j + 1) / kKSlots) & 1, abort_flag);
-        if (ok && j >= kNSB) ok = mbar_wait(&bars.p_empty[sb], ((j >> 1) - 1) & 1, abort_flag);
+        ok = mbar_wait(&bars.k_full[x0], ((2 * j) / kKSlots) & 1, abort_flag, p.wait_limit) &&
+             mbar_wait(&bars.k_full[x1], ((2 * j + 1) / kKSlots) & 1, abort_flag, p.wait_limit);
+        if (ok && j >= kNSB) ok = mbar_wait(&bars.p_empty[sb], ((j >> 1) - 1) & 1, abort_flag, p.wait_limit);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -429,8 +429,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       bool ok = true;
       for (int j = 0; j < ntiles && ok; ++j) {
         const int pb = j & 1;
-        ok = mbar_wait(&bars.p_full[pb], (j >> 1) & 1, abort_flag) &&
-             mbar_wait(&bars.v_full[0], j & 1, abort_flag) && mbar_wait(&bars.v_full[1], j & 1, abort_flag);
+        ok = mbar_wait(&bars.p_full[pb], (j >> 1) & 1, abort_flag, p.wait_limit) &&
+             mbar_wait(&bars.v_full[0], j & 1, abort_flag, p.wait_limit) && mbar_wait(&bars.v_full[1], j & 1, abort_flag, p.wait_limit);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1, x2 = j & 1;  // S / P buffer; parity slot of the max exchange
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[sb], (j >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars.s_full[sb], (j >> 1) & 1, abort_flag, p.wait_limit));
       if (!ok) break;
       tc_fence_after();
       float s[64];
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc_fence_before();  // this warp's S reads are ordered before the partner's P writes
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.xm[rg][x2]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xm[rg][x2], (j >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.xm[rg][x2], (j >> 1) & 1, abort_flag, p.wait_limit));
       if (!ok) break;
       tc_fence_after();
       const float mx = fmaxf(hm, xbuf[(x2 * 2 + (1 - hc)) * kPM + r]) * p.scale_log2;
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // O must hold PV(j - 1) before it is rescaled; this warp rescales its half of O
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.wait_limit));
         if (!ok) break;
         tc_fence_after();
         for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int xs = ntiles & 1;  // exchange slot for the row sums (last used at tile ntiles - 2)
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_empty[jl & 1], (jl >> 1) & 1, abort_flag, p.wait_limit));
       // the row's sum is the two halves' sums
       if (ok) {
         if (warp < kSoftmaxWarps) {
@@ -573,9 +573,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.xl[eq]);
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.xl[eq], 0, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.xl[eq], 0, abort_flag, p.wait_limit));
       }
-      if (ok && p.fuse_gate) ok = __all_sync(0xffffffffu, mbar_wait(&bars.g, 0, abort_flag));
+      if (ok && p.fuse_gate) ok = __all_sync(0xffffffffu, mbar_wait(&bars.g, 0, abort_flag, p.wait_limit));
       if (!ok) fail();
       tc_fence_after();
     }
@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (tid == 0) {
         // every warp has staged its part: four TMA stores, then wait until they have read
         // the staging buffer before the CTA's shared memory goes away
-        if (mbar_wait(&bars.ost, 0, abort_flag)) {
+        if (mbar_wait(&bars.ost, 0, abort_flag, p.wait_limit)) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tma_store_4d(&to, 64 * c, h, i0, b, ostage + c * kBlk);
           tma_store_commit_and_wait_read();

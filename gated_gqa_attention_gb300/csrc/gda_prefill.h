@@ -17,6 +17,8 @@ struct PrefillParams {
   float scale_log2;            // scale * log2(e)
   int causal;
   int fuse_gate;
+  long long wait_limit;        // SM cycles after which a pipeline wait gives up (kWaitLimitCycles;
+                               // shorter only in the failure-path test)
 };
 
 // Prefill / extend gated SDPA (tcgen05); q, k, v, gate are [B, S, H, 256] BF16.

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
         nxt_kvh = pc.kvh / p.npass;
       }
       // issue the current tile
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) {
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag, p.wait_limit)) {
         ok = false;
         break;
       }
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
     for (int t0 = pc.j0; t0 < pc.j1; t0 += kTile) {
       const int n = min(kTile, pc.j1 - t0);
       const int nv = max(0, min(WTOK, n - warp * WTOK));
-      if (!aborted && !mbar_wait(&sm.full[stage], phase, abort_flag)) {
+      if (!aborted && !mbar_wait(&sm.full[stage], phase, abort_flag, p.wait_limit)) {
         aborted = true;
         if (lane == 0) {
           atomicOr(&p.hdr->error, kErrTimeout);
@@ -356,7 +356,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
       if (!aborted && nv > 0)
         math.tile(&sm.k[stage][warp * WTOK][0], &sm.v[stage][warp * WTOK][0], nv, p.scale_log2, lane);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);
+      // a warp that gave up frees no stage: its copies may still be landing, and the
+      // producer (which then sees the abort) must not refill it
+      if (lane == 0 && !aborted) mbar_arrive(&sm.empty[stage]);
       if (++stage == NSTAGE) {
         stage = 0;
         phase ^= 1u;

@@ -395,6 +395,19 @@ int gda_read_error(const void* workspace, gda_stream_t stream, int clear, uint32
 int gda_timing_begin(int max_calls);
 int gda_timing_end(int* n_timed, double* total_ms);
 
+/* Failure-path testing.  The kernels that wait on mbarriers (gda_prefill, and the
+ * GDA_VARIANT_TMA stage 1 of the decode) give up a wait after a limit of SM cycles
+ * (about two seconds by default), set GDA_DEVERR_TIMEOUT in their error word (the
+ * workspace's, or gda_prefill's), wait with the default limit for the copies and MMAs
+ * they already started, and return, so the context stays usable and the host reads a
+ * typed error instead of a hang (cuDNN FE-OSS "Gated Attention Block (SM107)",
+ * Forward: errors are reported, not hung on).  This sets the limit for calls enqueued
+ * after it, in this process, on every device: 0 < cycles < the default makes every
+ * such pipeline wait poll and give up after `cycles` (a test then sees the timeout
+ * path run, and the outputs of those calls are undefined); cycles <= 0 restores the
+ * default.  Not for production use.  Returns GDA_OK. */
+int gda_debug_wait_limit(int64_t cycles);
+
 /* Static description of a status code. */
 const char* gda_status_str(int status);
 
