@@ -290,6 +290,9 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p2.grid1 = grid;
   p2.min_chunk = min_chunk;
   p2.fuse_gate = a->fuse_gate ? 1 : 0;
+  // batched merge: when the B * Hq stage-2 CTAs fit one wave at its register count
+  // (six CTAs per SM) and a warp merges more than one partial (automatic splits may)
+  p2.batched = ((long long)a->B * a->Hq <= 6LL * sms && (splits == 0 || splits > 4)) ? 1 : 0;
   if (gda::launch_stage2(p2, stream) != cudaSuccess) return GDA_ERR_CUDA;
   return GDA_OK;
 }

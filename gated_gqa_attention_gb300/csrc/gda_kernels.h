@@ -52,6 +52,7 @@ struct Stage2Params {
   int grid1;           // stage-1 grid (automatic-mode chunking)
   int min_chunk;
   int fuse_gate;
+  int batched;         // merge with four partials' loads in flight per warp (small grids)
 };
 
 struct PrepParams {

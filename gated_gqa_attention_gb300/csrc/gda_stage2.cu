@@ -14,8 +14,9 @@
 // One CTA per (sequence, query head), 4 warps.  The prologue -- loading the gate
 // and computing its BF16 sigmoid -- runs before griddepcontrol.wait, overlapping
 // the tail of stage 1 under programmatic dependent launch.  Warp w merges
-// partials w, w+4, ... online (lane = 8 dims, two 16-byte loads per partial);
-// the four warp states are then combined through shared memory.
+// partials w, w+4, ... online (lane = 8 dims, two 16-byte loads per partial),
+// up to four partials' loads in flight at a time; the four warp states are
+// then combined through shared memory.
 #include "gda_device.cuh"
 #include "gda_kernels.h"
 
@@ -23,6 +24,10 @@ namespace gda {
 
 constexpr int kS2Warps = 4;
 
+// kBatch: partials whose loads a warp has in flight at a time (1 or 4; 4 takes 80
+// registers a thread against 46, so the host picks it only when the grid fits one wave
+// at that size and there are several partials per warp).
+template <int kBatch>
 __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   __shared__ float s_acc[kS2Warps][kD];
   __shared__ float s_m[kS2Warps];
@@ -62,21 +67,37 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int k = warp; k < n; k += kS2Warps) {
-    const long long id = (first + k) * id_mul + id_add;
-    // the LSE and the O rows are loaded together (no dependent round trip)
-    const float lse = __ldcg(p.lse_part + id * kG + g);
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + (id * kG + g) * kD + lane * 8);
-    const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-    if (lse == -INFINITY) continue;
-    const float Mn = fmaxf(M, lse);
-    const float fo = (M == -INFINITY) ? 0.0f : exp2f(M - Mn);
-    const float fn = exp2f(lse - Mn);
-    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  // Warp w merges partials w, w + 4, w + 8, ... in that order, online.  The LSE and O
+  // rows of kBatch of them are requested before any is merged, so a warp waits for
+  // one round trip per kBatch partials instead of one per partial (the same order,
+  // so the same bits, for either kBatch).
+  for (int k0 = warp; k0 < n; k0 += kBatch * kS2Warps) {
+    float lse[kBatch];
+    float4 x0[kBatch], x1[kBatch];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = acc[i] * fo + xv[i] * fn;
-    W = W * fo + fn;
-    M = Mn;
+    for (int t = 0; t < kBatch; ++t) {
+      const int k = k0 + t * kS2Warps;
+      lse[t] = -INFINITY;
+      if (k < n) {
+        const long long id = (first + k) * id_mul + id_add;
+        lse[t] = __ldcg(p.lse_part + id * kG + g);
+        const float4* src = reinterpret_cast<const float4*>(p.o_part + (id * kG + g) * kD + lane * 8);
+        x0[t] = __ldcg(src);
+        x1[t] = __ldcg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) {
+      if (lse[t] == -INFINITY) continue;
+      const float Mn = fmaxf(M, lse[t]);
+      const float fo = (M == -INFINITY) ? 0.0f : exp2f(M - Mn);
+      const float fn = exp2f(lse[t] - Mn);
+      const float xv[8] = {x0[t].x, x0[t].y, x0[t].z, x0[t].w, x1[t].x, x1[t].y, x1[t].z, x1[t].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = acc[i] * fo + xv[i] * fn;
+      W = W * fo + fn;
+      M = Mn;
+    }
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) s_acc[warp][lane * 8 + i] = acc[i];
@@ -128,7 +149,7 @@ cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stage2_kernel, p);
+  return p.batched ? cudaLaunchKernelEx(&cfg, stage2_kernel<4>, p) : cudaLaunchKernelEx(&cfg, stage2_kernel<1>, p);
 }
 
 // ------------------------------------------------------------------ standalone gate
