@@ -121,6 +121,11 @@ __global__ void __launch_bounds__(kSW * 32, 1) small_decode_kernel(SmallParams p
   const int h = lane >> 2, qd = lane & 3;  // fragment row (query head of the group) and quad lane
   const int G = p.G;
 
+  // launched as a programmatic dependent of the previous kernel in the stream: its
+  // results are visible after this wait, which comes before any global read; the next
+  // call's kernel may then launch (and set up) while this one runs
+  pdl_wait_prior_grid();
+  pdl_launch_dependents();
   // independent loads first: the range, Q as A fragments (rows 8..15 and heads >= G
   // are zero), the gate element this CTA finalises (its sigmoid comes later)
   int L;
@@ -475,8 +480,11 @@ cudaError_t launch_small(const SmallParams& p, int C, cudaStream_t stream) {
   e = small_attr(dev, C);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cluster_config(&cfg, attr, C, dim3((unsigned)C, (unsigned)p.Hkv, (unsigned)p.B), stream);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   if (p.kv_fp8) {
     if (C == 8) return cudaLaunchKernelEx(&cfg, small_decode_kernel<8, true>, p);
     if (C == 4) return cudaLaunchKernelEx(&cfg, small_decode_kernel<4, true>, p);

@@ -44,6 +44,9 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   const int sched_n = p.paired ? p.Hkv : p.Hkv * p.npass;
   const int id_mul = p.paired ? p.npass : 1, id_add = p.paired ? pass : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the next call's one-kernel decode (a programmatic dependent) may launch and set up
+  // now; it waits for this grid before it reads anything
+  pdl_launch_dependents();
 
   // prologue: this thread's two gate values and their BF16 sigmoids
   const size_t row = (size_t)bh * kD;
