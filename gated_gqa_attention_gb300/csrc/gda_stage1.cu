@@ -321,9 +321,6 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   static_assert(NG * 16 * 32 == 2 * NG * NWARP * 32, "2 NG Q fragments per thread");
   static_assert(!PAIR || NWARP == 8, "PAIR: four pairs, named barriers 1 .. 4");
 
-  // Stage 2 may start its prologue (gate loads and sigmoids) now.
-  pdl_launch_dependents();
-
   Sched sched;
   sched.begin(p.indptr, p.B, PAIR ? p.Hkv : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk,
               p.window);
@@ -381,8 +378,14 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
     if (nmine > 0) st.load_k(p.k_pool + (size_t)kv_head(pp) * kRowBytes, stride, s0, lane);
   };
 
+  // Stage 2 may start its prologue (gate loads and sigmoids) once this CTA knows it has
+  // work: an idle CTA (the automatic plan launches a full grid) exits without the
+  // trigger, which counts as one, so stage 2's CTAs are placed after the idle CTAs have
+  // left.  (Measured: idle CTAs that stay resident while stage 2 is placed slowed stage
+  // 2's merge by ~3 us on B1 L32768.)
   Piece pc;
   bool have = sched.next(pc);
+  if (have) pdl_launch_dependents();
   if (have) piece_head(pc);
   while (have) {
     const unsigned char* kb = p.k_pool + (size_t)kv_head(pc) * kRowBytes;
@@ -696,12 +699,19 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
   __shared__ __align__(16) DirectSmem sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Stage 2 may start its prologue (gate loads and sigmoids) now.
-  pdl_launch_dependents();
-
   Sched sched;
   sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
+  // Stage 2 may start its prologue (gate loads and sigmoids) once this CTA knows it has
+  // work: an idle CTA (the automatic plan launches a full grid) exits without the
+  // trigger, which counts as one, so stage 2's CTAs are placed after the idle CTAs have
+  // left.  (Measured: idle CTAs that stay resident while stage 2 is placed slowed stage
+  // 2's merge by ~3 us on B1 L32768.)
+  {
+    Sched peek = sched;
+    Piece first;
+    if (peek.next(first)) pdl_launch_dependents();
+  }
 
   auto fetch_slot = [&](const int* idx, int tok0, int n) -> int {
     int s = -1;

@@ -215,11 +215,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
   for (int i = threadIdx.x; i < kG * kD; i += blockDim.x) (&sm.obuf[0][0])[i] = 0.0f;
   if (threadIdx.x < kG) sm.lbuf[threadIdx.x] = 0.0f;
   __syncthreads();
-  // Stage 2 may start its prologue (gate loads and sigmoids) now.
-  pdl_launch_dependents();
 
   Sched sched;
   sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window);
+  // Stage 2 may start its prologue (gate loads and sigmoids) once this CTA knows it has
+  // work: an idle CTA (the automatic plan launches a full grid) exits without the
+  // trigger, which counts as one, so stage 2's CTAs are placed after the idle CTAs have
+  // left.  (Measured: idle CTAs that stay resident while stage 2 is placed slowed stage
+  // 2's merge by ~3 us on B1 L32768.)
+  {
+    Sched peek = sched;
+    Piece first;
+    if (peek.next(first)) pdl_launch_dependents();
+  }
   volatile int* abort_flag = &sm.abort_flag;
 
   if (warp == NCW) {
