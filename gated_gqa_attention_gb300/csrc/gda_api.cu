@@ -75,11 +75,16 @@ struct Layout {
 };
 
 // Header, then FP32 partial O [pieces][8][D], then partial LSE [pieces][8].  With two
-// passes the size covers both schedules: per virtual head, and paired (one piece per
-// KV head holding both groups' partials), which needs 2 num_pieces(B, Hkv).
+// or more passes the size covers both schedules: per virtual head, and paired (one
+// piece per KV head and pair of groups holding both groups' partials), which needs
+// 2 num_pieces(B, Hkv * ceil(passes / 2)).
 Layout layout(int B, int Hq, int Hkv, int D, int num_splits) {
   const int np = passes(Hq, Hkv);
-  const size_t pieces = (np == 2) ? 2 * num_pieces(B, Hkv, num_splits) : num_pieces(B, Hkv * np, num_splits);
+  size_t pieces = num_pieces(B, Hkv * np, num_splits);
+  if (np >= 2) {
+    const size_t pp = 2 * num_pieces(B, Hkv * ((np + 1) / 2), num_splits);
+    if (pp > pieces) pieces = pp;
+  }
   Layout l;
   l.o_off = gda::kHeaderBytes;
   l.lse_off = round_up(l.o_off + pieces * gda::kG * (size_t)D * sizeof(float), 256);
@@ -202,10 +207,12 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   const int variant = (a->variant == GDA_VARIANT_SIMT)  ? gda::kVariantSimt
                       : (a->variant == GDA_VARIANT_TMA) ? gda::kVariantTma
                                                         : gda::kVariantMma;
-  // G = 9..16 on the MMA kernel: both groups of a KV head in one piece (one HBM read)
-  const bool paired = npass == 2 && !fp8 && variant == gda::kVariantMma;
+  // G > 8 on the MMA kernel: the groups of 8 query heads in pairs, both groups of a
+  // pair in one piece (one HBM read of the KV head's rows per pair)
+  const bool paired = npass >= 2 && !fp8 && variant == gda::kVariantMma;
+  const int npair = (npass + 1) / 2;
   // the heads that split the batch into segments for the schedule
-  const long long vheads = paired ? (long long)a->Hkv : (long long)a->Hkv * npass;
+  const long long vheads = paired ? (long long)a->Hkv * npair : (long long)a->Hkv * npass;
   const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
   const int auto_grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
   int splits = a->num_splits > 0 ? a->num_splits : 0;
@@ -248,6 +255,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.G = a->Hq / a->Hkv;
   p1.npass = npass;
   p1.paired = paired ? 1 : 0;
+  p1.npair = npair;
   p1.window = a->window;
   // e4m3 pools: k_descale joins the score scale (one rounding, from double)
   p1.scale_log2 = fp8 ? (float)((double)a->scale * (double)a->k_descale * 1.4426950408889634074)
@@ -285,6 +293,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p2.G = p1.G;
   p2.npass = npass;
   p2.paired = p1.paired;
+  p2.npair = npair;
   p2.window = a->window;
   p2.num_splits = p1.num_splits;
   p2.grid1 = grid;

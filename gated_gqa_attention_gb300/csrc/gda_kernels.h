@@ -26,7 +26,9 @@ struct Stage1Params {
   int B, Hq, Hkv;
   int G;               // query heads per KV head (Hq / Hkv)
   int npass;           // ceil(G / 8): groups of 8 query heads per KV head ("virtual heads")
-  int paired;          // npass == 2, one piece per (sequence, KV head) for both groups
+  int paired;          // npass >= 2 on the MMA kernel: the groups go in pairs, one piece per
+                       // (sequence, KV head, pair) serving both groups of the pair
+  int npair;           // ceil(npass / 2): pairs per KV head
   int window;          // > 0: attend to the last `window` positions only
   float scale_log2;    // scale * log2(e) (e4m3 pools: scale * k_descale * log2(e))
   int num_splits;      // > 0 explicit, else automatic
@@ -47,7 +49,8 @@ struct Stage2Params {
   const float* sinks;  // [Hq] sink logits (natural units), or nullptr
   int B, Hq, Hkv;
   int G, npass, window;
-  int paired;          // stage 1 ran paired: partial (piece, group) is at piece * 2 + group
+  int paired;          // stage 1 ran paired: partial (piece, group of the pair) is at piece * 2 + group
+  int npair;           // ceil(npass / 2)
   int num_splits;
   int grid1;           // stage-1 grid (automatic-mode chunking)
   int min_chunk;

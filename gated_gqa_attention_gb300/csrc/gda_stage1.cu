@@ -298,8 +298,9 @@ __device__ __forceinline__ void issue_v_tile(unsigned char* stage, const unsigne
   cp_async_commit();
 }
 
-// PAIR (G = 9..16, two groups of 8 query heads per KV head): one piece per
-// (sequence, KV head) serves both groups, and every K/V row is loaded once.
+// PAIR (G > 8: the groups of 8 query heads of a KV head in pairs): one piece per
+// (sequence, KV head, pair) serves both groups of the pair, and every K/V row is
+// loaded once per pair (once for G = 9..16, twice for G = 17..32).
 // Warp w loads tiles w + NWARP*k as without PAIR and computes S^T of its tile for
 // both groups (one K fragment, two MMA chains); warps w and w ^ NWARP/2 form a
 // pair, the first half of the warps owning group 0 and the second half group 1.
@@ -322,12 +323,12 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   static_assert(!PAIR || NWARP == 8, "PAIR: four pairs, named barriers 1 .. 4");
 
   Sched sched;
-  sched.begin(p.indptr, p.B, PAIR ? p.Hkv : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk,
-              p.window);
+  sched.begin(p.indptr, p.B, PAIR ? p.Hkv * p.npair : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x,
+              p.min_chunk, p.window);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
   const uint64_t pol_v = l2_policy_evict_first();
-  // KV head of a piece (its scheduled head is the KV head itself when PAIR)
-  auto kv_head = [&](const Piece& pp) -> int { return PAIR ? pp.kvh : pp.kvh / p.npass; };
+  // KV head of a piece (with PAIR the scheduled head is kvh * npair + the pair)
+  auto kv_head = [&](const Piece& pp) -> int { return PAIR ? pp.kvh / p.npair : pp.kvh / p.npass; };
 
   // Warp w's tiles of a piece of `len` positions: tile w + NWARP*k.
   auto nmine_for = [&](int w, int len) -> int {
@@ -360,14 +361,25 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   // after the first this runs before the previous piece's merge, so the loads
   // are in flight while the warps merge.
   auto piece_head = [&](const Piece& pp) {
+    // PAIR: the piece's KV head and the first group of its pair
+    const int pkv = PAIR ? pp.kvh / p.npair : 0, pg0 = PAIR ? 2 * (pp.kvh - pkv * p.npair) : 0;
 #pragma unroll
     for (int r = 0; r < 2 * NG; ++r) {
       const int e = threadIdx.x + r * NWARP * 32;
       const int fg = e >> 9, kk = (e >> 5) & 15, ln = e & 31;  // group, k-step, lane
       int gv;
-      const __nv_bfloat16* qg = group_q(p, pp.b, PAIR ? pp.kvh * p.npass + fg : pp.kvh, &gv);
+      const __nv_bfloat16* qg;
+      if (PAIR) {
+        // group 2 * pair + fg of the KV head; past the last group (odd npass) the group
+        // is empty: its Q is zero and its partial is never read
+        const int gi = pg0 + fg;
+        qg = group_q(p, pp.b, pkv * p.npass + min(gi, p.npass - 1), &gv);
+        if (gi >= p.npass) gv = 0;
+      } else {
+        qg = group_q(p, pp.b, pp.kvh, &gv);
+      }
       const int g = ln >> 2, t = ln & 3, c = kk >> 1, h = kk & 1;
-      const __nv_bfloat16* row = qg + min(g, gv - 1) * kD;  // never addresses a row beyond the group
+      const __nv_bfloat16* row = qg + max(0, min(g, gv - 1)) * kD;  // never addresses a row beyond the group
       qfrag[r] = (g < gv) ? __ldg(reinterpret_cast<const uint2*>(row + 32 * c + 8 * t + 4 * h)) : make_uint2(0u, 0u);
     }
     const int* idx = p.indices + pp.base + pp.j0;

@@ -37,12 +37,13 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   const int b = bh / p.Hq, h = bh % p.Hq;
   // query head h belongs to KV head h / G; its slot g in group `pass` (groups of 8).
   // Stage 1 scheduled pieces per virtual head vh = kvh * npass + pass, or, paired,
-  // per KV head with the partial of (piece, group) at piece * npass + group.
+  // per (KV head, pair of groups) kvh * npair + pass / 2 with the partial of (piece,
+  // group of the pair) at piece * 2 + pass % 2.
   const int kvh = h / p.G, r = h - kvh * p.G;
   const int pass = r / kG, g = r % kG;
-  const int sched_h = p.paired ? kvh : kvh * p.npass + pass;
-  const int sched_n = p.paired ? p.Hkv : p.Hkv * p.npass;
-  const int id_mul = p.paired ? p.npass : 1, id_add = p.paired ? pass : 0;
+  const int sched_h = p.paired ? kvh * p.npair + (pass >> 1) : kvh * p.npass + pass;
+  const int sched_n = p.paired ? p.Hkv * p.npair : p.Hkv * p.npass;
+  const int id_mul = p.paired ? 2 : 1, id_add = p.paired ? (pass & 1) : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the next call's one-kernel decode (a programmatic dependent) may launch and set up
   // now; it waits for this grid before it reads anything

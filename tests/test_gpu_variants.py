@@ -77,7 +77,7 @@ def test_sinks_lse_and_empty_rows(gda, batch):
 
 
 @pytest.mark.parametrize("hq,hkv", [(16, 16), (16, 8), (6, 2), (16, 4), (12, 2), (14, 2), (32, 2), (20, 2), (15, 1),
-                                     (48, 2), (24, 1)])
+                                     (48, 2), (24, 1), (40, 2), (64, 2), (56, 1)])
 @pytest.mark.parametrize("variant", [1, 2, 3])
 def test_gqa_group_sizes(gda, hq, hkv, variant):
     inp = workloads.make([1, 37, 300, 0, 129], seed=300 + hq + hkv, hq=hq, hkv=hkv, layout="perm", pool_slots=1000)
@@ -106,12 +106,14 @@ def test_window_on_the_ragged_workload(gda):
     check_close(got[idx], ref.out[idx])
 
 
-# G = 9..16 on the MMA kernel: one piece per (sequence, KV head) serves both groups of
-# 8 query heads, half of the CTA's warps each, and stage 2 reads the partial of
-# (piece, group) at piece * 2 + group.  Long ragged batches make pieces cross
-# sequences and CTAs; a window, sinks, the LSE and explicit splits go through the
-# same mapping.  The TMA variant (3) runs the same case per virtual head.
-@pytest.mark.parametrize("hq,hkv", [(32, 2), (20, 2), (16, 1), (30, 3)])
+# G > 8 on the MMA kernel: the groups of 8 query heads go in pairs; one piece per
+# (sequence, KV head, pair) serves both groups of the pair, half of the CTA's warps
+# each, and stage 2 reads the partial of (piece, group of the pair) at piece * 2 +
+# group.  G = 24 and G = 56 have an odd number of groups (the last pair's second group
+# is empty).  Long ragged batches make pieces cross sequences and CTAs; a window,
+# sinks, the LSE and explicit splits go through the same mapping.  The TMA variant (3)
+# runs the same case per virtual head.
+@pytest.mark.parametrize("hq,hkv", [(32, 2), (20, 2), (16, 1), (30, 3), (48, 2), (64, 2), (56, 1)])
 def test_paired_groups_long_ragged(gda, hq, hkv):
     lens = [4096, 1, 0, 3000, 777, 65, 2049, 16, 5000, 129, 1500, 2]
     inp = workloads.make(lens, seed=500 + hq + hkv, hq=hq, hkv=hkv, layout="perm", pool_slots=20000,
@@ -126,10 +128,13 @@ def test_paired_groups_long_ragged(gda, hq, hkv):
     np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
 
 
-def test_paired_groups_workload_sample(gda):
-    # b64_l4096's lengths with Hq = 32, Hkv = 2 (G = 16), sampled (sequence, head) pairs
-    inp = workloads.make([4096] * 64, seed=77, hq=32, hkv=2, layout="perm", pool_slots=64 * 4096 + 1000)
-    pairs = np.array([(b, h) for b in range(0, 64, 9) for h in (0, 7, 8, 15, 16, 31)])
+@pytest.mark.parametrize("hq", [32, 48])
+def test_paired_groups_workload_sample(gda, hq):
+    # b64_l4096's lengths with Hq = 32 or 48, Hkv = 2 (G = 16: one pair; G = 24: a pair
+    # and a half-empty pair), sampled (sequence, head) pairs
+    inp = workloads.make([4096] * 64, seed=77, hq=hq, hkv=2, layout="perm", pool_slots=64 * 4096 + 1000)
+    heads = sorted({0, 7, 8, 15, 16, hq // 2 - 1, hq // 2, hq - 9, hq - 8, hq - 1})
+    pairs = np.array([(b, h) for b in range(0, 64, 9) for h in heads])
     ref = reference(inp, pairs=pairs)
     got = run(gda, inp)
     idx = tuple(pairs.T)

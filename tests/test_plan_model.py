@@ -153,10 +153,12 @@ def test_small_batches_get_one_piece_per_cta():
 
 
 def test_paired_partials_fit_the_workspace():
-    # G = 9..16 on the MMA kernel: pieces are scheduled per (sequence, KV head) and
-    # the partial of (piece, group) sits at piece * 2 + group.  The workspace holds
-    # 2 x the pieces of the per-KV-head schedule, at least what the per-virtual-head
-    # schedule of the other kernels needs; stage 2 finds exactly stage 1's slots.
+    # G > 8 on the MMA kernel: the npass groups of 8 query heads of a KV head go in
+    # npair = ceil(npass / 2) pairs; pieces are scheduled per (sequence, KV head, pair)
+    # and the partial of (piece, group of the pair) sits at piece * 2 + group.  The
+    # workspace holds max(2 x the pieces of that schedule, the pieces of the
+    # per-virtual-head schedule of the other kernels); stage 2 finds exactly stage 1's
+    # slots for every query-head group.
     rng = random.Random(11)
     for _ in range(300):
         B = rng.randint(1, 80)
@@ -165,19 +167,22 @@ def test_paired_partials_fit_the_workspace():
         for L in lens:
             indptr.append(indptr[-1] + L)
         Hkv = rng.choice([1, 2, 4])
+        npass = rng.choice([2, 2, 3, 4, 7])
+        npair = (npass + 1) // 2
         grid = rng.choice([7, 152, 1024])
         S_user = rng.choice([0, 0, 2, 8])
-        pieces, S, T = stage1_pieces(indptr, Hkv, grid, 64, S_user)
-        cap = 2 * (B * Hkv * S_user if S_user > 0 else AUTO_MAX_CTAS + B * Hkv)
-        cap_vheads = B * 2 * Hkv * S_user if S_user > 0 else AUTO_MAX_CTAS + B * 2 * Hkv
-        assert cap >= cap_vheads
+        heads = Hkv * npair
+        pieces, S, T = stage1_pieces(indptr, heads, grid, 64, S_user)
+        num_pieces = lambda vh: B * vh * S_user if S_user > 0 else AUTO_MAX_CTAS + B * vh
+        cap = max(2 * num_pieces(heads), num_pieces(Hkv * npass))
         slots = [p[4] * 2 + g for p in pieces for g in (0, 1)]
         assert len(slots) == len(set(slots)) and all(0 <= s < cap for s in slots)
         for b in range(B):
             for kvh in range(Hkv):
-                for g in (0, 1):
-                    want = sorted(p[4] * 2 + g for p in pieces if p[0] == b and p[1] == kvh)
-                    assert [i * 2 + g for i in stage2_ids(indptr, Hkv, b, kvh, S, T)] == want
+                for gp in range(npass):  # query-head group gp of KV head kvh
+                    sched_h, g = kvh * npair + gp // 2, gp % 2
+                    want = sorted(p[4] * 2 + g for p in pieces if p[0] == b and p[1] == sched_h)
+                    assert [i * 2 + g for i in stage2_ids(indptr, heads, b, sched_h, S, T)] == want
 
 
 def test_paired_kernel_tile_arithmetic():
