@@ -10,9 +10,10 @@
  *   slot_j     = kv_indices[kv_indptr[b] + j],  0 <= j < kv_indptr[b+1]-kv_indptr[b]
  *
  * with G = Hq / Hkv consecutive query heads sharing one KV head (any G >= 1; the
- * kernels handle the query heads of a KV head in groups of up to 8: for G = 9 .. 16
- * the default kernel serves both groups from one read of the KV head's rows, and
- * otherwise, or on the other kernels, the rows are read once per group).  Sources: FreeToken
+ * kernels handle the query heads of a KV head in groups of up to 8: for G > 8 the
+ * default kernel serves the groups in pairs, both groups of a pair from one read of
+ * the KV head's rows (one read for G = 9 .. 16, two for 17 .. 32), and the other
+ * kernels read the rows once per group).  Sources: FreeToken
  * PR #781 "Fuse the BF16 attention output sigmoid gate into the existing Triton
  * decode stage2" (Summary: split-KV stage 1, FP32 LSE merge in stage 2 with the
  * BF16 gate and an explicit round-to-nearest-even product fused into its epilogue;
