@@ -196,11 +196,15 @@ __device__ __forceinline__ float safe_exp2_diff(float a, float m) {
 //     equal splits still gives at most one split per CTA (B*Hkv*S <= grid) -- use
 //     those uniform splits exactly as the explicit mode does: every CTA then has
 //     one piece and no piece boundary to cross (the latency-bound regime);
-//   * otherwise the whole stream of total = Hkv * nnz positions is cut into
-//     chunks of T = max(ceil(total/grid), min_chunk) positions, chunk c to CTA c
-//     (equal work per CTA for any length mix); the piece (segment sigma, chunk c)
-//     lives at index c + sigma.  That index is unique (a later chunk can only meet
-//     a later-or-equal segment) and below grid + B*Hkv, which bounds the workspace.
+//   * otherwise the whole stream of total = Hkv * nnz positions is cut into grid
+//     chunks of equal cost, chunk c to CTA c: a position costs 1 and, when there are
+//     more segments than CTAs, every segment start after the first kPieceCost more
+//     (the measured price of one more piece), so T = max(ceil(cost / grid),
+//     min_chunk) cost units per CTA and a CTA that crosses more segment starts takes
+//     fewer positions (equal time per CTA for any length mix); the piece (segment
+//     sigma, chunk c) lives at index c + sigma.
+//     That index is unique (a later chunk can only meet a later-or-equal segment)
+//     and below grid + B*Hkv, which bounds the workspace.
 
 struct Piece {
   int b, kvh, sigma;  // kvh: the (virtual) head of the piece, sigma = b * heads + kvh
@@ -226,10 +230,19 @@ __device__ __forceinline__ void seq_range(const int* indptr, int b, int window, 
 // even for batches that fit one wave of uniform splits.
 constexpr int kStreamMinPerCta = 3072;
 
+// Stream schedule: what starting one more (sequence, KV head) segment costs a CTA, in
+// positions of streaming.  Measured on GB300 (per-CTA end times on b224_ragged, ~3
+// segment starts per CTA): a CTA ends ~5 us later per extra piece -- the piece's
+// merge, its partial tile round and the restart of its loads -- while it streams ~42
+// positions per us; the chunks are then cut in a cost space where each segment start
+// adds this much.  With fewer segments than CTAs (b64_l4096: every CTA meets one or
+// two) the weighting measured slower, and the cost is 0.
+constexpr int kPieceCost = 200;
+
 struct Sched {
   const int* indptr;
   int B, Hkv, S, grid, cta, window;
-  long long T, total;
+  long long T, total, X;
   // iteration state
   long long pos, end;  // automatic
   int b;
@@ -256,12 +269,37 @@ struct Sched {
       u = cta;
       return;
     }
+    // the stream of total = Hkv * nnz positions in a cost space where every segment
+    // start after the first adds kPieceCost: CTA c takes the costs [c T, (c + 1) T) and
+    // so the positions between the first ones costing at least c T and (c + 1) T
     total = (long long)Hkv * (long long)ntot;
-    T = auto_chunk(total, grid, min_chunk);
-    pos = (long long)cta * T;
-    end = min(total, pos + T);
+    X = piece_cost(B, Hkv, grid);
+    const long long ctot = stream_cost(total, B, Hkv, X);
+    T = auto_chunk(ctot, grid, min_chunk);
+    const long long t0 = (long long)cta * T, t1 = t0 + T;
     b = 0;
-    if (pos < end) b = first_seq_ending_after(indptr, B, Hkv, pos, v0);
+    pos = end = total;
+    if (t0 < ctot) {
+      int b0, b1;
+      if (X == 0) {
+        // costs are positions: no second search, no mapping back (every dependent
+        // load here delays the CTA's first tile)
+        pos = t0;
+        end = min(total, t1);
+        b0 = first_seq_ending_after(indptr, B, Hkv, pos, v0);
+      } else {
+        first_seqs_costing_beyond(indptr, B, Hkv, X, t0, t1, v0, &b0, &b1);
+        pos = position_at_cost(indptr, Hkv, X, b0, t0);
+        end = (t1 >= ctot) ? total : position_at_cost(indptr, Hkv, X, b1, t1);
+      }
+      b = b0;
+    }
+  }
+
+  // The cost of a segment start: kPieceCost when the batch has more segments than
+  // there are CTAs, else 0 (plain equal chunks of positions).
+  static __device__ __forceinline__ long long piece_cost(int B, int Hkv, int grid) {
+    return ((long long)B * Hkv > grid) ? kPieceCost : 0;
   }
 
   // First sequence b whose (Hkv-scaled) end Hkv*indptr[b+1] lies beyond pos (one
@@ -291,6 +329,74 @@ struct Sched {
       }
     }
     return lo;
+  }
+
+  // Cost of the whole stream (positions plus X per segment start after the first).
+  static __device__ __forceinline__ long long stream_cost(long long total, int B, int Hkv, long long X) {
+    const long long nseg = (long long)B * Hkv;
+    return total + X * (nseg > 0 ? nseg - 1 : 0);
+  }
+
+  // Cost at which sequence b's first segment starts: Hkv * indptr[b] + X * b * Hkv.
+  static __device__ __forceinline__ long long seq_cost_start(long long ib, int b, int Hkv, long long X) {
+    return (long long)Hkv * ib + X * b * Hkv;
+  }
+
+  // The first position whose cost is at least t (t < the stream cost), with b the
+  // sequence whose cost range holds t.  Segment (b, k) covers positions
+  // Hkv indptr[b] + k L + [0, L) at costs seq_cost_start + k (L + X) + [0, L), followed
+  // by X of cost with no positions (a t there maps to the next segment's first position).
+  static __device__ __forceinline__ long long position_at_cost(const int* indptr, int Hkv, long long X, int b,
+                                                               long long t) {
+    const long long ib = __ldg(indptr + b);
+    const long long L = __ldg(indptr + b + 1) - ib;
+    const long long cs = seq_cost_start(ib, b, Hkv, X);
+    long long k = (L + X > 0) ? (t - cs) / (L + X) : 0;
+    k = k < 0 ? 0 : (k > Hkv - 1 ? Hkv - 1 : k);
+    const long long into = t - (cs + k * (L + X));
+    return (long long)Hkv * ib + k * L + (into < 0 ? 0 : (into > L ? L : into));
+  }
+
+  // The first sequences whose cost range ends beyond ta and beyond tb (both below the
+  // stream cost, so sequence B - 1 qualifies): the end of sequence b's range is
+  // seq_cost_start(indptr[b + 1], b + 1, Hkv, X).  Called by every lane of a full warp: two
+  // 32-way searches in lockstep, each round one load per lane and search, so ceil(log32
+  // B) dependent loads instead of log2 B.  v0: this lane's value of the first round
+  // (shared by both), indptr[min(B-1, lane*step0) + 1].
+  static __device__ __forceinline__ void first_seqs_costing_beyond(const int* indptr, int B, int Hkv, long long X,
+                                                                   long long ta, long long tb, int v0, int* ba,
+                                                                   int* bb) {
+    const int lane = (int)(threadIdx.x & 31);
+    int lo[2] = {0, 0}, hi[2] = {B - 1, B - 1};  // each answer lies in [lo, hi]
+    const long long tt[2] = {ta, tb};
+    bool first = true;
+    while (lo[0] < hi[0] || lo[1] < hi[1]) {
+      int step[2], cand[2], v[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        step[x] = (hi[x] - lo[x] + 32) / 32;  // 32 candidates cover [lo, hi]
+        cand[x] = min(hi[x], lo[x] + lane * step[x]);
+        v[x] = first ? v0 : ((lo[x] < hi[x]) ? __ldg(indptr + cand[x] + 1) : 0);
+      }
+      first = false;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const bool past = seq_cost_start(v[x], cand[x] + 1, Hkv, X) > tt[x];
+        const unsigned ball = __ballot_sync(0xffffffffu, past);
+        if (lo[x] >= hi[x]) continue;  // (warp-uniform) this search is done
+        // candidates are non-decreasing in the lane index; hi itself satisfies `past`
+        if (ball == 0u) {
+          lo[x] = min(hi[x], lo[x] + 31 * step[x]) + 1;
+        } else {
+          const int f = __ffs(ball) - 1;
+          const int cf = min(hi[x], lo[x] + f * step[x]);
+          lo[x] = (f == 0) ? lo[x] : min(hi[x], lo[x] + (f - 1) * step[x]) + 1;
+          hi[x] = cf;
+        }
+      }
+    }
+    *ba = lo[0];
+    *bb = lo[1];
   }
 
   // Automatic mode: the uniform split count S (every segment cut into S equal
@@ -420,8 +526,11 @@ __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh
     return;
   }
   const long long total = (long long)Hkv * (long long)__ldg(indptr + B);
-  const long long T = Sched::auto_chunk(total, grid, min_chunk);
-  const long long start = (long long)Hkv * ib + (long long)kvh * L;
+  const long long X = Sched::piece_cost(B, Hkv, grid);
+  const long long T = Sched::auto_chunk(Sched::stream_cost(total, B, Hkv, X), grid, min_chunk);
+  // the segment's positions in the stream's cost space (Sched::begin): they start at
+  // cost Hkv indptr[b] + kvh L + X (b Hkv + kvh), one cost unit each
+  const long long start = (long long)Hkv * ib + (long long)kvh * L + X * sigma;
   const long long c0 = start / T, c1 = (start + L - 1) / T;
   *first = c0 + sigma;
   *n = (int)(c1 - c0 + 1);

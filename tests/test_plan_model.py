@@ -43,6 +43,36 @@ def uniform_splits(indptr, Hkv, grid, min_chunk):
     return s
 
 
+PIECE_COST = 200
+
+
+def piece_cost(B, Hkv, grid):
+    """The cost of a segment start (Sched::piece_cost): PIECE_COST with more segments
+    than CTAs, else 0."""
+    return PIECE_COST if B * Hkv > grid else 0
+
+
+def stream_cost(total, B, Hkv, X):
+    """The stream's cost: one per position, X more per segment start after the first
+    (Sched::stream_cost)."""
+    return total + X * max(B * Hkv - 1, 0)
+
+
+def position_at_cost(indptr, Hkv, X, t):
+    """The first stream position whose cost is at least t (the stream's end past
+    it): position p of segment sigma costs p + X * sigma.  A plain scan over the
+    positions, not the device's search."""
+    B = len(indptr) - 1
+    for b in range(B):
+        L = indptr[b + 1] - indptr[b]
+        for k in range(Hkv):
+            sigma = b * Hkv + k
+            start = Hkv * indptr[b] + k * L
+            if L > 0 and start + L - 1 + X * sigma >= t:
+                return start + max(0, t - (start + X * sigma))
+    return Hkv * indptr[B]
+
+
 def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
     B = len(indptr) - 1
     if S <= 0:
@@ -62,9 +92,10 @@ def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
                 u += grid
         return out, S, None
     total = Hkv * indptr[B]
-    T = max(-(-total // grid), min_chunk)
+    X = piece_cost(B, Hkv, grid)
+    T = max(-(-stream_cost(total, B, Hkv, X) // grid), min_chunk)
     for c in range(grid):
-        pos, end = c * T, min(total, c * T + T)
+        pos, end = position_at_cost(indptr, Hkv, X, c * T), position_at_cost(indptr, Hkv, X, c * T + T)
         if pos >= end:
             continue
         b = 0
@@ -80,7 +111,7 @@ def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
     return out, 0, T
 
 
-def stage2_ids(indptr, Hkv, b, kvh, S, T):
+def stage2_ids(indptr, Hkv, b, kvh, S, T, grid):
     L = indptr[b + 1] - indptr[b]
     if L <= 0:
         return []
@@ -88,7 +119,8 @@ def stage2_ids(indptr, Hkv, b, kvh, S, T):
     if S > 0:
         c = -(-L // S)
         return [sig * S + k for k in range(-(-L // c))]
-    start = Hkv * indptr[b] + kvh * L
+    X = piece_cost(len(indptr) - 1, Hkv, grid)
+    start = Hkv * indptr[b] + kvh * L + X * sig  # the segment's first position's cost
     return [c + sig for c in range(start // T, (start + L - 1) // T + 1)]
 
 
@@ -118,7 +150,7 @@ def test_plan_invariants_random_batches():
         for b in range(B):
             for kvh in range(Hkv):
                 mine = sorted(p[4] for p in pieces if p[0] == b and p[1] == kvh)
-                assert stage2_ids(indptr, Hkv, b, kvh, S, T) == mine
+                assert stage2_ids(indptr, Hkv, b, kvh, S, T, grid) == mine
 
 
 def test_split_rule_on_measured_buckets():
@@ -144,12 +176,27 @@ def test_small_batches_get_one_piece_per_cta():
     indptr = [4096 * i for i in range(65)]
     assert uniform_splits(indptr, 2, 152, 64) == 0
     pieces, S, T = stage1_pieces(indptr, 2, 152, 64, 0)
+    # fewer segments (128) than CTAs: equal positions per CTA
     per_cta = {}
     for b, kvh, j0, j1, pid in pieces:
         c = pid - (b * 2 + kvh)
         per_cta[c] = per_cta.get(c, 0) + (j1 - j0)
     assert max(per_cta.values()) - min(per_cta.values()) <= T
     assert max(per_cta.values()) == T
+    # more segments than CTAs (a ragged batch of 224): equal cost ranges per CTA; its
+    # positions plus PIECE_COST per piece after its first leave out the parts of a
+    # segment-start gap at either end of its range, at most 2 PIECE_COST
+    rng = random.Random(3)
+    indptr = [0]
+    for _ in range(224):
+        indptr.append(indptr[-1] + rng.randint(1, 6142))
+    pieces, S, T = stage1_pieces(indptr, 2, 152, 64, 0)
+    cost = {}
+    for b, kvh, j0, j1, pid in pieces:
+        c = pid - (b * 2 + kvh)
+        cost[c] = cost.get(c, -PIECE_COST) + (j1 - j0) + PIECE_COST
+    assert max(cost.values()) - min(cost.values()) <= 2 * PIECE_COST
+    assert max(cost.values()) == T and len(cost) == 152
 
 
 def test_paired_partials_fit_the_workspace():
@@ -182,7 +229,7 @@ def test_paired_partials_fit_the_workspace():
                 for gp in range(npass):  # query-head group gp of KV head kvh
                     sched_h, g = kvh * npair + gp // 2, gp % 2
                     want = sorted(p[4] * 2 + g for p in pieces if p[0] == b and p[1] == sched_h)
-                    assert [i * 2 + g for i in stage2_ids(indptr, heads, b, sched_h, S, T)] == want
+                    assert [i * 2 + g for i in stage2_ids(indptr, heads, b, sched_h, S, T, grid)] == want
 
 
 def test_paired_kernel_tile_arithmetic():
