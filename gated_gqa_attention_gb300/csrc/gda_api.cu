@@ -263,6 +263,9 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.v_descale = fp8 ? a->v_descale : 1.0f;
   p1.num_splits = splits;
   p1.min_chunk = min_chunk;
+  // automatic stream schedule with more segments than CTAs: a segment start costs a CTA
+  // about as much as kPieceCost positions (twice as many positions of an e4m3 cache)
+  p1.piece_cost = (splits == 0 && (long long)a->B * vheads > grid) ? (fp8 ? gda::kPieceCostE4m3 : gda::kPieceCost) : 0;
   p1.check_indices = a->check_indices ? 1 : 0;
   p1.wait_limit = wait_limit();
   cudaEvent_t t_end = nullptr;
@@ -298,6 +301,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p2.num_splits = p1.num_splits;
   p2.grid1 = grid;
   p2.min_chunk = min_chunk;
+  p2.piece_cost = p1.piece_cost;
   p2.fuse_gate = a->fuse_gate ? 1 : 0;
   // batched merge: when the B * Hq stage-2 CTAs fit one wave at its register count
   // (six CTAs per SM) and a warp merges more than one partial (automatic splits may)

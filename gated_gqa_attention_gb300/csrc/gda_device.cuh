@@ -234,10 +234,14 @@ constexpr int kStreamMinPerCta = 3072;
 // positions of streaming.  Measured on GB300 (per-CTA end times on b224_ragged, ~3
 // segment starts per CTA): a CTA ends ~5 us later per extra piece -- the piece's
 // merge, its partial tile round and the restart of its loads -- while it streams ~42
-// positions per us; the chunks are then cut in a cost space where each segment start
-// adds this much.  With fewer segments than CTAs (b64_l4096: every CTA meets one or
-// two) the weighting measured slower, and the cost is 0.
-constexpr int kPieceCost = 200;
+// positions per us of a BF16 cache (twice as many of an e4m3 cache, half the bytes);
+// the chunks are then cut in a cost space where each segment start adds this much.
+// A sweep of the cost on that batch put the best at 300 (BF16; 200 and 400 ~1 %
+// slower) and 600 (e4m3; 400 1 %, 1000 3 % slower).  With fewer segments than CTAs
+// (b64_l4096: every CTA meets one or two) the weighting measured slower, and the cost
+// is 0 (the host passes the cost it picks).
+constexpr int kPieceCost = 300;
+constexpr int kPieceCostE4m3 = 600;
 
 struct Sched {
   const int* indptr;
@@ -251,7 +255,7 @@ struct Sched {
   // Hkv_ here is the number of (virtual) heads that split the batch into segments.
   // window > 0 requires S_ > 0 (the host picks the split count then).
   __device__ __forceinline__ void begin(const int* indptr_, int B_, int Hkv_, int S_, int grid_,
-                                        int cta_, int min_chunk, int window_) {
+                                        int cta_, int min_chunk, int window_, int piece_cost_) {
     indptr = indptr_;
     B = B_;
     Hkv = Hkv_;
@@ -273,7 +277,7 @@ struct Sched {
     // start after the first adds kPieceCost: CTA c takes the costs [c T, (c + 1) T) and
     // so the positions between the first ones costing at least c T and (c + 1) T
     total = (long long)Hkv * (long long)ntot;
-    X = piece_cost(B, Hkv, grid);
+    X = piece_cost_;
     const long long ctot = stream_cost(total, B, Hkv, X);
     T = auto_chunk(ctot, grid, min_chunk);
     const long long t0 = (long long)cta * T, t1 = t0 + T;
@@ -294,12 +298,6 @@ struct Sched {
       }
       b = b0;
     }
-  }
-
-  // The cost of a segment start: kPieceCost when the batch has more segments than
-  // there are CTAs, else 0 (plain equal chunks of positions).
-  static __device__ __forceinline__ long long piece_cost(int B, int Hkv, int grid) {
-    return ((long long)B * Hkv > grid) ? kPieceCost : 0;
   }
 
   // First sequence b whose (Hkv-scaled) end Hkv*indptr[b+1] lies beyond pos (one
@@ -507,7 +505,8 @@ struct Sched {
 // mode: first = c_first + sigma), or sigma*S + k (explicit mode), in position order.
 // (With a window the split count is explicit and L is the windowed length.)
 __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh, int Hkv, int B, int S,
-                                               int grid, int min_chunk, int window, long long* first, int* n) {
+                                               int grid, int min_chunk, int window, int piece_cost, long long* first,
+                                               int* n) {
   const int ib = __ldg(indptr + b);
   int L;
   long long base;
@@ -526,7 +525,7 @@ __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh
     return;
   }
   const long long total = (long long)Hkv * (long long)__ldg(indptr + B);
-  const long long X = Sched::piece_cost(B, Hkv, grid);
+  const long long X = piece_cost;
   const long long T = Sched::auto_chunk(Sched::stream_cost(total, B, Hkv, X), grid, min_chunk);
   // the segment's positions in the stream's cost space (Sched::begin): they start at
   // cost Hkv indptr[b] + kvh L + X (b Hkv + kvh), one cost unit each

@@ -33,6 +33,7 @@ struct Stage1Params {
   float scale_log2;    // scale * log2(e) (e4m3 pools: scale * k_descale * log2(e))
   int num_splits;      // > 0 explicit, else automatic
   int min_chunk;       // automatic mode
+  int piece_cost;      // automatic stream schedule: cost of a segment start in positions (0: none)
   int check_indices;
   float v_descale;     // e4m3 pools: V = v_descale * e4m3(code)
   long long wait_limit;  // SM cycles after which a pipeline wait gives up (kWaitLimitCycles;
@@ -54,6 +55,7 @@ struct Stage2Params {
   int num_splits;
   int grid1;           // stage-1 grid (automatic-mode chunking)
   int min_chunk;
+  int piece_cost;      // the stage-1 schedule's cost of a segment start
   int fuse_gate;
   int batched;         // merge with four partials' loads in flight per warp (small grids)
 };

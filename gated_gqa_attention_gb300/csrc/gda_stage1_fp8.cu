@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_kernel(Stage1Params p)
 
   if (threadIdx.x == 0) sm.qmax = 0u;
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window);
+  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window, p.piece_cost);
   const size_t stride = (size_t)p.Hkv * kRowBytes8;
   const uint64_t pol_v = l2_policy_evict_first();
 

@@ -43,13 +43,14 @@ def uniform_splits(indptr, Hkv, grid, min_chunk):
     return s
 
 
-PIECE_COST = 200
+PIECE_COST = 300        # a BF16 cache
+PIECE_COST_E4M3 = 600   # an e4m3 cache streams twice the positions per microsecond
 
 
-def piece_cost(B, Hkv, grid):
-    """The cost of a segment start (Sched::piece_cost): PIECE_COST with more segments
-    than CTAs, else 0."""
-    return PIECE_COST if B * Hkv > grid else 0
+def piece_cost(B, Hkv, grid, cost=PIECE_COST):
+    """The cost of a segment start (the host's Stage1Params::piece_cost): `cost` with
+    more segments than CTAs, else 0."""
+    return cost if B * Hkv > grid else 0
 
 
 def stream_cost(total, B, Hkv, X):
@@ -73,7 +74,7 @@ def position_at_cost(indptr, Hkv, X, t):
     return Hkv * indptr[B]
 
 
-def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
+def stage1_pieces(indptr, Hkv, grid, min_chunk, S, cost=PIECE_COST):
     B = len(indptr) - 1
     if S <= 0:
         S = uniform_splits(indptr, Hkv, grid, min_chunk)
@@ -92,7 +93,7 @@ def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
                 u += grid
         return out, S, None
     total = Hkv * indptr[B]
-    X = piece_cost(B, Hkv, grid)
+    X = piece_cost(B, Hkv, grid, cost)
     T = max(-(-stream_cost(total, B, Hkv, X) // grid), min_chunk)
     for c in range(grid):
         pos, end = position_at_cost(indptr, Hkv, X, c * T), position_at_cost(indptr, Hkv, X, c * T + T)
@@ -111,7 +112,7 @@ def stage1_pieces(indptr, Hkv, grid, min_chunk, S):
     return out, 0, T
 
 
-def stage2_ids(indptr, Hkv, b, kvh, S, T, grid):
+def stage2_ids(indptr, Hkv, b, kvh, S, T, grid, cost=PIECE_COST):
     L = indptr[b + 1] - indptr[b]
     if L <= 0:
         return []
@@ -119,7 +120,7 @@ def stage2_ids(indptr, Hkv, b, kvh, S, T, grid):
     if S > 0:
         c = -(-L // S)
         return [sig * S + k for k in range(-(-L // c))]
-    X = piece_cost(len(indptr) - 1, Hkv, grid)
+    X = piece_cost(len(indptr) - 1, Hkv, grid, cost)
     start = Hkv * indptr[b] + kvh * L + X * sig  # the segment's first position's cost
     return [c + sig for c in range(start // T, (start + L - 1) // T + 1)]
 
@@ -136,7 +137,8 @@ def test_plan_invariants_random_batches():
         grid = rng.choice([1, 7, 152, 1024])
         min_chunk = rng.choice([1, 16, 64])
         S_user = rng.choice([0, 0, 0, 1, 3, 8])
-        pieces, S, T = stage1_pieces(indptr, Hkv, grid, min_chunk, S_user)
+        cost = rng.choice([PIECE_COST, PIECE_COST_E4M3])
+        pieces, S, T = stage1_pieces(indptr, Hkv, grid, min_chunk, S_user, cost)
         ids = [p[4] for p in pieces]
         assert len(ids) == len(set(ids))
         cap = B * Hkv * S_user if S_user > 0 else AUTO_MAX_CTAS + B * Hkv
@@ -150,7 +152,7 @@ def test_plan_invariants_random_batches():
         for b in range(B):
             for kvh in range(Hkv):
                 mine = sorted(p[4] for p in pieces if p[0] == b and p[1] == kvh)
-                assert stage2_ids(indptr, Hkv, b, kvh, S, T, grid) == mine
+                assert stage2_ids(indptr, Hkv, b, kvh, S, T, grid, cost) == mine
 
 
 def test_split_rule_on_measured_buckets():
@@ -184,19 +186,20 @@ def test_small_batches_get_one_piece_per_cta():
     assert max(per_cta.values()) - min(per_cta.values()) <= T
     assert max(per_cta.values()) == T
     # more segments than CTAs (a ragged batch of 224): equal cost ranges per CTA; its
-    # positions plus PIECE_COST per piece after its first leave out the parts of a
-    # segment-start gap at either end of its range, at most 2 PIECE_COST
+    # positions plus the piece cost per piece after its first leave out the parts of a
+    # segment-start gap at either end of its range, at most twice the piece cost
     rng = random.Random(3)
     indptr = [0]
     for _ in range(224):
         indptr.append(indptr[-1] + rng.randint(1, 6142))
-    pieces, S, T = stage1_pieces(indptr, 2, 152, 64, 0)
-    cost = {}
-    for b, kvh, j0, j1, pid in pieces:
-        c = pid - (b * 2 + kvh)
-        cost[c] = cost.get(c, -PIECE_COST) + (j1 - j0) + PIECE_COST
-    assert max(cost.values()) - min(cost.values()) <= 2 * PIECE_COST
-    assert max(cost.values()) == T and len(cost) == 152
+    for X in (PIECE_COST, PIECE_COST_E4M3):
+        pieces, S, T = stage1_pieces(indptr, 2, 152, 64, 0, X)
+        cost = {}
+        for b, kvh, j0, j1, pid in pieces:
+            c = pid - (b * 2 + kvh)
+            cost[c] = cost.get(c, -X) + (j1 - j0) + X
+        assert max(cost.values()) - min(cost.values()) <= 2 * X
+        assert max(cost.values()) == T and len(cost) == 152
 
 
 def test_paired_partials_fit_the_workspace():
