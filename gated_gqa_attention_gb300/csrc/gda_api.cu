@@ -74,15 +74,20 @@ struct Layout {
   size_t o_off, lse_off, total;
 };
 
+// Groups of 8 per piece on the MMA kernel: one pass, or teams of two (2 or 4 passes)
+// or three (3 or 5 and more passes: fewer reads of every row than pairs).
+int team_size(int npass) { return npass <= 1 ? 1 : (npass == 2 || npass == 4) ? 2 : 3; }
+
 // Header, then FP32 partial O [pieces][8][D], then partial LSE [pieces][8].  With two
-// or more passes the size covers both schedules: per virtual head, and paired (one
-// piece per KV head and pair of groups holding both groups' partials), which needs
-// 2 num_pieces(B, Hkv * ceil(passes / 2)).
+// or more passes the size covers both schedules: per virtual head, and in teams (one
+// piece per KV head and team of groups holding every group's partial), which needs
+// team num_pieces(B, Hkv * ceil(passes / team)).
 Layout layout(int B, int Hq, int Hkv, int D, int num_splits) {
   const int np = passes(Hq, Hkv);
   size_t pieces = num_pieces(B, Hkv * np, num_splits);
-  if (np >= 2) {
-    const size_t pp = 2 * num_pieces(B, Hkv * ((np + 1) / 2), num_splits);
+  const int t = team_size(np);
+  if (t > 1) {
+    const size_t pp = (size_t)t * num_pieces(B, Hkv * ((np + t - 1) / t), num_splits);
     if (pp > pieces) pieces = pp;
   }
   Layout l;
@@ -207,12 +212,12 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   const int variant = (a->variant == GDA_VARIANT_SIMT)  ? gda::kVariantSimt
                       : (a->variant == GDA_VARIANT_TMA) ? gda::kVariantTma
                                                         : gda::kVariantMma;
-  // G > 8 on the MMA kernel: the groups of 8 query heads in pairs, both groups of a
-  // pair in one piece (one HBM read of the KV head's rows per pair)
-  const bool paired = npass >= 2 && !fp8 && variant == gda::kVariantMma;
-  const int npair = (npass + 1) / 2;
+  // G > 8 on the MMA kernel: the groups of 8 query heads in teams of 2 or 3, every
+  // group of a team in one piece (one HBM read of the KV head's rows per team)
+  const int team = (!fp8 && variant == gda::kVariantMma) ? team_size(npass) : 1;
+  const int nteam = (npass + team - 1) / team;
   // the heads that split the batch into segments for the schedule
-  const long long vheads = paired ? (long long)a->Hkv * npair : (long long)a->Hkv * npass;
+  const long long vheads = (long long)a->Hkv * nteam;
   const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
   const int auto_grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
   int splits = a->num_splits > 0 ? a->num_splits : 0;
@@ -254,8 +259,8 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p1.Hkv = a->Hkv;
   p1.G = a->Hq / a->Hkv;
   p1.npass = npass;
-  p1.paired = paired ? 1 : 0;
-  p1.npair = npair;
+  p1.team = team;
+  p1.nteam = nteam;
   p1.window = a->window;
   // e4m3 pools: k_descale joins the score scale (one rounding, from double)
   p1.scale_log2 = fp8 ? (float)((double)a->scale * (double)a->k_descale * 1.4426950408889634074)
@@ -295,8 +300,8 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p2.Hkv = a->Hkv;
   p2.G = p1.G;
   p2.npass = npass;
-  p2.paired = p1.paired;
-  p2.npair = npair;
+  p2.team = team;
+  p2.nteam = nteam;
   p2.window = a->window;
   p2.num_splits = p1.num_splits;
   p2.grid1 = grid;

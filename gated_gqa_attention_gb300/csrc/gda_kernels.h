@@ -26,9 +26,10 @@ struct Stage1Params {
   int B, Hq, Hkv;
   int G;               // query heads per KV head (Hq / Hkv)
   int npass;           // ceil(G / 8): groups of 8 query heads per KV head ("virtual heads")
-  int paired;          // npass >= 2 on the MMA kernel: the groups go in pairs, one piece per
-                       // (sequence, KV head, pair) serving both groups of the pair
-  int npair;           // ceil(npass / 2): pairs per KV head
+  int team;            // groups per piece: 1, or on the MMA kernel with npass >= 2 the groups
+                       // go in teams of 2 or 3, one piece per (sequence, KV head, team)
+                       // serving every group of the team
+  int nteam;           // ceil(npass / team): teams per KV head
   int window;          // > 0: attend to the last `window` positions only
   float scale_log2;    // scale * log2(e) (e4m3 pools: scale * k_descale * log2(e))
   int num_splits;      // > 0 explicit, else automatic
@@ -50,8 +51,9 @@ struct Stage2Params {
   const float* sinks;  // [Hq] sink logits (natural units), or nullptr
   int B, Hq, Hkv;
   int G, npass, window;
-  int paired;          // stage 1 ran paired: partial (piece, group of the pair) is at piece * 2 + group
-  int npair;           // ceil(npass / 2)
+  int team;            // stage 1's groups per piece: partial (piece, group of the team) is at
+                       // piece * team + group
+  int nteam;           // ceil(npass / team)
   int num_splits;
   int grid1;           // stage-1 grid (automatic-mode chunking)
   int min_chunk;

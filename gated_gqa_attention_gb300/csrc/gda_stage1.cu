@@ -99,7 +99,9 @@ struct MmaSmem {
   unsigned char vring[NWARP][NV][16][kSmemRow];          // per-warp V rings
   float mbuf[NWARP][kG];                                 // each warp's running max
   float lsum[NWARP][kG];                                 // each warp's rescaled sum
-  float4 xs[NG > 1 ? NWARP : 1][2][32];                  // two groups: S^T for the partner warp's group
+  // NG > 1: each warp's S^T of its tile for the other NG - 1 groups of its team
+  // (slot i for group i, or i - 1 past the warp's own group), double-buffered
+  float4 xs[NG > 1 ? NWARP : 1][2][NG > 1 ? NG - 1 : 1][32];
 };
 
 // Lazy-rescale threshold of the MMA softmax, in log2 units.
@@ -183,12 +185,15 @@ struct MmaWarpState {
     l1 += __uint_as_float(P0 & 0xFFFF0000u) + __uint_as_float(P1 & 0xFFFF0000u);
   }
 
-  // Unscaled S^T of the register K tile against both groups' Q^T fragments (one
+  // Unscaled S^T of the register K tile against the Q^T fragments of NG groups (one
   // A fragment, two MMA chains per group; the same summation order as qk_softmax).
-  __device__ __forceinline__ void qk_raw2(const uint2 (*qa)[32], const uint2 (*qb)[32], float* sa_out,
-                                          float* sb_out, int lane) {
-    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-    float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
+  template <int NG>
+  __device__ __forceinline__ void qk_rawN(const uint2 (*const qf)[16][32], float (*s_out)[4], int lane) {
+    float a[NG][2][4];
+#pragma unroll
+    for (int x = 0; x < NG; ++x)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[x][0][i] = a[x][1][i] = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
       const int c = kk >> 1, h = kk & 1;
@@ -196,34 +201,34 @@ struct MmaWarpState {
       const uint4& r1 = kr[8 + c];
       const uint32_t x0 = h ? r0.z : r0.x, x2 = h ? r0.w : r0.y;
       const uint32_t x1 = h ? r1.z : r1.x, x3 = h ? r1.w : r1.y;
-      const uint2 fa = qa[kk][lane], fb = qb[kk][lane];
-      mma_bf16_16816(h ? a1 : a0, x0, x1, x2, x3, fa.x, fa.y);
-      mma_bf16_16816(h ? b1 : b0, x0, x1, x2, x3, fb.x, fb.y);
+#pragma unroll
+      for (int x = 0; x < NG; ++x) {
+        const uint2 f = qf[x][kk][lane];
+        mma_bf16_16816(a[x][h], x0, x1, x2, x3, f.x, f.y);
+      }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      sa_out[i] = a0[i] + a1[i];
-      sb_out[i] = b0[i] + b1[i];
-    }
+    for (int x = 0; x < NG; ++x)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s_out[x][i] = a[x][0][i] + a[x][1][i];
   }
 
-  // Online softmax over two 16-token tiles of the same 8 heads: s (na valid rows)
-  // and u (nb valid rows), both unscaled.  Same lazy rescale as qk_softmax; returns
-  // the BF16 P fragments of each tile and adds their rounded values to the sums.
-  __device__ __forceinline__ void softmax2(float* s, int na, float* u, int nb, float sl2, int lane,
-                                           uint32_t& A0, uint32_t& A1, uint32_t& B0, uint32_t& B1) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      s[i] *= sl2;
-      u[i] *= sl2;
-    }
+  // Online softmax over NT 16-token tiles of the same 8 heads: tile x has n[x] valid
+  // rows and unscaled scores s[x].  Same lazy rescale as qk_softmax; returns the BF16 P
+  // fragments of each tile and adds their rounded values to the sums, tile by tile.
+  template <int NT>
+  __device__ __forceinline__ void softmaxN(float (*s)[4], const int* n, float sl2, int lane, uint32_t (*P)[2]) {
     const int tg = lane >> 2;
-    if (tg >= na) s[0] = s[1] = -INFINITY;
-    if (tg + 8 >= na) s[2] = s[3] = -INFINITY;
-    if (tg >= nb) u[0] = u[1] = -INFINITY;
-    if (tg + 8 >= nb) u[2] = u[3] = -INFINITY;
-    float xa = fmaxf(fmaxf(s[0], s[2]), fmaxf(u[0], u[2]));
-    float xb = fmaxf(fmaxf(s[1], s[3]), fmaxf(u[1], u[3]));
+    float xa = -INFINITY, xb = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < NT; ++x) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[x][i] *= sl2;
+      if (tg >= n[x]) s[x][0] = s[x][1] = -INFINITY;
+      if (tg + 8 >= n[x]) s[x][2] = s[x][3] = -INFINITY;
+      xa = fmaxf(xa, fmaxf(s[x][0], s[x][2]));
+      xb = fmaxf(xb, fmaxf(s[x][1], s[x][3]));
+    }
     const bool grow = xa > m0 + kLazyLog2 || xb > m1 + kLazyLog2;
     if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
@@ -245,14 +250,16 @@ struct MmaWarpState {
         o[i][3] *= ab;
       }
     }
-    A0 = pack_bf16x2(safe_exp2_diff(s[0], m0), safe_exp2_diff(s[1], m1));
-    A1 = pack_bf16x2(safe_exp2_diff(s[2], m0), safe_exp2_diff(s[3], m1));
-    B0 = pack_bf16x2(safe_exp2_diff(u[0], m0), safe_exp2_diff(u[1], m1));
-    B1 = pack_bf16x2(safe_exp2_diff(u[2], m0), safe_exp2_diff(u[3], m1));
-    l0 += __uint_as_float(A0 << 16) + __uint_as_float(A1 << 16) + __uint_as_float(B0 << 16) +
-          __uint_as_float(B1 << 16);
-    l1 += __uint_as_float(A0 & 0xFFFF0000u) + __uint_as_float(A1 & 0xFFFF0000u) +
-          __uint_as_float(B0 & 0xFFFF0000u) + __uint_as_float(B1 & 0xFFFF0000u);
+    float la = 0.0f, lb = 0.0f;
+#pragma unroll
+    for (int x = 0; x < NT; ++x) {
+      P[x][0] = pack_bf16x2(safe_exp2_diff(s[x][0], m0), safe_exp2_diff(s[x][1], m1));
+      P[x][1] = pack_bf16x2(safe_exp2_diff(s[x][2], m0), safe_exp2_diff(s[x][3], m1));
+      la += __uint_as_float(P[x][0] << 16) + __uint_as_float(P[x][1] << 16);
+      lb += __uint_as_float(P[x][0] & 0xFFFF0000u) + __uint_as_float(P[x][1] & 0xFFFF0000u);
+    }
+    l0 += la;
+    l1 += lb;
   }
 
   // O^T += V^T P^T with V^T fragments from a 16-row shared-memory tile
@@ -298,37 +305,37 @@ __device__ __forceinline__ void issue_v_tile(unsigned char* stage, const unsigne
   cp_async_commit();
 }
 
-// PAIR (G > 8: the groups of 8 query heads of a KV head in pairs): one piece per
-// (sequence, KV head, pair) serves both groups of the pair, and every K/V row is
-// loaded once per pair (once for G = 9..16, twice for G = 17..32).
-// Warp w loads tiles w + NWARP*k as without PAIR and computes S^T of its tile for
-// both groups (one K fragment, two MMA chains); warps w and w ^ NWARP/2 form a
-// pair, the first half of the warps owning group 0 and the second half group 1.
-// Each step a warp leaves the partner group's S^T in shared memory, the pair meets
-// at a named barrier, and each warp then runs the softmax and PV of its own group
-// over both tiles: its own (its V ring) and the partner's (the partner's V ring).
-// The partial of (piece, group) is written at piece * 2 + group.  Without PAIR,
-// one piece per (sequence, virtual head).
-template <int NWARP, int NV, bool PAIR>
+// Teams (NG > 1, G > 8: the groups of 8 query heads of a KV head in teams of NG):
+// one piece per (sequence, KV head, team) serves the NG groups of the team, and every
+// K/V row is loaded once per team (NG = 2: once for G = 9..16; NG = 3: once for
+// G = 17..24).  Warp w loads tiles w + NWARP*k as with NG = 1 and computes S^T of its
+// tile for all NG groups (one K fragment, NG MMA chains).  Warp w is member w / WPG
+// of team w % WPG and owns group w / WPG.  Each step a warp leaves the other groups'
+// S^T in shared memory, the team meets at a named barrier, and each warp then runs
+// the softmax and PV of its own group over the team's NG tiles: its own (its V ring)
+// and its partners' (their V rings).  The partial of (piece, group) is written at
+// piece * NG + group.  With NG = 1, one piece per (sequence, virtual head).
+template <int NWARP, int NV, int NG>
 __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params p) {
-  constexpr int NG = PAIR ? 2 : 1;  // query-head groups per piece
-  constexpr int WPG = NWARP / NG;   // warps per group
+  constexpr bool TEAM = NG > 1;
+  constexpr int WPG = NWARP / NG;        // warps per group (= teams per CTA)
+  constexpr int QPT = NG * 16 / NWARP;   // Q^T fragments per thread
   using Smem = MmaSmem<NWARP, NV, NG>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = warp / WPG;                 // this warp's group
-  const int partner = warp ^ (NWARP / 2);     // PAIR: the warp of the other group on the same tiles
-  static_assert(NG * 16 * 32 == 2 * NG * NWARP * 32, "2 NG Q fragments per thread");
-  static_assert(!PAIR || NWARP == 8, "PAIR: four pairs, named barriers 1 .. 4");
+  const int grp = warp / WPG;   // this warp's group (its member index in the team)
+  const int team = warp % WPG;  // its team: warps team + WPG * j, j = 0 .. NG - 1
+  static_assert(NWARP % NG == 0 && (NG * 16) % NWARP == 0, "whole teams, whole Q fragments per thread");
+  static_assert(WPG <= 15, "named barriers 1 .. WPG");
 
   Sched sched;
-  sched.begin(p.indptr, p.B, PAIR ? p.Hkv * p.npair : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x,
+  sched.begin(p.indptr, p.B, TEAM ? p.Hkv * p.nteam : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x,
               p.min_chunk, p.window, p.piece_cost);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
   const uint64_t pol_v = l2_policy_evict_first();
-  // KV head of a piece (with PAIR the scheduled head is kvh * npair + the pair)
-  auto kv_head = [&](const Piece& pp) -> int { return PAIR ? pp.kvh / p.npair : pp.kvh / p.npass; };
+  // KV head of a piece (in teams the scheduled head is kvh * nteam + the team)
+  auto kv_head = [&](const Piece& pp) -> int { return TEAM ? pp.kvh / p.nteam : pp.kvh / p.npass; };
 
   // Warp w's tiles of a piece of `len` positions: tile w + NWARP*k.
   auto nmine_for = [&](int w, int len) -> int {
@@ -354,24 +361,24 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
   };
 
   MmaWarpState st;
-  uint2 qfrag[2 * NG];
+  uint2 qfrag[QPT];
   int s0 = -1, s1 = -1, s2 = -1;
   // Head of a piece: its Q^T fragments (requested first), the slots of this
   // warp's first three tiles and the K rows of its first tile.  For every piece
   // after the first this runs before the previous piece's merge, so the loads
   // are in flight while the warps merge.
   auto piece_head = [&](const Piece& pp) {
-    // PAIR: the piece's KV head and the first group of its pair
-    const int pkv = PAIR ? pp.kvh / p.npair : 0, pg0 = PAIR ? 2 * (pp.kvh - pkv * p.npair) : 0;
+    // teams: the piece's KV head and the first group of its team
+    const int pkv = TEAM ? pp.kvh / p.nteam : 0, pg0 = TEAM ? NG * (pp.kvh - pkv * p.nteam) : 0;
 #pragma unroll
-    for (int r = 0; r < 2 * NG; ++r) {
+    for (int r = 0; r < QPT; ++r) {
       const int e = threadIdx.x + r * NWARP * 32;
       const int fg = e >> 9, kk = (e >> 5) & 15, ln = e & 31;  // group, k-step, lane
       int gv;
       const __nv_bfloat16* qg;
-      if (PAIR) {
-        // group 2 * pair + fg of the KV head; past the last group (odd npass) the group
-        // is empty: its Q is zero and its partial is never read
+      if (TEAM) {
+        // group NG * team + fg of the KV head; past the last group (npass not a
+        // multiple of NG) the group is empty: its Q is zero and its partial is never read
         const int gi = pg0 + fg;
         qg = group_q(p, pp.b, pkv * p.npass + min(gi, p.npass - 1), &gv);
         if (gi >= p.npass) gv = 0;
@@ -408,9 +415,9 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
 
     st.reset();  // O, max and sum; the K rows of tile 0 are already in flight
     unsigned char(*ring)[16][kSmemRow] = sm.vring[warp];
-    // steps of this warp's loop: its tiles, or with PAIR those of the pair's first
-    // warp (the one with more tiles), so that both partners meet at every barrier
-    const int nsteps = PAIR ? nmine_for(warp & (NWARP / 2 - 1), len) : nmine;
+    // steps of this warp's loop: its tiles, or in teams those of the team's first
+    // warp (the one with the most tiles), so that all members meet at every barrier
+    const int nsteps = TEAM ? nmine_for(team, len) : nmine;
     if (nsteps > 0) {
       issue_v_tile(&ring[0][0][0], vb, stride, s0, tile_n(0, len, nmine), lane, pol_v);
       issue_v_tile(&ring[1 % NV][0][0], vb, stride, s1, tile_n(1, len, nmine), lane, pol_v);
@@ -418,40 +425,75 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
     }
     // the previous piece's merge ended with a barrier: the fragment buffer is free
 #pragma unroll
-    for (int r = 0; r < 2 * NG; ++r) {
+    for (int r = 0; r < QPT; ++r) {
       const int e = threadIdx.x + r * NWARP * 32;
       sm.qf[e >> 9][(e >> 5) & 15][e & 31] = qfrag[r];
     }
     __syncthreads();
 
     int stage = 0;
-    if constexpr (PAIR) {
-      unsigned char(*pring)[16][kSmemRow] = sm.vring[partner];
-      const int nmp = nmine_for(partner, len);
-      const int bar = 1 + (warp & (NWARP / 2 - 1));
+    if constexpr (TEAM) {
+      // tile x of a step: x = 0 this warp's own, then its partners in member order
+      int pw[NG];  // warp of tile x
+      int nmp[NG];
+#pragma unroll
+      for (int x = 0; x < NG; ++x) {
+        const int j = (x == 0) ? grp : (x - 1 < grp ? x - 1 : x);
+        pw[x] = team + WPG * j;
+        nmp[x] = nmine_for(pw[x], len);
+      }
+      const int bar = 1 + team;
       for (int k = 0; k < nsteps; ++k) {
-        // K rows of tile k+2 into L2 and the slots of tile k+3; tile k's S^T for both
-        // groups (the partner's group to shared memory); the K rows of tile k+1
+        // K rows of tile k+2 into L2 and the slots of tile k+3; tile k's S^T for all
+        // groups (the other groups' to shared memory); the K rows of tile k+1
         prefetch_k_tile(kb, stride, s2, lane);
         const int s3 = fetch(idx, k + 3, len, nmine);
         const int nown = tile_n(k, len, nmine);
-        float so[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
-        if (nown > 0) st.qk_raw2(sm.qf[grp], sm.qf[grp ^ 1], so, sx, lane);
-        sm.xs[warp][k & 1][lane] = make_float4(sx[0], sx[1], sx[2], sx[3]);
+        float sg[NG][4];
+#pragma unroll
+        for (int x = 0; x < NG; ++x) sg[x][0] = sg[x][1] = sg[x][2] = sg[x][3] = 0.0f;
+        if (nown > 0) st.qk_rawN<NG>(sm.qf, sg, lane);
+#pragma unroll
+        for (int i = 0; i < NG; ++i)
+          if (i != grp) sm.xs[warp][k & 1][i < grp ? i : i - 1][lane] = make_float4(sg[i][0], sg[i][1], sg[i][2], sg[i][3]);
         if (k + 1 < nmine) st.load_k(kb, stride, s1, lane);
         cp_async_wait<1>();  // this warp's V tile k has landed (tile k+1 may be in flight)
-        // The pair meets: both V tiles k and both S^T are visible, and the partner
-        // has finished step k-1, so ring stage (k+2) % NV (read as stage (k-1) % NV)
-        // and the S^T buffer of step k+2 are free.
-        named_bar_sync(bar, 64);
+        // The team meets: all V tiles k and all S^T are visible, and every member has
+        // finished step k-1, so ring stage (k+2) % NV (read as stage (k-1) % NV) and
+        // the S^T buffer of step k+2 are free.
+        named_bar_sync(bar, NG * 32);
         issue_v_tile(&ring[(k + 2) % NV][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
-        const float4 sp = sm.xs[partner][k & 1][lane];
-        float su[4] = {sp.x, sp.y, sp.z, sp.w};
-        const int npar = tile_n_for(partner, k, len, nmp);
-        uint32_t A0, A1, B0, B1;
-        st.softmax2(so, nown, su, npar, p.scale_log2, lane, A0, A1, B0, B1);
-        if (nown > 0) st.pv_with(&ring[stage][0][0], A0, A1, lane);
-        if (npar > 0) st.pv_with(&pring[stage][0][0], B0, B1, lane);
+        float sc[NG][4];
+        int nt[NG];
+#pragma unroll
+        for (int x = 0; x < NG; ++x) {
+          if (x == 0) {
+            // this warp's group's S^T (a select per group: no dynamic register index)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[0][i] = sg[0][i];
+#pragma unroll
+            for (int y = 1; y < NG; ++y)
+              if (grp == y) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[0][i] = sg[y][i];
+              }
+            nt[0] = nown;
+          } else {
+            // the partner's slot for this warp's group
+            const int j = pw[x] / WPG;
+            const float4 sp = sm.xs[pw[x]][k & 1][grp < j ? grp : grp - 1][lane];
+            sc[x][0] = sp.x;
+            sc[x][1] = sp.y;
+            sc[x][2] = sp.z;
+            sc[x][3] = sp.w;
+            nt[x] = tile_n_for(pw[x], k, len, nmp[x]);
+          }
+        }
+        uint32_t P[NG][2];
+        st.softmaxN<NG>(sc, nt, p.scale_log2, lane, P);
+#pragma unroll
+        for (int x = 0; x < NG; ++x)
+          if (nt[x] > 0) st.pv_with(&sm.vring[pw[x]][stage][0][0], P[x][0], P[x][1], lane);
         stage = (stage + 1 == NV) ? 0 : stage + 1;
         s1 = s2;
         s2 = s3;
@@ -806,10 +848,10 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
 
 cudaError_t launch_stage1_tma(const Stage1Params& p, int grid, cudaStream_t stream);
 
-template <int NWARP, int NV, bool PAIR>
+template <int NWARP, int NV, int NG>
 cudaError_t launch_mma(const Stage1Params& p, int grid, cudaStream_t stream) {
-  using Smem = MmaSmem<NWARP, NV, PAIR ? 2 : 1>;
-  auto kern = stage1_mma_kernel<NWARP, NV, PAIR>;
+  using Smem = MmaSmem<NWARP, NV, NG>;
+  auto kern = stage1_mma_kernel<NWARP, NV, NG>;
   static std::atomic<bool> attr_set[64];  // zero-initialised: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -831,7 +873,10 @@ cudaError_t launch_stage1(const Stage1Params& p, int variant, int grid, cudaStre
     return cudaGetLastError();
   }
   constexpr int kW = 8, kNV = 3;
-  return p.paired ? launch_mma<kW, kNV, true>(p, grid, stream) : launch_mma<kW, kNV, false>(p, grid, stream);
+  // teams of three groups run on 6 warps (two teams per CTA)
+  return p.team == 3   ? launch_mma<6, kNV, 3>(p, grid, stream)
+         : p.team == 2 ? launch_mma<kW, kNV, 2>(p, grid, stream)
+                       : launch_mma<kW, kNV, 1>(p, grid, stream);
 }
 
 }  // namespace gda

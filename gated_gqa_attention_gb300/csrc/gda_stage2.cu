@@ -36,14 +36,14 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, h = bh % p.Hq;
   // query head h belongs to KV head h / G; its slot g in group `pass` (groups of 8).
-  // Stage 1 scheduled pieces per virtual head vh = kvh * npass + pass, or, paired,
-  // per (KV head, pair of groups) kvh * npair + pass / 2 with the partial of (piece,
-  // group of the pair) at piece * 2 + pass % 2.
+  // Stage 1 scheduled pieces per (KV head, team of `team` groups) kvh * nteam +
+  // pass / team, with the partial of (piece, group of the team) at piece * team +
+  // pass % team (team = 1: per virtual head kvh * npass + pass).
   const int kvh = h / p.G, r = h - kvh * p.G;
   const int pass = r / kG, g = r % kG;
-  const int sched_h = p.paired ? kvh * p.npair + (pass >> 1) : kvh * p.npass + pass;
-  const int sched_n = p.paired ? p.Hkv * p.npair : p.Hkv * p.npass;
-  const int id_mul = p.paired ? 2 : 1, id_add = p.paired ? (pass & 1) : 0;
+  const int sched_h = kvh * p.nteam + pass / p.team;
+  const int sched_n = p.Hkv * p.nteam;
+  const int id_mul = p.team, id_add = pass % p.team;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the next call's one-kernel decode (a programmatic dependent) may launch and set up
   // now; it waits for this grid before it reads anything

@@ -106,15 +106,17 @@ def test_window_on_the_ragged_workload(gda):
     check_close(got[idx], ref.out[idx])
 
 
-# G > 8 on the MMA kernel: the groups of 8 query heads go in pairs; one piece per
-# (sequence, KV head, pair) serves both groups of the pair, half of the CTA's warps
-# each, and stage 2 reads the partial of (piece, group of the pair) at piece * 2 +
-# group.  G = 24 and G = 56 have an odd number of groups (the last pair's second group
-# is empty).  Long ragged batches make pieces cross sequences and CTAs; a window,
-# sinks, the LSE and explicit splits go through the same mapping.  The TMA variant (3)
-# runs the same case per virtual head.
-@pytest.mark.parametrize("hq,hkv", [(32, 2), (20, 2), (16, 1), (30, 3), (48, 2), (64, 2), (56, 1)])
-def test_paired_groups_long_ragged(gda, hq, hkv):
+# G > 8 on the MMA kernel: the groups of 8 query heads go in teams (pairs for 2 or 4
+# groups on 8 warps, threes otherwise on 6 warps); one piece per (sequence, KV head,
+# team) serves every group of the team, a share of the CTA's warps each, and stage 2
+# reads the partial of (piece, group of the team) at piece * team + group.  G = 20 and
+# G = 24 are one three; G = 40 (5 groups) and G = 56 (7 groups) leave the last three
+# with empty groups; G = 32 is two pairs.  Long ragged batches make pieces cross
+# sequences and CTAs; a window, sinks, the LSE and explicit splits go through the same
+# mapping.  The TMA variant (3) runs the same case per virtual head.
+@pytest.mark.parametrize("hq,hkv", [(32, 2), (20, 2), (16, 1), (30, 3), (40, 2), (48, 2), (24, 1), (64, 2),
+                                    (80, 2), (56, 1)])
+def test_team_groups_long_ragged(gda, hq, hkv):
     lens = [4096, 1, 0, 3000, 777, 65, 2049, 16, 5000, 129, 1500, 2]
     inp = workloads.make(lens, seed=500 + hq + hkv, hq=hq, hkv=hkv, layout="perm", pool_slots=20000,
                          peaky_frac=0.01)
@@ -129,9 +131,9 @@ def test_paired_groups_long_ragged(gda, hq, hkv):
 
 
 @pytest.mark.parametrize("hq", [32, 48])
-def test_paired_groups_workload_sample(gda, hq):
-    # b64_l4096's lengths with Hq = 32 or 48, Hkv = 2 (G = 16: one pair; G = 24: a pair
-    # and a half-empty pair), sampled (sequence, head) pairs
+def test_team_groups_workload_sample(gda, hq):
+    # b64_l4096's lengths with Hq = 32 or 48, Hkv = 2 (G = 16: one pair; G = 24: one
+    # three), sampled (sequence, head) pairs
     inp = workloads.make([4096] * 64, seed=77, hq=hq, hkv=2, layout="perm", pool_slots=64 * 4096 + 1000)
     heads = sorted({0, 7, 8, 15, 16, hq // 2 - 1, hq // 2, hq - 9, hq - 8, hq - 1})
     pairs = np.array([(b, h) for b in range(0, 64, 9) for h in heads])
@@ -141,10 +143,11 @@ def test_paired_groups_workload_sample(gda, hq):
     check_close(got[idx], ref.out[idx])
 
 
-def test_paired_groups_deterministic_and_placement_invariant(gda):
-    # the paired kernel merges the four warps of a group in a fixed order: repeated
-    # calls and a permuted pool (same rows at other slots) give the same bits
-    inp = workloads.make([4096, 700, 1, 2500], seed=611, hq=32, hkv=2, layout="perm", pool_slots=9000)
+@pytest.mark.parametrize("hq", [32, 48])
+def test_team_groups_deterministic_and_placement_invariant(gda, hq):
+    # the team kernel merges the warps of a group in a fixed order: repeated calls and
+    # a permuted pool (same rows at other slots) give the same bits
+    inp = workloads.make([4096, 700, 1, 2500], seed=611, hq=hq, hkv=2, layout="perm", pool_slots=9000)
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     n = inp["k_pool"].shape[0]
     perm = torch.randperm(n, generator=torch.Generator().manual_seed(3))
@@ -159,9 +162,10 @@ def test_paired_groups_deterministic_and_placement_invariant(gda):
         assert np.array_equal(a, b) and np.array_equal(a, c)
 
 
-def test_paired_groups_check_indices(gda):
-    inp = workloads.make([300, 200], seed=612, hq=32, hkv=2, layout="perm", pool_slots=600)
-    ws = torch.empty(gda.workspace_bytes(2, 32, 2, 256, 0), dtype=torch.uint8, device="cuda")
+@pytest.mark.parametrize("hq", [32, 48])
+def test_team_groups_check_indices(gda, hq):
+    inp = workloads.make([300, 200], seed=612, hq=hq, hkv=2, layout="perm", pool_slots=600)
+    ws = torch.empty(gda.workspace_bytes(2, hq, 2, 256, 0), dtype=torch.uint8, device="cuda")
     gda.workspace_init(ws)
     run(gda, inp, workspace=ws, check_indices=True)
     assert gda.read_error(ws) == 0
@@ -172,13 +176,15 @@ def test_paired_groups_check_indices(gda):
     assert gda.read_error(ws) & gda.DEVERR_INDEX
 
 
-def test_paired_groups_caller_workspace_sizes(gda):
-    # the caller-sized workspace (workspace_bytes) holds the paired schedule's
-    # partials in automatic and explicit-split modes, with a window too
+@pytest.mark.parametrize("hq", [24, 48, 80])
+def test_team_groups_caller_workspace_sizes(gda, hq):
+    # the caller-sized workspace (workspace_bytes) holds the team schedule's partials
+    # (pairs at G = 12, threes at G = 24 and 40) in automatic and explicit-split modes,
+    # with a window too
     lens = [1, 4096, 33, 2000, 0, 5000, 65]
-    inp = workloads.make(lens, seed=613, hq=24, hkv=2, layout="perm", pool_slots=12000)
+    inp = workloads.make(lens, seed=613, hq=hq, hkv=2, layout="perm", pool_slots=12000)
     for splits, window in ((0, 0), (3, 0), (0, 700)):
-        ws = torch.empty(gda.workspace_bytes(len(lens), 24, 2, 256, splits), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(gda.workspace_bytes(len(lens), hq, 2, 256, splits), dtype=torch.uint8, device="cuda")
         gda.workspace_init(ws)
         ref = reference(inp, window=window)
         check_close(run(gda, inp, workspace=ws, num_splits=splits, window=window), ref.out)

@@ -202,11 +202,30 @@ def test_small_batches_get_one_piece_per_cta():
         assert max(cost.values()) == T and len(cost) == 152
 
 
-def test_paired_partials_fit_the_workspace():
+def team_size(npass):
+    """Groups of 8 per piece on the MMA kernel: 1 for one pass, pairs for 2 or 4
+    passes, threes otherwise (3 passes: one read instead of two; 5 .. 6: two instead of
+    three)."""
+    return 1 if npass <= 1 else 2 if npass in (2, 4) else 3
+
+
+def test_team_size_reads_every_row_fewest_times():
+    # reads of every K/V row per KV head = ceil(npass / team); teams of three never
+    # read more often than pairs, and pairs are kept where they read as rarely
+    for npass in range(1, 17):
+        t = team_size(npass)
+        reads = -(-npass // t)
+        assert reads == min(-(-npass // 2), -(-npass // 3)) or npass == 1
+        if npass in (2, 4):
+            assert t == 2 and reads == -(-npass // 3)
+    assert [-(-n // team_size(n)) for n in (2, 3, 4, 5, 6, 7)] == [1, 1, 2, 2, 2, 3]
+
+
+def test_team_partials_fit_the_workspace():
     # G > 8 on the MMA kernel: the npass groups of 8 query heads of a KV head go in
-    # npair = ceil(npass / 2) pairs; pieces are scheduled per (sequence, KV head, pair)
-    # and the partial of (piece, group of the pair) sits at piece * 2 + group.  The
-    # workspace holds max(2 x the pieces of that schedule, the pieces of the
+    # nteam = ceil(npass / team) teams; pieces are scheduled per (sequence, KV head,
+    # team) and the partial of (piece, group of the team) sits at piece * team + group.
+    # The workspace holds max(team x the pieces of that schedule, the pieces of the
     # per-virtual-head schedule of the other kernels); stage 2 finds exactly stage 1's
     # slots for every query-head group.
     rng = random.Random(11)
@@ -217,61 +236,66 @@ def test_paired_partials_fit_the_workspace():
         for L in lens:
             indptr.append(indptr[-1] + L)
         Hkv = rng.choice([1, 2, 4])
-        npass = rng.choice([2, 2, 3, 4, 7])
-        npair = (npass + 1) // 2
+        npass = rng.choice([2, 2, 3, 3, 4, 5, 7])
+        team = team_size(npass)
+        nteam = -(-npass // team)
         grid = rng.choice([7, 152, 1024])
         S_user = rng.choice([0, 0, 2, 8])
-        heads = Hkv * npair
+        heads = Hkv * nteam
         pieces, S, T = stage1_pieces(indptr, heads, grid, 64, S_user)
         num_pieces = lambda vh: B * vh * S_user if S_user > 0 else AUTO_MAX_CTAS + B * vh
-        cap = max(2 * num_pieces(heads), num_pieces(Hkv * npass))
-        slots = [p[4] * 2 + g for p in pieces for g in (0, 1)]
+        cap = max(team * num_pieces(heads), num_pieces(Hkv * npass))
+        slots = [p[4] * team + g for p in pieces for g in range(team)]
         assert len(slots) == len(set(slots)) and all(0 <= s < cap for s in slots)
         for b in range(B):
             for kvh in range(Hkv):
                 for gp in range(npass):  # query-head group gp of KV head kvh
-                    sched_h, g = kvh * npair + gp // 2, gp % 2
-                    want = sorted(p[4] * 2 + g for p in pieces if p[0] == b and p[1] == sched_h)
-                    assert [i * 2 + g for i in stage2_ids(indptr, heads, b, sched_h, S, T, grid)] == want
+                    sched_h, g = kvh * nteam + gp // team, gp % team
+                    want = sorted(p[4] * team + g for p in pieces if p[0] == b and p[1] == sched_h)
+                    assert [i * team + g for i in stage2_ids(indptr, heads, b, sched_h, S, T, grid)] == want
 
 
-def test_paired_kernel_tile_arithmetic():
-    # The paired stage-1 loop (G = 9 .. 16, 8 warps): warp w loads tiles w + 8k of a
-    # piece (16 positions each); warps w and w ^ 4 are partners; both run the step
-    # count of the pair's first warp (w & 3), and at step k warp w takes its own tile
-    # (when k < its tile count) and its partner's (when k < the partner's count) for
-    # its own group (w // 4).  Every tile is loaded once, every group sees every tile
-    # once, and the shared step count covers both partners' tiles.
-    NW = 8
+def test_team_kernel_tile_arithmetic():
+    # The team stage-1 loop (NG groups per piece on NW warps: pairs on 8, threes on 6):
+    # warp w loads tiles w + NW k of a piece (16 positions each); it is member w // WPG
+    # of team w % WPG (WPG = NW / NG) and owns group w // WPG.  All members run the
+    # step count of the team's first warp (w % WPG), and at step k warp w takes its own
+    # tile and each partner's (when k < that warp's tile count) for its own group.
+    # Every tile is loaded once, every group sees every tile once, and the shared step
+    # count covers all members' tiles.
+    for NW, NG in ((8, 2), (6, 3)):
+        WPG = NW // NG
 
-    def nmine(w, length):
-        ntiles = (length + 15) // 16
-        return (ntiles - w + NW - 1) // NW if ntiles > w else 0
+        def nmine(w, length):
+            ntiles = (length + 15) // 16
+            return (ntiles - w + NW - 1) // NW if ntiles > w else 0
 
-    def tile_n(w, k, length):
-        return min(16, length - 16 * (w + NW * k)) if k < nmine(w, length) else 0
+        def tile_n(w, k, length):
+            return min(16, length - 16 * (w + NW * k)) if k < nmine(w, length) else 0
 
-    for length in list(range(0, 700)) + [1023, 1024, 1025, 4096, 3449, 5000]:
-        ntiles = (length + 15) // 16
-        loaded = [0] * ntiles
-        seen = {0: [0] * ntiles, 1: [0] * ntiles}
-        positions = {0: 0, 1: 0}
-        for w in range(NW):
-            partner, grp = w ^ 4, w // 4
-            steps = nmine(w & 3, length)
-            assert steps >= nmine(w, length) and steps >= nmine(partner, length)
-            assert steps == nmine(partner & 3, length)  # both partners meet at every barrier
-            for k in range(nmine(w, length)):
-                loaded[w + NW * k] += 1
-            for k in range(steps):
-                for owner in (w, partner):
-                    n = tile_n(owner, k, length)
-                    if n > 0:
-                        seen[grp][owner + NW * k] += 1
-                        positions[grp] += n
-        assert loaded == [1] * ntiles
-        assert seen[0] == [1] * ntiles and seen[1] == [1] * ntiles
-        assert positions[0] == positions[1] == length
+        for length in list(range(0, 700)) + [1023, 1024, 1025, 4096, 3449, 5000]:
+            ntiles = (length + 15) // 16
+            loaded = [0] * ntiles
+            seen = {g: [0] * ntiles for g in range(NG)}
+            positions = {g: 0 for g in range(NG)}
+            for w in range(NW):
+                team, grp = w % WPG, w // WPG
+                members = [team + WPG * j for j in range(NG)]
+                # tile order of a step: own first, then the partners in member order
+                order = [w] + [m for m in members if m != w]
+                steps = nmine(team, length)
+                assert all(steps >= nmine(m, length) for m in members)
+                for k in range(nmine(w, length)):
+                    loaded[w + NW * k] += 1
+                for k in range(steps):
+                    for owner in order:
+                        n = tile_n(owner, k, length)
+                        if n > 0:
+                            seen[grp][owner + NW * k] += 1
+                            positions[grp] += n
+            assert loaded == [1] * ntiles
+            assert all(seen[g] == [1] * ntiles for g in range(NG))
+            assert all(positions[g] == length for g in range(NG))
 
 
 def test_cluster_kernel_partition_and_merge_slots():
