@@ -138,7 +138,7 @@ int host_uniform_splits(long long B, long long heads, long long grid, int min_ch
   if (heads * n >= (long long)gda::kStreamMinPerCta * grid) return 0;
   if (4 * lmax * B > 5 * n) return 0;
   long long s_opt = 1;
-  while (16 * s_opt * s_opt <= lmax) s_opt *= 2;
+  while (4 * s_opt * s_opt <= lmax) s_opt *= 2;
   const long long s_len = lmax > 0 ? (lmax + min_chunk - 1) / min_chunk : 1;
   long long s = s_opt < s_len ? s_opt : s_len;
   const long long s_wave = grid / units1;

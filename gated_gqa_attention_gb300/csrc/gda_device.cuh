@@ -403,9 +403,9 @@ struct Sched {
   // The rule comes from split sweeps on GB300 (equal lengths, B = 1 .. 128, L = 512
   // .. 32768, every S in 1 .. 128):
   //  * a call costs about a + b L/S (stage 1, one piece per CTA) + c S (stage 2
-  //    merges S partials per head), c/b ~ 8 positions, so the best S is near
-  //    sqrt(lmax / 8): S_opt, the smallest power of two with 16 S^2 > lmax, and at
-  //    most ceil(lmax / min_chunk);
+  //    merges S partials per head), c/b ~ 2 positions (stage 2 keeps four partials'
+  //    loads in flight), so the best S is near sqrt(lmax / 2): S_opt, the smallest
+  //    power of two with 4 S^2 > lmax, and at most ceil(lmax / min_chunk);
   //  * at most one wave of CTAs (B Hkv S <= grid); when the wave bounds S, the
   //    power of two below the bound if it keeps >= 80 % of the CTAs busy (pieces
   //    aligned to the warps' tiles), else the bound itself, and with < 80 % busy
@@ -434,9 +434,9 @@ struct Sched {
     if ((long long)Hkv * n >= (long long)kStreamMinPerCta * grid) return 0;
     if (4LL * lmax * B > 5LL * n) return 0;
     // (closed forms, short dependent chains: every CTA's start waits on this)
-    // s_opt: the smallest power of two p with 16 p^2 > lmax, 2^max(0, (h - 2) / 2)
-    // with h the index of lmax's top bit
-    const int s_opt = (lmax > 0) ? (1 << max(0, (31 - __clz(lmax) - 2) / 2)) : 1;
+    // s_opt: the smallest power of two p with 4 p^2 > lmax, 2^(h / 2) with h the index
+    // of lmax's top bit
+    const int s_opt = (lmax > 0) ? (1 << ((31 - __clz(lmax)) >> 1)) : 1;
     const int s_len = max(1, (lmax + min_chunk - 1) / min_chunk);
     int s = min(s_opt, s_len);
     const int s_wave = grid / units1;

@@ -29,7 +29,7 @@ def uniform_splits(indptr, Hkv, grid, min_chunk):
     if Hkv * n >= STREAM_MIN_PER_CTA * grid or 4 * lmax * B > 5 * n:
         return 0
     s_opt = 1
-    while 16 * s_opt * s_opt <= lmax:
+    while 4 * s_opt * s_opt <= lmax:
         s_opt *= 2
     s = min(s_opt, max(1, -(-lmax // min_chunk)))
     s_wave = grid // units1
@@ -158,7 +158,7 @@ def test_plan_invariants_random_batches():
 def test_split_rule_on_measured_buckets():
     # the choices the GB300 sweeps found best (Hkv = 2, 152 CTAs, equal lengths)
     eq = lambda B, L: [L * i for i in range(B + 1)]
-    want = {(1, 512): 8, (1, 2048): 16, (1, 8192): 32, (1, 32768): 64, (2, 32768): 32, (4, 2048): 16,
+    want = {(1, 512): 8, (1, 2048): 32, (1, 8192): 64, (1, 32768): 64, (2, 2048): 32, (2, 32768): 32, (4, 2048): 16,
             (4, 32768): 16, (8, 2048): 8, (16, 512): 4, (24, 8192): 3, (32, 2048): 2, (64, 512): 1,
             (64, 2048): 1, (64, 3072): 1,
             # stream schedule: >= 3072 positions per CTA, < 80 % of the CTAs busy, more than a wave
@@ -329,12 +329,12 @@ def test_cluster_kernel_partition_and_merge_slots():
 
 def test_device_closed_forms_equal_the_loops():
     # The device evaluates the rule with closed forms (Sched::auto_uniform_splits):
-    # s_opt = 2^max(0, (h - 2) / 2) with h the index of lmax's top bit (C's truncating
-    # division), and the largest power of two <= s_wave from its top bit.  The host
-    # rule and this model use the loops; the two agree everywhere.
+    # s_opt = 2^(h / 2) with h the index of lmax's top bit, and the largest power of
+    # two <= s_wave from its top bit.  The host rule and this model use the loops; the
+    # two agree everywhere.
     def s_opt_loop(lmax):
         p = 1
-        while 16 * p * p <= lmax:
+        while 4 * p * p <= lmax:
             p *= 2
         return p
 
@@ -342,8 +342,7 @@ def test_device_closed_forms_equal_the_loops():
         if lmax <= 0:
             return 1
         h = lmax.bit_length() - 1
-        k = int((h - 2) / 2)          # truncation toward zero, as in C
-        return 1 << max(0, k)
+        return 1 << (h >> 1)
 
     def p2_loop(w):
         p = 1
