@@ -85,8 +85,10 @@ int team_size(int npass) { return npass <= 1 ? 1 : (npass == 2 || npass == 4) ? 
 Layout layout(int B, int Hq, int Hkv, int D, int num_splits) {
   const int np = passes(Hq, Hkv);
   size_t pieces = num_pieces(B, Hkv * np, num_splits);
-  const int t = team_size(np);
-  if (t > 1) {
+  // the BF16 kernel's team and the FP8 kernel's pairs
+  const int ts[2] = {team_size(np), np >= 2 ? 2 : 1};
+  for (int t : ts) {
+    if (t <= 1) continue;
     const size_t pp = (size_t)t * num_pieces(B, Hkv * ((np + t - 1) / t), num_splits);
     if (pp > pieces) pieces = pp;
   }
@@ -213,8 +215,10 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
                       : (a->variant == GDA_VARIANT_TMA) ? gda::kVariantTma
                                                         : gda::kVariantMma;
   // G > 8 on the MMA kernel: the groups of 8 query heads in teams of 2 or 3, every
-  // group of a team in one piece (one HBM read of the KV head's rows per team)
-  const int team = (!fp8 && variant == gda::kVariantMma) ? team_size(npass) : 1;
+  // group of a team in one piece (one HBM read of the KV head's rows per team); on the
+  // FP8 kernel in pairs, except for three groups (a pair costs ~1.6 single passes, so
+  // a pair and a half-empty pair lose to three passes: measured 143.0 against 135.8 us)
+  const int team = (variant != gda::kVariantMma || npass < 2) ? 1 : fp8 ? (npass == 3 ? 1 : 2) : team_size(npass);
   const int nteam = (npass + team - 1) / team;
   // the heads that split the batch into segments for the schedule
   const long long vheads = (long long)a->Hkv * nteam;

@@ -97,6 +97,17 @@ struct Fp8Smem {
   float lsum[kW8][kG];                               // each warp's rescaled sum
   unsigned int qmax;                                 // largest |q| of the piece's group (float bits)
 };
+// Pairs of groups: both groups' Q^T fragments and each warp's S^T of its tile for its
+// partner's group (one buffer; the partner signals a read-done barrier once it has
+// taken it).
+struct Fp8PairSmem {
+  uint2 qf[2][16][32];
+  unsigned char vring[kW8][kNV8][kTok8][kRing8Row];
+  float mbuf[kW8][kG];
+  float lsum[kW8][kG];
+  float4 xs[kW8][2][32];
+  unsigned int qmax;                                 // largest |q| of the piece's groups (float bits)
+};
 static_assert(sizeof(float4) * 16 * 32 <= kTok8 * kRing8Row, "merge slice fits a ring stage");
 
 __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
@@ -120,7 +131,7 @@ struct Fp8WarpState {
   uint4 kr[16];  // K of the next tile: kr[4j + c] = token g + 8j, dims 64c + 16t .. +15
   float o[16][4];
   float m0, m1, l0, l1;
-  uint32_t P[4];  // FP16 probabilities: P[j] = tokens g + 8j, heads (2t, 2t+1)
+  uint32_t P[4];  // one group: FP16 probabilities, P[j] = tokens g + 8j, heads (2t, 2t+1)
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -143,7 +154,7 @@ struct Fp8WarpState {
     }
   }
 
-  // QK of the tile in kr, then the softmax update.  After the K registers of chunk
+  // QK of the tile in kr, then the softmax update (one group: the probabilities go to P).  After the K registers of chunk
   // c have had their last use, chunk c of the next tile (slots slot_next) is
   // loaded into them one chunk later (measured: one chunk later than the earliest
   // point is faster on randomly placed rows), so every K load is about one tile
@@ -232,10 +243,121 @@ struct Fp8WarpState {
     }
   }
 
+  // Unscaled S^T of the tile in kr against one group's Q^T fragments: s[4 mt + i] is
+  // accumulator i of m-tile mt (tokens g + 16 mt and g + 16 mt + 8, heads 2t, 2t + 1).
+  // With REFILL, after the K registers of chunk c have had their last use, chunk c of
+  // the next tile (slots slot_next) is loaded into them one chunk later (measured: one
+  // chunk later than the earliest point is faster on randomly placed rows), so every K
+  // load is about one tile ahead of its use.
+  template <bool REFILL>
+  __device__ __forceinline__ void qk_raw(const uint2 (*qf)[32], int lane, const unsigned char* kb, size_t stride,
+                                         int slot_next, bool more, float* s) {
+    const int g = lane >> 2, t = lane & 3;
+    const unsigned char* rn[4];
+    bool okn[4];
+    if (REFILL) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int sn = __shfl_sync(0xffffffffu, slot_next, g + 8 * j);
+        okn[j] = more && sn >= 0;
+        rn[j] = kb + (size_t)max(sn, 0) * stride + 16 * t;
+      }
+    }
+    float acc[4][4];  // [m-tile * 2 + (kk & 1)][4]
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int kk = 4 * c + h;
+        const uint2 b = qf[kk][lane];
+#pragma unroll
+        for (int mtile = 0; mtile < 2; ++mtile) {
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(word(kr[8 * mtile + c], h), a0, a2);
+          e4m3x4_to_f16x2x2(word(kr[8 * mtile + 4 + c], h), a1, a3);
+          mma_f16_16816(acc[2 * mtile + (kk & 1)], a0, a1, a2, a3, b.x, b.y);
+        }
+      }
+      if (REFILL && more && c >= 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) kr[4 * j + c - 1] = okn[j] ? ld_stream16(rn[j] + 64 * (c - 1)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (REFILL && more) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kr[4 * j + 3] = okn[j] ? ld_stream16(rn[j] + 64 * 3) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s[i] = acc[0][i] + acc[1][i];
+      s[4 + i] = acc[2][i] + acc[3][i];
+    }
+  }
+
+  // Online softmax over NT 32-token tiles of the same 8 heads: tile x has nv[x] valid
+  // tokens and unscaled scores s[x] (qk_raw's layout).  Lazy rescale (as in the BF16
+  // kernel): the reference maxima move only when a score exceeds them by more than
+  // kLazyLog2F8, so probabilities stay <= 2^8.  P[x][j]: FP16 probabilities of tile x,
+  // tokens g + 8j, heads (2t, 2t+1); their rounded values join the sums tile by tile.
+  template <int NT>
+  __device__ __forceinline__ void softmax_tiles(float (*s)[8], const int* nv, float sl2, int lane,
+                                                uint32_t (*P)[4]) {
+    const int tg = lane >> 2;
+    float xa0 = -INFINITY, xb0 = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < NT; ++x) {
+      // s[x][2j], s[x][2j + 1]: token g + 8j (j = 0 .. 3), heads 2t, 2t + 1
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[x][i] *= sl2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (tg + 8 * j >= nv[x]) s[x][2 * j] = s[x][2 * j + 1] = -INFINITY;
+      xa0 = fmaxf(xa0, fmaxf(fmaxf(s[x][0], s[x][2]), fmaxf(s[x][4], s[x][6])));
+      xb0 = fmaxf(xb0, fmaxf(fmaxf(s[x][1], s[x][3]), fmaxf(s[x][5], s[x][7])));
+    }
+    const bool grow = xa0 > m0 + kLazyLog2F8 || xb0 > m1 + kLazyLog2F8;
+    if (__any_sync(0xffffffffu, grow)) {
+      float xa = xa0, xb = xb0;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, off));
+      }
+      const float na = fmaxf(m0, xa), nb = fmaxf(m1, xb);
+      const float aa = safe_exp2_diff(m0, na), ab = safe_exp2_diff(m1, nb);
+      l0 *= aa;
+      l1 *= ab;
+      m0 = na;
+      m1 = nb;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= aa;
+        o[i][1] *= ab;
+        o[i][2] *= aa;
+        o[i][3] *= ab;
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < NT; ++x)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        P[x][j] = pack_f16x2(safe_exp2_diff(s[x][2 * j], m0), safe_exp2_diff(s[x][2 * j + 1], m1));
+        const float2 pf = unpack_f16x2(P[x][j]);
+        l0 += pf.x;
+        l1 += pf.y;
+      }
+  }
+
   // O^T += V^T P^T from a 32-row ring stage: per k-step of 16 tokens, the lane's
   // four tokens are read (two 16-byte halves each), paired by byte permutes and
   // widened to FP16.
-  __device__ __forceinline__ void pv(const unsigned char* vtile, int lane) {
+  __device__ __forceinline__ void pv(const unsigned char* vtile, int lane) { pv_with(vtile, P, lane); }
+
+  __device__ __forceinline__ void pv_with(const unsigned char* vtile, const uint32_t* P, int lane) {
     const int g = lane >> 2, t = lane & 3;
     const uint32_t base = smem_u32(vtile) + 16 * g;
 #pragma unroll
@@ -501,21 +623,323 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_kernel(Stage1Params p)
   }
 }
 
+// PAIR (G > 8): the groups of 8 query heads of a KV head in pairs, one piece per
+// (sequence, KV head, pair) serving both groups, so every K/V row is read once per
+// pair.  Warp w loads its tiles as without PAIR and computes S^T of its tile for both
+// groups (the partner group's first, then its own with the next tile's K loads);
+// warps w and w ^ 4 form a pair, warps 0-3 owning group 0 and 4-7 group 1.  Each step
+// a warp leaves the partner group's S^T in shared memory, the pair meets at a named
+// barrier, and each warp runs the softmax and PV of its own group over both tiles:
+// its own (its V ring) and the partner's (the partner's V ring).  The S^T buffer is
+// single: its reader arrives on the writer's read-done barrier once it has taken it,
+// and the writer waits on that barrier before the next write.  The partial of
+// (piece, group) is written at piece * 2 + group.
+__global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_pair_kernel(Stage1Params p) {
+  constexpr bool PAIR = true;
+  constexpr int NG = 2;
+  constexpr int WPG = kW8 / NG;  // warps per group
+  constexpr int QPT = 2 * NG;    // Q^T fragments per thread
+  using Smem = Fp8PairSmem;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / WPG;              // this warp's group
+  const int partner = warp ^ (kW8 / 2);    // PAIR: the warp of the other group on the same tiles
+  const int team = warp & (kW8 / 2 - 1);   // PAIR: the pair (named barrier 1 + team)
+  // PAIR: read-done barrier of warp x's S^T buffer (named barriers 5 .. 12)
+  auto read_bar = [](int x) -> int { return 5 + x; };
+
+  if (threadIdx.x == 0) sm.qmax = 0u;
+  Sched sched;
+  sched.begin(p.indptr, p.B, PAIR ? p.Hkv * p.nteam : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x,
+              p.min_chunk, p.window, p.piece_cost);
+  const size_t stride = (size_t)p.Hkv * kRowBytes8;
+  const uint64_t pol_v = l2_policy_evict_first();
+  auto kv_head = [&](const Piece& pp) -> int { return PAIR ? pp.kvh / p.nteam : pp.kvh / p.npass; };
+
+  auto nmine_for = [&](int w, int len) -> int {
+    const int ntiles = (len + kTok8 - 1) / kTok8;
+    return (ntiles > w) ? (ntiles - w + kW8 - 1) / kW8 : 0;
+  };
+  auto tile_n_for = [&](int w, int k, int len, int nm) -> int {
+    return (k < nm) ? min(kTok8, len - kTok8 * (w + kW8 * k)) : 0;
+  };
+  auto nmine_of = [&](int len) -> int { return nmine_for(warp, len); };
+  auto tile_n = [&](int k, int len, int nmine) -> int { return tile_n_for(warp, k, len, nmine); };
+  // slot of token `lane` of this warp's tile k (-1 past the tile's end or for a bad index)
+  auto fetch = [&](const int* idx, int k, int len, int nmine) -> int {
+    const int n = tile_n(k, len, nmine);
+    int s = -1;
+    if (lane < n) {
+      s = __ldg(idx + kTok8 * (warp + kW8 * k) + lane);
+      if (p.check_indices && (s < 0 || (long long)s >= p.num_slots)) {
+        atomicOr(&p.hdr->error, kErrIndex);
+        s = -1;
+      }
+    }
+    return s;
+  };
+
+  Fp8WarpState st;
+  uint2 qraw[QPT];  // this thread's BF16 Q^T fragments of the next piece
+  int s0 = -1, s1 = -1, s2 = -1;
+  // Head of a piece: its Q rows (BF16, converted at the piece start), the slots of
+  // this warp's first three tiles and the K rows of its first tile.  For every
+  // piece after the first this runs before the previous piece's merge.
+  auto piece_head = [&](const Piece& pp) {
+    // PAIR: the piece's KV head and the first group of its pair
+    const int pkv = kv_head(pp), pg0 = PAIR ? 2 * (pp.kvh - pkv * p.nteam) : 0;
+#pragma unroll
+    for (int r = 0; r < QPT; ++r) {
+      const int e = threadIdx.x + r * kW8 * 32;
+      const int fg = e >> 9, kk = (e >> 5) & 15, ln = e & 31;  // group, k-step, lane
+      const int g = ln >> 2, t = ln & 3, c = kk >> 2, h = kk & 3;
+      // group pg0 + fg of the KV head (PAIR; past the last group it is empty: Q = 0, its
+      // partial never read), else the piece's virtual head
+      const int pass = PAIR ? min(pg0 + fg, p.npass - 1) : pp.kvh - pkv * p.npass;
+      const int gv = (PAIR && pg0 + fg >= p.npass) ? 0 : min(kG, p.G - kG * pass);
+      const __nv_bfloat16* qg = p.q + ((size_t)pp.b * p.Hq + (size_t)pkv * p.G + (size_t)kG * pass) * kD;
+      const __nv_bfloat16* row = qg + max(0, min(g, gv - 1)) * kD;  // never addresses a row beyond the group
+      qraw[r] = (g < gv) ? __ldg(reinterpret_cast<const uint2*>(row + 64 * c + 16 * t + 4 * h)) : make_uint2(0u, 0u);
+    }
+    const int* idx = p.indices + pp.base + pp.j0;
+    const int len = pp.j1 - pp.j0, nmine = nmine_of(len);
+    s0 = fetch(idx, 0, len, nmine);
+    s1 = fetch(idx, 1, len, nmine);
+    s2 = fetch(idx, 2, len, nmine);
+    if (nmine > 0) st.load_k(p.k_pool + (size_t)pkv * kRowBytes8, stride, s0, lane);
+  };
+
+  __syncthreads();  // qmax initialised
+  // Stage 2 may start its prologue (gate loads and sigmoids) once this CTA knows it has
+  // work: an idle CTA (the automatic plan launches a full grid) exits without the
+  // trigger, which counts as one, so stage 2's CTAs are placed after the idle CTAs have
+  // left.  (Measured: idle CTAs that stay resident while stage 2 is placed slowed stage
+  // 2's merge by ~3 us on B1 L32768.)
+  Piece pc;
+  bool have = sched.next(pc);
+  if (have) pdl_launch_dependents();
+  if (have) piece_head(pc);
+  while (have) {
+    const size_t head_off = (size_t)kv_head(pc) * kRowBytes8;
+    const unsigned char* kb = p.k_pool + head_off;
+    const unsigned char* vb = p.v_pool + head_off;
+    const int* idx = p.indices + pc.base + pc.j0;
+    const int len = pc.j1 - pc.j0;
+    const int nmine = nmine_of(len);
+    // steps of this warp's loop: its tiles, or with PAIR those of the pair's first
+    // warp (the one with more tiles), so that both partners meet at every barrier
+    const int nsteps = PAIR ? nmine_for(team, len) : nmine;
+
+    st.reset();
+    unsigned char(*ring)[kTok8][kRing8Row] = sm.vring[warp];
+    if (nsteps > 0) {
+      issue_v_tile8(&ring[0][0][0], vb, stride, s0, tile_n(0, len, nmine), lane, pol_v);
+      issue_v_tile8(&ring[1 % kNV8][0][0], vb, stride, s1, tile_n(1, len, nmine), lane, pol_v);
+      prefetch_k_tile8(kb, stride, s1);
+    }
+
+    // Q into FP16: one power-of-two factor 2^e for the piece's groups puts their largest
+    // magnitude in [2^14, 2^15) (every BF16 value at most 2^28 below it is exact).
+    {
+      float mx = 0.0f;
+#pragma unroll
+      for (int r = 0; r < QPT; ++r) {
+        const uint32_t w2[2] = {qraw[r].x, qraw[r].y};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          mx = fmaxf(mx, fabsf(__uint_as_float(w2[j] << 16)));
+          mx = fmaxf(mx, fabsf(__uint_as_float(w2[j] & 0xFFFF0000u)));
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane == 0) atomicMax(&sm.qmax, __float_as_uint(mx));
+    }
+    __syncthreads();  // also: the previous piece's merge is done with the rings and Q fragments
+    const unsigned int qm = sm.qmax;
+    int e = (qm == 0u) ? 0 : 141 - (int)((qm >> 23) & 0xFFu);  // 2^e * max in [2^14, 2^15)
+    e = max(-126, min(127, e));
+    const float qs = __uint_as_float((uint32_t)(e + 127) << 23);
+    const float sl2 = ldexpf(p.scale_log2, -e);
+#pragma unroll
+    for (int r = 0; r < QPT; ++r) {
+      const int idxq = threadIdx.x + r * kW8 * 32;
+      const uint32_t x = qraw[r].x, y = qraw[r].y;
+      uint2 f;
+      f.x = pack_f16x2(__uint_as_float(x << 16) * qs, __uint_as_float(x & 0xFFFF0000u) * qs);
+      f.y = pack_f16x2(__uint_as_float(y << 16) * qs, __uint_as_float(y & 0xFFFF0000u) * qs);
+      sm.qf[idxq >> 9][(idxq >> 5) & 15][idxq & 31] = f;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) sm.qmax = 0u;  // every thread has read it; the next write follows a barrier
+
+    int stage = 0;
+    if constexpr (PAIR) {
+      const int nmp = nmine_for(partner, len);
+      for (int k = 0; k < nsteps; ++k) {
+        // K rows of tile k+2 into L2, the slots of tile k+3; tile k's S^T for the
+        // partner's group (to shared memory), then for this warp's own group with the
+        // next tile's K loads
+        prefetch_k_tile8(kb, stride, s2);
+        const int s3 = fetch(idx, k + 3, len, nmine);
+        const int nown = tile_n(k, len, nmine);
+        float sc[2][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc[0][i] = sc[1][i] = 0.0f;
+        if (nown > 0) st.qk_raw<false>(sm.qf[grp ^ 1], lane, kb, stride, s1, false, sc[1]);
+        if (k > 0) named_bar_sync(read_bar(warp), 64);  // the partner has taken step k-1's
+        sm.xs[warp][0][lane] = make_float4(sc[1][0], sc[1][1], sc[1][2], sc[1][3]);
+        sm.xs[warp][1][lane] = make_float4(sc[1][4], sc[1][5], sc[1][6], sc[1][7]);
+        if (nown > 0) st.qk_raw<true>(sm.qf[grp], lane, kb, stride, s1, k + 1 < nmine, sc[0]);
+        cp_async_wait_group<1>();  // this warp's V tile k has landed (tile k+1 may be in flight)
+        // The pair meets: both V tiles k and both S^T are visible, and the partner has
+        // finished step k-1, so ring stage (k+2) % 3 (read as stage (k-1) % 3) is free.
+        named_bar_sync(1 + team, 64);
+        issue_v_tile8(&ring[(k + 2) % kNV8][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
+        {
+          const float4 u0 = sm.xs[partner][0][lane], u1 = sm.xs[partner][1][lane];
+          sc[1][0] = u0.x;
+          sc[1][1] = u0.y;
+          sc[1][2] = u0.z;
+          sc[1][3] = u0.w;
+          sc[1][4] = u1.x;
+          sc[1][5] = u1.y;
+          sc[1][6] = u1.z;
+          sc[1][7] = u1.w;
+        }
+        __syncwarp();
+        named_bar_arrive(read_bar(partner), 64);
+        const int nt[2] = {nown, tile_n_for(partner, k, len, nmp)};
+        uint32_t P[2][4];
+        st.softmax_tiles<2>(sc, nt, sl2, lane, P);
+        if (nt[0] > 0) st.pv_with(&ring[stage][0][0], P[0], lane);
+        if (nt[1] > 0) st.pv_with(&sm.vring[partner][stage][0][0], P[1], lane);
+        stage = (stage + 1 == kNV8) ? 0 : stage + 1;
+        s1 = s2;
+        s2 = s3;
+      }
+      if (nsteps > 0) named_bar_sync(read_bar(warp), 64);  // the partner's last read-done
+    } else {
+      for (int k = 0; k < nmine; ++k) {
+        // V two tiles ahead (an empty group when there is no such tile), K rows of
+        // that tile into L2, the slots three tiles ahead; then tile k's QK
+        issue_v_tile8(&ring[(k + 2) % kNV8][0][0], vb, stride, s2, tile_n(k + 2, len, nmine), lane, pol_v);
+        prefetch_k_tile8(kb, stride, s2);
+        const int s3 = fetch(idx, k + 3, len, nmine);
+        st.qk_softmax(sm.qf[0], tile_n(k, len, nmine), sl2, lane, kb, stride, s1, k + 1 < nmine);
+        cp_async_wait_group<2>();
+        __syncwarp();
+        st.pv(&ring[stage][0][0], lane);
+        __syncwarp();
+        stage = (stage + 1 == kNV8) ? 0 : stage + 1;
+        s1 = s2;
+        s2 = s3;
+      }
+    }
+    cp_async_wait_group<0>();
+    __syncwarp();
+
+    // look ahead: the next piece's first loads go out before this piece's merge
+    Piece nx;
+    const bool have_next = sched.next(nx);
+    if (have_next) piece_head(nx);
+
+    // ---- merge: fragment-order slices in the (now idle) rings, summed in a fixed order
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
+      st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
+    }
+    if (lane < 4) {
+      sm.mbuf[warp][2 * lane] = st.m0;
+      sm.mbuf[warp][2 * lane + 1] = st.m1;
+    }
+    __syncthreads();
+    {
+      const int ha = 2 * (lane & 3), hb = ha + 1;
+      const int x0 = grp * WPG;  // this group's warps: x0 .. x0 + WPG - 1
+      float Ma = sm.mbuf[x0][ha], Mb = sm.mbuf[x0][hb];
+#pragma unroll
+      for (int x = 1; x < WPG; ++x) {
+        Ma = fmaxf(Ma, sm.mbuf[x0 + x][ha]);
+        Mb = fmaxf(Mb, sm.mbuf[x0 + x][hb]);
+      }
+      const float fa = (Ma == -INFINITY) ? 0.0f : safe_exp2_diff(st.m0, Ma);
+      const float fb = (Mb == -INFINITY) ? 0.0f : safe_exp2_diff(st.m1, Mb);
+      float4* slice = reinterpret_cast<float4*>(&sm.vring[warp][0][0][0]);
+#pragma unroll
+      for (int mt = 0; mt < 16; ++mt)
+        slice[mt * 32 + lane] = make_float4(st.o[mt][0] * fa, st.o[mt][1] * fb, st.o[mt][2] * fa, st.o[mt][3] * fb);
+      if (lane < 4) {
+        sm.lsum[warp][ha] = st.l0 * fa;
+        sm.lsum[warp][hb] = st.l1 * fb;
+      }
+    }
+    __syncthreads();
+    // partial (piece, group) at piece * NG + group
+    for (int f = threadIdx.x; f < NG * 16 * 32; f += blockDim.x) {
+      const int fg = f >> 9, fl = f & 511;
+      const int mt = fl >> 5, ln = fl & 31;
+      const int g = ln >> 2, ha = 2 * (ln & 3), hb = ha + 1;
+      const int x0 = fg * WPG;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float la = 0.0f, lb = 0.0f;
+#pragma unroll
+      for (int x = x0; x < x0 + WPG; ++x) {
+        const float4 v = reinterpret_cast<const float4*>(&sm.vring[x][0][0][0])[fl];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+        la += sm.lsum[x][ha];
+        lb += sm.lsum[x][hb];
+      }
+      const float ia = (la > 0.0f) ? p.v_descale / la : 0.0f;
+      const float ib = (lb > 0.0f) ? p.v_descale / lb : 0.0f;
+      const int d0 = 128 * (mt >> 3) + 16 * g + 2 * (mt & 7);
+      float* op = p.o_part + (pc.id * NG + fg) * (kG * kD);
+      *reinterpret_cast<float2*>(op + ha * kD + d0) = make_float2(acc.x * ia, acc.z * ia);
+      *reinterpret_cast<float2*>(op + hb * kD + d0) = make_float2(acc.y * ib, acc.w * ib);
+    }
+    if (threadIdx.x < NG * kG) {
+      const int x0 = (threadIdx.x / kG) * WPG, h = threadIdx.x % kG;
+      float M = sm.mbuf[x0][h], lt = 0.0f;
+#pragma unroll
+      for (int x = 1; x < WPG; ++x) M = fmaxf(M, sm.mbuf[x0 + x][h]);
+#pragma unroll
+      for (int x = 0; x < WPG; ++x) lt += sm.lsum[x0 + x][h];
+      p.lse_part[pc.id * (NG * kG) + threadIdx.x] = (lt > 0.0f) ? M + log2f(lt) : -INFINITY;
+    }
+    __syncthreads();  // rings, Q fragments and merge buffers free for the next piece
+    pc = nx;
+    have = have_next;
+  }
+}
+
+
 }  // namespace
 
-cudaError_t launch_stage1_fp8(const Stage1Params& p, int grid, cudaStream_t stream) {
-  static std::atomic<bool> attr_set[64];  // zero-initialised: false
+template <typename Smem>
+cudaError_t launch_fp8(void (*kern)(Stage1Params), const Stage1Params& p, int grid, cudaStream_t stream,
+                       std::atomic<bool>* attr_set) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(stage1_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Fp8Smem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  stage1_fp8_kernel<<<grid, kW8 * 32, sizeof(Fp8Smem), stream>>>(p);
+  kern<<<grid, kW8 * 32, sizeof(Smem), stream>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_stage1_fp8(const Stage1Params& p, int grid, cudaStream_t stream) {
+  static std::atomic<bool> single_set[64], pair_set[64];  // zero-initialised: false
+  return p.team == 2 ? launch_fp8<Fp8PairSmem>(stage1_fp8_pair_kernel, p, grid, stream, pair_set)
+                     : launch_fp8<Fp8Smem>(stage1_fp8_kernel, p, grid, stream, single_set);
 }
 
 }  // namespace gda

@@ -13,7 +13,8 @@
  * kernels handle the query heads of a KV head in groups of up to 8: for G > 8 the
  * default kernel serves the groups in teams, every group of a team from one read of
  * the KV head's rows -- pairs for 2 or 4 groups, threes otherwise: one read for
- * G = 9 .. 24, two for 25 .. 48 -- and the other kernels read the rows once per group).  Sources: FreeToken
+ * G = 9 .. 24, two for 25 .. 48; an e4m3 cache's kernel takes pairs except for three
+ * groups -- and the other kernels read the rows once per group).  Sources: FreeToken
  * PR #781 "Fuse the BF16 attention output sigmoid gate into the existing Triton
  * decode stage2" (Summary: split-KV stage 1, FP32 LSE merge in stage 2 with the
  * BF16 gate and an explicit round-to-nearest-even product fused into its epilogue;

@@ -69,6 +69,31 @@ def test_workspace_bytes(lib):
     assert gda.workspace_bytes(4, 16, 2, 256, 257) == 0    # too many splits
 
 
+def test_workspace_holds_every_team_layout(lib):
+    # G > 8: the BF16 MMA kernel serves the groups of 8 in teams (pairs for 2 or 4
+    # groups, threes otherwise), the FP8 kernel in pairs (not for 3 groups), the other
+    # kernels one group per piece; a team piece holds t partials at piece * t + group.
+    # The caller-sized workspace holds the largest of these layouts.
+    G8, D = 8, 256
+    piece = G8 * D * 4 + G8 * 4
+
+    def pieces(B, vheads, S):
+        return B * vheads * S if S > 0 else 1024 + B * vheads
+
+    def teams(npass):
+        bf16 = 1 if npass <= 1 else 2 if npass in (2, 4) else 3
+        fp8 = 1 if npass in (1, 3) else 2
+        return {1, bf16, fp8}
+
+    for B in (1, 7, 64, 224):
+        for Hkv in (1, 2, 4):
+            for G in (1, 8, 9, 16, 20, 24, 32, 40, 56, 64):
+                npass = -(-G // 8)
+                for S in (0, 1, 3, 8):
+                    need = max(t * pieces(B, Hkv * -(-npass // t), S) for t in teams(npass)) * piece
+                    assert gda.workspace_bytes(B, G * Hkv, Hkv, D, S) >= 256 + need, (B, Hkv, G, S)
+
+
 def _decode(lib, ptrs=None, B=1, Hq=16, Hkv=2, D=256, scale=0.0625, splits=0):
     p = dict(q=16, gate=16, k=16, v=16, indptr=16, indices=16, out=16)
     if ptrs:

@@ -137,14 +137,38 @@ def test_attention_sinks(gda, batch):
         check_close(run(gda, dev, sinks=sinks, num_splits=splits), ref.out)
 
 
-@pytest.mark.parametrize("hq,hkv", [(16, 16), (16, 8), (6, 2), (12, 2), (32, 2), (24, 1)])
+@pytest.mark.parametrize("hq,hkv", [(16, 16), (16, 8), (6, 2), (12, 2), (32, 2), (24, 1), (16, 1), (40, 2),
+                                    (64, 2)])
 def test_group_sizes(gda, hq, hkv):
+    # G > 8: the groups of 8 go in pairs (one piece, one read of the rows per pair); G =
+    # 24 and 20 leave the second pair half empty, G = 32 is two pairs
     inp = workloads.make([0, 3, 77, 600, 1500], seed=311, hq=hq, hkv=hkv, layout="perm", pool_slots=3000,
                          kv="e4m3")
     dev = to_cuda(inp)
     ref = reference(inp)
     for splits in (0, 4):
         check_close(run(gda, dev, num_splits=splits), ref.out)
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 2), (48, 2)])
+def test_pairs_long_ragged_window_sinks_lse(gda, hq, hkv):
+    # pairs over a long ragged batch: pieces cross sequences and CTAs, the partner warps
+    # meet at every step; a window, sinks and the LSE go through the same mapping, and
+    # repeated calls give the same bits
+    lens = [4096, 1, 0, 3000, 777, 65, 2049, 16, 5000, 129, 1500, 2]
+    inp = workloads.make(lens, seed=520 + hq, hq=hq, hkv=hkv, layout="perm", pool_slots=20000, peaky_frac=0.01,
+                         kv="e4m3")
+    dev = to_cuda(inp)
+    ref = reference(inp)
+    for kw in ({}, {"min_chunk": 16}, {"num_splits": 7}):
+        a = run(gda, dev, **kw)
+        check_close(a, ref.out)
+        assert np.array_equal(a, run(gda, dev, **kw))
+    sinks = np.linspace(-2.0, 2.0, hq).astype(np.float32)
+    ref = reference(inp, window=1000, sinks=sinks.astype(np.float64))
+    lse = torch.empty(len(lens), hq, dtype=torch.float32, device="cuda")
+    check_close(run(gda, dev, window=1000, sinks=sinks, lse=lse), ref.out)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref.lse, atol=2e-3, rtol=1e-4)
 
 
 def test_all_codes_and_extreme_q(gda):
