@@ -106,7 +106,7 @@ struct Fp8PairSmem {
   float mbuf[kW8][kG];
   float lsum[kW8][kG];
   float4 xs[kW8][2][32];
-  unsigned int qmax;                                 // largest |q| of the piece's groups (float bits)
+  unsigned int qmax[2];                              // largest |q| of each group of the piece (float bits)
 };
 static_assert(sizeof(float4) * 16 * 32 <= kTok8 * kRing8Row, "merge slice fits a ring stage");
 
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_pair_kernel(Stage1Para
   // PAIR: read-done barrier of warp x's S^T buffer (named barriers 5 .. 12)
   auto read_bar = [](int x) -> int { return 5 + x; };
 
-  if (threadIdx.x == 0) sm.qmax = 0u;
+  if (threadIdx.x < 2) sm.qmax[threadIdx.x] = 0u;
   Sched sched;
   sched.begin(p.indptr, p.B, PAIR ? p.Hkv * p.nteam : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x,
               p.min_chunk, p.window, p.piece_cost);
@@ -739,40 +739,52 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_pair_kernel(Stage1Para
       prefetch_k_tile8(kb, stride, s1);
     }
 
-    // Q into FP16: one power-of-two factor 2^e for the piece's groups puts their largest
-    // magnitude in [2^14, 2^15) (every BF16 value at most 2^28 below it is exact).
+    // Q into FP16: per group, one power-of-two factor 2^e puts the group's largest
+    // magnitude in [2^14, 2^15) (every BF16 value at most 2^28 below it is exact).  Each
+    // group has its own factor, so a group of ordinary magnitude beside a much larger
+    // one keeps its scores; a warp's scores are those of its own group, scaled by its
+    // group's factor.  Fragments r = 0, 1 of a thread are group 0's, r = 2, 3 group 1's.
     {
-      float mx = 0.0f;
+      float mx[2] = {0.0f, 0.0f};
 #pragma unroll
       for (int r = 0; r < QPT; ++r) {
         const uint32_t w2[2] = {qraw[r].x, qraw[r].y};
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          mx = fmaxf(mx, fabsf(__uint_as_float(w2[j] << 16)));
-          mx = fmaxf(mx, fabsf(__uint_as_float(w2[j] & 0xFFFF0000u)));
+          mx[r >> 1] = fmaxf(mx[r >> 1], fabsf(__uint_as_float(w2[j] << 16)));
+          mx[r >> 1] = fmaxf(mx[r >> 1], fabsf(__uint_as_float(w2[j] & 0xFFFF0000u)));
         }
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      if (lane == 0) atomicMax(&sm.qmax, __float_as_uint(mx));
+      for (int x = 0; x < 2; ++x) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx[x] = fmaxf(mx[x], __shfl_xor_sync(0xffffffffu, mx[x], off));
+        if (lane == 0) atomicMax(&sm.qmax[x], __float_as_uint(mx[x]));
+      }
     }
     __syncthreads();  // also: the previous piece's merge is done with the rings and Q fragments
-    const unsigned int qm = sm.qmax;
-    int e = (qm == 0u) ? 0 : 141 - (int)((qm >> 23) & 0xFFu);  // 2^e * max in [2^14, 2^15)
-    e = max(-126, min(127, e));
-    const float qs = __uint_as_float((uint32_t)(e + 127) << 23);
-    const float sl2 = ldexpf(p.scale_log2, -e);
+    float qs[2];
+    float sl2 = 0.0f;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const unsigned int qm = sm.qmax[x];
+      int e = (qm == 0u) ? 0 : 141 - (int)((qm >> 23) & 0xFFu);  // 2^e * max in [2^14, 2^15)
+      e = max(-126, min(127, e));
+      qs[x] = __uint_as_float((uint32_t)(e + 127) << 23);
+      if (x == grp) sl2 = ldexpf(p.scale_log2, -e);
+    }
 #pragma unroll
     for (int r = 0; r < QPT; ++r) {
       const int idxq = threadIdx.x + r * kW8 * 32;
       const uint32_t x = qraw[r].x, y = qraw[r].y;
+      const float f_s = qs[r >> 1];
       uint2 f;
-      f.x = pack_f16x2(__uint_as_float(x << 16) * qs, __uint_as_float(x & 0xFFFF0000u) * qs);
-      f.y = pack_f16x2(__uint_as_float(y << 16) * qs, __uint_as_float(y & 0xFFFF0000u) * qs);
+      f.x = pack_f16x2(__uint_as_float(x << 16) * f_s, __uint_as_float(x & 0xFFFF0000u) * f_s);
+      f.y = pack_f16x2(__uint_as_float(y << 16) * f_s, __uint_as_float(y & 0xFFFF0000u) * f_s);
       sm.qf[idxq >> 9][(idxq >> 5) & 15][idxq & 31] = f;
     }
     __syncthreads();
-    if (threadIdx.x == 0) sm.qmax = 0u;  // every thread has read it; the next write follows a barrier
+    if (threadIdx.x < 2) sm.qmax[threadIdx.x] = 0u;  // every thread has read them; the next writes follow a barrier
 
     int stage = 0;
     if constexpr (PAIR) {

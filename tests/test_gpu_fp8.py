@@ -196,6 +196,24 @@ def test_all_codes_and_extreme_q(gda):
             check_close(run(gda, dev, num_splits=splits, variant=form), ref.out, v_scale=v_std)
 
 
+def test_pairs_scale_q_per_group(gda):
+    """G = 16 runs the two groups of 8 query heads of a KV head as one piece; each group
+    gets its own power-of-two factor into FP16, so a group of ordinary magnitude next
+    to a group ~2^66 larger keeps its scores (one shared factor would flush it to
+    zero and flatten its softmax)."""
+    inp = workloads.make([1, 300, 2048, 77], seed=331, hq=32, hkv=2, layout="perm", pool_slots=3000,
+                         kv="e4m3")
+    q = inp["q"].clone()
+    q[:, 0:8] *= 1e20        # group 0 of KV head 0
+    q[:, 24:32] *= 1e-20     # group 1 of KV head 1
+    q[2, 8:16] *= 1e-30      # group 1 of KV head 0, one sequence: tiny
+    inp["q"] = q
+    dev = to_cuda(inp)
+    ref = reference(inp)
+    for splits in (0, 5):
+        check_close(run(gda, dev, num_splits=splits), ref.out)
+
+
 def test_check_indices_flags_bad_rows(gda, batch):
     inp, dev = batch
     bad = dev["kv_indices"].clone()
