@@ -214,6 +214,29 @@ def test_pairs_scale_q_per_group(gda):
         check_close(run(gda, dev, num_splits=splits), ref.out)
 
 
+def test_pairs_many_segments_and_bad_indices(gda):
+    # G = 16 pairs with more (sequence, KV head, pair) segments than CTAs (the
+    # cost-weighted stream schedule), then one bad index under check_indices
+    rng = np.random.default_rng(341)
+    lens = [int(x) for x in rng.integers(1, 600, 160)]
+    lens[9] = 0
+    lens[100] = 3000
+    inp = workloads.make(lens, seed=342, hq=32, hkv=2, layout="perm", pool_slots=sum(lens) + 500, kv="e4m3")
+    dev = to_cuda(inp)
+    ref = reference(inp)
+    for kw in ({}, {"max_len": max(lens), "total_len": sum(lens)}, {"num_splits": 3}):
+        check_close(run(gda, dev, **kw), ref.out)
+    B, Hq, D = dev["q"].shape
+    ws = torch.empty(gda.workspace_bytes(B, Hq, 2, D, 0), dtype=torch.uint8, device="cuda")
+    gda.workspace_init(ws)
+    bad = dev["kv_indices"].clone()
+    bad[1234] = 10 ** 8
+    gda.decode_ex(dev["q"], dev["gate"], dev["k_pool"], dev["v_pool"], dev["kv_indptr"], bad,
+                  scale=dev["scale"], k_descale=dev["k_descale"], v_descale=dev["v_descale"],
+                  check_indices=True, workspace=ws)
+    assert gda.read_error(ws) == gda.DEVERR_INDEX
+
+
 def test_check_indices_flags_bad_rows(gda, batch):
     inp, dev = batch
     bad = dev["kv_indices"].clone()

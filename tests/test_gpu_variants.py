@@ -189,3 +189,19 @@ def test_team_groups_caller_workspace_sizes(gda, hq):
         ref = reference(inp, window=window)
         check_close(run(gda, inp, workspace=ws, num_splits=splits, window=window), ref.out)
         assert gda.read_error(ws) == 0
+
+
+@pytest.mark.parametrize("hq", [32, 48])
+def test_team_groups_many_segments(gda, hq):
+    # more (sequence, KV head, team) segments than CTAs: the stream schedule charges a
+    # cost per segment start (the stage-1 and stage-2 views of the pieces must agree),
+    # with pairs (hq 32) and threes (hq 48)
+    rng = np.random.default_rng(700 + hq)
+    lens = [int(x) for x in rng.integers(1, 600, 160)]
+    lens[5] = 0
+    lens[77] = 4000
+    inp = workloads.make(lens, seed=701 + hq, hq=hq, hkv=2, layout="perm", pool_slots=sum(lens) + 500)
+    ref = reference(inp)
+    for kw in ({}, {"max_len": max(lens), "total_len": sum(lens)}, {"num_splits": 3}):
+        check_close(run(gda, inp, **kw), ref.out)
+
