@@ -298,6 +298,60 @@ struct Fp8WarpState {
     }
   }
 
+  // Unscaled S^T of the tile in kr for two groups at once (qk_raw's layout and summation
+  // order for each): every converted K fragment feeds both groups' MMAs.  One m-tile
+  // (16 tokens) at a time, so the two groups' accumulators stay within qk_raw's
+  // register count; the next tile's K chunks are loaded as in qk_raw, per m-tile.  The
+  // second group's scores go straight to shared memory: m-tile mt at xb[mt][lane].
+  __device__ __forceinline__ void qk_raw_pair(const uint2 (*qa)[32], const uint2 (*qb)[32], int lane,
+                                              const unsigned char* kb, size_t stride, int slot_next, bool more,
+                                              float* sa, float4 (*xb)[32]) {
+    const int g = lane >> 2, t = lane & 3;
+    const unsigned char* rn[4];
+    bool okn[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int sn = __shfl_sync(0xffffffffu, slot_next, g + 8 * j);
+      okn[j] = more && sn >= 0;
+      rn[j] = kb + (size_t)max(sn, 0) * stride + 16 * t;
+    }
+#pragma unroll
+    for (int mtile = 0; mtile < 2; ++mtile) {
+      float acc[2][2][4];  // [group][kk & 1][4]
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[x][0][i] = acc[x][1][i] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int kk = 4 * c + h;
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(word(kr[8 * mtile + c], h), a0, a2);
+          e4m3x4_to_f16x2x2(word(kr[8 * mtile + 4 + c], h), a1, a3);
+          const uint2 ba = qa[kk][lane], bb = qb[kk][lane];
+          mma_f16_16816(acc[0][kk & 1], a0, a1, a2, a3, ba.x, ba.y);
+          mma_f16_16816(acc[1][kk & 1], a0, a1, a2, a3, bb.x, bb.y);
+        }
+        if (more && c >= 1) {
+#pragma unroll
+          for (int j = 2 * mtile; j < 2 * mtile + 2; ++j)
+            kr[4 * j + c - 1] = okn[j] ? ld_stream16(rn[j] + 64 * (c - 1)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (more) {
+#pragma unroll
+        for (int j = 2 * mtile; j < 2 * mtile + 2; ++j)
+          kr[4 * j + 3] = okn[j] ? ld_stream16(rn[j] + 64 * 3) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sa[4 * mtile + i] = acc[0][0][i] + acc[0][1][i];
+      xb[mtile][lane] = make_float4(acc[1][0][0] + acc[1][1][0], acc[1][0][1] + acc[1][1][1],
+                                    acc[1][0][2] + acc[1][1][2], acc[1][0][3] + acc[1][1][3]);
+    }
+  }
+
   // Online softmax over NT 32-token tiles of the same 8 heads: tile x has nv[x] valid
   // tokens and unscaled scores s[x] (qk_raw's layout).  Lazy rescale (as in the BF16
   // kernel): the reference maxima move only when a score exceeds them by more than
@@ -799,11 +853,13 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_pair_kernel(Stage1Para
         float sc[2][8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) sc[0][i] = sc[1][i] = 0.0f;
-        if (nown > 0) st.qk_raw<false>(sm.qf[grp ^ 1], lane, kb, stride, s1, false, sc[1]);
         if (k > 0) named_bar_sync(read_bar(warp), 64);  // the partner has taken step k-1's
-        sm.xs[warp][0][lane] = make_float4(sc[1][0], sc[1][1], sc[1][2], sc[1][3]);
-        sm.xs[warp][1][lane] = make_float4(sc[1][4], sc[1][5], sc[1][6], sc[1][7]);
-        if (nown > 0) st.qk_raw<true>(sm.qf[grp], lane, kb, stride, s1, k + 1 < nmine, sc[0]);
+        if (nown > 0) {
+          st.qk_raw_pair(sm.qf[grp], sm.qf[grp ^ 1], lane, kb, stride, s1, k + 1 < nmine, sc[0], sm.xs[warp]);
+        } else {
+          sm.xs[warp][0][lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+          sm.xs[warp][1][lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         cp_async_wait_group<1>();  // this warp's V tile k has landed (tile k+1 may be in flight)
         // The pair meets: both V tiles k and both S^T are visible, and the partner has
         // finished step k-1, so ring stage (k+2) % 3 (read as stage (k-1) % 3) is free.
