@@ -231,7 +231,9 @@ __device__ __forceinline__ void seq_range(const int* indptr, int b, int window, 
 }
 
 // Automatic mode: per-CTA stream length from which the chunked schedule is used
-// even for batches that fit one wave of uniform splits.
+// even for batches that fit one wave of uniform splits (a BF16 cache; with an e4m3
+// cache one-wave uniform splits measured faster at every length, and the host passes 0:
+// no such bound).
 constexpr int kStreamMinPerCta = 3072;
 
 // Stream schedule: what starting one more (sequence, KV head) segment costs a CTA, in
@@ -259,7 +261,7 @@ struct Sched {
   // Hkv_ here is the number of (virtual) heads that split the batch into segments.
   // window > 0 requires S_ > 0 (the host picks the split count then).
   __device__ __forceinline__ void begin(const int* indptr_, int B_, int Hkv_, int S_, int grid_,
-                                        int cta_, int min_chunk, int window_, int piece_cost_) {
+                                        int cta_, int min_chunk, int window_, int piece_cost_, int stream_min) {
     indptr = indptr_;
     B = B_;
     Hkv = Hkv_;
@@ -272,7 +274,7 @@ struct Sched {
     const int cand0 = min(B - 1, (int)(threadIdx.x & 31) * step0);
     const int v0 = __ldg(indptr + cand0 + 1);
     const int ntot = __ldg(indptr + B);
-    S = (S_ > 0) ? S_ : auto_uniform_splits(indptr_, B_, Hkv_, grid_, min_chunk);
+    S = (S_ > 0) ? S_ : auto_uniform_splits(indptr_, B_, Hkv_, grid_, min_chunk, stream_min);
     if (S > 0) {
       u = cta;
       return;
@@ -418,7 +420,7 @@ struct Sched {
   //    wins by 1-3 %: no idle SMs) or when the lengths are far from equal
   //    (lmax > 1.25 x the mean: S pieces of the longest sequence bound the call).
   static __device__ __forceinline__ int auto_uniform_splits(const int* indptr, int B, int Hkv, int grid,
-                                                            int min_chunk) {
+                                                            int min_chunk, int stream_min) {
     if ((long long)B * Hkv > grid) return 0;
     const int units1 = B * Hkv;  // one piece per segment; <= grid
     if (units1 == 0) return 1;
@@ -435,7 +437,7 @@ struct Sched {
       lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
       n += __shfl_xor_sync(0xffffffffu, n, off);
     }
-    if ((long long)Hkv * n >= (long long)kStreamMinPerCta * grid) return 0;
+    if (stream_min > 0 && (long long)Hkv * n >= (long long)stream_min * grid) return 0;
     if (4LL * lmax * B > 5LL * n) return 0;
     // (closed forms, short dependent chains: every CTA's start waits on this)
     // s_opt: the smallest power of two p with 4 p^2 > lmax, 2^(h / 2) with h the index
@@ -509,8 +511,8 @@ struct Sched {
 // mode: first = c_first + sigma), or sigma*S + k (explicit mode), in position order.
 // (With a window the split count is explicit and L is the windowed length.)
 __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh, int Hkv, int B, int S,
-                                               int grid, int min_chunk, int window, int piece_cost, long long* first,
-                                               int* n) {
+                                               int grid, int min_chunk, int window, int piece_cost, int stream_min,
+                                               long long* first, int* n) {
   const int ib = __ldg(indptr + b);
   int L;
   long long base;
@@ -521,7 +523,7 @@ __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh
     *n = 0;
     return;
   }
-  if (S <= 0) S = Sched::auto_uniform_splits(indptr, B, Hkv, grid, min_chunk);
+  if (S <= 0) S = Sched::auto_uniform_splits(indptr, B, Hkv, grid, min_chunk, stream_min);
   if (S > 0) {
     const int c = (L + S - 1) / S;
     *first = (long long)sigma * S;
