@@ -134,14 +134,15 @@ int validate_args(const gda_args* a) {
 // (Sched::auto_uniform_splits) on a longest length lmax and a total n that the
 // caller knows; 0 selects the stream schedule.
 int host_uniform_splits(long long B, long long heads, long long grid, int min_chunk, long long lmax, long long n,
-                        int stream_min) {
+                        int kv8) {
   const long long units1 = B * heads;
   if (units1 > grid) return 0;
   if (units1 == 0) return 1;
-  if (stream_min > 0 && heads * n >= (long long)stream_min * grid) return 0;
+  if (!kv8 && heads * n >= (long long)gda::kStreamMinPerCta * grid) return 0;
   if (4 * lmax * B > 5 * n) return 0;
   long long s_opt = 1;
-  while (4 * s_opt * s_opt <= lmax) s_opt *= 2;
+  const long long k = kv8 ? 16 : 4;
+  while (k * s_opt * s_opt <= lmax) s_opt *= 2;
   const long long s_len = lmax > 0 ? (lmax + min_chunk - 1) / min_chunk : 1;
   long long s = s_opt < s_len ? s_opt : s_len;
   const long long s_wave = grid / units1;
@@ -224,16 +225,17 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   // the heads that split the batch into segments for the schedule
   const long long vheads = (long long)a->Hkv * nteam;
   const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
-  // the rule's per-CTA bound for the stream schedule: a BF16 cache only (with e4m3 rows
-  // one-wave uniform splits measured 1-8 % faster at 3450 .. 10348 positions per CTA)
-  const int stream_min = fp8 ? 0 : gda::kStreamMinPerCta;
+  // the rule's e4m3 variant: no per-CTA bound for the stream schedule (one-wave uniform
+  // splits measured 1-8 % faster at 3450 .. 10348 positions per CTA) and S_opt from
+  // 16 S^2 > lmax (half the BF16 count: a position streams in half the time)
+  const int kv8 = fp8 ? 1 : 0;
   const int auto_grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
   int splits = a->num_splits > 0 ? a->num_splits : 0;
   if (splits == 0 && a->window == 0 && a->max_len > 0 && a->total_len > 0) {
     // the caller knows a bound on the longest length and the exact total: the rule
     // runs here, and uniform splits launch as explicit ones (no scan of kv_indptr
     // on the device, no idle CTAs)
-    splits = host_uniform_splits(a->B, vheads, auto_grid, min_chunk, a->max_len, a->total_len, stream_min);
+    splits = host_uniform_splits(a->B, vheads, auto_grid, min_chunk, a->max_len, a->total_len, kv8);
   }
   if (splits == 0 && a->window > 0) {
     // A window bounds every sequence's range by `window`: equal splits of at least
@@ -279,7 +281,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   // automatic stream schedule with more segments than CTAs: a segment start costs a CTA
   // about as much as kPieceCost positions (twice as many positions of an e4m3 cache)
   p1.piece_cost = (splits == 0 && (long long)a->B * vheads > grid) ? (fp8 ? gda::kPieceCostE4m3 : gda::kPieceCost) : 0;
-  p1.stream_min = stream_min;
+  p1.rule_kv8 = kv8;
   p1.check_indices = a->check_indices ? 1 : 0;
   p1.wait_limit = wait_limit();
   cudaEvent_t t_end = nullptr;
@@ -316,7 +318,7 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   p2.grid1 = grid;
   p2.min_chunk = min_chunk;
   p2.piece_cost = p1.piece_cost;
-  p2.stream_min = stream_min;
+  p2.rule_kv8 = kv8;
   p2.fuse_gate = a->fuse_gate ? 1 : 0;
   // batched merge: when the B * Hq stage-2 CTAs fit one wave at its register count
   // (six CTAs per SM) and a warp merges more than one partial (automatic splits may)
@@ -647,8 +649,7 @@ int gda_reserve(int max_B, int Hq, int Hkv, int D, int max_splits) {
 
 int gda_auto_splits(int B, int heads, int grid, int min_chunk, int lmax, int64_t total) {
   if (B < 0 || heads < 1 || grid < 1 || lmax < 0 || total < 0) return -1;
-  return host_uniform_splits(B, heads, grid, min_chunk > 0 ? min_chunk : kDefaultMinChunk, lmax, total,
-                             gda::kStreamMinPerCta);
+  return host_uniform_splits(B, heads, grid, min_chunk > 0 ? min_chunk : kDefaultMinChunk, lmax, total, 0);
 }
 
 int gda_small_path_cluster(int64_t pairs, int max_len) {

@@ -232,8 +232,7 @@ __device__ __forceinline__ void seq_range(const int* indptr, int b, int window, 
 
 // Automatic mode: per-CTA stream length from which the chunked schedule is used
 // even for batches that fit one wave of uniform splits (a BF16 cache; with an e4m3
-// cache one-wave uniform splits measured faster at every length, and the host passes 0:
-// no such bound).
+// cache one-wave uniform splits measured faster at every length: no such bound).
 constexpr int kStreamMinPerCta = 3072;
 
 // Stream schedule: what starting one more (sequence, KV head) segment costs a CTA, in
@@ -261,7 +260,7 @@ struct Sched {
   // Hkv_ here is the number of (virtual) heads that split the batch into segments.
   // window > 0 requires S_ > 0 (the host picks the split count then).
   __device__ __forceinline__ void begin(const int* indptr_, int B_, int Hkv_, int S_, int grid_,
-                                        int cta_, int min_chunk, int window_, int piece_cost_, int stream_min) {
+                                        int cta_, int min_chunk, int window_, int piece_cost_, int kv8) {
     indptr = indptr_;
     B = B_;
     Hkv = Hkv_;
@@ -274,7 +273,7 @@ struct Sched {
     const int cand0 = min(B - 1, (int)(threadIdx.x & 31) * step0);
     const int v0 = __ldg(indptr + cand0 + 1);
     const int ntot = __ldg(indptr + B);
-    S = (S_ > 0) ? S_ : auto_uniform_splits(indptr_, B_, Hkv_, grid_, min_chunk, stream_min);
+    S = (S_ > 0) ? S_ : auto_uniform_splits(indptr_, B_, Hkv_, grid_, min_chunk, kv8);
     if (S > 0) {
       u = cta;
       return;
@@ -411,16 +410,18 @@ struct Sched {
   //  * a call costs about a + b L/S (stage 1, one piece per CTA) + c S (stage 2
   //    merges S partials per head), c/b ~ 2 positions (stage 2 keeps four partials'
   //    loads in flight), so the best S is near sqrt(lmax / 2): S_opt, the smallest
-  //    power of two with 4 S^2 > lmax, and at most ceil(lmax / min_chunk);
+  //    power of two with 4 S^2 > lmax, and at most ceil(lmax / min_chunk).  An e4m3
+  //    cache (kv8) streams a position in half the time, c/b ~ 8: 16 S^2 > lmax;
   //  * at most one wave of CTAs (B Hkv S <= grid); when the wave bounds S, the
   //    power of two below the bound if it keeps >= 80 % of the CTAs busy (pieces
   //    aligned to the warps' tiles), else the bound itself, and with < 80 % busy
   //    the stream schedule;
   //  * the stream schedule once each CTA would stream >= 3072 positions (it then
-  //    wins by 1-3 %: no idle SMs) or when the lengths are far from equal
+  //    wins by 1-3 %: no idle SMs; not with an e4m3 cache, where one-wave uniform
+  //    splits won at every length) or when the lengths are far from equal
   //    (lmax > 1.25 x the mean: S pieces of the longest sequence bound the call).
   static __device__ __forceinline__ int auto_uniform_splits(const int* indptr, int B, int Hkv, int grid,
-                                                            int min_chunk, int stream_min) {
+                                                            int min_chunk, int kv8) {
     if ((long long)B * Hkv > grid) return 0;
     const int units1 = B * Hkv;  // one piece per segment; <= grid
     if (units1 == 0) return 1;
@@ -437,12 +438,12 @@ struct Sched {
       lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
       n += __shfl_xor_sync(0xffffffffu, n, off);
     }
-    if (stream_min > 0 && (long long)Hkv * n >= (long long)stream_min * grid) return 0;
+    if (!kv8 && (long long)Hkv * n >= (long long)kStreamMinPerCta * grid) return 0;
     if (4LL * lmax * B > 5LL * n) return 0;
     // (closed forms, short dependent chains: every CTA's start waits on this)
     // s_opt: the smallest power of two p with 4 p^2 > lmax, 2^(h / 2) with h the index
-    // of lmax's top bit
-    const int s_opt = (lmax > 0) ? (1 << ((31 - __clz(lmax)) >> 1)) : 1;
+    // of lmax's top bit (kv8: 16 p^2 > lmax, 2^max(0, h / 2 - 1))
+    const int s_opt = (lmax > 0) ? (1 << max(0, ((31 - __clz(lmax)) >> 1) - (kv8 ? 1 : 0))) : 1;
     const int s_len = max(1, (lmax + min_chunk - 1) / min_chunk);
     int s = min(s_opt, s_len);
     const int s_wave = grid / units1;
@@ -511,7 +512,7 @@ struct Sched {
 // mode: first = c_first + sigma), or sigma*S + k (explicit mode), in position order.
 // (With a window the split count is explicit and L is the windowed length.)
 __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh, int Hkv, int B, int S,
-                                               int grid, int min_chunk, int window, int piece_cost, int stream_min,
+                                               int grid, int min_chunk, int window, int piece_cost, int kv8,
                                                long long* first, int* n) {
   const int ib = __ldg(indptr + b);
   int L;
@@ -523,7 +524,7 @@ __device__ __forceinline__ void segment_pieces(const int* indptr, int b, int kvh
     *n = 0;
     return;
   }
-  if (S <= 0) S = Sched::auto_uniform_splits(indptr, B, Hkv, grid, min_chunk, stream_min);
+  if (S <= 0) S = Sched::auto_uniform_splits(indptr, B, Hkv, grid, min_chunk, kv8);
   if (S > 0) {
     const int c = (L + S - 1) / S;
     *first = (long long)sigma * S;

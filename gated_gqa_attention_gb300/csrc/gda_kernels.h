@@ -35,8 +35,8 @@ struct Stage1Params {
   int num_splits;      // > 0 explicit, else automatic
   int min_chunk;       // automatic mode
   int piece_cost;      // automatic stream schedule: cost of a segment start in positions (0: none)
-  int stream_min;      // automatic rule: positions per CTA from which the stream schedule is
-                       // used for one-wave batches (0: no such bound)
+  int rule_kv8;        // automatic rule, e4m3 variant: no per-CTA bound for the stream
+                       // schedule and S_opt from 16 S^2 > lmax (BF16: 4 S^2)
   int check_indices;
   float v_descale;     // e4m3 pools: V = v_descale * e4m3(code)
   long long wait_limit;  // SM cycles after which a pipeline wait gives up (kWaitLimitCycles;
@@ -60,7 +60,7 @@ struct Stage2Params {
   int grid1;           // stage-1 grid (automatic-mode chunking)
   int min_chunk;
   int piece_cost;      // the stage-1 schedule's cost of a segment start
-  int stream_min;      // the stage-1 rule's per-CTA stream bound
+  int rule_kv8;        // the stage-1 rule's e4m3 variant
   int fuse_gate;
   int batched;         // merge with four partials' loads in flight per warp (small grids)
 };

@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(NWARP * 32, 1) stage1_mma_kernel(Stage1Params 
 
   Sched sched;
   sched.begin(p.indptr, p.B, TEAM ? p.Hkv * p.nteam : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x,
-              p.min_chunk, p.window, p.piece_cost, p.stream_min);
+              p.min_chunk, p.window, p.piece_cost, p.rule_kv8);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
   const uint64_t pol_v = l2_policy_evict_first();
   // KV head of a piece (in teams the scheduled head is kvh * nteam + the team)
@@ -754,7 +754,7 @@ __global__ void __launch_bounds__(kDirectWarps * 32, 1) stage1_direct_kernel(Sta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window, p.piece_cost, p.stream_min);
+  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window, p.piece_cost, p.rule_kv8);
   const size_t stride = (size_t)p.Hkv * kRowBytes;
   // Stage 2 may start its prologue (gate loads and sigmoids) once this CTA knows it has
   // work: an idle CTA (the automatic plan launches a full grid) exits without the

@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_kernel(Stage1Params p)
 
   if (threadIdx.x == 0) sm.qmax = 0u;
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window, p.piece_cost, p.stream_min);
+  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window, p.piece_cost, p.rule_kv8);
   const size_t stride = (size_t)p.Hkv * kRowBytes8;
   const uint64_t pol_v = l2_policy_evict_first();
 
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(kW8 * 32, 1) stage1_fp8_pair_kernel(Stage1Para
   if (threadIdx.x < 2) sm.qmax[threadIdx.x] = 0u;
   Sched sched;
   sched.begin(p.indptr, p.B, PAIR ? p.Hkv * p.nteam : p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x,
-              p.min_chunk, p.window, p.piece_cost, p.stream_min);
+              p.min_chunk, p.window, p.piece_cost, p.rule_kv8);
   const size_t stride = (size_t)p.Hkv * kRowBytes8;
   const uint64_t pol_v = l2_policy_evict_first();
   auto kv_head = [&](const Piece& pp) -> int { return PAIR ? pp.kvh / p.nteam : pp.kvh / p.npass; };

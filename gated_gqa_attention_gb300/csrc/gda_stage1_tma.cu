@@ -217,7 +217,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) stage1_kernel(Stage1Params 
   __syncthreads();
 
   Sched sched;
-  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window, p.piece_cost, p.stream_min);
+  sched.begin(p.indptr, p.B, p.Hkv * p.npass, p.num_splits, gridDim.x, blockIdx.x, p.min_chunk, p.window, p.piece_cost, p.rule_kv8);
   // Stage 2 may start its prologue (gate loads and sigmoids) once this CTA knows it has
   // work: an idle CTA (the automatic plan launches a full grid) exits without the
   // trigger, which counts as one, so stage 2's CTAs are placed after the idle CTAs have

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kS2Warps * 32) stage2_kernel(Stage2Params p) {
   // which partials hold this segment: from kv_indptr, an input, so before the wait
   long long first;
   int n;
-  segment_pieces(p.indptr, b, sched_h, sched_n, p.B, p.num_splits, p.grid1, p.min_chunk, p.window, p.piece_cost, p.stream_min,
+  segment_pieces(p.indptr, b, sched_h, sched_n, p.B, p.num_splits, p.grid1, p.min_chunk, p.window, p.piece_cost, p.rule_kv8,
                  &first, &n);
   // attention sink (a logit in the softmax denominator with no value row), log2 units
   const float sink2 = (p.sinks != nullptr) ? __ldg(p.sinks + h) * 1.44269504088896340736f : -INFINITY;

@@ -12,12 +12,13 @@ import random
 AUTO_MAX_CTAS = 1024
 
 
-STREAM_MIN_PER_CTA = 3072   # a BF16 cache; an e4m3 cache has no such bound (0)
+STREAM_MIN_PER_CTA = 3072   # a BF16 cache; the e4m3 variant has no such bound
 
 
-def uniform_splits(indptr, Hkv, grid, min_chunk, stream_min=STREAM_MIN_PER_CTA):
+def uniform_splits(indptr, Hkv, grid, min_chunk, kv8=False):
     """The automatic split rule (Sched::auto_uniform_splits): S uniform splits, or 0
-    for the stream schedule."""
+    for the stream schedule.  kv8: the e4m3 variant (no per-CTA bound for the stream,
+    S_opt from 16 S^2 > lmax instead of 4 S^2)."""
     B = len(indptr) - 1
     units1 = B * Hkv
     if units1 > grid:
@@ -26,10 +27,11 @@ def uniform_splits(indptr, Hkv, grid, min_chunk, stream_min=STREAM_MIN_PER_CTA):
         return 1
     lmax = max([indptr[b + 1] - indptr[b] for b in range(B)] + [0])
     n = indptr[B]
-    if (stream_min > 0 and Hkv * n >= stream_min * grid) or 4 * lmax * B > 5 * n:
+    if (not kv8 and Hkv * n >= STREAM_MIN_PER_CTA * grid) or 4 * lmax * B > 5 * n:
         return 0
+    k = 16 if kv8 else 4
     s_opt = 1
-    while 4 * s_opt * s_opt <= lmax:
+    while k * s_opt * s_opt <= lmax:
         s_opt *= 2
     s = min(s_opt, max(1, -(-lmax // min_chunk)))
     s_wave = grid // units1
@@ -168,10 +170,14 @@ def test_split_rule_on_measured_buckets():
     # an e4m3 cache: no per-CTA bound, one-wave uniform splits at every length (measured
     # 1-8 % faster than the stream at 3450 .. 10348 positions per CTA); a wave that
     # leaves < 80 % of the CTAs busy still takes the stream
+    # and at small batches half the BF16 count (the e4m3 sweep: B1 L2048 best at 16, B1
+    # L8192 at 32, B2 L2048 at 16)
     want8 = {(64, 4096): 1, (64, 12288): 1, (32, 8192): 2, (16, 16384): 4, (8, 131072): 8, (4, 65536): 16,
-             (24, 16384): 3, (48, 4096): 0, (40, 8192): 0, (128, 512): 0}
+             (24, 16384): 3, (48, 4096): 0, (40, 8192): 0, (128, 512): 0,
+             (1, 2048): 16, (1, 8192): 32, (1, 32768): 64, (2, 2048): 16, (2, 8192): 32, (4, 2048): 16,
+             (8, 2048): 8}
     for (B, L), S in want8.items():
-        assert uniform_splits(eq(B, L), 2, 152, 64, stream_min=0) == S, (B, L)
+        assert uniform_splits(eq(B, L), 2, 152, 64, kv8=True) == S, (B, L)
     # far from equal lengths: the stream schedule balances them
     assert uniform_splits([0, 8000, 8100, 8200, 30000], 2, 152, 64) == 0
     assert uniform_splits([0], 2, 152, 64) == 1 and uniform_splits([0, 0, 0], 2, 152, 64) == 1
@@ -345,11 +351,17 @@ def test_device_closed_forms_equal_the_loops():
             p *= 2
         return p
 
-    def s_opt_closed(lmax):
+    def s_opt_closed(lmax, kv8=False):
         if lmax <= 0:
             return 1
         h = lmax.bit_length() - 1
-        return 1 << (h >> 1)
+        return 1 << max(0, (h >> 1) - (1 if kv8 else 0))
+
+    def s_opt_loop8(lmax):
+        p = 1
+        while 16 * p * p <= lmax:
+            p *= 2
+        return p
 
     def p2_loop(w):
         p = 1
@@ -361,5 +373,6 @@ def test_device_closed_forms_equal_the_loops():
     cases = list(range(0, 1 << 15)) + [rng.randrange(0, 2 ** 31) for _ in range(20000)] + [2 ** 31 - 1]
     for lmax in cases:
         assert s_opt_closed(lmax) == s_opt_loop(lmax), lmax
+        assert s_opt_closed(lmax, kv8=True) == s_opt_loop8(lmax), lmax
     for w in range(1, 4096):
         assert (1 << (w.bit_length() - 1)) == p2_loop(w), w
