@@ -912,6 +912,18 @@ def _sweep_batch(B, L, seed, hq=16, hkv=2, d=256):
 SWEEP_SPLITS = (1, 2, 4, 8, 16, 32, 64, 128)
 
 
+def _sweep_batch8(B, L, seed):
+    """An equal-length batch over an e4m3 cache (the workloads module's recipe, values
+    drawn on the device): q, gate, k_pool, v_pool, kv_indptr, kv_indices, k_descale,
+    v_descale, scale."""
+    import torch
+    from gated_gqa_attention_gb300 import workloads
+    d = workloads.make([L] * B, seed=seed, layout="perm", pool_slots=B * L + 64, values_device="cuda", kv="e4m3")
+    dv = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    return (dv["q"], dv["gate"], dv["k_pool"], dv["v_pool"], dv["kv_indptr"], dv["kv_indices"], d["k_descale"],
+            d["v_descale"], d["scale"])
+
+
 def run_split_sweep(args):
     """The split-count sweep ("chosen per (B, length) from measured time", FreeToken PR
     #781): for B equal-length sequences, B in {1 .. 128} and L in {512 .. 32768} (B L <=
@@ -931,18 +943,24 @@ def run_split_sweep(args):
         for L in (512, 2048, 8192, 32768):
             if B * L > (1 << 21):
                 continue
-            q, gate, kp, vp, indptr, idx = _sweep_batch(B, L, seed=1000 + B + L)
+            if args.kv == "e4m3":
+                q, gate, kp, vp, indptr, idx, kd, vd, sc = _sweep_batch8(B, L, seed=1000 + B + L)
+            else:
+                q, gate, kp, vp, indptr, idx = _sweep_batch(B, L, seed=1000 + B + L)
+                kd, vd, sc = 1.0, 1.0, D ** -0.5
             out = torch.empty_like(q)
             t = {}
             for S in SWEEP_SPLITS + (0,):
                 ws = torch.empty(gda.workspace_bytes(B, HQ, HKV, D, S), dtype=torch.uint8, device="cuda")
                 gda.workspace_init(ws)
                 t[S] = _per_call_us(lambda: gda.decode_ex(q, gate, kp, vp, indptr, idx, out=out, workspace=ws,
-                                                          scale=D ** -0.5, num_splits=S), calls=100)
+                                                          scale=sc, k_descale=kd, v_descale=vd, num_splits=S),
+                                    calls=100)
             ws = torch.empty(gda.workspace_bytes(B, HQ, HKV, D, 0), dtype=torch.uint8, device="cuda")
             gda.workspace_init(ws)
             disp = _per_call_us(lambda: gda.decode_ex(q, gate, kp, vp, indptr, idx, out=out, workspace=ws,
-                                                      scale=D ** -0.5, max_len=L, total_len=B * L), calls=100)
+                                                      scale=sc, k_descale=kd, v_descale=vd, max_len=L,
+                                                      total_len=B * L), calls=100)
             best = min(SWEEP_SPLITS, key=lambda s: t[s])
             rows.append({"B": B, "L": L, "us_by_splits": {str(s): round(t[s], 3) for s in SWEEP_SPLITS},
                          "best_splits": best, "best_us": round(t[best], 3), "auto_us": round(t[0], 3),
@@ -975,14 +993,19 @@ def run_split_cross(args):
     gda.load()
     HQ, HKV, D = 16, 2, 256
     for B, L, S in SPLIT_CROSS:
-        q, gate, kp, vp, indptr, idx = _sweep_batch(B, L, seed=5)
+        if args.kv == "e4m3":
+            q, gate, kp, vp, indptr, idx, kd, vd, sc = _sweep_batch8(B, L, seed=5)
+        else:
+            q, gate, kp, vp, indptr, idx = _sweep_batch(B, L, seed=5)
+            kd, vd, sc = 1.0, 1.0, D ** -0.5
         out = torch.empty_like(q)
         t = {}
         for s in (0, S):
             ws = torch.empty(gda.workspace_bytes(B, HQ, HKV, D, s), dtype=torch.uint8, device="cuda")
             gda.workspace_init(ws)
             t[s] = _per_call_us(lambda: gda.decode_ex(q, gate, kp, vp, indptr, idx, out=out, workspace=ws,
-                                                      scale=D ** -0.5, num_splits=s), calls=200)
+                                                      scale=sc, k_descale=kd, v_descale=vd, num_splits=s),
+                                calls=200)
         print("B %3d L %6d per-CTA %6d | auto %8.2f | S=%3d %8.2f | S/auto %.3f" % (
             B, L, (HKV * B * L + 151) // 152, t[0], S, t[S], t[S] / t[0]), flush=True)
         del q, gate, kp, vp, indptr, idx, out, ws

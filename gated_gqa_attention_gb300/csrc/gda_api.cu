@@ -138,7 +138,7 @@ int host_uniform_splits(long long B, long long heads, long long grid, int min_ch
   const long long units1 = B * heads;
   if (units1 > grid) return 0;
   if (units1 == 0) return 1;
-  if (!kv8 && heads * n >= (long long)gda::kStreamMinPerCta * grid) return 0;
+  if (heads * n >= (long long)gda::kStreamMinPerCta * (kv8 ? 2 : 1) * grid) return 0;
   if (4 * lmax * B > 5 * n) return 0;
   long long s_opt = 1;
   const long long k = kv8 ? 16 : 4;
@@ -225,9 +225,9 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
   // the heads that split the batch into segments for the schedule
   const long long vheads = (long long)a->Hkv * nteam;
   const int min_chunk = a->min_chunk > 0 ? a->min_chunk : kDefaultMinChunk;
-  // the rule's e4m3 variant: no per-CTA bound for the stream schedule (one-wave uniform
-  // splits measured 1-8 % faster at 3450 .. 10348 positions per CTA) and S_opt from
-  // 16 S^2 > lmax (half the BF16 count: a position streams in half the time)
+  // the rule's e4m3 variant: a position streams in half the time, so the per-CTA bound
+  // for the stream schedule is twice as many positions and S_opt comes from 16 S^2 >
+  // lmax (half the BF16 count)
   const int kv8 = fp8 ? 1 : 0;
   const int auto_grid = sms < gda::kAutoMaxCtas ? sms : gda::kAutoMaxCtas;
   int splits = a->num_splits > 0 ? a->num_splits : 0;

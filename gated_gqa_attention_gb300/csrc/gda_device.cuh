@@ -231,8 +231,10 @@ __device__ __forceinline__ void seq_range(const int* indptr, int b, int window, 
 }
 
 // Automatic mode: per-CTA stream length from which the chunked schedule is used
-// even for batches that fit one wave of uniform splits (a BF16 cache; with an e4m3
-// cache one-wave uniform splits measured faster at every length: no such bound).
+// even for batches that fit one wave of uniform splits: 3072 positions of a BF16
+// cache, twice as many of an e4m3 cache (the same streaming time; measured: one-wave
+// uniform splits win at 3450 .. 5174 e4m3 positions per CTA, tie at 6899 and lose from
+// ~13800).
 constexpr int kStreamMinPerCta = 3072;
 
 // Stream schedule: what starting one more (sequence, KV head) segment costs a CTA, in
@@ -416,9 +418,9 @@ struct Sched {
   //    power of two below the bound if it keeps >= 80 % of the CTAs busy (pieces
   //    aligned to the warps' tiles), else the bound itself, and with < 80 % busy
   //    the stream schedule;
-  //  * the stream schedule once each CTA would stream >= 3072 positions (it then
-  //    wins by 1-3 %: no idle SMs; not with an e4m3 cache, where one-wave uniform
-  //    splits won at every length) or when the lengths are far from equal
+  //  * the stream schedule once each CTA would stream >= 3072 positions (6144 of an
+  //    e4m3 cache; it then wins by 1-3 %: no idle SMs) or when the lengths are far
+  //    from equal
   //    (lmax > 1.25 x the mean: S pieces of the longest sequence bound the call).
   static __device__ __forceinline__ int auto_uniform_splits(const int* indptr, int B, int Hkv, int grid,
                                                             int min_chunk, int kv8) {
@@ -438,7 +440,7 @@ struct Sched {
       lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
       n += __shfl_xor_sync(0xffffffffu, n, off);
     }
-    if (!kv8 && (long long)Hkv * n >= (long long)kStreamMinPerCta * grid) return 0;
+    if ((long long)Hkv * n >= (long long)kStreamMinPerCta * (kv8 ? 2 : 1) * grid) return 0;
     if (4LL * lmax * B > 5LL * n) return 0;
     // (closed forms, short dependent chains: every CTA's start waits on this)
     // s_opt: the smallest power of two p with 4 p^2 > lmax, 2^(h / 2) with h the index

@@ -35,8 +35,8 @@ struct Stage1Params {
   int num_splits;      // > 0 explicit, else automatic
   int min_chunk;       // automatic mode
   int piece_cost;      // automatic stream schedule: cost of a segment start in positions (0: none)
-  int rule_kv8;        // automatic rule, e4m3 variant: no per-CTA bound for the stream
-                       // schedule and S_opt from 16 S^2 > lmax (BF16: 4 S^2)
+  int rule_kv8;        // automatic rule, e4m3 variant: the per-CTA bound for the stream
+                       // schedule doubled, S_opt from 16 S^2 > lmax (BF16: 4 S^2)
   int check_indices;
   float v_descale;     // e4m3 pools: V = v_descale * e4m3(code)
   long long wait_limit;  // SM cycles after which a pipeline wait gives up (kWaitLimitCycles;

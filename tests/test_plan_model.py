@@ -12,13 +12,13 @@ import random
 AUTO_MAX_CTAS = 1024
 
 
-STREAM_MIN_PER_CTA = 3072   # a BF16 cache; the e4m3 variant has no such bound
+STREAM_MIN_PER_CTA = 3072   # a BF16 cache; twice as many positions of an e4m3 cache
 
 
 def uniform_splits(indptr, Hkv, grid, min_chunk, kv8=False):
     """The automatic split rule (Sched::auto_uniform_splits): S uniform splits, or 0
-    for the stream schedule.  kv8: the e4m3 variant (no per-CTA bound for the stream,
-    S_opt from 16 S^2 > lmax instead of 4 S^2)."""
+    for the stream schedule.  kv8: the e4m3 variant (the per-CTA bound for the stream
+    doubled, S_opt from 16 S^2 > lmax instead of 4 S^2)."""
     B = len(indptr) - 1
     units1 = B * Hkv
     if units1 > grid:
@@ -27,7 +27,7 @@ def uniform_splits(indptr, Hkv, grid, min_chunk, kv8=False):
         return 1
     lmax = max([indptr[b + 1] - indptr[b] for b in range(B)] + [0])
     n = indptr[B]
-    if (not kv8 and Hkv * n >= STREAM_MIN_PER_CTA * grid) or 4 * lmax * B > 5 * n:
+    if Hkv * n >= STREAM_MIN_PER_CTA * (2 if kv8 else 1) * grid or 4 * lmax * B > 5 * n:
         return 0
     k = 16 if kv8 else 4
     s_opt = 1
@@ -167,13 +167,12 @@ def test_split_rule_on_measured_buckets():
             (64, 4096): 0, (16, 32768): 0, (8, 131072): 0, (48, 4096): 0, (128, 512): 0}
     for (B, L), S in want.items():
         assert uniform_splits(eq(B, L), 2, 152, 64) == S, (B, L)
-    # an e4m3 cache: no per-CTA bound, one-wave uniform splits at every length (measured
-    # 1-8 % faster than the stream at 3450 .. 10348 positions per CTA); a wave that
-    # leaves < 80 % of the CTAs busy still takes the stream
-    # and at small batches half the BF16 count (the e4m3 sweep: B1 L2048 best at 16, B1
-    # L8192 at 32, B2 L2048 at 16)
-    want8 = {(64, 4096): 1, (64, 12288): 1, (32, 8192): 2, (16, 16384): 4, (8, 131072): 8, (4, 65536): 16,
-             (24, 16384): 3, (48, 4096): 0, (40, 8192): 0, (128, 512): 0,
+    # an e4m3 cache: the per-CTA bound doubled (one-wave uniform splits won at 3450 ..
+    # 5174 positions per CTA, tied at 6899 and lost from ~13800), a wave that leaves
+    # < 80 % of the CTAs busy still takes the stream; at small batches half the BF16
+    # count (the e4m3 sweep: B1 L2048 best at 16, B1 L8192 at 32, B2 L2048 at 16)
+    want8 = {(64, 4096): 1, (64, 6144): 1, (64, 8192): 0, (32, 8192): 2, (32, 32768): 0, (16, 16384): 4,
+             (8, 131072): 0, (4, 65536): 16, (24, 16384): 3, (48, 4096): 0, (40, 8192): 0, (128, 512): 0,
              (1, 2048): 16, (1, 8192): 32, (1, 32768): 64, (2, 2048): 16, (2, 8192): 32, (4, 2048): 16,
              (8, 2048): 8}
     for (B, L), S in want8.items():
