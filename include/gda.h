@@ -292,12 +292,15 @@ int gda_small_path_cluster(int64_t pairs, int max_len);
  * batch).  The device applies the same rule to kv_indptr when the caller passes no
  * bound; gda_args.max_len with total_len applies it on the host.  -1 for invalid
  * arguments; min_chunk <= 0 takes the library default (64).  Pure host arithmetic.
- * The rule, measured on GB300:
- *  - about sqrt(lmax / 8) splits (a power of two), at least min_chunk positions each;
+ * The rule, measured on GB300 (this function gives it for a BF16 cache):
+ *  - the smallest power of two S with 4 S^2 > lmax (about sqrt(lmax / 2)), at least
+ *    min_chunk positions each;
  *  - at most one wave of CTAs; when the wave bounds S, the power of two below it if
  *    >= 80 % of the CTAs stay busy, else the bound; below 80 % busy, the stream;
  *  - the stream once each CTA would take >= 3072 positions, or when the longest
- *    sequence is more than 1.25 x the mean. */
+ *    sequence is more than 1.25 x the mean.
+ * An e4m3 cache streams a position in half the time: its variant of the rule takes
+ * 16 S^2 > lmax and moves to the stream from 6144 positions per CTA. */
 int gda_auto_splits(int B, int heads, int grid, int min_chunk, int lmax, int64_t total);
 
 /* Byte layout of one decode step's inputs packed into a single block, as
