@@ -218,8 +218,9 @@ int enqueue(const gda_args* a, void* ws, cudaStream_t stream) {
                                                         : gda::kVariantMma;
   // G > 8 on the MMA kernel: the groups of 8 query heads in teams of 2 or 3, every
   // group of a team in one piece (one HBM read of the KV head's rows per team); on the
-  // FP8 kernel in pairs, except for three groups (a pair costs ~1.6 single passes, so
-  // a pair and a half-empty pair lose to three passes: measured 143.0 against 135.8 us)
+  // FP8 kernel in pairs, except for three groups (a half-empty pair costs a full one, and
+  // two pairs measured no faster than three single passes on b64_l4096 lengths: 135.0
+  // us for G = 32's two pairs against 135.9 us for G = 24's three passes)
   const int team = (variant != gda::kVariantMma || npass < 2) ? 1 : fp8 ? (npass == 3 ? 1 : 2) : team_size(npass);
   const int nteam = (npass + team - 1) / team;
   // the heads that split the batch into segments for the schedule
